@@ -1,0 +1,146 @@
+/*
+ * libtriattn — triangular (pair-biased, slice-batched) attention, forward and
+ * backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("TurboPairFormer: Fast and Stable Protein Folding Model
+ * Training with an Optimized Triangle Attention Kernel", Abstract, Figure 1(a),
+ * Table 1 and Figure 6): for every example b, outer slice o, head h,
+ *
+ *   S[q,k]  = Q[b,o,h,q,:] . K[b,o,h,k,:] / sqrt(D) + bias[b,h,q,k] + mask[b,o,k]
+ *   O[b,o,h,q,:] = sum_k softmax_k(S)[q,k] V[b,o,h,k,:]
+ *
+ * with ONE pair bias shared by all N_o slices.  The backward returns dQ, dK,
+ * dV and dbias, where dbias[b,h] is the sum over slices o of dS_o
+ * (Figure 1(a): the third reduction axis).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays,
+ *    16-byte aligned.  "bf16" means IEEE bfloat16 stored as uint16.
+ *  - Layouts: q, k, v, o, o_resid, dO, dq, dk, dv  [B, N_o, H, N, D] bf16
+ *             bias, dbias                         [B, H, N, N]      bf16
+ *             mask (optional, additive)           [B, N_o, N]       bf16
+ *             lse                                 [B, N_o, H, N]    fp32 (natural log)
+ *  - N_o must equal N (Table 1: "N_o = N"), D must be 16 or 32, N >= 1.
+ *  - A row whose keys are all masked (every score -inf) yields O = 0,
+ *    residual 0, lse = -inf and zero gradient contributions.
+ *  - The caller owns every buffer, the workspace and the stream.  The library
+ *    allocates no device memory; it keeps only host-side state (TMA
+ *    descriptors are built per call, kernel attributes are set once).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are returned synchronously and nothing
+ *    is launched.  A launch failure returns TRIATTN_ERR_CUDA.  A device-side
+ *    wait that exceeds its time limit (about 2 s) is recorded in a device
+ *    status word that triattn_device_status() reads back.
+ *  - Results are bitwise reproducible across calls with the same inputs and
+ *    shape: no floating-point atomics are used, every reduction has a fixed
+ *    order, and the kernel configuration depends only on (D, N).
+ */
+#ifndef TRIATTN_H_
+#define TRIATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int B;          /* examples */
+  int N_o;        /* outer slices; must equal N */
+  int N;          /* tokens per crop (queries = keys = N) */
+  int H;          /* heads */
+  int D;          /* features per head: 16 or 32 */
+  unsigned flags; /* reserved, must be 0 */
+} triattn_shape;
+
+typedef enum {
+  TRIATTN_OK = 0,
+  TRIATTN_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad shape field */
+  TRIATTN_ERR_UNSUPPORTED = 2,  /* D not in {16, 32}, N_o != N, size overflow */
+  TRIATTN_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  TRIATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+  TRIATTN_ERR_TIMEOUT = 5       /* a device wait exceeded its limit */
+} triattn_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* triattn_status_string(triattn_status s);
+
+/*
+ * Forward.  "TurboPairFormer", Abstract and Figure 1(a) (the operation),
+ * Figure 7(b) and Figure 9 (the saved output residual).
+ *
+ *   o       [B,N_o,H,N,D] bf16  out: O rounded once (round-to-nearest) from FP32.
+ *   lse     [B,N_o,H,N]   fp32  out: log sum_k exp(S[q,k]) (natural log).
+ *   o_resid [B,N_o,H,N,D] bf16  out, optional (NULL = not written): the
+ *           output-rounding residual E = bf16(O_fp32 - float(o)), the BF16
+ *           approximation of what rounding O to BF16 lost.  The backward uses
+ *           o + o_resid for its softmax correction.
+ *   mask    optional (NULL = no mask).
+ * Launches one kernel.
+ */
+triattn_status tri_attn_fwd(const triattn_shape* shape,
+                            const void* q, const void* k, const void* v,
+                            const void* bias, const void* mask,
+                            void* o, float* lse, void* o_resid,
+                            void* stream);
+
+/*
+ * Workspace bytes tri_attn_bwd needs for `shape` (0 on an invalid shape).
+ * The workspace holds the FP32 row corrections delta, the single-writer FP32
+ * dQ partials (one per key tile) and the single-writer FP32 dbias partials
+ * (one per outer group of slices) ("TurboPairFormer", Figure 2(b), Figure 7,
+ * Table 11).
+ */
+size_t triattn_bwd_workspace_bytes(const triattn_shape* shape);
+
+/*
+ * Backward.  "TurboPairFormer", Abstract, Figure 2, Figure 7(b)-(d),
+ * Figure 11(a) and Table 11 (key-tile-parallel partition):
+ *   1. preprocess: delta[q] = sum_d dO[q,d] * (o[q,d] + o_resid[q,d]) in FP32
+ *      (o_resid NULL: compensation off, delta = sum_d dO*o);
+ *   2. main: one CTA per (b, h, key tile, outer group of slices) recomputes
+ *      S, P, dP and dS once per query tile, keeps dK and dV on chip and
+ *      writes one FP32 dQ partial per key tile and one FP32 dbias partial per
+ *      outer group, each with a single writer;
+ *   3. a reduction kernel adds the dQ partials in ascending key-tile order;
+ *   4. a reduction kernel adds the dbias partials in ascending group order.
+ *
+ *   q,k,v,bias,mask  the forward's inputs (mask may be NULL).
+ *   o, lse           the forward's outputs; o_resid optional (see above).
+ *   dO               [B,N_o,H,N,D] bf16 incoming gradient.
+ *   dq, dk, dv       [B,N_o,H,N,D] bf16 out.
+ *   dbias            [B,H,N,N] bf16 out.
+ *   workspace        device scratch of at least
+ *                    triattn_bwd_workspace_bytes(shape) bytes, 256-byte
+ *                    aligned; contents on entry are ignored.
+ * Launches four kernels in stream order.
+ */
+triattn_status tri_attn_bwd(const triattn_shape* shape,
+                            const void* q, const void* k, const void* v,
+                            const void* bias, const void* mask,
+                            const void* o, const void* o_resid, const float* lse,
+                            const void* dO,
+                            void* dq, void* dk, void* dv, void* dbias,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that
+ * kernels set when a bounded wait gives up.  Returns TRIATTN_OK,
+ * TRIATTN_ERR_TIMEOUT, or TRIATTN_ERR_CUDA if the synchronisation failed.
+ */
+triattn_status triattn_device_status(void* stream);
+
+/*
+ * Test hook, off by default: when `cap_ns` > 0 every bounded device wait of
+ * later launches gives up after `cap_ns` nanoseconds instead of the default
+ * limit (about 2 s).  0 restores the default.
+ */
+void triattn_set_wait_limit_ns(unsigned long long cap_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRIATTN_H_ */

@@ -1,0 +1,245 @@
+// C ABI of libtriattn: argument validation, TMA descriptor construction and
+// kernel launches.  Declared in include/triattn.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/triattn.h"
+#include "kernels.cuh"
+
+namespace triattn {
+namespace {
+
+__device__ uint32_t g_status_word;
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+std::mutex g_init_mu;
+uint64_t g_init_mask = 0;            // devices whose kernel attributes are set
+uint32_t* g_status_ptr[64] = {};     // device address of g_status_word per device
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+triattn_status init_device(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TRIATTN_ERR_CUDA;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lk(g_init_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        fn == nullptr || q != cudaDriverEntryPointSuccess)
+      return TRIATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (g_init_mask & (1ull << dev)) return TRIATTN_OK;
+  if (setup_fwd<16>() != cudaSuccess || setup_fwd<32>() != cudaSuccess || setup_bwd<16>() != cudaSuccess ||
+      setup_bwd<32>() != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  void* sp = nullptr;
+  if (cudaGetSymbolAddress(&sp, g_status_word) != cudaSuccess) return TRIATTN_ERR_CUDA;
+  g_status_ptr[dev] = static_cast<uint32_t*>(sp);
+  g_init_mask |= (1ull << dev);
+  return TRIATTN_OK;
+}
+
+triattn_status check_shape(const triattn_shape* s) {
+  if (s == nullptr) return TRIATTN_ERR_INVALID_ARG;
+  if (s->B < 1 || s->N < 1 || s->N_o < 1 || s->H < 1 || s->flags != 0) return TRIATTN_ERR_INVALID_ARG;
+  if (s->D != 16 && s->D != 32) return TRIATTN_ERR_UNSUPPORTED;
+  if (s->N_o != s->N) return TRIATTN_ERR_UNSUPPORTED;
+  // TMA row strides of the [N, N] bias must be multiples of 16 bytes.
+  if (s->N % 8 != 0) return TRIATTN_ERR_UNSUPPORTED;
+  // grid limits: outer groups in gridDim.y, B*H in gridDim.z
+  if (s->N_o / kGroupFwd > 65535 || static_cast<long long>(s->B) * s->H > 65535) return TRIATTN_ERR_UNSUPPORTED;
+  // the forward stages the key mask of all key tiles in shared memory
+  if (s->N > 4096) return TRIATTN_ERR_UNSUPPORTED;
+  // TMA outer dimension B*N_o*H (slices) must fit in 32 bits
+  if (static_cast<long long>(s->B) * s->N_o * s->H >= (1ll << 31)) return TRIATTN_ERR_UNSUPPORTED;
+  return TRIATTN_OK;
+}
+
+// 3-D map over a [slices, N, D] bf16 tensor, box = 128 rows x D.
+bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->D), static_cast<cuuint64_t>(s->N),
+                              static_cast<cuuint64_t>(s->B) * s->N_o * s->H};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s->D) * 2, static_cast<cuuint64_t>(s->N) * s->D * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(s->D), 128u, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  const CUtensorMapSwizzle sw = (s->D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over the [B*H, N (q), N (k)] bf16 bias, box = 128 q rows x 64 keys.
+bool make_bias_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->N), static_cast<cuuint64_t>(s->N),
+                              static_cast<cuuint64_t>(s->B) * s->H};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s->N) * 2, static_cast<cuuint64_t>(s->N) * s->N * 2};
+  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t delta_off, dq_off, db_off, total;
+};
+
+WsLayout ws_layout(const triattn_shape* s) {
+  const size_t rows = static_cast<size_t>(s->B) * s->N_o * s->H * s->N;
+  const size_t jk = (s->N + kTileK - 1) / kTileK;
+  const size_t groups = s->N_o / kGroupBwd;
+  WsLayout w;
+  w.delta_off = 0;
+  w.dq_off = round_up(rows * 4, 256);
+  w.db_off = w.dq_off + round_up(jk * rows * s->D * 4, 256);
+  w.total = w.db_off + round_up(groups * s->B * s->H * static_cast<size_t>(s->N) * s->N * 4, 256);
+  return w;
+}
+
+WaitCtl wait_ctl(int dev) {
+  WaitCtl wc;
+  wc.limit_ns = g_wait_limit_ns.load();
+  wc.status = g_status_ptr[dev];
+  return wc;
+}
+
+}  // namespace
+}  // namespace triattn
+
+using namespace triattn;
+
+extern "C" {
+
+const char* triattn_status_string(triattn_status s) {
+  switch (s) {
+    case TRIATTN_OK: return "TRIATTN_OK";
+    case TRIATTN_ERR_INVALID_ARG: return "TRIATTN_ERR_INVALID_ARG";
+    case TRIATTN_ERR_UNSUPPORTED: return "TRIATTN_ERR_UNSUPPORTED";
+    case TRIATTN_ERR_WORKSPACE: return "TRIATTN_ERR_WORKSPACE";
+    case TRIATTN_ERR_CUDA: return "TRIATTN_ERR_CUDA";
+    case TRIATTN_ERR_TIMEOUT: return "TRIATTN_ERR_TIMEOUT";
+  }
+  return "TRIATTN_ERR_UNKNOWN";
+}
+
+size_t triattn_bwd_workspace_bytes(const triattn_shape* shape) {
+  if (check_shape(shape) != TRIATTN_OK) return 0;
+  return ws_layout(shape).total;
+}
+
+triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                            const void* bias, const void* mask, void* o, float* lse, void* o_resid, void* stream) {
+  triattn_status st = check_shape(shape);
+  if (st != TRIATTN_OK) return st;
+  const void* req[] = {q, k, v, bias, o, lse};
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
+  if ((mask && !aligned16(mask)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  if ((st = init_device(&dev)) != TRIATTN_OK) return st;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
+      !make_bias_map(&a.tm_bias, bias, shape))
+    return TRIATTN_ERR_CUDA;
+  a.mask = mask;
+  a.o = o;
+  a.lse = lse;
+  a.o_resid = o_resid;
+  a.B = shape->B;
+  a.N_o = shape->N_o;
+  a.N = shape->N;
+  a.H = shape->H;
+  a.wc = wait_ctl(dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = (shape->D == 32) ? launch_fwd<32>(a, s) : launch_fwd<16>(a, s);
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+}
+
+triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                            const void* bias, const void* mask, const void* o, const void* o_resid, const float* lse,
+                            const void* dO, void* dq, void* dk, void* dv, void* dbias, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  triattn_status st = check_shape(shape);
+  if (st != TRIATTN_OK) return st;
+  const void* req[] = {q, k, v, bias, o, lse, dO, dq, dk, dv, dbias};
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
+  if ((mask && !aligned16(mask)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(shape);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return TRIATTN_ERR_WORKSPACE;
+  int dev = 0;
+  if ((st = init_device(&dev)) != TRIATTN_OK) return st;
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
+      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_bias, bias, shape))
+    return TRIATTN_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.mask = mask;
+  a.o = o;
+  a.o_resid = o_resid;
+  a.lse = lse;
+  a.dO = dO;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dbias = dbias;
+  a.delta = reinterpret_cast<float*>(ws + w.delta_off);
+  a.dq_part = reinterpret_cast<float*>(ws + w.dq_off);
+  a.dbias_part = reinterpret_cast<float*>(ws + w.db_off);
+  a.B = shape->B;
+  a.N_o = shape->N_o;
+  a.N = shape->N;
+  a.H = shape->H;
+  a.wc = wait_ctl(dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (shape->D == 32) {
+    e = launch_bwd_preprocess<32>(a, s);
+    if (e == cudaSuccess) e = launch_bwd_main<32>(a, s);
+    if (e == cudaSuccess) e = launch_bwd_reduce_dq<32>(a, s);
+  } else {
+    e = launch_bwd_preprocess<16>(a, s);
+    if (e == cudaSuccess) e = launch_bwd_main<16>(a, s);
+    if (e == cudaSuccess) e = launch_bwd_reduce_dq<16>(a, s);
+  }
+  if (e == cudaSuccess) e = launch_bwd_reduce_dbias(a, s);
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+}
+
+triattn_status triattn_device_status(void* stream) {
+  int dev = 0;
+  triattn_status st = init_device(&dev);
+  if (st != TRIATTN_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TRIATTN_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, g_status_ptr[dev], sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  if (word == 0) return TRIATTN_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(g_status_ptr[dev], &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  return (word & kDevTimeout) ? TRIATTN_ERR_TIMEOUT : TRIATTN_ERR_CUDA;
+}
+
+void triattn_set_wait_limit_ns(unsigned long long cap_ns) {
+  g_wait_limit_ns.store(cap_ns > 0 ? cap_ns : kDefaultWaitNs);
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Kernel argument blocks and launch entry points shared by the C ABI layer.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace triattn {
+
+// Tile shape shared by all kernels: 128 query rows x 128 keys.
+constexpr int kTileQ = 128;
+constexpr int kTileK = 128;
+// Outer slices per CTA: forward (shared bias tile) and backward (outer group
+// of the key-tile-parallel backward).
+constexpr int kGroupFwd = 4;
+constexpr int kGroupBwd = 4;
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_bias;
+  const void* mask;
+  void* o;
+  float* lse;
+  void* o_resid;
+  int B, N_o, N, H;
+  WaitCtl wc;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_bias;
+  const void* mask;
+  const void* o;
+  const void* o_resid;
+  const float* lse;
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* dbias;
+  float* delta;      // [rows]
+  float* dq_part;    // [J_K][rows][D]
+  float* dbias_part; // [L][B*H*N*N]
+  int B, N_o, N, H;
+  WaitCtl wc;
+};
+
+template <int D> cudaError_t setup_fwd();
+template <int D> cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+template <int D> int fwd_smem_bytes(int N);
+
+template <int D> cudaError_t setup_bwd();
+template <int D> cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream);
+template <int D> cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
+template <int D> cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream);
+template <int D> int bwd_smem_bytes();
+
+}  // namespace triattn

@@ -1,0 +1,200 @@
+"""Python binding of libtriattn (ctypes; argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels behind the C ABI in
+``include/triattn.h``.  This module only checks tensor dtypes and shapes,
+allocates outputs with torch (device memory), passes raw pointers and the
+current CUDA stream, and raises on a non-OK status.  There is no fallback:
+if the shared library is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_LIB = None
+_LOCK = threading.Lock()
+
+STATUS = {
+    0: "TRIATTN_OK",
+    1: "TRIATTN_ERR_INVALID_ARG",
+    2: "TRIATTN_ERR_UNSUPPORTED",
+    3: "TRIATTN_ERR_WORKSPACE",
+    4: "TRIATTN_ERR_CUDA",
+    5: "TRIATTN_ERR_TIMEOUT",
+}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
+
+EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fwd", "tri_attn_bwd",
+            "triattn_device_status", "triattn_set_wait_limit_ns")
+
+
+class TriAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("N_o", ctypes.c_int), ("N", ctypes.c_int), ("H", ctypes.c_int),
+                ("D", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+def _declare(lib):
+    vp, sp = ctypes.c_void_p, ctypes.POINTER(Shape)
+    lib.triattn_status_string.argtypes = [ctypes.c_int]
+    lib.triattn_status_string.restype = ctypes.c_char_p
+    lib.triattn_bwd_workspace_bytes.argtypes = [sp]
+    lib.triattn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.tri_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.tri_attn_fwd.restype = ctypes.c_int
+    lib.tri_attn_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.tri_attn_bwd.restype = ctypes.c_int
+    lib.triattn_device_status.argtypes = [vp]
+    lib.triattn_device_status.restype = ctypes.c_int
+    lib.triattn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.triattn_set_wait_limit_ns.restype = None
+    return lib
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load(path: Optional[str] = None):
+    """Load libtriattn (built in-tree by ``build.build()``); raises if absent."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            p = path or library_path()
+            if not os.path.exists(p):
+                raise RuntimeError(f"libtriattn is not built ({p} missing): run __graft_entry__.build()")
+            _LIB = _declare(ctypes.CDLL(p))
+    return _LIB
+
+
+def shape_of(q: torch.Tensor) -> Shape:
+    if q.dim() != 5:
+        raise ValueError("q must be [B, N_o, H, N, D]")
+    B, No, H, N, D = q.shape
+    return Shape(B, No, N, H, D, 0)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, shape, dtype=torch.bfloat16):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _raise(code: int, where: str):
+    if code != OK:
+        raise TriAttnError(code, where)
+
+
+def bwd_workspace_bytes(q_or_shape) -> int:
+    s = q_or_shape if isinstance(q_or_shape, Shape) else shape_of(q_or_shape)
+    return int(load().triattn_bwd_workspace_bytes(ctypes.byref(s)))
+
+
+def tri_attn_fwd(q, k, v, bias, mask=None, *, save_residual: bool = True, out=None, stream=None):
+    """Forward.  Returns (o [B,N_o,H,N,D] bf16, lse [B,N_o,H,N] fp32,
+    o_resid bf16 or None).  ``out`` may pass preallocated (o, lse, o_resid)."""
+    s = shape_of(q)
+    B, No, H, N, D = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, name, (B, No, H, N, D))
+    _check(bias, "bias", (B, H, N, N))
+    if mask is not None:
+        _check(mask, "mask", (B, No, N))
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, No, H, N), dtype=torch.float32, device=q.device)
+        resid = torch.empty_like(q) if save_residual else None
+    else:
+        o, lse, resid = out
+    code = load().tri_attn_fwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(mask), _ptr(o),
+                               _ptr(lse), _ptr(resid), _stream_ptr(stream))
+    _raise(code, "tri_attn_fwd")
+    return o, lse, resid
+
+
+def tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, workspace=None, out=None, stream=None):
+    """Backward.  ``o_resid=None`` turns the residual compensation off.
+    Returns (dq, dk, dv, dbias) in bf16."""
+    s = shape_of(q)
+    B, No, H, N, D = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(t, name, (B, No, H, N, D))
+    if o_resid is not None:
+        _check(o_resid, "o_resid", (B, No, H, N, D))
+    _check(bias, "bias", (B, H, N, N))
+    _check(lse, "lse", (B, No, H, N), torch.float32)
+    if mask is not None:
+        _check(mask, "mask", (B, No, N))
+    need = bwd_workspace_bytes(s)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        dbias = torch.empty_like(bias)
+    else:
+        dq, dk, dv, dbias = out
+    code = load().tri_attn_bwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(mask), _ptr(o),
+                               _ptr(o_resid), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+                               _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                               _stream_ptr(stream))
+    _raise(code, "tri_attn_bwd")
+    return dq, dk, dv, dbias
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (then clear) the device status code."""
+    return int(load().triattn_device_status(_stream_ptr(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    load().triattn_set_wait_limit_ns(ctypes.c_ulonglong(int(ns)))
+
+
+class TriAttnFunction(torch.autograd.Function):
+    """Autograd wrapper: forward saves o, lse and the residual; backward runs
+    the compensated key-tile-parallel backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, bias, mask=None):
+        o, lse, resid = tri_attn_fwd(q, k, v, bias, mask, save_residual=True)
+        ctx.save_for_backward(q, k, v, bias, o, lse, resid)
+        ctx.mask = mask
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, bias, o, lse, resid = ctx.saved_tensors
+        dq, dk, dv, dbias = tri_attn_bwd(q, k, v, bias, ctx.mask, o, resid, lse, do.contiguous())
+        return dq, dk, dv, dbias, None
+
+
+def triangle_attention(q, k, v, bias, mask=None):
+    """Differentiable triangular attention (BF16 in, BF16 out)."""
+    return TriAttnFunction.apply(q, k, v, bias, mask)

@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark of triangular attention forward + backward on GB300.
+
+One step = tri_attn_fwd + tri_attn_bwd (preprocess, key-tile-parallel main
+kernel, dQ and dbias reductions) over one batch of seeded synthetic BF16
+inputs of the headline crop (B=1, N=N_o=768, H=4, D=32, last 8% of keys
+masked).  FLOPs follow the convention fwd = 4U, bwd = 10U (five GEMMs with
+the S recompute), step = 14U, U = B*N_o*H*N*N*D.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the FP64 CPU
+oracle instead (the only reference this path has; it is a deliberately slow
+program, so the ratio is context, not a headline).
+
+Multi-GPU (torchrun): every rank runs its own independent problem of the
+same shape (the method's slices are independent; no data-path collective),
+so scaling is weak and ``value`` is the total over all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tri-attn fwd+bwd TFLOP/s (N=768 H=4 D=32)"
+UNIT = "TFLOP/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="crop768")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def flops(w):
+    U = w.B * w.No * w.H * w.N * w.N * w.D
+    return 4 * U, 10 * U, 14 * U
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_burst": d.get("bf16_tflops", 1900.0), "bf16_sustained": d.get("bf16_tflops_sustained", 1700.0),
+                "hbm_gbs": d.get("hbm_gbs", 6800.0), "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"triattn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        try:
+            self.f.close()
+        except Exception:
+            pass
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                    power.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def combine_ranks(local_ms: float, flop_per_step: int, steps: int, world: int, device=None) -> tuple:
+    """Max of the per-rank elapsed times over all ranks (the slowest rank
+    defines the job's time) and the whole-job throughput in TFLOP/s: every
+    rank processed `steps` steps of its own problem."""
+    import torch
+    import torch.distributed as dist
+    ms = float(local_ms)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, flop_per_step * steps * world / (ms * 1e-3) / 1e12
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "tri_attn_fwd": ["protein_folding_triangle_gb300/csrc/fwd.cu", "protein_folding_triangle_gb300/csrc/ptx.cuh"],
+    "bwd_main": ["protein_folding_triangle_gb300/csrc/bwd.cu", "protein_folding_triangle_gb300/csrc/ptx.cuh"],
+    "bwd_preprocess": ["protein_folding_triangle_gb300/csrc/bwd.cu"],
+    "bwd_reduce_dq": ["protein_folding_triangle_gb300/csrc/bwd.cu"],
+    "bwd_reduce_dbias": ["protein_folding_triangle_gb300/csrc/bwd.cu"],
+}
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != source_sha(KERNEL_SOURCES[kernel]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def kernel_work(w, name):
+    """Algorithmic work per launch: (amount, unit, bound)."""
+    U = w.B * w.No * w.H * w.N * w.N * w.D
+    rows = w.B * w.No * w.H * w.N
+    jk = (w.N + 127) // 128
+    groups = w.No // 4
+    if name == "tri_attn_fwd":
+        return 4 * U, "flop", "tensor"
+    if name == "bwd_main":
+        return 10 * U, "flop", "tensor"
+    if name == "bwd_preprocess":
+        return 3 * rows * w.D * 2 + rows * 4, "byte", "hbm"
+    if name == "bwd_reduce_dq":
+        return jk * rows * w.D * 4 + rows * w.D * 2, "byte", "hbm"
+    if name == "bwd_reduce_dbias":
+        return groups * w.B * w.H * w.N * w.N * 4 + w.B * w.H * w.N * w.N * 2, "byte", "hbm"
+    raise KeyError(name)
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w, x, seconds: float, gpu_out=None):
+    """Time the FP64 oracle (fwd + bwd) on a bounded sample of the workload:
+    the first n outer slices of example 0, all heads.  Returns the
+    cpu_baseline dict and, if GPU outputs are given, the relative RMSE of the
+    GPU's O, dQ, dK and dV on the sampled slices."""
+    import numpy as np
+    from oracle import oracle as O
+
+    O.build()
+
+    def run(n):
+        sub = {k: (None if v is None else v[:1, :n].contiguous()) for k, v in x.items() if k != "bias"}
+        bias = x["bias"][:1]
+        t0 = time.perf_counter()
+        o, lse = O.fwd(sub["q"], sub["k"], sub["v"], bias, sub["mask"])
+        dq, dk, dv, _ = O.bwd(sub["q"], sub["k"], sub["v"], bias, sub["mask"], sub["do"])
+        return time.perf_counter() - t0, {"o": o, "dq": dq, "dk": dk, "dv": dv}
+
+    t_cal, _ = run(2)
+    per_slice = t_cal / 2
+    n = int(max(2, min(w.No, seconds / max(per_slice, 1e-6))))
+    dt, ref = run(n)
+    U = 1 * n * w.H * w.N * w.N * w.D
+    value = 14 * U / dt / 1e12
+    res = {"value": value, "unit": UNIT, "cores": O.max_threads(), "kind": "oracle",
+           "sample": f"FP64 oracle fwd+bwd on outer slices 0..{n - 1} of example 0, all {w.H} heads "
+                     f"({n}/{w.No * w.B} slices, {dt:.1f} s; 14*U FLOP convention)",
+           "seconds": dt}
+    rm = None
+    if gpu_out is not None:
+        def rel(a, r):
+            a = a[:1, :n].float().cpu().double().numpy()
+            return float(np.sqrt(np.mean((a - r) ** 2)) / np.sqrt(np.mean(r ** 2)))
+        rm = {k: rel(gpu_out[k], ref[k]) for k in ("o", "dq", "dk", "dv")}
+    return res, rm
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch  # noqa: F401
+    from protein_folding_triangle_gb300 import synthetic as S
+    w = S.WORKLOADS[args.workload]
+    x = S.make_inputs(w, seed=args.seed)
+    per_step = []
+    info = None
+    budget = max(2.0, args.cpu_seconds / max(args.steps + args.warmup, 1))
+    for i in range(args.warmup + args.steps):
+        res, _ = oracle_sample(w, x, budget)
+        if i >= args.warmup:
+            per_step.append(res)
+            info = res
+    val = statistics.median(r["value"] for r in per_step)
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "impl": "reference", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.describe(), "B": w.B, "N": w.N, "H": w.H, "D": w.D},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU leg
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from protein_folding_triangle_gb300 import build as B
+    from protein_folding_triangle_gb300 import synthetic as S
+    from protein_folding_triangle_gb300 import triattn as T
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    B.build()
+    T.load()
+    w = S.WORKLOADS[args.workload]
+    x = S.make_inputs(w, seed=args.seed + rank)
+    xd = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_mem = torch.cuda.memory_allocated(dev)
+    o = torch.empty_like(xd["q"])
+    lse = torch.empty(xd["q"].shape[:-1], dtype=torch.float32, device=dev)
+    resid = torch.empty_like(xd["q"])
+    dq, dk, dv = torch.empty_like(xd["q"]), torch.empty_like(xd["q"]), torch.empty_like(xd["q"])
+    dbias = torch.empty_like(xd["bias"])
+    wsb = torch.empty(T.bwd_workspace_bytes(xd["q"]), dtype=torch.uint8, device=dev)
+
+    def step(inp):
+        T.tri_attn_fwd(inp["q"], inp["k"], inp["v"], inp["bias"], inp["mask"], out=(o, lse, resid))
+        T.tri_attn_bwd(inp["q"], inp["k"], inp["v"], inp["bias"], inp["mask"], o, resid, lse, inp["do"],
+                       workspace=wsb, out=(dq, dk, dv, dbias))
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step(xd)
+    torch.cuda.synchronize(dev)
+    if T.device_status() != T.OK:
+        raise SystemExit("device status not OK after warm-up")
+
+    # ---------------- device-timed region (inputs resident in HBM)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        T.trace_enable(True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(xd)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        T.trace_enable(False)
+        barrier()
+    trace = T.trace_read()
+    peak_mem = torch.cuda.max_memory_allocated(dev) - base_mem
+    f_fwd, f_bwd, f_step = flops(w)
+    ms, value = combine_ranks(e0.elapsed_time(e1), f_step, args.steps, ws, dev)
+
+    # ---------------- end-to-end: pinned host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hx = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
+        hgrads = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv, dbias)]
+        h2d = sum(v.numel() * v.element_size() for v in hx.values() if v is not None)
+        d2h = sum(t.numel() * t.element_size() for t in hgrads)
+        dx = {k: (None if v is None else torch.empty_like(xd[k])) for k, v in hx.items()}
+
+        def e2e_step():
+            for k, v in hx.items():
+                if v is not None:
+                    dx[k].copy_(v, non_blocking=True)
+            step(dx)
+            for hg, g in zip(hgrads, (dq, dk, dv, dbias)):
+                hg.copy_(g, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems, evalue = combine_ranks(a0.elapsed_time(a1), f_step, args.steps, ws, dev)
+        e2e = {"value": round(evalue, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(ems / args.steps, 4)}
+    if T.device_status() != T.OK:
+        raise SystemExit("device status not OK after timing")
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    # per-kernel summary from the live trace
+    kernels = {}
+    total_k = sum(e["total_ms"] for e in trace.values())
+    for name, e in trace.items():
+        amount, unit, bound = kernel_work(w, name)
+        mean_ms = e["mean_ms"]
+        rate = amount / (mean_ms * 1e-3)
+        kernels[name] = {"launches": e["launches"], "mean_ms": round(mean_ms, 4),
+                         "share": round(e["total_ms"] / total_k, 4),
+                         ("TFLOP/s" if unit == "flop" else "GB/s"): round(rate / (1e12 if unit == "flop" else 1e9), 2)}
+    dom = max(trace, key=lambda n: trace[n]["total_ms"])
+    amount, unit, bound = kernel_work(w, dom)
+    dom_ms = trace[dom]["mean_ms"]
+    if unit == "flop":
+        achieved = amount / (dom_ms * 1e-3) / 1e12
+        peak = pk["bf16_sustained"]
+        runit = "TFLOP/s"
+    else:
+        achieved = amount / (dom_ms * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        runit = "GB/s"
+    traffic = ncu_traffic(dom)
+    fwd_ms = trace.get("tri_attn_fwd", {}).get("mean_ms")
+    bwd_ms = sum(trace[n]["mean_ms"] for n in ("bwd_preprocess", "bwd_main", "bwd_reduce_dq", "bwd_reduce_dbias")
+                 if n in trace)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.describe(), "B": w.B, "N": w.N, "N_o": w.No, "H": w.H, "D": w.D,
+                   "seed": args.seed, "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                   "l2": "inputs larger than L2 (Q,K,V,dO,O,E 6x144 MiB + FP32 partials per step), no flush",
+                   "flop_convention": "fwd 4U, bwd 10U, step 14U, U=B*N_o*H*N*N*D (dense keys)"},
+        "fwd_tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2) if fwd_ms else None,
+        "bwd_tflops": round(f_bwd / (bwd_ms * 1e-3) / 1e12, 2) if bwd_ms else None,
+        "frac_bf16_peak": {"sustained": round(value / ws / pk["bf16_sustained"], 4),
+                           "burst": round(value / ws / pk["bf16_burst"], 4), "peaks": pk["source"]},
+        "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{pk['source']} ({'bf16 sustained' if unit == 'flop' else 'hbm copy'})"},
+        "kernels": kernels,
+        "gpu_launches": sum(e["launches"] for e in trace.values()),
+        "peak_mem_bytes": int(peak_mem),
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        cb, rm = oracle_sample(w, x, args.cpu_seconds, gpu_out={"o": o, "dq": dq, "dk": dk, "dv": dv})
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["rel_rmse_vs_fp64_on_sample"] = rm
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

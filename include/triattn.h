@@ -21,7 +21,11 @@
  *             bias, dbias                         [B, H, N, N]      bf16
  *             mask (optional, additive)           [B, N_o, N]       bf16
  *             lse                                 [B, N_o, H, N]    fp32 (natural log)
- *  - N_o must equal N (Table 1: "N_o = N"), D must be 16 or 32, N >= 1.
+ *  - N_o must equal N (Table 1: "N_o = N"), D must be 16 or 32, and N must
+ *    be a multiple of 8 with 8 <= N <= 4096 (TMA needs 16-byte row strides
+ *    of the [N, N] bias; the forward stages the key mask of every key tile
+ *    in shared memory).  Any N in that set works, ragged or not relative to
+ *    the 128-row tiles.
  *  - A row whose keys are all masked (every score -inf) yields O = 0,
  *    residual 0, lse = -inf and zero gradient contributions.
  *  - The caller owns every buffer, the workspace and the stream.  The library
@@ -138,6 +142,36 @@ triattn_status triattn_device_status(void* stream);
  * limit (about 2 s).  0 restores the default.
  */
 void triattn_set_wait_limit_ns(unsigned long long cap_ns);
+
+/*
+ * Kernel tracing.  triattn_trace_enable(1) clears earlier records and makes
+ * every later kernel launch of the library record a pair of CUDA events on
+ * its launch stream (on = 0 stops recording; records are kept).
+ * triattn_trace_read() synchronises the recorded events and writes one entry
+ * per kernel kind that launched (at most `max_entries`), returning the
+ * number written, or -1 if an event query failed.  Kernel names are static
+ * strings.  Recording costs one cudaEventRecord before and after each launch.
+ */
+typedef struct {
+  const char* kernel;
+  int launches;
+  double total_ms;
+  double min_ms;
+  double max_ms;
+} triattn_trace_entry;
+
+void triattn_trace_enable(int on);
+int triattn_trace_read(triattn_trace_entry* out, int max_entries);
+
+/*
+ * Test hook, off by default.  While `on` is nonzero, the forward kernel's
+ * producer warp skips its first K-tile load, so nothing ever completes the
+ * barrier the MMA warp waits on: the bounded wait runs out, the kernel
+ * records TRIATTN_ERR_TIMEOUT in the device status word and every CTA
+ * returns.  Used only to test timeout reporting (with a short limit set by
+ * triattn_set_wait_limit_ns); outputs of such a call are undefined.
+ */
+void triattn_test_set_starve(int on);
 
 #ifdef __cplusplus
 }

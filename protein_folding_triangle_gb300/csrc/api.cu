@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/triattn.h"
 #include "kernels.cuh"
@@ -110,6 +111,46 @@ WsLayout ws_layout(const triattn_shape* s) {
   return w;
 }
 
+// ---------------------------------------------------------------- tracing
+enum KernelKind { kKFwd = 0, kKPre, kKMain, kKRedDq, kKRedDb, kKinds };
+const char* const kKernelName[kKinds] = {"tri_attn_fwd", "bwd_preprocess", "bwd_main", "bwd_reduce_dq",
+                                         "bwd_reduce_dbias"};
+struct TraceRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;  // events owned by the library, reused
+size_t g_event_next = 0;
+std::atomic<int> g_test_starve{0};
+
+cudaEvent_t next_event() {
+  if (g_event_next == g_event_pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_event_pool.push_back(e);
+  }
+  return g_event_pool[g_event_next++];
+}
+
+template <typename F>
+cudaError_t traced(int kind, cudaStream_t s, F launch) {
+  std::unique_lock<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on) {
+    lk.unlock();
+    return launch();
+  }
+  cudaEvent_t ea = next_event(), eb = next_event();
+  if (ea == nullptr || eb == nullptr) return cudaErrorMemoryAllocation;
+  cudaEventRecord(ea, s);
+  const cudaError_t e = launch();
+  cudaEventRecord(eb, s);
+  g_trace.push_back({kind, ea, eb});
+  return e;
+}
+
 WaitCtl wait_ctl(int dev) {
   WaitCtl wc;
   wc.limit_ns = g_wait_limit_ns.load();
@@ -164,9 +205,11 @@ triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const voi
   a.N_o = shape->N_o;
   a.N = shape->N;
   a.H = shape->H;
+  a.test_starve = g_test_starve.load();
   a.wc = wait_ctl(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = (shape->D == 32) ? launch_fwd<32>(a, s) : launch_fwd<16>(a, s);
+  const cudaError_t e =
+      traced(kKFwd, s, [&] { return (shape->D == 32) ? launch_fwd<32>(a, s) : launch_fwd<16>(a, s); });
   return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
 }
 
@@ -209,17 +252,13 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
   a.H = shape->H;
   a.wc = wait_ctl(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (shape->D == 32) {
-    e = launch_bwd_preprocess<32>(a, s);
-    if (e == cudaSuccess) e = launch_bwd_main<32>(a, s);
-    if (e == cudaSuccess) e = launch_bwd_reduce_dq<32>(a, s);
-  } else {
-    e = launch_bwd_preprocess<16>(a, s);
-    if (e == cudaSuccess) e = launch_bwd_main<16>(a, s);
-    if (e == cudaSuccess) e = launch_bwd_reduce_dq<16>(a, s);
-  }
-  if (e == cudaSuccess) e = launch_bwd_reduce_dbias(a, s);
+  const bool d32 = shape->D == 32;
+  cudaError_t e = traced(kKPre, s, [&] { return d32 ? launch_bwd_preprocess<32>(a, s) : launch_bwd_preprocess<16>(a, s); });
+  if (e == cudaSuccess)
+    e = traced(kKMain, s, [&] { return d32 ? launch_bwd_main<32>(a, s) : launch_bwd_main<16>(a, s); });
+  if (e == cudaSuccess)
+    e = traced(kKRedDq, s, [&] { return d32 ? launch_bwd_reduce_dq<32>(a, s) : launch_bwd_reduce_dq<16>(a, s); });
+  if (e == cudaSuccess) e = traced(kKRedDb, s, [&] { return launch_bwd_reduce_dbias(a, s); });
   return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
 }
 
@@ -241,5 +280,35 @@ triattn_status triattn_device_status(void* stream) {
 void triattn_set_wait_limit_ns(unsigned long long cap_ns) {
   g_wait_limit_ns.store(cap_ns > 0 ? cap_ns : kDefaultWaitNs);
 }
+
+void triattn_trace_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (on) {
+    g_trace.clear();
+    g_event_next = 0;
+  }
+  g_trace_on = on != 0;
+}
+
+int triattn_trace_read(triattn_trace_entry* out, int max_entries) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  triattn_trace_entry acc[kKinds];
+  for (int k = 0; k < kKinds; ++k) acc[k] = {kKernelName[k], 0, 0.0, 1e30, 0.0};
+  for (const TraceRec& r : g_trace) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return -1;
+    triattn_trace_entry& e = acc[r.kind];
+    e.launches += 1;
+    e.total_ms += ms;
+    if (ms < e.min_ms) e.min_ms = ms;
+    if (ms > e.max_ms) e.max_ms = ms;
+  }
+  int n = 0;
+  for (int k = 0; k < kKinds && n < max_entries; ++k)
+    if (acc[k].launches > 0 && out != nullptr) out[n++] = acc[k];
+  return n;
+}
+
+void triattn_test_set_starve(int on) { g_test_starve.store(on != 0 ? 1 : 0); }
 
 }  // extern "C"

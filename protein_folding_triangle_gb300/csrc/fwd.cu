@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
                const uint16_t* __restrict__ mask, uint16_t* __restrict__ out_o, float* __restrict__ out_lse,
-               uint16_t* __restrict__ out_resid, int N_o, int N, int H, WaitCtl wc) {
+               uint16_t* __restrict__ out_resid, int N_o, int N, int H, int test_starve, WaitCtl wc) {
   using L = FwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -143,8 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t par = ((s / NSLOT) & 1) ^ 1;
           const int boh = (b * N_o + o0 + g) * H + h;
           if (!mbar_wait(&bars->k_empty[slot], par, wc, abort)) break;
-          mbar_expect_tx(&bars->k_full[slot], L::kTile);
-          tma_load_3d(sm + L::kK + slot * L::kTile, &tm_k, &bars->k_full[slot], 0, j * BN, boh);
+          if (!(test_starve && s == 0)) {
+            mbar_expect_tx(&bars->k_full[slot], L::kTile);
+            tma_load_3d(sm + L::kK + slot * L::kTile, &tm_k, &bars->k_full[slot], 0, j * BN, boh);
+          }
           if (!mbar_wait(&bars->v_empty[slot], par, wc, abort)) break;
           mbar_expect_tx(&bars->v_full[slot], L::kTile);
           tma_load_3d(sm + L::kV + slot * L::kTile, &tm_v, &bars->v_full[slot], 0, j * BN, boh);
@@ -389,7 +391,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (JK > FwdSmem<D>::kMaxJK) return cudaErrorInvalidValue;
   fwd_kernel<D><<<grid, kThreads, FwdSmem<D>::bytes(JK), stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_bias, static_cast<const uint16_t*>(a.mask), static_cast<uint16_t*>(a.o), a.lse,
-      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.wc);
+      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.test_starve, a.wc);
   return cudaGetLastError();
 }
 

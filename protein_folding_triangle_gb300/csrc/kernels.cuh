@@ -24,6 +24,7 @@ struct FwdArgs {
   float* lse;
   void* o_resid;
   int B, N_o, N, H;
+  int test_starve;   // test hook: skip the first K-tile load
   WaitCtl wc;
 };
 

@@ -31,7 +31,13 @@ STATUS = {
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 
 EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fwd", "tri_attn_bwd",
-            "triattn_device_status", "triattn_set_wait_limit_ns")
+            "triattn_device_status", "triattn_set_wait_limit_ns", "triattn_trace_enable", "triattn_trace_read",
+            "triattn_test_set_starve")
+
+
+class TraceEntry(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_char_p), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double),
+                ("min_ms", ctypes.c_double), ("max_ms", ctypes.c_double)]
 
 
 class TriAttnError(RuntimeError):
@@ -59,6 +65,12 @@ def _declare(lib):
     lib.triattn_device_status.restype = ctypes.c_int
     lib.triattn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.triattn_set_wait_limit_ns.restype = None
+    lib.triattn_trace_enable.argtypes = [ctypes.c_int]
+    lib.triattn_trace_enable.restype = None
+    lib.triattn_trace_read.argtypes = [ctypes.POINTER(TraceEntry), ctypes.c_int]
+    lib.triattn_trace_read.restype = ctypes.c_int
+    lib.triattn_test_set_starve.argtypes = [ctypes.c_int]
+    lib.triattn_test_set_starve.restype = None
     return lib
 
 
@@ -175,6 +187,31 @@ def device_status(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     load().triattn_set_wait_limit_ns(ctypes.c_ulonglong(int(ns)))
+
+
+def trace_enable(on: bool = True) -> None:
+    """Start (clearing old records) or stop per-kernel CUDA-event tracing."""
+    load().triattn_trace_enable(1 if on else 0)
+
+
+def trace_read() -> dict:
+    """Per-kernel totals of the traced launches: {name: {launches, total_ms,
+    mean_ms, min_ms, max_ms}} (synchronises the recorded events)."""
+    buf = (TraceEntry * 16)()
+    n = load().triattn_trace_read(buf, 16)
+    if n < 0:
+        raise TriAttnError(ERR_CUDA, "triattn_trace_read")
+    out = {}
+    for e in buf[:n]:
+        name = e.kernel.decode()
+        out[name] = {"launches": e.launches, "total_ms": e.total_ms, "mean_ms": e.total_ms / max(e.launches, 1),
+                     "min_ms": e.min_ms, "max_ms": e.max_ms}
+    return out
+
+
+def test_set_starve(on: bool) -> None:
+    """Test hook: starve the forward's MMA warp so its bounded wait runs out."""
+    load().triattn_test_set_starve(1 if on else 0)
 
 
 class TriAttnFunction(torch.autograd.Function):

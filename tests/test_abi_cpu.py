@@ -1,0 +1,137 @@
+"""CPU-only checks of the C ABI boundary: the library loads, exports every
+function include/triattn.h declares, and rejects bad arguments before it
+touches a GPU.  Also the multi-rank timing combination of bench.py over two
+gloo ranks."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from protein_folding_triangle_gb300 import build as B
+from protein_folding_triangle_gb300 import triattn as T
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return T.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "triattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    return sorted(set(n for n in names if n.startswith(("tri_attn", "triattn"))))
+
+
+def test_exports_every_declared_function(lib):
+    declared = header_functions()
+    assert "tri_attn_fwd" in declared and "tri_attn_bwd" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(T.EXPORTED) >= set(declared)
+
+
+def test_status_strings(lib):
+    for code, name in T.STATUS.items():
+        assert lib.triattn_status_string(code).decode() == name
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: validation fails first
+
+
+def call_fwd(lib, shape, **ptrs):
+    p = {n: ctypes.c_void_p(FAKE) for n in ("q", "k", "v", "bias", "o", "lse")}
+    p.update({"mask": None, "o_resid": None})
+    p.update(ptrs)
+    return lib.tri_attn_fwd(ctypes.byref(shape), p["q"], p["k"], p["v"], p["bias"], p["mask"], p["o"], p["lse"],
+                            p["o_resid"], None)
+
+
+def call_bwd(lib, shape, ws_bytes, ws=FAKE, **ptrs):
+    names = ("q", "k", "v", "bias", "o", "lse", "dO", "dq", "dk", "dv", "dbias")
+    p = {n: ctypes.c_void_p(FAKE) for n in names}
+    p.update({"mask": None, "o_resid": None})
+    p.update(ptrs)
+    return lib.tri_attn_bwd(ctypes.byref(shape), p["q"], p["k"], p["v"], p["bias"], p["mask"], p["o"],
+                            p["o_resid"], p["lse"], p["dO"], p["dq"], p["dk"], p["dv"], p["dbias"],
+                            None if ws is None else ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((1, 48, 48, 2, 24, 0), T.ERR_UNSUPPORTED),   # D not in {16, 32}
+    ((1, 40, 48, 2, 16, 0), T.ERR_UNSUPPORTED),   # N_o != N
+    ((1, 44, 44, 2, 16, 0), T.ERR_UNSUPPORTED),   # N not a multiple of 8
+    ((1, 8192, 8192, 1, 16, 0), T.ERR_UNSUPPORTED),  # N beyond 4096
+    ((0, 48, 48, 2, 16, 0), T.ERR_INVALID_ARG),   # empty batch
+    ((1, 0, 0, 2, 16, 0), T.ERR_INVALID_ARG),     # empty crop
+    ((1, 48, 48, 0, 16, 0), T.ERR_INVALID_ARG),   # no heads
+    ((1, 48, 48, 2, 16, 1), T.ERR_INVALID_ARG),   # reserved flags
+])
+def test_bad_shapes(lib, shape, code):
+    s = T.Shape(*shape)
+    assert call_fwd(lib, s) == code
+    assert call_bwd(lib, s, 1 << 40) == code
+    assert lib.triattn_bwd_workspace_bytes(ctypes.byref(s)) == 0
+
+
+def test_null_and_misaligned_pointers(lib):
+    s = T.Shape(1, 48, 48, 2, 16, 0)
+    assert call_fwd(lib, s, q=None) == T.ERR_INVALID_ARG
+    assert call_fwd(lib, s, lse=None) == T.ERR_INVALID_ARG
+    assert call_fwd(lib, s, k=ctypes.c_void_p(FAKE + 2)) == T.ERR_INVALID_ARG
+    assert call_fwd(lib, s, mask=ctypes.c_void_p(FAKE + 8)) == T.ERR_INVALID_ARG
+    assert call_bwd(lib, s, 1 << 40, dbias=None) == T.ERR_INVALID_ARG
+    assert call_bwd(lib, s, 1 << 40, o_resid=ctypes.c_void_p(FAKE + 4)) == T.ERR_INVALID_ARG
+
+
+def test_workspace_checks(lib):
+    s = T.Shape(1, 48, 48, 2, 16, 0)
+    need = lib.triattn_bwd_workspace_bytes(ctypes.byref(s))
+    # layout: delta [rows] + dQ partials [J_K][rows][D] + dbias partials [N_o/4][B*H*N*N], FP32, 256-aligned
+    rows = 1 * 48 * 2 * 48
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert need == r256(rows * 4) + r256(1 * rows * 16 * 4) + r256(12 * 1 * 2 * 48 * 48 * 4)
+    assert call_bwd(lib, s, need - 1) == T.ERR_WORKSPACE
+    assert call_bwd(lib, s, need, ws=None) == T.ERR_WORKSPACE
+    assert call_bwd(lib, s, need, ws=FAKE + 16) == T.ERR_WORKSPACE
+
+
+def test_trace_read_empty(lib):
+    T.trace_enable(True)
+    T.trace_enable(False)
+    assert T.trace_read() == {}
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms, value = bench.combine_ranks(10.0 * (rank + 1), flop_per_step=10 ** 12, steps=4, world=world)
+    out.put((rank, ms, value))
+    dist.destroy_process_group()
+
+
+def test_combine_ranks_two_gloo_ranks():
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, value in res:
+        assert ms == 20.0                      # the slowest rank's time
+        assert abs(value - 2 * 4 / 0.020) < 1e-9  # 2 ranks x 4 steps x 1 TFLOP over 20 ms, in TFLOP/s

@@ -130,6 +130,42 @@ triattn_status tri_attn_bwd(const triattn_shape* shape,
                             void* stream);
 
 /*
+ * Allocation-free backward.  The paper has no counterpart to this entry
+ * point; it is a deployment convenience of this library.
+ *
+ * Some callers cannot allocate device memory: a plugin inside a host
+ * framework that owns all device memory and does not let extensions call
+ * cudaMalloc, or a latency-critical loop that cannot pay for cudaMalloc's
+ * implicit device synchronisation.  This entry point runs the same four
+ * backward kernels as tri_attn_bwd but takes no workspace: its scratch
+ * (delta and the FP32 partials) lives in a file-scope device array of
+ * TRIATTN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - A shape whose triattn_bwd_workspace_bytes() exceeds
+ *     TRIATTN_NOALLOC_SCRATCH_BYTES is rejected with TRIATTN_ERR_WORKSPACE
+ *     before anything is launched (B=1, N=48, H=2, D=16 needs 0.5 MiB;
+ *     a 384-token crop with H=4, D=32 needs 455 MiB and is rejected).
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress while that device is current.  Make that first
+ *     call before any stream capture.
+ *   - It calls no cudaMalloc, no cudaFree and no allocating library routine.
+ *   - Every call uses the same array, which keeps the previous call's
+ *     contents.  Nothing needs clearing: the kernels write every scratch word
+ *     before they read it.  Calls that overlap on the GPU (other streams, or
+ *     other host threads without ordering) race on the array; the caller
+ *     must serialise them.
+ * Arguments, layouts and the other error codes are those of tri_attn_bwd.
+ */
+#define TRIATTN_NOALLOC_SCRATCH_BYTES (64ull << 20)
+triattn_status tri_attn_bwd_noalloc(const triattn_shape* shape,
+                                    const void* q, const void* k, const void* v,
+                                    const void* bias, const void* mask,
+                                    const void* o, const void* o_resid, const float* lse,
+                                    const void* dO,
+                                    void* dq, void* dk, void* dv, void* dbias,
+                                    void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * kernels set when a bounded wait gives up.  Returns TRIATTN_OK,
  * TRIATTN_ERR_TIMEOUT, or TRIATTN_ERR_CUDA if the synchronisation failed.

@@ -1,0 +1,50 @@
+// Allocation-free entry point of the backward: the same four kernels as
+// tri_attn_bwd, with their scratch memory in a file-scope device array
+// instead of a caller-provided workspace.  Declared in include/triattn.h.
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/triattn.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = TRIATTN_NOALLOC_SCRATCH_BYTES;
+
+// The scratch array.  In host code this name is only a host-side stand-in;
+// its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void* g_scratch_dev[64] = {};  // device address of g_noalloc_scratch, per device
+
+}  // namespace
+
+extern "C" triattn_status tri_attn_bwd_noalloc(const triattn_shape* shape, const void* q, const void* k,
+                                               const void* v, const void* bias, const void* mask, const void* o,
+                                               const void* o_resid, const float* lse, const void* dO, void* dq,
+                                               void* dk, void* dv, void* dbias, void* stream) {
+  const size_t need = triattn_bwd_workspace_bytes(shape);
+  if (need == 0) {
+    // invalid shape: let the regular entry point report which check failed
+    return tri_attn_bwd(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, nullptr, 0, stream);
+  }
+  if (need > kScratchBytes) return TRIATTN_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TRIATTN_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_scratch_dev[dev] == nullptr) {
+      // one-time set-up on this device (the device is current here)
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return TRIATTN_ERR_CUDA;
+      g_scratch_dev[dev] = p;
+    }
+    scratch = g_scratch_dev[dev];
+  }
+  return tri_attn_bwd(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, scratch, kScratchBytes,
+                      stream);
+}

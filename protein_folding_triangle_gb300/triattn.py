@@ -32,7 +32,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = ran
 
 EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fwd", "tri_attn_bwd",
             "triattn_device_status", "triattn_set_wait_limit_ns", "triattn_trace_enable", "triattn_trace_read",
-            "triattn_test_set_starve")
+            "triattn_test_set_starve", "tri_attn_bwd_noalloc")
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class TraceEntry(ctypes.Structure):
@@ -71,6 +73,8 @@ def _declare(lib):
     lib.triattn_trace_read.restype = ctypes.c_int
     lib.triattn_test_set_starve.argtypes = [ctypes.c_int]
     lib.triattn_test_set_starve.restype = None
+    lib.tri_attn_bwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.tri_attn_bwd_noalloc.restype = ctypes.c_int
     return lib
 
 

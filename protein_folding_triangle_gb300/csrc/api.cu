@@ -10,7 +10,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/triattn.h"
+#include "triattn.h"
 #include "kernels.cuh"
 
 namespace triattn {
@@ -99,15 +99,19 @@ struct WsLayout {
   size_t delta_off, dq_off, db_off, total;
 };
 
+// delta [rows] FP32; dQ partials [J_K][slices][J_Q][128 x D] FP32; dbias partials
+// [N_o/G][B*H][J_Q][J_K][128 x 128] FP32 (partials padded to whole tiles).
 WsLayout ws_layout(const triattn_shape* s) {
   const size_t rows = static_cast<size_t>(s->B) * s->N_o * s->H * s->N;
+  const size_t slices = static_cast<size_t>(s->B) * s->N_o * s->H;
   const size_t jk = (s->N + kTileK - 1) / kTileK;
+  const size_t jq = (s->N + kTileQ - 1) / kTileQ;
   const size_t groups = s->N_o / kGroupBwd;
   WsLayout w;
   w.delta_off = 0;
   w.dq_off = round_up(rows * 4, 256);
-  w.db_off = w.dq_off + round_up(jk * rows * s->D * 4, 256);
-  w.total = w.db_off + round_up(groups * s->B * s->H * static_cast<size_t>(s->N) * s->N * 4, 256);
+  w.db_off = w.dq_off + round_up(jk * slices * jq * kTileQ * s->D * 4, 256);
+  w.total = w.db_off + round_up(groups * s->B * s->H * jq * jk * kTileQ * kTileK * 4, 256);
   return w;
 }
 

@@ -19,7 +19,6 @@ namespace {
 constexpr int BM = kTileQ;   // query rows per tile
 constexpr int BN = kTileK;   // keys per CTA (TMEM lanes of dK / dV)
 constexpr int G = kGroupBwd; // outer slices per CTA
-constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- preprocess
@@ -52,6 +51,28 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
 }
 
 // ---------------------------------------------------------------- main kernel
+//
+// Thread roles (18 warps):
+//   warp 0       TMA producer: K, V of the G slices once; per query tile one
+//                bias tile; per (query tile, slice) the Q and dO tiles.
+//   warp 1       TMEM owner and tcgen05 MMA issuer (converged warp, one
+//                elected lane issues; descriptors are precomputed).
+//   warps 2-17   four elementwise warpgroups.  Each covers all 128 TMEM lanes
+//                (thread = query row for S / dP / dQ, key row for dK / dV);
+//                warpgroup w handles key columns [32w, 32w + 32).
+//
+// Per step s = (query tile i, slice g), two elementwise phases:
+//   P-phase   P = 2^(S log2e/sqrt(D) + (bias + mask) log2e - lse log2e)
+//             -> BF16 P into 128-byte-swizzled shared memory (FP32 P stays
+//             in registers); the S columns of TMEM are then free.
+//   dS-phase  dS = P (dP - delta); dbias accumulator += dS (FP32 registers);
+//             BF16 dS into shared memory.
+// MMA order: S(s+1) and dV_g += P^T dO are issued when the P-phase of s ends
+// (they overlap the dS-phase); dK_g += dS^T Q and the dQ tile dS K after the
+// dS-phase; the dQ tile reuses the dP columns, and dP(s+1) is issued once the
+// dQ tile has been read.  dK is scaled by 1/sqrt(D) when it leaves TMEM, the
+// dQ tile when it is read.  After slice G-1 of a query tile the FP32 dbias
+// partial of the outer group is written once.
 template <int D>
 struct BwdSmem {
   static constexpr int kTile = BM * D * 2;              // 128 rows x D bf16
@@ -63,22 +84,28 @@ struct BwdSmem {
   static constexpr int kQ = kV + G * kTile;             // 2 stages of Q tiles
   static constexpr int kDO = kQ + 2 * kTile;            // 2 stages of dO tiles
   static constexpr int kMask = kDO + 2 * kTile;         // G x 128 fp32 (base-2 scaled key mask)
-  static constexpr int kBar = kMask + G * BN * 4;
+  static constexpr int kFlag = kMask + G * BN * 4;      // G x 16 bytes: 8-key chunk has a nonzero mask
+  static constexpr int kBar = kFlag + G * 16;
   static constexpr int kBytes = kBar + 256;
   static_assert(kBytes <= 232448, "shared memory budget");
 };
+
+constexpr int kNWG = 4;                // elementwise warpgroups
+constexpr int kCols = BN / kNWG;       // key columns per warpgroup
+constexpr int kEW = 128 * kNWG;        // elementwise threads
+constexpr int kMainThreads = 64 + kEW;
 
 struct BwdBars {
   uint64_t kv_full;
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t b_full[2], b_empty[2];
-  uint64_t sdp_full, ds_ready, mma_done, tmem_free;
+  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free;
   uint32_t tmem_slot;
   int abort;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_bias, const uint16_t* __restrict__ mask,
@@ -102,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = bh - b * H;
   const int JQ = (N + BM - 1) / BM;
   const int nsteps = JQ * G;
-  const size_t rows_total_bh = static_cast<size_t>(N);  // rows per (b,o,h)
 
   // The swizzled tiles below need a 1024-byte aligned base.
   if ((smem_u32(sm) & 1023u) != 0) {
@@ -110,9 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  constexpr uint32_t kTS = 8 * D;                       // S (128 cols)
-  constexpr uint32_t kTDP = kTS + 128;                  // dP (128 cols)
-  constexpr uint32_t kTDQ = (D == 32) ? kTS : kTDP + 128;  // dQ tile (D cols)
+  // TMEM columns: dV_g at g*D, dK_g at 4D + g*D, S (128), dP (128); the dQ
+  // tile (D columns) reuses the first dP columns.
+  constexpr uint32_t kTS = 8 * D;
+  constexpr uint32_t kTDP = kTS + 128;
+  constexpr uint32_t kTDQ = kTDP;
+  static_assert(kTDP + 128 <= 512, "TMEM budget");
 
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -120,12 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->qdo_full[i], 1);
       mbar_init(&bars->qdo_empty[i], 1);
       mbar_init(&bars->b_full[i], 1);
-      mbar_init(&bars->b_empty[i], BM);
+      mbar_init(&bars->b_empty[i], kEW);
     }
-    mbar_init(&bars->sdp_full, 1);
-    mbar_init(&bars->ds_ready, BM);
-    mbar_init(&bars->mma_done, 1);
-    mbar_init(&bars->tmem_free, BM);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, kEW);
+    mbar_init(&bars->ds_ready, kEW);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, kEW);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -169,67 +200,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;  // 64B / 32B swizzle for D-wide rows
-      constexpr uint32_t kSbo = 8u * D * 2u;
-      constexpr uint32_t idSS = idesc_bf16_f32(BM, BN, 0, 0);     // S, dP
-      constexpr uint32_t idKV = idesc_bf16_f32(BN, D, 1, 1);      // dV, dK: A MN-major, B MN-major
-      constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 0, 1);       // dQ: A K-major, B MN-major
-      const uint32_t sP = smem_u32(sm + L::kP), sDS = smem_u32(sm + L::kDS);
-      const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
-      const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO);
-      bool ok = mbar_wait(&bars->kv_full, 0, wc, abort);
-      for (int s = 0; s < nsteps && ok; ++s) {
-        const int i = s / G, g = s % G, st = s & 1;
-        if (!mbar_wait(&bars->qdo_full[st], (s >> 1) & 1, wc, abort)) { ok = false; break; }
-        if (s > 0 && !mbar_wait(&bars->tmem_free, (s - 1) & 1, wc, abort)) { ok = false; break; }
+    constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;  // 64B / 32B swizzle for D-wide rows
+    constexpr uint32_t kSbo = 8u * D * 2u;
+    constexpr uint32_t idSS = idesc_bf16_f32(BM, BN, 0, 0);     // S, dP
+    constexpr uint32_t idKV = idesc_bf16_f32(BN, D, 1, 1);      // dV, dK: A MN-major, B MN-major
+    constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 0, 1);       // dQ: A K-major, B MN-major
+    constexpr uint32_t kTile16 = L::kTile >> 4;                 // tile size in descriptor units
+    constexpr uint32_t kRowStep = (16 * D * 2) >> 4;            // 16 rows of a D-wide tile
+    // base descriptors; per-MMA offsets are added to the start-address field
+    const uint64_t dQb = smem_desc(smem_u32(sm + L::kQ), 16, kSbo, kSwz);
+    const uint64_t dDOb = smem_desc(smem_u32(sm + L::kDO), 16, kSbo, kSwz);
+    const uint64_t dKb = smem_desc(smem_u32(sm + L::kK), 16, kSbo, kSwz);
+    const uint64_t dVb = smem_desc(smem_u32(sm + L::kV), 16, kSbo, kSwz);
+    const uint64_t dPmn = smem_desc(smem_u32(sm + L::kP), 16384, 1024, 2);   // P as MN-major A
+    const uint64_t dDSmn = smem_desc(smem_u32(sm + L::kDS), 16384, 1024, 2); // dS as MN-major A
+    const uint64_t dDSk = smem_desc(smem_u32(sm + L::kDS), 16, 1024, 2);     // dS as K-major A
+    auto issue_s = [&](int s) {  // S = Q K^T
+      const uint64_t qd = dQb + (s & 1) * kTile16, kd = dKb + (s % G) * kTile16;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTS, qd + 2 * kk, kd + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->s_full);
+      }
+      __syncwarp();
+    };
+    auto issue_dp = [&](int s) {  // dP = dO V^T
+      const uint64_t dod = dDOb + (s & 1) * kTile16, vd = dVb + (s % G) * kTile16;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTDP, dod + 2 * kk, vd + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dp_full);
+      }
+      __syncwarp();
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, wc, abort)) &&
+              __all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[0], 0, wc, abort));
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int i = s / G, g = s % G, st = s & 1;
+      const uint64_t qd = dQb + st * kTile16, dod = dDOb + st * kTile16, kd = dKb + g * kTile16;
+      // P-phase of s done: S columns free, P in shared memory
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_ready, s & 1, wc, abort))) { ok = false; break; }
+      tc_fence_after();
+      if (s + 1 < nsteps) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t qb = sQ + st * L::kTile, dob = sDO + st * L::kTile;
-        const uint32_t kb = sK + g * L::kTile, vb = sV + g * L::kTile;
+        issue_s(s + 1);
+      }
+      if (elect_one()) {
+        const uint32_t tdv = tmem + g * D;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          mma_ss(tmem + kTS, smem_desc(qb + kk * 32, 16, kSbo, kSwz), smem_desc(kb + kk * 32, 16, kSbo, kSwz), idSS,
-                 kk > 0 ? 1u : 0u);
-          mma_ss(tmem + kTDP, smem_desc(dob + kk * 32, 16, kSbo, kSwz), smem_desc(vb + kk * 32, 16, kSbo, kSwz),
-                 idSS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->sdp_full);
-        if (!mbar_wait(&bars->ds_ready, s & 1, wc, abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t tdv = tmem + g * D, tdk = tmem + 4 * D + g * D;
+        for (int kk = 0; kk < BM / 16; ++kk)  // dV_g += P^T dO (A = P^T: keys contiguous, MN-major)
+          mma_ss(tdv, dPmn + kk * 128, dod + kk * kRowStep, idKV, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+      // dS-phase of s done: dP columns free, dS in shared memory
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, s & 1, wc, abort))) { ok = false; break; }
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t tdk = tmem + 4 * D + g * D;
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          // dV_g += P^T dO ; dK_g += dS^T Q   (A = P^T / dS^T: keys contiguous, MN-major)
-          const uint64_t bdo = smem_desc(dob + kk * 16 * D * 2, 16, kSbo, kSwz);
-          const uint64_t bq = smem_desc(qb + kk * 16 * D * 2, 16, kSbo, kSwz);
-          mma_ss(tdv, smem_desc(sP + kk * 2048, 16384, 1024, 2), bdo, idKV, (i > 0 || kk > 0) ? 1u : 0u);
-          mma_ss(tdk, smem_desc(sDS + kk * 2048, 16384, 1024, 2), bq, idKV, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BM / 16; ++kk)  // dK_g += dS^T Q
+          mma_ss(tdk, dDSmn + kk * 128, qd + kk * kRowStep, idKV, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // dQ tile = dS K  (A = dS: keys contiguous = K-major; B = K: D contiguous = MN-major)
-          const uint64_t a = smem_desc(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-          const uint64_t bk = smem_desc(kb + kk * 16 * D * 2, 16, kSbo, kSwz);
-          mma_ss(tmem + kTDQ, a, bk, idQ, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->mma_done);
+        for (int kk = 0; kk < BN / 16; ++kk)  // dQ tile = dS K (A = dS K-major, B = K MN-major)
+          mma_ss(tmem + kTDQ, dDSk + (kk >> 2) * 1024 + (kk & 3) * 2, kd + kk * kRowStep, idQ, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dq_full);        // covers every MMA issued so far
         mma_commit(&bars->qdo_empty[st]);
+      }
+      __syncwarp();
+      if (s + 1 < nsteps) {
+        // the dQ tile must be read before dP(s+1) overwrites those columns
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_free, s & 1, wc, abort))) { ok = false; break; }
+        tc_fence_after();
+        issue_dp(s + 1);
       }
     }
   } else {
-    // ------------------------------------------------------------ elementwise warpgroup
-    const int ew = tid - 64;
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;   // query row in tile (S / dP / dQ lane) and key row (dK / dV lane)
+    // ------------------------------------------------------------ elementwise warpgroups
+    const int ew = tid - 64;                  // 0..511
+    const int quarter = warp & 3;             // TMEM lane quarter of this warp
+    const int wg = (warp - 2) >> 2;           // key-column quarter handled by this warpgroup
+    const int r = quarter * 32 + lane;        // TMEM lane: query row (S, dP, dQ) / key row (dK, dV)
+    const int col0 = wg * kCols;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float scale_log2 = kLog2e * rsqrtf(static_cast<float>(D));
     const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
     float* mask2 = reinterpret_cast<float*>(sm + L::kMask);
+    uint8_t* mflag = sm + L::kFlag;
     uint8_t* sP = sm + L::kP;
     uint8_t* sDS = sm + L::kDS;
-    const int key = ktile * BN + ew;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
+
+    // Base-2 key mask of the G slices (-inf past N) and, per 8-key chunk, a
+    // flag telling whether any of its mask values is nonzero.  Staged before
+    // any bounded wait so the two barriers below are always fully entered.
+    for (int idx = ew; idx < G * BN; idx += kEW) {
+      const int g = idx / BN, key = ktile * BN + (idx % BN);
       float mv = -INFINITY;
       if (key < N) {
         mv = 0.f;
@@ -238,170 +311,200 @@ __global__ void __launch_bounds__(kThreads, 1)
                                << 16) *
                kLog2e;
       }
-      mask2[g * BN + ew] = mv;
+      mask2[idx] = mv;
     }
-    named_bar_sync(1, BM);
-
-    auto row_stats = [&](int s, float& lse2, float& dl) {
-      const int i = s / G, g = s % G;
-      const int q = i * BM + r;
-      lse2 = INFINITY;
-      dl = 0.f;
-      if (q < N) {
-        const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * rows_total_bh + q;
-        const float l = __ldg(lse + row);
-        if (l != -INFINITY) lse2 = l * kLog2e;
-        dl = __ldg(delta + row);
-      }
-    };
-    float lse2_n, dl_n;
-    row_stats(0, lse2_n, dl_n);
-    float dbacc[BN];
+    named_bar_sync(1, kEW);
+    if (ew < G * 16) {
+      bool any = false;
 #pragma unroll
-    for (int k = 0; k < BN; ++k) dbacc[k] = 0.f;
+      for (int e = 0; e < 8; ++e) any |= (mask2[ew * 8 + e] != 0.f);
+      mflag[ew] = any ? 1 : 0;
+    }
+    named_bar_sync(1, kEW);
+
+    // lse and delta of this thread's query row, loaded one step ahead; the
+    // raw values are converted only when used.  Rows past N get P = 0.
+    auto row_stats = [&](int s, float& l, float& dl) {
+      const int i = s / G, g = s % G;
+      const int q = min(i * BM + r, N - 1);
+      const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + q;
+      l = ldg_f32_pinned(lse + row);
+      dl = ldg_f32_pinned(delta + row);
+    };
+    float lse_n, dl_n;
+    row_stats(0, lse_n, dl_n);
+    float2 dbacc[kCols / 2];  // dbias accumulators for this thread's key columns
+#pragma unroll
+    for (int k = 0; k < kCols / 2; ++k) dbacc[k] = make_float2(0.f, 0.f);
+    const float2 c2 = make_float2(scale_log2, scale_log2);
+    const float2 l2e2 = make_float2(kLog2e, kLog2e);
     bool ok = true;
 
     for (int s = 0; s < nsteps && ok; ++s) {
       const int i = s / G, g = s % G;
-      const float lse2 = lse2_n, dl = dl_n;
-      if (s + 1 < nsteps) row_stats(s + 1, lse2_n, dl_n);
+      const float lse_raw = lse_n, dl_raw = dl_n;
+      if (s + 1 < nsteps) row_stats(s + 1, lse_n, dl_n);
+      const bool row_ok = i * BM + r < N;
       const int bst = i & 1;
       if (g == 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->b_full[bst], (i >> 1) & 1, wc, abort))) {
         ok = false;
         break;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->sdp_full, s & 1, wc, abort))) { ok = false; break; }
-      tc_fence_after();
       const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
       const float* mk = mask2 + g * BN;
+
+      // ---------------- P-phase
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, wc, abort))) { ok = false; break; }
+      tc_fence_after();
+      float2 p[kCols / 2];
+      {
+        uint32_t sv[kCols];
+        tmem_ld32(tmem + lane_addr + kTS + col0, sv);
+        // fully masked rows (lse = -inf) and rows past N: P = 0
+        const float lse2 = (row_ok && lse_raw != -INFINITY) ? lse_raw * kLog2e : INFINITY;
+        tc_wait_ld_regs(sv);
+        const float2 nl2 = make_float2(-lse2, -lse2);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 keys per chunk
-        uint32_t sraw[32], praw[32];
-        tmem_ld32(tmem + lane_addr + kTS + c * 32, sraw);
-        tmem_ld32(tmem + lane_addr + kTDP + c * 32, praw);
-        tc_wait_ld();
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {  // 8 keys per 16-byte chunk
-          const int cc = c * 4 + v;      // 16-byte chunk index along the key axis (0..15)
-          const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + (cc >> 3) * (BM * 128) + sw128(r, cc & 7));
-          const float4 m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
-          const float bb[8] = {bf16lo_to_f32(bw.x), bf16hi_to_f32(bw.x), bf16lo_to_f32(bw.y), bf16hi_to_f32(bw.y),
-                               bf16lo_to_f32(bw.z), bf16hi_to_f32(bw.z), bf16lo_to_f32(bw.w), bf16hi_to_f32(bw.w)};
-          const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-          float pv[8], dsv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int kk = v * 8 + e;
-            const float t = fmaf(__uint_as_float(sraw[kk]), scale_log2, fmaf(bb[e], kLog2e, mm[e] - lse2));
-            const float p = ex2_approx(t);
-            const float ds = p * (__uint_as_float(praw[kk]) - dl);
-            dbacc[c * 32 + kk] += ds;
-            pv[e] = p;
-            dsv[e] = ds * inv_sqrt_d;
+        for (int v = 0; v < kCols / 8; ++v) {  // 8 keys per 16-byte chunk
+          const int cc = (col0 >> 3) + v;
+          const uint32_t off = (cc >> 3) * (BM * 128) + sw128(r, cc & 7);
+          const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + off);
+          const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
+          const bool masked = mflag[g * 16 + cc] != 0;
+          float4 m0 = make_float4(0.f, 0.f, 0.f, 0.f), m1 = m0;
+          if (masked) {
+            m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
+            m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
           }
+          const float2 mm[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                                make_float2(m1.z, m1.w)};
+          uint32_t pw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            pw[v * 4 + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-            dw[v * 4 + e] = pack_bf16x2(dsv[2 * e], dsv[2 * e + 1]);
+            const float2 s2 = make_float2(__uint_as_float(sv[v * 8 + 2 * e]), __uint_as_float(sv[v * 8 + 2 * e + 1]));
+            const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
+            float2 t = ffma2(b2, l2e2, ffma2(s2, c2, nl2));
+            if (masked) t = fadd2(t, mm[e]);
+            const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            p[v * 4 + e] = pp;
+            pw[e] = pack_bf16x2(pp.x, pp.y);
           }
+          *reinterpret_cast<uint4*>(sP + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      if (g == G - 1) mbar_arrive(&bars->b_empty[bst]);
+
+      // ---------------- dS-phase
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, s & 1, wc, abort))) { ok = false; break; }
+      tc_fence_after();
+      {
+        const float dl = row_ok ? dl_raw : 0.f;
+        const float2 ndl2 = make_float2(-dl, -dl);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int cc = c * 4 + v;
-          const uint32_t off = (cc >> 3) * (BM * 128) + sw128(r, cc & 7);
-          *reinterpret_cast<uint4*>(sP + off) = make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
-          *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * v], dw[4 * v + 1], dw[4 * v + 2], dw[4 * v + 3]);
+        for (int hh = 0; hh < 2; ++hh) {  // 16 keys at a time
+          uint32_t a[8], bq[8];
+          tmem_ld8(tmem + lane_addr + kTDP + col0 + hh * 16, a);
+          tmem_ld8(tmem + lane_addr + kTDP + col0 + hh * 16 + 8, bq);
+          tc_wait_ld_regs(a, bq);
+          uint32_t dw[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t x0 = e < 4 ? a[2 * e] : bq[2 * e - 8];
+            const uint32_t x1 = e < 4 ? a[2 * e + 1] : bq[2 * e - 7];
+            const float2 dp2 = make_float2(__uint_as_float(x0), __uint_as_float(x1));
+            const float2 ds = fmul2(p[hh * 8 + e], fadd2(dp2, ndl2));
+            dbacc[hh * 8 + e] = fadd2(dbacc[hh * 8 + e], ds);
+            dw[e] = pack_bf16x2(ds.x, ds.y);
+          }
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const int cc = (col0 >> 3) + hh * 2 + v;
+            const uint32_t off = (cc >> 3) * (BM * 128) + sw128(r, cc & 7);
+            *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * v], dw[4 * v + 1], dw[4 * v + 2], dw[4 * v + 3]);
+          }
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->ds_ready);
       if (g == G - 1) {
-        mbar_arrive(&bars->b_empty[bst]);
-        // single-writer dbias partial of this outer group: rows of query tile i,
-        // columns of key tile ktile
-        const int q = i * BM + r;
-        if (q < N) {
-          float* dst = dbias_part + (static_cast<size_t>(grp) * gridDim.z + bh) * static_cast<size_t>(N) * N +
-                       static_cast<size_t>(q) * N + static_cast<size_t>(ktile) * BN;
-          const int nk = min(BN, N - ktile * BN);
+        // single-writer dbias partial of this outer group for tile (i, ktile),
+        // stored chunk-major ([32 float4 chunks][128 rows]) so that each warp
+        // store covers 512 contiguous bytes
+        float4* dst = reinterpret_cast<float4*>(dbias_part) +
+                      ((((static_cast<size_t>(grp) * gridDim.z + bh) * JQ + i) * gridDim.x + ktile) * (BM * BN / 4)) +
+                      (col0 / 4) * BM + r;
 #pragma unroll
-          for (int k4 = 0; k4 < BN / 4; ++k4)
-            if (k4 * 4 < nk)
-              reinterpret_cast<float4*>(dst)[k4] =
-                  make_float4(dbacc[4 * k4], dbacc[4 * k4 + 1], dbacc[4 * k4 + 2], dbacc[4 * k4 + 3]);
-        }
+        for (int k4 = 0; k4 < kCols / 4; ++k4)
+          dst[k4 * BM] = make_float4(dbacc[2 * k4].x, dbacc[2 * k4].y, dbacc[2 * k4 + 1].x, dbacc[2 * k4 + 1].y);
 #pragma unroll
-        for (int k = 0; k < BN; ++k) dbacc[k] = 0.f;
+        for (int k = 0; k < kCols / 2; ++k) dbacc[k] = make_float2(0.f, 0.f);
       }
-      // dQ partial of this key tile
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done, s & 1, wc, abort))) { ok = false; break; }
+
+      // ---------------- dQ tile of this key tile: D/4 columns per warpgroup
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, s & 1, wc, abort))) { ok = false; break; }
       tc_fence_after();
       {
-        const int q = i * BM + r;
-        const size_t rows_all = static_cast<size_t>(gridDim.z) * N_o * N;  // B*H*N_o*N
-        const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + q;
-        float* out = dq_part + (static_cast<size_t>(ktile) * rows_all + row) * D;
+        // chunk-major per 128-row tile: [J_K][slices][J_Q][D/4 float4 chunks][128 rows]
+        const size_t slice = static_cast<size_t>((b * N_o + o0 + g) * H + h);
+        const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
+        float4* out = reinterpret_cast<float4*>(dq_part) +
+                      ((static_cast<size_t>(ktile) * nslices + slice) * JQ + i) * (BM * D / 4) + wg * (D / 16) * BM + r;
         if constexpr (D == 32) {
-          uint32_t qr[32];
-          tmem_ld32(tmem + lane_addr + kTDQ, qr);
+          uint32_t qr[8];
+          tmem_ld8(tmem + lane_addr + kTDQ + 8 * wg, qr);
           tc_wait_ld();
-          if (q < N) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              reinterpret_cast<float4*>(out)[v] =
-                  make_float4(__uint_as_float(qr[4 * v]), __uint_as_float(qr[4 * v + 1]),
-                              __uint_as_float(qr[4 * v + 2]), __uint_as_float(qr[4 * v + 3]));
-          }
+          for (int v = 0; v < 2; ++v)
+            out[v * BM] = make_float4(__uint_as_float(qr[4 * v]) * inv_sqrt_d, __uint_as_float(qr[4 * v + 1]) * inv_sqrt_d,
+                                      __uint_as_float(qr[4 * v + 2]) * inv_sqrt_d,
+                                      __uint_as_float(qr[4 * v + 3]) * inv_sqrt_d);
         } else {
-          uint32_t qr[16];
-          tmem_ld16(tmem + lane_addr + kTDQ, qr);
+          uint32_t qr[4];
+          tmem_ld4(tmem + lane_addr + kTDQ + 4 * wg, qr);
           tc_wait_ld();
-          if (q < N) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              reinterpret_cast<float4*>(out)[v] =
-                  make_float4(__uint_as_float(qr[4 * v]), __uint_as_float(qr[4 * v + 1]),
-                              __uint_as_float(qr[4 * v + 2]), __uint_as_float(qr[4 * v + 3]));
-          }
+          out[0] = make_float4(__uint_as_float(qr[0]) * inv_sqrt_d, __uint_as_float(qr[1]) * inv_sqrt_d,
+                               __uint_as_float(qr[2]) * inv_sqrt_d, __uint_as_float(qr[3]) * inv_sqrt_d);
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->tmem_free);
+      mbar_arrive(&bars->dq_free);
     }
 
-    // ------------------------------------------------------------ epilogue: dK, dV
+    // ------------------------------------------------------------ epilogue: dV_g and dK_g of slice g = wg
     if (ok) {
-      // the last mma_done wait above covers every MMA of this CTA
+      // the last dq_full wait above covers every MMA of this CTA
       tc_fence_after();
       const int krow = ktile * BN + r;  // key of this thread's TMEM lane
+      const int g = wg;
+      const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + krow;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + krow;
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t t = tmem + lane_addr + which * 4 * D + g * D;
+        const float sc = which == 0 ? 1.f : inv_sqrt_d;
+        uint32_t w[D / 2];
+        if constexpr (D == 32) {
+          uint32_t raw[32];
+          tmem_ld32(t, raw);
+          tc_wait_ld();
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t t = tmem + lane_addr + (which == 0 ? g * D : 4 * D + g * D);
-          uint32_t w[D / 2];
-          if constexpr (D == 32) {
-            uint32_t raw[32];
-            tmem_ld32(t, raw);
-            tc_wait_ld();
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]) * sc, __uint_as_float(raw[2 * e + 1]) * sc);
+        } else {
+          uint32_t raw[16];
+          tmem_ld16(t, raw);
+          tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]), __uint_as_float(raw[2 * e + 1]));
-          } else {
-            uint32_t raw[16];
-            tmem_ld16(t, raw);
-            tc_wait_ld();
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]) * sc, __uint_as_float(raw[2 * e + 1]) * sc);
+        }
+        if (krow < N) {
+          uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + row * D);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]), __uint_as_float(raw[2 * e + 1]));
-          }
-          if (krow < N) {
-            uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + row * D);
-#pragma unroll
-            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-          }
+          for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
       }
     }
@@ -416,36 +519,95 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- reductions
-// dQ[row, :] = sum_{t = 0 .. J_K-1} dq_part[t][row, :]   (ascending t, FP32)
-__global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict__ part, uint2* __restrict__ out,
-                                                        size_t n4, int jk) {
-  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= n4) return;
-  float4 acc = __ldcs(part + idx);
-  for (int t = 1; t < jk; ++t) {
-    const float4 v = __ldcs(part + static_cast<size_t>(t) * n4 + idx);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+// dQ[row, :] = sum_{t = 0 .. J_K-1} dq_part[t][row, :]   (ascending t, FP32).
+// One block per 128-row tile of one slice: coalesced float4 reads of the
+// chunk-major partials, FP32 sums in fixed order, transpose through shared
+// memory, coalesced BF16 row writes.
+template <int D>
+__global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict__ part, uint16_t* __restrict__ dq,
+                                                        int N, int JQ, int JK, size_t tiles) {
+  constexpr int kChunks = BM * D / 4;      // float4 per tile
+  constexpr int kStride = D + 4;           // padded row stride (floats) of the transpose buffer
+  __shared__ float tile[BM * kStride];
+  const size_t t = blockIdx.x;             // tile = slice * JQ + i
+  const int i = static_cast<int>(t % JQ);
+  const size_t slice = t / JQ;
+  for (int e = threadIdx.x; e < kChunks; e += blockDim.x) {
+    const float4* p = part + t * kChunks + e;
+    float4 acc = __ldcs(p);
+    for (int kt = 1; kt < JK; ++kt) {
+      const float4 v = __ldcs(p + static_cast<size_t>(kt) * tiles * kChunks);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int c = e / BM, r = e % BM;
+    *reinterpret_cast<float4*>(&tile[r * kStride + 4 * c]) = acc;
   }
-  out[idx] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  __syncthreads();
+  constexpr int kItems = BM * D / 8;       // 16-byte output items (8 bf16)
+  for (int e = threadIdx.x; e < kItems; e += blockDim.x) {
+    const int r = e / (D / 8), c8 = e % (D / 8);
+    const int q = i * BM + r;
+    if (q >= N) continue;
+    const float* src = &tile[r * kStride + 8 * c8];
+    const uint4 w = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]), pack_bf16x2(src[4], src[5]),
+                               pack_bf16x2(src[6], src[7]));
+    *reinterpret_cast<uint4*>(dq + (slice * N + q) * D + 8 * c8) = w;
+  }
 }
 
-// dbias[b,h,q,k] = sum_{l = 0 .. L-1} dbias_part[l][b,h,q,k]   (ascending l, FP32)
-__global__ void __launch_bounds__(256) reduce_dbias_kernel(const float4* __restrict__ part, uint2* __restrict__ out,
-                                                           size_t n4, int ngroups) {
-  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= n4) return;
-  float4 acc = __ldcs(part + idx);
-  for (int l = 1; l < ngroups; ++l) {
-    const float4 v = __ldcs(part + static_cast<size_t>(l) * n4 + idx);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+// dbias[b,h,q,k] = sum_{l = 0 .. L-1} dbias_part[l][b,h,q,k]   (ascending l, FP32).
+// One block per 16-row slab of a 128 x 128 tile (b*h, query tile i, key tile
+// t); the loads of four consecutive partials are issued together, the adds
+// stay in ascending order.
+constexpr int kSlab = 16;
+__global__ void __launch_bounds__(256) reduce_dbias_kernel(const float4* __restrict__ part,
+                                                           uint16_t* __restrict__ dbias, int N, int JQ, int JK,
+                                                           int ngroups, size_t tiles) {
+  constexpr int kChunks = BM * BN / 4;     // float4 per tile
+  constexpr int kSlabChunks = kSlab * BN / 4;
+  constexpr int kStride = BN + 8;          // padded row stride (bf16) of the transpose buffer
+  __shared__ uint16_t tile[kSlab * kStride];
+  const size_t t = blockIdx.x / (BM / kSlab);
+  const int slab = blockIdx.x % (BM / kSlab);
+  const int kt = static_cast<int>(t % JK);
+  const int i = static_cast<int>((t / JK) % JQ);
+  const size_t bh = t / (static_cast<size_t>(JK) * JQ);
+  const size_t lstride = tiles * kChunks;
+  for (int e = threadIdx.x; e < kSlabChunks; e += blockDim.x) {
+    const int c = e / kSlab, rr = e % kSlab;
+    const float4* p = part + t * kChunks + c * BM + slab * kSlab + rr;
+    float4 acc = __ldcs(p);
+    int l = 1;
+    for (; l + 4 <= ngroups; l += 4) {
+      const float4 v0 = __ldcs(p + static_cast<size_t>(l) * lstride);
+      const float4 v1 = __ldcs(p + static_cast<size_t>(l + 1) * lstride);
+      const float4 v2 = __ldcs(p + static_cast<size_t>(l + 2) * lstride);
+      const float4 v3 = __ldcs(p + static_cast<size_t>(l + 3) * lstride);
+      acc.x = (((acc.x + v0.x) + v1.x) + v2.x) + v3.x;
+      acc.y = (((acc.y + v0.y) + v1.y) + v2.y) + v3.y;
+      acc.z = (((acc.z + v0.z) + v1.z) + v2.z) + v3.z;
+      acc.w = (((acc.w + v0.w) + v1.w) + v2.w) + v3.w;
+    }
+    for (; l < ngroups; ++l) {
+      const float4 v = __ldcs(p + static_cast<size_t>(l) * lstride);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<uint2*>(&tile[rr * kStride + 4 * c]) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
-  out[idx] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  __syncthreads();
+  constexpr int kItems = kSlab * BN / 8;   // 16-byte items
+  for (int e = threadIdx.x; e < kItems; e += blockDim.x) {
+    const int rr = e / (BN / 8), c8 = e % (BN / 8);
+    const int q = i * BM + slab * kSlab + rr, k = kt * BN + 8 * c8;
+    if (q >= N || k >= N) continue;        // N is a multiple of 8: an item is all in or all out
+    *reinterpret_cast<uint4*>(dbias + (bh * N + q) * N + k) = *reinterpret_cast<const uint4*>(&tile[rr * kStride + 8 * c8]);
+  }
 }
 
 }  // namespace
@@ -472,7 +634,7 @@ template <int D>
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
   dim3 grid(JK, a.N_o / G, a.B * a.H);
-  bwd_main_kernel<D><<<grid, kThreads, BwdSmem<D>::kBytes, stream>>>(
+  bwd_main_kernel<D><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_bias, static_cast<const uint16_t*>(a.mask), a.lse, a.delta,
       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
   return cudaGetLastError();
@@ -480,19 +642,18 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
 
 template <int D>
 cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream) {
-  const int JK = (a.N + BN - 1) / BN;
-  const size_t n4 = static_cast<size_t>(a.B) * a.N_o * a.H * a.N * D / 4;
-  const unsigned grid = static_cast<unsigned>((n4 + 255) / 256);
-  reduce_dq_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_part),
-                                             static_cast<uint2*>(a.dq), n4, JK);
+  const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
+  const size_t tiles = static_cast<size_t>(a.B) * a.N_o * a.H * JQ;
+  reduce_dq_kernel<D><<<static_cast<unsigned>(tiles), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, JQ, JK, tiles);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream) {
-  const size_t n4 = static_cast<size_t>(a.B) * a.H * a.N * a.N / 4;
-  const unsigned grid = static_cast<unsigned>((n4 + 255) / 256);
-  reduce_dbias_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dbias_part),
-                                                static_cast<uint2*>(a.dbias), n4, a.N_o / G);
+  const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
+  const size_t tiles = static_cast<size_t>(a.B) * a.H * JQ * JK;
+  reduce_dbias_kernel<<<static_cast<unsigned>(tiles * (BM / kSlab)), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK, a.N_o / G, tiles);
   return cudaGetLastError();
 }
 

@@ -10,21 +10,24 @@
 // The four slices of the group use the same bias tile for every key tile, so
 // each bias tile is loaded once into shared memory and read by four slices.
 //
-// Warp roles (6 warps):
+// Warp roles (10 warps):
 //   warp 0     TMA producer: Q tiles once, then per key tile one bias tile and
 //              one K and one V tile per slice (rings of 2 / 4 / 4 stages).
 //   warp 1     TMEM allocator and single-thread tcgen05 MMA issuer:
-//              S = Q K^T into one of two TMEM score buffers, then
+//              S = Q K^T into the score buffer of the slice's warpgroup, then
 //              O_g += P V with P read from TMEM (the score buffer's first
 //              64 columns, rewritten as packed BF16 by the softmax warps).
-//   warps 2-5  softmax warpgroup: thread = query row (TMEM lane).  Adds the
-//              bias and the key mask, keeps a running max / sum per slice in
-//              base-2 units, writes P as BF16 into TMEM, rescales O in TMEM
-//              when the running max grows by more than 2^8, and finally
-//              writes O (BF16), the residual E = bf16(O32 - O) and lse.
+//   warps 2-9  two softmax warpgroups; warpgroup w owns the slices g with
+//              g % 2 == w, so while one warpgroup computes a softmax the MMA
+//              for the other one runs.  Thread = query row (TMEM lane).
+//              Pass 1 adds bias and key mask and writes the scores back to
+//              TMEM while taking the row max; pass 2 exponentiates (base 2),
+//              sums, and writes P as BF16 into TMEM.  O is rescaled in TMEM
+//              only when the running max grows by more than 2^8.  The
+//              epilogue writes O (BF16), the residual E = bf16(O32 - O) and lse.
 //
-// TMEM (512 columns): score buffers at [0,128) and [128,256); O_g at
-// 256 + g*D.  Steps s = j*GF + g alternate score buffers (s % 2).
+// TMEM (512 columns): score buffers at [0,128) (warpgroup 0) and [128,256)
+// (warpgroup 1); O_g at 256 + g*D.  Step s = j*GF + g uses buffer s % 2.
 #include "kernels.cuh"
 
 namespace triattn {
@@ -36,9 +39,9 @@ constexpr int BN = 128;     // keys per tile
 constexpr int GF = 4;       // outer slices per CTA (share a bias tile)
 constexpr int NSLOT = 4;    // K ring and V ring depth
 constexpr int NBIAS = 2;    // bias ring depth
-constexpr int kThreads = 192;
+constexpr int kEW = 256;               // softmax threads (two warpgroups)
+constexpr int kThreads = 64 + kEW;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;  // log2 units
 
 template <int D>
@@ -49,12 +52,12 @@ struct FwdSmem {
   static constexpr int kV = kK + NSLOT * kTile;      // NSLOT V tiles
   static constexpr int kBias = kV + NSLOT * kTile;   // NBIAS x 32 KB (1024-aligned)
   static constexpr int kBar = kBias + NBIAS * BM * BN * 2;
-  static constexpr int kMask = kBar + 256;           // GF x JK x 128 fp32 (base-2 key mask)
+  static constexpr int kMask = kBar + 256;           // GF x JK x 128 fp32 (key mask), then GF x JK x 16 flags
   static constexpr int kFixed = kMask + 1024;        // + slack for 1024-byte alignment
   static_assert(kBias % 1024 == 0, "bias tiles need 1024-byte alignment");
   // bytes for a problem with JK key tiles
-  static constexpr int bytes(int JK) { return kFixed + GF * JK * BN * 4; }
-  static constexpr int kMaxJK = (232448 - kFixed) / (GF * BN * 4);
+  static constexpr int bytes(int JK) { return kFixed + GF * JK * (BN * 4 + 16); }
+  static constexpr int kMaxJK = (232448 - kFixed) / (GF * (BN * 4 + 16));
 };
 
 struct FwdBars {
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < NBIAS; ++i) {
       mbar_init(&bars->b_full[i], 1);
-      mbar_init(&bars->b_empty[i], BM);
+      mbar_init(&bars->b_empty[i], kEW);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -197,33 +200,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars->all_done);
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int ew = tid - 64;              // 0..127
+    // ------------------------------------------------------------ softmax warpgroups
+    const int ew = tid - 64;              // 0..255
+    const int wg = (warp - 2) >> 2;       // warpgroup: slices g with g % 2 == wg
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;    // query row within the tile (= TMEM lane)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const float scale_log2 = kLog2e * rsqrtf(static_cast<float>(D));
+    const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
     float* mask2 = reinterpret_cast<float*>(sm + L::kMask);
-    float m_run[GF], l_run[GF];
-#pragma unroll
-    for (int g = 0; g < GF; ++g) { m_run[g] = -INFINITY; l_run[g] = 0.f; }
+    uint8_t* mflag = sm + L::kMask + nsteps * BN * 4;
 
-    // Key mask of every (key tile, slice) step, base-2 scaled, -inf past N:
-    // staged once, before any bounded wait, so the only CTA barrier among the
-    // softmax warps cannot be left half-entered by an aborting warp.
-    for (int idx = ew; idx < nsteps * BN; idx += BM) {
+    // Key mask of every (key tile, slice) step (natural-log units, -inf past
+    // N) and per 8-key chunk a flag "some mask value is nonzero": staged once,
+    // before any bounded wait, so the two barriers are always fully entered.
+    for (int idx = ew; idx < nsteps * BN; idx += kEW) {
       const int s = idx / BN, key = (s / GF) * BN + (idx % BN), g = s % GF;
       float mv = -INFINITY;
       if (key < N) {
         mv = 0.f;
         if (mask != nullptr)
           mv = __uint_as_float(static_cast<uint32_t>(__ldg(mask + (static_cast<size_t>(b) * N_o + o0 + g) * N + key))
-                               << 16) *
-               kLog2e;
+                               << 16);
       }
       mask2[idx] = mv;
     }
-    named_bar_sync(1, BM);
+    named_bar_sync(1, kEW);
+    for (int idx = ew; idx < nsteps * 16; idx += kEW) {
+      bool any = false;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) any |= (mask2[idx * 8 + e] != 0.f);
+      mflag[idx] = any ? 1 : 0;
+    }
+    named_bar_sync(1, kEW);
+
+    // running max (natural units) and sum for this warpgroup's two slices
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    const float2 isd2 = make_float2(inv_sqrt_d, inv_sqrt_d);
+    const float2 l2e2 = make_float2(kLog2e, kLog2e);
     bool ok = true;
 
     for (int j = 0; j < JK && ok; ++j) {
@@ -231,73 +244,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->b_full[st], (j / NBIAS) & 1, wc, abort))) { ok = false; break; }
       const uint8_t* bias_s = sm + L::kBias + st * (BM * BN * 2);
 #pragma unroll
-      for (int g = 0; g < GF; ++g) {
+      for (int sl = 0; sl < 2; ++sl) {
+        const int g = wg + 2 * sl;
         const int s = j * GF + g;
-
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[s & 1], (s >> 1) & 1, wc, abort))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[wg], (s >> 1) & 1, wc, abort))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tS = tmem + lane_addr + (s & 1) * BN;
-        float x[BN];
-        {
-          uint32_t raw[32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tS + c * 32, raw);
-            tc_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[e]);
-          }
-        }
-        // t = S*log2e/sqrt(D) + (bias + mask)*log2e ; running tile max
-        float mt = -INFINITY;
+        const uint32_t tS = tmem + lane_addr + wg * BN;
         const float* mk = mask2 + s * BN;
+        const uint8_t* fl = mflag + s * 16;
+
+        // pass 1: u = S / sqrt(D) + bias + mask, written back to TMEM; row max.
+        // 32-key chunks, the load of chunk c+1 in flight while c is computed.
+        float mt = -INFINITY;
+        uint32_t buf[2][32];
+        tmem_ld32(tS, buf[0]);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + (c >> 3) * (BM * 128) + sw128(r, c & 7));
-          const float4 m0 = *reinterpret_cast<const float4*>(mk + c * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(mk + c * 8 + 4);
-          const float bb[8] = {bf16lo_to_f32(bw.x), bf16hi_to_f32(bw.x), bf16lo_to_f32(bw.y), bf16hi_to_f32(bw.y),
-                               bf16lo_to_f32(bw.z), bf16hi_to_f32(bw.z), bf16lo_to_f32(bw.w), bf16hi_to_f32(bw.w)};
-          const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float t = fmaf(x[c * 8 + e], scale_log2, fmaf(bb[e], kLog2e, mm[e]));
-            x[c * 8 + e] = t;
-            mt = fmaxf(mt, t);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t(&raw)[32] = buf[c & 1];
+          tc_wait_ld_regs(raw);
+          if (c + 1 < 4) {
+            if (c >= 1) tc_wait_st();  // buf[(c+1)&1] fed the store of chunk c-1
+            tmem_ld32(tS + (c + 1) * 32, buf[(c + 1) & 1]);
           }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int cc = c * 4 + v;  // 8-key chunk (0..15)
+            const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + (cc >> 3) * (BM * 128) + sw128(r, cc & 7));
+            const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
+            const bool masked = fl[cc] != 0;
+            float4 m0 = make_float4(0.f, 0.f, 0.f, 0.f), m1 = m0;
+            if (masked) {
+              m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
+              m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
+            }
+            const float2 mm[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                                  make_float2(m1.z, m1.w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = v * 8 + 2 * e;
+              const float2 s2 = make_float2(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]));
+              const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
+              float2 u = ffma2(s2, isd2, b2);
+              if (masked) u = fadd2(u, mm[e]);
+              mt = fmax3(mt, u.x, u.y);
+              raw[k] = __float_as_uint(u.x);
+              raw[k + 1] = __float_as_uint(u.y);
+            }
+          }
+          tmem_st32(tS + c * 32, raw);
         }
-        if (g == GF - 1) mbar_arrive(&bars->b_empty[st]);  // last reader of this bias tile
+        if (sl == 1) mbar_arrive(&bars->b_empty[st]);  // this warpgroup's last read of the bias tile
 
         // online softmax with lazy rescaling of O (kept in TMEM)
-        const float m_new = fmaxf(m_run[g], mt);
+        const float m_new = fmaxf(m_run[sl], mt);
         float alpha = 1.f;
         bool need = false;
         if (j == 0) {
-          m_run[g] = m_new;
+          m_run[sl] = m_new;
         } else {
-          need = m_new > m_run[g] + kRescaleThresh;
-          if (need) { alpha = ex2_approx(m_run[g] - m_new); m_run[g] = m_new; }
+          need = (m_new - m_run[sl]) * kLog2e > kRescaleThresh;
+          if (need) {
+            alpha = ex2_approx((m_run[sl] - m_new) * kLog2e);
+            m_run[sl] = m_new;
+          }
         }
-        const float msub = (m_run[g] == -INFINITY) ? 0.f : m_run[g];
-        float lsum = 0.f;
-        uint32_t p[BN / 2];
+        const float msub = (m_run[sl] == -INFINITY) ? 0.f : m_run[sl];
+        const float2 nm2 = make_float2(-msub * kLog2e, -msub * kLog2e);
+        tc_wait_st();
+
+        // pass 2: p = 2^((u - m) log2 e); P (BF16) into the first 64 columns
+        float2 lsum = make_float2(0.f, 0.f);
+        uint32_t pw[2][16];
+        tmem_ld32(tS, buf[0]);
 #pragma unroll
-        for (int e = 0; e < BN / 2; ++e) {
-          const float p0 = ex2_approx(x[2 * e] - msub);
-          const float p1 = ex2_approx(x[2 * e + 1] - msub);
-          lsum += p0 + p1;
-          p[e] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t(&raw)[32] = buf[c & 1];
+          tc_wait_ld_regs(raw);
+          if (c + 1 < 4) tmem_ld32(tS + (c + 1) * 32, buf[(c + 1) & 1]);
+          if (c >= 2) tc_wait_st();  // pw[c&1] fed the store of chunk c-2
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 u = make_float2(__uint_as_float(raw[2 * e]), __uint_as_float(raw[2 * e + 1]));
+            const float2 t = ffma2(u, l2e2, nm2);
+            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            lsum = fadd2(lsum, p);
+            pw[c & 1][e] = pack_bf16x2(p.x, p.y);
+          }
+          // P of keys [32c, 32c+32) lands in columns [16c, 16c+16): already read
+          tmem_st16(tS + c * 16, pw[c & 1]);
         }
-        l_run[g] = l_run[g] * alpha + lsum;
-        {
-          uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[0]);
-          uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[32]);
-          tmem_st32(tS, p0);
-          tmem_st32(tS + 32, p1);
-        }
+        l_run[sl] = l_run[sl] * alpha + (lsum.x + lsum.y);
         if (__any_sync(0xffffffffu, need)) {
-          // O_g's previous P.V was issued before this step's S (in-order
-          // tcgen05 pipe), so s_full of this step implies it has completed.
+          // O_g's previous P.V (step s - 4) was issued before this warpgroup's
+          // previous S (step s - 2); s_full of this step implies it finished.
           const uint32_t tO = tmem + lane_addr + 256 + g * D;
           if constexpr (D == 32) {
             uint32_t ov[32];
@@ -317,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[s & 1]);
+        mbar_arrive(&bars->p_full[wg]);
       }
     }
 
@@ -326,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int q = qtile * BM + r;
 #pragma unroll
-      for (int g = 0; g < GF; ++g) {
+      for (int sl = 0; sl < 2; ++sl) {
+        const int g = wg + 2 * sl;
         float ov[D];
         {
           const uint32_t tO = tmem + lane_addr + 256 + g * D;
@@ -345,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (q < N) {
-          const float l = l_run[g];
+          const float l = l_run[sl];
           const float inv = l > 0.f ? 1.0f / l : 0.f;
           const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + q;
           uint32_t ob[D / 2], eb[D / 2];
@@ -366,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int v4 = 0; v4 < D / 8; ++v4)
               ep[v4] = make_uint4(eb[4 * v4], eb[4 * v4 + 1], eb[4 * v4 + 2], eb[4 * v4 + 3]);
           }
-          out_lse[row] = l > 0.f ? (m_run[g] + __log2f(l)) * kLn2 : -INFINITY;
+          out_lse[row] = l > 0.f ? m_run[sl] + __logf(l) : -INFINITY;
         }
       }
     }

@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/triattn.h"
+#include "triattn.h"
 
 namespace {
 

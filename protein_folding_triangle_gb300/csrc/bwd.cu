@@ -68,11 +68,13 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
 //   dS-phase  dS = P (dP - delta); dbias accumulator += dS (FP32 registers);
 //             BF16 dS into shared memory.
 // MMA order: S(s+1) and dV_g += P^T dO are issued when the P-phase of s ends
-// (they overlap the dS-phase); dK_g += dS^T Q and the dQ tile dS K after the
-// dS-phase; the dQ tile reuses the dP columns, and dP(s+1) is issued once the
-// dQ tile has been read.  dK is scaled by 1/sqrt(D) when it leaves TMEM, the
-// dQ tile when it is read.  After slice G-1 of a query tile the FP32 dbias
-// partial of the outer group is written once.
+// (they overlap the dS-phase); dK_g += dS^T Q and dP(s+1) when the dS-phase
+// ends; the dQ tile dS K goes into the S columns as soon as the warps have
+// loaded S(s+1) into registers, so it runs under the P-phase of s+1, which
+// then reads it (and only then writes P(s+1) to shared memory).  dK is scaled
+// by 1/sqrt(D) when it leaves TMEM, the dQ tile when it is read.  After slice
+// G-1 of a query tile the FP32 dbias partial of the outer group is written
+// once.
 template <int D>
 struct BwdSmem {
   static constexpr int kTile = BM * D * 2;              // 128 rows x D bf16
@@ -99,7 +101,7 @@ struct BwdBars {
   uint64_t kv_full;
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t b_full[2], b_empty[2];
-  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free;
+  uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full;
   uint32_t tmem_slot;
   int abort;
 };
@@ -137,10 +139,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   }
 
   // TMEM columns: dV_g at g*D, dK_g at 4D + g*D, S (128), dP (128); the dQ
-  // tile (D columns) reuses the first dP columns.
+  // tile (D columns) reuses the first S columns once S has been loaded.
   constexpr uint32_t kTS = 8 * D;
   constexpr uint32_t kTDP = kTS + 128;
-  constexpr uint32_t kTDQ = kTDP;
+  constexpr uint32_t kTDQ = kTS;
   static_assert(kTDP + 128 <= 512, "TMEM budget");
 
   if (tid == 0) {
@@ -153,10 +155,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->s_cons, kEW);
     mbar_init(&bars->p_ready, kEW);
     mbar_init(&bars->ds_ready, kEW);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, kEW);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     for (int s = 0; s < nsteps && ok; ++s) {
       const int i = s / G, g = s % G, st = s & 1;
       const uint64_t qd = dQb + st * kTile16, dod = dDOb + st * kTile16, kd = dKb + g * kTile16;
-      // P-phase of s done: S columns free, P in shared memory
+      // P-phase of s done: S columns free (dQ of s-1 read), P in shared memory
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_ready, s & 1, wc, abort))) { ok = false; break; }
       tc_fence_after();
       if (s + 1 < nsteps) {
@@ -269,6 +271,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)  // dK_g += dS^T Q
           mma_ss(tdk, dDSmn + kk * 128, qd + kk * kRowStep, idKV, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+      if (s + 1 < nsteps) {
+        issue_dp(s + 1);
+        // the dQ tile goes into the S columns once S(s+1) has been loaded
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_cons, (s + 1) & 1, wc, abort))) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)  // dQ tile = dS K (A = dS K-major, B = K MN-major)
           mma_ss(tmem + kTDQ, dDSk + (kk >> 2) * 1024 + (kk & 3) * 2, kd + kk * kRowStep, idQ, kk > 0 ? 1u : 0u);
@@ -276,12 +287,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         mma_commit(&bars->qdo_empty[st]);
       }
       __syncwarp();
-      if (s + 1 < nsteps) {
-        // the dQ tile must be read before dP(s+1) overwrites those columns
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_free, s & 1, wc, abort))) { ok = false; break; }
-        tc_fence_after();
-        issue_dp(s + 1);
-      }
     }
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
@@ -331,6 +336,32 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       l = ldg_f32_pinned(lse + row);
       dl = ldg_f32_pinned(delta + row);
     };
+    // this key tile's dQ tile of step t (in the S columns of TMEM): D/4
+    // columns per warpgroup, scaled by 1/sqrt(D), stored chunk-major per
+    // 128-row tile: [J_K][slices][J_Q][D/4 float4 chunks][128 rows]
+    auto store_dq_tile = [&](int t) {
+      const int ti = t / G, tg = t % G;
+      const size_t slice = static_cast<size_t>((b * N_o + o0 + tg) * H + h);
+      const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
+      float4* out = reinterpret_cast<float4*>(dq_part) +
+                    ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D / 4) + wg * (D / 16) * BM + r;
+      if constexpr (D == 32) {
+        uint32_t qr[8];
+        tmem_ld8(tmem + lane_addr + kTDQ + 8 * wg, qr);
+        tc_wait_ld();
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+          out[v * BM] = make_float4(__uint_as_float(qr[4 * v]) * inv_sqrt_d, __uint_as_float(qr[4 * v + 1]) * inv_sqrt_d,
+                                    __uint_as_float(qr[4 * v + 2]) * inv_sqrt_d,
+                                    __uint_as_float(qr[4 * v + 3]) * inv_sqrt_d);
+      } else {
+        uint32_t qr[4];
+        tmem_ld4(tmem + lane_addr + kTDQ + 4 * wg, qr);
+        tc_wait_ld();
+        out[0] = make_float4(__uint_as_float(qr[0]) * inv_sqrt_d, __uint_as_float(qr[1]) * inv_sqrt_d,
+                             __uint_as_float(qr[2]) * inv_sqrt_d, __uint_as_float(qr[3]) * inv_sqrt_d);
+      }
+    };
     float lse_n, dl_n;
     row_stats(0, lse_n, dl_n);
     float2 dbacc[kCols / 2];  // dbias accumulators for this thread's key columns
@@ -363,6 +394,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // fully masked rows (lse = -inf) and rows past N: P = 0
         const float lse2 = (row_ok && lse_raw != -INFINITY) ? lse_raw * kLog2e : INFINITY;
         tc_wait_ld_regs(sv);
+        // S is in registers: the MMA warp may put the previous dQ tile there
+        tc_fence_before();
+        mbar_arrive(&bars->s_cons);
         const float2 nl2 = make_float2(-lse2, -lse2);
 #pragma unroll
         for (int v = 0; v < kCols / 8; ++v) {  // 8 keys per 16-byte chunk
@@ -378,24 +412,35 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           }
           const float2 mm[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
                                 make_float2(m1.z, m1.w)};
-          uint32_t pw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 s2 = make_float2(__uint_as_float(sv[v * 8 + 2 * e]), __uint_as_float(sv[v * 8 + 2 * e + 1]));
             const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
             float2 t = ffma2(b2, l2e2, ffma2(s2, c2, nl2));
             if (masked) t = fadd2(t, mm[e]);
-            const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            p[v * 4 + e] = pp;
-            pw[e] = pack_bf16x2(pp.x, pp.y);
+            p[v * 4 + e] = make_float2(ex2_approx(t.x), ex2_approx(t.y));
           }
-          *reinterpret_cast<uint4*>(sP + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
+      }
+      if (g == G - 1) mbar_arrive(&bars->b_empty[bst]);  // last read of this bias tile
+      if (s > 0) {
+        // the previous step's MMAs are complete: dQ tile in the S columns,
+        // P and dS in shared memory no longer read
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (s - 1) & 1, wc, abort))) { ok = false; break; }
+        tc_fence_after();
+        store_dq_tile(s - 1);
+      }
+#pragma unroll
+      for (int v = 0; v < kCols / 8; ++v) {
+        const int cc = (col0 >> 3) + v;
+        const uint32_t off = (cc >> 3) * (BM * 128) + sw128(r, cc & 7);
+        *reinterpret_cast<uint4*>(sP + off) =
+            make_uint4(pack_bf16x2(p[4 * v].x, p[4 * v].y), pack_bf16x2(p[4 * v + 1].x, p[4 * v + 1].y),
+                       pack_bf16x2(p[4 * v + 2].x, p[4 * v + 2].y), pack_bf16x2(p[4 * v + 3].x, p[4 * v + 3].y));
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
-      if (g == G - 1) mbar_arrive(&bars->b_empty[bst]);
 
       // ---------------- dS-phase
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, s & 1, wc, abort))) { ok = false; break; }
@@ -443,41 +488,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
         for (int k = 0; k < kCols / 2; ++k) dbacc[k] = make_float2(0.f, 0.f);
       }
-
-      // ---------------- dQ tile of this key tile: D/4 columns per warpgroup
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, s & 1, wc, abort))) { ok = false; break; }
+    }
+    // the last step's dQ tile
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (nsteps - 1) & 1, wc, abort))) {
       tc_fence_after();
-      {
-        // chunk-major per 128-row tile: [J_K][slices][J_Q][D/4 float4 chunks][128 rows]
-        const size_t slice = static_cast<size_t>((b * N_o + o0 + g) * H + h);
-        const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
-        float4* out = reinterpret_cast<float4*>(dq_part) +
-                      ((static_cast<size_t>(ktile) * nslices + slice) * JQ + i) * (BM * D / 4) + wg * (D / 16) * BM + r;
-        if constexpr (D == 32) {
-          uint32_t qr[8];
-          tmem_ld8(tmem + lane_addr + kTDQ + 8 * wg, qr);
-          tc_wait_ld();
-#pragma unroll
-          for (int v = 0; v < 2; ++v)
-            out[v * BM] = make_float4(__uint_as_float(qr[4 * v]) * inv_sqrt_d, __uint_as_float(qr[4 * v + 1]) * inv_sqrt_d,
-                                      __uint_as_float(qr[4 * v + 2]) * inv_sqrt_d,
-                                      __uint_as_float(qr[4 * v + 3]) * inv_sqrt_d);
-        } else {
-          uint32_t qr[4];
-          tmem_ld4(tmem + lane_addr + kTDQ + 4 * wg, qr);
-          tc_wait_ld();
-          out[0] = make_float4(__uint_as_float(qr[0]) * inv_sqrt_d, __uint_as_float(qr[1]) * inv_sqrt_d,
-                               __uint_as_float(qr[2]) * inv_sqrt_d, __uint_as_float(qr[3]) * inv_sqrt_d);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
+      store_dq_tile(nsteps - 1);
+    } else {
+      ok = false;
     }
 
     // ------------------------------------------------------------ epilogue: dV_g and dK_g of slice g = wg
     if (ok) {
       // the last dq_full wait above covers every MMA of this CTA
-      tc_fence_after();
       const int krow = ktile * BN + r;  // key of this thread's TMEM lane
       const int g = wg;
       const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + krow;

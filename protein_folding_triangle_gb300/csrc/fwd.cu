@@ -13,21 +13,27 @@
 // Warp roles (10 warps):
 //   warp 0     TMA producer: Q tiles once, then per key tile one bias tile and
 //              one K and one V tile per slice (rings of 2 / 4 / 4 stages).
-//   warp 1     TMEM allocator and single-thread tcgen05 MMA issuer:
-//              S = Q K^T into the score buffer of the slice's warpgroup, then
-//              O_g += P V with P read from TMEM (the score buffer's first
-//              64 columns, rewritten as packed BF16 by the softmax warps).
+//   warp 1     TMEM allocator and tcgen05 MMA issuer (one elected lane of a
+//              converged warp, descriptors precomputed): S = Q K^T into score
+//              buffer s % 3, then O_g += P V with P read from TMEM (the score
+//              buffer's first 64 columns, rewritten as packed BF16 by the
+//              softmax warps).  With three score buffers S(s+3) is issued
+//              right after P V(s), so a warpgroup's next scores are ready
+//              when it finishes a step.
 //   warps 2-9  two softmax warpgroups; warpgroup w owns the slices g with
 //              g % 2 == w, so while one warpgroup computes a softmax the MMA
 //              for the other one runs.  Thread = query row (TMEM lane).
-//              Pass 1 adds bias and key mask and writes the scores back to
-//              TMEM while taking the row max; pass 2 exponentiates (base 2),
-//              sums, and writes P as BF16 into TMEM.  O is rescaled in TMEM
-//              only when the running max grows by more than 2^8.  The
-//              epilogue writes O (BF16), the residual E = bf16(O32 - O) and lse.
+//              One pass over the scores exponentiates (base 2) against the
+//              running base m of the row and keeps P (BF16) in registers;
+//              if the tile's maximum lies more than 8 (log2 units) above m,
+//              or the row has nothing accumulated yet and the maximum lies
+//              more than 64 below m, the warp redoes the pass with the new
+//              base and O is rescaled in TMEM.  Only then is P written to
+//              TMEM.  The epilogue writes O (BF16), the residual
+//              E = bf16(O32 - O) and lse = m + ln l.
 //
-// TMEM (512 columns): score buffers at [0,128) (warpgroup 0) and [128,256)
-// (warpgroup 1); O_g at 256 + g*D.  Step s = j*GF + g uses buffer s % 2.
+// TMEM (512 columns): score buffers at [0,128), [128,256), [256,384); O_g at
+// 384 + g*D.  Step s = j*GF + g uses buffer s % 3.
 #include "kernels.cuh"
 
 namespace triattn {
@@ -42,7 +48,10 @@ constexpr int NBIAS = 2;    // bias ring depth
 constexpr int kEW = 256;               // softmax threads (two warpgroups)
 constexpr int kThreads = 64 + kEW;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThresh = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThresh = 8.0f;  // log2 units: P stays below 2^8
+constexpr float kLowThresh = -64.0f;    // log2 units: rebase an empty row whose maximum is this far below
+constexpr int kTO = 384;                // first O column in TMEM
 
 template <int D>
 struct FwdSmem {
@@ -65,7 +74,7 @@ struct FwdBars {
   uint64_t k_full[NSLOT], k_empty[NSLOT];
   uint64_t v_full[NSLOT], v_empty[NSLOT];
   uint64_t b_full[NBIAS], b_empty[NBIAS];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[3], p_full[3];
   uint64_t all_done;
   uint32_t tmem_slot;
   int abort;
@@ -108,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->b_full[i], 1);
       mbar_init(&bars->b_empty[i], kEW);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], BM);
     }
@@ -158,47 +167,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;       // 64B / 32B swizzle
-      constexpr uint32_t kSbo = 8u * D * 2u;               // 8 rows of D bf16
-      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
-      const uint32_t sQ = smem_u32(sm + L::kQ), sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
-      bool ok = mbar_wait(&bars->q_full, 0, wc, abort);
-      auto issue_s = [&](int s) -> bool {
-        const int g = s % GF, slot = s % NSLOT;
-        if (!mbar_wait(&bars->k_full[slot], (s / NSLOT) & 1, wc, abort)) return false;
-        tc_fence_after();
-        const uint32_t dS = tmem + (s & 1) * BN;
+    constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;       // 64B / 32B swizzle
+    constexpr uint32_t kSbo = 8u * D * 2u;               // 8 rows of D bf16
+    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
+    constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
+    constexpr uint32_t kTile16 = L::kTile >> 4;          // tile size in descriptor units
+    constexpr uint32_t kRowStep = (16 * D * 2) >> 4;     // 16 rows of a D-wide tile
+    // base descriptors; per-MMA offsets are added to the start-address field
+    const uint64_t dQb = smem_desc(smem_u32(sm + L::kQ), 16, kSbo, kSwz);
+    const uint64_t dKb = smem_desc(smem_u32(sm + L::kK), 16, kSbo, kSwz);
+    const uint64_t dVb = smem_desc(smem_u32(sm + L::kV), 16, kSbo, kSwz);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wc, abort));
+    auto issue_s = [&](int s) -> bool {
+      const int g = s % GF, slot = s % NSLOT;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[slot], (s / NSLOT) & 1, wc, abort))) return false;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t dS = tmem + (s % 3) * BN;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = smem_desc(sQ + g * L::kTile + kk * 32, 16, kSbo, kSwz);
-          const uint64_t bdesc = smem_desc(sK + slot * L::kTile + kk * 32, 16, kSbo, kSwz);
-          mma_ss(dS, a, bdesc, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->s_full[s & 1]);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(dS, dQb + g * kTile16 + 2 * kk, dKb + slot * kTile16 + 2 * kk, idS, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->s_full[s % 3]);
         mma_commit(&bars->k_empty[slot]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && nsteps > 1) ok = issue_s(1);
-      for (int s = 0; s < nsteps && ok; ++s) {
-        const int g = s % GF, j = s / GF, slot = s % NSLOT;
-        if (!mbar_wait(&bars->p_full[s & 1], (s >> 1) & 1, wc, abort)) { ok = false; break; }
-        if (!mbar_wait(&bars->v_full[slot], (s / NSLOT) & 1, wc, abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t dO = tmem + 256 + g * D;
-        const uint32_t aP = tmem + (s & 1) * BN;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bdesc = smem_desc(sV + slot * L::kTile + kk * 16 * D * 2, 16, kSbo, kSwz);
-          mma_ts(dO, aP + kk * 8, bdesc, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bars->v_empty[slot]);
-        if (s + 2 < nsteps) ok = issue_s(s + 2);
       }
-      mma_commit(&bars->all_done);
+      __syncwarp();
+      return true;
+    };
+    for (int s = 0; s < 3 && s < nsteps && ok; ++s) ok = issue_s(s);
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int g = s % GF, j = s / GF, slot = s % NSLOT, buf = s % 3;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[buf], (s / 3) & 1, wc, abort))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[slot], (s / NSLOT) & 1, wc, abort))) { ok = false; break; }
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t dO = tmem + kTO + g * D;
+        const uint32_t aP = tmem + buf * BN;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(dO, aP + kk * 8, dVb + slot * kTile16 + kk * kRowStep, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->v_empty[slot]);
+      }
+      __syncwarp();
+      if (s + 3 < nsteps) ok = issue_s(s + 3);
     }
+    if (elect_one()) mma_commit(&bars->all_done);
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int ew = tid - 64;              // 0..255
@@ -233,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     named_bar_sync(1, kEW);
 
-    // running max (natural units) and sum for this warpgroup's two slices
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    const float2 isd2 = make_float2(inv_sqrt_d, inv_sqrt_d);
+    // running base m (natural units) and sum l for this warpgroup's two slices
+    float m_run[2] = {0.f, 0.f}, l_run[2] = {0.f, 0.f};
+    const float2 c2 = make_float2(inv_sqrt_d * kLog2e, inv_sqrt_d * kLog2e);
     const float2 l2e2 = make_float2(kLog2e, kLog2e);
     bool ok = true;
 
@@ -243,120 +256,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j % NBIAS;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->b_full[st], (j / NBIAS) & 1, wc, abort))) { ok = false; break; }
       const uint8_t* bias_s = sm + L::kBias + st * (BM * BN * 2);
-#pragma unroll
+#pragma unroll 1
       for (int sl = 0; sl < 2; ++sl) {
         const int g = wg + 2 * sl;
         const int s = j * GF + g;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[wg], (s >> 1) & 1, wc, abort))) { ok = false; break; }
+        const int buf = s % 3;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], (s / 3) & 1, wc, abort))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tS = tmem + lane_addr + wg * BN;
+        const uint32_t tS = tmem + lane_addr + buf * BN;
         const float* mk = mask2 + s * BN;
         const uint8_t* fl = mflag + s * 16;
 
-        // pass 1: u = S / sqrt(D) + bias + mask, written back to TMEM; row max.
-        // 32-key chunks, the load of chunk c+1 in flight while c is computed.
-        float mt = -INFINITY;
-        uint32_t buf[2][32];
-        tmem_ld32(tS, buf[0]);
+        // t = (S / sqrt(D) + bias + mask - base) log2 e; returns max t and,
+        // with_exp, p = 2^t packed to BF16 in pw and sum p.  16-key chunks,
+        // the TMEM load of chunk c+1 in flight while chunk c is computed.
+        uint32_t pw[2][32];
+        auto score_pass = [&](float base, bool with_exp, float& tmax, float& lsum) {
+          const float2 nb2 = make_float2(-base * kLog2e, -base * kLog2e);
+          float2 ls = make_float2(0.f, 0.f);
+          float tm = -INFINITY;
+          uint32_t sb[2][16];
+          tmem_ld16(tS, sb[0]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t(&raw)[32] = buf[c & 1];
-          tc_wait_ld_regs(raw);
-          if (c + 1 < 4) {
-            if (c >= 1) tc_wait_st();  // buf[(c+1)&1] fed the store of chunk c-1
-            tmem_ld32(tS + (c + 1) * 32, buf[(c + 1) & 1]);
-          }
+          for (int c = 0; c < 8; ++c) {
+            uint32_t(&raw)[16] = sb[c & 1];
+            tc_wait_ld_regs(raw);
+            if (c + 1 < 8) tmem_ld16(tS + (c + 1) * 16, sb[(c + 1) & 1]);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int cc = c * 4 + v;  // 8-key chunk (0..15)
-            const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + (cc >> 3) * (BM * 128) + sw128(r, cc & 7));
-            const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
-            const bool masked = fl[cc] != 0;
-            float4 m0 = make_float4(0.f, 0.f, 0.f, 0.f), m1 = m0;
-            if (masked) {
-              m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
-              m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
+            for (int v = 0; v < 2; ++v) {
+              const int cc = c * 2 + v;  // 8-key chunk (0..15)
+              const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + (cc >> 3) * (BM * 128) + sw128(r, cc & 7));
+              const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
+              const bool masked = fl[cc] != 0;
+              float4 m0 = make_float4(0.f, 0.f, 0.f, 0.f), m1 = m0;
+              if (masked) {
+                m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
+                m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
+              }
+              const float2 mm[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                                    make_float2(m1.z, m1.w)};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = v * 8 + 2 * e;
+                const float2 s2 = make_float2(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]));
+                const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
+                float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nb2));
+                if (masked) t = ffma2(mm[e], l2e2, t);
+                tm = fmax3(tm, t.x, t.y);
+                if (with_exp) {
+                  const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+                  ls = fadd2(ls, p);
+                  pw[c >> 2][(c & 3) * 8 + v * 4 + e] = pack_bf16x2(p.x, p.y);
+                }
+              }
             }
-            const float2 mm[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
-                                  make_float2(m1.z, m1.w)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k = v * 8 + 2 * e;
-              const float2 s2 = make_float2(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]));
-              const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
-              float2 u = ffma2(s2, isd2, b2);
-              if (masked) u = fadd2(u, mm[e]);
-              mt = fmax3(mt, u.x, u.y);
-              raw[k] = __float_as_uint(u.x);
-              raw[k + 1] = __float_as_uint(u.y);
-            }
           }
-          tmem_st32(tS + c * 32, raw);
+          tmax = tm;
+          lsum = ls.x + ls.y;
+        };
+
+        float tmax, lsum;
+        if (j == 0) {
+          // first key tile: the base is the tile's row maximum
+          score_pass(0.f, false, tmax, lsum);
+          m_run[sl] = tmax == -INFINITY ? 0.f : tmax * kLn2;
+        }
+        score_pass(m_run[sl], true, tmax, lsum);
+        // later tiles keep the base unless the tile maximum overshoots it (P
+        // would grow past 2^8), or nothing is accumulated yet and the maximum
+        // lies far below it; then the warp redoes the pass with a new base
+        const bool up = tmax > kRescaleThresh;
+        const bool down = l_run[sl] == 0.f && tmax < kLowThresh && tmax != -INFINITY;
+        const bool need = up || down;
+        float alpha = 1.f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_old = m_run[sl];
+          if (need) m_run[sl] = m_old + tmax * kLn2;
+          float t2;
+          score_pass(m_run[sl], true, t2, lsum);
+          if (need && l_run[sl] > 0.f) alpha = ex2_approx((m_old - m_run[sl]) * kLog2e);
         }
         if (sl == 1) mbar_arrive(&bars->b_empty[st]);  // this warpgroup's last read of the bias tile
-
-        // online softmax with lazy rescaling of O (kept in TMEM)
-        const float m_new = fmaxf(m_run[sl], mt);
-        float alpha = 1.f;
-        bool need = false;
-        if (j == 0) {
-          m_run[sl] = m_new;
-        } else {
-          need = (m_new - m_run[sl]) * kLog2e > kRescaleThresh;
-          if (need) {
-            alpha = ex2_approx((m_run[sl] - m_new) * kLog2e);
-            m_run[sl] = m_new;
-          }
-        }
-        const float msub = (m_run[sl] == -INFINITY) ? 0.f : m_run[sl];
-        const float2 nm2 = make_float2(-msub * kLog2e, -msub * kLog2e);
-        tc_wait_st();
-
-        // pass 2: p = 2^((u - m) log2 e); P (BF16) into the first 64 columns
-        float2 lsum = make_float2(0.f, 0.f);
-        uint32_t pw[2][16];
-        tmem_ld32(tS, buf[0]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t(&raw)[32] = buf[c & 1];
-          tc_wait_ld_regs(raw);
-          if (c + 1 < 4) tmem_ld32(tS + (c + 1) * 32, buf[(c + 1) & 1]);
-          if (c >= 2) tc_wait_st();  // pw[c&1] fed the store of chunk c-2
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 u = make_float2(__uint_as_float(raw[2 * e]), __uint_as_float(raw[2 * e + 1]));
-            const float2 t = ffma2(u, l2e2, nm2);
-            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            lsum = fadd2(lsum, p);
-            pw[c & 1][e] = pack_bf16x2(p.x, p.y);
-          }
-          // P of keys [32c, 32c+32) lands in columns [16c, 16c+16): already read
-          tmem_st16(tS + c * 16, pw[c & 1]);
-        }
-        l_run[sl] = l_run[sl] * alpha + (lsum.x + lsum.y);
-        if (__any_sync(0xffffffffu, need)) {
-          // O_g's previous P.V (step s - 4) was issued before this warpgroup's
-          // previous S (step s - 2); s_full of this step implies it finished.
-          const uint32_t tO = tmem + lane_addr + 256 + g * D;
-          if constexpr (D == 32) {
-            uint32_t ov[32];
-            tmem_ld32(tO, ov);
-            tc_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(tO, ov);
-          } else {
+        l_run[sl] = l_run[sl] * alpha + lsum;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // O_g's previous P.V (step s - 4) was issued before S(s - 1); the
+          // S of this step was issued after it, so s_full implies it finished.
+          const uint32_t tO = tmem + lane_addr + kTO + g * D;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 16) {
             uint32_t ov[16];
-            tmem_ld16(tO, ov);
-            tc_wait_ld();
+            tmem_ld16(tO + c0, ov);
+            tc_wait_ld_regs(ov);
 #pragma unroll
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st16(tO, ov);
+            tmem_st16(tO + c0, ov);
           }
         }
+        // P of keys [32c, 32c+32) into columns [16c, 16c+16): S is no longer read
+        tmem_st32(tS, pw[0]);
+        tmem_st32(tS + 32, pw[1]);
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[wg]);
+        mbar_arrive(&bars->p_full[buf]);
       }
     }
 
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = wg + 2 * sl;
         float ov[D];
         {
-          const uint32_t tO = tmem + lane_addr + 256 + g * D;
+          const uint32_t tO = tmem + lane_addr + kTO + g * D;
           if constexpr (D == 32) {
             uint32_t raw[32];
             tmem_ld32(tO, raw);

@@ -140,3 +140,22 @@ def test_autograd_wrapper_matches_direct_calls():
     assert torch.equal(o.detach(), direct["o"])
     for t, g in ((q, "dq"), (k, "dk"), (v, "dv"), (bias, "dbias")):
         assert torch.equal(t.grad, direct[g]), g
+
+
+def test_large_logit_shifts_across_key_tiles():
+    """Rows whose logits jump by tens of units between key tiles: some rows
+    start far below zero (-90 on the first key tile), some jump up by +40 on
+    the second, others stay near zero.  The online softmax must rebase each
+    such row (and rescale its partial output) without losing precision."""
+    w = S.custom(1, 384, 2, 32, name="shift", mask="tail", mask_frac=0.05)
+    x = S.make_inputs(w, seed=11)
+    bias = x["bias"].float()
+    rows = torch.arange(384)
+    low = (rows % 3 == 0).float()[:, None]          # rows starting at -90
+    high = (rows % 2 == 0).float()[:, None]         # rows jumping by +40 on key tile 1
+    bias[..., :128] += -90.0 * low
+    bias[..., 128:256] += 40.0 * high
+    x["bias"] = bias.to(torch.bfloat16)
+    out = gpu_fwd_bwd(to_dev(x))
+    errs = compare_full(out, oracle_full(x))
+    check_errs(errs, "logit_shifts")

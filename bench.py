@@ -157,6 +157,7 @@ KERNEL_SOURCES = {
     "tri_attn_fwd": ["protein_folding_triangle_gb300/csrc/fwd.cu", "protein_folding_triangle_gb300/csrc/ptx.cuh"],
     "bwd_main": ["protein_folding_triangle_gb300/csrc/bwd.cu", "protein_folding_triangle_gb300/csrc/ptx.cuh"],
     "bwd_preprocess": ["protein_folding_triangle_gb300/csrc/bwd.cu"],
+    "bwd_transpose_bias": ["protein_folding_triangle_gb300/csrc/bwd.cu"],
     "bwd_reduce_dq": ["protein_folding_triangle_gb300/csrc/bwd.cu"],
     "bwd_reduce_dbias": ["protein_folding_triangle_gb300/csrc/bwd.cu"],
 }
@@ -187,7 +188,10 @@ def kernel_work(w, name):
     if name == "bwd_main":
         return 10 * U, "flop", "tensor"
     if name == "bwd_preprocess":
-        return 3 * rows * w.D * 2 + rows * 4, "byte", "hbm"
+        jq = (w.N + 127) // 128
+        return 3 * rows * w.D * 2 + rows * 4 + w.B * w.No * w.H * jq * 128 * 8, "byte", "hbm"
+    if name == "bwd_transpose_bias":
+        return 2 * w.B * w.H * w.N * w.N * 2, "byte", "hbm"
     if name == "bwd_reduce_dq":
         return jk * rows * w.D * 4 + rows * w.D * 2, "byte", "hbm"
     if name == "bwd_reduce_dbias":
@@ -386,7 +390,8 @@ def run_ours(args):
         runit = "GB/s"
     traffic = ncu_traffic(dom)
     fwd_ms = trace.get("tri_attn_fwd", {}).get("mean_ms")
-    bwd_ms = sum(trace[n]["mean_ms"] for n in ("bwd_preprocess", "bwd_main", "bwd_reduce_dq", "bwd_reduce_dbias")
+    bwd_ms = sum(trace[n]["mean_ms"] for n in ("bwd_preprocess", "bwd_transpose_bias", "bwd_main", "bwd_reduce_dq",
+                                                "bwd_reduce_dbias")
                  if n in trace)
     clocks = clk.summary()
     line = {

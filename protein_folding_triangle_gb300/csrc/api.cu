@@ -81,7 +81,8 @@ bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over the [B*H, N (q), N (k)] bf16 bias, box = 128 q rows x 64 keys.
+// 3-D map over a [B*H, N, N] bf16 matrix (the bias, or its transposed copy),
+// box = 128 rows x 64 columns.
 bool make_bias_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->N), static_cast<cuuint64_t>(s->N),
                               static_cast<cuuint64_t>(s->B) * s->H};
@@ -96,29 +97,31 @@ bool make_bias_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t delta_off, dq_off, db_off, total;
+  size_t stat_off, biasT_off, dq_off, db_off, total;
 };
 
-// delta [rows] FP32; dQ partials [J_K][slices][J_Q][128 x D] FP32; dbias partials
-// [N_o/G][B*H][J_Q][J_K][128 x 128] FP32 (partials padded to whole tiles).
+// -lse log2 e / -delta records [slices][J_Q][2 x 128] FP32; transposed bias
+// [B*H][N][N] BF16; dQ partials [J_K][slices][J_Q][128 x D] FP32; dbias
+// partials [N_o/G][B*H][J_Q][J_K][128 x 128] FP32 (padded to whole tiles);
+// each part 256-byte aligned.
 WsLayout ws_layout(const triattn_shape* s) {
-  const size_t rows = static_cast<size_t>(s->B) * s->N_o * s->H * s->N;
   const size_t slices = static_cast<size_t>(s->B) * s->N_o * s->H;
   const size_t jk = (s->N + kTileK - 1) / kTileK;
   const size_t jq = (s->N + kTileQ - 1) / kTileQ;
   const size_t groups = s->N_o / kGroupBwd;
   WsLayout w;
-  w.delta_off = 0;
-  w.dq_off = round_up(rows * 4, 256);
+  w.stat_off = 0;
+  w.biasT_off = round_up(slices * jq * 2 * kTileQ * 4, 256);
+  w.dq_off = w.biasT_off + round_up(static_cast<size_t>(s->B) * s->H * s->N * s->N * 2, 256);
   w.db_off = w.dq_off + round_up(jk * slices * jq * kTileQ * s->D * 4, 256);
   w.total = w.db_off + round_up(groups * s->B * s->H * jq * jk * kTileQ * kTileK * 4, 256);
   return w;
 }
 
 // ---------------------------------------------------------------- tracing
-enum KernelKind { kKFwd = 0, kKPre, kKMain, kKRedDq, kKRedDb, kKinds };
-const char* const kKernelName[kKinds] = {"tri_attn_fwd", "bwd_preprocess", "bwd_main", "bwd_reduce_dq",
-                                         "bwd_reduce_dbias"};
+enum KernelKind { kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKinds };
+const char* const kKernelName[kKinds] = {"tri_attn_fwd",  "bwd_preprocess", "bwd_transpose_bias",
+                                         "bwd_main",      "bwd_reduce_dq",  "bwd_reduce_dbias"};
 struct TraceRec {
   int kind;
   cudaEvent_t a, b;
@@ -234,10 +237,12 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
   if ((st = init_device(&dev)) != TRIATTN_OK) return st;
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
-      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_bias, bias, shape))
-    return TRIATTN_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.biasT = ws + w.biasT_off;
+  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
+      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_biasT, a.biasT, shape))
+    return TRIATTN_ERR_CUDA;
+  a.bias = bias;
   a.mask = mask;
   a.o = o;
   a.o_resid = o_resid;
@@ -247,7 +252,7 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
   a.dk = dk;
   a.dv = dv;
   a.dbias = dbias;
-  a.delta = reinterpret_cast<float*>(ws + w.delta_off);
+  a.stat = reinterpret_cast<float*>(ws + w.stat_off);
   a.dq_part = reinterpret_cast<float*>(ws + w.dq_off);
   a.dbias_part = reinterpret_cast<float*>(ws + w.db_off);
   a.B = shape->B;
@@ -258,6 +263,7 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool d32 = shape->D == 32;
   cudaError_t e = traced(kKPre, s, [&] { return d32 ? launch_bwd_preprocess<32>(a, s) : launch_bwd_preprocess<16>(a, s); });
+  if (e == cudaSuccess) e = traced(kKTrans, s, [&] { return launch_bwd_transpose_bias(a, s); });
   if (e == cudaSuccess)
     e = traced(kKMain, s, [&] { return d32 ? launch_bwd_main<32>(a, s) : launch_bwd_main<16>(a, s); });
   if (e == cudaSuccess)

@@ -29,7 +29,8 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_bias;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_biasT;
+  const void* bias;  // [B*H][N][N]
   const void* mask;
   const void* o;
   const void* o_resid;
@@ -39,8 +40,9 @@ struct BwdArgs {
   void* dk;
   void* dv;
   void* dbias;
-  float* delta;      // [rows]
-  float* dq_part;    // [J_K][rows][D]
+  void* biasT;       // [B*H][N (k)][N (q)] transposed copy of the bias
+  float* stat;       // [slices][J_Q][2 x 128]: -lse log2 e, -delta
+  float* dq_part;    // [J_K][slices][J_Q][128 x D]
   float* dbias_part; // [L][B*H*N*N]
   int B, N_o, N, H;
   WaitCtl wc;
@@ -52,6 +54,7 @@ template <int D> int fwd_smem_bytes(int N);
 
 template <int D> cudaError_t setup_bwd();
 template <int D> cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_transpose_bias(const BwdArgs& a, cudaStream_t stream);
 template <int D> cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 template <int D> cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream);

@@ -99,13 +99,20 @@ __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __r
 // column = query, so P^T and dS^T land in TMEM where the dV and dK MMAs read
 // them as their A operand, and the key mask of a slice is one value per thread.
 //
-// Thread roles (18 warps):
+// Thread roles (20 warps):
 //   warp 0       TMA producer: K, V of the G slices once; per query tile one
 //                transposed bias tile; per (query tile, slice) the Q and dO
 //                tiles and the record of -lse log2 e and -delta.
-//   warp 1       TMEM owner and tcgen05 MMA issuer (converged warp, one
-//                elected lane issues; descriptors are precomputed).
-//   warps 2-17   four elementwise warpgroups.  Each covers all 128 TMEM lanes
+//   warps 1-3    three tcgen05 MMA issuers (converged warps, one elected lane
+//                issues one group per step; descriptors are precomputed).  A
+//                single issuing thread spends ~27 cycles per N = 32 MMA and
+//                ~100 per group boundary, so the step's 28 MMAs are split:
+//                warp 1 (also TMEM owner): dV_g += P^T dO, then S^T(s+1);
+//                warp 2: dK_g += dS^T Q, then dP^T(s+1);
+//                warp 3: the dQ tile dS K.
+//                Each pair stays in one thread, so dV (dK) reads P^T (dS^T)
+//                before S^T (dP^T) of the next step overwrites it.
+//   warps 4-19   four elementwise warpgroups.  Each covers all 128 TMEM lanes
 //                (thread = key row for S^T / dP^T / dK / dV, query row for the
 //                dQ tile); warpgroup w handles query columns [32w, 32w + 32).
 //
@@ -118,8 +125,8 @@ __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __r
 //             and into shared memory (the A operand of the dQ MMA).
 // MMA order per step: dV_g += P^T dO (A from TMEM) and S^T(s+1) after the
 // P-phase; dK_g += dS^T Q (A from TMEM) and dP^T(s+1) after the dS-phase; the
-// dQ tile dS K (into S^T columns [64, 64 + D)) once every warp has loaded
-// S^T(s+1).  The P-phase of s+1 reads that dQ tile.  dK is scaled by
+// dQ tile dS K (into S^T columns [64, 64 + D)) after the dS-phase, once every
+// warp has loaded S^T(s+1).  The P-phase of s+1 reads that dQ tile.  dK is scaled by
 // 1/sqrt(D) when it leaves TMEM, the dQ tile when it is read.  After slice
 // G-1 of a query tile the FP32 dbias partial of the outer group is written
 // once.
@@ -142,13 +149,13 @@ struct BwdSmem {
 constexpr int kNWG = 4;                // elementwise warpgroups
 constexpr int kCols = BM / kNWG;       // query columns per warpgroup
 constexpr int kEW = 128 * kNWG;        // elementwise threads
-constexpr int kMainThreads = 64 + kEW;
+constexpr int kMainThreads = 128 + kEW;
 
 struct BwdBars {
   uint64_t kv_full;
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t b_full[2], b_empty[2];
-  uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full;
+  uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full, all_done;
   uint32_t tmem_slot;
   int abort;
 };
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->qdo_full[i], 1);
-      mbar_init(&bars->qdo_empty[i], 1);
+      mbar_init(&bars->qdo_empty[i], 2);  // issuers A (S, dV) and C (dP, dK)
       mbar_init(&bars->b_full[i], 1);
       mbar_init(&bars->b_empty[i], kEW);
     }
@@ -207,6 +214,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&bars->p_ready, kEW);
     mbar_init(&bars->ds_ready, kEW);
     mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->all_done, 3);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -250,8 +258,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                   kStatFloats * 4, &bars->qdo_full[st]);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp <= 3) {
+    // ------------------------------------------------------------ MMA issuers
     constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;  // 64B / 32B swizzle for D-wide rows
     constexpr uint32_t kSbo = 8u * D * 2u;
     constexpr uint32_t idSS = idesc_bf16_f32(BN, BM, 0, 0);     // S^T, dP^T: A, B K-major
@@ -265,82 +273,110 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const uint64_t dKb = smem_desc(smem_u32(sm + L::kK), 16, kSbo, kSwz);
     const uint64_t dVb = smem_desc(smem_u32(sm + L::kV), 16, kSbo, kSwz);
     const uint64_t dDSmn = smem_desc(smem_u32(sm + L::kDS), 16384, 1024, 2);  // dS (queries contiguous)
-    auto issue_s = [&](int s) {  // S^T = K Q^T
-      const uint64_t qd = dQb + (s & 1) * kTile16, kd = dKb + (s % G) * kTile16;
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTS, kd + 2 * kk, qd + 2 * kk, idSS, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->s_full);
-      }
-      __syncwarp();
-    };
-    auto issue_dp = [&](int s) {  // dP^T = V dO^T
-      const uint64_t dod = dDOb + (s & 1) * kTile16, vd = dVb + (s % G) * kTile16;
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTDP, vd + 2 * kk, dod + 2 * kk, idSS, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->dp_full);
-      }
-      __syncwarp();
-    };
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, wc, abort)) &&
-              __all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[0], 0, wc, abort));
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-    }
-    for (int s = 0; s < nsteps && ok; ++s) {
-      const int i = s / G, g = s % G, st = s & 1;
-      const uint64_t qd = dQb + st * kTile16, dod = dDOb + st * kTile16, kd = dKb + g * kTile16;
-      // P-phase of s done: P^T in TMEM, the previous dQ tile read
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_ready, s & 1, wc, abort))) { ok = false; break; }
-      tc_fence_after();
-      if (elect_one()) {
-        const uint32_t tdv = tmem + g * D;
+              (warp == 3 || __all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[0], 0, wc, abort)));
+    if (warp == 1) {
+      // ---- issuer A: dV_g += P^T dO, then S^T(s+1) = K Q^T
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)  // dV_g += P^T dO
-          mma_ts(tdv, tmem + kTS + 8 * kk, dod + kk * kRowStep, idKV, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTS, dKb + 2 * kk, dQb + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->s_full);
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      if (s + 1 < nsteps) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort))) {
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int i = s / G, g = s % G, st = s & 1;
+        const bool next = s + 1 < nsteps;
+        // P-phase of s done (P^T in TMEM, the previous dQ tile read); Q(s+1) loaded
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_ready, s & 1, wc, abort)) ||
+            (next && !__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort)))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_s(s + 1);  // after dV_g in the pipe: P^T is read before it is overwritten
-      }
-      // dS-phase of s done: dS^T in TMEM and shared memory
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, s & 1, wc, abort))) { ok = false; break; }
-      tc_fence_after();
-      if (elect_one()) {
-        const uint32_t tdk = tmem + 4 * D + g * D;
+        const uint64_t dod = dDOb + st * kTile16;
+        const uint64_t qn = dQb + ((s + 1) & 1) * kTile16, kn = dKb + ((s + 1) % G) * kTile16;
+        if (elect_one()) {
+          const uint32_t tdv = tmem + g * D;
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)  // dK_g += dS^T Q
-          mma_ts(tdk, tmem + kTDP + 32 * (kk >> 1) + 8 * (kk & 1), qd + kk * kRowStep, idKV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BM / 16; ++kk)  // dV_g += P^T dO
+            mma_ts(tdv, tmem + kTS + 8 * kk, dod + kk * kRowStep, idKV, (i > 0 || kk > 0) ? 1u : 0u);
+          if (next) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTS, kn + 2 * kk, qn + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+            mma_commit(&bars->s_full);
+          }
+          mma_commit(&bars->qdo_empty[st]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      if (s + 1 < nsteps) {
-        issue_dp(s + 1);  // after dK_g in the pipe
-        // the dQ tile goes into S^T columns once every warp has loaded S^T(s+1)
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_cons, (s + 1) & 1, wc, abort))) { ok = false; break; }
+    } else if (warp == 2) {
+      // ---- issuer C: dK_g += dS^T Q, then dP^T(s+1) = V dO^T
+      if (ok) {
         tc_fence_after();
-      }
-      if (elect_one()) {
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)  // dQ tile = dS K (A = dS, queries contiguous; B = K MN-major)
-          mma_ss(tmem + kTDQ, dDSmn + kk * 128, kd + kk * kRowStep, idQ, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);        // covers every MMA issued so far
-        mma_commit(&bars->qdo_empty[st]);
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTDP, dVb + 2 * kk, dDOb + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->dp_full);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int i = s / G, st = s & 1;
+        const bool next = s + 1 < nsteps;
+        // dS-phase of s done (dS^T in TMEM); dO(s+1) loaded
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, s & 1, wc, abort)) ||
+            (next && !__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort)))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t qd = dQb + st * kTile16;
+        const uint64_t don = dDOb + ((s + 1) & 1) * kTile16, vn = dVb + ((s + 1) % G) * kTile16;
+        if (elect_one()) {
+          const uint32_t tdk = tmem + 4 * D + (s % G) * D;
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)  // dK_g += dS^T Q
+            mma_ts(tdk, tmem + kTDP + 32 * (kk >> 1) + 8 * (kk & 1), qd + kk * kRowStep, idKV,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+          if (next) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTDP, vn + 2 * kk, don + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+            mma_commit(&bars->dp_full);
+          }
+          mma_commit(&bars->qdo_empty[st]);
+        }
+        __syncwarp();
+      }
+    } else {
+      // ---- issuer B: the dQ tile dS K into S^T columns [64, 64 + D)
+      for (int s = 0; s < nsteps && ok; ++s) {
+        // dS of s in shared memory; every warp has loaded S^T(s+1)
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, s & 1, wc, abort)) ||
+            (s + 1 < nsteps && !__all_sync(0xffffffffu, mbar_wait(&bars->s_cons, (s + 1) & 1, wc, abort)))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t kd = dKb + (s % G) * kTile16;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)  // A = dS (queries contiguous), B = K MN-major
+            mma_ss(tmem + kTDQ, dDSmn + kk * 128, kd + kk * kRowStep, idQ, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->dq_full);
+        }
+        __syncwarp();
+      }
     }
+    // every MMA this issuer started is complete when all_done fires
+    if (elect_one()) mma_commit(&bars->all_done);
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
-    const int wg = (warp - 2) >> 2;           // query-column quarter handled by this warpgroup
+    const int wg = (warp - 4) >> 2;           // query-column quarter handled by this warpgroup
     const int r = quarter * 32 + lane;        // TMEM lane: key row (S^T, dP^T, dK, dV) / query row (dQ)
     const int col0 = wg * kCols;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
@@ -526,8 +562,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue: dV_g and dK_g of slice g = wg
-    if (ok) {
-      // the last dq_full wait above covers every MMA of this CTA
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->all_done, 0, wc, abort))) {
+      tc_fence_after();
       const int g = wg;
       const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + key;
 #pragma unroll

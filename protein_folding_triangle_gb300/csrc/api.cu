@@ -68,12 +68,12 @@ triattn_status check_shape(const triattn_shape* s) {
   return TRIATTN_OK;
 }
 
-// 3-D map over a [slices, N, D] bf16 tensor, box = 128 rows x D.
-bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
+// 3-D map over a [slices, N, D] bf16 tensor, box = box_rows rows x D.
+bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s, unsigned box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->D), static_cast<cuuint64_t>(s->N),
                               static_cast<cuuint64_t>(s->B) * s->N_o * s->H};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s->D) * 2, static_cast<cuuint64_t>(s->N) * s->D * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(s->D), 128u, 1u};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(s->D), box_rows, 1u};
   const cuuint32_t es[3] = {1u, 1u, 1u};
   const CUtensorMapSwizzle sw = (s->D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -201,8 +201,8 @@ triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const voi
   if ((st = init_device(&dev)) != TRIATTN_OK) return st;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
-      !make_bias_map(&a.tm_bias, bias, shape))
+  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape, 64) ||
+      !make_rows_map(&a.tm_v, v, shape, 64) || !make_bias_map(&a.tm_bias, bias, shape))
     return TRIATTN_ERR_CUDA;
   a.mask = mask;
   a.o = o;

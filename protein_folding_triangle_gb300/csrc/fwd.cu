@@ -6,34 +6,38 @@
 // [B, N_o, H, N, D]; Figure 9 and the Abstract describe the saved BF16
 // output-rounding residual used by the backward.
 //
-// One CTA owns (b, h, a 128-row query tile i, a group of GF = 4 outer slices).
-// The four slices of the group use the same bias tile for every key tile, so
-// each bias tile is loaded once into shared memory and read by four slices.
+// One CTA owns (b, h, a 128-row query tile, a group of GF = 4 outer slices).
+// The four slices use the same bias tile for every key tile, so each bias
+// tile is loaded once into shared memory and read by four warpgroups.  Key
+// tiles are 64 wide, so the four slices each get their own softmax
+// warpgroup and their own score, P and O columns in TMEM.
 //
-// Warp roles (10 warps):
-//   warp 0     TMA producer: Q tiles once, then per key tile one bias tile and
-//              one K and one V tile per slice (rings of 2 / 4 / 4 stages).
-//   warp 1     TMEM allocator and tcgen05 MMA issuer (one elected lane of a
-//              converged warp, descriptors precomputed): S = Q K^T into score
-//              buffer s % 3, then O_g += P V with P read from TMEM (the score
-//              buffer's first 64 columns, rewritten as packed BF16 by the
-//              softmax warps).  With three score buffers S(s+3) is issued
-//              right after P V(s), so a warpgroup's next scores are ready
-//              when it finishes a step.
-//   warps 2-9  two softmax warpgroups; warpgroup w owns the slices g with
-//              g % 2 == w, so while one warpgroup computes a softmax the MMA
-//              for the other one runs.  Thread = query row (TMEM lane).
-//              One pass over the scores exponentiates (base 2) against the
-//              running base m of the row and keeps P (BF16) in registers;
-//              if the tile's maximum lies more than 8 (log2 units) above m,
-//              or the row has nothing accumulated yet and the maximum lies
-//              more than 64 below m, the warp redoes the pass with the new
-//              base and O is rescaled in TMEM.  Only then is P written to
-//              TMEM.  The epilogue writes O (BF16), the residual
-//              E = bf16(O32 - O) and lse = m + ln l.
+// Warp roles (20 warps):
+//   warp 0       TMA producer: the four Q tiles once; per 64-key tile one
+//                bias tile and, per slice, one K and one V tile (rings of
+//                3 / 2 / 2 stages).
+//   warps 1, 2   tcgen05 MMA issuers (converged warps, one elected lane
+//                issues, descriptors precomputed), for slices {0,1} and
+//                {2,3}: S(j+1) = Q K^T as soon as the warpgroup has loaded
+//                S(j) into registers, O += P V(j) once it has written P(j).
+//   warp 3       idle (completes warpgroup 0 for the register split).
+//   warps 4-19   four softmax warpgroups; warpgroup g owns slice g.
+//                Thread = query row (TMEM lane).  A thread loads the 64
+//                scores of a tile into registers at once (so the next S can
+//                be computed meanwhile), forms t = (S/sqrt(D) + bias + mask
+//                - m) log2 e in place and the tile maximum; on the first key
+//                tile, or when the maximum lies more than 8 (log2 units)
+//                above the base m, or when the row has nothing accumulated
+//                yet and the maximum lies more than 64 below m, it shifts t
+//                and m to the maximum (O rescaled in TMEM).  Then
+//                p = 2^t, the row sum, and P (BF16) into TMEM.  The epilogue
+//                writes O (BF16), the residual E = bf16(O32 - O) and
+//                lse = m + ln l.
 //
-// TMEM (512 columns): score buffers at [0,128), [128,256), [256,384); O_g at
-// 384 + g*D.  Step s = j*GF + g uses buffer s % 3.
+// TMEM (512 columns): slice g owns [128g, 128g + 128): scores at +0 (64),
+// P at +64 (32), O at +96 (D).
+#include <type_traits>
+
 #include "kernels.cuh"
 
 namespace triattn {
@@ -41,44 +45,49 @@ namespace triattn {
 namespace {
 
 constexpr int BM = 128;     // query rows per tile (TMEM lanes)
-constexpr int BN = 128;     // keys per tile
+constexpr int BN = 64;      // keys per step
 constexpr int GF = 4;       // outer slices per CTA (share a bias tile)
-constexpr int NSLOT = 4;    // K ring and V ring depth
-constexpr int NBIAS = 2;    // bias ring depth
-constexpr int kEW = 256;               // softmax threads (two warpgroups)
-constexpr int kThreads = 64 + kEW;
+constexpr int NSLOT = 2;    // K ring and V ring depth per slice
+constexpr int NBIAS = 3;    // bias ring depth
+constexpr int kSoftmax = 128 * GF;      // softmax threads (one warpgroup per slice)
+constexpr int kThreads = 128 + kSoftmax;
+constexpr int kRegsLaunch = 96;         // per thread at launch (__launch_bounds__(kThreads, 1))
+constexpr int kRegsCtl = 32;            // warpgroup 0: producer and MMA issuers
+constexpr int kRegsSoftmax = 112;     // softmax warpgroups
+static_assert(128 * kRegsCtl + kSoftmax * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;  // log2 units: P stays below 2^8
 constexpr float kLowThresh = -64.0f;    // log2 units: rebase an empty row whose maximum is this far below
-constexpr int kTO = 384;                // first O column in TMEM
+constexpr uint32_t kTP = 64;            // P columns within a slice's TMEM block
+constexpr uint32_t kTO = 96;            // O columns within a slice's TMEM block
 
 template <int D>
 struct FwdSmem {
-  static constexpr int kTile = BM * D * 2;           // one Q / K / V tile in bytes
-  static constexpr int kQ = 0;                       // GF Q tiles
-  static constexpr int kK = kQ + GF * kTile;         // NSLOT K tiles
-  static constexpr int kV = kK + NSLOT * kTile;      // NSLOT V tiles
-  static constexpr int kBias = kV + NSLOT * kTile;   // NBIAS x 32 KB (1024-aligned)
+  static constexpr int kTileQ = BM * D * 2;                  // one Q tile (128 rows x D bf16)
+  static constexpr int kTileKV = BN * D * 2;                 // one K / V tile (64 keys x D bf16)
+  static constexpr int kQ = 0;                               // GF Q tiles
+  static constexpr int kK = kQ + GF * kTileQ;                // GF x NSLOT K tiles
+  static constexpr int kV = kK + GF * NSLOT * kTileKV;       // GF x NSLOT V tiles
+  static constexpr int kBias = kV + GF * NSLOT * kTileKV;    // NBIAS x [128 q][64 k] bf16, SW128
   static constexpr int kBar = kBias + NBIAS * BM * BN * 2;
-  static constexpr int kMask = kBar + 256;           // GF x JK x 128 fp32 (key mask), then GF x JK x 16 flags
-  static constexpr int kFixed = kMask + 1024;        // + slack for 1024-byte alignment
+  static constexpr int kMask = kBar + 512;   // GF x (JK*64) fp32 key mask, GF x JK x 8 chunk flags, GF x JK tile flags
+  static constexpr int kFixed = kMask + 1024;                // + slack for 1024-byte alignment
   static_assert(kBias % 1024 == 0, "bias tiles need 1024-byte alignment");
-  // bytes for a problem with JK key tiles
-  static constexpr int bytes(int JK) { return kFixed + GF * JK * (BN * 4 + 16); }
-  static constexpr int kMaxJK = (232448 - kFixed) / (GF * (BN * 4 + 16));
+  static constexpr int bytes(int JK) { return kFixed + GF * JK * (BN * 4 + BN / 8 + 1); }
+  static constexpr int kMaxJK = (232448 - kFixed) / (GF * (BN * 4 + BN / 8 + 1));
 };
 
 struct FwdBars {
-  uint64_t q_full;
-  uint64_t k_full[NSLOT], k_empty[NSLOT];
-  uint64_t v_full[NSLOT], v_empty[NSLOT];
+  uint64_t k_full[GF][NSLOT], k_empty[GF][NSLOT];
+  uint64_t v_full[GF][NSLOT], v_empty[GF][NSLOT];
   uint64_t b_full[NBIAS], b_empty[NBIAS];
-  uint64_t s_full[3], p_full[3];
-  uint64_t all_done;
+  uint64_t s_full[GF], s_cons[GF], p_full[GF], pv_done[GF];
+  uint64_t q_full, all_done;
   uint32_t tmem_slot;
   int abort;
 };
+static_assert(sizeof(FwdBars) <= 512, "barrier block");
 
 }  // namespace
 
@@ -103,25 +112,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / H;
   const int h = bh - b * H;
   const int JK = (N + BN - 1) / BN;
-  const int nsteps = JK * GF;
 
   if (tid == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->k_empty[i], 1);
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->v_empty[i], 1);
+    for (int g = 0; g < GF; ++g) {
+      for (int i = 0; i < NSLOT; ++i) {
+        mbar_init(&bars->k_full[g][i], 1);
+        mbar_init(&bars->k_empty[g][i], 1);
+        mbar_init(&bars->v_full[g][i], 1);
+        mbar_init(&bars->v_empty[g][i], 1);
+      }
+      mbar_init(&bars->s_full[g], 1);
+      mbar_init(&bars->s_cons[g], 128);
+      mbar_init(&bars->p_full[g], 128);
+      mbar_init(&bars->pv_done[g], 1);
     }
     for (int i = 0; i < NBIAS; ++i) {
       mbar_init(&bars->b_full[i], 1);
-      mbar_init(&bars->b_empty[i], kEW);
+      mbar_init(&bars->b_empty[i], kSoftmax);
     }
-    for (int i = 0; i < 3; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], BM);
-    }
-    mbar_init(&bars->all_done, 1);
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->all_done, 2);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -131,6 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
+  if (warp < 4) regs_dec<kRegsCtl>();
+  else regs_inc<kRegsSoftmax>();
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -139,276 +152,302 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_bias);
       const int row0 = qtile * BM;
-      mbar_expect_tx(&bars->q_full, GF * L::kTile);
+      mbar_expect_tx(&bars->q_full, GF * L::kTileQ);
       for (int g = 0; g < GF; ++g)
-        tma_load_3d(sm + L::kQ + g * L::kTile, &tm_q, &bars->q_full, 0, row0, (b * N_o + o0 + g) * H + h);
+        tma_load_3d(sm + L::kQ + g * L::kTileQ, &tm_q, &bars->q_full, 0, row0, (b * N_o + o0 + g) * H + h);
       for (int j = 0; j < JK && !*abort; ++j) {
-        const int st = j % NBIAS;
-        if (!mbar_wait(&bars->b_empty[st], ((j / NBIAS) & 1) ^ 1, wc, abort)) break;
-        mbar_expect_tx(&bars->b_full[st], BM * BN * 2);
-        uint8_t* bdst = sm + L::kBias + st * (BM * BN * 2);
-        tma_load_3d(bdst, &tm_bias, &bars->b_full[st], j * BN, row0, bh);
-        tma_load_3d(bdst + BM * 128, &tm_bias, &bars->b_full[st], j * BN + 64, row0, bh);
-        for (int g = 0; g < GF; ++g) {
-          const int s = j * GF + g;
-          const int slot = s % NSLOT;
-          const uint32_t par = ((s / NSLOT) & 1) ^ 1;
+        const int bst = j % NBIAS;
+        if (!mbar_wait(&bars->b_empty[bst], ((j / NBIAS) & 1) ^ 1, wc, abort)) break;
+        mbar_expect_tx(&bars->b_full[bst], BM * BN * 2);
+        tma_load_3d(sm + L::kBias + bst * (BM * BN * 2), &tm_bias, &bars->b_full[bst], j * BN, row0, bh);
+        const int slot = j % NSLOT;
+        const uint32_t par = ((j / NSLOT) & 1) ^ 1;
+        bool go = true;
+        for (int g = 0; g < GF && go; ++g) {
           const int boh = (b * N_o + o0 + g) * H + h;
-          if (!mbar_wait(&bars->k_empty[slot], par, wc, abort)) break;
-          if (!(test_starve && s == 0)) {
-            mbar_expect_tx(&bars->k_full[slot], L::kTile);
-            tma_load_3d(sm + L::kK + slot * L::kTile, &tm_k, &bars->k_full[slot], 0, j * BN, boh);
+          if (!mbar_wait(&bars->k_empty[g][slot], par, wc, abort)) { go = false; break; }
+          if (!(test_starve && j == 0 && g == 0)) {
+            mbar_expect_tx(&bars->k_full[g][slot], L::kTileKV);
+            tma_load_3d(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], 0, j * BN, boh);
           }
-          if (!mbar_wait(&bars->v_empty[slot], par, wc, abort)) break;
-          mbar_expect_tx(&bars->v_full[slot], L::kTile);
-          tma_load_3d(sm + L::kV + slot * L::kTile, &tm_v, &bars->v_full[slot], 0, j * BN, boh);
+          if (!mbar_wait(&bars->v_empty[g][slot], par, wc, abort)) { go = false; break; }
+          mbar_expect_tx(&bars->v_full[g][slot], L::kTileKV);
+          tma_load_3d(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], 0, j * BN, boh);
         }
+        if (!go) break;
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;       // 64B / 32B swizzle
+  } else if (warp <= 2) {
+    // ------------------------------------------------------------ MMA issuers (slices 2(warp-1), 2(warp-1)+1)
+    constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;       // 64B / 32B swizzle of D-wide rows
     constexpr uint32_t kSbo = 8u * D * 2u;               // 8 rows of D bf16
-    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
-    constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
-    constexpr uint32_t kTile16 = L::kTile >> 4;          // tile size in descriptor units
+    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);   // S = Q K^T: A (Q), B (K) K-major
+    constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);   // O += P V: A (P) in TMEM, B (V) MN-major
+    constexpr uint32_t kTileQ16 = L::kTileQ >> 4;
+    constexpr uint32_t kTile16 = L::kTileKV >> 4;
     constexpr uint32_t kRowStep = (16 * D * 2) >> 4;     // 16 rows of a D-wide tile
-    // base descriptors; per-MMA offsets are added to the start-address field
     const uint64_t dQb = smem_desc(smem_u32(sm + L::kQ), 16, kSbo, kSwz);
     const uint64_t dKb = smem_desc(smem_u32(sm + L::kK), 16, kSbo, kSwz);
     const uint64_t dVb = smem_desc(smem_u32(sm + L::kV), 16, kSbo, kSwz);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wc, abort));
-    auto issue_s = [&](int s) -> bool {
-      const int g = s % GF, slot = s % NSLOT;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[slot], (s / NSLOT) & 1, wc, abort))) return false;
-      tc_fence_after();
+    const int g0 = 2 * (warp - 1);
+    auto issue_s = [&](int g, int slot) {  // S_g = Q_g K^T into the slice's score columns
       if (elect_one()) {
-        const uint32_t dS = tmem + (s % 3) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(dS, dQb + g * kTile16 + 2 * kk, dKb + slot * kTile16 + 2 * kk, idS, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->s_full[s % 3]);
-        mma_commit(&bars->k_empty[slot]);
+          mma_ss(tmem + 128 * g, dQb + g * kTileQ16 + 2 * kk, dKb + (g * NSLOT + slot) * kTile16 + 2 * kk, idS,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&bars->s_full[g]);
+        mma_commit(&bars->k_empty[g][slot]);
       }
       __syncwarp();
-      return true;
     };
-    for (int s = 0; s < 3 && s < nsteps && ok; ++s) ok = issue_s(s);
-    for (int s = 0; s < nsteps && ok; ++s) {
-      const int g = s % GF, j = s / GF, slot = s % NSLOT, buf = s % 3;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[buf], (s / 3) & 1, wc, abort))) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[slot], (s / NSLOT) & 1, wc, abort))) { ok = false; break; }
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wc, abort));
+    for (int g = g0; g < g0 + 2 && ok; ++g) {  // S_g(0)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[g][0], 0, wc, abort))) { ok = false; break; }
       tc_fence_after();
-      if (elect_one()) {
-        const uint32_t dO = tmem + kTO + g * D;
-        const uint32_t aP = tmem + buf * BN;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(dO, aP + kk * 8, dVb + slot * kTile16 + kk * kRowStep, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->v_empty[slot]);
+      issue_s(g, 0);
+    }
+    for (int j = 0; j < JK && ok; ++j) {
+      const int slot = j % NSLOT, slot1 = (j + 1) % NSLOT;
+      if (j + 1 < JK) {
+        for (int g = g0; g < g0 + 2; ++g) {
+          // S(j) of slice g is in registers; K(j+1) loaded
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_cons[g], j & 1, wc, abort)) ||
+              !__all_sync(0xffffffffu, mbar_wait(&bars->k_full[g][slot1], ((j + 1) / NSLOT) & 1, wc, abort))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(g, slot1);
+        }
+        if (!ok) break;
       }
-      __syncwarp();
-      if (s + 3 < nsteps) ok = issue_s(s + 3);
+      for (int g = g0; g < g0 + 2; ++g) {
+        // P(j) of slice g in TMEM; V(j) loaded
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[g], j & 1, wc, abort)) ||
+            !__all_sync(0xffffffffu, mbar_wait(&bars->v_full[g][slot], (j / NSLOT) & 1, wc, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + 128 * g + kTO, tmem + 128 * g + kTP + 8 * kk, dVb + (g * NSLOT + slot) * kTile16 + kk * kRowStep,
+                   idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->pv_done[g]);
+          mma_commit(&bars->v_empty[g][slot]);
+        }
+        __syncwarp();
+      }
     }
     if (elect_one()) mma_commit(&bars->all_done);
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax warpgroups
-    const int ew = tid - 64;              // 0..255
-    const int wg = (warp - 2) >> 2;       // warpgroup: slices g with g % 2 == wg
+    const int ew = tid - 128;             // 0..511
+    const int g = (warp - 4) >> 2;        // slice of this warpgroup
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;    // query row within the tile (= TMEM lane)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
-    float* mask2 = reinterpret_cast<float*>(sm + L::kMask);
-    uint8_t* mflag = sm + L::kMask + nsteps * BN * 4;
+    const int nkeys = JK * BN;
+    float* mask2 = reinterpret_cast<float*>(sm + L::kMask);       // [GF][nkeys], natural units, -inf past N
+    uint8_t* mflag = sm + L::kMask + GF * nkeys * 4;              // [GF][JK*8]: 8-key chunk has a nonzero value
+    uint8_t* tflag = mflag + GF * JK * (BN / 8);                  // [GF][JK]: tile has a nonzero value
 
-    // Key mask of every (key tile, slice) step (natural-log units, -inf past
-    // N) and per 8-key chunk a flag "some mask value is nonzero": staged once,
-    // before any bounded wait, so the two barriers are always fully entered.
-    for (int idx = ew; idx < nsteps * BN; idx += kEW) {
-      const int s = idx / BN, key = (s / GF) * BN + (idx % BN), g = s % GF;
+    // Key mask of the four slices and its chunk / tile flags, staged once,
+    // before any bounded wait, so the barriers are always fully entered.
+    for (int idx = ew; idx < GF * nkeys; idx += kSoftmax) {
+      const int gg = idx / nkeys, key = idx - gg * nkeys;
       float mv = -INFINITY;
       if (key < N) {
         mv = 0.f;
         if (mask != nullptr)
-          mv = __uint_as_float(static_cast<uint32_t>(__ldg(mask + (static_cast<size_t>(b) * N_o + o0 + g) * N + key))
+          mv = __uint_as_float(static_cast<uint32_t>(__ldg(mask + (static_cast<size_t>(b) * N_o + o0 + gg) * N + key))
                                << 16);
       }
       mask2[idx] = mv;
     }
-    named_bar_sync(1, kEW);
-    for (int idx = ew; idx < nsteps * 16; idx += kEW) {
+    named_bar_sync(1, kSoftmax);
+    for (int idx = ew; idx < GF * JK * (BN / 8); idx += kSoftmax) {
       bool any = false;
 #pragma unroll
       for (int e = 0; e < 8; ++e) any |= (mask2[idx * 8 + e] != 0.f);
       mflag[idx] = any ? 1 : 0;
     }
-    named_bar_sync(1, kEW);
+    named_bar_sync(1, kSoftmax);
+    for (int idx = ew; idx < GF * JK; idx += kSoftmax) {
+      bool any = false;
+      for (int e = 0; e < BN / 8; ++e) any |= (mflag[idx * (BN / 8) + e] != 0);
+      tflag[idx] = any ? 1 : 0;
+    }
+    named_bar_sync(1, kSoftmax);
 
-    // running base m (natural units) and sum l for this warpgroup's two slices
-    float m_run[2] = {0.f, 0.f}, l_run[2] = {0.f, 0.f};
+    const int q = qtile * BM + r;
+    const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + q;
+
+    // running base m (natural units) and sum l of this row
+    float m_run = 0.f, l_run = 0.f;
     const float2 c2 = make_float2(inv_sqrt_d * kLog2e, inv_sqrt_d * kLog2e);
     const float2 l2e2 = make_float2(kLog2e, kLog2e);
+    const uint32_t tS = tmem + lane_addr + 128 * g;
     bool ok = true;
 
     for (int j = 0; j < JK && ok; ++j) {
-      const int st = j % NBIAS;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->b_full[st], (j / NBIAS) & 1, wc, abort))) { ok = false; break; }
-      const uint8_t* bias_s = sm + L::kBias + st * (BM * BN * 2);
-#pragma unroll 1
-      for (int sl = 0; sl < 2; ++sl) {
-        const int g = wg + 2 * sl;
-        const int s = j * GF + g;
-        const int buf = s % 3;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], (s / 3) & 1, wc, abort))) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t tS = tmem + lane_addr + buf * BN;
-        const float* mk = mask2 + s * BN;
-        const uint8_t* fl = mflag + s * 16;
-
-        // t = (S / sqrt(D) + bias + mask - base) log2 e; returns max t and,
-        // with_exp, p = 2^t packed to BF16 in pw and sum p.  16-key chunks,
-        // the TMEM load of chunk c+1 in flight while chunk c is computed.
-        uint32_t pw[2][32];
-        auto score_pass = [&](float base, bool with_exp, float& tmax, float& lsum) {
-          const float2 nb2 = make_float2(-base * kLog2e, -base * kLog2e);
-          float2 ls = make_float2(0.f, 0.f);
-          float tm = -INFINITY;
-          uint32_t sb[2][16];
-          tmem_ld16(tS, sb[0]);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t(&raw)[16] = sb[c & 1];
-            tc_wait_ld_regs(raw);
-            if (c + 1 < 8) tmem_ld16(tS + (c + 1) * 16, sb[(c + 1) & 1]);
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              const int cc = c * 2 + v;  // 8-key chunk (0..15)
-              const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + (cc >> 3) * (BM * 128) + sw128(r, cc & 7));
-              const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
-              const bool masked = fl[cc] != 0;
-              float4 m0 = make_float4(0.f, 0.f, 0.f, 0.f), m1 = m0;
-              if (masked) {
-                m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
-                m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
-              }
-              const float2 mm[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
-                                    make_float2(m1.z, m1.w)};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int k = v * 8 + 2 * e;
-                const float2 s2 = make_float2(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]));
-                const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
-                float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nb2));
-                if (masked) t = ffma2(mm[e], l2e2, t);
-                tm = fmax3(tm, t.x, t.y);
-                if (with_exp) {
-                  const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-                  ls = fadd2(ls, p);
-                  pw[c >> 2][(c & 3) * 8 + v * 4 + e] = pack_bf16x2(p.x, p.y);
-                }
-              }
-            }
-          }
-          tmax = tm;
-          lsum = ls.x + ls.y;
-        };
-
-        float tmax, lsum;
-        if (j == 0) {
-          // first key tile: the base is the tile's row maximum
-          score_pass(0.f, false, tmax, lsum);
-          m_run[sl] = tmax == -INFINITY ? 0.f : tmax * kLn2;
-        }
-        score_pass(m_run[sl], true, tmax, lsum);
-        // later tiles keep the base unless the tile maximum overshoots it (P
-        // would grow past 2^8), or nothing is accumulated yet and the maximum
-        // lies far below it; then the warp redoes the pass with a new base
-        const bool up = tmax > kRescaleThresh;
-        const bool down = l_run[sl] == 0.f && tmax < kLowThresh && tmax != -INFINITY;
-        const bool need = up || down;
-        float alpha = 1.f;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_old = m_run[sl];
-          if (need) m_run[sl] = m_old + tmax * kLn2;
-          float t2;
-          score_pass(m_run[sl], true, t2, lsum);
-          if (need && l_run[sl] > 0.f) alpha = ex2_approx((m_old - m_run[sl]) * kLog2e);
-        }
-        if (sl == 1) mbar_arrive(&bars->b_empty[st]);  // this warpgroup's last read of the bias tile
-        l_run[sl] = l_run[sl] * alpha + lsum;
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          // O_g's previous P.V (step s - 4) was issued before S(s - 1); the
-          // S of this step was issued after it, so s_full implies it finished.
-          const uint32_t tO = tmem + lane_addr + kTO + g * D;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t ov[16];
-            tmem_ld16(tO + c0, ov);
-            tc_wait_ld_regs(ov);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st16(tO + c0, ov);
-          }
-        }
-        // P of keys [32c, 32c+32) into columns [16c, 16c+16): S is no longer read
-        tmem_st32(tS, pw[0]);
-        tmem_st32(tS + 32, pw[1]);
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[buf]);
+      const int bst = j % NBIAS;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->b_full[bst], (j / NBIAS) & 1, wc, abort)) ||
+          !__all_sync(0xffffffffu, mbar_wait(&bars->s_full[g], j & 1, wc, abort))) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
+      // the tile's 64 scores into registers; the score columns are free again
+      // sv0 holds keys [0, 32), sv1 keys [32, 64)
+      uint32_t sv0[32], sv1[32];
+      tmem_ld32(tS, sv0);
+      tmem_ld32(tS + 32, sv1);
+      tc_wait_ld_regs(sv0);
+      tc_wait_ld_regs(sv1);
+      tc_fence_before();
+      mbar_arrive(&bars->s_cons[g]);
+
+      // t = (S / sqrt(D) + bias + mask - m) log2 e in place, and its maximum
+      const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
+      const float* mk = mask2 + g * nkeys + j * BN;
+      const bool tile_masked = tflag[g * JK + j] != 0;
+      const float2 nb2 = make_float2(-m_run * kLog2e, -m_run * kLog2e);
+      float tm = -INFINITY;
+      // MASKED selects, per key tile (warp-uniform), the version of the loop
+      // that adds the key mask; tiles without a nonzero mask value skip it
+      auto scores = [&](uint32_t (&sv)[32], const int cc0, auto masked_tile) {
+        constexpr bool MASKED = decltype(masked_tile)::value;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // 8-key chunks
+          const int cc = cc0 + c;
+          const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + sw128(r, cc));
+          const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
+          float2 mm[4];
+          if constexpr (MASKED) {
+            const float4 m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
+            const float4 m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
+            mm[0] = make_float2(m0.x, m0.y);
+            mm[1] = make_float2(m0.z, m0.w);
+            mm[2] = make_float2(m1.x, m1.y);
+            mm[3] = make_float2(m1.z, m1.w);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = c * 8 + 2 * e;
+            const float2 s2 = make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
+            const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
+            float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nb2));
+            if constexpr (MASKED) t = ffma2(mm[e], l2e2, t);
+            tm = fmax3(tm, t.x, t.y);
+            sv[k] = __float_as_uint(t.x);
+            sv[k + 1] = __float_as_uint(t.y);
+          }
+        }
+      };
+      if (tile_masked) {
+        scores(sv0, 0, std::true_type{});
+        scores(sv1, 4, std::true_type{});
+      } else {
+        scores(sv0, 0, std::false_type{});
+        scores(sv1, 4, std::false_type{});
+      }
+      mbar_arrive(&bars->b_empty[bst]);  // this thread's last read of the bias tile
+
+      // new base at the tile maximum: on the first tile, when the maximum
+      // overshoots the base (P would grow past 2^8), or when nothing is
+      // accumulated yet and it lies far below the base
+      float sh = 0.f;
+      if (tm != -INFINITY && (j == 0 || tm > kRescaleThresh || (l_run == 0.f && tm < kLowThresh))) sh = tm;
+      const float2 sh2 = make_float2(-sh, -sh);  // applied in the exponent below (t - 0 is exact)
+      float alpha = 1.f;
+      m_run += sh * kLn2;
+      if (l_run > 0.f && sh != 0.f) alpha = ex2_approx(-sh);
+
+      // P.V(j-1) is complete: the P columns are free and O is up to date
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], (j - 1) & 1, wc, abort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint32_t tO = tS + kTO;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t ov[16];
+          tmem_ld16(tO + c0, ov);
+          tc_wait_ld_regs(ov);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st16(tO + c0, ov);
+        }
+      }
+
+      // p = 2^(t - shift), the row sum, and P (BF16) into the P columns
+      uint32_t pw[BN / 2];
+      float2 ls = make_float2(0.f, 0.f);
+      auto expo = [&](const uint32_t (&sv)[32], const int w0) {
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float2 t = fadd2(make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), sh2);
+          const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+          ls = fadd2(ls, p);
+          pw[w0 + k / 2] = pack_bf16x2(p.x, p.y);
+        }
+      };
+      expo(sv0, 0);
+      expo(sv1, 16);
+      l_run = l_run * alpha + (ls.x + ls.y);
+      tmem_st32(tS + kTP, pw);
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[g]);
     }
 
     // ------------------------------------------------------------ epilogue
     if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->all_done, 0, wc, abort))) {
       tc_fence_after();
-      const int q = qtile * BM + r;
+      float ov[D];
+      {
+        const uint32_t tO = tmem + lane_addr + 128 * g + kTO;
+        if constexpr (D == 32) {
+          uint32_t raw[32];
+          tmem_ld32(tO, raw);
+          tc_wait_ld();
 #pragma unroll
-      for (int sl = 0; sl < 2; ++sl) {
-        const int g = wg + 2 * sl;
-        float ov[D];
-        {
-          const uint32_t tO = tmem + lane_addr + kTO + g * D;
-          if constexpr (D == 32) {
-            uint32_t raw[32];
-            tmem_ld32(tO, raw);
-            tc_wait_ld();
+          for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(raw[e]);
+        } else {
+          uint32_t raw[16];
+          tmem_ld16(tO, raw);
+          tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(raw[e]);
-          } else {
-            uint32_t raw[16];
-            tmem_ld16(tO, raw);
-            tc_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ov[e] = __uint_as_float(raw[e]);
-          }
+          for (int e = 0; e < 16; ++e) ov[e] = __uint_as_float(raw[e]);
         }
-        if (q < N) {
-          const float l = l_run[sl];
-          const float inv = l > 0.f ? 1.0f / l : 0.f;
-          const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + q;
-          uint32_t ob[D / 2], eb[D / 2];
+      }
+      if (q < N) {
+        const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+        uint32_t ob[D / 2], eb[D / 2];
 #pragma unroll
-          for (int e = 0; e < D / 2; ++e) {
-            const float y0 = ov[2 * e] * inv, y1 = ov[2 * e + 1] * inv;
-            const uint32_t w = pack_bf16x2(y0, y1);
-            ob[e] = w;
-            eb[e] = pack_bf16x2(y0 - bf16lo_to_f32(w), y1 - bf16hi_to_f32(w));
-          }
-          uint4* op = reinterpret_cast<uint4*>(out_o + row * D);
+        for (int e = 0; e < D / 2; ++e) {
+          const float y0 = ov[2 * e] * inv, y1 = ov[2 * e + 1] * inv;
+          const uint32_t w = pack_bf16x2(y0, y1);
+          ob[e] = w;
+          eb[e] = pack_bf16x2(y0 - bf16lo_to_f32(w), y1 - bf16hi_to_f32(w));
+        }
+        uint4* op = reinterpret_cast<uint4*>(out_o + row * D);
+#pragma unroll
+        for (int v4 = 0; v4 < D / 8; ++v4) op[v4] = make_uint4(ob[4 * v4], ob[4 * v4 + 1], ob[4 * v4 + 2], ob[4 * v4 + 3]);
+        if (out_resid != nullptr) {
+          uint4* ep = reinterpret_cast<uint4*>(out_resid + row * D);
 #pragma unroll
           for (int v4 = 0; v4 < D / 8; ++v4)
-            op[v4] = make_uint4(ob[4 * v4], ob[4 * v4 + 1], ob[4 * v4 + 2], ob[4 * v4 + 3]);
-          if (out_resid != nullptr) {
-            uint4* ep = reinterpret_cast<uint4*>(out_resid + row * D);
-#pragma unroll
-            for (int v4 = 0; v4 < D / 8; ++v4)
-              ep[v4] = make_uint4(eb[4 * v4], eb[4 * v4 + 1], eb[4 * v4 + 2], eb[4 * v4 + 3]);
-          }
-          out_lse[row] = l > 0.f ? m_run[sl] + __logf(l) : -INFINITY;
+            ep[v4] = make_uint4(eb[4 * v4], eb[4 * v4 + 1], eb[4 * v4 + 2], eb[4 * v4 + 3]);
         }
+        out_lse[row] = l_run > 0.f ? m_run + __logf(l_run) : -INFINITY;
       }
     }
   }
@@ -431,13 +470,20 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
   if (JK > FwdSmem<D>::kMaxJK) return cudaErrorInvalidValue;
   fwd_kernel<D><<<grid, kThreads, FwdSmem<D>::bytes(JK), stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_bias, static_cast<const uint16_t*>(a.mask), static_cast<uint16_t*>(a.o), a.lse,
-      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.test_starve, a.wc);
+      a.tm_q, a.tm_k, a.tm_v, a.tm_bias, static_cast<const uint16_t*>(a.mask),
+      static_cast<uint16_t*>(a.o), a.lse, static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.test_starve, a.wc);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t setup_fwd() {
+  // setmaxnreg.inc waits until the registers it asks for are free in the
+  // block's launch allocation: refuse to run a build whose launch register
+  // count could not cover the split.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
   return cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
 }
 

@@ -18,7 +18,7 @@ constexpr int kGroupFwd = 4;
 constexpr int kGroupBwd = 4;
 
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_bias;
+  CUtensorMap tm_q, tm_k, tm_v, tm_bias;  // Q: 128-row boxes; K, V: 64-row boxes
   const void* mask;
   void* o;
   float* lse;

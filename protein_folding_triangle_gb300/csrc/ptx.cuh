@@ -50,21 +50,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// while the phase is incomplete, so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Bounded wait for the phase with the given parity.  `abort` is a CTA-shared
 // flag: once any thread of the CTA has given up, the others stop waiting.
 static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
                                        volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > wc.limit_ns) {
-        atomicOr(wc.status, kDevTimeout);
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > wc.limit_ns) {
+      atomicOr(wc.status, kDevTimeout);
+      *abort = 1;
+      return false;
     }
   }
 }
@@ -167,6 +178,17 @@ __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
   asm volatile("{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}\n" : "=r"(pred));
   return pred != 0;
+}
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same instruction; the new count is a multiple of 8 in [24, 256]).
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Warp-collective TMEM allocation of `ncols` columns; address written to *slot.

@@ -59,6 +59,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;  // log2 units: P stays below 2^8
 constexpr float kLowThresh = -64.0f;    // log2 units: rebase an empty row whose maximum is this far below
+constexpr float kSumThresh = 65536.0f;  // a later tile whose row sum exceeds this (some p > 2^16) is rebased
 constexpr uint32_t kTP = 64;            // P columns within a slice's TMEM block
 constexpr uint32_t kTO = 96;            // O columns within a slice's TMEM block
 
@@ -312,16 +313,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->s_cons[g]);
 
-      // t = (S / sqrt(D) + bias + mask - m) log2 e in place, and its maximum
+      // P.V(j-1) is complete: the P columns are free and O is up to date
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], (j - 1) & 1, wc, abort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+
+      // t = (S / sqrt(D) + bias + mask - m) log2 e in place.  The exact
+      // path (first key tile, or a row of the warp with nothing accumulated
+      // yet) also takes the tile maximum and moves the base to it; later
+      // tiles keep the base and only look at the maximum when the row sum
+      // of the tile exceeds 2^16 (some p > 2^16).
       const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
       const float* mk = mask2 + g * nkeys + j * BN;
       const bool tile_masked = tflag[g * JK + j] != 0;
+      const bool exact = j == 0 || __any_sync(0xffffffffu, l_run == 0.f);
       const float2 nb2 = make_float2(-m_run * kLog2e, -m_run * kLog2e);
       float tm = -INFINITY;
       // MASKED selects, per key tile (warp-uniform), the version of the loop
-      // that adds the key mask; tiles without a nonzero mask value skip it
-      auto scores = [&](uint32_t (&sv)[32], const int cc0, auto masked_tile) {
+      // that adds the key mask; WITH_MAX also takes the maximum of t
+      auto scores = [&](uint32_t (&sv)[32], const int cc0, auto masked_tile, auto with_max) {
         constexpr bool MASKED = decltype(masked_tile)::value;
+        constexpr bool WITH_MAX = decltype(with_max)::value;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // 8-key chunks
           const int cc = cc0 + c;
@@ -343,66 +357,103 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
             float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nb2));
             if constexpr (MASKED) t = ffma2(mm[e], l2e2, t);
-            tm = fmax3(tm, t.x, t.y);
+            if constexpr (WITH_MAX) tm = fmax3(tm, t.x, t.y);
             sv[k] = __float_as_uint(t.x);
             sv[k + 1] = __float_as_uint(t.y);
           }
         }
       };
-      if (tile_masked) {
-        scores(sv0, 0, std::true_type{});
-        scores(sv1, 4, std::true_type{});
-      } else {
-        scores(sv0, 0, std::false_type{});
-        scores(sv1, 4, std::false_type{});
-      }
-      mbar_arrive(&bars->b_empty[bst]);  // this thread's last read of the bias tile
-
-      // new base at the tile maximum: on the first tile, when the maximum
-      // overshoots the base (P would grow past 2^8), or when nothing is
-      // accumulated yet and it lies far below the base
-      float sh = 0.f;
-      if (tm != -INFINITY && (j == 0 || tm > kRescaleThresh || (l_run == 0.f && tm < kLowThresh))) sh = tm;
-      const float2 sh2 = make_float2(-sh, -sh);  // applied in the exponent below (t - 0 is exact)
-      float alpha = 1.f;
-      m_run += sh * kLn2;
-      if (l_run > 0.f && sh != 0.f) alpha = ex2_approx(-sh);
-
-      // P.V(j-1) is complete: the P columns are free and O is up to date
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], (j - 1) & 1, wc, abort))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        const uint32_t tO = tS + kTO;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t ov[16];
-          tmem_ld16(tO + c0, ov);
-          tc_wait_ld_regs(ov);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st16(tO + c0, ov);
-        }
-      }
-
-      // p = 2^(t - shift), the row sum, and P (BF16) into the P columns
-      uint32_t pw[BN / 2];
-      float2 ls = make_float2(0.f, 0.f);
-      auto expo = [&](const uint32_t (&sv)[32], const int w0) {
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float2 t = fadd2(make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), sh2);
-          const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-          ls = fadd2(ls, p);
-          pw[w0 + k / 2] = pack_bf16x2(p.x, p.y);
+      auto pass1 = [&](auto with_max) {
+        if (tile_masked) {
+          scores(sv0, 0, std::true_type{}, with_max);
+          scores(sv1, 4, std::true_type{}, with_max);
+        } else {
+          scores(sv0, 0, std::false_type{}, with_max);
+          scores(sv1, 4, std::false_type{}, with_max);
         }
       };
-      expo(sv0, 0);
-      expo(sv1, 16);
-      l_run = l_run * alpha + (ls.x + ls.y);
-      tmem_st32(tS + kTP, pw);
+      if (exact) pass1(std::true_type{});
+      else pass1(std::false_type{});
+      mbar_arrive(&bars->b_empty[bst]);  // this thread's last read of the bias tile
+
+
+      // p = 2^(t - sh), the row sum, and P (BF16) into the P columns, 32
+      // keys at a time; returns the row sum
+      auto expo = [&](const float sh, auto shifted) -> float {
+        constexpr bool SHIFT = decltype(shifted)::value;
+        const float2 sh2 = make_float2(-sh, -sh);
+        float2 ls = make_float2(0.f, 0.f);
+        {
+          uint32_t pw[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            float2 t = make_float2(__uint_as_float(sv0[k]), __uint_as_float(sv0[k + 1]));
+            if constexpr (SHIFT) t = fadd2(t, sh2);
+            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            ls = fadd2(ls, p);
+            pw[k / 2] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st16(tS + kTP, pw);
+        }
+        {
+          uint32_t pw[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            float2 t = make_float2(__uint_as_float(sv1[k]), __uint_as_float(sv1[k + 1]));
+            if constexpr (SHIFT) t = fadd2(t, sh2);
+            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            ls = fadd2(ls, p);
+            pw[k / 2] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st16(tS + kTP + 16, pw);
+        }
+        return ls.x + ls.y;
+      };
+      // Rebase this row to sh (the maximum of its t values, or 0): m moves
+      // by sh, O and l are scaled by 2^-sh when something is accumulated.
+      // Returns the scale.
+      auto rebase = [&](const float sh) -> float {
+        const float a = (l_run > 0.f && sh != 0.f) ? ex2_approx(-sh) : 1.f;
+        m_run += sh * kLn2;
+        if (__any_sync(0xffffffffu, a != 1.f)) {
+          const uint32_t tO = tS + kTO;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t ov[16];
+            tmem_ld16(tO + c0, ov);
+            tc_wait_ld_regs(ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * a);
+            tmem_st16(tO + c0, ov);
+          }
+        }
+        return a;
+      };
+      float alpha = 1.f, lsum;
+      if (exact) {
+        // new base at the tile maximum: on the first tile, when the maximum
+        // overshoots the base (P would grow past 2^8), or when nothing is
+        // accumulated yet and it lies far below the base
+        const float sh =
+            (tm != -INFINITY && (j == 0 || tm > kRescaleThresh || (l_run == 0.f && tm < kLowThresh))) ? tm : 0.f;
+        alpha = rebase(sh);
+        lsum = expo(sh, std::true_type{});
+      } else {
+        lsum = expo(0.f, std::false_type{});
+        const bool need = !(lsum <= kSumThresh);
+        if (__any_sync(0xffffffffu, need)) {
+          // rare: rebase the rows whose sum overflowed to their tile maximum
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) mx = fmax3(mx, __uint_as_float(sv0[k]), __uint_as_float(sv0[k + 1]));
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) mx = fmax3(mx, __uint_as_float(sv1[k]), __uint_as_float(sv1[k + 1]));
+          const float sh = need ? mx : 0.f;
+          alpha = rebase(sh);
+          lsum = expo(sh, std::true_type{});
+        }
+      }
+      l_run = l_run * alpha + lsum;
       tc_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[g]);

@@ -91,10 +91,11 @@ triattn_status tri_attn_fwd(const triattn_shape* shape,
 
 /*
  * Workspace bytes tri_attn_bwd needs for `shape` (0 on an invalid shape).
- * The workspace holds the FP32 row corrections delta, the single-writer FP32
- * dQ partials (one per key tile) and the single-writer FP32 dbias partials
- * (one per outer group of slices) ("TurboPairFormer", Figure 2(b), Figure 7,
- * Table 11).
+ * The workspace holds, per (slice, 128-row query tile), a record of the FP32
+ * values -lse*log2(e) and -delta; a transposed copy of the bias; the
+ * single-writer FP32 dQ partials (one per key tile) and the single-writer
+ * FP32 dbias partials (one per outer group of slices) ("TurboPairFormer",
+ * Figure 2(b), Figure 7, Table 11).
  */
 size_t triattn_bwd_workspace_bytes(const triattn_shape* shape);
 
@@ -102,13 +103,16 @@ size_t triattn_bwd_workspace_bytes(const triattn_shape* shape);
  * Backward.  "TurboPairFormer", Abstract, Figure 2, Figure 7(b)-(d),
  * Figure 11(a) and Table 11 (key-tile-parallel partition):
  *   1. preprocess: delta[q] = sum_d dO[q,d] * (o[q,d] + o_resid[q,d]) in FP32
- *      (o_resid NULL: compensation off, delta = sum_d dO*o);
- *   2. main: one CTA per (b, h, key tile, outer group of slices) recomputes
+ *      (o_resid NULL: compensation off, delta = sum_d dO*o), stored with
+ *      -lse[q]*log2(e) per (slice, query tile);
+ *   2. a small kernel writes the bias transposed (key-major) into the
+ *      workspace;
+ *   3. main: one CTA per (b, h, key tile, outer group of slices) recomputes
  *      S, P, dP and dS once per query tile, keeps dK and dV on chip and
  *      writes one FP32 dQ partial per key tile and one FP32 dbias partial per
  *      outer group, each with a single writer;
- *   3. a reduction kernel adds the dQ partials in ascending key-tile order;
- *   4. a reduction kernel adds the dbias partials in ascending group order.
+ *   4. a reduction kernel adds the dQ partials in ascending key-tile order;
+ *   5. a reduction kernel adds the dbias partials in ascending group order.
  *
  *   q,k,v,bias,mask  the forward's inputs (mask may be NULL).
  *   o, lse           the forward's outputs; o_resid optional (see above).
@@ -118,7 +122,7 @@ size_t triattn_bwd_workspace_bytes(const triattn_shape* shape);
  *   workspace        device scratch of at least
  *                    triattn_bwd_workspace_bytes(shape) bytes, 256-byte
  *                    aligned; contents on entry are ignored.
- * Launches four kernels in stream order.
+ * Launches five kernels in stream order.
  */
 triattn_status tri_attn_bwd(const triattn_shape* shape,
                             const void* q, const void* k, const void* v,
@@ -136,15 +140,16 @@ triattn_status tri_attn_bwd(const triattn_shape* shape,
  * Some callers cannot allocate device memory: a plugin inside a host
  * framework that owns all device memory and does not let extensions call
  * cudaMalloc, or a latency-critical loop that cannot pay for cudaMalloc's
- * implicit device synchronisation.  This entry point runs the same four
+ * implicit device synchronisation.  This entry point runs the same five
  * backward kernels as tri_attn_bwd but takes no workspace: its scratch
- * (delta and the FP32 partials) lives in a file-scope device array of
+ * (the row records, the transposed bias and the FP32 partials) lives in a
+ * file-scope device array of
  * TRIATTN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, which every GPU
  * that loads the library holds until the process exits.
  *   - A shape whose triattn_bwd_workspace_bytes() exceeds
  *     TRIATTN_NOALLOC_SCRATCH_BYTES is rejected with TRIATTN_ERR_WORKSPACE
- *     before anything is launched (B=1, N=48, H=2, D=16 needs 0.5 MiB;
- *     a 384-token crop with H=4, D=32 needs 455 MiB and is rejected).
+ *     before anything is launched (B=1, N=48, H=2, D=16 needs 2.4 MiB;
+ *     a 384-token crop with H=4, D=32 needs 438 MiB and is rejected).
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress while that device is current.  Make that first
  *     call before any stream capture.

@@ -17,8 +17,8 @@
 //                bias tile and, per slice, one K and one V tile (rings of
 //                3 / 2 / 2 stages).
 //   warps 1, 2   tcgen05 MMA issuers (converged warps, one elected lane
-//                issues, descriptors precomputed), for slices {0,1} and
-//                {2,3}: S(j+1) = Q K^T as soon as the warpgroup has loaded
+//                issues, descriptors precomputed), for slices {0,2} and
+//                {1,3}: S(j+1) = Q K^T as soon as the warpgroup has loaded
 //                S(j) into registers, O += P V(j) once it has written P(j).
 //   warp 3       idle (completes warpgroup 0 for the register split).
 //   warps 4-19   four softmax warpgroups; warpgroup g owns slice g.
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dQb = smem_desc(smem_u32(sm + L::kQ), 16, kSbo, kSwz);
     const uint64_t dKb = smem_desc(smem_u32(sm + L::kK), 16, kSbo, kSwz);
     const uint64_t dVb = smem_desc(smem_u32(sm + L::kV), 16, kSbo, kSwz);
-    const int g0 = 2 * (warp - 1);
+    const int g0 = warp - 1;  // slices g0 and g0 + 2 (one warpgroup pair)
     auto issue_s = [&](int g, int slot) {  // S_g = Q_g K^T into the slice's score columns
       if (elect_one()) {
 #pragma unroll
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wc, abort));
-    for (int g = g0; g < g0 + 2 && ok; ++g) {  // S_g(0)
+    for (int g = g0; g < GF && ok; g += 2) {  // S_g(0)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[g][0], 0, wc, abort))) { ok = false; break; }
       tc_fence_after();
       issue_s(g, 0);
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < JK && ok; ++j) {
       const int slot = j % NSLOT, slot1 = (j + 1) % NSLOT;
       if (j + 1 < JK) {
-        for (int g = g0; g < g0 + 2; ++g) {
+        for (int g = g0; g < GF; g += 2) {
           // S(j) of slice g is in registers; K(j+1) loaded
           if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_cons[g], j & 1, wc, abort)) ||
               !__all_sync(0xffffffffu, mbar_wait(&bars->k_full[g][slot1], ((j + 1) / NSLOT) & 1, wc, abort))) {
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
-      for (int g = g0; g < g0 + 2; ++g) {
+      for (int g = g0; g < GF; g += 2) {
         // P(j) of slice g in TMEM; V(j) loaded
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[g], j & 1, wc, abort)) ||
             !__all_sync(0xffffffffu, mbar_wait(&bars->v_full[g][slot], (j / NSLOT) & 1, wc, abort))) {

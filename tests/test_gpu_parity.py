@@ -159,3 +159,16 @@ def test_large_logit_shifts_across_key_tiles():
     out = gpu_fwd_bwd(to_dev(x))
     errs = compare_full(out, oracle_full(x))
     check_errs(errs, "logit_shifts")
+
+
+def test_large_ragged_n_sampled():
+    """N = 2040 (16 key tiles, the last one ragged; 255 query tiles of 8 rows
+    short of a multiple of 128): sampled parity against the FP64 oracle on
+    three slices and six dbias rows, with every output finite."""
+    w = S.custom(1, 2040, 1, 32, name="n2040", mask="tail", mask_frac=0.05)
+    x = S.make_inputs(w, seed=3)
+    out = gpu_fwd_bwd(to_dev(x))
+    for t in ("o", "dq", "dk", "dv", "dbias"):
+        assert torch.isfinite(out[t].float()).all(), t
+    errs = compare_sampled(x, out, w, n_slices=3, n_rows=6, seed=7)
+    check_errs(errs, "n2040")

@@ -155,7 +155,7 @@ struct BwdBars {
   uint64_t kv_full;
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t b_full[2], b_empty[2];
-  uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full, all_done;
+  uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full, dq_read, all_done;
   uint32_t tmem_slot;
   int abort;
 };
@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&bars->p_ready, kEW);
     mbar_init(&bars->ds_ready, kEW);
     mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_read, 128);
     mbar_init(&bars->all_done, 3);
     bars->abort = 0;
     fence_mbar_init();
@@ -224,9 +225,38 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
+  // Warpgroup 0 (producer and the three issuers: one warp per TMEM lane
+  // quarter) drains each dQ tile: warp w stores rows [32w, 32w + 32), all D
+  // columns scaled by 1/sqrt(D), as this key tile's FP32 partial, chunk-major
+  // per 128-row tile: [J_K][slices][J_Q][D/4 float4 chunks][128 rows].  Then
+  // S^T(t+2), which overwrites those columns, may be issued.
+  auto drain_dq = [&](int t) -> bool {
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, t & 1, wc, abort))) return false;
+    tc_fence_after();
+    const int ti = t / G, tg = t % G;
+    const int r = (warp & 3) * 32 + lane;
+    const size_t slice = static_cast<size_t>((b * N_o + o0 + tg) * H + h);
+    const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
+    float4* out = reinterpret_cast<float4*>(dq_part) +
+                  ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D / 4) + r;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTS + 64;
+    const float isd = rsqrtf(static_cast<float>(D));
+    uint32_t qr[D];
+    if constexpr (D == 32) tmem_ld32(taddr, qr);
+    else tmem_ld16(taddr, qr);
+    tc_wait_ld_regs(qr);
+#pragma unroll
+    for (int c = 0; c < D / 4; ++c)
+      out[c * BM] = make_float4(__uint_as_float(qr[4 * c]) * isd, __uint_as_float(qr[4 * c + 1]) * isd,
+                                __uint_as_float(qr[4 * c + 2]) * isd, __uint_as_float(qr[4 * c + 3]) * isd);
+    tc_fence_before();
+    mbar_arrive(&bars->dq_read);
+    return true;
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ producer (converged warp)
+    if (elect_one()) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
@@ -238,18 +268,31 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tma_load_3d(sm + L::kK + g * L::kTile, &tm_k, &bars->kv_full, 0, ktile * BN, boh);
         tma_load_3d(sm + L::kV + g * L::kTile, &tm_v, &bars->kv_full, 0, ktile * BN, boh);
       }
-      for (int s = 0; s < nsteps && !*abort; ++s) {
-        const int i = s / G, g = s % G;
-        if (g == 0) {
-          const int st = i & 1;
-          if (!mbar_wait(&bars->b_empty[st], ((i >> 1) & 1) ^ 1, wc, abort)) break;
+    }
+    __syncwarp();
+    bool ok = true;
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int i = s / G, g = s % G;
+      if (g == 0) {
+        const int st = i & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->b_empty[st], ((i >> 1) & 1) ^ 1, wc, abort))) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
           mbar_expect_tx(&bars->b_full[st], BM * BN * 2);
           uint8_t* bdst = sm + L::kBias + st * (BM * BN * 2);
           tma_load_3d(bdst, &tm_biasT, &bars->b_full[st], i * BM, ktile * BN, bh);
           tma_load_3d(bdst + BN * 128, &tm_biasT, &bars->b_full[st], i * BM + 64, ktile * BN, bh);
         }
-        const int st = s & 1;
-        if (!mbar_wait(&bars->qdo_empty[st], ((s >> 1) & 1) ^ 1, wc, abort)) break;
+        __syncwarp();
+      }
+      const int st = s & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->qdo_empty[st], ((s >> 1) & 1) ^ 1, wc, abort))) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
         const int boh = (b * N_o + o0 + g) * H + h;
         mbar_expect_tx(&bars->qdo_full[st], 2 * L::kTile + kStatFloats * 4);
         tma_load_3d(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], 0, i * BM, boh);
@@ -257,7 +300,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         bulk_load(sm + L::kStat + st * kStatFloats * 4, stat + (static_cast<size_t>(boh) * JQ + i) * kStatFloats,
                   kStatFloats * 4, &bars->qdo_full[st]);
       }
+      __syncwarp();
+      if (s >= 2) ok = drain_dq(s - 2);
     }
+    for (int t = nsteps >= 2 ? nsteps - 2 : 0; t < nsteps && ok; ++t) ok = drain_dq(t);
   } else if (warp <= 3) {
     // ------------------------------------------------------------ MMA issuers
     constexpr uint32_t kSwz = (D == 32) ? 4u : 6u;  // 64B / 32B swizzle for D-wide rows
@@ -289,9 +335,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int s = 0; s < nsteps && ok; ++s) {
         const int i = s / G, g = s % G, st = s & 1;
         const bool next = s + 1 < nsteps;
-        // P-phase of s done (P^T in TMEM, the previous dQ tile read); Q(s+1) loaded
+        // P-phase of s done (P^T in TMEM); Q(s+1) loaded; the dQ tile of s-1,
+        // which S^T(s+1) overwrites, drained
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_ready, s & 1, wc, abort)) ||
-            (next && !__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort)))) {
+            (next && !__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort))) ||
+            (next && s > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->dq_read, (s - 1) & 1, wc, abort)))) {
           ok = false;
           break;
         }
@@ -311,6 +359,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_commit(&bars->qdo_empty[st]);
         }
         __syncwarp();
+        if (!drain_dq(s)) { ok = false; break; }
       }
     } else if (warp == 2) {
       // ---- issuer C: dK_g += dS^T Q, then dP^T(s+1) = V dO^T
@@ -349,6 +398,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_commit(&bars->qdo_empty[st]);
         }
         __syncwarp();
+        if (!drain_dq(s)) { ok = false; break; }
       }
     } else {
       // ---- issuer B: the dQ tile dS K into S^T columns [64, 64 + D)
@@ -368,6 +418,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_commit(&bars->dq_full);
         }
         __syncwarp();
+        if (!drain_dq(s)) { ok = false; break; }
       }
     }
     // every MMA this issuer started is complete when all_done fires
@@ -403,32 +454,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     named_bar_sync(1, kEW);
 
-    // this key tile's dQ tile of step t (in S^T columns [64, 64 + D) of TMEM,
-    // lane = query row): D/4 columns per warpgroup, scaled by 1/sqrt(D),
-    // stored chunk-major per 128-row tile: [J_K][slices][J_Q][D/4 float4 chunks][128 rows]
-    auto store_dq_tile = [&](int t) {
-      const int ti = t / G, tg = t % G;
-      const size_t slice = static_cast<size_t>((b * N_o + o0 + tg) * H + h);
-      const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
-      float4* out = reinterpret_cast<float4*>(dq_part) +
-                    ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D / 4) + wg * (D / 16) * BM + r;
-      if constexpr (D == 32) {
-        uint32_t qr[8];
-        tmem_ld8(tmem + lane_addr + kTDQ + 8 * wg, qr);
-        tc_wait_ld();
-#pragma unroll
-        for (int v = 0; v < 2; ++v)
-          out[v * BM] = make_float4(__uint_as_float(qr[4 * v]) * inv_sqrt_d, __uint_as_float(qr[4 * v + 1]) * inv_sqrt_d,
-                                    __uint_as_float(qr[4 * v + 2]) * inv_sqrt_d,
-                                    __uint_as_float(qr[4 * v + 3]) * inv_sqrt_d);
-      } else {
-        uint32_t qr[4];
-        tmem_ld4(tmem + lane_addr + kTDQ + 4 * wg, qr);
-        tc_wait_ld();
-        out[0] = make_float4(__uint_as_float(qr[0]) * inv_sqrt_d, __uint_as_float(qr[1]) * inv_sqrt_d,
-                             __uint_as_float(qr[2]) * inv_sqrt_d, __uint_as_float(qr[3]) * inv_sqrt_d);
-      }
-    };
     float2 dbacc[kCols / 2];  // dbias accumulators of this thread's key for its query columns
 #pragma unroll
     for (int k = 0; k < kCols / 2; ++k) dbacc[k] = make_float2(0.f, 0.f);
@@ -489,19 +514,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       // every warp has loaded S^T: BF16 P^T may overwrite its first 64 columns
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_cons, s & 1, wc, abort))) { ok = false; break; }
       tmem_st16(tmem + lane_addr + kTS + 16 * wg, pw);
-      if (s > 0) {
-        // the previous step's MMAs are complete: dQ tile in S^T columns
-        // [64, 64 + D), dS in shared memory no longer read
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (s - 1) & 1, wc, abort))) { ok = false; break; }
-        tc_fence_after();
-        store_dq_tile(s - 1);
-      }
       tc_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
 
-      // ---------------- dS-phase
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, s & 1, wc, abort))) { ok = false; break; }
+      // ---------------- dS-phase (dS in shared memory is free once the previous dQ tile is done)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, s & 1, wc, abort)) ||
+          (s > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (s - 1) & 1, wc, abort)))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {  // 16 queries at a time
@@ -552,13 +574,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
         for (int k = 0; k < kCols / 2; ++k) dbacc[k] = make_float2(0.f, 0.f);
       }
-    }
-    // the last step's dQ tile
-    if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (nsteps - 1) & 1, wc, abort))) {
-      tc_fence_after();
-      store_dq_tile(nsteps - 1);
-    } else {
-      ok = false;
     }
 
     // ------------------------------------------------------------ epilogue: dV_g and dK_g of slice g = wg

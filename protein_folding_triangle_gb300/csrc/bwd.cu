@@ -126,8 +126,9 @@ __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __r
 // MMA order per step: dV_g += P^T dO (A from TMEM) and S^T(s+1) after the
 // P-phase; dK_g += dS^T Q (A from TMEM) and dP^T(s+1) after the dS-phase; the
 // dQ tile dS K (into S^T columns [64, 64 + D)) after the dS-phase, once every
-// warp has loaded S^T(s+1).  The P-phase of s+1 reads that dQ tile.  dK is scaled by
-// 1/sqrt(D) when it leaves TMEM, the dQ tile when it is read.  After slice
+// warp has loaded S^T(s+1).  Warpgroup 0 (one warp per TMEM lane quarter)
+// stores that dQ tile as soon as it completes; S^T(s+2) waits for that.  dK
+// is scaled by 1/sqrt(D) when it leaves TMEM, the dQ tile when it is stored.  After slice
 // G-1 of a query tile the FP32 dbias partial of the outer group is written
 // once.
 template <int D>

@@ -182,7 +182,7 @@ def kernel_work(w, name):
     U = w.B * w.No * w.H * w.N * w.N * w.D
     rows = w.B * w.No * w.H * w.N
     jk = (w.N + 127) // 128
-    groups = w.No // 4
+    groups = w.No // (8 if w.D == 16 else 4)  # outer slices per backward CTA
     if name == "tri_attn_fwd":
         return 4 * U, "flop", "tensor"
     if name == "bwd_main":

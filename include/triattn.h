@@ -94,7 +94,8 @@ triattn_status tri_attn_fwd(const triattn_shape* shape,
  * The workspace holds, per (slice, 128-row query tile), a record of the FP32
  * values -lse*log2(e) and -delta; a transposed copy of the bias; the
  * single-writer FP32 dQ partials (one per key tile) and the single-writer
- * FP32 dbias partials (one per outer group of slices) ("TurboPairFormer",
+ * FP32 dbias partials (one per outer group of 4 slices at D = 32, 8 at
+ * D = 16) ("TurboPairFormer",
  * Figure 2(b), Figure 7, Table 11).
  */
 size_t triattn_bwd_workspace_bytes(const triattn_shape* shape);
@@ -148,7 +149,7 @@ triattn_status tri_attn_bwd(const triattn_shape* shape,
  * that loads the library holds until the process exits.
  *   - A shape whose triattn_bwd_workspace_bytes() exceeds
  *     TRIATTN_NOALLOC_SCRATCH_BYTES is rejected with TRIATTN_ERR_WORKSPACE
- *     before anything is launched (B=1, N=48, H=2, D=16 needs 2.4 MiB;
+ *     before anything is launched (B=1, N=48, H=2, D=16 needs 1.6 MiB;
  *     a 384-token crop with H=4, D=32 needs 438 MiB and is rejected).
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress while that device is current.  Make that first

@@ -108,7 +108,7 @@ WsLayout ws_layout(const triattn_shape* s) {
   const size_t slices = static_cast<size_t>(s->B) * s->N_o * s->H;
   const size_t jk = (s->N + kTileK - 1) / kTileK;
   const size_t jq = (s->N + kTileQ - 1) / kTileQ;
-  const size_t groups = s->N_o / kGroupBwd;
+  const size_t groups = s->N_o / kGroupBwdFor(s->D);
   WsLayout w;
   w.stat_off = 0;
   w.biasT_off = round_up(slices * jq * 2 * kTileQ * 4, 256);
@@ -259,6 +259,7 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
   a.N_o = shape->N_o;
   a.N = shape->N;
   a.H = shape->H;
+  a.D = shape->D;
   a.wc = wait_ctl(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool d32 = shape->D == 32;

@@ -18,7 +18,6 @@ namespace {
 
 constexpr int BM = kTileQ;   // query rows per tile
 constexpr int BN = kTileK;   // keys per CTA (TMEM lanes of S^T, dP^T, dK, dV)
-constexpr int G = kGroupBwd; // outer slices per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kStatFloats = 2 * BM;  // per (slice, query tile): -lse log2 e [128], -delta [128]
 
@@ -100,6 +99,9 @@ __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __r
 // them as their A operand, and the key mask of a slice is one value per thread.
 //
 // Thread roles (20 warps):
+// G = 4 slices per CTA at D = 32, 8 at D = 16 (TMEM: dV and dK of every slice
+// in 2 G D columns, S^T and dP^T in 256).
+//
 //   warp 0       TMA producer: K, V of the G slices once; per query tile one
 //                transposed bias tile; per (query tile, slice) the Q and dO
 //                tiles and the record of -lse log2 e and -delta.
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __r
 // once.
 template <int D>
 struct BwdSmem {
+  static constexpr int G = kGroupBwdFor(D);             // outer slices per CTA
   static constexpr int kTile = BM * D * 2;              // 128 rows x D bf16
   static constexpr int kDS = 0;                         // dS^T [2 query blocks][128 k][64 q] bf16, SW128
   static constexpr int kBias = kDS + BN * BM * 2;       // 2 stages of bias^T, same layout
@@ -169,6 +172,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                     const float* __restrict__ stat, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv,
                     float* __restrict__ dq_part, float* __restrict__ dbias_part, int N_o, int N, int H, WaitCtl wc) {
   using L = BwdSmem<D>;
+  constexpr int G = L::G;  // outer slices per CTA
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   BwdBars* bars = reinterpret_cast<BwdBars*>(sm + L::kBar);
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   // BF16 P^T is packed into S^T columns [0, 64), the dQ tile (D columns) into
   // S^T columns [64, 64 + D); BF16 dS^T of warpgroup w into dP^T columns
   // [32w, 32w + 16).
-  constexpr uint32_t kTS = 8 * D;
+  constexpr uint32_t kTS = 2 * G * D;
   constexpr uint32_t kTDP = kTS + 128;
   constexpr uint32_t kTDQ = kTS + 64;
   static_assert(kTDP + 128 <= 512, "TMEM budget");
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const uint64_t qd = dQb + st * kTile16;
         const uint64_t don = dDOb + ((s + 1) & 1) * kTile16, vn = dVb + ((s + 1) % G) * kTile16;
         if (elect_one()) {
-          const uint32_t tdk = tmem + 4 * D + (s % G) * D;
+          const uint32_t tdk = tmem + G * D + (s % G) * D;
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)  // dK_g += dS^T Q
             mma_ts(tdk, tmem + kTDP + 32 * (kk >> 1) + 8 * (kk & 1), qd + kk * kRowStep, idKV,
@@ -437,21 +441,20 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     uint8_t* sDS = sm + L::kDS;
 
     // base-2 key mask of each slice of the group (-inf past N): warpgroup w
-    // stages slice w.  Staged before any bounded wait, so the barrier below
-    // is always entered by every elementwise thread.
-    static_assert(kNWG == G, "one warpgroup per slice stages the key mask");
+    // stages slices w, w + 4, ...  Staged before any bounded wait, so the
+    // barrier below is always entered by every elementwise thread.
     const int key = ktile * BN + r;
     float* mask_s = reinterpret_cast<float*>(sm + L::kMask);
-    {
+    for (int gg = wg; gg < G; gg += kNWG) {
       float mv = -INFINITY;
       if (key < N) {
         mv = 0.f;
         if (mask != nullptr)
-          mv = __uint_as_float(static_cast<uint32_t>(__ldg(mask + (static_cast<size_t>(b) * N_o + o0 + wg) * N + key))
+          mv = __uint_as_float(static_cast<uint32_t>(__ldg(mask + (static_cast<size_t>(b) * N_o + o0 + gg) * N + key))
                                << 16) *
                kLog2e;
       }
-      mask_s[wg * BN + r] = mv;
+      mask_s[gg * BN + r] = mv;
     }
     named_bar_sync(1, kEW);
 
@@ -577,14 +580,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
     }
 
-    // ------------------------------------------------------------ epilogue: dV_g and dK_g of slice g = wg
+    // ------------------------------------------------------------ epilogue: dV_g and dK_g of slices g = wg, wg + 4, ...
     if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->all_done, 0, wc, abort))) {
       tc_fence_after();
-      const int g = wg;
-      const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + key;
+#pragma unroll 1
+      for (int g = wg; g < G; g += kNWG)
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t t = tmem + lane_addr + which * 4 * D + g * D;
+        const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + key;
+        const uint32_t t = tmem + lane_addr + which * G * D + g * D;
         const float sc = which == 0 ? 1.f : inv_sqrt_d;
         uint32_t w[D / 2];
         if constexpr (D == 32) {
@@ -747,7 +751,7 @@ cudaError_t launch_bwd_transpose_bias(const BwdArgs& a, cudaStream_t stream) {
 template <int D>
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
-  dim3 grid(JK, a.N_o / G, a.B * a.H);
+  dim3 grid(JK, a.N_o / BwdSmem<D>::G, a.B * a.H);
   bwd_main_kernel<D><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.stat,
       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
@@ -767,7 +771,8 @@ cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
   const size_t tiles = static_cast<size_t>(a.B) * a.H * JQ * JK;
   reduce_dbias_kernel<<<static_cast<unsigned>(tiles * (BM / kSlab)), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK, a.N_o / G, tiles);
+      reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK,
+      a.N_o / kGroupBwdFor(a.D), tiles);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,9 @@ constexpr int kTileK = 128;
 // Outer slices per CTA: forward (shared bias tile) and backward (outer group
 // of the key-tile-parallel backward).
 constexpr int kGroupFwd = 4;
-constexpr int kGroupBwd = 4;
+// Backward: dK and dV of all slices of the group stay in TMEM (2 * G * D of
+// its 512 columns next to 256 for S^T and dP^T), so G = 8 at D = 16.
+constexpr int kGroupBwdFor(int D) { return D == 16 ? 8 : 4; }
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_bias;  // Q: 128-row boxes; K, V: 64-row boxes
@@ -44,7 +46,7 @@ struct BwdArgs {
   float* stat;       // [slices][J_Q][2 x 128]: -lse log2 e, -delta
   float* dq_part;    // [J_K][slices][J_Q][128 x D]
   float* dbias_part; // [L][B*H*N*N]
-  int B, N_o, N, H;
+  int B, N_o, N, H, D;
   WaitCtl wc;
 };
 

@@ -160,6 +160,7 @@ struct BwdBars {
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t b_full[2], b_empty[2];
   uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full, dq_read, all_done;
+  uint64_t never;  // completes no phase: a parity-1 wait on it always passes
   uint32_t tmem_slot;
   int abort;
 };
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_read, 128);
     mbar_init(&bars->all_done, 3);
+    mbar_init(&bars->never, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -341,10 +343,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int i = s / G, g = s % G, st = s & 1;
         const bool next = s + 1 < nsteps;
         // P-phase of s done (P^T in TMEM); Q(s+1) loaded; the dQ tile of s-1,
-        // which S^T(s+1) overwrites, drained
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_ready, s & 1, wc, abort)) ||
-            (next && !__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort))) ||
-            (next && s > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->dq_read, (s - 1) & 1, wc, abort)))) {
+        // which S^T(s+1) overwrites, drained (parity 1 passes at s = 0)
+        const uint32_t wb[3] = {smem_u32(&bars->p_ready), smem_u32(next ? &bars->qdo_full[(s + 1) & 1] : &bars->never),
+                               smem_u32(next ? &bars->dq_read : &bars->never)};
+        const uint32_t wp[3] = {static_cast<uint32_t>(s & 1), next ? ((s + 1) >> 1) & 1 : 1u,
+                                next ? (s - 1) & 1 : 1u};
+        if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
           break;
         }
@@ -381,8 +385,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int i = s / G, st = s & 1;
         const bool next = s + 1 < nsteps;
         // dS-phase of s done (dS^T in TMEM); dO(s+1) loaded
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, s & 1, wc, abort)) ||
-            (next && !__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[(s + 1) & 1], ((s + 1) >> 1) & 1, wc, abort)))) {
+        const uint32_t wb[2] = {smem_u32(&bars->ds_ready), smem_u32(next ? &bars->qdo_full[(s + 1) & 1] : &bars->never)};
+        const uint32_t wp[2] = {static_cast<uint32_t>(s & 1), next ? ((s + 1) >> 1) & 1 : 1u};
+        if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
           break;
         }
@@ -407,10 +412,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
     } else {
       // ---- issuer B: the dQ tile dS K into S^T columns [64, 64 + D)
+      // S^T(0) loaded, so that the s_cons poll below never sees the barrier
+      // two phases behind
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars->s_cons, 0, wc, abort));
       for (int s = 0; s < nsteps && ok; ++s) {
         // dS of s in shared memory; every warp has loaded S^T(s+1)
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, s & 1, wc, abort)) ||
-            (s + 1 < nsteps && !__all_sync(0xffffffffu, mbar_wait(&bars->s_cons, (s + 1) & 1, wc, abort)))) {
+        const bool next = s + 1 < nsteps;
+        const uint32_t wb[2] = {smem_u32(&bars->ds_ready), smem_u32(next ? &bars->s_cons : &bars->never)};
+        const uint32_t wp[2] = {static_cast<uint32_t>(s & 1), next ? (s + 1) & 1 : 1u};
+        if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
           break;
         }
@@ -468,18 +478,25 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     for (int s = 0; s < nsteps && ok; ++s) {
       const int i = s / G, g = s % G, st = s & 1;
       const int bst = i & 1;
+      // bias^T tile of query tile i, this step's -lse log2 e / -delta record
+      // and S^T(s)
       if (g == 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->b_full[bst], (i >> 1) & 1, wc, abort))) {
         ok = false;
         break;
       }
-      // this step's -lse log2 e / -delta record
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[st], (s >> 1) & 1, wc, abort))) { ok = false; break; }
+      {
+        const uint32_t wb[2] = {smem_u32(&bars->qdo_full[st]), smem_u32(&bars->s_full)};
+        const uint32_t wp[2] = {static_cast<uint32_t>((s >> 1) & 1), static_cast<uint32_t>(s & 1)};
+        if (!mbar_wait_all(wb, wp, wc, abort)) {
+          ok = false;
+          break;
+        }
+      }
       const float* nlse2 = reinterpret_cast<const float*>(sm + L::kStat + st * kStatFloats * 4) + col0;
       const float* ndelta = nlse2 + BM;
       const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
 
       // ---------------- P-phase
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, wc, abort))) { ok = false; break; }
       tc_fence_after();
       float2 p[kCols / 2];
       uint32_t pw[kCols / 2];
@@ -523,10 +540,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_arrive(&bars->p_ready);
 
       // ---------------- dS-phase (dS in shared memory is free once the previous dQ tile is done)
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, s & 1, wc, abort)) ||
-          (s > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, (s - 1) & 1, wc, abort)))) {
-        ok = false;
-        break;
+      {
+        // dP^T(s); the dQ tile of s-1 has read dS (parity 1 passes at s = 0)
+        const uint32_t wb[2] = {smem_u32(&bars->dp_full), smem_u32(&bars->dq_full)};
+        const uint32_t wp[2] = {static_cast<uint32_t>(s & 1), static_cast<uint32_t>((s - 1) & 1)};
+        if (!mbar_wait_all(wb, wp, wc, abort)) {
+          ok = false;
+          break;
+        }
       }
       tc_fence_after();
 #pragma unroll

@@ -80,6 +80,57 @@ static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Bounded wait for several phases at once (barriers given by shared-memory
+// address).  The first polls of all barriers are issued back to back, so
+// phases that are already complete cost one round trip instead of one each.
+// A slot that is not needed passes a barrier that never completes a phase
+// together with parity 1 (the phase before the first), which is always
+// reported complete.
+// Precondition: for every barrier, the calling thread already knows the phase
+// before the awaited one to be complete (from an earlier wait of its own).
+// The polls are independent, so one may run while another is still pending;
+// a barrier two phases behind would then match the awaited parity on its
+// previous phase and pass too early.
+__device__ __forceinline__ bool mbar_try_wait_at(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+template <int N>
+static __device__ __forceinline__ bool mbar_wait_all(const uint32_t (&bar)[N], const uint32_t (&parity)[N],
+                                                     const WaitCtl& wc, volatile int* abort) {
+  uint32_t done = 1;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar[k]), "r"(parity[k])
+        : "memory");
+    done &= ok;
+  }
+  if (__all_sync(0xffffffffu, done != 0)) return true;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+      if (__all_sync(0xffffffffu, mbar_try_wait_at(bar[k], parity[k], kSuspendHintNs))) break;
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > wc.limit_ns) {
+        atomicOr(wc.status, kDevTimeout);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2) {

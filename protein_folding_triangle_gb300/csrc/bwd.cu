@@ -20,6 +20,10 @@ constexpr int BM = kTileQ;   // query rows per tile
 constexpr int BN = kTileK;   // keys per CTA (TMEM lanes of S^T, dP^T, dK, dV)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kStatFloats = 2 * BM;  // per (slice, query tile): -lse log2 e [128], -delta [128]
+// Stages of the Q / dO / record ring.  A stage is refilled once dK of its
+// step is done, and the next-but-one step's S^T needs it: three stages leave
+// more than a step of time for the load.
+constexpr int NQ = 3;
 
 // ---------------------------------------------------------------- preprocess
 // One record of 2 x 128 FP32 per (slice, query tile), padded to whole tiles:
@@ -141,10 +145,10 @@ struct BwdSmem {
   static constexpr int kBias = kDS + BN * BM * 2;       // 2 stages of bias^T, same layout
   static constexpr int kK = kBias + 2 * BN * BM * 2;    // G K tiles (stationary)
   static constexpr int kV = kK + G * kTile;             // G V tiles (stationary)
-  static constexpr int kQ = kV + G * kTile;             // 2 stages of Q tiles
-  static constexpr int kDO = kQ + 2 * kTile;            // 2 stages of dO tiles
-  static constexpr int kStat = kDO + 2 * kTile;         // 2 stages of the -lse / -delta record
-  static constexpr int kMask = kStat + 2 * kStatFloats * 4;  // G x 128 fp32: base-2 key mask
+  static constexpr int kQ = kV + G * kTile;             // NQ stages of Q tiles
+  static constexpr int kDO = kQ + NQ * kTile;           // NQ stages of dO tiles
+  static constexpr int kStat = kDO + NQ * kTile;        // NQ stages of the -lse / -delta record
+  static constexpr int kMask = kStat + NQ * kStatFloats * 4;  // G x 128 fp32: base-2 key mask
   static constexpr int kBar = kMask + G * BN * 4;
   static constexpr int kBytes = kBar + 256;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -157,7 +161,7 @@ constexpr int kMainThreads = 128 + kEW;
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t qdo_full[NQ], qdo_empty[NQ];
   uint64_t b_full[2], b_empty[2];
   uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full, dq_read, all_done;
   uint64_t never;  // completes no phase: a parity-1 wait on it always passes
@@ -208,9 +212,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NQ; ++i) {
       mbar_init(&bars->qdo_full[i], 1);
       mbar_init(&bars->qdo_empty[i], 2);  // issuers A (S, dV) and C (dP, dK)
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->b_full[i], 1);
       mbar_init(&bars->b_empty[i], kEW);
     }
@@ -294,8 +300,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
         __syncwarp();
       }
-      const int st = s & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->qdo_empty[st], ((s >> 1) & 1) ^ 1, wc, abort))) {
+      const int st = s % NQ;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->qdo_empty[st], ((s / NQ) & 1) ^ 1, wc, abort))) {
         ok = false;
         break;
       }
@@ -340,13 +346,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         __syncwarp();
       }
       for (int s = 0; s < nsteps && ok; ++s) {
-        const int i = s / G, g = s % G, st = s & 1;
+        const int i = s / G, g = s % G, st = s % NQ, st1 = (s + 1) % NQ;
         const bool next = s + 1 < nsteps;
         // P-phase of s done (P^T in TMEM); Q(s+1) loaded; the dQ tile of s-1,
         // which S^T(s+1) overwrites, drained (parity 1 passes at s = 0)
-        const uint32_t wb[3] = {smem_u32(&bars->p_ready), smem_u32(next ? &bars->qdo_full[(s + 1) & 1] : &bars->never),
+        const uint32_t wb[3] = {smem_u32(&bars->p_ready), smem_u32(next ? &bars->qdo_full[st1] : &bars->never),
                                smem_u32(next ? &bars->dq_read : &bars->never)};
-        const uint32_t wp[3] = {static_cast<uint32_t>(s & 1), next ? ((s + 1) >> 1) & 1 : 1u,
+        const uint32_t wp[3] = {static_cast<uint32_t>(s & 1), next ? ((s + 1) / NQ) & 1 : 1u,
                                 next ? (s - 1) & 1 : 1u};
         if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
         tc_fence_after();
         const uint64_t dod = dDOb + st * kTile16;
-        const uint64_t qn = dQb + ((s + 1) & 1) * kTile16, kn = dKb + ((s + 1) % G) * kTile16;
+        const uint64_t qn = dQb + st1 * kTile16, kn = dKb + ((s + 1) % G) * kTile16;
         if (elect_one()) {
           const uint32_t tdv = tmem + g * D;
 #pragma unroll
@@ -382,18 +388,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         __syncwarp();
       }
       for (int s = 0; s < nsteps && ok; ++s) {
-        const int i = s / G, st = s & 1;
+        const int i = s / G, st = s % NQ, st1 = (s + 1) % NQ;
         const bool next = s + 1 < nsteps;
         // dS-phase of s done (dS^T in TMEM); dO(s+1) loaded
-        const uint32_t wb[2] = {smem_u32(&bars->ds_ready), smem_u32(next ? &bars->qdo_full[(s + 1) & 1] : &bars->never)};
-        const uint32_t wp[2] = {static_cast<uint32_t>(s & 1), next ? ((s + 1) >> 1) & 1 : 1u};
+        const uint32_t wb[2] = {smem_u32(&bars->ds_ready), smem_u32(next ? &bars->qdo_full[st1] : &bars->never)};
+        const uint32_t wp[2] = {static_cast<uint32_t>(s & 1), next ? ((s + 1) / NQ) & 1 : 1u};
         if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint64_t qd = dQb + st * kTile16;
-        const uint64_t don = dDOb + ((s + 1) & 1) * kTile16, vn = dVb + ((s + 1) % G) * kTile16;
+        const uint64_t don = dDOb + st1 * kTile16, vn = dVb + ((s + 1) % G) * kTile16;
         if (elect_one()) {
           const uint32_t tdk = tmem + G * D + (s % G) * D;
 #pragma unroll
@@ -476,7 +482,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     bool ok = true;
 
     for (int s = 0; s < nsteps && ok; ++s) {
-      const int i = s / G, g = s % G, st = s & 1;
+      const int i = s / G, g = s % G, st = s % NQ;
       const int bst = i & 1;
       // bias^T tile of query tile i, this step's -lse log2 e / -delta record
       // and S^T(s)
@@ -486,7 +492,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       {
         const uint32_t wb[2] = {smem_u32(&bars->qdo_full[st]), smem_u32(&bars->s_full)};
-        const uint32_t wp[2] = {static_cast<uint32_t>((s >> 1) & 1), static_cast<uint32_t>(s & 1)};
+        const uint32_t wp[2] = {static_cast<uint32_t>((s / NQ) & 1), static_cast<uint32_t>(s & 1)};
         if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
           break;

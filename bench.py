@@ -189,7 +189,7 @@ def kernel_work(w, name):
         return 10 * U, "flop", "tensor"
     if name == "bwd_preprocess":
         jq = (w.N + 127) // 128
-        return 3 * rows * w.D * 2 + rows * 4 + w.B * w.No * w.H * jq * 128 * 8, "byte", "hbm"
+        return 3 * rows * w.D * 2 + rows * 4 + w.B * w.No * w.H * jq * 128 * 16, "byte", "hbm"
     if name == "bwd_transpose_bias":
         return 2 * w.B * w.H * w.N * w.N * 2, "byte", "hbm"
     if name == "bwd_reduce_dq":

@@ -91,8 +91,8 @@ triattn_status tri_attn_fwd(const triattn_shape* shape,
 
 /*
  * Workspace bytes tri_attn_bwd needs for `shape` (0 on an invalid shape).
- * The workspace holds, per (slice, 128-row query tile), a record of the FP32
- * values -lse*log2(e) and -delta; a transposed copy of the bias; the
+ * The workspace holds, per query row, a 16-byte record of -lse*sqrt(D) and
+ * -delta (each split into three BF16 terms); a transposed copy of the bias; the
  * single-writer FP32 dQ partials (one per key tile) and the single-writer
  * FP32 dbias partials (one per outer group of 4 slices at D = 32, 8 at
  * D = 16) ("TurboPairFormer",

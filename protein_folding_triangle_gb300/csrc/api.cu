@@ -97,10 +97,11 @@ bool make_bias_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t stat_off, biasT_off, dq_off, db_off, total;
+  size_t rec_off, biasT_off, dq_off, db_off, total;
 };
 
-// -lse log2 e / -delta records [slices][J_Q][2 x 128] FP32; transposed bias
+// query-row records [slices][J_Q * 128][8] BF16 (three-term splits of
+// -lse sqrt(D) and -delta); transposed bias
 // [B*H][N][N] BF16; dQ partials [J_K][slices][J_Q][128 x D] FP32; dbias
 // partials [N_o/G][B*H][J_Q][J_K][128 x 128] FP32 (padded to whole tiles);
 // each part 256-byte aligned.
@@ -110,8 +111,8 @@ WsLayout ws_layout(const triattn_shape* s) {
   const size_t jq = (s->N + kTileQ - 1) / kTileQ;
   const size_t groups = s->N_o / kGroupBwdFor(s->D);
   WsLayout w;
-  w.stat_off = 0;
-  w.biasT_off = round_up(slices * jq * 2 * kTileQ * 4, 256);
+  w.rec_off = 0;
+  w.biasT_off = round_up(slices * jq * kTileQ * 16, 256);
   w.dq_off = w.biasT_off + round_up(static_cast<size_t>(s->B) * s->H * s->N * s->N * 2, 256);
   w.db_off = w.dq_off + round_up(jk * slices * jq * kTileQ * s->D * 4, 256);
   w.total = w.db_off + round_up(groups * s->B * s->H * jq * jk * kTileQ * kTileK * 4, 256);
@@ -252,7 +253,7 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
   a.dk = dk;
   a.dv = dv;
   a.dbias = dbias;
-  a.stat = reinterpret_cast<float*>(ws + w.stat_off);
+  a.rec = reinterpret_cast<uint4*>(ws + w.rec_off);
   a.dq_part = reinterpret_cast<float*>(ws + w.dq_off);
   a.dbias_part = reinterpret_cast<float*>(ws + w.db_off);
   a.B = shape->B;

@@ -19,7 +19,16 @@ namespace {
 constexpr int BM = kTileQ;   // query rows per tile
 constexpr int BN = kTileK;   // keys per CTA (TMEM lanes of S^T, dP^T, dK, dV)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kStatFloats = 2 * BM;  // per (slice, query tile): -lse log2 e [128], -delta [128]
+// Per query row the backward keeps an 8-wide BF16 record
+//   [x0, x1, x2, 0, y0, y1, y2, 0],  x0 + x1 + x2 = -lse sqrt(D),  y0 + y1 + y2 = -delta
+// (each value split into three BF16 terms, together about FP32 precision).
+// It is the B operand of one extra K = 16 step of the S^T and dP^T MMAs,
+// whose A operand is a constant [1, 1, 1, 0, 0, 0, 0, 0] (S^T) or
+// [0, 0, 0, 0, 1, 1, 1, 0] (dP^T) per key, with the upper 8 K columns zero,
+// so the tensor core adds -lse sqrt(D) to every score and -delta to every
+// dP value of the query.  A row without any key gets x0 = -1e30 (P = 0).
+constexpr int kRecRow = 16;            // bytes per query row
+constexpr int kRecTile = BM * kRecRow;  // bytes per (slice, query tile)
 // Stages of the Q / dO / record ring.  A stage is refilled once dK of its
 // step is done, and the next-but-one step's S^T needs it: three stages leave
 // more than a step of time for the load.
@@ -34,7 +43,7 @@ template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restrict__ dO,
                                                          const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ e,
-                                                         const float* __restrict__ lse, float* __restrict__ stat,
+                                                         const float* __restrict__ lse, uint4* __restrict__ rec,
                                                          int N, int JQ, size_t padded_rows) {
   const size_t pr = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (slice * JQ + i) * 128 + qq
   if (pr >= padded_rows) return;
@@ -43,7 +52,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
   const int i = static_cast<int>(tile % JQ);
   const size_t slice = tile / JQ;
   const int q = i * BM + qq;
-  float nl2 = -INFINITY, acc = 0.f;
+  float xs = -1e30f, acc = 0.f;
   if (q < N) {
     const size_t row = slice * N + q;
     const uint4* gp = reinterpret_cast<const uint4*>(dO + row * D);
@@ -63,10 +72,21 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
       }
     }
     const float l = __ldg(lse + row);
-    nl2 = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+    if (l != -INFINITY) xs = -l * sqrtf(static_cast<float>(D));
   }
-  stat[tile * kStatFloats + qq] = nl2;
-  stat[tile * kStatFloats + BM + qq] = -acc;
+  // three-term BF16 splits: v = h + m + lo to about 24 significant bits
+  auto split3 = [](float v, uint32_t& w01, uint32_t& w2) {
+    const uint32_t h = pack_bf16x2(v, 0.f) & 0xFFFFu;
+    const float r1 = v - bf16lo_to_f32(h);
+    const uint32_t m = pack_bf16x2(r1, 0.f) & 0xFFFFu;
+    const uint32_t lo = pack_bf16x2(r1 - bf16lo_to_f32(m), 0.f) & 0xFFFFu;
+    w01 = h | (m << 16);
+    w2 = lo;
+  };
+  uint4 w;
+  split3(xs, w.x, w.y);
+  split3(-acc, w.z, w.w);
+  rec[pr] = w;
 }
 
 // biasT[bh][k][q] = bias[bh][q][k]: 64 x 64 tiles through shared memory (N is
@@ -123,7 +143,7 @@ __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __r
 //                dQ tile); warpgroup w handles query columns [32w, 32w + 32).
 //
 // Per step s = (query tile i, slice g), two elementwise phases:
-//   P-phase   P^T = 2^(S^T log2e/sqrt(D) + (bias^T + mask) log2e - lse log2e),
+//   P-phase   P^T = 2^((S^T - lse sqrt(D)) log2e/sqrt(D) + (bias^T + mask) log2e),
 //             FP32 P kept in registers, BF16 P^T written over the first 64
 //             S^T columns of TMEM once every warp has loaded its S^T.
 //   dS-phase  dS^T = P^T (dP^T - delta); dbias accumulator += dS^T (FP32
@@ -147,8 +167,11 @@ struct BwdSmem {
   static constexpr int kV = kK + G * kTile;             // G V tiles (stationary)
   static constexpr int kQ = kV + G * kTile;             // NQ stages of Q tiles
   static constexpr int kDO = kQ + NQ * kTile;           // NQ stages of dO tiles
-  static constexpr int kStat = kDO + NQ * kTile;        // NQ stages of the -lse / -delta record
-  static constexpr int kMask = kStat + NQ * kStatFloats * 4;  // G x 128 fp32: base-2 key mask
+  static constexpr int kAugS = kDO + NQ * kTile;        // constant A of the record step of S^T
+  static constexpr int kAugP = kAugS + kRecTile;        // constant A of the record step of dP^T
+  static constexpr int kRec = kAugP + kRecTile;         // NQ stages of the query-row record
+  static constexpr int kZero = kRec + NQ * kRecTile;    // zeros: K columns 8-15 of the record step
+  static constexpr int kMask = kZero + kRecTile;        // G x 128 fp32: base-2 key mask
   static constexpr int kBar = kMask + G * BN * 4;
   static constexpr int kBytes = kBar + 256;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -174,7 +197,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_biasT, const uint16_t* __restrict__ mask,
-                    const float* __restrict__ stat, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv,
+                    const uint4* __restrict__ rec, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv,
                     float* __restrict__ dq_part, float* __restrict__ dbias_part, int N_o, int N, int H, WaitCtl wc) {
   using L = BwdSmem<D>;
   constexpr int G = L::G;  // outer slices per CTA
@@ -269,6 +292,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (converged warp)
+    // constant A operands of the record step and the zero K columns, made
+    // visible to the tensor core before kv_full (which the issuers wait for)
+    {
+      const uint32_t one2 = 0x3F803F80u, one1 = 0x00003F80u;  // BF16 1.0 pairs
+      uint4* augS = reinterpret_cast<uint4*>(sm + L::kAugS);
+      uint4* augP = reinterpret_cast<uint4*>(sm + L::kAugP);
+      uint4* zero = reinterpret_cast<uint4*>(sm + L::kZero);
+      for (int rr = lane; rr < BM; rr += 32) {
+        augS[rr] = make_uint4(one2, one1, 0u, 0u);
+        augP[rr] = make_uint4(0u, 0u, one2, one1);
+        zero[rr] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
     if (elect_one()) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
@@ -307,11 +345,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       if (elect_one()) {
         const int boh = (b * N_o + o0 + g) * H + h;
-        mbar_expect_tx(&bars->qdo_full[st], 2 * L::kTile + kStatFloats * 4);
+        mbar_expect_tx(&bars->qdo_full[st], 2 * L::kTile + kRecTile);
         tma_load_3d(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], 0, i * BM, boh);
         tma_load_3d(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], 0, i * BM, boh);
-        bulk_load(sm + L::kStat + st * kStatFloats * 4, stat + (static_cast<size_t>(boh) * JQ + i) * kStatFloats,
-                  kStatFloats * 4, &bars->qdo_full[st]);
+        bulk_load(sm + L::kRec + st * kRecTile, rec + (static_cast<size_t>(boh) * JQ + i) * BM, kRecTile,
+                  &bars->qdo_full[st]);
       }
       __syncwarp();
       if (s >= 2) ok = drain_dq(s - 2);
@@ -332,6 +370,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const uint64_t dKb = smem_desc(smem_u32(sm + L::kK), 16, kSbo, kSwz);
     const uint64_t dVb = smem_desc(smem_u32(sm + L::kV), 16, kSbo, kSwz);
     const uint64_t dDSmn = smem_desc(smem_u32(sm + L::kDS), 16384, 1024, 2);  // dS (queries contiguous)
+    // record step (no swizzle, K-major: 8-row core matrices 128 B apart,
+    // K columns 8-15 in the zero block)
+    const uint64_t dAugS = smem_desc(smem_u32(sm + L::kAugS), L::kZero - L::kAugS, 128, 0);
+    const uint64_t dAugP = smem_desc(smem_u32(sm + L::kAugP), L::kZero - L::kAugP, 128, 0);
+    auto rec_desc = [&](int stage) {
+      const uint32_t off = L::kRec + stage * kRecTile;
+      return smem_desc(smem_u32(sm + off), L::kZero - off, 128, 0);
+    };
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, wc, abort)) &&
               (warp == 3 || __all_sync(0xffffffffu, mbar_wait(&bars->qdo_full[0], 0, wc, abort)));
     if (warp == 1) {
@@ -341,6 +387,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTS, dKb + 2 * kk, dQb + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + kTS, dAugS, rec_desc(0), idSS, 1u);  // + (-lse sqrt(D))
           mma_commit(&bars->s_full);
         }
         __syncwarp();
@@ -369,6 +416,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           if (next) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTS, kn + 2 * kk, qn + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + kTS, dAugS, rec_desc(st1), idSS, 1u);
             mma_commit(&bars->s_full);
           }
           mma_commit(&bars->qdo_empty[st]);
@@ -383,6 +431,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTDP, dVb + 2 * kk, dDOb + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + kTDP, dAugP, rec_desc(0), idSS, 1u);  // + (-delta)
           mma_commit(&bars->dp_full);
         }
         __syncwarp();
@@ -409,6 +458,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           if (next) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTDP, vn + 2 * kk, don + 2 * kk, idSS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + kTDP, dAugP, rec_desc(st1), idSS, 1u);
             mma_commit(&bars->dp_full);
           }
           mma_commit(&bars->qdo_empty[st]);
@@ -482,24 +532,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     bool ok = true;
 
     for (int s = 0; s < nsteps && ok; ++s) {
-      const int i = s / G, g = s % G, st = s % NQ;
+      const int i = s / G, g = s % G;
       const int bst = i & 1;
-      // bias^T tile of query tile i, this step's -lse log2 e / -delta record
-      // and S^T(s)
+      // bias^T tile of query tile i and S^T(s) (-lse sqrt(D) already added)
       if (g == 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->b_full[bst], (i >> 1) & 1, wc, abort))) {
         ok = false;
         break;
       }
-      {
-        const uint32_t wb[2] = {smem_u32(&bars->qdo_full[st]), smem_u32(&bars->s_full)};
-        const uint32_t wp[2] = {static_cast<uint32_t>((s / NQ) & 1), static_cast<uint32_t>(s & 1)};
-        if (!mbar_wait_all(wb, wp, wc, abort)) {
-          ok = false;
-          break;
-        }
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, s & 1, wc, abort))) {
+        ok = false;
+        break;
       }
-      const float* nlse2 = reinterpret_cast<const float*>(sm + L::kStat + st * kStatFloats * 4) + col0;
-      const float* ndelta = nlse2 + BM;
       const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
 
       // ---------------- P-phase
@@ -513,7 +556,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars->s_cons);
         const float m = mask_s[g * BN + r];  // 0 for most keys, -inf for masked keys and keys past N
-        const bool madd = m != 0.f;
         const float2 m2 = make_float2(m, m);
 #pragma unroll
         for (int v = 0; v < kCols / 8; ++v) {  // 8 queries per 16-byte chunk
@@ -521,16 +563,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           const uint32_t off = (cc >> 3) * (BN * 128) + sw128(r, cc & 7);
           const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + off);
           const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
-          const float4 l0 = *reinterpret_cast<const float4*>(nlse2 + 8 * v);
-          const float4 l1 = *reinterpret_cast<const float4*>(nlse2 + 8 * v + 4);
-          const float2 nl[4] = {make_float2(l0.x, l0.y), make_float2(l0.z, l0.w), make_float2(l1.x, l1.y),
-                                make_float2(l1.z, l1.w)};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 s2 = make_float2(__uint_as_float(sv[v * 8 + 2 * e]), __uint_as_float(sv[v * 8 + 2 * e + 1]));
             const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
-            float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nl[e]));
-            if (madd) t = fadd2(t, m2);
+            const float2 t = ffma2(s2, c2, ffma2(b2, l2e2, m2));
             const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
             p[v * 4 + e] = pp;
             pw[v * 4 + e] = pack_bf16x2(pp.x, pp.y);
@@ -561,13 +598,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t a[8], bq[8];
         tmem_ld8(tmem + lane_addr + kTDP + col0 + hh * 16, a);
         tmem_ld8(tmem + lane_addr + kTDP + col0 + hh * 16 + 8, bq);
-        const float4 d0 = *reinterpret_cast<const float4*>(ndelta + 16 * hh);
-        const float4 d1 = *reinterpret_cast<const float4*>(ndelta + 16 * hh + 4);
-        const float4 d2 = *reinterpret_cast<const float4*>(ndelta + 16 * hh + 8);
-        const float4 d3 = *reinterpret_cast<const float4*>(ndelta + 16 * hh + 12);
-        const float2 nd[8] = {make_float2(d0.x, d0.y), make_float2(d0.z, d0.w), make_float2(d1.x, d1.y),
-                              make_float2(d1.z, d1.w), make_float2(d2.x, d2.y), make_float2(d2.z, d2.w),
-                              make_float2(d3.x, d3.y), make_float2(d3.z, d3.w)};
         tc_wait_ld_regs(a, bq);
         uint32_t dw[8];
 #pragma unroll
@@ -575,7 +605,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           const uint32_t x0 = e < 4 ? a[2 * e] : bq[2 * e - 8];
           const uint32_t x1 = e < 4 ? a[2 * e + 1] : bq[2 * e - 7];
           const float2 dp2 = make_float2(__uint_as_float(x0), __uint_as_float(x1));
-          const float2 ds = fmul2(p[hh * 8 + e], fadd2(dp2, nd[e]));
+          const float2 ds = fmul2(p[hh * 8 + e], dp2);  // dP^T - delta from the MMA
           dbacc[hh * 8 + e] = fadd2(dbacc[hh * 8 + e], ds);
           dw[e] = pack_bf16x2(ds.x, ds.y);
         }
@@ -763,7 +793,7 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
   const size_t padded = static_cast<size_t>(a.B) * a.N_o * a.H * JQ * BM;
   const unsigned grid = static_cast<unsigned>((padded + 255) / 256);
   preprocess_kernel<D><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(a.dO), static_cast<const uint16_t*>(a.o),
-                                                 static_cast<const uint16_t*>(a.o_resid), a.lse, a.stat, a.N, JQ,
+                                                 static_cast<const uint16_t*>(a.o_resid), a.lse, a.rec, a.N, JQ,
                                                  padded);
   return cudaGetLastError();
 }
@@ -780,7 +810,7 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
   dim3 grid(JK, a.N_o / BwdSmem<D>::G, a.B * a.H);
   bwd_main_kernel<D><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.stat,
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
   return cudaGetLastError();
 }

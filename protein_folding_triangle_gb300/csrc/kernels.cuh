@@ -43,7 +43,7 @@ struct BwdArgs {
   void* dv;
   void* dbias;
   void* biasT;       // [B*H][N (k)][N (q)] transposed copy of the bias
-  float* stat;       // [slices][J_Q][2 x 128]: -lse log2 e, -delta
+  uint4* rec;        // [slices][J_Q * 128] query-row records (BF16 splits of -lse sqrt(D), -delta)
   float* dq_part;    // [J_K][slices][J_Q][128 x D]
   float* dbias_part; // [L][B*H*N*N]
   int B, N_o, N, H, D;

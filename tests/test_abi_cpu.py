@@ -92,13 +92,13 @@ def test_null_and_misaligned_pointers(lib):
 def test_workspace_checks(lib):
     s = T.Shape(1, 48, 48, 2, 16, 0)
     need = lib.triattn_bwd_workspace_bytes(ctypes.byref(s))
-    # layout: -lse / -delta records [slices][J_Q][2 x 128] FP32 + transposed bias [B*H][N][N]
+    # layout: query-row records [slices][J_Q * 128][8] BF16 + transposed bias [B*H][N][N]
     # BF16 + dQ partials [J_K][slices][J_Q][128 x D] FP32 + dbias partials
     # [N_o/G][B*H][J_Q][J_K][128 x 128] FP32 (G = 8 outer slices per CTA at D = 16),
     # each 256-aligned (padded to whole tiles)
     slices = 1 * 48 * 2
     r256 = lambda x: (x + 255) // 256 * 256
-    assert need == (r256(slices * 1 * 256 * 4) + r256(1 * 2 * 48 * 48 * 2) + r256(1 * slices * 1 * 128 * 16 * 4)
+    assert need == (r256(slices * 1 * 128 * 16) + r256(1 * 2 * 48 * 48 * 2) + r256(1 * slices * 1 * 128 * 16 * 4)
                     + r256(6 * 1 * 2 * 1 * 1 * 128 * 128 * 4))
     assert call_bwd(lib, s, need - 1) == T.ERR_WORKSPACE
     assert call_bwd(lib, s, need, ws=None) == T.ERR_WORKSPACE

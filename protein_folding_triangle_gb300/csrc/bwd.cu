@@ -144,14 +144,14 @@ __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __r
 //
 // Per step s = (query tile i, slice g), two elementwise phases:
 //   P-phase   P^T = 2^((S^T - lse sqrt(D)) log2e/sqrt(D) + (bias^T + mask) log2e),
-//             FP32 P kept in registers, BF16 P^T written over the first 64
-//             S^T columns of TMEM once every warp has loaded its S^T.
+//             FP32 P kept in registers, BF16 P^T written into half of the
+//             S^T columns the warpgroup has just read.
 //   dS-phase  dS^T = P^T (dP^T - delta); dbias accumulator += dS^T (FP32
 //             registers); BF16 dS^T into this warpgroup's own dP^T columns
 //             and into shared memory (the A operand of the dQ MMA).
 // MMA order per step: dV_g += P^T dO (A from TMEM) and S^T(s+1) after the
 // P-phase; dK_g += dS^T Q (A from TMEM) and dP^T(s+1) after the dS-phase; the
-// dQ tile dS K (into S^T columns [64, 64 + D)) after the dS-phase, once every
+// dQ tile dS K (into S^T columns [48, 48 + D)) after the dS-phase, once every
 // warp has loaded S^T(s+1).  Warpgroup 0 (one warp per TMEM lane quarter)
 // stores that dQ tile as soon as it completes; S^T(s+2) waits for that.  dK
 // is scaled by 1/sqrt(D) when it leaves TMEM, the dQ tile when it is stored.  After slice
@@ -224,13 +224,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     return;
   }
 
-  // TMEM columns: dV_g at g*D, dK_g at 4D + g*D, S^T (128), dP^T (128).
-  // BF16 P^T is packed into S^T columns [0, 64), the dQ tile (D columns) into
-  // S^T columns [64, 64 + D); BF16 dS^T of warpgroup w into dP^T columns
-  // [32w, 32w + 16).
+  // TMEM columns: dV_g at g*D, dK_g at G*D + g*D, S^T (128), dP^T (128).
+  // Warpgroup w reads S^T and dP^T columns [32w, 32w + 32) and writes its
+  // BF16 P^T (16 columns) back into half of them: the upper half for w = 0,
+  // 2, the lower half for w = 1, 3 (columns 16, 32, 80, 96).  Every column
+  // a thread overwrites it has read itself, so no other warp has to be
+  // waited for, and S^T columns [48, 80) stay free for the dQ tile (D
+  // columns).  BF16 dS^T of warpgroup w goes into dP^T columns [32w, 32w + 16).
   constexpr uint32_t kTS = 2 * G * D;
   constexpr uint32_t kTDP = kTS + 128;
-  constexpr uint32_t kTDQ = kTS + 64;
+  constexpr uint32_t kTDQ = kTS + 48;
+  auto p_col = [](int w) { return static_cast<uint32_t>(16 + 16 * w + 32 * (w >> 1)); };
   static_assert(kTDP + 128 <= 512, "TMEM budget");
 
   if (tid == 0) {
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
     float4* out = reinterpret_cast<float4*>(dq_part) +
                   ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D / 4) + r;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTS + 64;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTDQ;
     const float isd = rsqrtf(static_cast<float>(D));
     uint32_t qr[D];
     if constexpr (D == 32) tmem_ld32(taddr, qr);
@@ -412,7 +416,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           const uint32_t tdv = tmem + g * D;
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)  // dV_g += P^T dO
-            mma_ts(tdv, tmem + kTS + 8 * kk, dod + kk * kRowStep, idKV, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tdv, tmem + kTS + p_col(kk >> 1) + 8 * (kk & 1), dod + kk * kRowStep, idKV,
+                   (i > 0 || kk > 0) ? 1u : 0u);
           if (next) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kTS, kn + 2 * kk, qn + 2 * kk, idSS, kk > 0 ? 1u : 0u);
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!drain_dq(s)) { ok = false; break; }
       }
     } else {
-      // ---- issuer B: the dQ tile dS K into S^T columns [64, 64 + D)
+      // ---- issuer B: the dQ tile dS K into S^T columns [48, 48 + D)
       // S^T(0) loaded, so that the s_cons poll below never sees the barrier
       // two phases behind
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars->s_cons, 0, wc, abort));
@@ -575,9 +580,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
       }
       if (g == G - 1) mbar_arrive(&bars->b_empty[bst]);  // last read of this bias tile
-      // every warp has loaded S^T: BF16 P^T may overwrite its first 64 columns
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_cons, s & 1, wc, abort))) { ok = false; break; }
-      tmem_st16(tmem + lane_addr + kTS + 16 * wg, pw);
+      // BF16 P^T into columns this thread has read itself
+      tmem_st16(tmem + lane_addr + kTS + col0 + ((wg & 1) ? 0 : 16), pw);  // = p_col(wg)
       tc_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);

@@ -726,11 +726,13 @@ __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict
 
 // dbias[b,h,q,k] = sum_{l = 0 .. L-1} dbias_part[l][b,h,q,k]   (ascending l, FP32).
 // A partial tile is stored [32 chunks of 4 queries][128 keys] float4.  One
-// block per 16-query slab of a 128 x 128 tile (b*h, query tile i, key tile
-// t); the loads of four consecutive partials are issued together, the adds
-// stay in ascending order.
-constexpr int kSlab = 16;
-__global__ void __launch_bounds__(256) reduce_dbias_kernel(const float4* __restrict__ part,
+// block per 8-query slab of a 128 x 128 tile (b*h, query tile i, key tile t),
+// one float4 per thread; the loads of four consecutive partials are issued
+// together, the adds stay in ascending order.  Small blocks keep the SMs
+// evenly loaded to the end (16-query slabs left the last wave ragged).
+constexpr int kSlab = 8;
+constexpr int kRedThreads = kSlab / 4 * BN;  // one float4 chunk per thread
+__global__ void __launch_bounds__(kRedThreads) reduce_dbias_kernel(const float4* __restrict__ part,
                                                            uint16_t* __restrict__ dbias, int N, int JQ, int JK,
                                                            int ngroups, size_t tiles) {
   constexpr int kChunks = BM * BN / 4;     // float4 per tile
@@ -831,7 +833,7 @@ cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
   const size_t tiles = static_cast<size_t>(a.B) * a.H * JQ * JK;
-  reduce_dbias_kernel<<<static_cast<unsigned>(tiles * (BM / kSlab)), 256, 0, stream>>>(
+  reduce_dbias_kernel<<<static_cast<unsigned>(tiles * (BM / kSlab)), kRedThreads, 0, stream>>>(
       reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK,
       a.N_o / kGroupBwdFor(a.D), tiles);
   return cudaGetLastError();

@@ -172,3 +172,59 @@ def test_large_ragged_n_sampled():
         assert torch.isfinite(out[t].float()).all(), t
     errs = compare_sampled(x, out, w, n_slices=3, n_rows=6, seed=7)
     check_errs(errs, "n2040")
+
+
+def test_fully_masked_and_single_key_slices_multi_tile():
+    """D = 32 (four slices per backward CTA), N = 136 (two key and query
+    tiles, ragged): one slice with every key masked (O = 0, lse = -inf, zero
+    gradients for that slice) and one with a single unmasked key (softmax
+    weight 1 on it, dS = 0 everywhere in that slice)."""
+    w = S.custom(1, 136, 2, 32, name="fm136")
+    x = S.make_inputs(w, seed=21)
+    mask = torch.zeros((1, 136, 136), dtype=torch.float32)
+    mask[0, 5, :] = float("-inf")
+    mask[0, 9, :] = float("-inf")
+    mask[0, 9, 130] = 0.0                      # only key 130 (second key tile) is visible
+    x["mask"] = mask.to(torch.bfloat16)
+    out = gpu_fwd_bwd(to_dev(x))
+    assert torch.all(out["o"][0, 5] == 0) and torch.all(torch.isneginf(out["lse"][0, 5]))
+    for g in ("dq", "dk", "dv"):
+        assert torch.all(out[g][0, 5] == 0), g
+    errs = compare_full(out, oracle_full(x))
+    check_errs(errs, "fm136")
+
+
+def test_deterministic_five_calls_d16():
+    """The D = 16 path (eight slices per backward CTA) is bitwise
+    reproducible as well."""
+    w = S.custom(2, 200, 2, 16, name="det16", mask="random", mask_frac=0.05)
+    x = to_dev(S.make_inputs(w, seed=4))
+    ref = gpu_fwd_bwd(x)
+    for _ in range(4):
+        out = gpu_fwd_bwd(x)
+        for t in ("o", "lse", "resid", "dq", "dk", "dv", "dbias"):
+            assert torch.equal(out[t], ref[t]), t
+
+
+def test_finite_additive_mask():
+    """The mask is additive: finite values (a soft penalty of -3.5 on some
+    keys, +1.25 on others, per outer slice) enter the logits like the bias."""
+    w = S.custom(1, 192, 2, 32, name="softmask")
+    x = S.make_inputs(w, seed=8)
+    g = torch.Generator().manual_seed(99)
+    r = torch.rand((1, 192, 192), generator=g)
+    mask = torch.where(r < 0.2, torch.tensor(-3.5), torch.where(r > 0.9, torch.tensor(1.25), torch.tensor(0.0)))
+    mask[0, :, 100] = float("-inf")            # and one hard-masked key
+    x["mask"] = mask.to(torch.bfloat16)
+    out = gpu_fwd_bwd(to_dev(x))
+    errs = compare_full(out, oracle_full(x))
+    check_errs(errs, "softmask")
+
+
+def test_batch2_d16_random_mask():
+    """B = 2, D = 16, N = 264 (three tiles, ragged), random per-slice key mask."""
+    w = S.custom(2, 264, 2, 16, name="b2d16", mask="random", mask_frac=0.05)
+    x = S.make_inputs(w, seed=13)
+    out = gpu_fwd_bwd(to_dev(x))
+    errs = compare_full(out, oracle_full(x))
+    check_errs(errs, "b2d16")

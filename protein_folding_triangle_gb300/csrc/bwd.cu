@@ -268,8 +268,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   // Warpgroup 0 (producer and the three issuers: one warp per TMEM lane
   // quarter) drains each dQ tile: warp w stores rows [32w, 32w + 32), all D
   // columns scaled by 1/sqrt(D), as this key tile's FP32 partial, chunk-major
-  // per 128-row tile: [J_K][slices][J_Q][D/4 float4 chunks][128 rows].  Then
-  // S^T(t+2), which overwrites those columns, may be issued.
+  // per 128-row tile: [J_K][slices][J_Q][D/8 chunks][128 rows] x 8 floats,
+  // with 32-byte stores.  Then S^T(t+2), which overwrites those columns, may
+  // be issued.
   auto drain_dq = [&](int t) -> bool {
     if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, t & 1, wc, abort))) return false;
     tc_fence_after();
@@ -277,8 +278,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int r = (warp & 3) * 32 + lane;
     const size_t slice = static_cast<size_t>((b * N_o + o0 + tg) * H + h);
     const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
-    float4* out = reinterpret_cast<float4*>(dq_part) +
-                  ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D / 4) + r;
+    float* out = dq_part + ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D) + r * 8;
     const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTDQ;
     const float isd = rsqrtf(static_cast<float>(D));
     uint32_t qr[D];
@@ -286,9 +286,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     else tmem_ld16(taddr, qr);
     tc_wait_ld_regs(qr);
 #pragma unroll
-    for (int c = 0; c < D / 4; ++c)
-      out[c * BM] = make_float4(__uint_as_float(qr[4 * c]) * isd, __uint_as_float(qr[4 * c + 1]) * isd,
-                                __uint_as_float(qr[4 * c + 2]) * isd, __uint_as_float(qr[4 * c + 3]) * isd);
+    for (int c = 0; c < D / 8; ++c)
+      st_global_v8(out + c * BM * 8, __uint_as_float(qr[8 * c]) * isd, __uint_as_float(qr[8 * c + 1]) * isd,
+                   __uint_as_float(qr[8 * c + 2]) * isd, __uint_as_float(qr[8 * c + 3]) * isd,
+                   __uint_as_float(qr[8 * c + 4]) * isd, __uint_as_float(qr[8 * c + 5]) * isd,
+                   __uint_as_float(qr[8 * c + 6]) * isd, __uint_as_float(qr[8 * c + 7]) * isd);
     tc_fence_before();
     mbar_arrive(&bars->dq_read);
     return true;
@@ -628,14 +630,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_arrive(&bars->ds_ready);
       if (g == G - 1) {
         // single-writer dbias partial of this outer group for tile (i, ktile),
-        // stored chunk-major ([32 chunks of 4 queries][128 keys] float4) so
-        // that each warp store covers 512 contiguous bytes
-        float4* dst = reinterpret_cast<float4*>(dbias_part) +
-                      ((((static_cast<size_t>(grp) * gridDim.z + bh) * JQ + i) * gridDim.x + ktile) * (BM * BN / 4)) +
-                      (col0 / 4) * BN + r;
+        // stored chunk-major ([16 chunks of 8 queries][128 keys] x 8 floats)
+        // with 32-byte stores, so that each warp store covers 1 KB
+        float* dst = dbias_part +
+                     ((((static_cast<size_t>(grp) * gridDim.z + bh) * JQ + i) * gridDim.x + ktile) * (BM * BN)) +
+                     ((col0 / 8) * BN + r) * 8;
 #pragma unroll
-        for (int k4 = 0; k4 < kCols / 4; ++k4)
-          dst[k4 * BN] = make_float4(dbacc[2 * k4].x, dbacc[2 * k4].y, dbacc[2 * k4 + 1].x, dbacc[2 * k4 + 1].y);
+        for (int k8 = 0; k8 < kCols / 8; ++k8)
+          st_global_v8(dst + k8 * BN * 8, dbacc[4 * k8].x, dbacc[4 * k8].y, dbacc[4 * k8 + 1].x, dbacc[4 * k8 + 1].y,
+                       dbacc[4 * k8 + 2].x, dbacc[4 * k8 + 2].y, dbacc[4 * k8 + 3].x, dbacc[4 * k8 + 3].y);
 #pragma unroll
         for (int k = 0; k < kCols / 2; ++k) dbacc[k] = make_float2(0.f, 0.f);
       }
@@ -708,7 +711,7 @@ __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict
       acc.z += v.z;
       acc.w += v.w;
     }
-    const int c = e / BM, r = e % BM;
+    const int rem = e % (2 * BM), c = 2 * (e / (2 * BM)) + (rem & 1), r = rem >> 1;
     *reinterpret_cast<float4*>(&tile[r * kStride + 4 * c]) = acc;
   }
   __syncthreads();
@@ -725,11 +728,12 @@ __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict
 }
 
 // dbias[b,h,q,k] = sum_{l = 0 .. L-1} dbias_part[l][b,h,q,k]   (ascending l, FP32).
-// A partial tile is stored [32 chunks of 4 queries][128 keys] float4.  One
-// block per 8-query slab of a 128 x 128 tile (b*h, query tile i, key tile t),
-// one float4 per thread; the loads of four consecutive partials are issued
-// together, the adds stay in ascending order.  Small blocks keep the SMs
-// evenly loaded to the end (16-query slabs left the last wave ragged).
+// A partial tile is stored [16 chunks of 8 queries][128 keys] x 8 floats, so
+// an 8-query slab is 4 KB contiguous.  One block per slab of a 128 x 128 tile
+// (b*h, query tile i, key tile t), one float4 per thread (key e/2, queries
+// 4(e&1) .. +4); the loads of four consecutive partials are issued together,
+// the adds stay in ascending order.  Small blocks keep the SMs evenly loaded
+// to the end (16-query slabs left the last wave ragged).
 constexpr int kSlab = 8;
 constexpr int kRedThreads = kSlab / 4 * BN;  // one float4 chunk per thread
 __global__ void __launch_bounds__(kRedThreads) reduce_dbias_kernel(const float4* __restrict__ part,
@@ -745,9 +749,10 @@ __global__ void __launch_bounds__(kRedThreads) reduce_dbias_kernel(const float4*
   const int i = static_cast<int>((t / JK) % JQ);
   const size_t bh = t / (static_cast<size_t>(JK) * JQ);
   const size_t lstride = tiles * kChunks;
+  static_assert(kSlab == 8, "a slab is one 8-query chunk of the partial tile");
   for (int e = threadIdx.x; e < kSlabChunks; e += blockDim.x) {
-    const int cl = e / BN, k = e % BN;     // chunk within the slab, key
-    const float4* p = part + t * kChunks + (slab * (kSlab / 4) + cl) * BN + k;
+    const int cl = e & 1, k = e >> 1;      // 4-query half of the chunk, key
+    const float4* p = part + t * kChunks + slab * kSlabChunks + e;
     float4 acc = __ldcs(p);
     int l = 1;
     for (; l + 4 <= ngroups; l += 4) {

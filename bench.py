@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ablation", choices=["atomic"], default=None,
+                    help="instead of the bench line: time the ordered backward against its non-deterministic "
+                         "FP32-atomic variants (dbias; dbias and dQ) on the same inputs and print one JSON line")
     return ap.parse_args()
 
 
@@ -459,8 +462,73 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- ablation
+def run_atomic_ablation(args):
+    """Backward only: the ordered single-writer partials + fixed-order reductions
+    against FP32 atomics for dbias, and for dbias and dQ (the pages' Table 12
+    trade-off).  Same inputs, same launch stream, CUDA events, median of
+    ``--steps`` timed calls after ``--warmup``; every call re-zeroes its
+    accumulators, as a training step would."""
+    import statistics
+    import torch
+    from protein_folding_triangle_gb300 import build as B
+    from protein_folding_triangle_gb300 import synthetic as S
+    from protein_folding_triangle_gb300 import triattn as T
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    B.build()
+    T.load()
+    dev = torch.device("cuda", 0)
+    w = S.WORKLOADS[args.workload]
+    xd = {k: (None if v is None else v.to(dev)) for k, v in S.make_inputs(w, seed=args.seed).items()}
+    o, lse, resid = T.tri_attn_fwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"])
+    outs = (torch.empty_like(xd["q"]), torch.empty_like(xd["q"]), torch.empty_like(xd["q"]), torch.empty_like(xd["bias"]))
+    arms = {"ordered": None, "atomic_dbias": T.ATOMIC_DBIAS, "atomic_dbias_dq": T.ATOMIC_DBIAS_DQ}
+    wsb = {}
+    for name, m in arms.items():
+        need = T.bwd_workspace_bytes(xd["q"]) if m is None else T.bwd_atomic_workspace_bytes(xd["q"], m)
+        wsb[name] = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def call(name):
+        m = arms[name]
+        args_ = (xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], o, resid, lse, xd["do"])
+        if m is None:
+            T.tri_attn_bwd(*args_, workspace=wsb[name], out=outs)
+        else:
+            T.tri_attn_bwd_atomic_ablation(*args_, m, workspace=wsb[name], out=outs)
+
+    times = {n: [] for n in arms}
+    for _ in range(max(3, args.warmup)):
+        for n in arms:
+            call(n)
+    torch.cuda.synchronize(dev)
+    for _ in range(args.steps):
+        for n in arms:  # interleaved, so that clock drift hits every arm alike
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call(n)
+            e1.record()
+            e1.synchronize()
+            times[n].append(e0.elapsed_time(e1))
+    if T.device_status() != T.OK:
+        raise SystemExit("device status not OK after the ablation")
+    med = {n: statistics.median(v) for n, v in times.items()}
+    line = {"ablation": "ordered FP32 partials vs FP32 atomics (backward only)",
+            "config": {"workload": w.describe(), "B": w.B, "N": w.N, "H": w.H, "D": w.D},
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "bwd_ms_median": {n: round(v, 4) for n, v in med.items()},
+            "saving_vs_ordered": {n: round(1.0 - med[n] / med["ordered"], 4) for n in arms if n != "ordered"},
+            "deterministic": {"ordered": True, "atomic_dbias": False, "atomic_dbias_dq": False},
+            "pages_table12_context": "atomic dbias saves 2.8-8.0% of the backward on the pages' GPUs"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.ablation == "atomic":
+        run_atomic_ablation(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -172,6 +172,32 @@ triattn_status tri_attn_bwd_noalloc(const triattn_shape* shape,
                                     void* stream);
 
 /*
+ * ABLATION ONLY, not the library's backward: the same computation with the
+ * single-writer FP32 partials of dbias (atomic_mask = 2) or of dbias and dQ
+ * (atomic_mask = 3) replaced by FP32 atomic adds into zero-initialised FP32
+ * accumulators, which small kernels then round to BF16 (the non-deterministic
+ * variants of "TurboPairFormer", Section "Deterministic reductions", Table 12).
+ * It exists to measure what the ordered partials cost; its dQ / dbias are
+ * NOT bitwise reproducible between calls (FP32 addition order varies), dK and
+ * dV are.  Arguments are those of tri_attn_bwd; the workspace must hold
+ * triattn_bwd_atomic_workspace_bytes(shape, atomic_mask) bytes (the row
+ * records, the transposed bias, then the FP32 accumulators
+ * [B*N_o*H][J_Q*128][D] for dQ and [B*H][J_K*128][J_Q*128] for dbias, or
+ * the partials of the operand that stays ordered).  atomic_mask other than
+ * 2 or 3 returns TRIATTN_ERR_INVALID_ARG (and 0 bytes).
+ */
+size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask);
+triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape,
+                                            const void* q, const void* k, const void* v,
+                                            const void* bias, const void* mask,
+                                            const void* o, const void* o_resid, const float* lse,
+                                            const void* dO,
+                                            void* dq, void* dk, void* dv, void* dbias,
+                                            int atomic_mask,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * kernels set when a bounded wait gives up.  Returns TRIATTN_OK,
  * TRIATTN_ERR_TIMEOUT, or TRIATTN_ERR_CUDA if the synchronisation failed.

@@ -105,7 +105,7 @@ struct WsLayout {
 // [B*H][N][N] BF16; dQ partials [J_K][slices][J_Q][128 x D] FP32; dbias
 // partials [N_o/G][B*H][J_Q][J_K][128 x 128] FP32 (padded to whole tiles);
 // each part 256-byte aligned.
-WsLayout ws_layout(const triattn_shape* s) {
+WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
   const size_t slices = static_cast<size_t>(s->B) * s->N_o * s->H;
   const size_t jk = (s->N + kTileK - 1) / kTileK;
   const size_t jq = (s->N + kTileQ - 1) / kTileQ;
@@ -114,15 +114,20 @@ WsLayout ws_layout(const triattn_shape* s) {
   w.rec_off = 0;
   w.biasT_off = round_up(slices * jq * kTileQ * 16, 256);
   w.dq_off = w.biasT_off + round_up(static_cast<size_t>(s->B) * s->H * s->N * s->N * 2, 256);
-  w.db_off = w.dq_off + round_up(jk * slices * jq * kTileQ * s->D * 4, 256);
-  w.total = w.db_off + round_up(groups * s->B * s->H * jq * jk * kTileQ * kTileK * 4, 256);
+  // ablation: FP32 accumulators instead of the partials (see tri_attn_bwd_atomic_ablation)
+  const size_t dq_bytes = (atomic_mask & 1) ? slices * jq * kTileQ * s->D * 4 : jk * slices * jq * kTileQ * s->D * 4;
+  const size_t db_bytes = (atomic_mask & 2) ? static_cast<size_t>(s->B) * s->H * jk * kTileK * jq * kTileQ * 4
+                                            : groups * s->B * s->H * jq * jk * kTileQ * kTileK * 4;
+  w.db_off = w.dq_off + round_up(dq_bytes, 256);
+  w.total = w.db_off + round_up(db_bytes, 256);
   return w;
 }
 
 // ---------------------------------------------------------------- tracing
-enum KernelKind { kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKinds };
-const char* const kKernelName[kKinds] = {"tri_attn_fwd",  "bwd_preprocess", "bwd_transpose_bias",
-                                         "bwd_main",      "bwd_reduce_dq",  "bwd_reduce_dbias"};
+enum KernelKind { kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKinds };
+const char* const kKernelName[kKinds] = {"tri_attn_fwd",     "bwd_preprocess",  "bwd_transpose_bias",
+                                         "bwd_main",         "bwd_reduce_dq",   "bwd_reduce_dbias",
+                                         "bwd_main_atomic",  "bwd_finish_dq",   "bwd_finish_dbias"};
 struct TraceRec {
   int kind;
   cudaEvent_t a, b;
@@ -170,6 +175,76 @@ WaitCtl wait_ctl(int dev) {
 }  // namespace triattn
 
 using namespace triattn;
+
+namespace {
+
+// The backward: atomic_mask 0 is the library's ordered path; 2 and 3 are the
+// non-deterministic ablation (FP32 atomics for dbias, and for dQ).
+triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k, const void* v, const void* bias,
+                        const void* mask, const void* o, const void* o_resid, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, void* dbias, int atomic_mask, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  triattn_status st = check_shape(shape);
+  if (st != TRIATTN_OK) return st;
+  const void* req[] = {q, k, v, bias, o, lse, dO, dq, dk, dv, dbias};
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
+  if ((mask && !aligned16(mask)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(shape, atomic_mask);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return TRIATTN_ERR_WORKSPACE;
+  int dev = 0;
+  if ((st = init_device(&dev)) != TRIATTN_OK) return st;
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.biasT = ws + w.biasT_off;
+  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
+      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_biasT, a.biasT, shape))
+    return TRIATTN_ERR_CUDA;
+  a.bias = bias;
+  a.mask = mask;
+  a.o = o;
+  a.o_resid = o_resid;
+  a.lse = lse;
+  a.dO = dO;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dbias = dbias;
+  a.rec = reinterpret_cast<uint4*>(ws + w.rec_off);
+  a.dq_part = reinterpret_cast<float*>(ws + w.dq_off);
+  a.dbias_part = reinterpret_cast<float*>(ws + w.db_off);
+  a.B = shape->B;
+  a.N_o = shape->N_o;
+  a.N = shape->N;
+  a.H = shape->H;
+  a.D = shape->D;
+  a.wc = wait_ctl(dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool d32 = shape->D == 32;
+  cudaError_t e = cudaSuccess;
+  if (atomic_mask & 1) e = cudaMemsetAsync(ws + w.dq_off, 0, w.db_off - w.dq_off, s);
+  if (e == cudaSuccess && (atomic_mask & 2)) e = cudaMemsetAsync(ws + w.db_off, 0, w.total - w.db_off, s);
+  if (e == cudaSuccess)
+    e = traced(kKPre, s, [&] { return d32 ? launch_bwd_preprocess<32>(a, s) : launch_bwd_preprocess<16>(a, s); });
+  if (e == cudaSuccess) e = traced(kKTrans, s, [&] { return launch_bwd_transpose_bias(a, s); });
+  if (e == cudaSuccess && atomic_mask == 0)
+    e = traced(kKMain, s, [&] { return d32 ? launch_bwd_main<32>(a, s) : launch_bwd_main<16>(a, s); });
+  if (e == cudaSuccess && atomic_mask != 0)
+    e = traced(kKMainAtomic, s, [&] {
+      return d32 ? launch_bwd_main_atomic<32>(a, atomic_mask, s) : launch_bwd_main_atomic<16>(a, atomic_mask, s);
+    });
+  if (e == cudaSuccess && !(atomic_mask & 1))
+    e = traced(kKRedDq, s, [&] { return d32 ? launch_bwd_reduce_dq<32>(a, s) : launch_bwd_reduce_dq<16>(a, s); });
+  if (e == cudaSuccess && (atomic_mask & 1))
+    e = traced(kKFinDq, s, [&] { return d32 ? launch_bwd_finish_dq<32>(a, s) : launch_bwd_finish_dq<16>(a, s); });
+  if (e == cudaSuccess && !(atomic_mask & 2)) e = traced(kKRedDb, s, [&] { return launch_bwd_reduce_dbias(a, s); });
+  if (e == cudaSuccess && (atomic_mask & 2)) e = traced(kKFinDb, s, [&] { return launch_bwd_finish_dbias(a, s); });
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -225,53 +300,23 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
                             const void* bias, const void* mask, const void* o, const void* o_resid, const float* lse,
                             const void* dO, void* dq, void* dk, void* dv, void* dbias, void* workspace,
                             size_t workspace_bytes, void* stream) {
-  triattn_status st = check_shape(shape);
-  if (st != TRIATTN_OK) return st;
-  const void* req[] = {q, k, v, bias, o, lse, dO, dq, dk, dv, dbias};
-  for (const void* p : req)
-    if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
-  if ((mask && !aligned16(mask)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
-  const WsLayout w = ws_layout(shape);
-  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
-    return TRIATTN_ERR_WORKSPACE;
-  int dev = 0;
-  if ((st = init_device(&dev)) != TRIATTN_OK) return st;
-  BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.biasT = ws + w.biasT_off;
-  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
-      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_biasT, a.biasT, shape))
-    return TRIATTN_ERR_CUDA;
-  a.bias = bias;
-  a.mask = mask;
-  a.o = o;
-  a.o_resid = o_resid;
-  a.lse = lse;
-  a.dO = dO;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.dbias = dbias;
-  a.rec = reinterpret_cast<uint4*>(ws + w.rec_off);
-  a.dq_part = reinterpret_cast<float*>(ws + w.dq_off);
-  a.dbias_part = reinterpret_cast<float*>(ws + w.db_off);
-  a.B = shape->B;
-  a.N_o = shape->N_o;
-  a.N = shape->N;
-  a.H = shape->H;
-  a.D = shape->D;
-  a.wc = wait_ctl(dev);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool d32 = shape->D == 32;
-  cudaError_t e = traced(kKPre, s, [&] { return d32 ? launch_bwd_preprocess<32>(a, s) : launch_bwd_preprocess<16>(a, s); });
-  if (e == cudaSuccess) e = traced(kKTrans, s, [&] { return launch_bwd_transpose_bias(a, s); });
-  if (e == cudaSuccess)
-    e = traced(kKMain, s, [&] { return d32 ? launch_bwd_main<32>(a, s) : launch_bwd_main<16>(a, s); });
-  if (e == cudaSuccess)
-    e = traced(kKRedDq, s, [&] { return d32 ? launch_bwd_reduce_dq<32>(a, s) : launch_bwd_reduce_dq<16>(a, s); });
-  if (e == cudaSuccess) e = traced(kKRedDb, s, [&] { return launch_bwd_reduce_dbias(a, s); });
-  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+  return bwd_impl(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, 0, workspace, workspace_bytes,
+                  stream);
+}
+
+size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask) {
+  if (check_shape(shape) != TRIATTN_OK || (atomic_mask != 2 && atomic_mask != 3)) return 0;
+  return ws_layout(shape, atomic_mask).total;
+}
+
+triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                                            const void* bias, const void* mask, const void* o, const void* o_resid,
+                                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                            void* dbias, int atomic_mask, void* workspace, size_t workspace_bytes,
+                                            void* stream) {
+  if (atomic_mask != 2 && atomic_mask != 3) return TRIATTN_ERR_INVALID_ARG;
+  return bwd_impl(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, atomic_mask, workspace,
+                  workspace_bytes, stream);
 }
 
 triattn_status triattn_device_status(void* stream) {

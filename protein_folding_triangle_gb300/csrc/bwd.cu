@@ -192,7 +192,11 @@ struct BwdBars {
   int abort;
 };
 
-template <int D>
+// kAtomic (non-deterministic ablation only; 0 in the product path): bit 0
+// adds the dQ tiles into an FP32 [slices][J_Q*128][D] accumulator, bit 1 the
+// dbias tiles into an FP32 [B*H][J_K*128 (k)][J_Q*128 (q)] accumulator, with
+// FP32 atomics instead of writing single-writer partials.
+template <int D, int kAtomic = 0>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -285,12 +289,20 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     if constexpr (D == 32) tmem_ld32(taddr, qr);
     else tmem_ld16(taddr, qr);
     tc_wait_ld_regs(qr);
+    if constexpr ((kAtomic & 1) != 0) {
+      float* acc = dq_part + ((slice * JQ + ti) * BM + r) * D;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c)
-      st_global_v8(out + c * BM * 8, __uint_as_float(qr[8 * c]) * isd, __uint_as_float(qr[8 * c + 1]) * isd,
-                   __uint_as_float(qr[8 * c + 2]) * isd, __uint_as_float(qr[8 * c + 3]) * isd,
-                   __uint_as_float(qr[8 * c + 4]) * isd, __uint_as_float(qr[8 * c + 5]) * isd,
-                   __uint_as_float(qr[8 * c + 6]) * isd, __uint_as_float(qr[8 * c + 7]) * isd);
+      for (int c = 0; c < D / 4; ++c)
+        red_add_v4(acc + 4 * c, __uint_as_float(qr[4 * c]) * isd, __uint_as_float(qr[4 * c + 1]) * isd,
+                   __uint_as_float(qr[4 * c + 2]) * isd, __uint_as_float(qr[4 * c + 3]) * isd);
+    } else {
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        st_global_v8(out + c * BM * 8, __uint_as_float(qr[8 * c]) * isd, __uint_as_float(qr[8 * c + 1]) * isd,
+                     __uint_as_float(qr[8 * c + 2]) * isd, __uint_as_float(qr[8 * c + 3]) * isd,
+                     __uint_as_float(qr[8 * c + 4]) * isd, __uint_as_float(qr[8 * c + 5]) * isd,
+                     __uint_as_float(qr[8 * c + 6]) * isd, __uint_as_float(qr[8 * c + 7]) * isd);
+    }
     tc_fence_before();
     mbar_arrive(&bars->dq_read);
     return true;
@@ -632,13 +644,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // single-writer dbias partial of this outer group for tile (i, ktile),
         // stored chunk-major ([16 chunks of 8 queries][128 keys] x 8 floats)
         // with 32-byte stores, so that each warp store covers 1 KB
-        float* dst = dbias_part +
-                     ((((static_cast<size_t>(grp) * gridDim.z + bh) * JQ + i) * gridDim.x + ktile) * (BM * BN)) +
-                     ((col0 / 8) * BN + r) * 8;
+        if constexpr ((kAtomic & 2) != 0) {
+          float* acc = dbias_part + ((static_cast<size_t>(bh) * gridDim.x * BN + ktile * BN + r) * JQ + i) * BM + col0;
 #pragma unroll
-        for (int k8 = 0; k8 < kCols / 8; ++k8)
-          st_global_v8(dst + k8 * BN * 8, dbacc[4 * k8].x, dbacc[4 * k8].y, dbacc[4 * k8 + 1].x, dbacc[4 * k8 + 1].y,
-                       dbacc[4 * k8 + 2].x, dbacc[4 * k8 + 2].y, dbacc[4 * k8 + 3].x, dbacc[4 * k8 + 3].y);
+          for (int k4 = 0; k4 < kCols / 4; ++k4)
+            red_add_v4(acc + 4 * k4, dbacc[2 * k4].x, dbacc[2 * k4].y, dbacc[2 * k4 + 1].x, dbacc[2 * k4 + 1].y);
+        } else {
+          float* dst = dbias_part +
+                       ((((static_cast<size_t>(grp) * gridDim.z + bh) * JQ + i) * gridDim.x + ktile) * (BM * BN)) +
+                       ((col0 / 8) * BN + r) * 8;
+#pragma unroll
+          for (int k8 = 0; k8 < kCols / 8; ++k8)
+            st_global_v8(dst + k8 * BN * 8, dbacc[4 * k8].x, dbacc[4 * k8].y, dbacc[4 * k8 + 1].x,
+                         dbacc[4 * k8 + 1].y, dbacc[4 * k8 + 2].x, dbacc[4 * k8 + 2].y, dbacc[4 * k8 + 3].x,
+                         dbacc[4 * k8 + 3].y);
+        }
 #pragma unroll
         for (int k = 0; k < kCols / 2; ++k) dbacc[k] = make_float2(0.f, 0.f);
       }
@@ -788,6 +808,49 @@ __global__ void __launch_bounds__(kRedThreads) reduce_dbias_kernel(const float4*
   }
 }
 
+// ---------------------------------------------------------------- ablation only
+// The non-deterministic variant of the backward adds dQ and / or dbias into
+// FP32 accumulators with atomics; these two kernels round them to BF16.
+
+// dQ accumulator [slices][J_Q*128][D] FP32 -> dq [slices][N][D] BF16; one
+// thread per 8 outputs.
+template <int D>
+__global__ void __launch_bounds__(256) finish_dq_kernel(const float4* __restrict__ acc, uint16_t* __restrict__ dq,
+                                                        int N, int JQ, size_t rows) {
+  const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= rows * (D / 8)) return;
+  const size_t row = e / (D / 8);
+  const int c8 = static_cast<int>(e % (D / 8));
+  const size_t slice = row / N;
+  const int q = static_cast<int>(row % N);
+  const float4* src = acc + ((slice * JQ * BM + q) * D + 8 * c8) / 4;
+  const float4 x = src[0], y = src[1];
+  *reinterpret_cast<uint4*>(dq + row * D + 8 * c8) =
+      make_uint4(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w), pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+}
+
+// dbias accumulator [B*H][J_K*128 (k)][J_Q*128 (q)] FP32 -> dbias [B*H][N][N]
+// BF16, transposed through 64 x 64 shared-memory tiles.
+__global__ void __launch_bounds__(256) finish_dbias_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dbias,
+                                                           int N, int JK, int JQ) {
+  __shared__ float tile[64][65];
+  const int q0 = blockIdx.y * 64, k0 = blockIdx.x * 64;
+  const size_t ld = static_cast<size_t>(JQ) * BM;
+  const float* base = acc + static_cast<size_t>(blockIdx.z) * JK * BN * ld;
+  for (int e = threadIdx.x; e < 64 * 64; e += blockDim.x) {
+    const int kk = e / 64, qq = e % 64;  // inside the padded accumulator
+    tile[kk][qq] = base[static_cast<size_t>(k0 + kk) * ld + q0 + qq];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 64 * 32; e += blockDim.x) {
+    const int qq = e / 32, kp = e % 32;
+    const int q = q0 + qq, k = k0 + 2 * kp;
+    if (q >= N || k >= N) continue;  // N is even: k + 1 < N too
+    *reinterpret_cast<uint32_t*>(dbias + (static_cast<size_t>(blockIdx.z) * N + q) * N + k) =
+        pack_bf16x2(tile[2 * kp][qq], tile[2 * kp + 1][qq]);
+  }
+}
+
 }  // namespace
 
 template <int D>
@@ -795,7 +858,13 @@ int bwd_smem_bytes() { return BwdSmem<D>::kBytes; }
 
 template <int D>
 cudaError_t setup_bwd() {
-  return cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       BwdSmem<D>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_main_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_main_kernel<D, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
+  return e;
 }
 
 template <int D>
@@ -816,13 +885,43 @@ cudaError_t launch_bwd_transpose_bias(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
+template <int D, int kAtomic>
+cudaError_t launch_main_variant(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
   dim3 grid(JK, a.N_o / BwdSmem<D>::G, a.B * a.H);
-  bwd_main_kernel<D><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
+  bwd_main_kernel<D, kAtomic><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
+  return launch_main_variant<D, 0>(a, stream);
+}
+
+template <int D>
+cudaError_t launch_bwd_main_atomic(const BwdArgs& a, int atomic_mask, cudaStream_t stream) {
+  if (atomic_mask == 2) return launch_main_variant<D, 2>(a, stream);
+  if (atomic_mask == 3) return launch_main_variant<D, 3>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t stream) {
+  const int JQ = (a.N + BM - 1) / BM;
+  const size_t rows = static_cast<size_t>(a.B) * a.N_o * a.H * a.N;
+  const size_t items = rows * (D / 8);
+  finish_dq_kernel<D><<<static_cast<unsigned>((items + 255) / 256), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, JQ, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_finish_dbias(const BwdArgs& a, cudaStream_t stream) {
+  const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
+  const unsigned t = static_cast<unsigned>((a.N + 63) / 64);
+  finish_dbias_kernel<<<dim3(t, t, a.B * a.H), 256, 0, stream>>>(a.dbias_part, static_cast<uint16_t*>(a.dbias), a.N,
+                                                                 JK, JQ);
   return cudaGetLastError();
 }
 
@@ -846,6 +945,10 @@ cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream) {
 
 template cudaError_t setup_bwd<16>();
 template cudaError_t setup_bwd<32>();
+template cudaError_t launch_bwd_main_atomic<16>(const BwdArgs&, int, cudaStream_t);
+template cudaError_t launch_bwd_main_atomic<32>(const BwdArgs&, int, cudaStream_t);
+template cudaError_t launch_bwd_finish_dq<16>(const BwdArgs&, cudaStream_t);
+template cudaError_t launch_bwd_finish_dq<32>(const BwdArgs&, cudaStream_t);
 template cudaError_t launch_bwd_preprocess<16>(const BwdArgs&, cudaStream_t);
 template cudaError_t launch_bwd_preprocess<32>(const BwdArgs&, cudaStream_t);
 template cudaError_t launch_bwd_main<16>(const BwdArgs&, cudaStream_t);

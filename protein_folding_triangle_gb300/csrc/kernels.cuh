@@ -61,5 +61,10 @@ template <int D> cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stre
 template <int D> cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream);
 template <int D> int bwd_smem_bytes();
+// Non-deterministic ablation of the backward (FP32 atomics; never used by
+// tri_attn_bwd): atomic_mask 2 = dbias, 3 = dbias and dQ.
+template <int D> cudaError_t launch_bwd_main_atomic(const BwdArgs& a, int atomic_mask, cudaStream_t stream);
+template <int D> cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_finish_dbias(const BwdArgs& a, cudaStream_t stream);
 
 }  // namespace triattn

@@ -337,6 +337,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// FP32 atomic add of four consecutive floats (16-byte aligned).  Used only by
+// the non-deterministic ablation of the backward.
+__device__ __forceinline__ void red_add_v4(float* p, float a0, float a1, float a2, float a3) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a0), "f"(a1), "f"(a2), "f"(a3)
+               : "memory");
+}
 // 32-byte global store (address 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(float* p, float a0, float a1, float a2, float a3, float a4, float a5,
                                              float a6, float a7) {

@@ -32,7 +32,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = ran
 
 EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fwd", "tri_attn_bwd",
             "triattn_device_status", "triattn_set_wait_limit_ns", "triattn_trace_enable", "triattn_trace_read",
-            "triattn_test_set_starve", "tri_attn_bwd_noalloc")
+            "triattn_test_set_starve", "tri_attn_bwd_noalloc", "triattn_bwd_atomic_workspace_bytes",
+            "tri_attn_bwd_atomic_ablation")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -75,6 +76,11 @@ def _declare(lib):
     lib.triattn_test_set_starve.restype = None
     lib.tri_attn_bwd_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.tri_attn_bwd_noalloc.restype = ctypes.c_int
+    lib.triattn_bwd_atomic_workspace_bytes.argtypes = [sp, ctypes.c_int]
+    lib.triattn_bwd_atomic_workspace_bytes.restype = ctypes.c_size_t
+    lib.tri_attn_bwd_atomic_ablation.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                                 vp, ctypes.c_size_t, vp]
+    lib.tri_attn_bwd_atomic_ablation.restype = ctypes.c_int
     return lib
 
 
@@ -181,6 +187,50 @@ def tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, workspace=None, ou
                                _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                                _stream_ptr(stream))
     _raise(code, "tri_attn_bwd")
+    return dq, dk, dv, dbias
+
+
+ATOMIC_DBIAS, ATOMIC_DBIAS_DQ = 2, 3
+
+
+def bwd_atomic_workspace_bytes(q_or_shape, atomic_mask: int) -> int:
+    """Workspace of the atomic ablation (0 for an invalid shape or mask)."""
+    s = q_or_shape if isinstance(q_or_shape, Shape) else shape_of(q_or_shape)
+    return int(load().triattn_bwd_atomic_workspace_bytes(ctypes.byref(s), int(atomic_mask)))
+
+
+def tri_attn_bwd_atomic_ablation(q, k, v, bias, mask, o, o_resid, lse, do, atomic_mask=ATOMIC_DBIAS_DQ, *,
+                                 workspace=None, out=None, stream=None):
+    """Ablation only (not the library's backward): the backward with FP32
+    atomics for dbias (``atomic_mask=2``) or for dbias and dQ (3) instead of
+    the ordered single-writer partials.  dQ / dbias are not bitwise
+    reproducible between calls.  Returns (dq, dk, dv, dbias) in bf16."""
+    s = shape_of(q)
+    B, No, H, N, D = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(t, name, (B, No, H, N, D))
+    if o_resid is not None:
+        _check(o_resid, "o_resid", (B, No, H, N, D))
+    _check(bias, "bias", (B, H, N, N))
+    _check(lse, "lse", (B, No, H, N), torch.float32)
+    if mask is not None:
+        _check(mask, "mask", (B, No, N))
+    need = bwd_atomic_workspace_bytes(s, atomic_mask)
+    if need == 0:
+        raise TriAttnError(ERR_INVALID_ARG, "tri_attn_bwd_atomic_ablation")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        dbias = torch.empty_like(bias)
+    else:
+        dq, dk, dv, dbias = out
+    code = load().tri_attn_bwd_atomic_ablation(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(mask),
+                                               _ptr(o), _ptr(o_resid), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                               _ptr(dv), _ptr(dbias), int(atomic_mask), _ptr(workspace),
+                                               ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                               _stream_ptr(stream))
+    _raise(code, "tri_attn_bwd_atomic_ablation")
     return dq, dk, dv, dbias
 
 

@@ -21,11 +21,13 @@
  *             bias, dbias                         [B, H, N, N]      bf16
  *             mask (optional, additive)           [B, N_o, N]       bf16
  *             lse                                 [B, N_o, H, N]    fp32 (natural log)
- *  - N_o must equal N (Table 1: "N_o = N"), D must be 16 or 32, and N must
- *    be a multiple of 8 with 8 <= N <= 4096 (TMA needs 16-byte row strides
- *    of the [N, N] bias; the forward stages the key mask of every key tile
- *    in shared memory).  Any N in that set works, ragged or not relative to
- *    the 128-row tiles.
+ *  - The method has N_o = N outer slices (Table 1); a call may also take a
+ *    contiguous shard of them (one GPU's part when the outer axis is split
+ *    across GPUs): 8 <= N_o <= N with N_o a multiple of 8.  D must be 16 or
+ *    32, and N a multiple of 8 with 8 <= N <= 4096 (TMA needs 16-byte row
+ *    strides of the [N, N] bias; the forward stages the key mask of every
+ *    key tile in shared memory).  Any N in that set works, ragged or not
+ *    relative to the 128-row tiles.
  *  - A row whose keys are all masked (every score -inf) yields O = 0,
  *    residual 0, lse = -inf and zero gradient contributions.
  *  - The caller owns every buffer, the workspace and the stream.  The library
@@ -51,12 +53,22 @@ extern "C" {
 
 typedef struct {
   int B;          /* examples */
-  int N_o;        /* outer slices; must equal N */
+  int N_o;        /* outer slices: N, or a shard (multiple of 8, <= N) */
   int N;          /* tokens per crop (queries = keys = N) */
   int H;          /* heads */
   int D;          /* features per head: 16 or 32 */
-  unsigned flags; /* reserved, must be 0 */
+  unsigned flags; /* 0, or TRIATTN_FLAG_DBIAS_FP32 (backward only) */
 } triattn_shape;
+
+/*
+ * Backward flag: write dbias as FP32 [B, H, N, N] (the FP32 sum over this
+ * call's outer slices, not rounded) instead of BF16.  Used when the outer
+ * axis is split across GPUs: every GPU's FP32 dbias is gathered and
+ * tri_attn_dbias_combine() adds them in rank order and rounds once.  Other
+ * flag bits are rejected with TRIATTN_ERR_INVALID_ARG; the forward accepts
+ * and ignores this one.
+ */
+#define TRIATTN_FLAG_DBIAS_FP32 1u
 
 typedef enum {
   TRIATTN_OK = 0,
@@ -196,6 +208,17 @@ triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape,
                                             int atomic_mask,
                                             void* workspace, size_t workspace_bytes,
                                             void* stream);
+
+/*
+ * dbias of an outer axis split across R GPUs: dbias = bf16(sum over r of
+ * parts[r]), the FP32 additions in ascending r (so the result is bitwise
+ * reproducible and independent of how the parts were gathered).  `parts` is
+ * [R][B, H, N, N] FP32 (each part written by tri_attn_bwd with
+ * TRIATTN_FLAG_DBIAS_FP32 on its shard), `dbias` [B, H, N, N] BF16; the
+ * shape's N_o and flags are not used.  R < 1 returns TRIATTN_ERR_INVALID_ARG.
+ */
+triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* parts, int R, void* dbias,
+                                      void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word that

@@ -54,9 +54,12 @@ triattn_status init_device(int* dev_out) {
 
 triattn_status check_shape(const triattn_shape* s) {
   if (s == nullptr) return TRIATTN_ERR_INVALID_ARG;
-  if (s->B < 1 || s->N < 1 || s->N_o < 1 || s->H < 1 || s->flags != 0) return TRIATTN_ERR_INVALID_ARG;
+  if (s->B < 1 || s->N < 1 || s->N_o < 1 || s->H < 1 || (s->flags & ~TRIATTN_FLAG_DBIAS_FP32) != 0)
+    return TRIATTN_ERR_INVALID_ARG;
   if (s->D != 16 && s->D != 32) return TRIATTN_ERR_UNSUPPORTED;
-  if (s->N_o != s->N) return TRIATTN_ERR_UNSUPPORTED;
+  // N outer slices, or a shard of them: whole groups of 8 (both backward
+  // group sizes divide it)
+  if (s->N_o > s->N || s->N_o % 8 != 0) return TRIATTN_ERR_UNSUPPORTED;
   // TMA row strides of the [N, N] bias must be multiples of 16 bytes.
   if (s->N % 8 != 0) return TRIATTN_ERR_UNSUPPORTED;
   // grid limits: outer groups in gridDim.y, B*H in gridDim.z
@@ -124,10 +127,13 @@ WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
 }
 
 // ---------------------------------------------------------------- tracing
-enum KernelKind { kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKinds };
+enum KernelKind {
+  kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine, kKinds
+};
 const char* const kKernelName[kKinds] = {"tri_attn_fwd",     "bwd_preprocess",  "bwd_transpose_bias",
                                          "bwd_main",         "bwd_reduce_dq",   "bwd_reduce_dbias",
-                                         "bwd_main_atomic",  "bwd_finish_dq",   "bwd_finish_dbias"};
+                                         "bwd_main_atomic",  "bwd_finish_dq",   "bwd_finish_dbias",
+                                         "dbias_combine"};
 struct TraceRec {
   int kind;
   cudaEvent_t a, b;
@@ -220,6 +226,7 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
   a.N = shape->N;
   a.H = shape->H;
   a.D = shape->D;
+  a.dbias_fp32 = (shape->flags & TRIATTN_FLAG_DBIAS_FP32) ? 1 : 0;
   a.wc = wait_ctl(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool d32 = shape->D == 32;
@@ -315,8 +322,23 @@ triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape, const vo
                                             void* dbias, int atomic_mask, void* workspace, size_t workspace_bytes,
                                             void* stream) {
   if (atomic_mask != 2 && atomic_mask != 3) return TRIATTN_ERR_INVALID_ARG;
+  if (shape != nullptr && shape->flags != 0) return TRIATTN_ERR_INVALID_ARG;
   return bwd_impl(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, atomic_mask, workspace,
                   workspace_bytes, stream);
+}
+
+triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* parts, int R, void* dbias,
+                                      void* stream) {
+  if (shape == nullptr || R < 1 || parts == nullptr || dbias == nullptr || !aligned16(parts) || !aligned16(dbias))
+    return TRIATTN_ERR_INVALID_ARG;
+  if (shape->B < 1 || shape->H < 1 || shape->N < 1 || shape->N % 8 != 0) return TRIATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  triattn_status st = init_device(&dev);
+  if (st != TRIATTN_OK) return st;
+  const size_t elems = static_cast<size_t>(shape->B) * shape->H * shape->N * shape->N;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = traced(kKCombine, s, [&] { return launch_dbias_combine(parts, R, elems, dbias, s); });
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
 }
 
 triattn_status triattn_device_status(void* stream) {

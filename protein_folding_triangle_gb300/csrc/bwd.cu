@@ -10,6 +10,8 @@
 //                and one dbias partial per outer group, each single-writer;
 //   Figure 11(a) ("materialized partials"): separate kernels add the
 //                partials in ascending index order in FP32.
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace triattn {
@@ -756,13 +758,17 @@ __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict
 // to the end (16-query slabs left the last wave ragged).
 constexpr int kSlab = 8;
 constexpr int kRedThreads = kSlab / 4 * BN;  // one float4 chunk per thread
+// OutT = uint16_t: BF16 dbias; float: the FP32 sum itself (one GPU's part of
+// an outer axis split across GPUs).
+template <typename OutT>
 __global__ void __launch_bounds__(kRedThreads) reduce_dbias_kernel(const float4* __restrict__ part,
-                                                           uint16_t* __restrict__ dbias, int N, int JQ, int JK,
+                                                           OutT* __restrict__ dbias, int N, int JQ, int JK,
                                                            int ngroups, size_t tiles) {
+  constexpr bool kF32 = sizeof(OutT) == 4;
   constexpr int kChunks = BM * BN / 4;     // float4 per tile
   constexpr int kSlabChunks = kSlab / 4 * BN;
-  constexpr int kStride = BN + 8;          // padded row stride (bf16) of the transpose buffer
-  __shared__ __align__(16) uint16_t tile[kSlab * kStride];
+  constexpr int kStride = BN + 16 / sizeof(OutT);  // padded row stride of the transpose buffer
+  __shared__ __align__(16) OutT tile[kSlab * kStride];
   const size_t t = blockIdx.x / (BM / kSlab);
   const int slab = blockIdx.x % (BM / kSlab);
   const int kt = static_cast<int>(t % JK);
@@ -792,19 +798,44 @@ __global__ void __launch_bounds__(kRedThreads) reduce_dbias_kernel(const float4*
       acc.z += v.z;
       acc.w += v.w;
     }
-    const uint32_t w01 = pack_bf16x2(acc.x, acc.y), w23 = pack_bf16x2(acc.z, acc.w);
-    tile[(4 * cl + 0) * kStride + k] = static_cast<uint16_t>(w01 & 0xFFFFu);
-    tile[(4 * cl + 1) * kStride + k] = static_cast<uint16_t>(w01 >> 16);
-    tile[(4 * cl + 2) * kStride + k] = static_cast<uint16_t>(w23 & 0xFFFFu);
-    tile[(4 * cl + 3) * kStride + k] = static_cast<uint16_t>(w23 >> 16);
+    if constexpr (kF32) {
+      tile[(4 * cl + 0) * kStride + k] = acc.x;
+      tile[(4 * cl + 1) * kStride + k] = acc.y;
+      tile[(4 * cl + 2) * kStride + k] = acc.z;
+      tile[(4 * cl + 3) * kStride + k] = acc.w;
+    } else {
+      const uint32_t w01 = pack_bf16x2(acc.x, acc.y), w23 = pack_bf16x2(acc.z, acc.w);
+      tile[(4 * cl + 0) * kStride + k] = static_cast<uint16_t>(w01 & 0xFFFFu);
+      tile[(4 * cl + 1) * kStride + k] = static_cast<uint16_t>(w01 >> 16);
+      tile[(4 * cl + 2) * kStride + k] = static_cast<uint16_t>(w23 & 0xFFFFu);
+      tile[(4 * cl + 3) * kStride + k] = static_cast<uint16_t>(w23 >> 16);
+    }
   }
   __syncthreads();
-  constexpr int kItems = kSlab * BN / 8;   // 16-byte items
+  constexpr int kPer = 16 / sizeof(OutT);  // elements per 16-byte item
+  constexpr int kItems = kSlab * BN / kPer;
   for (int e = threadIdx.x; e < kItems; e += blockDim.x) {
-    const int rr = e / (BN / 8), c8 = e % (BN / 8);
-    const int q = i * BM + slab * kSlab + rr, k = kt * BN + 8 * c8;
+    const int rr = e / (BN / kPer), c = e % (BN / kPer);
+    const int q = i * BM + slab * kSlab + rr, k = kt * BN + kPer * c;
     if (q >= N || k >= N) continue;        // N is a multiple of 8: an item is all in or all out
-    *reinterpret_cast<uint4*>(dbias + (bh * N + q) * N + k) = *reinterpret_cast<const uint4*>(&tile[rr * kStride + 8 * c8]);
+    *reinterpret_cast<uint4*>(dbias + (bh * N + q) * N + k) = *reinterpret_cast<const uint4*>(&tile[rr * kStride + kPer * c]);
+  }
+}
+
+// dbias = bf16(sum_r parts[r]) in ascending r, four elements per thread.
+__global__ void __launch_bounds__(256) dbias_combine_kernel(const float4* __restrict__ parts, int R, size_t n4,
+                                                            uint2* __restrict__ dbias) {
+  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float4 acc = __ldcs(parts + e);
+    for (int r = 1; r < R; ++r) {
+      const float4 v = __ldcs(parts + static_cast<size_t>(r) * n4 + e);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    dbias[e] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
 }
 
@@ -937,9 +968,23 @@ cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
   const size_t tiles = static_cast<size_t>(a.B) * a.H * JQ * JK;
-  reduce_dbias_kernel<<<static_cast<unsigned>(tiles * (BM / kSlab)), kRedThreads, 0, stream>>>(
-      reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK,
-      a.N_o / kGroupBwdFor(a.D), tiles);
+  const unsigned blocks = static_cast<unsigned>(tiles * (BM / kSlab));
+  if (a.dbias_fp32)
+    reduce_dbias_kernel<float><<<blocks, kRedThreads, 0, stream>>>(
+        reinterpret_cast<const float4*>(a.dbias_part), static_cast<float*>(a.dbias), a.N, JQ, JK,
+        a.N_o / kGroupBwdFor(a.D), tiles);
+  else
+    reduce_dbias_kernel<uint16_t><<<blocks, kRedThreads, 0, stream>>>(
+        reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK,
+        a.N_o / kGroupBwdFor(a.D), tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dbias_combine(const float* parts, int R, size_t elems, void* dbias, cudaStream_t stream) {
+  const size_t n4 = elems / 4;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
+  dbias_combine_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(parts), R, n4,
+                                                   static_cast<uint2*>(dbias));
   return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@ struct BwdArgs {
   float* dq_part;    // [J_K][slices][J_Q][128 x D]
   float* dbias_part; // [L][B*H*N*N]
   int B, N_o, N, H, D;
+  int dbias_fp32;    // write dbias as FP32 (the sum over this call's slices)
   WaitCtl wc;
 };
 
@@ -66,5 +67,7 @@ template <int D> int bwd_smem_bytes();
 template <int D> cudaError_t launch_bwd_main_atomic(const BwdArgs& a, int atomic_mask, cudaStream_t stream);
 template <int D> cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_finish_dbias(const BwdArgs& a, cudaStream_t stream);
+// dbias = bf16(sum over r of parts[r]) in ascending r (outer axis split across GPUs).
+cudaError_t launch_dbias_combine(const float* parts, int R, size_t elems, void* dbias, cudaStream_t stream);
 
 }  // namespace triattn

@@ -33,7 +33,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = ran
 EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fwd", "tri_attn_bwd",
             "triattn_device_status", "triattn_set_wait_limit_ns", "triattn_trace_enable", "triattn_trace_read",
             "triattn_test_set_starve", "tri_attn_bwd_noalloc", "triattn_bwd_atomic_workspace_bytes",
-            "tri_attn_bwd_atomic_ablation")
+            "tri_attn_bwd_atomic_ablation", "tri_attn_dbias_combine")
+
+FLAG_DBIAS_FP32 = 1
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -81,6 +83,8 @@ def _declare(lib):
     lib.tri_attn_bwd_atomic_ablation.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                                  vp, ctypes.c_size_t, vp]
     lib.tri_attn_bwd_atomic_ablation.restype = ctypes.c_int
+    lib.tri_attn_dbias_combine.argtypes = [sp, vp, ctypes.c_int, vp, vp]
+    lib.tri_attn_dbias_combine.restype = ctypes.c_int
     return lib
 
 
@@ -161,10 +165,14 @@ def tri_attn_fwd(q, k, v, bias, mask=None, *, save_residual: bool = True, out=No
     return o, lse, resid
 
 
-def tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, workspace=None, out=None, stream=None):
+def tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, workspace=None, out=None, stream=None,
+                 dbias_fp32: bool = False):
     """Backward.  ``o_resid=None`` turns the residual compensation off.
-    Returns (dq, dk, dv, dbias) in bf16."""
+    Returns (dq, dk, dv, dbias) in bf16; with ``dbias_fp32`` dbias is the FP32
+    sum over this call's outer slices (a shard's part, see tri_attn_dbias_combine)."""
     s = shape_of(q)
+    if dbias_fp32:
+        s.flags = FLAG_DBIAS_FP32
     B, No, H, N, D = q.shape
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check(t, name, (B, No, H, N, D))
@@ -179,9 +187,10 @@ def tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, workspace=None, ou
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-        dbias = torch.empty_like(bias)
+        dbias = torch.empty(bias.shape, dtype=torch.float32 if dbias_fp32 else torch.bfloat16, device=q.device)
     else:
         dq, dk, dv, dbias = out
+    _check(dbias, "dbias", tuple(bias.shape), torch.float32 if dbias_fp32 else torch.bfloat16)
     code = load().tri_attn_bwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(mask), _ptr(o),
                                _ptr(o_resid), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
                                _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
@@ -232,6 +241,24 @@ def tri_attn_bwd_atomic_ablation(q, k, v, bias, mask, o, o_resid, lse, do, atomi
                                                _stream_ptr(stream))
     _raise(code, "tri_attn_bwd_atomic_ablation")
     return dq, dk, dv, dbias
+
+
+def tri_attn_dbias_combine(parts, *, out=None, stream=None):
+    """dbias of an outer axis split across GPUs: ``parts`` is [R, B, H, N, N]
+    FP32 (each written by tri_attn_bwd(..., dbias_fp32=True) on one shard,
+    gathered in rank order); returns bf16 [B, H, N, N], the parts added in
+    ascending r in FP32 and rounded once."""
+    if parts.dim() != 5 or parts.dtype != torch.float32 or not parts.is_cuda or not parts.is_contiguous():
+        raise ValueError("parts must be a contiguous CUDA float32 tensor [R, B, H, N, N]")
+    R, B, H, N, N2 = parts.shape
+    if N != N2:
+        raise ValueError("parts must be [R, B, H, N, N]")
+    s = Shape(B, N, N, H, 16, 0)
+    dbias = out if out is not None else torch.empty((B, H, N, N), dtype=torch.bfloat16, device=parts.device)
+    _check(dbias, "dbias", (B, H, N, N))
+    code = load().tri_attn_dbias_combine(ctypes.byref(s), _ptr(parts), int(R), _ptr(dbias), _stream_ptr(stream))
+    _raise(code, "tri_attn_dbias_combine")
+    return dbias
 
 
 def device_status(stream=None) -> int:

@@ -64,13 +64,14 @@ def call_bwd(lib, shape, ws_bytes, ws=FAKE, **ptrs):
 
 @pytest.mark.parametrize("shape,code", [
     ((1, 48, 48, 2, 24, 0), T.ERR_UNSUPPORTED),   # D not in {16, 32}
-    ((1, 40, 48, 2, 16, 0), T.ERR_UNSUPPORTED),   # N_o != N
+    ((1, 44, 48, 2, 16, 0), T.ERR_UNSUPPORTED),   # outer shard not a multiple of 8
+    ((1, 56, 48, 2, 16, 0), T.ERR_UNSUPPORTED),   # more outer slices than N
     ((1, 44, 44, 2, 16, 0), T.ERR_UNSUPPORTED),   # N not a multiple of 8
     ((1, 8192, 8192, 1, 16, 0), T.ERR_UNSUPPORTED),  # N beyond 4096
     ((0, 48, 48, 2, 16, 0), T.ERR_INVALID_ARG),   # empty batch
     ((1, 0, 0, 2, 16, 0), T.ERR_INVALID_ARG),     # empty crop
     ((1, 48, 48, 0, 16, 0), T.ERR_INVALID_ARG),   # no heads
-    ((1, 48, 48, 2, 16, 1), T.ERR_INVALID_ARG),   # reserved flags
+    ((1, 48, 48, 2, 16, 2), T.ERR_INVALID_ARG),   # unknown flag bit
 ])
 def test_bad_shapes(lib, shape, code):
     s = T.Shape(*shape)
@@ -162,3 +163,81 @@ def test_atomic_ablation_workspace_and_mask_checks(lib):
         fake = ctypes.c_void_p(1 << 40)
         args = [ctypes.byref(s)] + [fake] * 13 + [bad, fake, ctypes.c_size_t(1 << 40), None]
         assert lib.tri_attn_bwd_atomic_ablation(*args) == T.ERR_INVALID_ARG
+
+
+def test_outer_shard_ranges():
+    from protein_folding_triangle_gb300.sharding import outer_shard
+    for n, world in ((768, 1), (768, 2), (768, 3), (768, 8), (200, 3), (48, 6), (8, 1)):
+        ranges = [outer_shard(n, r, world) for r in range(world)]
+        assert ranges[0][0] == 0 and ranges[-1][1] == n
+        for (lo, hi), (lo2, _) in zip(ranges, ranges[1:]):
+            assert hi == lo2
+        sizes = [hi - lo for lo, hi in ranges]
+        assert all(sz % 8 == 0 and sz >= 8 for sz in sizes) and max(sizes) - min(sizes) <= 8
+    with pytest.raises(ValueError):
+        outer_shard(44, 0, 1)
+    with pytest.raises(ValueError):
+        outer_shard(16, 0, 3)
+
+
+def test_shard_shapes_accepted(lib):
+    """A shard of the outer axis (N_o < N, a multiple of 8) is a valid shape;
+    its workspace counts only its own slices and groups."""
+    full = T.Shape(1, 48, 48, 2, 32, 0)
+    half = T.Shape(1, 24, 48, 2, 32, T.FLAG_DBIAS_FP32)
+    wf = lib.triattn_bwd_workspace_bytes(ctypes.byref(full))
+    wh = lib.triattn_bwd_workspace_bytes(ctypes.byref(half))
+    assert 0 < wh < wf
+
+
+def _combine_worker(rank, world, port, n_outer, q):
+    """One rank of a 2-rank gloo group: the FP64 oracle's dbias of its shard,
+    kept in FP32, gathered in rank order, then summed in rank order."""
+    import numpy as np
+    import torch.distributed as dist
+    from oracle import oracle as O
+    from protein_folding_triangle_gb300 import synthetic as S
+    from protein_folding_triangle_gb300.sharding import gather_rank_ordered, outer_shard
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = S.custom(1, n_outer, 2, 16, name="shard", mask="random", mask_frac=0.1)
+        x = S.make_inputs(w, seed=5)
+        lo, hi = outer_shard(n_outer, rank, world)
+        sh = {k: (None if v is None else (v if k == "bias" else v[:, lo:hi].contiguous())) for k, v in x.items()}
+        _, _, _, db = O.bwd(sh["q"], sh["k"], sh["v"], sh["bias"], sh["mask"], sh["do"])
+        parts = gather_rank_ordered(torch.from_numpy(db.astype(np.float32)))
+        total = parts[0].clone()
+        for r in range(1, world):
+            total += parts[r]
+        if rank == 0:
+            _, _, _, ref = O.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["do"])
+            err = float(np.sqrt(np.mean((total.double().numpy() - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)))
+            q.put(("ok", err, [tuple(p.shape) for p in parts]))
+    except Exception as e:  # noqa: BLE001
+        q.put(("error", repr(e), None))
+        raise
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sharded_dbias_gather_two_gloo_ranks():
+    """The host side of the outer-axis split: two gloo ranks each own half of
+    the slices; their FP32 dbias parts, gathered in rank order and added,
+    give the full dbias (FP64 oracle on each shard vs on the whole axis)."""
+    import multiprocessing as mp
+    import socket
+    ctx = mp.get_context("spawn")
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_combine_worker, args=(r, 2, port, 24, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    status, err, shapes = q.get(timeout=240)
+    for p in procs:
+        p.join(timeout=60)
+    assert status == "ok", err
+    assert shapes == [(1, 2, 24, 24)] * 2
+    assert err < 1e-6, err

@@ -47,7 +47,7 @@ namespace {
 constexpr int BM = 128;     // query rows per tile (TMEM lanes)
 constexpr int BN = 64;      // keys per step
 constexpr int GF = 4;       // outer slices per CTA (share a bias tile)
-constexpr int NSLOT = 2;    // K ring and V ring depth per slice
+constexpr int NSLOT = 3;    // K ring and V ring depth per slice
 constexpr int NBIAS = 3;    // bias ring depth
 constexpr int kSoftmax = 128 * GF;      // softmax threads (one warpgroup per slice)
 constexpr int kThreads = 128 + kSoftmax;
@@ -72,11 +72,11 @@ struct FwdSmem {
   static constexpr int kV = kK + GF * NSLOT * kTileKV;       // GF x NSLOT V tiles
   static constexpr int kBias = kV + GF * NSLOT * kTileKV;    // NBIAS x [128 q][64 k] bf16, SW128
   static constexpr int kBar = kBias + NBIAS * BM * BN * 2;
-  static constexpr int kMask = kBar + 512;   // GF x (JK*64) fp32 key mask, GF x JK x 8 chunk flags, GF x JK tile flags
+  static constexpr int kMask = kBar + 1024;  // GF x (JK*64) bf16 key mask, GF x JK x 8 chunk flags, GF x JK tile flags
   static constexpr int kFixed = kMask + 1024;                // + slack for 1024-byte alignment
   static_assert(kBias % 1024 == 0, "bias tiles need 1024-byte alignment");
-  static constexpr int bytes(int JK) { return kFixed + GF * JK * (BN * 4 + BN / 8 + 1); }
-  static constexpr int kMaxJK = (232448 - kFixed) / (GF * (BN * 4 + BN / 8 + 1));
+  static constexpr int bytes(int JK) { return kFixed + GF * JK * (BN * 2 + BN / 8 + 1); }
+  static constexpr int kMaxJK = (232448 - kFixed) / (GF * (BN * 2 + BN / 8 + 1));
 };
 
 struct FwdBars {
@@ -88,7 +88,7 @@ struct FwdBars {
   uint32_t tmem_slot;
   int abort;
 };
-static_assert(sizeof(FwdBars) <= 512, "barrier block");
+static_assert(sizeof(FwdBars) <= 1024, "barrier block");
 
 }  // namespace
 
@@ -253,20 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
     const int nkeys = JK * BN;
-    float* mask2 = reinterpret_cast<float*>(sm + L::kMask);       // [GF][nkeys], natural units, -inf past N
-    uint8_t* mflag = sm + L::kMask + GF * nkeys * 4;              // [GF][JK*8]: 8-key chunk has a nonzero value
+    uint16_t* mask2 = reinterpret_cast<uint16_t*>(sm + L::kMask);  // [GF][nkeys] bf16, -inf past N
+    uint8_t* mflag = sm + L::kMask + GF * nkeys * 2;              // [GF][JK*8]: 8-key chunk has a nonzero value
     uint8_t* tflag = mflag + GF * JK * (BN / 8);                  // [GF][JK]: tile has a nonzero value
 
     // Key mask of the four slices and its chunk / tile flags, staged once,
     // before any bounded wait, so the barriers are always fully entered.
     for (int idx = ew; idx < GF * nkeys; idx += kSoftmax) {
       const int gg = idx / nkeys, key = idx - gg * nkeys;
-      float mv = -INFINITY;
+      uint16_t mv = 0xFF80u;  // -inf
       if (key < N) {
-        mv = 0.f;
-        if (mask != nullptr)
-          mv = __uint_as_float(static_cast<uint32_t>(__ldg(mask + (static_cast<size_t>(b) * N_o + o0 + gg) * N + key))
-                               << 16);
+        mv = 0;
+        if (mask != nullptr) mv = __ldg(mask + (static_cast<size_t>(b) * N_o + o0 + gg) * N + key);
       }
       mask2[idx] = mv;
     }
@@ -274,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = ew; idx < GF * JK * (BN / 8); idx += kSoftmax) {
       bool any = false;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) any |= (mask2[idx * 8 + e] != 0.f);
+      for (int e = 0; e < 8; ++e) any |= (mask2[idx * 8 + e] & 0x7FFFu) != 0;  // a nonzero value
       mflag[idx] = any ? 1 : 0;
     }
     named_bar_sync(1, kSoftmax);
@@ -326,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tiles keep the base and only look at the maximum when the row sum
       // of the tile exceeds 2^16 (some p > 2^16).
       const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
-      const float* mk = mask2 + g * nkeys + j * BN;
+      const uint16_t* mk = mask2 + (g * nkeys + j * BN);
       const bool tile_masked = tflag[g * JK + j] != 0;
       const bool exact = j == 0 || __any_sync(0xffffffffu, l_run == 0.f);
       const float2 nb2 = make_float2(-m_run * kLog2e, -m_run * kLog2e);
@@ -341,22 +339,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int cc = cc0 + c;
           const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + sw128(r, cc));
           const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
-          float2 mm[4];
-          if constexpr (MASKED) {
-            const float4 m0 = *reinterpret_cast<const float4*>(mk + cc * 8);
-            const float4 m1 = *reinterpret_cast<const float4*>(mk + cc * 8 + 4);
-            mm[0] = make_float2(m0.x, m0.y);
-            mm[1] = make_float2(m0.z, m0.w);
-            mm[2] = make_float2(m1.x, m1.y);
-            mm[3] = make_float2(m1.z, m1.w);
-          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k = c * 8 + 2 * e;
             const float2 s2 = make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
             const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
             float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nb2));
-            if constexpr (MASKED) t = ffma2(mm[e], l2e2, t);
+            if constexpr (MASKED) {  // the pair's two mask values, loaded where they are used
+              const uint32_t mw = *reinterpret_cast<const uint32_t*>(mk + cc * 8 + 2 * e);
+              t = ffma2(make_float2(bf16lo_to_f32(mw), bf16hi_to_f32(mw)), l2e2, t);
+            }
             if constexpr (WITH_MAX) tm = fmax3(tm, t.x, t.y);
             sv[k] = __float_as_uint(t.x);
             sv[k + 1] = __float_as_uint(t.y);

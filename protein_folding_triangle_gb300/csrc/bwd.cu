@@ -47,35 +47,39 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
                                                          const uint16_t* __restrict__ e,
                                                          const float* __restrict__ lse, uint4* __restrict__ rec,
                                                          int N, int JQ, size_t padded_rows) {
-  const size_t pr = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (slice * JQ + i) * 128 + qq
-  if (pr >= padded_rows) return;
+  // One 16-byte chunk (8 features) of one row per thread, so that a warp's
+  // loads cover consecutive rows contiguously; the D/8 lanes of a row add
+  // their partial sums with a fixed butterfly.
+  constexpr int kCpr = D / 8;  // chunks per row
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t pr = t / kCpr;  // (slice * JQ + i) * 128 + qq
+  const int c = static_cast<int>(t % kCpr);
   const size_t tile = pr / BM;
   const int qq = static_cast<int>(pr % BM);
   const int i = static_cast<int>(tile % JQ);
   const size_t slice = tile / JQ;
   const int q = i * BM + qq;
+  const bool live = pr < padded_rows && q < N;
   float xs = -1e30f, acc = 0.f;
-  if (q < N) {
+  if (live) {
     const size_t row = slice * N + q;
-    const uint4* gp = reinterpret_cast<const uint4*>(dO + row * D);
-    const uint4* op = reinterpret_cast<const uint4*>(o + row * D);
-    const uint4* ep = e ? reinterpret_cast<const uint4*>(e + row * D) : nullptr;
+    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(dO + row * D) + c);
+    const uint4 ow = __ldg(reinterpret_cast<const uint4*>(o + row * D) + c);
+    uint4 ew = make_uint4(0, 0, 0, 0);
+    if (e != nullptr) ew = __ldg(reinterpret_cast<const uint4*>(e + row * D) + c);
+    const uint32_t g4[4] = {gw.x, gw.y, gw.z, gw.w}, o4[4] = {ow.x, ow.y, ow.z, ow.w},
+                   e4[4] = {ew.x, ew.y, ew.z, ew.w};
 #pragma unroll
-    for (int v = 0; v < D / 8; ++v) {
-      const uint4 gw = __ldg(gp + v), ow = __ldg(op + v);
-      uint4 ew = make_uint4(0, 0, 0, 0);
-      if (ep) ew = __ldg(ep + v);
-      const uint32_t g4[4] = {gw.x, gw.y, gw.z, gw.w}, o4[4] = {ow.x, ow.y, ow.z, ow.w},
-                     e4[4] = {ew.x, ew.y, ew.z, ew.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc = fmaf(bf16lo_to_f32(g4[u]), bf16lo_to_f32(o4[u]) + bf16lo_to_f32(e4[u]), acc);
-        acc = fmaf(bf16hi_to_f32(g4[u]), bf16hi_to_f32(o4[u]) + bf16hi_to_f32(e4[u]), acc);
-      }
+    for (int u = 0; u < 4; ++u) {
+      acc = fmaf(bf16lo_to_f32(g4[u]), bf16lo_to_f32(o4[u]) + bf16lo_to_f32(e4[u]), acc);
+      acc = fmaf(bf16hi_to_f32(g4[u]), bf16hi_to_f32(o4[u]) + bf16hi_to_f32(e4[u]), acc);
     }
     const float l = __ldg(lse + row);
     if (l != -INFINITY) xs = -l * sqrtf(static_cast<float>(D));
   }
+#pragma unroll
+  for (int off = kCpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (pr >= padded_rows || c != 0) return;
   // three-term BF16 splits: v = h + m + lo to about 24 significant bits
   auto split3 = [](float v, uint32_t& w01, uint32_t& w2) {
     const uint32_t h = pack_bf16x2(v, 0.f) & 0xFFFFu;
@@ -902,7 +906,7 @@ template <int D>
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
   const int JQ = (a.N + BM - 1) / BM;
   const size_t padded = static_cast<size_t>(a.B) * a.N_o * a.H * JQ * BM;
-  const unsigned grid = static_cast<unsigned>((padded + 255) / 256);
+  const unsigned grid = static_cast<unsigned>((padded * (D / 8) + 255) / 256);
   preprocess_kernel<D><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(a.dO), static_cast<const uint16_t*>(a.o),
                                                  static_cast<const uint16_t*>(a.o_resid), a.lse, a.rec, a.N, JQ,
                                                  padded);

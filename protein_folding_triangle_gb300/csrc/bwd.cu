@@ -292,9 +292,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTDQ;
     const float isd = rsqrtf(static_cast<float>(D));
     uint32_t qr[D];
-    if constexpr (D == 32) tmem_ld32(taddr, qr);
-    else tmem_ld16(taddr, qr);
-    tc_wait_ld_regs(qr);
+    if constexpr (D == 32) tmem_ld32_wait(taddr, qr);
+    else tmem_ld16_wait(taddr, qr);
     if constexpr ((kAtomic & 1) != 0) {
       float* acc = dq_part + ((slice * JQ + ti) * BM + r) * D;
 #pragma unroll
@@ -576,8 +575,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       uint32_t pw[kCols / 2];
       {
         uint32_t sv[kCols];
-        tmem_ld32(tmem + lane_addr + kTS + col0, sv);
-        tc_wait_ld_regs(sv);
+        tmem_ld32_wait(tmem + lane_addr + kTS + col0, sv);
         tc_fence_before();
         mbar_arrive(&bars->s_cons);
         const float m = mask_s[g * BN + r];  // 0 for most keys, -inf for masked keys and keys past N
@@ -620,9 +618,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {  // 16 queries at a time
         uint32_t a[8], bq[8];
-        tmem_ld8(tmem + lane_addr + kTDP + col0 + hh * 16, a);
-        tmem_ld8(tmem + lane_addr + kTDP + col0 + hh * 16 + 8, bq);
-        tc_wait_ld_regs(a, bq);
+        tmem_ld8x2_wait(tmem + lane_addr + kTDP + col0 + hh * 16, a, tmem + lane_addr + kTDP + col0 + hh * 16 + 8, bq);
         uint32_t dw[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -683,15 +679,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t w[D / 2];
         if constexpr (D == 32) {
           uint32_t raw[32];
-          tmem_ld32(t, raw);
-          tc_wait_ld();
+          tmem_ld32_wait(t, raw);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]) * sc, __uint_as_float(raw[2 * e + 1]) * sc);
         } else {
           uint32_t raw[16];
-          tmem_ld16(t, raw);
-          tc_wait_ld();
+          tmem_ld16_wait(t, raw);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]) * sc, __uint_as_float(raw[2 * e + 1]) * sc);

@@ -304,10 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the tile's 64 scores into registers; the score columns are free again
       // sv0 holds keys [0, 32), sv1 keys [32, 64)
       uint32_t sv0[32], sv1[32];
-      tmem_ld32(tS, sv0);
-      tmem_ld32(tS + 32, sv1);
-      tc_wait_ld_regs(sv0);
-      tc_wait_ld_regs(sv1);
+      tmem_ld32x2_wait(tS, sv0, tS + 32, sv1);
       tc_fence_before();
       mbar_arrive(&bars->s_cons[g]);
 
@@ -412,8 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 16) {
             uint32_t ov[16];
-            tmem_ld16(tO + c0, ov);
-            tc_wait_ld_regs(ov);
+            tmem_ld16_wait(tO + c0, ov);
 #pragma unroll
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * a);
             tmem_st16(tO + c0, ov);
@@ -459,14 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_addr + 128 * g + kTO;
         if constexpr (D == 32) {
           uint32_t raw[32];
-          tmem_ld32(tO, raw);
-          tc_wait_ld();
+          tmem_ld32_wait(tO, raw);
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(raw[e]);
         } else {
           uint32_t raw[16];
-          tmem_ld16(tO, raw);
-          tc_wait_ld();
+          tmem_ld16_wait(tO, raw);
 #pragma unroll
           for (int e = 0; e < 16; ++e) ov[e] = __uint_as_float(raw[e]);
         }

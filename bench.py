@@ -431,6 +431,19 @@ def run_ours(args):
                                                 "bwd_reduce_dbias")
                  if n in trace)
     clocks = clk.summary()
+    # Secondary ceiling of the two main kernels: the exponentials of the
+    # softmax (one exp2 per score in each) on the MUFU pipe, 32 per clock per
+    # SM (measured on GB300), at the SM clock sampled during the timed region.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+    mufu_peak = 32.0 * sms * mhz * 1e6
+    scores = w.B * w.No * w.H * w.N * w.N
+    secondary = {"bound": "mufu", "unit": "exp2/s", "peak": mufu_peak,
+                 "peak_source": f"32 exp2 per clock per SM x {sms} SMs x {mhz} MHz"}
+    for name in ("tri_attn_fwd", "bwd_main"):
+        if name in trace:
+            rate = scores / (trace[name]["mean_ms"] * 1e-3)
+            secondary[name] = {"achieved": rate, "frac": round(rate / mufu_peak, 4)}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -446,6 +459,7 @@ def run_ours(args):
         "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{pk['source']} ({'bf16 sustained' if unit == 'flop' else 'hbm copy'})"},
+        "secondary": secondary,
         "kernels": kernels,
         "gpu_launches": sum(e["launches"] for e in trace.values()),
         "peak_mem_bytes": int(peak_mem),

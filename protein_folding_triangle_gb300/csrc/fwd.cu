@@ -213,8 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j + 1 < JK) {
         for (int g = g0; g < GF; g += 2) {
           // S(j) of slice g is in registers; K(j+1) loaded
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_cons[g], j & 1, wc, abort)) ||
-              !__all_sync(0xffffffffu, mbar_wait(&bars->k_full[g][slot1], ((j + 1) / NSLOT) & 1, wc, abort))) {
+          const uint32_t wb[2] = {smem_u32(&bars->s_cons[g]), smem_u32(&bars->k_full[g][slot1])};
+          const uint32_t wp[2] = {static_cast<uint32_t>(j & 1), static_cast<uint32_t>(((j + 1) / NSLOT) & 1)};
+          if (!mbar_wait_all(wb, wp, wc, abort)) {
             ok = false;
             break;
           }
@@ -225,8 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int g = g0; g < GF; g += 2) {
         // P(j) of slice g in TMEM; V(j) loaded
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[g], j & 1, wc, abort)) ||
-            !__all_sync(0xffffffffu, mbar_wait(&bars->v_full[g][slot], (j / NSLOT) & 1, wc, abort))) {
+        const uint32_t wb[2] = {smem_u32(&bars->p_full[g]), smem_u32(&bars->v_full[g][slot])};
+        const uint32_t wp[2] = {static_cast<uint32_t>(j & 1), static_cast<uint32_t>((j / NSLOT) & 1)};
+        if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
           break;
         }
@@ -295,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < JK && ok; ++j) {
       const int bst = j % NBIAS;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->b_full[bst], (j / NBIAS) & 1, wc, abort)) ||
-          !__all_sync(0xffffffffu, mbar_wait(&bars->s_full[g], j & 1, wc, abort))) {
+      const uint32_t wb[2] = {smem_u32(&bars->b_full[bst]), smem_u32(&bars->s_full[g])};
+      const uint32_t wp[2] = {static_cast<uint32_t>((j / NBIAS) & 1), static_cast<uint32_t>(j & 1)};
+      if (!mbar_wait_all(wb, wp, wc, abort)) {
         ok = false;
         break;
       }

@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--ablation", choices=["atomic"], default=None,
                     help="instead of the bench line: time the ordered backward against its non-deterministic "
                          "FP32-atomic variants (dbias; dbias and dQ) on the same inputs and print one JSON line")
+    ap.add_argument("--module", type=int, default=0, metavar="C",
+                    help="instead of the bench line: time the whole module (LayerNorm, projections with C pair "
+                         "features, the core, output projection; forward + backward) and print one JSON line")
     return ap.parse_args()
 
 
@@ -538,8 +541,98 @@ def run_atomic_ablation(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- module
+def run_module(args):
+    """Forward + backward of the module around the core on the workload's
+    shape with ``--module`` pair features: CUDA events around each step on the
+    launching stream, then one traced step for the per-kernel split.  The
+    module's own kernels are HBM-bound; their algorithmic bytes per step are
+    counted below from the tensors each one must read and write once."""
+    import statistics
+    import torch
+    from protein_folding_triangle_gb300 import build as B
+    from protein_folding_triangle_gb300 import synthetic as S
+    from protein_folding_triangle_gb300 import triattn as T
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    B.build()
+    T.load()
+    dev = torch.device("cuda", 0)
+    w = S.WORKLOADS[args.workload]
+    C, H, D, N, Bn = args.module, w.H, w.D, w.N, w.B
+    x = S.make_module_inputs(Bn, N, C, H, D, seed=args.seed, mask_frac=w.mask_frac if w.mask != "none" else 0.0)
+    xd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    nctx, nws = T.module_sizes(Bn, N, C, H, D)
+    ctx = torch.empty(nctx, dtype=torch.uint8, device=dev)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(xd["z"])
+    F = 3 * H * D + H
+    f32 = dict(dtype=torch.float32, device=dev)
+    grads = (torch.empty_like(xd["z"]), torch.empty(C, **f32), torch.empty(C, **f32), torch.empty((C, F), **f32),
+             torch.empty((H * D, C), **f32))
+
+    def step():
+        T.tri_attn_module_fwd(xd["z"], xd["mask"], xd["ln_w"], xd["ln_b"], xd["w_in"], xd["w_o"], H, D, ctx=ctx,
+                              workspace=ws, out=out)
+        T.tri_attn_module_bwd(xd["z"], xd["mask"], xd["ln_w"], xd["w_in"], xd["w_o"], ctx, xd["d_out"], H, D,
+                              workspace=ws, out=grads)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    times = []
+    with ClockSampler(0) as clk:
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            step()
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+    T.trace_enable(True)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    tr = T.trace_read()
+    T.trace_enable(False)
+    if T.device_status() != T.OK:
+        raise SystemExit("device status not OK after the module bench")
+    M, HD = Bn * N * N, H * D
+    act = Bn * N * H * N * D * 2
+    fl_core = flops(w)[2]
+    gemm_flop = 3 * (2 * M * C * F + 2 * M * HD * C)  # forward, then dX and dW of each projection
+    by = {"module_ln_fwd": M * C * 4 + M * 8,             # z in, x out, mean and rstd
+          "module_ln_bwd": M * C * 8 + M * 8,             # z, dx (FP32) in, dz out, mean and rstd
+          "module_layout": 2 * (7 * act + 2 * Bn * H * N * N * 2)}  # q k v o / do dq dk dv, bias and dbias planes
+    pk = peaks()
+    per = {}
+    for name, e in tr.items():
+        ms = e["total_ms"] / 3.0
+        d = {"ms_per_step": round(ms, 4), "launches_per_step": e["launches"] // 3}
+        if name in by:
+            d["GB_per_s"] = round(by[name] / ms / 1e6, 1)
+            d["hbm_frac_of_measured"] = round(by[name] / ms / 1e6 / pk["hbm_gbs"], 3)
+        if name == "module_gemm":
+            d["TFLOP_per_s"] = round(gemm_flop / ms / 1e9, 1)
+        per[name] = d
+    med = statistics.median(times)
+    line = {"module": "LayerNorm -> projections -> triangle attention core -> output projection, fwd + bwd",
+            "config": {"workload": w.describe(), "B": Bn, "N": N, "C": C, "H": H, "D": D,
+                       "mask_frac": w.mask_frac if w.mask != "none" else 0.0},
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step_median": round(med, 4),
+            "ms_per_step_min": round(min(times), 4),
+            "core_share": round(sum(v["ms_per_step"] for k, v in per.items() if not k.startswith("module_")) / med, 3),
+            "flop_per_step": {"core": fl_core, "projections": gemm_flop},
+            "kernels": per, "clocks": clk.summary(), "peaks_source": pk["source"]}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.module:
+        run_module(args)
+        return
     if args.ablation == "atomic":
         run_atomic_ablation(args)
         return

@@ -221,6 +221,73 @@ triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* p
                                       void* stream);
 
 /*
+ * The triangle-attention module around the core ("TurboPairFormer",
+ * Figure 6 and its worked example; shapes from Table 1): with M = B*N*N
+ * pairs of C features each,
+ *
+ *   x    = LayerNorm(z; ln_w, ln_b)  over the C features of each pair, eps 1e-5
+ *   P    = x W_in                    W_in [C, 3HD + H]
+ *   q, k, v [b, i, h, j, :] = P[(b, i, j), {0, HD, 2HD} + h D + (0 .. D-1)]
+ *   bias [b, h, i, j]       = P[(b, i, j), 3HD + h]
+ *   o    = tri_attn_fwd(q, k, v, bias, mask)     (N_o = N)
+ *   out  = o_flat W_o                W_o [HD, C], o_flat[(b, i, j), h D + d] = o[b, i, h, j, d]
+ *
+ * No projection biases and no gate; the residual update z + out is left to
+ * the caller.  The projections are cuBLAS GEMMs (BF16 operands, FP32
+ * accumulation); the LayerNorm, the layout changes between the pair layout
+ * and the core's, and the LayerNorm's parameter-gradient sums are the
+ * library's kernels; the core is tri_attn_fwd / tri_attn_bwd.
+ *
+ * Shape: B >= 1, N as for the core (multiple of 8, 8..4096), C a multiple
+ * of 32 up to 256, H up to 64, D 16 or 32, flags 0.  Otherwise
+ * TRIATTN_ERR_INVALID_ARG (non-positive field, flags) or
+ * TRIATTN_ERR_UNSUPPORTED; the size queries return 0.
+ *
+ * Layouts (device pointers, contiguous row-major, 16-byte aligned):
+ *   z, dz    [B, N, N, C] bf16        out, d_out [B, N, N, C] bf16
+ *   ln_w, ln_b, d_ln_w, d_ln_b  [C] fp32
+ *   w_in [C, 3HD + H] bf16, w_o [HD, C] bf16
+ *   d_w_in [C, 3HD + H] fp32, d_w_o [HD, C] fp32   (overwritten, not accumulated)
+ *   mask  optional [B, N, N] bf16 additive key mask of each slice (the core's)
+ *   ctx   triattn_module_ctx_bytes(shape) bytes, 256-byte aligned: written by
+ *         the forward (x, the LayerNorm statistics, q, k, v, bias, o, lse, the
+ *         output residual, o_flat), read by the backward of the same inputs.
+ *   workspace  triattn_module_workspace_bytes(shape) bytes, 256-byte
+ *         aligned, contents ignored; either call may use it (it also serves
+ *         as cuBLAS's workspace and the core backward's).
+ *
+ * The first call on a host thread and device creates a cuBLAS handle there
+ * (cuBLAS's own small allocation); the library keeps it for the thread's
+ * lifetime.  Results are bitwise reproducible for a fixed shape and device:
+ * the kernels' reductions have a fixed order and cuBLAS runs a fixed
+ * configuration without atomics.  Argument errors return before anything is
+ * launched; a failed launch or cuBLAS call returns TRIATTN_ERR_CUDA.
+ */
+typedef struct {
+  int B;          /* examples */
+  int N;          /* tokens per crop */
+  int C;          /* pair features */
+  int H;          /* heads */
+  int D;          /* features per head: 16 or 32 */
+  unsigned flags; /* 0 */
+} triattn_module_shape;
+
+size_t triattn_module_ctx_bytes(const triattn_module_shape* shape);
+size_t triattn_module_workspace_bytes(const triattn_module_shape* shape);
+
+/* Forward: writes out and ctx. */
+triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void* z, const void* mask,
+                                   const float* ln_w, const float* ln_b, const void* w_in, const void* w_o,
+                                   void* out, void* ctx, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of <out, d_out>: dz (bf16), d_ln_w, d_ln_b, d_w_in, d_w_o (fp32).
+ * z, mask, ln_w, w_in, w_o and ctx must be those of the forward call. */
+triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void* z, const void* mask,
+                                   const float* ln_w, const void* w_in, const void* w_o, const void* ctx,
+                                   const void* d_out, void* dz, float* d_ln_w, float* d_ln_b, float* d_w_in,
+                                   float* d_w_o, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * kernels set when a bounded wait gives up.  Returns TRIATTN_OK,
  * TRIATTN_ERR_TIMEOUT, or TRIATTN_ERR_CUDA if the synchronisation failed.

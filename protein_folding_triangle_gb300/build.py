@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "noalloc.cu", "module.cu"]
 HEADERS = ["ptx.cuh", "kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
@@ -67,7 +67,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         list(ex.map(compile_one, zip(srcs, objs)))
     tmp = out + f".tmp{os.getpid()}"
-    cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(exe))), "lib64")
+    cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs + ["-L", cuda_lib, "-lcublas",
+                                                         "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

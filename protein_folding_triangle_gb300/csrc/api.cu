@@ -127,13 +127,11 @@ WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
 }
 
 // ---------------------------------------------------------------- tracing
-enum KernelKind {
-  kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine, kKinds
-};
 const char* const kKernelName[kKinds] = {"tri_attn_fwd",     "bwd_preprocess",  "bwd_transpose_bias",
                                          "bwd_main",         "bwd_reduce_dq",   "bwd_reduce_dbias",
                                          "bwd_main_atomic",  "bwd_finish_dq",   "bwd_finish_dbias",
-                                         "dbias_combine"};
+                                         "dbias_combine",    "module_ln_fwd",   "module_layout",
+                                         "module_gemm",      "module_ln_bwd",   "module_colsum"};
 struct TraceRec {
   int kind;
   cudaEvent_t a, b;
@@ -169,6 +167,14 @@ cudaError_t traced(int kind, cudaStream_t s, F launch) {
   g_trace.push_back({kind, ea, eb});
   return e;
 }
+
+}  // namespace
+
+cudaError_t trace_call(int kind, cudaStream_t s, const std::function<cudaError_t()>& launch) {
+  return traced(kind, s, launch);
+}
+
+namespace {
 
 WaitCtl wait_ctl(int dev) {
   WaitCtl wc;

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 
 #include "ptx.cuh"
 
@@ -69,5 +70,14 @@ template <int D> cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t
 cudaError_t launch_bwd_finish_dbias(const BwdArgs& a, cudaStream_t stream);
 // dbias = bf16(sum over r of parts[r]) in ascending r (outer axis split across GPUs).
 cudaError_t launch_dbias_combine(const float* parts, int R, size_t elems, void* dbias, cudaStream_t stream);
+
+// Kernel kinds of the trace (triattn_trace_enable / triattn_trace_read).
+enum KernelKind {
+  kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine,
+  kKModLnFwd, kKModLayout, kKModGemm, kKModLnBwd, kKModColSum, kKinds
+};
+// Runs `launch` on stream `s`, bracketed by a pair of trace events while
+// tracing is on.
+cudaError_t trace_call(int kind, cudaStream_t s, const std::function<cudaError_t()>& launch);
 
 }  // namespace triattn

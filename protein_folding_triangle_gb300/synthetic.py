@@ -111,3 +111,35 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     elif w.mask != "none":
         raise ValueError(w.mask)
     return {"q": q, "k": k, "v": v, "do": do, "bias": bias, "mask": mask}
+
+
+def make_module_inputs(B: int, N: int, C: int, H: int, D: int, seed: int = 0, mask_frac: float = 0.0) -> dict:
+    """Seeded inputs of the module around the core (CPU tensors): z and the
+    incoming gradient d_out [B, N, N, C] BF16 (standard normal), LayerNorm
+    scale 1 + 0.1 n and shift 0.1 n (FP32), W_in [C, 3HD + H] with entries
+    n / sqrt(C) and W_o [HD, C] with entries n / sqrt(HD) (BF16), so that q,
+    k, v and the bias channels have about unit variance, as the core's own
+    synthetic inputs do.  Draw order: z, d_out, ln_w, ln_b, W_in, W_o.  With
+    ``mask_frac`` > 0 the last ``int(mask_frac * N)`` keys of every slice are
+    masked ([B, N, N] additive BF16, -inf), else the mask is None."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+
+    def normal(shape, scale=1.0):
+        return torch.randn(shape, generator=g, dtype=torch.float32) * scale
+
+    F = 3 * H * D + H
+    z = normal((B, N, N, C)).to(torch.bfloat16)
+    d_out = normal((B, N, N, C)).to(torch.bfloat16)
+    ln_w = 1.0 + normal((C,), 0.1)
+    ln_b = normal((C,), 0.1)
+    w_in = normal((C, F), C ** -0.5).to(torch.bfloat16)
+    w_o = normal((H * D, C), (H * D) ** -0.5).to(torch.bfloat16)
+    mask = None
+    nm = int(mask_frac * N)
+    if nm > 0:
+        mask = torch.zeros((B, N, N), dtype=torch.float32)
+        mask[:, :, N - nm:] = float("-inf")
+        mask = mask.to(torch.bfloat16)
+    return {"z": z, "d_out": d_out, "ln_w": ln_w, "ln_b": ln_b, "w_in": w_in, "w_o": w_o, "mask": mask,
+            "H": H, "D": D}

@@ -33,7 +33,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = ran
 EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fwd", "tri_attn_bwd",
             "triattn_device_status", "triattn_set_wait_limit_ns", "triattn_trace_enable", "triattn_trace_read",
             "triattn_test_set_starve", "tri_attn_bwd_noalloc", "triattn_bwd_atomic_workspace_bytes",
-            "tri_attn_bwd_atomic_ablation", "tri_attn_dbias_combine")
+            "tri_attn_bwd_atomic_ablation", "tri_attn_dbias_combine", "triattn_module_ctx_bytes",
+            "triattn_module_workspace_bytes", "tri_attn_module_fwd", "tri_attn_module_bwd")
 
 FLAG_DBIAS_FP32 = 1
 
@@ -53,6 +54,11 @@ class TriAttnError(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("N_o", ctypes.c_int), ("N", ctypes.c_int), ("H", ctypes.c_int),
+                ("D", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+class ModuleShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int), ("H", ctypes.c_int),
                 ("D", ctypes.c_int), ("flags", ctypes.c_uint)]
 
 
@@ -85,6 +91,15 @@ def _declare(lib):
     lib.tri_attn_bwd_atomic_ablation.restype = ctypes.c_int
     lib.tri_attn_dbias_combine.argtypes = [sp, vp, ctypes.c_int, vp, vp]
     lib.tri_attn_dbias_combine.restype = ctypes.c_int
+    mp = ctypes.POINTER(ModuleShape)
+    lib.triattn_module_ctx_bytes.argtypes = [mp]
+    lib.triattn_module_ctx_bytes.restype = ctypes.c_size_t
+    lib.triattn_module_workspace_bytes.argtypes = [mp]
+    lib.triattn_module_workspace_bytes.restype = ctypes.c_size_t
+    lib.tri_attn_module_fwd.argtypes = [mp] + [vp] * 9 + [ctypes.c_size_t, vp]
+    lib.tri_attn_module_fwd.restype = ctypes.c_int
+    lib.tri_attn_module_bwd.argtypes = [mp] + [vp] * 13 + [ctypes.c_size_t, vp]
+    lib.tri_attn_module_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -293,6 +308,88 @@ def trace_read() -> dict:
 def test_set_starve(on: bool) -> None:
     """Test hook: starve the forward's MMA warp so its bounded wait runs out."""
     load().triattn_test_set_starve(1 if on else 0)
+
+
+def module_sizes(B: int, N: int, C: int, H: int, D: int):
+    """(ctx bytes, workspace bytes) of the module; (0, 0) for an unsupported shape."""
+    s = ModuleShape(B, N, C, H, D, 0)
+    lib = load()
+    return int(lib.triattn_module_ctx_bytes(ctypes.byref(s))), int(lib.triattn_module_workspace_bytes(ctypes.byref(s)))
+
+
+def _module_shape(z, H, D):
+    if z.dim() != 4 or z.shape[1] != z.shape[2]:
+        raise ValueError("z must be [B, N, N, C]")
+    B, N, _, C = z.shape
+    return ModuleShape(B, N, C, H, D, 0)
+
+
+def _bytes(t):
+    return ctypes.c_size_t(t.numel() * t.element_size())
+
+
+def tri_attn_module_fwd(z, mask, ln_w, ln_b, w_in, w_o, H: int, D: int, *, ctx=None, workspace=None, out=None,
+                        stream=None):
+    """Module forward: LayerNorm, projections into q, k, v and the bias, the
+    core, output projection.  Returns (out [B, N, N, C] bf16, ctx) where ctx
+    is the uint8 buffer the backward needs."""
+    s = _module_shape(z, H, D)
+    B, N, C = s.B, s.N, s.C
+    F = 3 * H * D + H
+    _check(z, "z", (B, N, N, C))
+    _check(ln_w, "ln_w", (C,), torch.float32)
+    _check(ln_b, "ln_b", (C,), torch.float32)
+    _check(w_in, "w_in", (C, F))
+    _check(w_o, "w_o", (H * D, C))
+    if mask is not None:
+        _check(mask, "mask", (B, N, N))
+    nctx, nws = module_sizes(B, N, C, H, D)
+    if nctx == 0:
+        raise TriAttnError(ERR_UNSUPPORTED, "tri_attn_module_fwd")
+    if ctx is None:
+        ctx = torch.empty(nctx, dtype=torch.uint8, device=z.device)
+    if workspace is None:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=z.device)
+    if out is None:
+        out = torch.empty_like(z)
+    _check(out, "out", (B, N, N, C))
+    code = load().tri_attn_module_fwd(ctypes.byref(s), _ptr(z), _ptr(mask), _ptr(ln_w), _ptr(ln_b), _ptr(w_in),
+                                      _ptr(w_o), _ptr(out), _ptr(ctx), _ptr(workspace), _bytes(workspace),
+                                      _stream_ptr(stream))
+    _raise(code, "tri_attn_module_fwd")
+    return out, ctx
+
+
+def tri_attn_module_bwd(z, mask, ln_w, w_in, w_o, ctx, d_out, H: int, D: int, *, workspace=None, out=None,
+                        stream=None):
+    """Module backward of <out, d_out>.  Returns (dz bf16, d_ln_w, d_ln_b,
+    d_w_in, d_w_o fp32)."""
+    s = _module_shape(z, H, D)
+    B, N, C = s.B, s.N, s.C
+    F = 3 * H * D + H
+    _check(z, "z", (B, N, N, C))
+    _check(d_out, "d_out", (B, N, N, C))
+    _check(ln_w, "ln_w", (C,), torch.float32)
+    _check(w_in, "w_in", (C, F))
+    _check(w_o, "w_o", (H * D, C))
+    if mask is not None:
+        _check(mask, "mask", (B, N, N))
+    nctx, nws = module_sizes(B, N, C, H, D)
+    if nctx == 0:
+        raise TriAttnError(ERR_UNSUPPORTED, "tri_attn_module_bwd")
+    _check(ctx, "ctx", (nctx,), torch.uint8)
+    if workspace is None:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=z.device)
+    if out is None:
+        f32 = dict(dtype=torch.float32, device=z.device)
+        out = (torch.empty_like(z), torch.empty(C, **f32), torch.empty(C, **f32), torch.empty((C, F), **f32),
+               torch.empty((H * D, C), **f32))
+    dz, dlw, dlb, dwi, dwo = out
+    code = load().tri_attn_module_bwd(ctypes.byref(s), _ptr(z), _ptr(mask), _ptr(ln_w), _ptr(w_in), _ptr(w_o),
+                                      _ptr(ctx), _ptr(d_out), _ptr(dz), _ptr(dlw), _ptr(dlb), _ptr(dwi), _ptr(dwo),
+                                      _ptr(workspace), _bytes(workspace), _stream_ptr(stream))
+    _raise(code, "tri_attn_module_bwd")
+    return dz, dlw, dlb, dwi, dwo
 
 
 class TriAttnFunction(torch.autograd.Function):

@@ -241,3 +241,57 @@ def test_sharded_dbias_gather_two_gloo_ranks():
     assert status == "ok", err
     assert shapes == [(1, 2, 24, 24)] * 2
     assert err < 1e-6, err
+
+
+def module_shape(B=1, N=40, C=64, H=2, D=16, flags=0):
+    return T.ModuleShape(B, N, C, H, D, flags)
+
+
+def call_module_fwd(lib, shape, ws_bytes, ws=FAKE, **ptrs):
+    names = ("z", "ln_w", "ln_b", "w_in", "w_o", "out", "ctx")
+    p = {n: ctypes.c_void_p(FAKE) for n in names}
+    p["mask"] = None
+    p.update(ptrs)
+    return lib.tri_attn_module_fwd(ctypes.byref(shape), p["z"], p["mask"], p["ln_w"], p["ln_b"], p["w_in"],
+                                   p["w_o"], p["out"], p["ctx"], ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes),
+                                   None)
+
+
+def call_module_bwd(lib, shape, ws_bytes, ws=FAKE, **ptrs):
+    names = ("z", "ln_w", "w_in", "w_o", "ctx", "d_out", "dz", "d_ln_w", "d_ln_b", "d_w_in", "d_w_o")
+    p = {n: ctypes.c_void_p(FAKE) for n in names}
+    p["mask"] = None
+    p.update(ptrs)
+    return lib.tri_attn_module_bwd(ctypes.byref(shape), p["z"], p["mask"], p["ln_w"], p["w_in"], p["w_o"],
+                                   p["ctx"], p["d_out"], p["dz"], p["d_ln_w"], p["d_ln_b"], p["d_w_in"],
+                                   p["d_w_o"], ctypes.c_void_p(ws), ctypes.c_size_t(ws_bytes), None)
+
+
+def test_module_sizes(lib):
+    ctx, ws = T.module_sizes(1, 40, 64, 2, 16)
+    B_, N, C, H, D = 1, 40, 64, 2, 16
+    act = B_ * N * H * N * D * 2
+    # ctx holds at least x, q, k, v, o, the residual, o_flat and the bias planes
+    assert ctx >= B_ * N * N * C * 2 + 5 * act + B_ * N * N * H * D * 2 + B_ * H * N * N * 2
+    core = T.bwd_workspace_bytes(T.Shape(B_, N, N, H, D, 0))
+    assert ws >= core + (32 << 20) + B_ * N * N * (3 * H * D + H) * 2
+    for bad in [(1, 40, 48, 2, 16), (1, 40, 288, 2, 16), (1, 44, 64, 2, 16), (1, 40, 64, 2, 8), (0, 40, 64, 2, 16),
+                (1, 40, 64, 65, 16)]:
+        assert T.module_sizes(*bad) == (0, 0), bad
+
+
+def test_module_rejects_bad_arguments(lib):
+    s = module_shape()
+    _, ws = T.module_sizes(1, 40, 64, 2, 16)
+    assert call_module_fwd(lib, module_shape(C=48), ws) == T.ERR_UNSUPPORTED
+    assert call_module_fwd(lib, module_shape(flags=1), ws) == T.ERR_INVALID_ARG
+    assert call_module_fwd(lib, module_shape(B=0), ws) == T.ERR_INVALID_ARG
+    assert call_module_fwd(lib, s, ws, z=None) == T.ERR_INVALID_ARG
+    assert call_module_fwd(lib, s, ws, w_in=ctypes.c_void_p(FAKE + 8)) == T.ERR_INVALID_ARG
+    assert call_module_fwd(lib, s, ws, ctx=ctypes.c_void_p(FAKE + 16)) == T.ERR_INVALID_ARG
+    assert call_module_fwd(lib, s, ws - 1) == T.ERR_WORKSPACE
+    assert call_module_fwd(lib, s, ws, ws=FAKE + 16) == T.ERR_WORKSPACE
+    assert call_module_bwd(lib, module_shape(D=24), ws) == T.ERR_UNSUPPORTED
+    assert call_module_bwd(lib, s, ws, d_w_o=None) == T.ERR_INVALID_ARG
+    assert call_module_bwd(lib, s, ws, mask=ctypes.c_void_p(FAKE + 2)) == T.ERR_INVALID_ARG
+    assert call_module_bwd(lib, s, 0) == T.ERR_WORKSPACE

@@ -1,0 +1,113 @@
+"""GPU parity of the triangle-attention module (LayerNorm, projections into
+q, k, v and the bias, the core, output projection; "TurboPairFormer",
+Figure 6) through the C ABI, against the FP64 module oracle on the same
+seeded BF16 inputs.
+
+Tolerances (relative RMSE against FP64): out <= 1e-2, every gradient
+(dz, dgamma, dbeta, dW_in, dW_o) <= 2e-2.  The module adds four BF16
+roundings to the core's own error (x, the projection P, the core output
+once more through o_flat, and out; in the backward d_oflat and dP), each a
+relative 2^-9 at most, on top of the core's 4e-3 / 1e-2 bars; the bars
+here leave about a factor two over the core's.
+"""
+import json
+
+import numpy as np
+import pytest
+import torch
+
+from parity_utils import cpu64, rel_rmse
+from oracle import module as MO
+from protein_folding_triangle_gb300 import synthetic as S
+from protein_folding_triangle_gb300 import triattn as T
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 1e-2
+TOL_GRADS = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from protein_folding_triangle_gb300 import build
+    build.build()
+    T.load()
+
+
+def run_gpu(x):
+    dev = {k: (v.cuda().contiguous() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    H, D = x["H"], x["D"]
+    out, ctx = T.tri_attn_module_fwd(dev["z"], dev["mask"], dev["ln_w"], dev["ln_b"], dev["w_in"], dev["w_o"], H, D)
+    grads = T.tri_attn_module_bwd(dev["z"], dev["mask"], dev["ln_w"], dev["w_in"], dev["w_o"], ctx, dev["d_out"],
+                                  H, D)
+    torch.cuda.synchronize()
+    assert T.device_status() == T.OK
+    return out, grads
+
+
+def run_oracle(x):
+    args = (x["z"], x["mask"], x["ln_w"], x["ln_b"], x["w_in"], x["w_o"])
+    f = MO.fwd(*args, x["H"], x["D"])
+    g = MO.bwd(*args, x["d_out"], x["H"], x["D"])
+    return f["out"], g
+
+
+CASES = [
+    # (B, N, C, H, D, mask_frac): one tile, a ragged tail, several tiles
+    (1, 40, 64, 2, 16, 0.0),
+    (2, 48, 32, 1, 32, 0.2),
+    (1, 136, 128, 4, 32, 0.1),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}N{c[1]}C{c[2]}H{c[3]}D{c[4]}" for c in CASES])
+def test_module_matches_oracle(case):
+    B, N, C, H, D, mf = case
+    x = S.make_module_inputs(B, N, C, H, D, seed=N + C, mask_frac=mf)
+    out, (dz, dlw, dlb, dwi, dwo) = run_gpu(x)
+    ref_out, ref = run_oracle(x)
+    errs = {"out": rel_rmse(cpu64(out), ref_out), "dz": rel_rmse(cpu64(dz), ref["dz"]),
+            "dgamma": rel_rmse(cpu64(dlw), ref["dgamma"]), "dbeta": rel_rmse(cpu64(dlb), ref["dbeta"]),
+            "dw_in": rel_rmse(cpu64(dwi), ref["dw_in"]), "dw_o": rel_rmse(cpu64(dwo), ref["dw_o"])}
+    print(json.dumps({"case": list(case), **{k: round(v, 6) for k, v in errs.items()}}))
+    assert errs["out"] <= TOL_OUT, errs
+    for k in ("dz", "dgamma", "dbeta", "dw_in", "dw_o"):
+        assert errs[k] <= TOL_GRADS, (k, errs)
+
+
+def test_module_bitwise_deterministic():
+    x = S.make_module_inputs(1, 72, 64, 2, 32, seed=3, mask_frac=0.1)
+    first = None
+    for _ in range(3):
+        out, grads = run_gpu(x)
+        cur = [out.view(torch.int16).cpu()] + [g.contiguous().view(torch.int16).cpu() for g in grads]
+        if first is None:
+            first = cur
+        else:
+            for a, b in zip(first, cur):
+                assert torch.equal(a, b)
+
+
+def test_module_layernorm_statistics_in_ctx():
+    """The saved x is LayerNorm(z) rounded to BF16: compared element by
+    element with the oracle's x (first bytes of ctx)."""
+    B, N, C, H, D = 1, 24, 96, 2, 16
+    x = S.make_module_inputs(B, N, C, H, D, seed=5)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    _, ctx = T.tri_attn_module_fwd(dev["z"], None, dev["ln_w"], dev["ln_b"], dev["w_in"], dev["w_o"], H, D)
+    torch.cuda.synchronize()
+    xg = ctx[:B * N * N * C * 2].view(torch.bfloat16).reshape(B, N, N, C)
+    ref, _, _ = MO.layernorm(cpu64(x["z"]), cpu64(x["ln_w"]), cpu64(x["ln_b"]))
+    # one BF16 rounding of an FP32 value: relative 2^-8 at most per element
+    err = np.abs(cpu64(xg) - ref)
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-6), float(err.max())
+
+
+def test_module_rejects_bad_shapes_without_launching():
+    z = torch.zeros((1, 40, 40, 48), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(48, dtype=torch.float32, device="cuda")
+    with pytest.raises(T.TriAttnError):
+        T.tri_attn_module_fwd(z, None, w, w, torch.zeros((48, 3 * 32 + 2), dtype=torch.bfloat16, device="cuda"),
+                              torch.zeros((32, 48), dtype=torch.bfloat16, device="cuda"), 2, 16)

@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--module", type=int, default=0, metavar="C",
                     help="instead of the bench line: time the whole module (LayerNorm, projections with C pair "
                          "features, the core, output projection; forward + backward) and print one JSON line")
+    ap.add_argument("--trimul", type=int, default=0, metavar="C",
+                    help="instead of the bench line: time the triangle multiplicative update (C pair features = "
+                         "C hidden channels, forward + backward, both directions) and print one JSON line each")
     return ap.parse_args()
 
 
@@ -628,8 +631,98 @@ def run_module(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- trimul
+def run_trimul(args):
+    """Forward + backward of the triangle multiplicative update on the
+    workload's B and N with C_z = C_h = ``--trimul`` (the pages' Table 10
+    shapes), each direction: CUDA events around each step on the launching
+    stream, then three traced steps for the per-kernel split.  Algorithmic
+    bytes of the HBM-bound kernels and FLOPs of the GEMMs per step are
+    counted below."""
+    import statistics
+    import torch
+    from protein_folding_triangle_gb300 import build as B
+    from protein_folding_triangle_gb300 import synthetic as S
+    from protein_folding_triangle_gb300 import triattn as T
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    B.build()
+    T.load()
+    dev = torch.device("cuda", 0)
+    w = S.WORKLOADS[args.workload]
+    Bn, N, C = w.B, w.N, args.trimul
+    Cz = Ch = C
+    x = S.make_trimul_inputs(Bn, N, Cz, Ch, seed=args.seed, pad_frac=0.0)
+    xd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    F = 4 * Ch + Cz
+    M = Bn * N * N
+    f32 = dict(dtype=torch.float32, device=dev)
+    pk = peaks()
+    for direction in ("outgoing", "incoming"):
+        nctx, nws = T.trimul_sizes(Bn, N, Cz, Ch, direction)
+        ctx = torch.empty(nctx, dtype=torch.uint8, device=dev)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        out = torch.empty_like(xd["z"])
+        grads = (torch.empty_like(xd["z"]), torch.empty(Cz, **f32), torch.empty(Cz, **f32), torch.empty((Cz, F), **f32),
+                 torch.empty(Ch, **f32), torch.empty(Ch, **f32), torch.empty((Ch, Cz), **f32))
+
+        def step():
+            T.triattn_trimul_fwd(xd["z"], xd["mask"], xd["ln_in_w"], xd["ln_in_b"], xd["w_p"], xd["ln_out_w"],
+                                 xd["ln_out_b"], xd["w_o"], direction, ctx=ctx, workspace=ws, out=out)
+            T.triattn_trimul_bwd(xd["z"], xd["mask"], xd["ln_in_w"], xd["w_p"], xd["ln_out_w"], xd["w_o"], ctx,
+                                 xd["d_out"], direction, workspace=ws, out=grads)
+
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize(dev)
+        times = []
+        with ClockSampler(0) as clk:
+            for _ in range(args.steps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                step()
+                e1.record()
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+        T.trace_enable(True)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
+        tr = T.trace_read()
+        T.trace_enable(False)
+        by = {"trimul_ln_in": M * Cz * 4 + 8 * M + M * Cz * 8 + 8 * M,
+              "trimul_gate": (M * 4 * Ch * 2 + 2 * M * Ch * 2) + (2 * M * Ch * 2 + 2 * M * 4 * Ch * 2),
+              "trimul_ln_out": (2 * M * Ch * 2 + 8 * M) + (M * Ch * 2 + M * Ch * 4 + 8 * M + M * Ch * 2),
+              "trimul_out_gate": 3 * M * Cz * 2 + 5 * M * Cz * 2}
+        fl = {"trimul_proj_gemm": 3 * (2 * M * Cz * F + 2 * M * Ch * Cz),
+              "trimul_contract_gemm": 3 * 2 * Bn * Ch * N ** 3}
+        per = {}
+        for name, e in tr.items():
+            ms = e["total_ms"] / 3.0
+            d = {"ms_per_step": round(ms, 4), "launches_per_step": e["launches"] // 3}
+            if name in by:
+                d["GB_per_s"] = round(by[name] / ms / 1e6, 1)
+                d["hbm_frac_of_measured"] = round(by[name] / ms / 1e6 / pk["hbm_gbs"], 3)
+            if name in fl:
+                d["TFLOP_per_s"] = round(fl[name] / ms / 1e9, 1)
+                d["tensor_frac_of_measured_sustained"] = round(fl[name] / ms / 1e9 / pk["bf16_sustained"], 3)
+            per[name] = d
+        med = statistics.median(times)
+        line = {"trimul": direction, "what": "triangle multiplicative update, forward + backward",
+                "config": {"B": Bn, "N": N, "C_z": Cz, "C_h": Ch, "mask": "none"},
+                "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step_median": round(med, 4),
+                "ms_per_step_min": round(min(times), 4), "flop_per_step": fl, "kernels": per,
+                "clocks": clk.summary(), "peaks_source": pk["source"],
+                "pages_table10_context_h100_ms": {"384/128": 1.32, "640/128": 3.33, "768/128": 4.78}}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.trimul:
+        run_trimul(args)
+        return
     if args.module:
         run_module(args)
         return

@@ -288,6 +288,79 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
                                    float* d_w_o, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Triangle multiplicative update, outgoing or incoming ("TurboPairFormer",
+ * Figure 12; shapes from Table 10).  With M = B*N*N pairs:
+ *
+ *   x   = LayerNorm(z; ln_in_w, ln_in_b)            over C_z, eps 1e-5
+ *   p   = x W_p                                     W_p [C_z, 4 C_h + C_z], columns
+ *                                                   a_v | a_g | b_v | b_g | g
+ *   a   = m * sigmoid(a_g) * a_v,  b = m * sigmoid(b_g) * b_v   (m: pair mask)
+ *   outgoing: X[b,i,j,c] = sum_k a[b,i,k,c] * b[b,j,k,c]
+ *   incoming: X[b,i,j,c] = sum_k a[b,k,i,c] * b[b,k,j,c]
+ *   out = sigmoid(g) * (LayerNorm(X; ln_out_w, ln_out_b) W_o)   W_o [C_h, C_z]
+ *
+ * No projection biases; the residual update z + out is left to the caller.
+ * The projections and the per-channel contraction are cuBLAS GEMMs (BF16
+ * operands, FP32 accumulation; the contraction one strided-batched GEMM over
+ * the B*C_h channel matrices); the LayerNorms, the gating and masking (with
+ * the transposes to and from channel-major operands), the output gate and
+ * the parameter-gradient sums are the library's kernels.
+ *
+ * Shape: B >= 1; N a multiple of 8, 8..4096, B*N*N < 2^31; C_z a multiple of
+ * 32 up to 256; C_h 32, 64, 96 or 128; direction TRIATTN_TRIMUL_OUTGOING or
+ * TRIATTN_TRIMUL_INCOMING; flags 0.  Otherwise TRIATTN_ERR_INVALID_ARG
+ * (non-positive field, direction, flags) or TRIATTN_ERR_UNSUPPORTED; the size
+ * queries return 0.
+ *
+ * Layouts (device pointers, contiguous row-major, 16-byte aligned):
+ *   z, dz, out, d_out  [B, N, N, C_z] bf16
+ *   mask               optional [B, N, N] bf16, multiplicative (1 keeps a pair, 0 drops it)
+ *   ln_in_w, ln_in_b, d_ln_in_w, d_ln_in_b    [C_z] fp32
+ *   ln_out_w, ln_out_b, d_ln_out_w, d_ln_out_b [C_h] fp32
+ *   w_p [C_z, 4 C_h + C_z] bf16, w_o [C_h, C_z] bf16
+ *   d_w_p, d_w_o       same shapes, fp32 (overwritten, not accumulated)
+ *   ctx   triattn_trimul_ctx_bytes(shape) bytes, 256-byte aligned: written
+ *         by the forward (x and its statistics, p, the channel-major a, b
+ *         and X, the output LayerNorm statistics, its output y, and
+ *         u = y W_o), read by the backward of the same inputs.
+ *   workspace  triattn_trimul_workspace_bytes(shape) bytes, 256-byte
+ *         aligned, contents ignored (also cuBLAS's workspace).
+ *
+ * Like the module entry points, the first call on a host thread and device
+ * creates a cuBLAS handle there.  Bitwise reproducible for a fixed shape
+ * and device.  Argument errors return before anything is launched; a failed
+ * launch or cuBLAS call returns TRIATTN_ERR_CUDA.
+ */
+#define TRIATTN_TRIMUL_OUTGOING 0
+#define TRIATTN_TRIMUL_INCOMING 1
+
+typedef struct {
+  int B;          /* examples */
+  int N;          /* tokens per crop */
+  int C_z;        /* pair features */
+  int C_h;        /* hidden channels of the contraction */
+  int direction;  /* TRIATTN_TRIMUL_OUTGOING or TRIATTN_TRIMUL_INCOMING */
+  unsigned flags; /* 0 */
+} triattn_trimul_shape;
+
+size_t triattn_trimul_ctx_bytes(const triattn_trimul_shape* shape);
+size_t triattn_trimul_workspace_bytes(const triattn_trimul_shape* shape);
+
+/* Forward: writes out and ctx. */
+triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void* z, const void* mask,
+                                  const float* ln_in_w, const float* ln_in_b, const void* w_p,
+                                  const float* ln_out_w, const float* ln_out_b, const void* w_o, void* out,
+                                  void* ctx, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of <out, d_out>: dz (bf16) and the fp32 parameter gradients.
+ * z, mask, the parameters and ctx must be those of the forward call. */
+triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void* z, const void* mask,
+                                  const float* ln_in_w, const void* w_p, const float* ln_out_w, const void* w_o,
+                                  const void* ctx, const void* d_out, void* dz, float* d_ln_in_w, float* d_ln_in_b,
+                                  float* d_w_p, float* d_ln_out_w, float* d_ln_out_b, float* d_w_o,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * kernels set when a bounded wait gives up.  Returns TRIATTN_OK,
  * TRIATTN_ERR_TIMEOUT, or TRIATTN_ERR_CUDA if the synchronisation failed.

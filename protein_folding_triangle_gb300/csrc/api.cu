@@ -131,7 +131,10 @@ const char* const kKernelName[kKinds] = {"tri_attn_fwd",     "bwd_preprocess",  
                                          "bwd_main",         "bwd_reduce_dq",   "bwd_reduce_dbias",
                                          "bwd_main_atomic",  "bwd_finish_dq",   "bwd_finish_dbias",
                                          "dbias_combine",    "module_ln_fwd",   "module_layout",
-                                         "module_gemm",      "module_ln_bwd",   "module_colsum"};
+                                         "module_gemm",      "module_ln_bwd",   "module_colsum",
+                                         "trimul_ln_in",     "trimul_proj_gemm", "trimul_gate",
+                                         "trimul_contract_gemm", "trimul_ln_out", "trimul_out_gate",
+                                         "trimul_colsum"};
 struct TraceRec {
   int kind;
   cudaEvent_t a, b;

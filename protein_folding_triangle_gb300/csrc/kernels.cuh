@@ -74,7 +74,8 @@ cudaError_t launch_dbias_combine(const float* parts, int R, size_t elems, void* 
 // Kernel kinds of the trace (triattn_trace_enable / triattn_trace_read).
 enum KernelKind {
   kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine,
-  kKModLnFwd, kKModLayout, kKModGemm, kKModLnBwd, kKModColSum, kKinds
+  kKModLnFwd, kKModLayout, kKModGemm, kKModLnBwd, kKModColSum,
+  kKTmLnIn, kKTmProj, kKTmGate, kKTmContract, kKTmLnOut, kKTmOutGate, kKTmColSum, kKinds
 };
 // Runs `launch` on stream `s`, bracketed by a pair of trace events while
 // tracing is on.

@@ -22,126 +22,13 @@
 #include <cstring>
 
 #include "kernels.cuh"
+#include "pairops.cuh"
 #include "triattn.h"
 
 namespace triattn {
 namespace {
 
-constexpr int kMaxC = 256;  // LayerNorm: up to 8 features per lane
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
-// One warp per pair: x = (z - mean) * rstd * gamma + beta (BF16), mean and
-// rstd saved in FP32.  Lane l holds features l, l + 32, ...
-template <int C>
-__global__ void __launch_bounds__(256) ln_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ gamma,
-                                                     const float* __restrict__ beta, uint16_t* __restrict__ x,
-                                                     float* __restrict__ mean_out, float* __restrict__ rstd_out,
-                                                     size_t M) {
-  constexpr int kPer = C / 32;
-  const int lane = threadIdx.x & 31;
-  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
-  for (size_t m = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; m < M; m += warps) {
-    float v[kPer];
-    float s = 0.f;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      v[e] = bf16lo_to_f32(z[m * C + lane + 32 * e]);
-      s += v[e];
-    }
-    const float mean = warp_sum(s) * (1.f / C);
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) ss += (v[e] - mean) * (v[e] - mean);
-    const float rstd = rsqrtf(warp_sum(ss) * (1.f / C) + 1e-5f);
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int c = lane + 32 * e;
-      x[m * C + c] = static_cast<uint16_t>(pack_bf16x2((v[e] - mean) * rstd * gamma[c] + beta[c], 0.f) & 0xFFFFu);
-    }
-    if (lane == 0) {
-      mean_out[m] = mean;
-      rstd_out[m] = rstd;
-    }
-  }
-}
-
-// One warp per pair: dz = rstd (g - mean(g) - xhat mean(g xhat)), g = dx gamma.
-// The warp also accumulates dgamma = sum dx xhat and dbeta = sum dx over its
-// pairs (fixed grid-stride assignment); the block adds its 8 warps' sums in
-// warp order and writes one partial row per block.
-template <int C>
-__global__ void __launch_bounds__(256) ln_bwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ dx,
-                                                     const float* __restrict__ gamma,
-                                                     const float* __restrict__ mean_in,
-                                                     const float* __restrict__ rstd_in, uint16_t* __restrict__ dz,
-                                                     float* __restrict__ part_gamma, float* __restrict__ part_beta,
-                                                     size_t M) {
-  constexpr int kPer = C / 32;
-  __shared__ float red_g[8][C], red_b[8][C];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
-  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
-  float accg[kPer], accb[kPer];
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) accg[e] = accb[e] = 0.f;
-  for (size_t m = static_cast<size_t>(blockIdx.x) * 8 + warp; m < M; m += warps) {
-    const float mean = mean_in[m], rstd = rstd_in[m];
-    float xh[kPer], g[kPer];
-    float sg = 0.f, sgx = 0.f;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int c = lane + 32 * e;
-      xh[e] = (bf16lo_to_f32(z[m * C + c]) - mean) * rstd;
-      const float d = dx[m * C + c];
-      accg[e] += d * xh[e];
-      accb[e] += d;
-      g[e] = d * gamma[c];
-      sg += g[e];
-      sgx += g[e] * xh[e];
-    }
-    const float a = warp_sum(sg) * (1.f / C), bb = warp_sum(sgx) * (1.f / C);
-#pragma unroll
-    for (int e = 0; e < kPer; ++e)
-      dz[m * C + lane + 32 * e] =
-          static_cast<uint16_t>(pack_bf16x2(rstd * (g[e] - a - xh[e] * bb), 0.f) & 0xFFFFu);
-  }
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    red_g[warp][lane + 32 * e] = accg[e];
-    red_b[warp][lane + 32 * e] = accb[e];
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < C; c += blockDim.x) {
-    float sg = 0.f, sb = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      sg += red_g[w][c];
-      sb += red_b[w][c];
-    }
-    part_gamma[static_cast<size_t>(blockIdx.x) * C + c] = sg;
-    part_beta[static_cast<size_t>(blockIdx.x) * C + c] = sb;
-  }
-}
-
-// One warp per output column (columns 0 .. C-1: dgamma from pg, C .. 2C-1:
-// dbeta from pb): lane l adds rows l, l + 32, ... in ascending order, then a
-// fixed butterfly adds the 32 lane sums.
-__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ pg, const float* __restrict__ pb,
-                                                         int rows, int C, float* __restrict__ dgamma,
-                                                         float* __restrict__ dbeta) {
-  const int col = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x & 31;
-  if (col >= 2 * C) return;
-  const float* part = col < C ? pg : pb;
-  const int c = col < C ? col : col - C;
-  float s = 0.f;
-  for (int r = lane; r < rows; r += 32) s += part[static_cast<size_t>(r) * C + c];
-  s = warp_sum(s);
-  if (lane == 0) (col < C ? dgamma : dbeta)[c] = s;
-}
+using namespace pairops;
 
 // Pair layout -> core layout for one H*D block of a row-major [M, ld] matrix:
 // dst[b, i, h, j, d] = src[(b, i, j), off + h D + d], 8 features per thread.
@@ -192,30 +79,6 @@ __global__ void __launch_bounds__(256) bias_plane_kernel(uint16_t* __restrict__ 
 }
 
 // ---------------------------------------------------------------- cuBLAS
-// One handle per host thread and device (created on first use, kept for the
-// thread's lifetime), so calls from different threads never share one.
-thread_local cublasHandle_t t_blas[64] = {};
-
-cublasHandle_t blas_handle(int dev) {
-  if (t_blas[dev] == nullptr) {
-    cublasHandle_t h = nullptr;
-    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
-    t_blas[dev] = h;
-  }
-  return t_blas[dev];
-}
-
-// Row-major C[M, N] = op(A) op(B), A [M, K] (or [K, M] when ta), B [K, N] (or
-// [N, K] when tb); lda / ldb / ldc are the stored row lengths.  In cuBLAS's
-// column-major terms this is C^T = op(B)^T op(A)^T.
-cublasStatus_t gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, const void* A, int lda,
-                       const void* B, int ldb, void* C, int ldc, cudaDataType_t ct) {
-  const float one = 1.f, zero = 0.f;
-  return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, N, M, K, &one, B,
-                      CUDA_R_16BF, ldb, A, CUDA_R_16BF, lda, &zero, C, ct, ldc, CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT);
-}
-
 // ---------------------------------------------------------------- layouts
 size_t rup(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -259,8 +122,6 @@ CtxLayout ctx_layout(const ModDims& d) {
   return c;
 }
 
-constexpr size_t kBlasWorkspace = 32u << 20;
-constexpr int kLnBlocks = 152 * 8;  // fixed: the dgamma / dbeta partial rows depend on it
 
 // Scratch of one forward or backward call.
 struct WsLayout2 {
@@ -289,7 +150,7 @@ WsLayout2 ws_layout2(const ModDims& d, const triattn_shape& core) {
 triattn_status check_module(const triattn_module_shape* s, triattn_shape* core) {
   if (s == nullptr || s->flags != 0 || s->B < 1 || s->N < 1 || s->C < 1 || s->H < 1 || s->D < 1)
     return TRIATTN_ERR_INVALID_ARG;
-  if (s->C % 32 != 0 || s->C > kMaxC || s->H > 64) return TRIATTN_ERR_UNSUPPORTED;
+  if (!ln_width_ok(s->C) || s->H > 64) return TRIATTN_ERR_UNSUPPORTED;
   *core = triattn_shape{s->B, s->N, s->N, s->H, s->D, 0u};
   if (triattn_bwd_workspace_bytes(core) == 0) return TRIATTN_ERR_UNSUPPORTED;  // the core's own shape rules
   return TRIATTN_OK;
@@ -298,50 +159,6 @@ triattn_status check_module(const triattn_module_shape* s, triattn_shape* core) 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 unsigned blocks_for(size_t n) { return static_cast<unsigned>((n + 255) / 256); }
-
-template <int C>
-cudaError_t ln_fwd_launch(const ModDims& d, const void* z, const float* g, const float* b, void* x, float* mean,
-                          float* rstd, cudaStream_t s) {
-  ln_fwd_kernel<C><<<kLnBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), g, b, static_cast<uint16_t*>(x),
-                                                mean, rstd, d.M);
-  return cudaGetLastError();
-}
-template <int C>
-cudaError_t ln_bwd_launch(const ModDims& d, const void* z, const float* dx, const float* g, const float* mean,
-                          const float* rstd, void* dz, float* pg, float* pb, cudaStream_t s) {
-  ln_bwd_kernel<C><<<kLnBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), dx, g, mean, rstd,
-                                                static_cast<uint16_t*>(dz), pg, pb, d.M);
-  return cudaGetLastError();
-}
-
-cudaError_t ln_fwd_any(const ModDims& d, const void* z, const float* g, const float* b, void* x, float* mean,
-                       float* rstd, cudaStream_t s) {
-  switch (d.C) {
-    case 32: return ln_fwd_launch<32>(d, z, g, b, x, mean, rstd, s);
-    case 64: return ln_fwd_launch<64>(d, z, g, b, x, mean, rstd, s);
-    case 96: return ln_fwd_launch<96>(d, z, g, b, x, mean, rstd, s);
-    case 128: return ln_fwd_launch<128>(d, z, g, b, x, mean, rstd, s);
-    case 160: return ln_fwd_launch<160>(d, z, g, b, x, mean, rstd, s);
-    case 192: return ln_fwd_launch<192>(d, z, g, b, x, mean, rstd, s);
-    case 224: return ln_fwd_launch<224>(d, z, g, b, x, mean, rstd, s);
-    case 256: return ln_fwd_launch<256>(d, z, g, b, x, mean, rstd, s);
-  }
-  return cudaErrorInvalidValue;
-}
-cudaError_t ln_bwd_any(const ModDims& d, const void* z, const float* dx, const float* g, const float* mean,
-                       const float* rstd, void* dz, float* pg, float* pb, cudaStream_t s) {
-  switch (d.C) {
-    case 32: return ln_bwd_launch<32>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-    case 64: return ln_bwd_launch<64>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-    case 96: return ln_bwd_launch<96>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-    case 128: return ln_bwd_launch<128>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-    case 160: return ln_bwd_launch<160>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-    case 192: return ln_bwd_launch<192>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-    case 224: return ln_bwd_launch<224>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-    case 256: return ln_bwd_launch<256>(d, z, dx, g, mean, rstd, dz, pg, pb, s);
-  }
-  return cudaErrorInvalidValue;
-}
 
 cudaError_t split_heads(const ModDims& d, const uint16_t* src, int ld, int off, uint16_t* dst, cudaStream_t s) {
   return trace_call(kKModLayout, s, [&] {
@@ -366,29 +183,6 @@ cudaError_t bias_planes(const ModDims& d, uint16_t* pairs, int ld, int off, uint
                                                              static_cast<int>(d.H), d.M, to_pairs);
     return cudaGetLastError();
   });
-}
-
-triattn_status gemm_traced(cublasHandle_t h, cudaStream_t s, bool ta, bool tb, int M, int N, int K, const void* A,
-                           int lda, const void* B, int ldb, void* C, int ldc, cudaDataType_t ct) {
-  cublasStatus_t bs = CUBLAS_STATUS_SUCCESS;
-  const cudaError_t e = trace_call(kKModGemm, s, [&] {
-    bs = gemm_rm(h, ta, tb, M, N, K, A, lda, B, ldb, C, ldc, ct);
-    return cudaGetLastError();
-  });
-  return (e == cudaSuccess && bs == CUBLAS_STATUS_SUCCESS) ? TRIATTN_OK : TRIATTN_ERR_CUDA;
-}
-
-// The device's cuBLAS handle, bound to this call's stream and workspace.
-triattn_status blas_for_call(void* blas_ws, cudaStream_t s, cublasHandle_t* out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TRIATTN_ERR_CUDA;
-  cublasHandle_t h = blas_handle(dev);
-  if (h == nullptr) return TRIATTN_ERR_CUDA;
-  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(h, blas_ws, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS)
-    return TRIATTN_ERR_CUDA;
-  *out = h;
-  return TRIATTN_OK;
 }
 
 }  // namespace
@@ -437,10 +231,10 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   float* rstd = reinterpret_cast<float*>(cx + c.rstd);
   uint16_t* P = reinterpret_cast<uint16_t*>(ws + w.p);
   // x = LayerNorm(z)
-  if (trace_call(kKModLnFwd, s, [&] { return ln_fwd_any(d, z, ln_w, ln_b, cx + c.x, mean, rstd, s); }) != cudaSuccess)
+  if (trace_call(kKModLnFwd, s, [&] { return ln_rows_fwd(d.M, C, z, ln_w, ln_b, cx + c.x, mean, rstd, s); }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // P = x W_in
-  if (gemm_traced(h, s, false, false, M, F, C, cx + c.x, C, w_in, F, P, Fp, CUDA_R_16BF) != TRIATTN_OK)
+  if (gemm_traced(kKModGemm, h, s, false, false, M, F, C, cx + c.x, C, w_in, F, P, Fp, CUDA_R_16BF) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // q, k, v and the bias planes
   const size_t dsts[3] = {c.q, c.k, c.v};
@@ -457,7 +251,7 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   if (merge_heads(d, reinterpret_cast<const uint16_t*>(cx + c.o), reinterpret_cast<uint16_t*>(cx + c.oflat), HD, 0,
                   s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  return gemm_traced(h, s, false, false, M, C, HD, cx + c.oflat, HD, w_o, C, out, C, CUDA_R_16BF);
+  return gemm_traced(kKModGemm, h, s, false, false, M, C, HD, cx + c.oflat, HD, w_o, C, out, C, CUDA_R_16BF);
 }
 
 triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void* z, const void* mask,
@@ -485,8 +279,8 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   const int M = static_cast<int>(d.M), C = static_cast<int>(d.C), HD = static_cast<int>(d.HD),
             F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
   // out = o_flat W_o:  dW_o = o_flat^T d_out,  d_oflat = d_out W_o^T
-  if (gemm_traced(h, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, CUDA_R_32F) != TRIATTN_OK ||
-      gemm_traced(h, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, CUDA_R_16BF) != TRIATTN_OK)
+  if (gemm_traced(kKModGemm, h, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, CUDA_R_32F) != TRIATTN_OK ||
+      gemm_traced(kKModGemm, h, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, CUDA_R_16BF) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   if (split_heads(d, reinterpret_cast<const uint16_t*>(ws + w.doflat), HD, 0,
                   reinterpret_cast<uint16_t*>(ws + w.dobuf), s) != cudaSuccess)
@@ -505,21 +299,20 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   if (bias_planes(d, dP, Fp, 3 * HD, reinterpret_cast<uint16_t*>(ws + w.dbias), true, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // P = x W_in:  dW_in = x^T dP,  dx = dP W_in^T (FP32)
-  if (gemm_traced(h, s, true, false, C, F, M, cx + c.x, C, dP, Fp, d_w_in, F, CUDA_R_32F) != TRIATTN_OK ||
-      gemm_traced(h, s, false, true, M, C, F, dP, Fp, w_in, F, ws + w.dx, C, CUDA_R_32F) != TRIATTN_OK)
+  if (gemm_traced(kKModGemm, h, s, true, false, C, F, M, cx + c.x, C, dP, Fp, d_w_in, F, CUDA_R_32F) != TRIATTN_OK ||
+      gemm_traced(kKModGemm, h, s, false, true, M, C, F, dP, Fp, w_in, F, ws + w.dx, C, CUDA_R_32F) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // x = LayerNorm(z)
   float* pg = reinterpret_cast<float*>(ws + w.pg);
   float* pb = reinterpret_cast<float*>(ws + w.pb);
   if (trace_call(kKModLnBwd, s, [&] {
-        return ln_bwd_any(d, z, reinterpret_cast<const float*>(ws + w.dx), ln_w,
+        return ln_rows_bwd(d.M, C, z, reinterpret_cast<const float*>(ws + w.dx), ln_w,
                           reinterpret_cast<const float*>(cx + c.mean), reinterpret_cast<const float*>(cx + c.rstd),
                           dz, pg, pb, s);
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   const cudaError_t e = trace_call(kKModColSum, s, [&] {
-    column_sum_kernel<<<static_cast<unsigned>((2 * d.C + 7) / 8), 256, 0, s>>>(pg, pb, kLnBlocks, C, d_ln_w, d_ln_b);
-    return cudaGetLastError();
+    return column_sums(pg, pb, kLnBlocks, C, d_ln_w, d_ln_b, s);
   });
   return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
 }

@@ -1,0 +1,254 @@
+// Kernels and helpers shared by the pair-tensor layers (the triangle-attention
+// module and the triangle multiplicative update): LayerNorm over the feature
+// axis of a row-major [M, C] pair tensor, forward and backward, the
+// fixed-order sums of the LayerNorm parameter gradients, and the cuBLAS
+// projection GEMMs in row-major terms.
+#pragma once
+#include <cublas_v2.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "kernels.cuh"
+#include "triattn.h"
+
+// Everything here has internal linkage: each translation unit that includes
+// this header gets its own copy of the kernels and of the handle table.
+namespace triattn {
+namespace {
+namespace pairops {
+
+constexpr int kMaxC = 256;          // LayerNorm: up to 8 features per lane
+constexpr int kLnBlocks = 152 * 8;  // fixed: the dgamma / dbeta partial rows depend on it
+constexpr size_t kBlasWorkspace = 32u << 20;
+
+inline bool ln_width_ok(int C) { return C >= 32 && C <= kMaxC && C % 32 == 0; }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// One warp per pair: x = (z - mean) * rstd * gamma + beta (BF16), mean and
+// rstd saved in FP32.  Lane l holds features l, l + 32, ...
+template <int C>
+__global__ void __launch_bounds__(256) ln_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ gamma,
+                                                     const float* __restrict__ beta, uint16_t* __restrict__ x,
+                                                     float* __restrict__ mean_out, float* __restrict__ rstd_out,
+                                                     size_t M) {
+  constexpr int kPer = C / 32;
+  const int lane = threadIdx.x & 31;
+  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
+  for (size_t m = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; m < M; m += warps) {
+    float v[kPer];
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      v[e] = bf16lo_to_f32(z[m * C + lane + 32 * e]);
+      s += v[e];
+    }
+    const float mean = warp_sum(s) * (1.f / C);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) ss += (v[e] - mean) * (v[e] - mean);
+    const float rstd = rsqrtf(warp_sum(ss) * (1.f / C) + 1e-5f);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int c = lane + 32 * e;
+      x[m * C + c] = static_cast<uint16_t>(pack_bf16x2((v[e] - mean) * rstd * gamma[c] + beta[c], 0.f) & 0xFFFFu);
+    }
+    if (lane == 0) {
+      mean_out[m] = mean;
+      rstd_out[m] = rstd;
+    }
+  }
+}
+
+// One warp per pair: dz = rstd (g - mean(g) - xhat mean(g xhat)), g = dx gamma.
+// The warp also accumulates dgamma = sum dx xhat and dbeta = sum dx over its
+// pairs (fixed grid-stride assignment); the block adds its 8 warps' sums in
+// warp order and writes one partial row per block.
+template <int C>
+__global__ void __launch_bounds__(256) ln_bwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ dx,
+                                                     const float* __restrict__ gamma,
+                                                     const float* __restrict__ mean_in,
+                                                     const float* __restrict__ rstd_in, uint16_t* __restrict__ dz,
+                                                     float* __restrict__ part_gamma, float* __restrict__ part_beta,
+                                                     size_t M) {
+  constexpr int kPer = C / 32;
+  __shared__ float red_g[8][C], red_b[8][C];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
+  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
+  float accg[kPer], accb[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) accg[e] = accb[e] = 0.f;
+  for (size_t m = static_cast<size_t>(blockIdx.x) * 8 + warp; m < M; m += warps) {
+    const float mean = mean_in[m], rstd = rstd_in[m];
+    float xh[kPer], g[kPer];
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int c = lane + 32 * e;
+      xh[e] = (bf16lo_to_f32(z[m * C + c]) - mean) * rstd;
+      const float d = dx[m * C + c];
+      accg[e] += d * xh[e];
+      accb[e] += d;
+      g[e] = d * gamma[c];
+      sg += g[e];
+      sgx += g[e] * xh[e];
+    }
+    const float a = warp_sum(sg) * (1.f / C), bb = warp_sum(sgx) * (1.f / C);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      dz[m * C + lane + 32 * e] =
+          static_cast<uint16_t>(pack_bf16x2(rstd * (g[e] - a - xh[e] * bb), 0.f) & 0xFFFFu);
+  }
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    red_g[warp][lane + 32 * e] = accg[e];
+    red_b[warp][lane + 32 * e] = accb[e];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    float sg = 0.f, sb = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      sg += red_g[w][c];
+      sb += red_b[w][c];
+    }
+    part_gamma[static_cast<size_t>(blockIdx.x) * C + c] = sg;
+    part_beta[static_cast<size_t>(blockIdx.x) * C + c] = sb;
+  }
+}
+
+// One warp per output column (columns 0 .. C-1: dgamma from pg, C .. 2C-1:
+// dbeta from pb): lane l adds rows l, l + 32, ... in ascending order, then a
+// fixed butterfly adds the 32 lane sums.
+__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ pg, const float* __restrict__ pb,
+                                                         int rows, int C, float* __restrict__ dgamma,
+                                                         float* __restrict__ dbeta) {
+  const int col = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x & 31;
+  if (col >= 2 * C) return;
+  const float* part = col < C ? pg : pb;
+  const int c = col < C ? col : col - C;
+  float s = 0.f;
+  for (int r = lane; r < rows; r += 32) s += part[static_cast<size_t>(r) * C + c];
+  s = warp_sum(s);
+  if (lane == 0) (col < C ? dgamma : dbeta)[c] = s;
+}
+
+template <int C>
+cudaError_t ln_fwd_launch(size_t M, const void* z, const float* g, const float* b, void* x, float* mean,
+                          float* rstd, cudaStream_t s) {
+  ln_fwd_kernel<C><<<kLnBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), g, b, static_cast<uint16_t*>(x),
+                                             mean, rstd, M);
+  return cudaGetLastError();
+}
+template <int C>
+cudaError_t ln_bwd_launch(size_t M, const void* z, const float* dx, const float* g, const float* mean,
+                          const float* rstd, void* dz, float* pg, float* pb, cudaStream_t s) {
+  ln_bwd_kernel<C><<<kLnBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), dx, g, mean, rstd,
+                                             static_cast<uint16_t*>(dz), pg, pb, M);
+  return cudaGetLastError();
+}
+
+// x = LayerNorm(z) over rows of C features (BF16 in and out), mean and rstd saved.
+inline cudaError_t ln_rows_fwd(size_t M, int C, const void* z, const float* g, const float* b, void* x, float* mean,
+                               float* rstd, cudaStream_t s) {
+  switch (C) {
+    case 32: return ln_fwd_launch<32>(M, z, g, b, x, mean, rstd, s);
+    case 64: return ln_fwd_launch<64>(M, z, g, b, x, mean, rstd, s);
+    case 96: return ln_fwd_launch<96>(M, z, g, b, x, mean, rstd, s);
+    case 128: return ln_fwd_launch<128>(M, z, g, b, x, mean, rstd, s);
+    case 160: return ln_fwd_launch<160>(M, z, g, b, x, mean, rstd, s);
+    case 192: return ln_fwd_launch<192>(M, z, g, b, x, mean, rstd, s);
+    case 224: return ln_fwd_launch<224>(M, z, g, b, x, mean, rstd, s);
+    case 256: return ln_fwd_launch<256>(M, z, g, b, x, mean, rstd, s);
+  }
+  return cudaErrorInvalidValue;
+}
+// dz (BF16) from dx (FP32); kLnBlocks partial rows of dgamma and dbeta.
+inline cudaError_t ln_rows_bwd(size_t M, int C, const void* z, const float* dx, const float* g, const float* mean,
+                               const float* rstd, void* dz, float* pg, float* pb, cudaStream_t s) {
+  switch (C) {
+    case 32: return ln_bwd_launch<32>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+    case 64: return ln_bwd_launch<64>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+    case 96: return ln_bwd_launch<96>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+    case 128: return ln_bwd_launch<128>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+    case 160: return ln_bwd_launch<160>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+    case 192: return ln_bwd_launch<192>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+    case 224: return ln_bwd_launch<224>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+    case 256: return ln_bwd_launch<256>(M, z, dx, g, mean, rstd, dz, pg, pb, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// dgamma / dbeta [C] from `rows` partial rows each, fixed order.
+inline cudaError_t column_sums(const float* pg, const float* pb, int rows, int C, float* dgamma, float* dbeta,
+                               cudaStream_t s) {
+  column_sum_kernel<<<static_cast<unsigned>((2 * C + 7) / 8), 256, 0, s>>>(pg, pb, rows, C, dgamma, dbeta);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- cuBLAS
+// One handle per host thread and device (created on first use, kept for the
+// thread's lifetime), so calls from different threads never share one.
+inline cublasHandle_t blas_handle(int dev) {
+  thread_local cublasHandle_t handles[64] = {};
+  if (handles[dev] == nullptr) {
+    cublasHandle_t h = nullptr;
+    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
+    handles[dev] = h;
+  }
+  return handles[dev];
+}
+
+// The device's cuBLAS handle, bound to this call's stream and a
+// kBlasWorkspace-byte slice of the caller's workspace.
+inline triattn_status blas_for_call(void* blas_ws, cudaStream_t s, cublasHandle_t* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TRIATTN_ERR_CUDA;
+  cublasHandle_t h = blas_handle(dev);
+  if (h == nullptr) return TRIATTN_ERR_CUDA;
+  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
+      cublasSetWorkspace(h, blas_ws, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS)
+    return TRIATTN_ERR_CUDA;
+  *out = h;
+  return TRIATTN_OK;
+}
+
+// Row-major C[M, N] = op(A) op(B), A [M, K] (or [K, M] when ta), B [K, N] (or
+// [N, K] when tb); lda / ldb / ldc are the stored row lengths.  In cuBLAS's
+// column-major terms this is C^T = op(B)^T op(A)^T.  `batch` > 1 repeats it
+// over matrices strideA / strideB / strideC elements apart.
+inline cublasStatus_t gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, const void* A, int lda,
+                              const void* B, int ldb, void* C, int ldc, cudaDataType_t ct, int batch = 1,
+                              long long strideA = 0, long long strideB = 0, long long strideC = 0) {
+  const float one = 1.f, zero = 0.f;
+  const cublasOperation_t opA = ta ? CUBLAS_OP_T : CUBLAS_OP_N, opB = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
+  if (batch == 1)
+    return cublasGemmEx(h, opB, opA, N, M, K, &one, B, CUDA_R_16BF, ldb, A, CUDA_R_16BF, lda, &zero, C, ct, ldc,
+                        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  return cublasGemmStridedBatchedEx(h, opB, opA, N, M, K, &one, B, CUDA_R_16BF, ldb, strideB, A, CUDA_R_16BF, lda,
+                                    strideA, &zero, C, ct, ldc, strideC, batch, CUBLAS_COMPUTE_32F,
+                                    CUBLAS_GEMM_DEFAULT);
+}
+
+// gemm_rm as one traced launch of kind `kind`.
+inline triattn_status gemm_traced(int kind, cublasHandle_t h, cudaStream_t s, bool ta, bool tb, int M, int N, int K,
+                                  const void* A, int lda, const void* B, int ldb, void* C, int ldc,
+                                  cudaDataType_t ct, int batch = 1, long long strideA = 0, long long strideB = 0,
+                                  long long strideC = 0) {
+  cublasStatus_t bs = CUBLAS_STATUS_SUCCESS;
+  const cudaError_t e = trace_call(kind, s, [&] {
+    bs = gemm_rm(h, ta, tb, M, N, K, A, lda, B, ldb, C, ldc, ct, batch, strideA, strideB, strideC);
+    return cudaGetLastError();
+  });
+  return (e == cudaSuccess && bs == CUBLAS_STATUS_SUCCESS) ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+}
+
+}  // namespace pairops
+}  // namespace
+}  // namespace triattn

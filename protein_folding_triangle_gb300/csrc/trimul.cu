@@ -1,0 +1,675 @@
+// Triangle multiplicative update, outgoing and incoming, forward and backward
+// ("TurboPairFormer", Figure 12; shapes from Table 10).  With M = B*N*N pairs:
+//
+//   x = LayerNorm(z)                               z, x  [M, C_z]
+//   p = x W_p                                      W_p   [C_z, 4 C_h + C_z]
+//   a = m sigmoid(p_ag) p_av,  b = m sigmoid(p_bg) p_bv   (m: optional pair mask)
+//   outgoing: X[b,i,j,c] = sum_k a[b,i,k,c] b[b,j,k,c]
+//   incoming: X[b,i,j,c] = sum_k a[b,k,i,c] b[b,k,j,c]
+//   out = sigmoid(p_g) (LayerNorm(X) W_o)          W_o   [C_h, C_z]
+//
+// Data layout.  The pair tensors z, x, p, y = LayerNorm(X), u = y W_o are
+// pair-major rows.  The branch operands a, b, the contraction output X and
+// their gradients are channel-major: [B][C_h][N][N], so that channel c of
+// example b is one row-major N x N matrix A_c (A_c[r][s] = a[b,r,s,c]).  Both
+// directions and all three products of the contraction are then one
+// strided-batched GEMM over the B*C_h matrices with the right operand flags:
+//   outgoing  X_c = A_c B_c^T    dA_c = dX_c B_c     dB_c = dX_c^T A_c
+//   incoming  X_c = A_c^T B_c    dA_c = B_c dX_c^T   dB_c = A_c dX_c
+// The kernels here do the gating and masking while transposing pair-major
+// projections into the channel-major operands (64 pairs per block through
+// shared memory), the output LayerNorm while transposing X back, the output
+// gate, and their backward passes; the projection GEMMs and the contraction
+// are cuBLAS (BF16 operands, FP32 accumulation).  No floating-point atomics:
+// every reduction has a fixed order.
+#include <cublas_v2.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <type_traits>
+
+#include "kernels.cuh"
+#include "pairops.cuh"
+#include "triattn.h"
+
+namespace triattn {
+namespace {
+
+using namespace pairops;
+
+constexpr int kPairs = 64;         // pairs per block of the channel-major kernels
+constexpr int kRow = kPairs + 1;   // padded shared-memory row (floats)
+constexpr int kCmBwdBlocks = 152 * 2;  // fixed: the output-LayerNorm partial rows depend on it
+
+__device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + __expf(-x)); }
+
+__device__ __forceinline__ void unpack8(const uint4 w, float (&f)[8]) {
+  f[0] = bf16lo_to_f32(w.x); f[1] = bf16hi_to_f32(w.x);
+  f[2] = bf16lo_to_f32(w.y); f[3] = bf16hi_to_f32(w.y);
+  f[4] = bf16lo_to_f32(w.z); f[5] = bf16hi_to_f32(w.z);
+  f[6] = bf16lo_to_f32(w.w); f[7] = bf16hi_to_f32(w.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 ld16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void st16(uint16_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+__device__ __forceinline__ float mask_at(const uint16_t* mask, size_t m) {
+  return mask == nullptr ? 1.f : bf16lo_to_f32(mask[m]);
+}
+
+// Load the [Ch][64] channel-major tile of pairs [pos0, pos0 + 64) of example b
+// into shared memory as FP32 rows of kRow.
+template <int Ch>
+__device__ __forceinline__ void load_cm_tile(const uint16_t* __restrict__ src, size_t b, size_t pos0, size_t NN,
+                                             float* s) {
+  for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
+    const int c = it >> 3, q = it & 7;
+    float f[8];
+    unpack8(ld16(src + (b * Ch + c) * NN + pos0 + 8 * q), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[c * kRow + 8 * q + e] = f[e];
+  }
+}
+// Store a [Ch][64] FP32 shared tile as BF16 channel-major rows.
+template <int Ch>
+__device__ __forceinline__ void store_cm_tile(const float* s, uint16_t* __restrict__ dst, size_t b, size_t pos0,
+                                              size_t NN) {
+  for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
+    const int c = it >> 3, q = it & 7;
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = s[c * kRow + 8 * q + e];
+    st16(dst + (b * Ch + c) * NN + pos0 + 8 * q, pack8(f));
+  }
+}
+
+// a = m sigmoid(p_ag) p_av and b = m sigmoid(p_bg) p_bv for 64 consecutive
+// pairs, written channel-major.  Phase 1: thread (pair couple pp, 8-channel
+// chunk cc) gates two pairs and packs them per channel into one shared word;
+// phase 2: every channel row of 64 pairs goes out as 8 16-byte stores.
+template <int Ch>
+__global__ void __launch_bounds__(256) gate_fwd_kernel(const uint16_t* __restrict__ p, int ld,
+                                                       const uint16_t* __restrict__ mask, uint16_t* __restrict__ A,
+                                                       uint16_t* __restrict__ Bo, size_t NN) {
+  __shared__ uint32_t sA[Ch][33], sB[Ch][33];
+  const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
+  const size_t b = m0 / NN, pos0 = m0 % NN;
+  for (int it = threadIdx.x; it < 32 * (Ch / 8); it += blockDim.x) {
+    const int pp = it & 31, cc = it >> 5;
+    float ga[2][8], gb[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const size_t m = m0 + 2 * pp + h;
+      const uint16_t* row = p + m * ld + 8 * cc;
+      float av[8], ag[8], bv[8], bg[8];
+      unpack8(ld16(row), av);
+      unpack8(ld16(row + Ch), ag);
+      unpack8(ld16(row + 2 * Ch), bv);
+      unpack8(ld16(row + 3 * Ch), bg);
+      const float mk = mask_at(mask, m);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        ga[h][e] = mk * sigm(ag[e]) * av[e];
+        gb[h][e] = mk * sigm(bg[e]) * bv[e];
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sA[8 * cc + e][pp] = pack_bf16x2(ga[0][e], ga[1][e]);
+      sB[8 * cc + e][pp] = pack_bf16x2(gb[0][e], gb[1][e]);
+    }
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
+    const int c = it >> 3, q = it & 7;
+    const size_t off = (b * Ch + c) * NN + pos0 + 8 * q;
+    st16(A + off, make_uint4(sA[c][4 * q], sA[c][4 * q + 1], sA[c][4 * q + 2], sA[c][4 * q + 3]));
+    st16(Bo + off, make_uint4(sB[c][4 * q], sB[c][4 * q + 1], sB[c][4 * q + 2], sB[c][4 * q + 3]));
+  }
+}
+
+// y = LayerNorm(X) for 64 pairs: X channel-major in, y pair-major out (BF16),
+// mean and rstd saved.  Thread (pair pr, quarter qq) owns the 8-channel
+// chunks qq, qq + 4, ...; the four threads of a pair are adjacent lanes.
+template <int Ch>
+__global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restrict__ X,
+                                                        const float* __restrict__ gamma,
+                                                        const float* __restrict__ beta, uint16_t* __restrict__ y,
+                                                        float* __restrict__ mean_out, float* __restrict__ rstd_out,
+                                                        size_t NN) {
+  extern __shared__ float sX[];  // [Ch][kRow]
+  constexpr int kCh = Ch / 32;
+  const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
+  const size_t b = m0 / NN, pos0 = m0 % NN;
+  load_cm_tile<Ch>(X, b, pos0, NN, sX);
+  __syncthreads();
+  const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
+  float v[kCh][8];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCh; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[i][e] = sX[(8 * (qq + 4 * i) + e) * kRow + pr];
+      s += v[i][e];
+    }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  const float mean = s * (1.f / Ch);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCh; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss += (v[i][e] - mean) * (v[i][e] - mean);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  const float rstd = rsqrtf(ss * (1.f / Ch) + 1e-5f);
+  const size_t m = m0 + pr;
+#pragma unroll
+  for (int i = 0; i < kCh; ++i) {
+    const int c0 = 8 * (qq + 4 * i);
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = (v[i][e] - mean) * rstd * gamma[c0 + e] + beta[c0 + e];
+    st16(y + m * Ch + c0, pack8(o));
+  }
+  if (qq == 0) {
+    mean_out[m] = mean;
+    rstd_out[m] = rstd;
+  }
+}
+
+// Backward of the output LayerNorm: dX (channel-major BF16) from dy (pair-major
+// FP32) and X; per block the dgamma / dbeta sums over its tiles, each channel
+// added by one thread over the tile's 64 pairs in order, one partial row per
+// block.
+template <int Ch>
+__global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restrict__ X,
+                                                        const float* __restrict__ dy,
+                                                        const float* __restrict__ gamma,
+                                                        const float* __restrict__ mean_in,
+                                                        const float* __restrict__ rstd_in,
+                                                        uint16_t* __restrict__ dX, float* __restrict__ part_g,
+                                                        float* __restrict__ part_b, size_t NN, size_t tiles) {
+  extern __shared__ float sm[];
+  float* sX = sm;                 // X, then dX
+  float* sG = sm + Ch * kRow;     // dy * xhat
+  float* sD = sm + 2 * Ch * kRow; // dy
+  constexpr int kCh = Ch / 32;
+  const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
+  float accg = 0.f, accb = 0.f;
+  for (size_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const size_t m0 = tile * kPairs;
+    const size_t b = m0 / NN, pos0 = m0 % NN;
+    load_cm_tile<Ch>(X, b, pos0, NN, sX);
+    __syncthreads();
+    const size_t m = m0 + pr;
+    const float mean = mean_in[m], rstd = rstd_in[m];
+    float xh[kCh][8], g[kCh][8];
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int i = 0; i < kCh; ++i) {
+      const int c0 = 8 * (qq + 4 * i);
+      const float4 d0 = *reinterpret_cast<const float4*>(dy + m * Ch + c0);
+      const float4 d1 = *reinterpret_cast<const float4*>(dy + m * Ch + c0 + 4);
+      const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = c0 + e;
+        xh[i][e] = (sX[c * kRow + pr] - mean) * rstd;
+        g[i][e] = dv[e] * gamma[c];
+        sg += g[i][e];
+        sgx += g[i][e] * xh[i][e];
+        sG[c * kRow + pr] = dv[e] * xh[i][e];
+        sD[c * kRow + pr] = dv[e];
+      }
+    }
+    sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+    sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+    sgx += __shfl_xor_sync(0xffffffffu, sgx, 1);
+    sgx += __shfl_xor_sync(0xffffffffu, sgx, 2);
+    const float a = sg * (1.f / Ch), bb = sgx * (1.f / Ch);
+#pragma unroll
+    for (int i = 0; i < kCh; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sX[(8 * (qq + 4 * i) + e) * kRow + pr] = rstd * (g[i][e] - a - xh[i][e] * bb);
+    __syncthreads();
+    store_cm_tile<Ch>(sX, dX, b, pos0, NN);
+    if (threadIdx.x < Ch) {
+      for (int q = 0; q < kPairs; ++q) {
+        accg += sG[threadIdx.x * kRow + q];
+        accb += sD[threadIdx.x * kRow + q];
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < Ch) {
+    part_g[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = accg;
+    part_b[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = accb;
+  }
+}
+
+// Backward of the gating: dp's first 4 C_h columns (pair-major) from dA, dB
+// (channel-major) and the saved projections.
+template <int Ch>
+__global__ void __launch_bounds__(256) gate_bwd_kernel(const uint16_t* __restrict__ dA,
+                                                       const uint16_t* __restrict__ dB,
+                                                       const uint16_t* __restrict__ p, int ld,
+                                                       const uint16_t* __restrict__ mask,
+                                                       uint16_t* __restrict__ dp, size_t NN) {
+  extern __shared__ float sm[];
+  float* sA = sm;
+  float* sB = sm + Ch * kRow;
+  constexpr int kCh = Ch / 32;
+  const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
+  const size_t b = m0 / NN, pos0 = m0 % NN;
+  load_cm_tile<Ch>(dA, b, pos0, NN, sA);
+  load_cm_tile<Ch>(dB, b, pos0, NN, sB);
+  __syncthreads();
+  const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
+  const size_t m = m0 + pr;
+  const float mk = mask_at(mask, m);
+  const uint16_t* row = p + m * ld;
+  uint16_t* drow = dp + m * ld;
+#pragma unroll
+  for (int i = 0; i < kCh; ++i) {
+    const int c0 = 8 * (qq + 4 * i);
+    float av[8], ag[8], bv[8], bg[8], dav[8], dag[8], dbv[8], dbg[8];
+    unpack8(ld16(row + c0), av);
+    unpack8(ld16(row + Ch + c0), ag);
+    unpack8(ld16(row + 2 * Ch + c0), bv);
+    unpack8(ld16(row + 3 * Ch + c0), bg);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float da = sA[(c0 + e) * kRow + pr] * mk, db = sB[(c0 + e) * kRow + pr] * mk;
+      const float sa = sigm(ag[e]), sb = sigm(bg[e]);
+      dav[e] = da * sa;
+      dag[e] = da * av[e] * sa * (1.f - sa);
+      dbv[e] = db * sb;
+      dbg[e] = db * bv[e] * sb * (1.f - sb);
+    }
+    st16(drow + c0, pack8(dav));
+    st16(drow + Ch + c0, pack8(dag));
+    st16(drow + 2 * Ch + c0, pack8(dbv));
+    st16(drow + 3 * Ch + c0, pack8(dbg));
+  }
+}
+
+// out = sigmoid(g) u, 8 features per thread (g = p's last C_z columns).
+__global__ void __launch_bounds__(256) gate_out_kernel(const uint16_t* __restrict__ p, int ld, int goff,
+                                                       const uint16_t* __restrict__ u, uint16_t* __restrict__ out,
+                                                       int Cz, size_t M) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int chunks = Cz / 8;
+  if (t >= M * chunks) return;
+  const size_t m = t / chunks;
+  const int c0 = 8 * static_cast<int>(t % chunks);
+  float g[8], uv[8], o[8];
+  unpack8(ld16(p + m * ld + goff + c0), g);
+  unpack8(ld16(u + m * Cz + c0), uv);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = sigm(g[e]) * uv[e];
+  st16(out + m * Cz + c0, pack8(o));
+}
+
+// Backward of the output gate: du = d_out sigmoid(g) (BF16 [M, C_z]) and
+// dp[:, goff + c] = d_out u sigmoid(g) (1 - sigmoid(g)).
+__global__ void __launch_bounds__(256) gate_out_bwd_kernel(const uint16_t* __restrict__ p, int ld, int goff,
+                                                           const uint16_t* __restrict__ u,
+                                                           const uint16_t* __restrict__ d_out,
+                                                           uint16_t* __restrict__ du, uint16_t* __restrict__ dp,
+                                                           int Cz, size_t M) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int chunks = Cz / 8;
+  if (t >= M * chunks) return;
+  const size_t m = t / chunks;
+  const int c0 = 8 * static_cast<int>(t % chunks);
+  float g[8], uv[8], d[8], o1[8], o2[8];
+  unpack8(ld16(p + m * ld + goff + c0), g);
+  unpack8(ld16(u + m * Cz + c0), uv);
+  unpack8(ld16(d_out + m * Cz + c0), d);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float sg = sigm(g[e]);
+    o1[e] = d[e] * sg;
+    o2[e] = d[e] * uv[e] * sg * (1.f - sg);
+  }
+  st16(du + m * Cz + c0, pack8(o1));
+  st16(dp + m * ld + goff + c0, pack8(o2));
+}
+
+// ---------------------------------------------------------------- host side
+size_t rup(size_t x) { return (x + 255) / 256 * 256; }
+
+struct TmDims {
+  size_t B, N, NN, M, Cz, Ch, F, Fp;
+  bool incoming;
+};
+TmDims tm_dims(const triattn_trimul_shape* s) {
+  TmDims d;
+  d.B = s->B;
+  d.N = s->N;
+  d.NN = d.N * d.N;
+  d.M = d.B * d.NN;
+  d.Cz = s->C_z;
+  d.Ch = s->C_h;
+  d.F = 4 * d.Ch + d.Cz;
+  d.Fp = (d.F + 7) / 8 * 8;
+  d.incoming = s->direction == TRIATTN_TRIMUL_INCOMING;
+  return d;
+}
+
+struct TmCtx {
+  size_t x, mean_in, rstd_in, p, a, b, X, mean_out, rstd_out, y, u, total;
+};
+TmCtx tm_ctx(const TmDims& d) {
+  TmCtx c;
+  size_t o = 0;
+  const size_t cm = d.B * d.Ch * d.NN * 2;
+  c.x = o;        o += rup(d.M * d.Cz * 2);
+  c.mean_in = o;  o += rup(d.M * 4);
+  c.rstd_in = o;  o += rup(d.M * 4);
+  c.p = o;        o += rup(d.M * d.Fp * 2);
+  c.a = o;        o += rup(cm);
+  c.b = o;        o += rup(cm);
+  c.X = o;        o += rup(cm);
+  c.mean_out = o; o += rup(d.M * 4);
+  c.rstd_out = o; o += rup(d.M * 4);
+  c.y = o;        o += rup(d.M * d.Ch * 2);
+  c.u = o;        o += rup(d.M * d.Cz * 2);
+  c.total = o;
+  return c;
+}
+
+struct TmWs {
+  size_t blas, du, dp, dy, dX, dA, dB, dx, pg_in, pb_in, pg_out, pb_out, total;
+};
+TmWs tm_ws(const TmDims& d) {
+  TmWs w;
+  size_t o = 0;
+  const size_t cm = d.B * d.Ch * d.NN * 2;
+  w.blas = o;   o += rup(kBlasWorkspace);
+  w.du = o;     o += rup(d.M * d.Cz * 2);
+  w.dp = o;     o += rup(d.M * d.Fp * 2);
+  w.dy = o;     o += rup(d.M * d.Ch * 4);
+  w.dX = o;     o += rup(cm);
+  w.dA = o;     o += rup(cm);
+  w.dB = o;     o += rup(cm);
+  w.dx = o;     o += rup(d.M * d.Cz * 4);
+  w.pg_in = o;  o += rup(static_cast<size_t>(kLnBlocks) * d.Cz * 4);
+  w.pb_in = o;  o += rup(static_cast<size_t>(kLnBlocks) * d.Cz * 4);
+  w.pg_out = o; o += rup(static_cast<size_t>(kCmBwdBlocks) * d.Ch * 4);
+  w.pb_out = o; o += rup(static_cast<size_t>(kCmBwdBlocks) * d.Ch * 4);
+  w.total = o;
+  return w;
+}
+
+triattn_status check_trimul(const triattn_trimul_shape* s) {
+  if (s == nullptr || s->flags != 0 || s->B < 1 || s->N < 1 || s->C_z < 1 || s->C_h < 1 ||
+      (s->direction != TRIATTN_TRIMUL_OUTGOING && s->direction != TRIATTN_TRIMUL_INCOMING))
+    return TRIATTN_ERR_INVALID_ARG;
+  if (s->N % 8 != 0 || s->N > 4096 || !ln_width_ok(s->C_z) || s->C_h % 32 != 0 || s->C_h > 128)
+    return TRIATTN_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(s->B) * s->N * s->N > 0x7fffffffull) return TRIATTN_ERR_UNSUPPORTED;
+  return TRIATTN_OK;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+unsigned blocks_for(size_t n) { return static_cast<unsigned>((n + 255) / 256); }
+
+template <int Ch>
+cudaError_t set_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(ln_cm_fwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Ch * kRow * 4);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ln_cm_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * Ch * kRow * 4);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gate_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * Ch * kRow * 4);
+  return e;
+}
+
+// The channel-major kernels, dispatched on C_h.
+struct CmLaunch {
+  const TmDims& d;
+  cudaStream_t s;
+
+  template <int Ch>
+  cudaError_t gate_fwd(const uint16_t* p, const uint16_t* mask, uint16_t* A, uint16_t* B) const {
+    gate_fwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, 0, s>>>(p, static_cast<int>(d.Fp), mask, A, B,
+                                                                            d.NN);
+    return cudaGetLastError();
+  }
+  template <int Ch>
+  cudaError_t ln_fwd(const uint16_t* X, const float* g, const float* b, uint16_t* y, float* mean, float* rstd) const {
+    cudaError_t e = set_attrs<Ch>();
+    if (e != cudaSuccess) return e;
+    ln_cm_fwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, Ch * kRow * 4, s>>>(X, g, b, y, mean, rstd,
+                                                                                          d.NN);
+    return cudaGetLastError();
+  }
+  template <int Ch>
+  cudaError_t ln_bwd(const uint16_t* X, const float* dy, const float* g, const float* mean, const float* rstd,
+                     uint16_t* dX, float* pg, float* pb) const {
+    cudaError_t e = set_attrs<Ch>();
+    if (e != cudaSuccess) return e;
+    const size_t tiles = d.M / kPairs;
+    ln_cm_bwd_kernel<Ch><<<kCmBwdBlocks, 256, 3 * Ch * kRow * 4, s>>>(X, dy, g, mean, rstd, dX, pg, pb, d.NN, tiles);
+    return cudaGetLastError();
+  }
+  template <int Ch>
+  cudaError_t gate_bwd(const uint16_t* dA, const uint16_t* dB, const uint16_t* p, const uint16_t* mask,
+                       uint16_t* dp) const {
+    cudaError_t e = set_attrs<Ch>();
+    if (e != cudaSuccess) return e;
+    gate_bwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, 2 * Ch * kRow * 4, s>>>(
+        dA, dB, p, static_cast<int>(d.Fp), mask, dp, d.NN);
+    return cudaGetLastError();
+  }
+};
+
+// f(std::integral_constant<int, Ch>) for the supported C_h.
+template <typename F>
+cudaError_t by_ch(size_t Ch, F&& f) {
+  switch (Ch) {
+    case 32: return f(std::integral_constant<int, 32>{});
+    case 64: return f(std::integral_constant<int, 64>{});
+    case 96: return f(std::integral_constant<int, 96>{});
+    case 128: return f(std::integral_constant<int, 128>{});
+  }
+  return cudaErrorInvalidValue;
+}
+
+// The contraction as one strided-batched GEMM over the B * C_h channel
+// matrices: C_c = op(P_c) op(Q_c), every matrix N x N, row-major.
+triattn_status contract(cublasHandle_t h, cudaStream_t s, const TmDims& d, bool tp, bool tq, const void* P,
+                        const void* Q, void* C) {
+  const int n = static_cast<int>(d.N);
+  const long long st = static_cast<long long>(d.NN);
+  return gemm_traced(kKTmContract, h, s, tp, tq, n, n, n, P, n, Q, n, C, n, CUDA_R_16BF, static_cast<int>(d.B * d.Ch),
+                     st, st, st);
+}
+
+}  // namespace
+}  // namespace triattn
+
+using namespace triattn;
+
+extern "C" {
+
+size_t triattn_trimul_ctx_bytes(const triattn_trimul_shape* shape) {
+  if (check_trimul(shape) != TRIATTN_OK) return 0;
+  return tm_ctx(tm_dims(shape)).total;
+}
+
+size_t triattn_trimul_workspace_bytes(const triattn_trimul_shape* shape) {
+  if (check_trimul(shape) != TRIATTN_OK) return 0;
+  return tm_ws(tm_dims(shape)).total;
+}
+
+triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void* z, const void* mask,
+                                  const float* ln_in_w, const float* ln_in_b, const void* w_p,
+                                  const float* ln_out_w, const float* ln_out_b, const void* w_o, void* out,
+                                  void* ctx, void* workspace, size_t workspace_bytes, void* stream) {
+  triattn_status st = check_trimul(shape);
+  if (st != TRIATTN_OK) return st;
+  const void* req[] = {z, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o, out, ctx};
+  for (const void* q : req)
+    if (q == nullptr || !al16(q)) return TRIATTN_ERR_INVALID_ARG;
+  if ((mask != nullptr && !al16(mask)) || (reinterpret_cast<uintptr_t>(ctx) & 255u) != 0)
+    return TRIATTN_ERR_INVALID_ARG;
+  const TmDims d = tm_dims(shape);
+  const TmCtx c = tm_ctx(d);
+  const TmWs w = tm_ws(d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return TRIATTN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* cx = static_cast<uint8_t*>(ctx);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cublasHandle_t h = nullptr;
+  if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
+  const int M = static_cast<int>(d.M), Cz = static_cast<int>(d.Cz), Ch = static_cast<int>(d.Ch),
+            F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
+  const uint16_t* mk = static_cast<const uint16_t*>(mask);
+  uint16_t* P = reinterpret_cast<uint16_t*>(cx + c.p);
+  uint16_t* A = reinterpret_cast<uint16_t*>(cx + c.a);
+  uint16_t* Bo = reinterpret_cast<uint16_t*>(cx + c.b);
+  uint16_t* X = reinterpret_cast<uint16_t*>(cx + c.X);
+  uint16_t* y = reinterpret_cast<uint16_t*>(cx + c.y);
+  uint16_t* u = reinterpret_cast<uint16_t*>(cx + c.u);
+  const CmLaunch L{d, s};
+  // x = LayerNorm(z);  p = x W_p
+  if (trace_call(kKTmLnIn, s, [&] {
+        return ln_rows_fwd(d.M, Cz, z, ln_in_w, ln_in_b, cx + c.x, reinterpret_cast<float*>(cx + c.mean_in),
+                           reinterpret_cast<float*>(cx + c.rstd_in), s);
+      }) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  if (gemm_traced(kKTmProj, h, s, false, false, M, F, Cz, cx + c.x, Cz, w_p, F, P, Fp, CUDA_R_16BF) != TRIATTN_OK)
+    return TRIATTN_ERR_CUDA;
+  // a, b: gated, masked, channel-major
+  if (trace_call(kKTmGate, s, [&] {
+        return by_ch(d.Ch, [&](auto ic) { return L.template gate_fwd<decltype(ic)::value>(P, mk, A, Bo); });
+      }) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  // X_c = A_c B_c^T (outgoing) or A_c^T B_c (incoming)
+  if (contract(h, s, d, d.incoming, !d.incoming, A, Bo, X) != TRIATTN_OK) return TRIATTN_ERR_CUDA;
+  // y = LayerNorm(X) (pair-major);  u = y W_o;  out = sigmoid(g) u
+  if (trace_call(kKTmLnOut, s, [&] {
+        return by_ch(d.Ch, [&](auto ic) {
+          return L.template ln_fwd<decltype(ic)::value>(X, ln_out_w, ln_out_b, y,
+                                                        reinterpret_cast<float*>(cx + c.mean_out),
+                                                        reinterpret_cast<float*>(cx + c.rstd_out));
+        });
+      }) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  if (gemm_traced(kKTmProj, h, s, false, false, M, Cz, Ch, y, Ch, w_o, Cz, u, Cz, CUDA_R_16BF) != TRIATTN_OK)
+    return TRIATTN_ERR_CUDA;
+  const cudaError_t e = trace_call(kKTmOutGate, s, [&] {
+    gate_out_kernel<<<blocks_for(d.M * d.Cz / 8), 256, 0, s>>>(P, Fp, 4 * Ch, u, static_cast<uint16_t*>(out), Cz,
+                                                               d.M);
+    return cudaGetLastError();
+  });
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+}
+
+triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void* z, const void* mask,
+                                  const float* ln_in_w, const void* w_p, const float* ln_out_w, const void* w_o,
+                                  const void* ctx, const void* d_out, void* dz, float* d_ln_in_w, float* d_ln_in_b,
+                                  float* d_w_p, float* d_ln_out_w, float* d_ln_out_b, float* d_w_o,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  triattn_status st = check_trimul(shape);
+  if (st != TRIATTN_OK) return st;
+  const void* req[] = {z, ln_in_w, w_p, ln_out_w, w_o, ctx, d_out, dz, d_ln_in_w, d_ln_in_b, d_w_p,
+                       d_ln_out_w, d_ln_out_b, d_w_o};
+  for (const void* q : req)
+    if (q == nullptr || !al16(q)) return TRIATTN_ERR_INVALID_ARG;
+  if ((mask != nullptr && !al16(mask)) || (reinterpret_cast<uintptr_t>(ctx) & 255u) != 0)
+    return TRIATTN_ERR_INVALID_ARG;
+  const TmDims d = tm_dims(shape);
+  const TmCtx c = tm_ctx(d);
+  const TmWs w = tm_ws(d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return TRIATTN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* cx = static_cast<const uint8_t*>(ctx);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cublasHandle_t h = nullptr;
+  if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
+  const int M = static_cast<int>(d.M), Cz = static_cast<int>(d.Cz), Ch = static_cast<int>(d.Ch),
+            F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
+  const uint16_t* mk = static_cast<const uint16_t*>(mask);
+  const uint16_t* P = reinterpret_cast<const uint16_t*>(cx + c.p);
+  const uint16_t* A = reinterpret_cast<const uint16_t*>(cx + c.a);
+  const uint16_t* Bo = reinterpret_cast<const uint16_t*>(cx + c.b);
+  const uint16_t* X = reinterpret_cast<const uint16_t*>(cx + c.X);
+  uint16_t* du = reinterpret_cast<uint16_t*>(ws + w.du);
+  uint16_t* dp = reinterpret_cast<uint16_t*>(ws + w.dp);
+  float* dy = reinterpret_cast<float*>(ws + w.dy);
+  uint16_t* dX = reinterpret_cast<uint16_t*>(ws + w.dX);
+  uint16_t* dA = reinterpret_cast<uint16_t*>(ws + w.dA);
+  uint16_t* dB = reinterpret_cast<uint16_t*>(ws + w.dB);
+  float* dx = reinterpret_cast<float*>(ws + w.dx);
+  const CmLaunch L{d, s};
+  // out = sigmoid(g) u:  du, and dp's output-gate columns
+  if (trace_call(kKTmOutGate, s, [&] {
+        gate_out_bwd_kernel<<<blocks_for(d.M * d.Cz / 8), 256, 0, s>>>(
+            P, Fp, 4 * Ch, reinterpret_cast<const uint16_t*>(cx + c.u), static_cast<const uint16_t*>(d_out), du, dp,
+            Cz, d.M);
+        return cudaGetLastError();
+      }) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  // u = y W_o:  dW_o = y^T du,  dy = du W_o^T (FP32)
+  if (gemm_traced(kKTmProj, h, s, true, false, Ch, Cz, M, cx + c.y, Ch, du, Cz, d_w_o, Cz, CUDA_R_32F) !=
+          TRIATTN_OK ||
+      gemm_traced(kKTmProj, h, s, false, true, M, Ch, Cz, du, Cz, w_o, Cz, dy, Ch, CUDA_R_32F) != TRIATTN_OK)
+    return TRIATTN_ERR_CUDA;
+  // y = LayerNorm(X):  dX (channel-major), output-LayerNorm partial sums
+  float* pg_out = reinterpret_cast<float*>(ws + w.pg_out);
+  float* pb_out = reinterpret_cast<float*>(ws + w.pb_out);
+  if (trace_call(kKTmLnOut, s, [&] {
+        return by_ch(d.Ch, [&](auto ic) {
+          return L.template ln_bwd<decltype(ic)::value>(X, dy, ln_out_w,
+                                                        reinterpret_cast<const float*>(cx + c.mean_out),
+                                                        reinterpret_cast<const float*>(cx + c.rstd_out), dX, pg_out,
+                                                        pb_out);
+        });
+      }) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  // the contraction
+  triattn_status cs;
+  if (!d.incoming) {
+    cs = contract(h, s, d, false, false, dX, Bo, dA);                      // dA_c = dX_c B_c
+    if (cs == TRIATTN_OK) cs = contract(h, s, d, true, false, dX, A, dB);  // dB_c = dX_c^T A_c
+  } else {
+    cs = contract(h, s, d, false, true, Bo, dX, dA);                       // dA_c = B_c dX_c^T
+    if (cs == TRIATTN_OK) cs = contract(h, s, d, false, false, A, dX, dB); // dB_c = A_c dX_c
+  }
+  if (cs != TRIATTN_OK) return cs;
+  // the gating:  dp's first 4 C_h columns
+  if (trace_call(kKTmGate, s, [&] {
+        return by_ch(d.Ch, [&](auto ic) { return L.template gate_bwd<decltype(ic)::value>(dA, dB, P, mk, dp); });
+      }) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  // p = x W_p:  dW_p = x^T dp,  dx = dp W_p^T (FP32)
+  if (gemm_traced(kKTmProj, h, s, true, false, Cz, F, M, cx + c.x, Cz, dp, Fp, d_w_p, F, CUDA_R_32F) != TRIATTN_OK ||
+      gemm_traced(kKTmProj, h, s, false, true, M, Cz, F, dp, Fp, w_p, F, dx, Cz, CUDA_R_32F) != TRIATTN_OK)
+    return TRIATTN_ERR_CUDA;
+  // x = LayerNorm(z)
+  float* pg_in = reinterpret_cast<float*>(ws + w.pg_in);
+  float* pb_in = reinterpret_cast<float*>(ws + w.pb_in);
+  if (trace_call(kKTmLnIn, s, [&] {
+        return ln_rows_bwd(d.M, Cz, z, dx, ln_in_w, reinterpret_cast<const float*>(cx + c.mean_in),
+                           reinterpret_cast<const float*>(cx + c.rstd_in), dz, pg_in, pb_in, s);
+      }) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
+  const cudaError_t e = trace_call(kKTmColSum, s, [&] {
+    cudaError_t r = column_sums(pg_in, pb_in, kLnBlocks, Cz, d_ln_in_w, d_ln_in_b, s);
+    if (r == cudaSuccess) r = column_sums(pg_out, pb_out, kCmBwdBlocks, Ch, d_ln_out_w, d_ln_out_b, s);
+    return r;
+  });
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -143,3 +143,37 @@ def make_module_inputs(B: int, N: int, C: int, H: int, D: int, seed: int = 0, ma
         mask = mask.to(torch.bfloat16)
     return {"z": z, "d_out": d_out, "ln_w": ln_w, "ln_b": ln_b, "w_in": w_in, "w_o": w_o, "mask": mask,
             "H": H, "D": D}
+
+
+def make_trimul_inputs(B: int, N: int, Cz: int, Ch: int, seed: int = 0, pad_frac: float = 0.0) -> dict:
+    """Seeded inputs of the triangle multiplicative update (CPU tensors): z
+    and d_out [B, N, N, C_z] BF16 (standard normal); LayerNorm scales
+    1 + 0.1 n and shifts 0.1 n (FP32) for the input (C_z) and output (C_h)
+    normalizations; W_p [C_z, 4 C_h + C_z] with entries n / sqrt(C_z) and W_o
+    [C_h, C_z] with entries n / sqrt(C_h) (BF16).  Draw order: z, d_out,
+    ln_in_w, ln_in_b, W_p, ln_out_w, ln_out_b, W_o.  With ``pad_frac`` > 0 the
+    last ``int(pad_frac * N)`` tokens are padding: the multiplicative pair
+    mask [B, N, N] (BF16) is 0 for every pair that touches one, else 1;
+    otherwise the mask is None."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+
+    def normal(shape, scale=1.0):
+        return torch.randn(shape, generator=g, dtype=torch.float32) * scale
+
+    z = normal((B, N, N, Cz)).to(torch.bfloat16)
+    d_out = normal((B, N, N, Cz)).to(torch.bfloat16)
+    ln_in_w = 1.0 + normal((Cz,), 0.1)
+    ln_in_b = normal((Cz,), 0.1)
+    w_p = normal((Cz, 4 * Ch + Cz), Cz ** -0.5).to(torch.bfloat16)
+    ln_out_w = 1.0 + normal((Ch,), 0.1)
+    ln_out_b = normal((Ch,), 0.1)
+    w_o = normal((Ch, Cz), Ch ** -0.5).to(torch.bfloat16)
+    mask = None
+    npad = int(pad_frac * N)
+    if npad > 0:
+        keep = torch.ones(N)
+        keep[N - npad:] = 0.0
+        mask = (keep[:, None] * keep[None, :]).expand(B, N, N).contiguous().to(torch.bfloat16)
+    return {"z": z, "d_out": d_out, "ln_in_w": ln_in_w, "ln_in_b": ln_in_b, "w_p": w_p, "ln_out_w": ln_out_w,
+            "ln_out_b": ln_out_b, "w_o": w_o, "mask": mask}

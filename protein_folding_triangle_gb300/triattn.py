@@ -34,7 +34,9 @@ EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fw
             "triattn_device_status", "triattn_set_wait_limit_ns", "triattn_trace_enable", "triattn_trace_read",
             "triattn_test_set_starve", "tri_attn_bwd_noalloc", "triattn_bwd_atomic_workspace_bytes",
             "tri_attn_bwd_atomic_ablation", "tri_attn_dbias_combine", "triattn_module_ctx_bytes",
-            "triattn_module_workspace_bytes", "tri_attn_module_fwd", "tri_attn_module_bwd")
+            "triattn_module_workspace_bytes", "tri_attn_module_fwd", "tri_attn_module_bwd",
+            "triattn_trimul_ctx_bytes", "triattn_trimul_workspace_bytes", "triattn_trimul_fwd",
+            "triattn_trimul_bwd")
 
 FLAG_DBIAS_FP32 = 1
 
@@ -60,6 +62,14 @@ class Shape(ctypes.Structure):
 class ModuleShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int), ("H", ctypes.c_int),
                 ("D", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+class TriMulShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("C_z", ctypes.c_int), ("C_h", ctypes.c_int),
+                ("direction", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+TRIMUL_DIRECTIONS = {"outgoing": 0, "incoming": 1}
 
 
 def _declare(lib):
@@ -100,6 +110,15 @@ def _declare(lib):
     lib.tri_attn_module_fwd.restype = ctypes.c_int
     lib.tri_attn_module_bwd.argtypes = [mp] + [vp] * 13 + [ctypes.c_size_t, vp]
     lib.tri_attn_module_bwd.restype = ctypes.c_int
+    tp = ctypes.POINTER(TriMulShape)
+    lib.triattn_trimul_ctx_bytes.argtypes = [tp]
+    lib.triattn_trimul_ctx_bytes.restype = ctypes.c_size_t
+    lib.triattn_trimul_workspace_bytes.argtypes = [tp]
+    lib.triattn_trimul_workspace_bytes.restype = ctypes.c_size_t
+    lib.triattn_trimul_fwd.argtypes = [tp] + [vp] * 11 + [ctypes.c_size_t, vp]
+    lib.triattn_trimul_fwd.restype = ctypes.c_int
+    lib.triattn_trimul_bwd.argtypes = [tp] + [vp] * 16 + [ctypes.c_size_t, vp]
+    lib.triattn_trimul_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -293,8 +312,8 @@ def trace_enable(on: bool = True) -> None:
 def trace_read() -> dict:
     """Per-kernel totals of the traced launches: {name: {launches, total_ms,
     mean_ms, min_ms, max_ms}} (synchronises the recorded events)."""
-    buf = (TraceEntry * 16)()
-    n = load().triattn_trace_read(buf, 16)
+    buf = (TraceEntry * 64)()
+    n = load().triattn_trace_read(buf, 64)
     if n < 0:
         raise TriAttnError(ERR_CUDA, "triattn_trace_read")
     out = {}
@@ -390,6 +409,86 @@ def tri_attn_module_bwd(z, mask, ln_w, w_in, w_o, ctx, d_out, H: int, D: int, *,
                                       _ptr(workspace), _bytes(workspace), _stream_ptr(stream))
     _raise(code, "tri_attn_module_bwd")
     return dz, dlw, dlb, dwi, dwo
+
+
+def trimul_shape(B: int, N: int, Cz: int, Ch: int, direction: str) -> TriMulShape:
+    if direction not in TRIMUL_DIRECTIONS:
+        raise ValueError(f"direction must be one of {tuple(TRIMUL_DIRECTIONS)}")
+    return TriMulShape(B, N, Cz, Ch, TRIMUL_DIRECTIONS[direction], 0)
+
+
+def trimul_sizes(B: int, N: int, Cz: int, Ch: int, direction: str = "outgoing"):
+    """(ctx bytes, workspace bytes) of the triangle multiplicative update; (0, 0)
+    for an unsupported shape."""
+    s = trimul_shape(B, N, Cz, Ch, direction)
+    lib = load()
+    return int(lib.triattn_trimul_ctx_bytes(ctypes.byref(s))), int(lib.triattn_trimul_workspace_bytes(ctypes.byref(s)))
+
+
+def _trimul_check(z, mask, ln_in_w, w_p, ln_out_w, w_o):
+    if z.dim() != 4 or z.shape[1] != z.shape[2]:
+        raise ValueError("z must be [B, N, N, C_z]")
+    B, N, _, Cz = z.shape
+    if w_o.dim() != 2:
+        raise ValueError("w_o must be [C_h, C_z]")
+    Ch = w_o.shape[0]
+    _check(z, "z", (B, N, N, Cz))
+    _check(ln_in_w, "ln_in_w", (Cz,), torch.float32)
+    _check(w_p, "w_p", (Cz, 4 * Ch + Cz))
+    _check(ln_out_w, "ln_out_w", (Ch,), torch.float32)
+    _check(w_o, "w_o", (Ch, Cz))
+    if mask is not None:
+        _check(mask, "mask", (B, N, N))
+    return B, N, Cz, Ch
+
+
+def triattn_trimul_fwd(z, mask, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o, direction: str, *, ctx=None,
+                       workspace=None, out=None, stream=None):
+    """Triangle multiplicative update forward ("outgoing" or "incoming").
+    Returns (out [B, N, N, C_z] bf16, ctx) where ctx is the uint8 buffer the
+    backward needs."""
+    B, N, Cz, Ch = _trimul_check(z, mask, ln_in_w, w_p, ln_out_w, w_o)
+    _check(ln_in_b, "ln_in_b", (Cz,), torch.float32)
+    _check(ln_out_b, "ln_out_b", (Ch,), torch.float32)
+    s = trimul_shape(B, N, Cz, Ch, direction)
+    nctx, nws = trimul_sizes(B, N, Cz, Ch, direction)
+    if nctx == 0:
+        raise TriAttnError(ERR_UNSUPPORTED, "triattn_trimul_fwd")
+    ctx = torch.empty(nctx, dtype=torch.uint8, device=z.device) if ctx is None else ctx
+    workspace = torch.empty(nws, dtype=torch.uint8, device=z.device) if workspace is None else workspace
+    out = torch.empty_like(z) if out is None else out
+    _check(out, "out", (B, N, N, Cz))
+    code = load().triattn_trimul_fwd(ctypes.byref(s), _ptr(z), _ptr(mask), _ptr(ln_in_w), _ptr(ln_in_b), _ptr(w_p),
+                                     _ptr(ln_out_w), _ptr(ln_out_b), _ptr(w_o), _ptr(out), _ptr(ctx),
+                                     _ptr(workspace), _bytes(workspace), _stream_ptr(stream))
+    _raise(code, "triattn_trimul_fwd")
+    return out, ctx
+
+
+def triattn_trimul_bwd(z, mask, ln_in_w, w_p, ln_out_w, w_o, ctx, d_out, direction: str, *, workspace=None,
+                       out=None, stream=None):
+    """Backward of <out, d_out>.  Returns (dz bf16, d_ln_in_w, d_ln_in_b, d_w_p,
+    d_ln_out_w, d_ln_out_b, d_w_o fp32)."""
+    B, N, Cz, Ch = _trimul_check(z, mask, ln_in_w, w_p, ln_out_w, w_o)
+    _check(d_out, "d_out", (B, N, N, Cz))
+    s = trimul_shape(B, N, Cz, Ch, direction)
+    nctx, nws = trimul_sizes(B, N, Cz, Ch, direction)
+    if nctx == 0:
+        raise TriAttnError(ERR_UNSUPPORTED, "triattn_trimul_bwd")
+    _check(ctx, "ctx", (nctx,), torch.uint8)
+    workspace = torch.empty(nws, dtype=torch.uint8, device=z.device) if workspace is None else workspace
+    if out is None:
+        f32 = dict(dtype=torch.float32, device=z.device)
+        out = (torch.empty_like(z), torch.empty(Cz, **f32), torch.empty(Cz, **f32),
+               torch.empty((Cz, 4 * Ch + Cz), **f32), torch.empty(Ch, **f32), torch.empty(Ch, **f32),
+               torch.empty((Ch, Cz), **f32))
+    dz, dliw, dlib, dwp, dlow, dlob, dwo = out
+    code = load().triattn_trimul_bwd(ctypes.byref(s), _ptr(z), _ptr(mask), _ptr(ln_in_w), _ptr(w_p), _ptr(ln_out_w),
+                                     _ptr(w_o), _ptr(ctx), _ptr(d_out), _ptr(dz), _ptr(dliw), _ptr(dlib), _ptr(dwp),
+                                     _ptr(dlow), _ptr(dlob), _ptr(dwo), _ptr(workspace), _bytes(workspace),
+                                     _stream_ptr(stream))
+    _raise(code, "triattn_trimul_bwd")
+    return out
 
 
 class TriAttnFunction(torch.autograd.Function):

@@ -295,3 +295,46 @@ def test_module_rejects_bad_arguments(lib):
     assert call_module_bwd(lib, s, ws, d_w_o=None) == T.ERR_INVALID_ARG
     assert call_module_bwd(lib, s, ws, mask=ctypes.c_void_p(FAKE + 2)) == T.ERR_INVALID_ARG
     assert call_module_bwd(lib, s, 0) == T.ERR_WORKSPACE
+
+
+def test_trimul_sizes_and_argument_checks(lib):
+    ctx, ws = T.trimul_sizes(1, 40, 64, 32)
+    M, Cz, Ch = 40 * 40, 64, 32
+    # ctx holds at least x, p, a, b, X, y and u
+    assert ctx >= M * Cz * 2 + M * (4 * Ch + Cz) * 2 + 3 * M * Ch * 2 + M * Ch * 2 + M * Cz * 2
+    assert ws >= (32 << 20) + M * (4 * Ch + Cz) * 2
+    assert T.trimul_sizes(1, 40, 64, 32, "incoming") == (ctx, ws)
+    for bad in [(1, 44, 64, 32), (1, 40, 48, 32), (1, 40, 64, 160), (1, 40, 64, 48), (0, 40, 64, 32)]:
+        assert T.trimul_sizes(*bad) == (0, 0), bad
+    with pytest.raises(ValueError):
+        T.trimul_shape(1, 40, 64, 32, "sideways")
+    f = ctypes.c_void_p(FAKE)
+
+    def fwd(shape, nbytes, **kw):
+        p = {n: f for n in ("z", "liw", "lib", "wp", "low", "lob", "wo", "out", "ctx")}
+        p["mask"] = None
+        p.update(kw)
+        return lib.triattn_trimul_fwd(ctypes.byref(shape), p["z"], p["mask"], p["liw"], p["lib"], p["wp"], p["low"],
+                                      p["lob"], p["wo"], p["out"], p["ctx"], f, ctypes.c_size_t(nbytes), None)
+
+    def bwd(shape, nbytes, **kw):
+        names = ("z", "liw", "wp", "low", "wo", "ctx", "dout", "dz", "dliw", "dlib", "dwp", "dlow", "dlob", "dwo")
+        p = {n: f for n in names}
+        p["mask"] = None
+        p.update(kw)
+        return lib.triattn_trimul_bwd(ctypes.byref(shape), p["z"], p["mask"], p["liw"], p["wp"], p["low"], p["wo"],
+                                      p["ctx"], p["dout"], p["dz"], p["dliw"], p["dlib"], p["dwp"], p["dlow"],
+                                      p["dlob"], p["dwo"], f, ctypes.c_size_t(nbytes), None)
+
+    s = T.TriMulShape(1, 40, 64, 32, 0, 0)
+    assert fwd(T.TriMulShape(1, 40, 64, 32, 2, 0), ws) == T.ERR_INVALID_ARG
+    assert fwd(T.TriMulShape(1, 40, 64, 32, 0, 1), ws) == T.ERR_INVALID_ARG
+    assert fwd(T.TriMulShape(1, 40, 64, 40, 0, 0), ws) == T.ERR_UNSUPPORTED
+    assert fwd(s, ws, z=None) == T.ERR_INVALID_ARG
+    assert fwd(s, ws, wp=ctypes.c_void_p(FAKE + 4)) == T.ERR_INVALID_ARG
+    assert fwd(s, ws, ctx=ctypes.c_void_p(FAKE + 32)) == T.ERR_INVALID_ARG
+    assert fwd(s, ws - 1) == T.ERR_WORKSPACE
+    assert bwd(s, ws, dwo=None) == T.ERR_INVALID_ARG
+    assert bwd(s, ws, mask=ctypes.c_void_p(FAKE + 6)) == T.ERR_INVALID_ARG
+    assert bwd(T.TriMulShape(1, 40, 288, 32, 1, 0), ws) == T.ERR_UNSUPPORTED
+    assert bwd(s, 100) == T.ERR_WORKSPACE

@@ -106,3 +106,33 @@ def bwd(z, mask, gamma, beta, w_in, w_o, d_out, H, D):
     dz = f["rstd"] * (dxhat - dxhat.mean(axis=-1, keepdims=True)
                       - f["xhat"] * (dxhat * f["xhat"]).mean(axis=-1, keepdims=True))
     return {"dz": dz, "dgamma": dgamma, "dbeta": dbeta, "dw_in": dw_in, "dw_o": dw_o}
+
+
+def fwd_pairs(z, mask, gamma, beta, w_in, w_o, H, D, pairs):
+    """out[b, i, j, :] for the listed (b, i, j) only, by the same steps as
+    ``fwd`` restricted to what they read: query j of slice i attends over the
+    pairs (i, k) of its slice, with the bias of score (j, k) taken from pair
+    (j, k) (row j).  Returns [len(pairs), C] float64."""
+    z, gamma, beta, w_in, w_o = (_f64(a) for a in (z, gamma, beta, w_in, w_o))
+    mask = _f64(mask)
+    HD = H * D
+    out = []
+    for (b, i, j) in pairs:
+        p_i = layernorm(z[b, i], gamma, beta)[0] @ w_in          # pairs (i, k), k = 0..N-1
+        p_j = layernorm(z[b, j], gamma, beta)[0] @ w_in          # pairs (j, k): the bias row
+        o = np.empty(HD)
+        for h in range(H):
+            q = p_i[j, h * D:(h + 1) * D]
+            k = p_i[:, HD + h * D:HD + (h + 1) * D]
+            v = p_i[:, 2 * HD + h * D:2 * HD + (h + 1) * D]
+            s = k @ q / np.sqrt(D) + p_j[:, 3 * HD + h]
+            if mask is not None:
+                s = s + mask[b, i]
+            mx = s.max()
+            if not np.isfinite(mx):
+                o[h * D:(h + 1) * D] = 0.0
+                continue
+            e = np.exp(s - mx)
+            o[h * D:(h + 1) * D] = (e / e.sum()) @ v
+        out.append(o @ w_o)
+    return np.stack(out)

@@ -137,3 +137,34 @@ def bwd(z, mask, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o, d_out, directio
     dz, dln_in_w, dln_in_b = layernorm_bwd(dx, f["xhat"], f["rstd"], ln_in_w)
     return {"dz": dz, "dln_in_w": dln_in_w, "dln_in_b": dln_in_b, "dw_p": dw_p, "dln_out_w": dln_out_w,
             "dln_out_b": dln_out_b, "dw_o": dw_o}
+
+
+def fwd_pairs(z, mask, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o, direction, pairs):
+    """out[b, i, j, :] for the listed (b, i, j) only, by the same steps as
+    ``fwd`` restricted to the pairs they read: outgoing X[b, i, j] needs rows
+    i and j of the branch operands (pairs (i, k) and (j, k)), incoming needs
+    columns i and j (pairs (k, i) and (k, j)); the gate needs pair (i, j).
+    Returns [len(pairs), C_z] float64."""
+    z, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o = (
+        _f64(t) for t in (z, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o))
+    mask = _f64(mask)
+    Ch = w_o.shape[0]
+
+    def branch_line(b, t):
+        """a and b of the N pairs on line t: row t (outgoing) or column t (incoming)."""
+        zl = z[b, t] if direction == "outgoing" else z[b, :, t]
+        ml = np.ones(zl.shape[0]) if mask is None else (mask[b, t] if direction == "outgoing" else mask[b, :, t])
+        x, _, _ = layernorm(zl, ln_in_w, ln_in_b)
+        av, ag, bv, bg, _ = split_projection(x @ w_p, Ch)
+        return ml[:, None] * sigmoid(ag) * av, ml[:, None] * sigmoid(bg) * bv
+
+    out = []
+    for (b, i, j) in pairs:
+        a_i, _ = branch_line(b, i)
+        _, b_j = branch_line(b, j)
+        X = (a_i * b_j).sum(axis=0)                      # sum over the third token k
+        y, _, _ = layernorm(X, ln_out_w, ln_out_b)
+        x_ij, _, _ = layernorm(z[b, i, j], ln_in_w, ln_in_b)
+        g = split_projection(x_ij @ w_p, Ch)[4]
+        out.append(sigmoid(g) * (y @ w_o))
+    return np.stack(out)

@@ -111,3 +111,37 @@ def test_module_rejects_bad_shapes_without_launching():
     with pytest.raises(T.TriAttnError):
         T.tri_attn_module_fwd(z, None, w, w, torch.zeros((48, 3 * 32 + 2), dtype=torch.bfloat16, device="cuda"),
                               torch.zeros((32, 48), dtype=torch.bfloat16, device="cuda"), 2, 16)
+
+
+def layernorm_row_sums_ok(dz):
+    """The LayerNorm makes the output invariant to a constant shift of one
+    pair's features, so sum_c dz[m, c] = 0 for every pair m.  dz is BF16:
+    each element carries a relative rounding of 2^-9 at most, so the sum of
+    the rounded values is bounded by 2^-8 times the sum of magnitudes."""
+    d = dz.float().reshape(-1, dz.shape[-1]).double()
+    s = d.sum(dim=1).abs()
+    bound = (2.0 ** -8) * d.abs().sum(dim=1) + 1e-30
+    return bool((s <= bound).all()), float((s / bound).max())
+
+
+def test_module_full_size_sampled():
+    """crop768 module (B=1, N=768, C=128, H=4, D=32, tail key mask) at the
+    bench's size: 12 sampled output pairs against the per-pair oracle, the
+    LayerNorm row sums of dz, and bitwise repeatability of a second call."""
+    B, N, C, H, D = 1, 768, 128, 4, 32
+    x = S.make_module_inputs(B, N, C, H, D, seed=0, mask_frac=0.08)
+    out, grads = run_gpu(x)
+    rng = np.random.default_rng(21)
+    pairs = [(0, int(rng.integers(N)), int(rng.integers(N))) for _ in range(10)] + [(0, 0, N - 1), (0, N - 1, 3)]
+    ref = MO.fwd_pairs(x["z"], x["mask"], x["ln_w"], x["ln_b"], x["w_in"], x["w_o"], H, D, pairs)
+    got = np.stack([cpu64(out[b, i, j]) for (b, i, j) in pairs])
+    err = rel_rmse(got, ref)
+    ok, ratio = layernorm_row_sums_ok(grads[0])
+    print(json.dumps({"case": "module crop768 C=128 sampled", "out_sampled": round(err, 6),
+                      "dz_row_sum_ratio_max": round(ratio, 4)}))
+    assert err <= TOL_OUT
+    assert ok
+    out2, grads2 = run_gpu(x)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    for a, b in zip(grads, grads2):
+        assert torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))

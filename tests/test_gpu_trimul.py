@@ -101,3 +101,30 @@ def test_trimul_bitwise_deterministic():
             else:
                 for a, b in zip(first, cur):
                     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("direction", ["outgoing", "incoming"])
+def test_trimul_full_size_sampled(direction):
+    """Table 10's largest shape (B=1, N=768, C_z=C_h=128) with 8% padding
+    tokens: 12 sampled output pairs against the per-pair oracle, the input
+    LayerNorm's row sums of dz (sum_c dz[m, c] = 0 up to the BF16 rounding of
+    dz), and bitwise repeatability of a second call."""
+    B, N, C = 1, 768, 128
+    x = S.make_trimul_inputs(B, N, C, C, seed=0, pad_frac=0.08)
+    out, grads = run_gpu(x, direction)
+    rng = np.random.default_rng(22)
+    pairs = [(0, int(rng.integers(N)), int(rng.integers(N))) for _ in range(10)] + [(0, 0, N - 1), (0, N - 1, 5)]
+    args = (x["z"], x["mask"], x["ln_in_w"], x["ln_in_b"], x["w_p"], x["ln_out_w"], x["ln_out_b"], x["w_o"])
+    ref = TMO.fwd_pairs(*args, direction, pairs)
+    got = np.stack([cpu64(out[b, i, j]) for (b, i, j) in pairs])
+    err = rel_rmse(got, ref)
+    d = grads[0].float().reshape(-1, C).double()
+    s = d.sum(dim=1).abs()
+    bound = (2.0 ** -8) * d.abs().sum(dim=1) + 1e-30
+    print(json.dumps({"case": f"trimul N768 C128 {direction} sampled", "out_sampled": round(err, 6),
+                      "dz_row_sum_ratio_max": round(float((s / bound).max()), 4)}))
+    assert err <= TOL_OUT
+    assert bool((s <= bound).all())
+    out2, grads2 = run_gpu(x, direction)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(grads[3].view(torch.int32), grads2[3].view(torch.int32))

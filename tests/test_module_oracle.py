@@ -141,3 +141,15 @@ def test_planted_mistake_in_projection_split_is_caught():
     tz, tg, tb, twi, two = (torch.tensor(a) for a in (z, gamma, beta, w_in, w_o))
     ref = torch_module(tz, None, tg, tb, twi, two, H, D).numpy()
     assert np.abs(bad - ref).max() > 1e-3
+
+
+def test_fwd_pairs_matches_full_forward():
+    """The per-pair forward used for sampled full-size checks gives the full
+    forward's values at the listed pairs (masked slices included)."""
+    B, N, C, H, D = 2, 6, 8, 2, 3
+    z, mask, gamma, beta, w_in, w_o = make(B, N, C, H, D, seed=13, masked=True)
+    full = M.fwd(z, mask, gamma, beta, w_in, w_o, H, D)["out"]
+    pairs = [(0, 1, 4), (1, 5, 0), (1, 2, 2), (0, 0, 5)]
+    got = M.fwd_pairs(z, mask, gamma, beta, w_in, w_o, H, D, pairs)
+    for r, (b, i, j) in enumerate(pairs):
+        np.testing.assert_allclose(got[r], full[b, i, j], rtol=1e-12, atol=1e-13)

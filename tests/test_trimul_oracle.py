@@ -178,3 +178,16 @@ def test_planted_mistake_swapped_branches_is_caught():
         TM.split_projection = orig
     ref = torch_update(*(torch.tensor(a) for a in [z]), None, *(torch.tensor(a) for a in w), "outgoing").numpy()
     assert np.abs(bad - ref).max() > 1e-3
+
+
+@pytest.mark.parametrize("direction", TM.DIRECTIONS)
+def test_fwd_pairs_matches_full_forward(direction):
+    """The per-pair forward used for sampled full-size checks gives the full
+    forward's values at the listed pairs."""
+    B, N, Cz, Ch = 2, 6, 5, 4
+    z, mask, *w = make(B, N, Cz, Ch, seed=12, masked=True)
+    full = TM.fwd(z, mask, *w, direction)["out"]
+    pairs = [(0, 1, 4), (1, 5, 0), (1, 2, 2), (0, 0, 5)]
+    got = TM.fwd_pairs(z, mask, *w, direction, pairs)
+    for r, (b, i, j) in enumerate(pairs):
+        np.testing.assert_allclose(got[r], full[b, i, j], rtol=1e-12, atol=1e-13)

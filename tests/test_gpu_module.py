@@ -7,7 +7,7 @@ Tolerances (relative RMSE against FP64): out <= 1e-2, every gradient
 (dz, dgamma, dbeta, dW_in, dW_o) <= 2e-2.  The module adds four BF16
 roundings to the core's own error (x, the projection P, the core output
 once more through o_flat, and out; in the backward d_oflat and dP), each a
-relative 2^-9 at most, on top of the core's 4e-3 / 1e-2 bars; the bars
+relative 2^-8 at most (BF16 round to nearest), on top of the core's 4e-3 / 1e-2 bars; the bars
 here leave about a factor two over the core's.
 """
 import json
@@ -116,11 +116,12 @@ def test_module_rejects_bad_shapes_without_launching():
 def layernorm_row_sums_ok(dz):
     """The LayerNorm makes the output invariant to a constant shift of one
     pair's features, so sum_c dz[m, c] = 0 for every pair m.  dz is BF16:
-    each element carries a relative rounding of 2^-9 at most, so the sum of
-    the rounded values is bounded by 2^-8 times the sum of magnitudes."""
+    each element carries a relative rounding of 2^-8 at most, so the sum of
+    the rounded values is at most 2^-8 times the sum of magnitudes; the
+    check allows 2^-7 (the FP32 arithmetic before the rounding adds a little)."""
     d = dz.float().reshape(-1, dz.shape[-1]).double()
     s = d.sum(dim=1).abs()
-    bound = (2.0 ** -8) * d.abs().sum(dim=1) + 1e-30
+    bound = (2.0 ** -7) * d.abs().sum(dim=1) + 1e-30
     return bool((s <= bound).all()), float((s / bound).max())
 
 

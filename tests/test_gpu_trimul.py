@@ -5,7 +5,7 @@ on the same seeded BF16 inputs.
 Tolerances (relative RMSE against FP64): out <= 1e-2, every gradient
 <= 2e-2.  The CUDA path rounds to BF16 at x, p, the gated operands a and b,
 the contraction output X, y = LayerNorm(X), u and out (forward), and at du,
-dX, dA, dB and dp (backward); each rounding is a relative 2^-9 at most and
+dX, dA, dB and dp (backward); each rounding is a relative 2^-8 at most and
 the contraction accumulates in FP32.  Seven to eight such roundings in
 sequence give a few 1e-3, the bars leave a factor two to four.
 """
@@ -107,8 +107,10 @@ def test_trimul_bitwise_deterministic():
 def test_trimul_full_size_sampled(direction):
     """Table 10's largest shape (B=1, N=768, C_z=C_h=128) with 8% padding
     tokens: 12 sampled output pairs against the per-pair oracle, the input
-    LayerNorm's row sums of dz (sum_c dz[m, c] = 0 up to the BF16 rounding of
-    dz), and bitwise repeatability of a second call."""
+    LayerNorm's row sums of dz (sum_c dz[m, c] = 0; the BF16 rounding of dz
+    bounds the sum of the rounded values by 2^-8 times the sum of
+    magnitudes, the check allows 2^-7), and bitwise repeatability of a
+    second call."""
     B, N, C = 1, 768, 128
     x = S.make_trimul_inputs(B, N, C, C, seed=0, pad_frac=0.08)
     out, grads = run_gpu(x, direction)
@@ -120,7 +122,7 @@ def test_trimul_full_size_sampled(direction):
     err = rel_rmse(got, ref)
     d = grads[0].float().reshape(-1, C).double()
     s = d.sum(dim=1).abs()
-    bound = (2.0 ** -8) * d.abs().sum(dim=1) + 1e-30
+    bound = (2.0 ** -7) * d.abs().sum(dim=1) + 1e-30
     print(json.dumps({"case": f"trimul N768 C128 {direction} sampled", "out_sampled": round(err, 6),
                       "dz_row_sum_ratio_max": round(float((s / bound).max()), 4)}))
     assert err <= TOL_OUT

@@ -74,8 +74,25 @@ __global__ void __launch_bounds__(256) bias_plane_kernel(uint16_t* __restrict__ 
   const size_t b = m / NN, qk = m % NN;
   uint16_t* pb = bias + (b * H + h) * NN + qk;
   uint16_t* pp = pairs + m * ld + off + h;
-  if (to_pairs) *pp = *pb;
-  else *pb = *pp;
+  if (to_pairs) {
+    *pp = *pb;
+    // the row's padding columns [off + H, ld) enter the backward GEMMs (times
+    // zero weights): they must hold zeros, not whatever the workspace held
+    if (h == 0)
+      for (int c = off + H; c < ld; ++c) pairs[m * ld + c] = 0;
+  } else {
+    *pb = *pp;
+  }
+}
+
+// dst [rows, ldd] = src [rows, cols] with zero columns [cols, ldd) (the
+// projection matrix padded to a row length that is a multiple of 8).
+__global__ void __launch_bounds__(256) pad_columns_kernel(const uint16_t* __restrict__ src, int cols,
+                                                          uint16_t* __restrict__ dst, int ldd, int rows) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= rows * ldd) return;
+  const int r = t / ldd, c = t % ldd;
+  dst[t] = c < cols ? src[static_cast<size_t>(r) * cols + c] : static_cast<uint16_t>(0);
 }
 
 // ---------------------------------------------------------------- cuBLAS
@@ -125,13 +142,15 @@ CtxLayout ctx_layout(const ModDims& d) {
 
 // Scratch of one forward or backward call.
 struct WsLayout2 {
-  size_t blas, p, doflat, dobuf, dq, dk, dv, dbias, dx, pg, pb, core, total;
+  size_t blas, w_in_pad, dw_in_pad, p, doflat, dobuf, dq, dk, dv, dbias, dx, pg, pb, core, total;
 };
 WsLayout2 ws_layout2(const ModDims& d, const triattn_shape& core) {
   const size_t act = d.B * d.N * d.H * d.N * d.D * 2;
   WsLayout2 w;
   size_t o = 0;
   w.blas = o;   o += rup(kBlasWorkspace);
+  w.w_in_pad = o;  o += rup(d.C * d.Fp * 2);   // W_in with zero columns up to Fp
+  w.dw_in_pad = o; o += rup(d.C * d.Fp * 4);   // dW_in, Fp wide
   w.p = o;      o += rup(d.M * d.Fp * 2);  // P (forward) / dP (backward)
   w.doflat = o; o += rup(d.M * d.HD * 2);
   w.dobuf = o;  o += rup(act);
@@ -185,6 +204,15 @@ cudaError_t bias_planes(const ModDims& d, uint16_t* pairs, int ld, int off, uint
   });
 }
 
+cudaError_t pad_w_in(const ModDims& d, const void* w_in, uint16_t* w_in_pad, cudaStream_t s) {
+  return trace_call(kKModLayout, s, [&] {
+    pad_columns_kernel<<<blocks_for(d.C * d.Fp), 256, 0, s>>>(static_cast<const uint16_t*>(w_in),
+                                                              static_cast<int>(d.F), w_in_pad, static_cast<int>(d.Fp),
+                                                              static_cast<int>(d.C));
+    return cudaGetLastError();
+  });
+}
+
 }  // namespace
 }  // namespace triattn
 
@@ -234,7 +262,12 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   if (trace_call(kKModLnFwd, s, [&] { return ln_rows_fwd(d.M, C, z, ln_w, ln_b, cx + c.x, mean, rstd, s); }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // P = x W_in
-  if (gemm_traced(kKModGemm, h, s, false, false, M, F, C, cx + c.x, C, w_in, F, P, Fp, CUDA_R_16BF) != TRIATTN_OK)
+  // (through W_in padded to Fp columns: cuBLAS is several times slower on
+  // widths that are not a multiple of 8)
+  uint16_t* w_in_pad = reinterpret_cast<uint16_t*>(ws + w.w_in_pad);
+  if (pad_w_in(d, w_in, w_in_pad, s) != cudaSuccess) return TRIATTN_ERR_CUDA;
+  if (gemm_traced(kKModGemm, h, s, false, false, M, Fp, C, cx + c.x, C, w_in_pad, Fp, P, Fp, CUDA_R_16BF) !=
+      TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // q, k, v and the bias planes
   const size_t dsts[3] = {c.q, c.k, c.v};
@@ -298,9 +331,19 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
       return TRIATTN_ERR_CUDA;
   if (bias_planes(d, dP, Fp, 3 * HD, reinterpret_cast<uint16_t*>(ws + w.dbias), true, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  // P = x W_in:  dW_in = x^T dP,  dx = dP W_in^T (FP32)
-  if (gemm_traced(kKModGemm, h, s, true, false, C, F, M, cx + c.x, C, dP, Fp, d_w_in, F, CUDA_R_32F) != TRIATTN_OK ||
-      gemm_traced(kKModGemm, h, s, false, true, M, C, F, dP, Fp, w_in, F, ws + w.dx, C, CUDA_R_32F) != TRIATTN_OK)
+  // P = x W_in:  dW_in = x^T dP,  dx = dP W_in^T (FP32), both Fp wide (dP's
+  // padding columns are zero, so are W_in's); dW_in's first F columns copied out
+  uint16_t* w_in_pad = reinterpret_cast<uint16_t*>(ws + w.w_in_pad);
+  float* dw_in_pad = reinterpret_cast<float*>(ws + w.dw_in_pad);
+  if (pad_w_in(d, w_in, w_in_pad, s) != cudaSuccess) return TRIATTN_ERR_CUDA;
+  if (gemm_traced(kKModGemm, h, s, true, false, C, Fp, M, cx + c.x, C, dP, Fp, dw_in_pad, Fp, CUDA_R_32F) !=
+          TRIATTN_OK ||
+      gemm_traced(kKModGemm, h, s, false, true, M, C, Fp, dP, Fp, w_in_pad, Fp, ws + w.dx, C, CUDA_R_32F) !=
+          TRIATTN_OK)
+    return TRIATTN_ERR_CUDA;
+  if (trace_call(kKModLayout, s, [&] {
+        return cudaMemcpy2DAsync(d_w_in, d.F * 4, dw_in_pad, d.Fp * 4, d.F * 4, d.C, cudaMemcpyDeviceToDevice, s);
+      }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // x = LayerNorm(z)
   float* pg = reinterpret_cast<float*>(ws + w.pg);

@@ -60,36 +60,48 @@ __device__ __forceinline__ float mask_at(const uint16_t* mask, size_t m) {
   return mask == nullptr ? 1.f : bf16lo_to_f32(mask[m]);
 }
 
-// Load the [Ch][64] channel-major tile of pairs [pos0, pos0 + 64) of example b
-// into shared memory as FP32 rows of kRow.
+// A [Ch][64] channel-major tile of pairs [pos0, pos0 + 64) of example b in
+// shared memory, as BF16: row c holds the 64 pairs as 32 words (even pair in
+// the low half) plus one padding word, so that both the row-wise fills /
+// drains and the column-wise reads of one pair are free of bank conflicts.
+constexpr int kRowW = kPairs / 2 + 1;
 template <int Ch>
-__device__ __forceinline__ void load_cm_tile(const uint16_t* __restrict__ src, size_t b, size_t pos0, size_t NN,
-                                             float* s) {
+__device__ __forceinline__ void load_cm_tile_h(const uint16_t* __restrict__ src, size_t b, size_t pos0, size_t NN,
+                                               uint32_t* s) {
   for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
     const int c = it >> 3, q = it & 7;
-    float f[8];
-    unpack8(ld16(src + (b * Ch + c) * NN + pos0 + 8 * q), f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s[c * kRow + 8 * q + e] = f[e];
+    const uint4 w = ld16(src + (b * Ch + c) * NN + pos0 + 8 * q);
+    uint32_t* d = s + c * kRowW + 4 * q;
+    d[0] = w.x;
+    d[1] = w.y;
+    d[2] = w.z;
+    d[3] = w.w;
   }
 }
-// Store a [Ch][64] FP32 shared tile as BF16 channel-major rows.
 template <int Ch>
-__device__ __forceinline__ void store_cm_tile(const float* s, uint16_t* __restrict__ dst, size_t b, size_t pos0,
-                                              size_t NN) {
+__device__ __forceinline__ void store_cm_tile_h(const uint32_t* s, uint16_t* __restrict__ dst, size_t b, size_t pos0,
+                                                size_t NN) {
   for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
     const int c = it >> 3, q = it & 7;
-    float f[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = s[c * kRow + 8 * q + e];
-    st16(dst + (b * Ch + c) * NN + pos0 + 8 * q, pack8(f));
+    const uint32_t* r = s + c * kRowW + 4 * q;
+    st16(dst + (b * Ch + c) * NN + pos0 + 8 * q, make_uint4(r[0], r[1], r[2], r[3]));
   }
+}
+__device__ __forceinline__ float tile_h(const uint32_t* s, int c, int pr) {
+  const uint32_t w = s[c * kRowW + (pr >> 1)];
+  return (pr & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
+}
+__device__ __forceinline__ void tile_h_set(uint32_t* s, int c, int pr, float v) {
+  reinterpret_cast<uint16_t*>(s + c * kRowW + (pr >> 1))[pr & 1] =
+      static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
 }
 
 // a = m sigmoid(p_ag) p_av and b = m sigmoid(p_bg) p_bv for 64 consecutive
 // pairs, written channel-major.  Phase 1: thread (pair couple pp, 8-channel
 // chunk cc) gates two pairs and packs them per channel into one shared word;
-// phase 2: every channel row of 64 pairs goes out as 8 16-byte stores.
+// the chunk index runs fastest, so a warp reads whole contiguous row
+// segments of p.  Phase 2: every channel row of 64 pairs goes out as 8
+// 16-byte stores.
 template <int Ch>
 __global__ void __launch_bounds__(256) gate_fwd_kernel(const uint16_t* __restrict__ p, int ld,
                                                        const uint16_t* __restrict__ mask, uint16_t* __restrict__ A,
@@ -98,7 +110,7 @@ __global__ void __launch_bounds__(256) gate_fwd_kernel(const uint16_t* __restric
   const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
   const size_t b = m0 / NN, pos0 = m0 % NN;
   for (int it = threadIdx.x; it < 32 * (Ch / 8); it += blockDim.x) {
-    const int pp = it & 31, cc = it >> 5;
+    const int pp = it / (Ch / 8), cc = it % (Ch / 8);
     float ga[2][8], gb[2][8];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -140,11 +152,11 @@ __global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restri
                                                         const float* __restrict__ beta, uint16_t* __restrict__ y,
                                                         float* __restrict__ mean_out, float* __restrict__ rstd_out,
                                                         size_t NN) {
-  extern __shared__ float sX[];  // [Ch][kRow]
+  extern __shared__ uint32_t sXh[];  // [Ch][kRowW] BF16 pairs
   constexpr int kCh = Ch / 32;
   const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
   const size_t b = m0 / NN, pos0 = m0 % NN;
-  load_cm_tile<Ch>(X, b, pos0, NN, sX);
+  load_cm_tile_h<Ch>(X, b, pos0, NN, sXh);
   __syncthreads();
   const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
   float v[kCh][8];
@@ -153,7 +165,7 @@ __global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restri
   for (int i = 0; i < kCh; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      v[i][e] = sX[(8 * (qq + 4 * i) + e) * kRow + pr];
+      v[i][e] = tile_h(sXh, 8 * (qq + 4 * i) + e, pr);
       s += v[i][e];
     }
   s += __shfl_xor_sync(0xffffffffu, s, 1);
@@ -195,16 +207,16 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
                                                         uint16_t* __restrict__ dX, float* __restrict__ part_g,
                                                         float* __restrict__ part_b, size_t NN, size_t tiles) {
   extern __shared__ float sm[];
-  float* sX = sm;                 // X, then dX
-  float* sG = sm + Ch * kRow;     // dy * xhat
-  float* sD = sm + 2 * Ch * kRow; // dy
+  float* sG = sm;                                          // dy * xhat
+  float* sD = sm + Ch * kRow;                              // dy
+  uint32_t* sXh = reinterpret_cast<uint32_t*>(sm + 2 * Ch * kRow);  // X, then dX (BF16)
   constexpr int kCh = Ch / 32;
   const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
   float accg = 0.f, accb = 0.f;
   for (size_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const size_t m0 = tile * kPairs;
     const size_t b = m0 / NN, pos0 = m0 % NN;
-    load_cm_tile<Ch>(X, b, pos0, NN, sX);
+    load_cm_tile_h<Ch>(X, b, pos0, NN, sXh);
     __syncthreads();
     const size_t m = m0 + pr;
     const float mean = mean_in[m], rstd = rstd_in[m];
@@ -219,7 +231,7 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int c = c0 + e;
-        xh[i][e] = (sX[c * kRow + pr] - mean) * rstd;
+        xh[i][e] = (tile_h(sXh, c, pr) - mean) * rstd;
         g[i][e] = dv[e] * gamma[c];
         sg += g[i][e];
         sgx += g[i][e] * xh[i][e];
@@ -235,9 +247,9 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
 #pragma unroll
     for (int i = 0; i < kCh; ++i)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sX[(8 * (qq + 4 * i) + e) * kRow + pr] = rstd * (g[i][e] - a - xh[i][e] * bb);
+      for (int e = 0; e < 8; ++e) tile_h_set(sXh, 8 * (qq + 4 * i) + e, pr, rstd * (g[i][e] - a - xh[i][e] * bb));
     __syncthreads();
-    store_cm_tile<Ch>(sX, dX, b, pos0, NN);
+    store_cm_tile_h<Ch>(sXh, dX, b, pos0, NN);
     if (threadIdx.x < Ch) {
       for (int q = 0; q < kPairs; ++q) {
         accg += sG[threadIdx.x * kRow + q];
@@ -260,14 +272,14 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const uint16_t* __restric
                                                        const uint16_t* __restrict__ p, int ld,
                                                        const uint16_t* __restrict__ mask,
                                                        uint16_t* __restrict__ dp, size_t NN) {
-  extern __shared__ float sm[];
-  float* sA = sm;
-  float* sB = sm + Ch * kRow;
+  extern __shared__ uint32_t smw[];
+  uint32_t* sA = smw;               // dA tile, BF16 pairs
+  uint32_t* sB = smw + Ch * kRowW;  // dB tile
   constexpr int kCh = Ch / 32;
   const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
   const size_t b = m0 / NN, pos0 = m0 % NN;
-  load_cm_tile<Ch>(dA, b, pos0, NN, sA);
-  load_cm_tile<Ch>(dB, b, pos0, NN, sB);
+  load_cm_tile_h<Ch>(dA, b, pos0, NN, sA);
+  load_cm_tile_h<Ch>(dB, b, pos0, NN, sB);
   __syncthreads();
   const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
   const size_t m = m0 + pr;
@@ -284,7 +296,7 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const uint16_t* __restric
     unpack8(ld16(row + 3 * Ch + c0), bg);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float da = sA[(c0 + e) * kRow + pr] * mk, db = sB[(c0 + e) * kRow + pr] * mk;
+      const float da = tile_h(sA, c0 + e, pr) * mk, db = tile_h(sB, c0 + e, pr) * mk;
       const float sa = sigm(ag[e]), sb = sigm(bg[e]);
       dav[e] = da * sa;
       dag[e] = da * av[e] * sa * (1.f - sa);
@@ -420,14 +432,20 @@ triattn_status check_trimul(const triattn_trimul_shape* s) {
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 unsigned blocks_for(size_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
+// Dynamic shared memory of the channel-major kernels.
+template <int Ch> constexpr int ln_cm_fwd_smem() { return Ch * kRowW * 4; }
+template <int Ch> constexpr int ln_cm_bwd_smem() { return 2 * Ch * kRow * 4 + Ch * kRowW * 4; }
+template <int Ch> constexpr int gate_bwd_smem() { return 2 * Ch * kRowW * 4; }
+
 template <int Ch>
 cudaError_t set_attrs() {
   cudaError_t e = cudaFuncSetAttribute(ln_cm_fwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Ch * kRow * 4);
+                                       ln_cm_fwd_smem<Ch>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(ln_cm_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * Ch * kRow * 4);
+    e = cudaFuncSetAttribute(ln_cm_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ln_cm_bwd_smem<Ch>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gate_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * Ch * kRow * 4);
+    e = cudaFuncSetAttribute(gate_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize, gate_bwd_smem<Ch>());
   return e;
 }
 
@@ -446,7 +464,7 @@ struct CmLaunch {
   cudaError_t ln_fwd(const uint16_t* X, const float* g, const float* b, uint16_t* y, float* mean, float* rstd) const {
     cudaError_t e = set_attrs<Ch>();
     if (e != cudaSuccess) return e;
-    ln_cm_fwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, Ch * kRow * 4, s>>>(X, g, b, y, mean, rstd,
+    ln_cm_fwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, ln_cm_fwd_smem<Ch>(), s>>>(X, g, b, y, mean, rstd,
                                                                                           d.NN);
     return cudaGetLastError();
   }
@@ -456,7 +474,7 @@ struct CmLaunch {
     cudaError_t e = set_attrs<Ch>();
     if (e != cudaSuccess) return e;
     const size_t tiles = d.M / kPairs;
-    ln_cm_bwd_kernel<Ch><<<kCmBwdBlocks, 256, 3 * Ch * kRow * 4, s>>>(X, dy, g, mean, rstd, dX, pg, pb, d.NN, tiles);
+    ln_cm_bwd_kernel<Ch><<<kCmBwdBlocks, 256, ln_cm_bwd_smem<Ch>(), s>>>(X, dy, g, mean, rstd, dX, pg, pb, d.NN, tiles);
     return cudaGetLastError();
   }
   template <int Ch>
@@ -464,7 +482,7 @@ struct CmLaunch {
                        uint16_t* dp) const {
     cudaError_t e = set_attrs<Ch>();
     if (e != cudaSuccess) return e;
-    gate_bwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, 2 * Ch * kRow * 4, s>>>(
+    gate_bwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, gate_bwd_smem<Ch>(), s>>>(
         dA, dB, p, static_cast<int>(d.Fp), mask, dp, d.NN);
     return cudaGetLastError();
   }

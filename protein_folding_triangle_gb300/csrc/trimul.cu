@@ -65,17 +65,27 @@ __device__ __forceinline__ float mask_at(const uint16_t* mask, size_t m) {
 // the low half) plus one padding word, so that both the row-wise fills /
 // drains and the column-wise reads of one pair are free of bank conflicts.
 constexpr int kRowW = kPairs / 2 + 1;
+// The same fill in two steps, so that all of a thread's loads are in flight
+// before the first shared-memory store (every kernel here runs 256 threads).
 template <int Ch>
-__device__ __forceinline__ void load_cm_tile_h(const uint16_t* __restrict__ src, size_t b, size_t pos0, size_t NN,
-                                               uint32_t* s) {
-  for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
-    const int c = it >> 3, q = it & 7;
-    const uint4 w = ld16(src + (b * Ch + c) * NN + pos0 + 8 * q);
-    uint32_t* d = s + c * kRowW + 4 * q;
-    d[0] = w.x;
-    d[1] = w.y;
-    d[2] = w.z;
-    d[3] = w.w;
+__device__ __forceinline__ void fetch_cm_tile(const uint16_t* __restrict__ src, size_t b, size_t pos0, size_t NN,
+                                              uint4 (&r)[Ch * 8 / 256]) {
+#pragma unroll
+  for (int k = 0; k < Ch * 8 / 256; ++k) {
+    const int it = threadIdx.x + 256 * k;
+    r[k] = ld16(src + (b * Ch + (it >> 3)) * NN + pos0 + 8 * (it & 7));
+  }
+}
+template <int Ch>
+__device__ __forceinline__ void put_cm_tile(const uint4 (&r)[Ch * 8 / 256], uint32_t* s) {
+#pragma unroll
+  for (int k = 0; k < Ch * 8 / 256; ++k) {
+    const int it = threadIdx.x + 256 * k;
+    uint32_t* d = s + (it >> 3) * kRowW + 4 * (it & 7);
+    d[0] = r[k].x;
+    d[1] = r[k].y;
+    d[2] = r[k].z;
+    d[3] = r[k].w;
   }
 }
 template <int Ch>
@@ -156,7 +166,11 @@ __global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restri
   constexpr int kCh = Ch / 32;
   const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
   const size_t b = m0 / NN, pos0 = m0 % NN;
-  load_cm_tile_h<Ch>(X, b, pos0, NN, sXh);
+  {
+    uint4 r[Ch * 8 / 256];
+    fetch_cm_tile<Ch>(X, b, pos0, NN, r);
+    put_cm_tile<Ch>(r, sXh);
+  }
   __syncthreads();
   const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
   float v[kCh][8];
@@ -195,9 +209,12 @@ __global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restri
 }
 
 // Backward of the output LayerNorm: dX (channel-major BF16) from dy (pair-major
-// FP32) and X; per block the dgamma / dbeta sums over its tiles, each channel
-// added by one thread over the tile's 64 pairs in order, one partial row per
-// block.
+// FP32) and X.  Each block walks its tiles of 64 pairs with the next tile's X
+// and dy loads issued while the current one drains.  dgamma / dbeta: per
+// tile, the 256 / C_h threads of a channel each add a fixed run of the
+// tile's pairs (four interleaved partial sums, combined in a fixed order)
+// into their own accumulator; at the end the runs are added in order: one
+// partial row per block.
 template <int Ch>
 __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restrict__ X,
                                                         const float* __restrict__ dy,
@@ -207,35 +224,52 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
                                                         uint16_t* __restrict__ dX, float* __restrict__ part_g,
                                                         float* __restrict__ part_b, size_t NN, size_t tiles) {
   extern __shared__ float sm[];
-  float* sG = sm;                                          // dy * xhat
-  float* sD = sm + Ch * kRow;                              // dy
+  float* sG = sm;                                                   // dy * xhat
+  float* sD = sm + Ch * kRow;                                       // dy
   uint32_t* sXh = reinterpret_cast<uint32_t*>(sm + 2 * Ch * kRow);  // X, then dX (BF16)
   constexpr int kCh = Ch / 32;
+  constexpr int kSplit = 256 / Ch;      // threads per channel in the per-tile sums
+  constexpr int kPP = kPairs / kSplit;  // pairs each of them adds
+  static_assert(kPP % 4 == 0, "per-thread pair run");
   const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
+  const int rc = threadIdx.x % Ch, rpart = threadIdx.x / Ch;
+  const bool reducer = threadIdx.x < kSplit * Ch;
   float accg = 0.f, accb = 0.f;
-  for (size_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+  uint4 xr[Ch * 8 / 256];
+  float4 dyr[kCh][2];
+  float mean = 0.f, rstd = 0.f;
+  auto fetch = [&](size_t tile) {
     const size_t m0 = tile * kPairs;
-    const size_t b = m0 / NN, pos0 = m0 % NN;
-    load_cm_tile_h<Ch>(X, b, pos0, NN, sXh);
-    __syncthreads();
+    fetch_cm_tile<Ch>(X, m0 / NN, m0 % NN, NN, xr);
     const size_t m = m0 + pr;
-    const float mean = mean_in[m], rstd = rstd_in[m];
-    float xh[kCh][8], g[kCh][8];
-    float sg = 0.f, sgx = 0.f;
 #pragma unroll
     for (int i = 0; i < kCh; ++i) {
       const int c0 = 8 * (qq + 4 * i);
-      const float4 d0 = *reinterpret_cast<const float4*>(dy + m * Ch + c0);
-      const float4 d1 = *reinterpret_cast<const float4*>(dy + m * Ch + c0 + 4);
-      const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+      dyr[i][0] = *reinterpret_cast<const float4*>(dy + m * Ch + c0);
+      dyr[i][1] = *reinterpret_cast<const float4*>(dy + m * Ch + c0 + 4);
+    }
+    mean = mean_in[m];
+    rstd = rstd_in[m];
+  };
+  if (blockIdx.x < tiles) fetch(blockIdx.x);
+  for (size_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const size_t m0 = tile * kPairs;
+    const size_t b = m0 / NN, pos0 = m0 % NN;
+    put_cm_tile<Ch>(xr, sXh);
+    __syncthreads();
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int i = 0; i < kCh; ++i) {
+      const float dv[8] = {dyr[i][0].x, dyr[i][0].y, dyr[i][0].z, dyr[i][0].w,
+                           dyr[i][1].x, dyr[i][1].y, dyr[i][1].z, dyr[i][1].w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int c = c0 + e;
-        xh[i][e] = (tile_h(sXh, c, pr) - mean) * rstd;
-        g[i][e] = dv[e] * gamma[c];
-        sg += g[i][e];
-        sgx += g[i][e] * xh[i][e];
-        sG[c * kRow + pr] = dv[e] * xh[i][e];
+        const int c = 8 * (qq + 4 * i) + e;
+        const float xh = (tile_h(sXh, c, pr) - mean) * rstd;
+        const float g = dv[e] * gamma[c];
+        sg += g;
+        sgx += g * xh;
+        sG[c * kRow + pr] = dv[e] * xh;
         sD[c * kRow + pr] = dv[e];
       }
     }
@@ -244,23 +278,51 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
     sgx += __shfl_xor_sync(0xffffffffu, sgx, 1);
     sgx += __shfl_xor_sync(0xffffffffu, sgx, 2);
     const float a = sg * (1.f / Ch), bb = sgx * (1.f / Ch);
+    // each thread overwrites only the X entries it read itself
 #pragma unroll
-    for (int i = 0; i < kCh; ++i)
+    for (int i = 0; i < kCh; ++i) {
+      const float dv[8] = {dyr[i][0].x, dyr[i][0].y, dyr[i][0].z, dyr[i][0].w,
+                           dyr[i][1].x, dyr[i][1].y, dyr[i][1].z, dyr[i][1].w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) tile_h_set(sXh, 8 * (qq + 4 * i) + e, pr, rstd * (g[i][e] - a - xh[i][e] * bb));
-    __syncthreads();
-    store_cm_tile_h<Ch>(sXh, dX, b, pos0, NN);
-    if (threadIdx.x < Ch) {
-      for (int q = 0; q < kPairs; ++q) {
-        accg += sG[threadIdx.x * kRow + q];
-        accb += sD[threadIdx.x * kRow + q];
+      for (int e = 0; e < 8; ++e) {
+        const int c = 8 * (qq + 4 * i) + e;
+        const float xh = (tile_h(sXh, c, pr) - mean) * rstd;
+        tile_h_set(sXh, c, pr, rstd * (dv[e] * gamma[c] - a - xh * bb));
       }
     }
     __syncthreads();
+    store_cm_tile_h<Ch>(sXh, dX, b, pos0, NN);
+    if (reducer) {
+      const float* rg = sG + rc * kRow + rpart * kPP;
+      const float* rd = sD + rc * kRow + rpart * kPP;
+      float g4[4] = {0.f, 0.f, 0.f, 0.f}, b4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < kPP; q += 4)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          g4[u] += rg[q + u];
+          b4[u] += rd[q + u];
+        }
+      accg += (g4[0] + g4[1]) + (g4[2] + g4[3]);
+      accb += (b4[0] + b4[1]) + (b4[2] + b4[3]);
+    }
+    if (tile + gridDim.x < tiles) fetch(tile + gridDim.x);
+    __syncthreads();
   }
+  if (reducer) {
+    sG[rpart * Ch + rc] = accg;
+    sD[rpart * Ch + rc] = accb;
+  }
+  __syncthreads();
   if (threadIdx.x < Ch) {
-    part_g[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = accg;
-    part_b[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = accb;
+    float g = 0.f, bsum = 0.f;
+#pragma unroll
+    for (int p = 0; p < kSplit; ++p) {
+      g += sG[p * Ch + threadIdx.x];
+      bsum += sD[p * Ch + threadIdx.x];
+    }
+    part_g[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = g;
+    part_b[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = bsum;
   }
 }
 
@@ -278,8 +340,13 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const uint16_t* __restric
   constexpr int kCh = Ch / 32;
   const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
   const size_t b = m0 / NN, pos0 = m0 % NN;
-  load_cm_tile_h<Ch>(dA, b, pos0, NN, sA);
-  load_cm_tile_h<Ch>(dB, b, pos0, NN, sB);
+  {
+    uint4 ra[Ch * 8 / 256], rb[Ch * 8 / 256];
+    fetch_cm_tile<Ch>(dA, b, pos0, NN, ra);
+    fetch_cm_tile<Ch>(dB, b, pos0, NN, rb);
+    put_cm_tile<Ch>(ra, sA);
+    put_cm_tile<Ch>(rb, sB);
+  }
   __syncthreads();
   const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
   const size_t m = m0 + pr;

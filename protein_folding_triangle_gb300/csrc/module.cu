@@ -30,59 +30,69 @@ namespace {
 
 using namespace pairops;
 
-// Pair layout -> core layout for one H*D block of a row-major [M, ld] matrix:
-// dst[b, i, h, j, d] = src[(b, i, j), off + h D + d], 8 features per thread.
+// Pair layout -> core layout for nblk consecutive H*D blocks of a row-major
+// [M, ld] matrix: dst_t[b, i, h, j, d] = src[(b, i, j), off + t H D + h D + d]
+// for t < nblk, 8 features per thread.
 __global__ void __launch_bounds__(256) heads_split_kernel(const uint16_t* __restrict__ src, int ld, int off,
-                                                          uint16_t* __restrict__ dst, int N, int H, int D,
+                                                          uint16_t* __restrict__ dst0, uint16_t* __restrict__ dst1,
+                                                          uint16_t* __restrict__ dst2, int nblk, int N, int H, int D,
                                                           size_t M) {
-  const int chunks = H * D / 8;
+  const int per = H * D / 8;
+  const int chunks = nblk * per;
   const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= M * chunks) return;
   const size_t m = t / chunks;
   const int c = static_cast<int>(t % chunks);
-  const int h = (8 * c) / D, d0 = (8 * c) % D;
+  const int blk = c / per, cc = c % per;
+  const int h = (8 * cc) / D, d0 = (8 * cc) % D;
   const size_t bi = m / N;
   const int j = static_cast<int>(m % N);
+  uint16_t* dst = blk == 0 ? dst0 : (blk == 1 ? dst1 : dst2);
   const uint4 w = *reinterpret_cast<const uint4*>(src + m * ld + off + 8 * c);
   *reinterpret_cast<uint4*>(dst + ((bi * H + h) * N + j) * D + d0) = w;
 }
 
-// Core layout -> pair layout: dst[(b, i, j), off + h D + d] = src[b, i, h, j, d].
-__global__ void __launch_bounds__(256) heads_merge_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                                                          int ld, int off, int N, int H, int D, size_t M) {
-  const int chunks = H * D / 8;
+// Core layout -> pair layout: dst[(b, i, j), off + t H D + h D + d] = src_t[b, i, h, j, d].
+__global__ void __launch_bounds__(256) heads_merge_kernel(const uint16_t* __restrict__ src0,
+                                                          const uint16_t* __restrict__ src1,
+                                                          const uint16_t* __restrict__ src2, int nblk,
+                                                          uint16_t* __restrict__ dst, int ld, int off, int N, int H,
+                                                          int D, size_t M) {
+  const int per = H * D / 8;
+  const int chunks = nblk * per;
   const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= M * chunks) return;
   const size_t m = t / chunks;
   const int c = static_cast<int>(t % chunks);
-  const int h = (8 * c) / D, d0 = (8 * c) % D;
+  const int blk = c / per, cc = c % per;
+  const int h = (8 * cc) / D, d0 = (8 * cc) % D;
   const size_t bi = m / N;
   const int j = static_cast<int>(m % N);
+  const uint16_t* src = blk == 0 ? src0 : (blk == 1 ? src1 : src2);
   *reinterpret_cast<uint4*>(dst + m * ld + off + 8 * c) =
       *reinterpret_cast<const uint4*>(src + ((bi * H + h) * N + j) * D + d0);
 }
 
-// bias[b, h, q, k] = src[(b, q, k), off + h]   (to_pairs = false)
-// dst[(b, q, k), off + h] = bias[b, h, q, k]   (to_pairs = true)
+// bias[b, h, q, k] = pairs[(b, q, k), off + h]   (to_pairs = false)
+// pairs[(b, q, k), off + h] = bias[b, h, q, k]   (to_pairs = true)
+// One thread per pair: its H values share one sector of the pair row, and
+// consecutive threads touch consecutive elements of every bias plane.
 __global__ void __launch_bounds__(256) bias_plane_kernel(uint16_t* __restrict__ pairs, int ld, int off,
                                                          uint16_t* __restrict__ bias, int NN, int H, size_t M,
                                                          bool to_pairs) {
-  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= M * H) return;
-  const size_t m = t % M;  // consecutive threads: consecutive pairs of one plane
-  const int h = static_cast<int>(t / M);
+  const size_t m = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (m >= M) return;
   const size_t b = m / NN, qk = m % NN;
-  uint16_t* pb = bias + (b * H + h) * NN + qk;
-  uint16_t* pp = pairs + m * ld + off + h;
-  if (to_pairs) {
-    *pp = *pb;
-    // the row's padding columns [off + H, ld) enter the backward GEMMs (times
-    // zero weights): they must hold zeros, not whatever the workspace held
-    if (h == 0)
-      for (int c = off + H; c < ld; ++c) pairs[m * ld + c] = 0;
-  } else {
-    *pb = *pp;
+  uint16_t* row = pairs + m * ld;
+  for (int h = 0; h < H; ++h) {
+    uint16_t* pb = bias + (b * H + h) * NN + qk;
+    if (to_pairs) row[off + h] = *pb;
+    else *pb = row[off + h];
   }
+  // the row's padding columns [off + H, ld) enter the backward GEMMs (times
+  // zero weights): they must hold zeros, not whatever the workspace held
+  if (to_pairs)
+    for (int c = off + H; c < ld; ++c) row[c] = 0;
 }
 
 // dst [rows, ldd] = src [rows, cols] with zero columns [cols, ldd) (the
@@ -179,26 +189,28 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 unsigned blocks_for(size_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
-cudaError_t split_heads(const ModDims& d, const uint16_t* src, int ld, int off, uint16_t* dst, cudaStream_t s) {
+// nblk (1 or 3) consecutive H*D blocks of the pair rows, to / from as many
+// [B, N, H, N, D] tensors.
+cudaError_t split_heads(const ModDims& d, const uint16_t* src, int ld, int off, int nblk, uint16_t* d0, uint16_t* d1,
+                        uint16_t* d2, cudaStream_t s) {
   return trace_call(kKModLayout, s, [&] {
-    heads_split_kernel<<<blocks_for(d.M * (d.HD / 8)), 256, 0, s>>>(src, ld, off, dst, static_cast<int>(d.N),
-                                                                    static_cast<int>(d.H), static_cast<int>(d.D),
-                                                                    d.M);
+    heads_split_kernel<<<blocks_for(d.M * nblk * (d.HD / 8)), 256, 0, s>>>(
+        src, ld, off, d0, d1, d2, nblk, static_cast<int>(d.N), static_cast<int>(d.H), static_cast<int>(d.D), d.M);
     return cudaGetLastError();
   });
 }
-cudaError_t merge_heads(const ModDims& d, const uint16_t* src, uint16_t* dst, int ld, int off, cudaStream_t s) {
+cudaError_t merge_heads(const ModDims& d, const uint16_t* s0, const uint16_t* s1, const uint16_t* s2, int nblk,
+                        uint16_t* dst, int ld, int off, cudaStream_t s) {
   return trace_call(kKModLayout, s, [&] {
-    heads_merge_kernel<<<blocks_for(d.M * (d.HD / 8)), 256, 0, s>>>(src, dst, ld, off, static_cast<int>(d.N),
-                                                                    static_cast<int>(d.H), static_cast<int>(d.D),
-                                                                    d.M);
+    heads_merge_kernel<<<blocks_for(d.M * nblk * (d.HD / 8)), 256, 0, s>>>(
+        s0, s1, s2, nblk, dst, ld, off, static_cast<int>(d.N), static_cast<int>(d.H), static_cast<int>(d.D), d.M);
     return cudaGetLastError();
   });
 }
 cudaError_t bias_planes(const ModDims& d, uint16_t* pairs, int ld, int off, uint16_t* bias, bool to_pairs,
                         cudaStream_t s) {
   return trace_call(kKModLayout, s, [&] {
-    bias_plane_kernel<<<blocks_for(d.M * d.H), 256, 0, s>>>(pairs, ld, off, bias, static_cast<int>(d.N * d.N),
+    bias_plane_kernel<<<blocks_for(d.M), 256, 0, s>>>(pairs, ld, off, bias, static_cast<int>(d.N * d.N),
                                                              static_cast<int>(d.H), d.M, to_pairs);
     return cudaGetLastError();
   });
@@ -254,7 +266,7 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   cublasHandle_t h = nullptr;
   if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
   const int M = static_cast<int>(d.M), C = static_cast<int>(d.C), HD = static_cast<int>(d.HD),
-            F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
+            Fp = static_cast<int>(d.Fp);
   float* mean = reinterpret_cast<float*>(cx + c.mean);
   float* rstd = reinterpret_cast<float*>(cx + c.rstd);
   uint16_t* P = reinterpret_cast<uint16_t*>(ws + w.p);
@@ -270,10 +282,9 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
       TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // q, k, v and the bias planes
-  const size_t dsts[3] = {c.q, c.k, c.v};
-  for (int t = 0; t < 3; ++t)
-    if (split_heads(d, P, Fp, t * HD, reinterpret_cast<uint16_t*>(cx + dsts[t]), s) != cudaSuccess)
-      return TRIATTN_ERR_CUDA;
+  if (split_heads(d, P, Fp, 0, 3, reinterpret_cast<uint16_t*>(cx + c.q), reinterpret_cast<uint16_t*>(cx + c.k),
+                  reinterpret_cast<uint16_t*>(cx + c.v), s) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
   if (bias_planes(d, P, Fp, 3 * HD, reinterpret_cast<uint16_t*>(cx + c.bias), false, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // the attention core
@@ -281,8 +292,8 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
                     reinterpret_cast<float*>(cx + c.lse), cx + c.resid, stream);
   if (st != TRIATTN_OK) return st;
   // out = o_flat W_o
-  if (merge_heads(d, reinterpret_cast<const uint16_t*>(cx + c.o), reinterpret_cast<uint16_t*>(cx + c.oflat), HD, 0,
-                  s) != cudaSuccess)
+  const uint16_t* o_core = reinterpret_cast<const uint16_t*>(cx + c.o);
+  if (merge_heads(d, o_core, o_core, o_core, 1, reinterpret_cast<uint16_t*>(cx + c.oflat), HD, 0, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   return gemm_traced(kKModGemm, h, s, false, false, M, C, HD, cx + c.oflat, HD, w_o, C, out, C, CUDA_R_16BF);
 }
@@ -310,13 +321,14 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   cublasHandle_t h = nullptr;
   if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
   const int M = static_cast<int>(d.M), C = static_cast<int>(d.C), HD = static_cast<int>(d.HD),
-            F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
+            Fp = static_cast<int>(d.Fp);
   // out = o_flat W_o:  dW_o = o_flat^T d_out,  d_oflat = d_out W_o^T
   if (gemm_traced(kKModGemm, h, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, CUDA_R_32F) != TRIATTN_OK ||
       gemm_traced(kKModGemm, h, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, CUDA_R_16BF) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
-  if (split_heads(d, reinterpret_cast<const uint16_t*>(ws + w.doflat), HD, 0,
-                  reinterpret_cast<uint16_t*>(ws + w.dobuf), s) != cudaSuccess)
+  uint16_t* dobuf = reinterpret_cast<uint16_t*>(ws + w.dobuf);
+  if (split_heads(d, reinterpret_cast<const uint16_t*>(ws + w.doflat), HD, 0, 1, dobuf, dobuf, dobuf, s) !=
+      cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // the attention core
   st = tri_attn_bwd(&core, cx + c.q, cx + c.k, cx + c.v, cx + c.bias, mask, cx + c.o, cx + c.resid,
@@ -325,10 +337,9 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   if (st != TRIATTN_OK) return st;
   // dP = [dq | dk | dv | dbias] in the pair layout
   uint16_t* dP = reinterpret_cast<uint16_t*>(ws + w.p);
-  const size_t srcs[3] = {w.dq, w.dk, w.dv};
-  for (int t = 0; t < 3; ++t)
-    if (merge_heads(d, reinterpret_cast<const uint16_t*>(ws + srcs[t]), dP, Fp, t * HD, s) != cudaSuccess)
-      return TRIATTN_ERR_CUDA;
+  if (merge_heads(d, reinterpret_cast<const uint16_t*>(ws + w.dq), reinterpret_cast<const uint16_t*>(ws + w.dk),
+                  reinterpret_cast<const uint16_t*>(ws + w.dv), 3, dP, Fp, 0, s) != cudaSuccess)
+    return TRIATTN_ERR_CUDA;
   if (bias_planes(d, dP, Fp, 3 * HD, reinterpret_cast<uint16_t*>(ws + w.dbias), true, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // P = x W_in:  dW_in = x^T dP,  dx = dP W_in^T (FP32), both Fp wide (dP's

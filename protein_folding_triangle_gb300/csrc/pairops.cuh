@@ -20,7 +20,8 @@ namespace {
 namespace pairops {
 
 constexpr int kMaxC = 256;          // LayerNorm: up to 8 features per lane
-constexpr int kLnBlocks = 152 * 8;  // fixed: the dgamma / dbeta partial rows depend on it
+constexpr int kLnBlocks = 152 * 5;     // backward grid, one wave; the dgamma / dbeta partial rows depend on it
+constexpr int kLnFwdBlocks = 152 * 8;  // forward grid (no partials): eight blocks per SM
 constexpr size_t kBlasWorkspace = 32u << 20;
 
 inline bool ln_width_ok(int C) { return C >= 32 && C <= kMaxC && C % 32 == 0; }
@@ -31,8 +32,91 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// K consecutive features of one row, in the widest aligned vector accesses
+// the count allows (rows are C = 32 K elements, so lane l's run starts at
+// l K, which is 2 K-byte aligned for BF16 and 4 K-byte aligned for FP32).
+template <int K>
+__device__ __forceinline__ void ld_bf16(const uint16_t* p, float (&f)[K]) {
+  if constexpr (K % 8 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 8; ++j) {
+      const uint4 w = reinterpret_cast<const uint4*>(p)[j];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        f[8 * j + 2 * h] = bf16lo_to_f32(ws[h]);
+        f[8 * j + 2 * h + 1] = bf16hi_to_f32(ws[h]);
+      }
+    }
+  } else if constexpr (K % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 4; ++j) {
+      const uint2 w = reinterpret_cast<const uint2*>(p)[j];
+      f[4 * j] = bf16lo_to_f32(w.x);
+      f[4 * j + 1] = bf16hi_to_f32(w.x);
+      f[4 * j + 2] = bf16lo_to_f32(w.y);
+      f[4 * j + 3] = bf16hi_to_f32(w.y);
+    }
+  } else if constexpr (K % 2 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 2; ++j) {
+      const uint32_t w = reinterpret_cast<const uint32_t*>(p)[j];
+      f[2 * j] = bf16lo_to_f32(w);
+      f[2 * j + 1] = bf16hi_to_f32(w);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < K; ++e) f[e] = bf16lo_to_f32(p[e]);
+  }
+}
+template <int K>
+__device__ __forceinline__ void st_bf16(uint16_t* p, const float (&f)[K]) {
+  if constexpr (K % 8 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 8; ++j)
+      reinterpret_cast<uint4*>(p)[j] =
+          make_uint4(pack_bf16x2(f[8 * j], f[8 * j + 1]), pack_bf16x2(f[8 * j + 2], f[8 * j + 3]),
+                     pack_bf16x2(f[8 * j + 4], f[8 * j + 5]), pack_bf16x2(f[8 * j + 6], f[8 * j + 7]));
+  } else if constexpr (K % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 4; ++j)
+      reinterpret_cast<uint2*>(p)[j] =
+          make_uint2(pack_bf16x2(f[4 * j], f[4 * j + 1]), pack_bf16x2(f[4 * j + 2], f[4 * j + 3]));
+  } else if constexpr (K % 2 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 2; ++j) reinterpret_cast<uint32_t*>(p)[j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < K; ++e) p[e] = static_cast<uint16_t>(pack_bf16x2(f[e], 0.f) & 0xFFFFu);
+  }
+}
+template <int K>
+__device__ __forceinline__ void ld_f32(const float* p, float (&f)[K]) {
+  if constexpr (K % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 4; ++j) {
+      const float4 v = reinterpret_cast<const float4*>(p)[j];
+      f[4 * j] = v.x;
+      f[4 * j + 1] = v.y;
+      f[4 * j + 2] = v.z;
+      f[4 * j + 3] = v.w;
+    }
+  } else if constexpr (K % 2 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 2; ++j) {
+      const float2 v = reinterpret_cast<const float2*>(p)[j];
+      f[2 * j] = v.x;
+      f[2 * j + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < K; ++e) f[e] = p[e];
+  }
+}
+
 // One warp per pair: x = (z - mean) * rstd * gamma + beta (BF16), mean and
-// rstd saved in FP32.  Lane l holds features l, l + 32, ...
+// rstd saved in FP32.  Lane l holds the C / 32 consecutive features from
+// l C / 32.
 template <int C>
 __global__ void __launch_bounds__(256) ln_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ gamma,
                                                      const float* __restrict__ beta, uint16_t* __restrict__ x,
@@ -40,25 +124,26 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const uint16_t* __restrict_
                                                      size_t M) {
   constexpr int kPer = C / 32;
   const int lane = threadIdx.x & 31;
+  const int c0 = lane * kPer;
+  float gm[kPer], bt[kPer];
+  ld_f32<kPer>(gamma + c0, gm);
+  ld_f32<kPer>(beta + c0, bt);
   const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
   for (size_t m = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; m < M; m += warps) {
     float v[kPer];
+    ld_bf16<kPer>(z + m * C + c0, v);
     float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      v[e] = bf16lo_to_f32(z[m * C + lane + 32 * e]);
-      s += v[e];
-    }
+    for (int e = 0; e < kPer; ++e) s += v[e];
     const float mean = warp_sum(s) * (1.f / C);
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) ss += (v[e] - mean) * (v[e] - mean);
     const float rstd = rsqrtf(warp_sum(ss) * (1.f / C) + 1e-5f);
+    float o[kPer];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int c = lane + 32 * e;
-      x[m * C + c] = static_cast<uint16_t>(pack_bf16x2((v[e] - mean) * rstd * gamma[c] + beta[c], 0.f) & 0xFFFFu);
-    }
+    for (int e = 0; e < kPer; ++e) o[e] = (v[e] - mean) * rstd * gm[e] + bt[e];
+    st_bf16<kPer>(x + m * C + c0, o);
     if (lane == 0) {
       mean_out[m] = mean;
       rstd_out[m] = rstd;
@@ -69,7 +154,8 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const uint16_t* __restrict_
 // One warp per pair: dz = rstd (g - mean(g) - xhat mean(g xhat)), g = dx gamma.
 // The warp also accumulates dgamma = sum dx xhat and dbeta = sum dx over its
 // pairs (fixed grid-stride assignment); the block adds its 8 warps' sums in
-// warp order and writes one partial row per block.
+// warp order and writes one partial row per block.  Lane l holds the C / 32
+// consecutive features from l C / 32.
 template <int C>
 __global__ void __launch_bounds__(256) ln_bwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ dx,
                                                      const float* __restrict__ gamma,
@@ -80,35 +166,38 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const uint16_t* __restrict_
   constexpr int kPer = C / 32;
   __shared__ float red_g[8][C], red_b[8][C];
   const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
+  const int c0 = lane * kPer;
+  float gm[kPer];
+  ld_f32<kPer>(gamma + c0, gm);
   const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
   float accg[kPer], accb[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) accg[e] = accb[e] = 0.f;
   for (size_t m = static_cast<size_t>(blockIdx.x) * 8 + warp; m < M; m += warps) {
     const float mean = mean_in[m], rstd = rstd_in[m];
-    float xh[kPer], g[kPer];
+    float xh[kPer], d[kPer], g[kPer];
+    ld_bf16<kPer>(z + m * C + c0, xh);
+    ld_f32<kPer>(dx + m * C + c0, d);
     float sg = 0.f, sgx = 0.f;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-      const int c = lane + 32 * e;
-      xh[e] = (bf16lo_to_f32(z[m * C + c]) - mean) * rstd;
-      const float d = dx[m * C + c];
-      accg[e] += d * xh[e];
-      accb[e] += d;
-      g[e] = d * gamma[c];
+      xh[e] = (xh[e] - mean) * rstd;
+      accg[e] += d[e] * xh[e];
+      accb[e] += d[e];
+      g[e] = d[e] * gm[e];
       sg += g[e];
       sgx += g[e] * xh[e];
     }
     const float a = warp_sum(sg) * (1.f / C), bb = warp_sum(sgx) * (1.f / C);
+    float o[kPer];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e)
-      dz[m * C + lane + 32 * e] =
-          static_cast<uint16_t>(pack_bf16x2(rstd * (g[e] - a - xh[e] * bb), 0.f) & 0xFFFFu);
+    for (int e = 0; e < kPer; ++e) o[e] = rstd * (g[e] - a - xh[e] * bb);
+    st_bf16<kPer>(dz + m * C + c0, o);
   }
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
-    red_g[warp][lane + 32 * e] = accg[e];
-    red_b[warp][lane + 32 * e] = accb[e];
+    red_g[warp][c0 + e] = accg[e];
+    red_b[warp][c0 + e] = accb[e];
   }
   __syncthreads();
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
@@ -142,7 +231,7 @@ __global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict
 template <int C>
 cudaError_t ln_fwd_launch(size_t M, const void* z, const float* g, const float* b, void* x, float* mean,
                           float* rstd, cudaStream_t s) {
-  ln_fwd_kernel<C><<<kLnBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), g, b, static_cast<uint16_t*>(x),
+  ln_fwd_kernel<C><<<kLnFwdBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), g, b, static_cast<uint16_t*>(x),
                                              mean, rstd, M);
   return cudaGetLastError();
 }

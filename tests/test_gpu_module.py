@@ -59,6 +59,10 @@ CASES = [
     (1, 40, 64, 2, 16, 0.0),
     (2, 48, 32, 1, 32, 0.2),
     (1, 136, 128, 4, 32, 0.1),
+    # LayerNorm runs of 3 and 6 features per lane (scalar and 4-byte accesses);
+    # H = 3 gives a projection width of 291 (padded to 296)
+    (1, 40, 96, 2, 16, 0.0),
+    (1, 32, 192, 3, 32, 0.1),
 ]
 
 

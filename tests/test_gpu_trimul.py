@@ -56,6 +56,12 @@ CASES = [
     (1, 40, 64, 32, 0.0),
     (2, 48, 32, 64, 0.2),
     (1, 136, 128, 128, 0.1),
+    # input-LayerNorm runs of 3, 5 and 8 features per lane (scalar and 16-byte
+    # accesses), and C_h = 96 (three channel-major loads per thread, two
+    # threads per channel in the output-LayerNorm sums, the rest idle)
+    (1, 48, 96, 96, 0.1),
+    (1, 40, 160, 32, 0.0),
+    (1, 40, 256, 64, 0.0),
 ]
 
 

@@ -14,6 +14,12 @@ the result does not depend on how the gather was scheduled.
 Shards are whole multiples of 8 slices (both backward group sizes divide
 them).  Every compute step runs in the library's kernels; this module only
 splits ranges and moves the FP32 parts.
+
+The same split also bounds memory on one GPU: ``chunked_tri_attn_bwd`` runs
+the outer axis in chunks whose FP32 partials fit a workspace cap (the
+partials of one call grow as N_o N^2, the reason the pages bound them by
+reusing chunked buffers, "TurboPairFormer", Table 2), and combines the
+chunks' FP32 dbias parts in order.
 """
 from __future__ import annotations
 
@@ -62,4 +68,57 @@ def sharded_tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *,
                                       stream=stream, dbias_fp32=True)
     parts = gather_rank_ordered(part, group)
     dbias = T.tri_attn_dbias_combine(parts, stream=stream)
+    return dq, dk, dv, dbias
+
+
+def chunk_slices(n_outer: int, bytes_for, max_workspace_bytes: int, multiple: int = SHARD_MULTIPLE) -> int:
+    """The largest chunk of outer slices (a multiple of ``multiple``, at most
+    ``n_outer``) whose backward workspace ``bytes_for(chunk)`` fits in
+    ``max_workspace_bytes``; raises if not even one block fits."""
+    if n_outer % multiple != 0:
+        raise ValueError(f"the outer axis ({n_outer}) must be a multiple of {multiple}")
+    best = 0
+    for c in range(multiple, n_outer + 1, multiple):
+        need = bytes_for(c)
+        if need == 0:
+            raise ValueError(f"unsupported shape for a chunk of {c} slices")
+        if need <= max_workspace_bytes:
+            best = c
+        else:
+            break  # the workspace grows with the chunk
+    if best == 0:
+        raise ValueError(f"a chunk of {multiple} slices needs {bytes_for(multiple)} workspace bytes, "
+                         f"more than {max_workspace_bytes}")
+    return best
+
+
+def chunked_tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, max_workspace_bytes: int, stream=None):
+    """Backward with a bounded workspace.  The FP32 dQ and dbias partials of
+    one call grow with N_o * N^2; this runs the outer axis in consecutive
+    chunks (per example) whose workspace fits ``max_workspace_bytes``, one
+    workspace reused by every chunk.  dQ, dK and dV are those of the one-call
+    backward, bit for bit (slices are independent); dbias is each chunk's FP32
+    sum added in chunk order and rounded once (``tri_attn_dbias_combine``), so
+    it is reproducible but its FP32 addition order differs from the one-call
+    backward's.  Returns (dq, dk, dv, dbias) in BF16."""
+    B, No, H, N, D = q.shape
+
+    def bytes_for(c):
+        return T.bwd_workspace_bytes(T.Shape(1, c, N, H, D, T.FLAG_DBIAS_FP32))
+
+    chunk = chunk_slices(No, bytes_for, max_workspace_bytes)
+    ws = torch.empty(bytes_for(chunk), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dbias = torch.empty_like(bias)
+    for b in range(B):
+        parts = []
+        for lo in range(0, No, chunk):
+            hi = min(No, lo + chunk)
+            sl = (slice(b, b + 1), slice(lo, hi))
+            part = torch.empty((1, H, N, N), dtype=torch.float32, device=q.device)
+            T.tri_attn_bwd(q[sl], k[sl], v[sl], bias[b:b + 1], None if mask is None else mask[sl], o[sl],
+                           None if o_resid is None else o_resid[sl], lse[sl], do[sl], workspace=ws,
+                           out=(dq[sl], dk[sl], dv[sl], part), stream=stream, dbias_fp32=True)
+            parts.append(part)
+        T.tri_attn_dbias_combine(torch.stack(parts), out=dbias[b:b + 1], stream=stream)
     return dq, dk, dv, dbias

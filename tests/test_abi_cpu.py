@@ -338,3 +338,28 @@ def test_trimul_sizes_and_argument_checks(lib):
     assert bwd(s, ws, mask=ctypes.c_void_p(FAKE + 6)) == T.ERR_INVALID_ARG
     assert bwd(T.TriMulShape(1, 40, 288, 32, 1, 0), ws) == T.ERR_UNSUPPORTED
     assert bwd(s, 100) == T.ERR_WORKSPACE
+
+
+def test_chunk_slices_picks_the_largest_fitting_multiple():
+    from protein_folding_triangle_gb300 import sharding as SH
+    per = lambda c: 1000 + 10 * c  # noqa: E731  (grows with the chunk)
+    assert SH.chunk_slices(64, per, 1000 + 10 * 24) == 24
+    assert SH.chunk_slices(64, per, 1000 + 10 * 31) == 24
+    assert SH.chunk_slices(64, per, 10 ** 9) == 64
+    with pytest.raises(ValueError):
+        SH.chunk_slices(64, per, 1000)          # not even 8 slices fit
+    with pytest.raises(ValueError):
+        SH.chunk_slices(60, per, 10 ** 9)       # not a multiple of 8
+
+
+def test_chunked_backward_workspace_is_bounded(lib):
+    """The per-chunk workspace of the chunked backward grows with the chunk,
+    so capping it bounds the backward's memory; the one-call workspace of a
+    4096-token crop (H = 4, D = 32) is far above any GPU's memory."""
+    from protein_folding_triangle_gb300 import sharding as SH
+    N, H, D = 4096, 4, 32
+    one_call = T.bwd_workspace_bytes(T.Shape(1, N, N, H, D, 0))
+    assert one_call > 400 * 2 ** 30
+    per = lambda c: T.bwd_workspace_bytes(T.Shape(1, c, N, H, D, T.FLAG_DBIAS_FP32))  # noqa: E731
+    c = SH.chunk_slices(N, per, 16 * 2 ** 30)
+    assert 8 <= c < N and per(c) <= 16 * 2 ** 30 < per(c + 8)

@@ -324,3 +324,28 @@ def test_residual_compensation_ablation_fp32_dbias():
     off = float(np.mean([e[1] for e in res]))
     print(json.dumps({"ablation_fp32_dbias_crop384": {"on": on, "off": off, "reduction": 1.0 - on / off}}))
     assert on < off, (on, off)
+
+
+def test_chunked_backward_matches_one_call():
+    """Memory-bounded backward (outer axis in chunks of 48, 48 and 40 slices
+    per example): dQ, dK, dV bit for bit those of the one-call backward; dbias
+    (chunk parts added in order in FP32, rounded once) within the bar of the
+    FP64 oracle."""
+    from protein_folding_triangle_gb300 import sharding as SH
+    w = S.custom(2, 136, 2, 32, name="chunked", mask="random", mask_frac=0.1)
+    x = S.make_inputs(w, seed=5)
+    xd = to_dev(x)
+    o, lse, resid = T.tri_attn_fwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"])
+    one = T.tri_attn_bwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], o, resid, lse, xd["do"])
+    cap = T.bwd_workspace_bytes(T.Shape(1, 48, 136, 2, 32, T.FLAG_DBIAS_FP32))
+    ch = SH.chunked_tri_attn_bwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], o, resid, lse, xd["do"],
+                                 max_workspace_bytes=cap)
+    torch.cuda.synchronize()
+    assert T.device_status() == T.OK
+    for a, b in zip(one[:3], ch[:3]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref = oracle_full(x)
+    err = rel_rmse(cpu64(ch[3]), ref["dbias"])
+    diff = rel_rmse(cpu64(ch[3]), cpu64(one[3]))
+    print(json.dumps({"case": "chunked backward", "dbias_vs_fp64": round(err, 6), "dbias_vs_one_call": round(diff, 6)}))
+    assert err <= TOL_GRAD

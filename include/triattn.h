@@ -238,8 +238,8 @@ triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* p
  * and the core's, and the LayerNorm's parameter-gradient sums are the
  * library's kernels; the core is tri_attn_fwd / tri_attn_bwd.
  *
- * Shape: B >= 1, N as for the core (multiple of 8, 8..4096), C a multiple
- * of 32 up to 256, H up to 64, D 16 or 32, flags 0.  Otherwise
+ * Shape: B >= 1, N as for the core (multiple of 8, 8..4096), B*N*N < 2^31,
+ * C a multiple of 32 up to 256, H up to 64, D 16 or 32, flags 0.  Otherwise
  * TRIATTN_ERR_INVALID_ARG (non-positive field, flags) or
  * TRIATTN_ERR_UNSUPPORTED; the size queries return 0.
  *

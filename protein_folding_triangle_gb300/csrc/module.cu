@@ -180,6 +180,8 @@ triattn_status check_module(const triattn_module_shape* s, triattn_shape* core) 
   if (s == nullptr || s->flags != 0 || s->B < 1 || s->N < 1 || s->C < 1 || s->H < 1 || s->D < 1)
     return TRIATTN_ERR_INVALID_ARG;
   if (!ln_width_ok(s->C) || s->H > 64) return TRIATTN_ERR_UNSUPPORTED;
+  // the projection GEMMs take the pair count as a 32-bit row count
+  if (static_cast<size_t>(s->B) * s->N * s->N > 0x7fffffffull) return TRIATTN_ERR_UNSUPPORTED;
   *core = triattn_shape{s->B, s->N, s->N, s->H, s->D, 0u};
   if (triattn_bwd_workspace_bytes(core) == 0) return TRIATTN_ERR_UNSUPPORTED;  // the core's own shape rules
   return TRIATTN_OK;

@@ -276,7 +276,7 @@ def test_module_sizes(lib):
     core = T.bwd_workspace_bytes(T.Shape(B_, N, N, H, D, 0))
     assert ws >= core + (32 << 20) + B_ * N * N * (3 * H * D + H) * 2
     for bad in [(1, 40, 48, 2, 16), (1, 40, 288, 2, 16), (1, 44, 64, 2, 16), (1, 40, 64, 2, 8), (0, 40, 64, 2, 16),
-                (1, 40, 64, 65, 16)]:
+                (1, 40, 64, 65, 16), (128, 4096, 64, 2, 16)]:
         assert T.module_sizes(*bad) == (0, 0), bad
 
 

@@ -5,7 +5,8 @@ update.
 
 ``triattn`` is the ctypes binding, ``build`` compiles the CUDA library
 in-tree, ``synthetic`` draws seeded inputs, ``sharding`` splits the outer axis
-across GPUs or into memory-bounded chunks on one GPU.
+across GPUs or into memory-bounded chunks on one GPU, ``layers`` wraps the
+module and the multiplicative update as autograd functions and torch modules.
 """
 from . import build, synthetic, triattn  # noqa: F401
 from .triattn import (TriAttnError, bwd_workspace_bytes, device_status, set_wait_limit_ns,  # noqa: F401

@@ -150,3 +150,26 @@ def test_module_full_size_sampled():
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     for a, b in zip(grads, grads2):
         assert torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))
+
+
+def test_module_autograd_matches_direct_calls():
+    """TriangleAttention (nn.Module + autograd) returns the direct calls'
+    output and gradients (FP32 gradients cast to each parameter's dtype)."""
+    from protein_folding_triangle_gb300 import layers
+    B, N, C, H, D = 1, 40, 64, 2, 16
+    x = S.make_module_inputs(B, N, C, H, D, seed=31, mask_frac=0.1)
+    dev = {k: (v.cuda().contiguous() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    m = layers.TriangleAttention(C, H, D, device="cuda")
+    with torch.no_grad():
+        m.ln_w.copy_(dev["ln_w"])
+        m.ln_b.copy_(dev["ln_b"])
+        m.w_in.copy_(dev["w_in"])
+        m.w_o.copy_(dev["w_o"])
+    z = dev["z"].clone().requires_grad_(True)
+    out = m(z, dev["mask"])
+    out.backward(dev["d_out"])
+    ref_out, grads = run_gpu(x)
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(z.grad.view(torch.int16), grads[0].view(torch.int16))
+    for p, g in ((m.ln_w, grads[1]), (m.ln_b, grads[2]), (m.w_in, grads[3]), (m.w_o, grads[4])):
+        assert torch.equal(p.grad, g.to(p.dtype))

@@ -136,3 +136,27 @@ def test_trimul_full_size_sampled(direction):
     out2, grads2 = run_gpu(x, direction)
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(grads[3].view(torch.int32), grads2[3].view(torch.int32))
+
+
+@pytest.mark.parametrize("direction", ["outgoing", "incoming"])
+def test_trimul_autograd_matches_direct_calls(direction):
+    """TriangleMultiplication (nn.Module + autograd) returns the direct calls'
+    output and gradients (FP32 gradients cast to each parameter's dtype)."""
+    from protein_folding_triangle_gb300 import layers
+    B, N, Cz, Ch = 1, 40, 64, 32
+    x = S.make_trimul_inputs(B, N, Cz, Ch, seed=32, pad_frac=0.1)
+    dev = {k: (v.cuda().contiguous() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    m = layers.TriangleMultiplication(Cz, Ch, direction, device="cuda")
+    names = ("ln_in_w", "ln_in_b", "w_p", "ln_out_w", "ln_out_b", "w_o")
+    with torch.no_grad():
+        for n in names:
+            getattr(m, n).copy_(dev[n])
+    z = dev["z"].clone().requires_grad_(True)
+    out = m(z, dev["mask"])
+    out.backward(dev["d_out"])
+    ref_out, grads = run_gpu(x, direction)
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(z.grad.view(torch.int16), grads[0].view(torch.int16))
+    for n, g in zip(names, grads[1:]):
+        p = getattr(m, n)
+        assert torch.equal(p.grad, g.to(p.dtype))

@@ -19,7 +19,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstring>
 
 #include "kernels.cuh"
 #include "pairops.cuh"
@@ -105,7 +104,6 @@ __global__ void __launch_bounds__(256) pad_columns_kernel(const uint16_t* __rest
   dst[t] = c < cols ? src[static_cast<size_t>(r) * cols + c] : static_cast<uint16_t>(0);
 }
 
-// ---------------------------------------------------------------- cuBLAS
 // ---------------------------------------------------------------- layouts
 size_t rup(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -148,7 +146,6 @@ CtxLayout ctx_layout(const ModDims& d) {
   c.total = o;
   return c;
 }
-
 
 // Scratch of one forward or backward call.
 struct WsLayout2 {

@@ -241,7 +241,7 @@ def oracle_sample(w, x, seconds: float, gpu_out=None):
     dt, ref = run(n)
     U = 1 * n * w.H * w.N * w.N * w.D
     value = 14 * U / dt / 1e12
-    res = {"value": value, "unit": UNIT, "cores": O.max_threads(), "kind": "oracle",
+    res = {"value": value, "unit": UNIT, "cores": O.max_threads(), "cpu": cpu_model(), "kind": "oracle",
            "sample": f"FP64 oracle fwd+bwd on outer slices 0..{n - 1} of example 0, all {w.H} heads "
                      f"({n}/{w.No * w.B} slices, {dt:.1f} s; 14*U FLOP convention)",
            "seconds": dt}
@@ -252,6 +252,26 @@ def oracle_sample(w, x, seconds: float, gpu_out=None):
             return float(np.sqrt(np.mean((a - r) ** 2)) / np.sqrt(np.mean(r ** 2)))
         rm = {k: rel(gpu_out[k], ref[k]) for k in ("o", "dq", "dk", "dv")}
     return res, rm
+
+
+def cpu_model() -> str:
+    """The host CPU's model as /proc/cpuinfo names it (x86: "model name"; Arm:
+    implementer and part numbers), else the machine type."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"{platform.machine()} (CPU implementer {fields.get('CPU implementer', '?')}, part {fields['CPU part']})"
+    return platform.machine()
 
 
 def run_reference(args):
@@ -275,8 +295,8 @@ def run_reference(args):
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.describe(), "B": w.B, "N": w.N, "H": w.H, "D": w.D},
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
-                             "sample": info["sample"]},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": info["cores"], "cpu": info["cpu"],
+                             "kind": "oracle", "sample": info["sample"]},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -482,7 +502,7 @@ def run_ours(args):
     }
     if not args.no_cpu_baseline:
         cb, rm = oracle_sample(w, x, args.cpu_seconds, gpu_out={"o": o, "dq": dq, "dk": dk, "dv": dv})
-        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "cpu", "kind", "sample")}
         line["rel_rmse_vs_fp64_on_sample"] = rm
     print(json.dumps(line), flush=True)
     if ws > 1:

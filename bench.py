@@ -235,8 +235,11 @@ def oracle_sample(w, x, seconds: float, gpu_out=None):
         dq, dk, dv, _ = O.bwd(sub["q"], sub["k"], sub["v"], bias, sub["mask"], sub["do"])
         return time.perf_counter() - t0, {"o": o, "dq": dq, "dk": dk, "dv": dv}
 
-    t_cal, _ = run(2)
-    per_slice = t_cal / 2
+    # calibrate on enough slices to keep every core busy (the oracle runs
+    # (slice, head) items in parallel), so the estimate scales to the sample
+    n_cal = int(min(w.No, 16))
+    t_cal, _ = run(n_cal)
+    per_slice = t_cal / n_cal
     n = int(max(2, min(w.No, seconds / max(per_slice, 1e-6))))
     dt, ref = run(n)
     U = 1 * n * w.H * w.N * w.N * w.D

@@ -52,9 +52,11 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--calls", type=int, default=100,
+                    help="individually timed fwd / bwd calls (after 10 warm-ups) for the median and mean")
     ap.add_argument("--ablation", choices=["atomic"], default=None,
                     help="instead of the bench line: time the ordered backward against its non-deterministic "
-                         "FP32-atomic variants (dbias; dbias and dQ) on the same inputs and print one JSON line")
+                         "FP32-atomic variants (dQ; dbias; both) on the same inputs and print one JSON line")
     ap.add_argument("--module", type=int, default=0, metavar="C",
                     help="instead of the bench line: time the whole module (LayerNorm, projections with C pair "
                          "features, the core, output projection; forward + backward) and print one JSON line")
@@ -431,6 +433,31 @@ def run_ours(args):
         e2e = {"value": round(evalue, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(ems / args.steps, 4),
                "copies": "overlapped with neighbouring steps (3 streams, double-buffered)"}
+    # ---------------- per-call times: each call bracketed by its own events
+    # (after 10 warm-up calls), median and mean over --calls calls
+    per_call = None
+    if args.calls > 0:
+        for _ in range(10):
+            step(xd)
+        torch.cuda.synchronize(dev)
+        tf, tb = [], []
+        for _ in range(args.calls):
+            c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            c0.record(stream)
+            T.tri_attn_fwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], out=(o, lse, resid))
+            c1.record(stream)
+            T.tri_attn_bwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], o, resid, lse, xd["do"],
+                           workspace=wsb, out=(dq, dk, dv, dbias))
+            c2.record(stream)
+            c2.synchronize()
+            tf.append(c0.elapsed_time(c1))
+            tb.append(c1.elapsed_time(c2))
+        ts = [a + b for a, b in zip(tf, tb)]
+        per_call = {"calls": args.calls, "warmup_calls": 10}
+        for name, v, fl in (("fwd", tf, f_fwd), ("bwd", tb, f_bwd), ("fwd_bwd", ts, f_step)):
+            med, mean = statistics.median(v), statistics.mean(v)
+            per_call[name] = {"median_ms": round(med, 4), "mean_ms": round(mean, 4),
+                              "tflops_at_median": round(fl / (med * 1e-3) / 1e12, 2)}
     if T.device_status() != T.OK:
         raise SystemExit("device status not OK after timing")
 
@@ -454,9 +481,13 @@ def run_ours(args):
     dom = max(trace, key=lambda n: trace[n]["total_ms"])
     amount, unit, bound = kernel_work(w, dom)
     dom_ms = trace[dom]["mean_ms"]
+    # The timed region lasts well under a second (no sustained power-cap
+    # regime), so a contraction is measured against the burst BF16 peak; a
+    # region of seconds would take the sustained one.
+    long_region = ms >= 1000.0
     if unit == "flop":
         achieved = amount / (dom_ms * 1e-3) / 1e12
-        peak = pk["bf16_sustained"]
+        peak = pk["bf16_sustained"] if long_region else pk["bf16_burst"]
         runit = "TFLOP/s"
     else:
         achieved = amount / (dom_ms * 1e-3) / 1e9
@@ -495,10 +526,13 @@ def run_ours(args):
                            "burst": round(value / ws / pk["bf16_burst"], 4), "peaks": pk["source"]},
         "roofline": {"kernel": dom, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{pk['source']} ({'bf16 sustained' if unit == 'flop' else 'hbm copy'})"},
+                     "peak_source": f"{pk['source']} ("
+                                    f"{('bf16 sustained' if long_region else 'bf16 burst') if unit == 'flop' else 'hbm copy'}"
+                                    f"; timed region {ms:.0f} ms)"},
         "secondary": secondary,
         "kernels": kernels,
         "gpu_launches": sum(e["launches"] for e in trace.values()),
+        "per_call": per_call,
         "peak_mem_bytes": int(peak_mem),
         "clocks": clocks,
         "e2e": e2e,
@@ -516,7 +550,7 @@ def run_ours(args):
 # ----------------------------------------------------------------------------- ablation
 def run_atomic_ablation(args):
     """Backward only: the ordered single-writer partials + fixed-order reductions
-    against FP32 atomics for dbias, and for dbias and dQ (the pages' Table 12
+    against FP32 atomics for dQ, for dbias, and for both (the pages' Table 12
     trade-off).  Same inputs, same launch stream, CUDA events, median of
     ``--steps`` timed calls after ``--warmup``; every call re-zeroes its
     accumulators, as a training step would."""
@@ -535,7 +569,8 @@ def run_atomic_ablation(args):
     xd = {k: (None if v is None else v.to(dev)) for k, v in S.make_inputs(w, seed=args.seed).items()}
     o, lse, resid = T.tri_attn_fwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"])
     outs = (torch.empty_like(xd["q"]), torch.empty_like(xd["q"]), torch.empty_like(xd["q"]), torch.empty_like(xd["bias"]))
-    arms = {"ordered": None, "atomic_dbias": T.ATOMIC_DBIAS, "atomic_dbias_dq": T.ATOMIC_DBIAS_DQ}
+    arms = {"ordered": None, "atomic_dq": T.ATOMIC_DQ, "atomic_dbias": T.ATOMIC_DBIAS,
+            "atomic_dbias_dq": T.ATOMIC_DBIAS_DQ}
     wsb = {}
     for name, m in arms.items():
         need = T.bwd_workspace_bytes(xd["q"]) if m is None else T.bwd_atomic_workspace_bytes(xd["q"], m)
@@ -570,7 +605,7 @@ def run_atomic_ablation(args):
             "steps": args.steps, "warmup": max(3, args.warmup),
             "bwd_ms_median": {n: round(v, 4) for n, v in med.items()},
             "saving_vs_ordered": {n: round(1.0 - med[n] / med["ordered"], 4) for n in arms if n != "ordered"},
-            "deterministic": {"ordered": True, "atomic_dbias": False, "atomic_dbias_dq": False},
+            "deterministic": {n: n == "ordered" for n in arms},
             "pages_table12_context": "atomic dbias saves 2.8-8.0% of the backward on the pages' GPUs"}
     print(json.dumps(line), flush=True)
 

@@ -32,7 +32,8 @@
  *    residual 0, lse = -inf and zero gradient contributions.
  *  - The caller owns every buffer, the workspace and the stream.  The library
  *    allocates no device memory; it keeps only host-side state (TMA
- *    descriptors are built per call, kernel attributes are set once).
+ *    descriptors are built per call; kernel attributes are set on a device's
+ *    first call, and set again if a device reset has cleared them).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Argument errors are returned synchronously and nothing
  *    is launched.  A launch failure returns TRIATTN_ERR_CUDA.  A device-side
@@ -73,7 +74,7 @@ typedef struct {
 typedef enum {
   TRIATTN_OK = 0,
   TRIATTN_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad shape field */
-  TRIATTN_ERR_UNSUPPORTED = 2,  /* D not in {16, 32}, N_o != N, size overflow */
+  TRIATTN_ERR_UNSUPPORTED = 2,  /* D not in {16, 32}, a shape outside the supported set, size overflow */
   TRIATTN_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   TRIATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
   TRIATTN_ERR_TIMEOUT = 5       /* a device wait exceeded its limit */
@@ -116,8 +117,9 @@ size_t triattn_bwd_workspace_bytes(const triattn_shape* shape);
  * Backward.  "TurboPairFormer", Abstract, Figure 2, Figure 7(b)-(d),
  * Figure 11(a) and Table 11 (key-tile-parallel partition):
  *   1. preprocess: delta[q] = sum_d dO[q,d] * (o[q,d] + o_resid[q,d]) in FP32
- *      (o_resid NULL: compensation off, delta = sum_d dO*o), stored with
- *      -lse[q]*log2(e) per (slice, query tile);
+ *      (o_resid NULL: compensation off, delta = sum_d dO*o); per query row a
+ *      16-byte record holds -lse[q]*sqrt(D) and -delta[q], each split into
+ *      three BF16 terms;
  *   2. a small kernel writes the bias transposed (key-major) into the
  *      workspace;
  *   3. main: one CTA per (b, h, key tile, outer group of slices) recomputes
@@ -163,9 +165,11 @@ triattn_status tri_attn_bwd(const triattn_shape* shape,
  *     TRIATTN_NOALLOC_SCRATCH_BYTES is rejected with TRIATTN_ERR_WORKSPACE
  *     before anything is launched (B=1, N=48, H=2, D=16 needs 1.6 MiB;
  *     a 384-token crop with H=4, D=32 needs 438 MiB and is rejected).
- *   - The first call on a device looks up the array's device address with
- *     cudaGetSymbolAddress while that device is current.  Make that first
- *     call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     with cudaGetSymbolAddress (no allocation; a device reset gives the
+ *     array a new address).  The first call on a device may also load the
+ *     library's device code there: make that first call before any stream
+ *     capture.
  *   - It calls no cudaMalloc, no cudaFree and no allocating library routine.
  *   - Every call uses the same array, which keeps the previous call's
  *     contents.  Nothing needs clearing: the kernels write every scratch word
@@ -185,18 +189,19 @@ triattn_status tri_attn_bwd_noalloc(const triattn_shape* shape,
 
 /*
  * ABLATION ONLY, not the library's backward: the same computation with the
- * single-writer FP32 partials of dbias (atomic_mask = 2) or of dbias and dQ
- * (atomic_mask = 3) replaced by FP32 atomic adds into zero-initialised FP32
- * accumulators, which small kernels then round to BF16 (the non-deterministic
- * variants of "TurboPairFormer", Section "Deterministic reductions", Table 12).
- * It exists to measure what the ordered partials cost; its dQ / dbias are
- * NOT bitwise reproducible between calls (FP32 addition order varies), dK and
- * dV are.  Arguments are those of tri_attn_bwd; the workspace must hold
+ * single-writer FP32 partials of dQ (atomic_mask = 1), of dbias (2) or of
+ * both (3) replaced by FP32 atomic adds into zero-initialised FP32
+ * accumulators, which small kernels then round to BF16 (the
+ * non-deterministic variants of "TurboPairFormer", Section "Deterministic
+ * reductions", Table 12).  It exists to measure what the ordered partials
+ * cost; the atomically added gradients are NOT bitwise reproducible between
+ * calls (FP32 addition order varies), dK, dV and the ordered one are.
+ * Arguments are those of tri_attn_bwd; the workspace must hold
  * triattn_bwd_atomic_workspace_bytes(shape, atomic_mask) bytes (the row
  * records, the transposed bias, then the FP32 accumulators
  * [B*N_o*H][J_Q*128][D] for dQ and [B*H][J_K*128][J_Q*128] for dbias, or
- * the partials of the operand that stays ordered).  atomic_mask other than
- * 2 or 3 returns TRIATTN_ERR_INVALID_ARG (and 0 bytes).
+ * the partials of the operand that stays ordered).  atomic_mask outside
+ * 1..3 returns TRIATTN_ERR_INVALID_ARG (and 0 bytes).
  */
 size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask);
 triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape,

@@ -16,6 +16,7 @@ import ctypes
 import os
 import platform
 import subprocess
+import tempfile
 import threading
 
 import numpy as np
@@ -73,9 +74,11 @@ def _lib():
 def compile_variant(source_text: str, tag: str) -> str:
     """Compile an edited copy of the oracle source (used by tests that plant
     a mistake in the oracle to show the pins catch it).  Returns the path."""
-    os.makedirs(_BUILD, exist_ok=True)
-    src = os.path.join(_BUILD, f"variant_{tag}_{os.getpid()}.c")
-    out = os.path.join(_BUILD, f"libvariant_{tag}_{os.getpid()}_{platform.machine()}.so")
+    # a private temporary folder, so that planted variants never pile up
+    # next to the oracle's own build
+    d = tempfile.mkdtemp(prefix=f"oracle_variant_{tag}_")
+    src = os.path.join(d, "variant.c")
+    out = os.path.join(d, f"libvariant_{platform.machine()}.so")
     with open(src, "w") as f:
         f.write(source_text)
     subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c99", src, "-o", out, "-lm"], check=True)

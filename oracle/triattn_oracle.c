@@ -31,7 +31,7 @@
  *     dK[k,:] = sum_q dS[q,k] Q[q,:] / sqrt(D)
  *     dbias[b,h,q,k] = sum_o dS_o[q,k]           (the cross-slice reduction)
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - the 1/sqrt(D) scale multiplies Q.K only;
  *   - the mask is additive, per (b, o, key), broadcast over queries and heads,
  *     and carries no gradient;

@@ -41,13 +41,16 @@ triattn_status init_device(int* dev_out) {
       return TRIATTN_ERR_CUDA;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  if (g_init_mask & (1ull << dev)) return TRIATTN_OK;
+  // The device address of the status word is looked up on every call (it is
+  // cheap): after a device reset the module is loaded again and a cached
+  // address would be stale.
+  void* sp = nullptr;
+  if (cudaGetSymbolAddress(&sp, g_status_word) != cudaSuccess || sp == nullptr) return TRIATTN_ERR_CUDA;
+  g_status_ptr[dev] = static_cast<uint32_t*>(sp);
+  if ((g_init_mask & (1ull << dev)) && fwd_attrs_current()) return TRIATTN_OK;
   if (setup_fwd<16>() != cudaSuccess || setup_fwd<32>() != cudaSuccess || setup_bwd<16>() != cudaSuccess ||
       setup_bwd<32>() != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  void* sp = nullptr;
-  if (cudaGetSymbolAddress(&sp, g_status_word) != cudaSuccess) return TRIATTN_ERR_CUDA;
-  g_status_ptr[dev] = static_cast<uint32_t*>(sp);
   g_init_mask |= (1ull << dev);
   return TRIATTN_OK;
 }
@@ -193,8 +196,8 @@ using namespace triattn;
 
 namespace {
 
-// The backward: atomic_mask 0 is the library's ordered path; 2 and 3 are the
-// non-deterministic ablation (FP32 atomics for dbias, and for dQ).
+// The backward: atomic_mask 0 is the library's ordered path; 1, 2 and 3 are
+// the non-deterministic ablation (FP32 atomics for dQ, dbias, or both).
 triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k, const void* v, const void* bias,
                         const void* mask, const void* o, const void* o_resid, const float* lse, const void* dO,
                         void* dq, void* dk, void* dv, void* dbias, int atomic_mask, void* workspace,
@@ -321,7 +324,7 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
 }
 
 size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask) {
-  if (check_shape(shape) != TRIATTN_OK || (atomic_mask != 2 && atomic_mask != 3)) return 0;
+  if (check_shape(shape) != TRIATTN_OK || atomic_mask < 1 || atomic_mask > 3) return 0;
   return ws_layout(shape, atomic_mask).total;
 }
 
@@ -330,7 +333,7 @@ triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape, const vo
                                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
                                             void* dbias, int atomic_mask, void* workspace, size_t workspace_bytes,
                                             void* stream) {
-  if (atomic_mask != 2 && atomic_mask != 3) return TRIATTN_ERR_INVALID_ARG;
+  if (atomic_mask < 1 || atomic_mask > 3) return TRIATTN_ERR_INVALID_ARG;
   if (shape != nullptr && shape->flags != 0) return TRIATTN_ERR_INVALID_ARG;
   return bwd_impl(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, atomic_mask, workspace,
                   workspace_bytes, stream);

@@ -37,10 +37,11 @@ constexpr int kRecTile = BM * kRecRow;  // bytes per (slice, query tile)
 constexpr int NQ = 3;
 
 // ---------------------------------------------------------------- preprocess
-// One record of 2 x 128 FP32 per (slice, query tile), padded to whole tiles:
-//   [0, 128)    -lse[q] log2 e      (-inf for fully masked rows and q >= N)
-//   [128, 256)  -delta[q],  delta[q] = sum_d dO[q,d] (O[q,d] + E[q,d])
-//               (E omitted when null; 0 for q >= N).
+// One 16-byte record per query row (rows padded to whole 128-row tiles):
+// BF16 [x0 x1 x2 0 y0 y1 y2 0] with x0 + x1 + x2 = -lse[q] sqrt(D) (x0 = -1e30
+// for a fully masked row and for q >= N) and y0 + y1 + y2 = -delta[q],
+// delta[q] = sum_d dO[q,d] (O[q,d] + E[q,d]) in FP32 (E omitted when null;
+// 0 for q >= N).
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restrict__ dO,
                                                          const uint16_t* __restrict__ o,
@@ -890,6 +891,8 @@ cudaError_t setup_bwd() {
   cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BwdSmem<D>::kBytes);
   if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_main_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
+  if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bwd_main_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bwd_main_kernel<D, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
@@ -931,6 +934,7 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
 
 template <int D>
 cudaError_t launch_bwd_main_atomic(const BwdArgs& a, int atomic_mask, cudaStream_t stream) {
+  if (atomic_mask == 1) return launch_main_variant<D, 1>(a, stream);
   if (atomic_mask == 2) return launch_main_variant<D, 2>(a, stream);
   if (atomic_mask == 3) return launch_main_variant<D, 3>(a, stream);
   return cudaErrorInvalidValue;

@@ -527,6 +527,13 @@ cudaError_t setup_fwd() {
   return cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
 }
 
+bool fwd_attrs_current() {
+  // The attribute set by setup_fwd is lost with the context (a device
+  // reset); the library then sets every attribute again.
+  cudaFuncAttributes fa;
+  return cudaFuncGetAttributes(&fa, fwd_kernel<32>) == cudaSuccess && fa.maxDynamicSharedSizeBytes >= 232448;
+}
+
 template cudaError_t launch_fwd<16>(const FwdArgs&, cudaStream_t);
 template cudaError_t launch_fwd<32>(const FwdArgs&, cudaStream_t);
 template cudaError_t setup_fwd<16>();

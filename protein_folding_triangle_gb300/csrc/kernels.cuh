@@ -10,7 +10,8 @@
 
 namespace triattn {
 
-// Tile shape shared by all kernels: 128 query rows x 128 keys.
+// Backward tile: 128 query rows x 128 keys (the forward steps over 64-key
+// tiles of 128 query rows, see fwd.cu).
 constexpr int kTileQ = 128;
 constexpr int kTileK = 128;
 // Outer slices per CTA: forward (shared bias tile) and backward (outer group
@@ -53,6 +54,8 @@ struct BwdArgs {
 };
 
 template <int D> cudaError_t setup_fwd();
+// false once the context that setup_fwd configured is gone (a device reset)
+bool fwd_attrs_current();
 template <int D> cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 template <int D> int fwd_smem_bytes(int N);
 
@@ -64,7 +67,7 @@ template <int D> cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t
 cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream);
 template <int D> int bwd_smem_bytes();
 // Non-deterministic ablation of the backward (FP32 atomics; never used by
-// tri_attn_bwd): atomic_mask 2 = dbias, 3 = dbias and dQ.
+// tri_attn_bwd): atomic_mask 1 = dQ, 2 = dbias, 3 = dbias and dQ.
 template <int D> cudaError_t launch_bwd_main_atomic(const BwdArgs& a, int atomic_mask, cudaStream_t stream);
 template <int D> cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_finish_dbias(const BwdArgs& a, cudaStream_t stream);

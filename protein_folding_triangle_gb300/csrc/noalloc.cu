@@ -1,11 +1,11 @@
-// Allocation-free entry point of the backward: the same four kernels as
-// tri_attn_bwd, with their scratch memory in a file-scope device array
-// instead of a caller-provided workspace.  Declared in include/triattn.h.
+// Allocation-free entry point of the backward: the same five kernels as
+// tri_attn_bwd (preprocess, bias transpose, main, dQ reduce, dbias reduce),
+// with their scratch memory in a file-scope device array instead of a
+// caller-provided workspace.  Declared in include/triattn.h.
 #include <cuda_runtime.h>
 
 #include <cstddef>
 #include <cstdint>
-#include <mutex>
 
 #include "triattn.h"
 
@@ -16,9 +16,6 @@ constexpr size_t kScratchBytes = TRIATTN_NOALLOC_SCRATCH_BYTES;
 // The scratch array.  In host code this name is only a host-side stand-in;
 // its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
-
-std::mutex g_mu;
-void* g_scratch_dev[64] = {};  // device address of g_noalloc_scratch, per device
 
 }  // namespace
 
@@ -32,19 +29,11 @@ extern "C" triattn_status tri_attn_bwd_noalloc(const triattn_shape* shape, const
     return tri_attn_bwd(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, nullptr, 0, stream);
   }
   if (need > kScratchBytes) return TRIATTN_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TRIATTN_ERR_CUDA;
+  // The array's device address on the current device, looked up on every
+  // call: the lookup allocates nothing and is cheap, and an address kept
+  // from an earlier call would be stale after a device reset.
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_scratch_dev[dev] == nullptr) {
-      // one-time set-up on this device (the device is current here)
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return TRIATTN_ERR_CUDA;
-      g_scratch_dev[dev] = p;
-    }
-    scratch = g_scratch_dev[dev];
-  }
+  if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr) return TRIATTN_ERR_CUDA;
   return tri_attn_bwd(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, scratch, kScratchBytes,
                       stream);
 }

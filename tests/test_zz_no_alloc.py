@@ -5,16 +5,18 @@ owns all device memory, or a loop that cannot pay for cudaMalloc's implicit
 synchronisation).  For them the library offers a backward that takes no
 workspace and keeps its scratch in a fixed 64 MiB device array of its own.
 This test calls it through the C ABI twice in a row and checks each result
-against the regular workspace entry point, within the gradient tolerance
-the parity tests use.  It sits in a file of its own that pytest collects
-last, so a run that stops at its first failure has run everything else.
+against the regular workspace entry point.  Both run the same kernels on the
+same inputs and the backward is deterministic, so the results must be equal
+bit for bit; stale scratch contents left by the previous call would show.
+It sits in a file of its own that pytest collects last, so a run that stops
+at its first failure has run everything else.
 """
 import ctypes
 
 import pytest
 import torch
 
-from parity_utils import TOL_GRAD, cpu64, rel_rmse, to_dev
+from parity_utils import cpu64, rel_rmse, to_dev
 from protein_folding_triangle_gb300 import synthetic as S
 from protein_folding_triangle_gb300 import triattn as T
 
@@ -59,8 +61,7 @@ def test_noalloc_matches_workspace_entry_point(lib, wname):
         torch.cuda.synchronize()
         assert T.device_status() == T.OK
         for name, g, r in zip(("dq", "dk", "dv", "dbias"), got, ref):
-            err = rel_rmse(cpu64(g), cpu64(r))
-            assert err <= TOL_GRAD, (call, name, err)
+            assert torch.equal(g, r), (call, name, rel_rmse(cpu64(g), cpu64(r)))
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):

@@ -23,11 +23,16 @@
  *             lse                                 [B, N_o, H, N]    fp32 (natural log)
  *  - The method has N_o = N outer slices (Table 1); a call may also take a
  *    contiguous shard of them (one GPU's part when the outer axis is split
- *    across GPUs): 8 <= N_o <= N with N_o a multiple of 8.  D must be 16 or
- *    32, and N a multiple of 8 with 8 <= N <= 4096 (TMA needs 16-byte row
- *    strides of the [N, N] bias; the forward stages the key mask of every
- *    key tile in shared memory).  Any N in that set works, ragged or not
- *    relative to the 128-row tiles.
+ *    across GPUs): 1 <= N_o <= N.  D must be 16 or 32; any N >= 1 works,
+ *    ragged or not relative to the tiles, up to the grid and 32-bit index
+ *    limits (ceil(N_o / 4) <= 65535, B*H <= 65535, B*(N_o + 4)*H < 2^31,
+ *    N * ceil(N / 128) * 128 < 2^31; beyond them TRIATTN_ERR_UNSUPPORTED).
+ *    When N is not a multiple of 8, the forward reads the bias from a copy
+ *    with rows padded to 16 bytes in its workspace, and the backward's
+ *    transposed copy is padded the same way.  The backward's FP32 partials
+ *    grow as N_o * N^2 (triattn_bwd_workspace_bytes); for long crops run the
+ *    outer axis in chunks with TRIATTN_FLAG_DBIAS_FP32 and combine them with
+ *    tri_attn_dbias_combine.
  *  - A row whose keys are all masked (every score -inf) yields O = 0,
  *    residual 0, lse = -inf and zero gradient contributions.
  *  - The caller owns every buffer, the workspace and the stream.  The library
@@ -54,7 +59,7 @@ extern "C" {
 
 typedef struct {
   int B;          /* examples */
-  int N_o;        /* outer slices: N, or a shard (multiple of 8, <= N) */
+  int N_o;        /* outer slices: N, or a contiguous shard of them (1 <= N_o <= N) */
   int N;          /* tokens per crop (queries = keys = N) */
   int H;          /* heads */
   int D;          /* features per head: 16 or 32 */
@@ -84,6 +89,14 @@ typedef enum {
 const char* triattn_status_string(triattn_status s);
 
 /*
+ * Workspace bytes tri_attn_fwd may need for `shape` (0 on an invalid shape,
+ * and 0 when no call of that shape needs one): the key-mask records, one of
+ * 144 bytes per (slice, 64-key tile) plus four padding slices, and, when N
+ * is not a multiple of 8, the bias copied with 16-byte aligned rows.
+ */
+size_t triattn_fwd_workspace_bytes(const triattn_shape* shape);
+
+/*
  * Forward.  "TurboPairFormer", Abstract and Figure 1(a) (the operation),
  * Figure 7(b) and Figure 9 (the saved output residual).
  *
@@ -94,12 +107,18 @@ const char* triattn_status_string(triattn_status s);
  *           approximation of what rounding O to BF16 lost.  The backward uses
  *           o + o_resid for its softmax correction.
  *   mask    optional (NULL = no mask).
- * Launches one kernel.
+ *   workspace  device scratch of triattn_fwd_workspace_bytes(shape) bytes,
+ *           256-byte aligned, contents ignored.  It may be NULL (with 0
+ *           bytes) when mask is NULL and N is a multiple of 64: the forward
+ *           then needs none.
+ * Launches the forward kernel, preceded (when the workspace is used) by one
+ * small kernel that writes the key-mask records and the padded bias.
  */
 triattn_status tri_attn_fwd(const triattn_shape* shape,
                             const void* q, const void* k, const void* v,
                             const void* bias, const void* mask,
                             void* o, float* lse, void* o_resid,
+                            void* workspace, size_t workspace_bytes,
                             void* stream);
 
 /*

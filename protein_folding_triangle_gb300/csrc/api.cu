@@ -60,19 +60,22 @@ triattn_status check_shape(const triattn_shape* s) {
   if (s->B < 1 || s->N < 1 || s->N_o < 1 || s->H < 1 || (s->flags & ~TRIATTN_FLAG_DBIAS_FP32) != 0)
     return TRIATTN_ERR_INVALID_ARG;
   if (s->D != 16 && s->D != 32) return TRIATTN_ERR_UNSUPPORTED;
-  // N outer slices, or a shard of them: whole groups of 8 (both backward
-  // group sizes divide it)
-  if (s->N_o > s->N || s->N_o % 8 != 0) return TRIATTN_ERR_UNSUPPORTED;
-  // TMA row strides of the [N, N] bias must be multiples of 16 bytes.
-  if (s->N % 8 != 0) return TRIATTN_ERR_UNSUPPORTED;
-  // grid limits: outer groups in gridDim.y, B*H in gridDim.z
-  if (s->N_o / kGroupFwd > 65535 || static_cast<long long>(s->B) * s->H > 65535) return TRIATTN_ERR_UNSUPPORTED;
-  // the forward stages the key mask of all key tiles in shared memory
-  if (s->N > 4096) return TRIATTN_ERR_UNSUPPORTED;
-  // TMA outer dimension B*N_o*H (slices) must fit in 32 bits
-  if (static_cast<long long>(s->B) * s->N_o * s->H >= (1ll << 31)) return TRIATTN_ERR_UNSUPPORTED;
+  // N outer slices, or a contiguous shard of them
+  if (s->N_o > s->N) return TRIATTN_ERR_UNSUPPORTED;
+  // grid limits: query / key tiles in gridDim.x, outer groups in gridDim.y,
+  // B*H in gridDim.z
+  if ((s->N_o + kGroupFwd - 1) / kGroupFwd > 65535 || static_cast<long long>(s->B) * s->H > 65535)
+    return TRIATTN_ERR_UNSUPPORTED;
+  // TMA outer dimension B*N_o*H (slices) and the [B*H, N, N] planes must fit
+  // the 32-bit index arithmetic of the kernels
+  if (static_cast<long long>(s->B) * (s->N_o + kGroupFwd) * s->H >= (1ll << 31)) return TRIATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(s->N) * ((s->N + 127) / 128 * 128) >= (1ll << 31)) return TRIATTN_ERR_UNSUPPORTED;
   return TRIATTN_OK;
 }
+
+// Row stride (elements) of the bias as the kernels read it: N, or N rounded up
+// to a multiple of 8 for the padded copy (TMA needs 16-byte row strides).
+int padded_n(int N) { return (N + 7) / 8 * 8; }
 
 // 3-D map over a [slices, N, D] bf16 tensor, box = box_rows rows x D.
 bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s, unsigned box_rows = 128) {
@@ -87,12 +90,13 @@ bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s, uns
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over a [B*H, N, N] bf16 matrix (the bias, or its transposed copy),
-// box = 128 rows x 64 columns.
-bool make_bias_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
+// 3-D map over a [B*H, N, ld] bf16 matrix (the bias, its padded copy or its
+// transposed copy; ld a multiple of 8), box = 128 rows x 64 columns; columns
+// N .. ld-1 are outside the map (zero fill).
+bool make_bias_map(CUtensorMap* m, const void* base, const triattn_shape* s, int ld) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->N), static_cast<cuuint64_t>(s->N),
                               static_cast<cuuint64_t>(s->B) * s->H};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s->N) * 2, static_cast<cuuint64_t>(s->N) * s->N * 2};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(ld) * s->N * 2};
   const cuuint32_t box[3] = {64u, 128u, 1u};
   const cuuint32_t es[3] = {1u, 1u, 1u};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -101,6 +105,23 @@ bool make_bias_map(CUtensorMap* m, const void* base, const triattn_shape* s) {
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Forward workspace: key-mask records [(B*N_o + 4) * J_K] (needed with a mask
+// or when N is not a multiple of 64), then the padded bias [B*H, N, Np] (when
+// N is not a multiple of 8); each part 256-byte aligned.
+struct FwdWs {
+  size_t rec_bytes, pad_off, pad_bytes;
+  size_t total() const { return pad_off + pad_bytes; }
+};
+FwdWs fwd_ws(const triattn_shape* s, bool with_mask) {
+  FwdWs w;
+  const size_t jk = (s->N + 63) / 64;
+  const bool need_rec = with_mask || s->N % 64 != 0;
+  w.rec_bytes = need_rec ? round_up((static_cast<size_t>(s->B) * s->N_o + kGroupFwd) * jk * kFwdMaskRec, 256) : 0;
+  w.pad_off = w.rec_bytes;
+  w.pad_bytes = s->N % 8 != 0 ? round_up(static_cast<size_t>(s->B) * s->H * s->N * padded_n(s->N) * 2, 256) : 0;
+  return w;
+}
 
 struct WsLayout {
   size_t rec_off, biasT_off, dq_off, db_off, total;
@@ -115,11 +136,11 @@ WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
   const size_t slices = static_cast<size_t>(s->B) * s->N_o * s->H;
   const size_t jk = (s->N + kTileK - 1) / kTileK;
   const size_t jq = (s->N + kTileQ - 1) / kTileQ;
-  const size_t groups = s->N_o / kGroupBwdFor(s->D);
+  const size_t groups = (s->N_o + kGroupBwdFor(s->D) - 1) / kGroupBwdFor(s->D);
   WsLayout w;
   w.rec_off = 0;
   w.biasT_off = round_up(slices * jq * kTileQ * 16, 256);
-  w.dq_off = w.biasT_off + round_up(static_cast<size_t>(s->B) * s->H * s->N * s->N * 2, 256);
+  w.dq_off = w.biasT_off + round_up(static_cast<size_t>(s->B) * s->H * s->N * padded_n(s->N) * 2, 256);
   // ablation: FP32 accumulators instead of the partials (see tri_attn_bwd_atomic_ablation)
   const size_t dq_bytes = (atomic_mask & 1) ? slices * jq * kTileQ * s->D * 4 : jk * slices * jq * kTileQ * s->D * 4;
   const size_t db_bytes = (atomic_mask & 2) ? static_cast<size_t>(s->B) * s->H * jk * kTileK * jq * kTileQ * 4
@@ -133,7 +154,7 @@ WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
 const char* const kKernelName[kKinds] = {"tri_attn_fwd",     "bwd_preprocess",  "bwd_transpose_bias",
                                          "bwd_main",         "bwd_reduce_dq",   "bwd_reduce_dbias",
                                          "bwd_main_atomic",  "bwd_finish_dq",   "bwd_finish_dbias",
-                                         "dbias_combine",    "module_ln_fwd",   "module_layout",
+                                         "dbias_combine",    "fwd_prep",        "module_ln_fwd",   "module_layout",
                                          "module_gemm",      "module_ln_bwd",   "module_colsum",
                                          "trimul_ln_in",     "trimul_proj_gemm", "trimul_gate",
                                          "trimul_contract_gemm", "trimul_ln_out", "trimul_out_gate",
@@ -218,7 +239,7 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.biasT = ws + w.biasT_off;
   if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
-      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_biasT, a.biasT, shape))
+      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_biasT, a.biasT, shape, padded_n(shape->N)))
     return TRIATTN_ERR_CUDA;
   a.bias = bias;
   a.mask = mask;
@@ -284,20 +305,36 @@ size_t triattn_bwd_workspace_bytes(const triattn_shape* shape) {
   return ws_layout(shape).total;
 }
 
+size_t triattn_fwd_workspace_bytes(const triattn_shape* shape) {
+  if (check_shape(shape) != TRIATTN_OK) return 0;
+  return fwd_ws(shape, true).total();
+}
+
 triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const void* k, const void* v,
-                            const void* bias, const void* mask, void* o, float* lse, void* o_resid, void* stream) {
+                            const void* bias, const void* mask, void* o, float* lse, void* o_resid,
+                            void* workspace, size_t workspace_bytes, void* stream) {
   triattn_status st = check_shape(shape);
   if (st != TRIATTN_OK) return st;
   const void* req[] = {q, k, v, bias, o, lse};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
   if ((mask && !aligned16(mask)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
+  const FwdWs fw = fwd_ws(shape, mask != nullptr);
+  if (fw.total() > 0 &&
+      (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < fw.total()))
+    return TRIATTN_ERR_WORKSPACE;
   int dev = 0;
   if ((st = init_device(&dev)) != TRIATTN_OK) return st;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.mrec = fw.rec_bytes > 0 ? ws : nullptr;
+  a.bias_padded = fw.pad_bytes > 0 ? ws + fw.pad_off : nullptr;
+  a.bias = bias;
+  const void* bias_read = a.bias_padded != nullptr ? a.bias_padded : bias;
   if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape, 64) ||
-      !make_rows_map(&a.tm_v, v, shape, 64) || !make_bias_map(&a.tm_bias, bias, shape))
+      !make_rows_map(&a.tm_v, v, shape, 64) ||
+      !make_bias_map(&a.tm_bias, bias_read, shape, a.bias_padded != nullptr ? padded_n(shape->N) : shape->N))
     return TRIATTN_ERR_CUDA;
   a.mask = mask;
   a.o = o;
@@ -310,8 +347,10 @@ triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const voi
   a.test_starve = g_test_starve.load();
   a.wc = wait_ctl(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e =
-      traced(kKFwd, s, [&] { return (shape->D == 32) ? launch_fwd<32>(a, s) : launch_fwd<16>(a, s); });
+  cudaError_t e = cudaSuccess;
+  if (a.mrec != nullptr || a.bias_padded != nullptr) e = traced(kKFwdPrep, s, [&] { return launch_fwd_prep(a, s); });
+  if (e == cudaSuccess)
+    e = traced(kKFwd, s, [&] { return (shape->D == 32) ? launch_fwd<32>(a, s) : launch_fwd<16>(a, s); });
   return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
 }
 
@@ -343,7 +382,7 @@ triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* p
                                       void* stream) {
   if (shape == nullptr || R < 1 || parts == nullptr || dbias == nullptr || !aligned16(parts) || !aligned16(dbias))
     return TRIATTN_ERR_INVALID_ARG;
-  if (shape->B < 1 || shape->H < 1 || shape->N < 1 || shape->N % 8 != 0) return TRIATTN_ERR_INVALID_ARG;
+  if (shape->B < 1 || shape->H < 1 || shape->N < 1) return TRIATTN_ERR_INVALID_ARG;
   int dev = 0;
   triattn_status st = init_device(&dev);
   if (st != TRIATTN_OK) return st;

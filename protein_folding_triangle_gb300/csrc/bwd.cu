@@ -96,30 +96,46 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
   rec[pr] = w;
 }
 
-// biasT[bh][k][q] = bias[bh][q][k]: 64 x 64 tiles through shared memory (N is
-// a multiple of 8, so an 8-element group is all inside or all outside).
+// biasT[bh][k][q] = bias[bh][q][k]: 64 x 64 tiles through shared memory.
+// biasT rows have Np = N rounded up to a multiple of 8 elements (16-byte
+// strides for TMA); columns q >= N of a row are written as zeros.  When N is
+// a multiple of 8 an 8-element group of a bias row is all inside or all
+// outside and moves as one 16-byte load; otherwise elements are read one by
+// one (bias rows are then not 16-byte aligned).
 __global__ void __launch_bounds__(256) transpose_bias_kernel(const uint16_t* __restrict__ bias,
-                                                             uint16_t* __restrict__ biasT, int N) {
+                                                             uint16_t* __restrict__ biasT, int N, int Np) {
   __shared__ __align__(16) uint16_t tile[64][72];
   const int q0 = blockIdx.y * 64, k0 = blockIdx.x * 64;
   const size_t base = static_cast<size_t>(blockIdx.z) * N * N;
+  const size_t baseT = static_cast<size_t>(blockIdx.z) * N * Np;
+  const bool vec = (N & 7) == 0;
   for (int e = threadIdx.x; e < 64 * 8; e += blockDim.x) {
     const int rr = e >> 3, c8 = e & 7;
     const int q = q0 + rr, k = k0 + 8 * c8;
     uint4 w = make_uint4(0, 0, 0, 0);
-    if (q < N && k < N) w = __ldg(reinterpret_cast<const uint4*>(bias + base + static_cast<size_t>(q) * N + k));
+    if (q < N && k < N) {
+      const uint16_t* src = bias + base + static_cast<size_t>(q) * N + k;
+      if (vec) {
+        w = __ldg(reinterpret_cast<const uint4*>(src));
+      } else {
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = k + j < N ? __ldg(src + j) : 0u;
+        w = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+      }
+    }
     *reinterpret_cast<uint4*>(&tile[rr][8 * c8]) = w;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < 64 * 8; e += blockDim.x) {
     const int rr = e >> 3, c8 = e & 7;
     const int k = k0 + rr, q = q0 + 8 * c8;
-    if (k >= N || q >= N) continue;
+    if (k >= N || q >= Np) continue;
     uint32_t w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       w[j] = static_cast<uint32_t>(tile[8 * c8 + 2 * j][rr]) | (static_cast<uint32_t>(tile[8 * c8 + 2 * j + 1][rr]) << 16);
-    *reinterpret_cast<uint4*>(biasT + base + static_cast<size_t>(k) * N + q) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(biasT + baseT + static_cast<size_t>(k) * Np + q) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -228,6 +244,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int h = bh - b * H;
   const int JQ = (N + BM - 1) / BM;
   const int nsteps = JQ * G;
+  // The last group may extend past N_o: its extra slices see every key
+  // masked (P = 0, so they add nothing), their records are read from the
+  // last real slice, and nothing of theirs is stored.
+  const int last_rec_slice = (static_cast<int>(gridDim.z) / H) * N_o * H - 1;
 
   // The swizzled tiles below need a 1024-byte aligned base.
   if ((smem_u32(sm) & 1023u) != 0) {
@@ -287,6 +307,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tc_fence_after();
     const int ti = t / G, tg = t % G;
     const int r = (warp & 3) * 32 + lane;
+    const bool live = o0 + tg < N_o;
     const size_t slice = static_cast<size_t>((b * N_o + o0 + tg) * H + h);
     const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
     float* out = dq_part + ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D) + r * 8;
@@ -295,7 +316,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     uint32_t qr[D];
     if constexpr (D == 32) tmem_ld32_wait(taddr, qr);
     else tmem_ld16_wait(taddr, qr);
-    if constexpr ((kAtomic & 1) != 0) {
+    if (!live) {
+      // a padded slice of the last group: nothing to store
+    } else if constexpr ((kAtomic & 1) != 0) {
       float* acc = dq_part + ((slice * JQ + ti) * BM + r) * D;
 #pragma unroll
       for (int c = 0; c < D / 4; ++c)
@@ -372,8 +395,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         mbar_expect_tx(&bars->qdo_full[st], 2 * L::kTile + kRecTile);
         tma_load_3d(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], 0, i * BM, boh);
         tma_load_3d(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], 0, i * BM, boh);
-        bulk_load(sm + L::kRec + st * kRecTile, rec + (static_cast<size_t>(boh) * JQ + i) * BM, kRecTile,
-                  &bars->qdo_full[st]);
+        bulk_load(sm + L::kRec + st * kRecTile, rec + (static_cast<size_t>(min(boh, last_rec_slice)) * JQ + i) * BM,
+                  kRecTile, &bars->qdo_full[st]);
       }
       __syncwarp();
       if (s >= 2) ok = drain_dq(s - 2);
@@ -538,7 +561,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     float* mask_s = reinterpret_cast<float*>(sm + L::kMask);
     for (int gg = wg; gg < G; gg += kNWG) {
       float mv = -INFINITY;
-      if (key < N) {
+      if (key < N && o0 + gg < N_o) {
         mv = 0.f;
         if (mask != nullptr)
           mv = __uint_as_float(static_cast<uint32_t>(__ldg(mask + (static_cast<size_t>(b) * N_o + o0 + gg) * N + key))
@@ -691,7 +714,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           for (int e = 0; e < 8; ++e)
             w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]) * sc, __uint_as_float(raw[2 * e + 1]) * sc);
         }
-        if (key < N) {
+        if (key < N && o0 + g < N_o) {
           uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + row * D);
 #pragma unroll
           for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
@@ -813,28 +836,47 @@ __global__ void __launch_bounds__(kRedThreads) reduce_dbias_kernel(const float4*
   __syncthreads();
   constexpr int kPer = 16 / sizeof(OutT);  // elements per 16-byte item
   constexpr int kItems = kSlab * BN / kPer;
+  const bool vec = N % kPer == 0;          // rows 16-byte aligned, an item all in or all out
   for (int e = threadIdx.x; e < kItems; e += blockDim.x) {
     const int rr = e / (BN / kPer), c = e % (BN / kPer);
     const int q = i * BM + slab * kSlab + rr, k = kt * BN + kPer * c;
-    if (q >= N || k >= N) continue;        // N is a multiple of 8: an item is all in or all out
-    *reinterpret_cast<uint4*>(dbias + (bh * N + q) * N + k) = *reinterpret_cast<const uint4*>(&tile[rr * kStride + kPer * c]);
+    if (q >= N || k >= N) continue;
+    OutT* dst = dbias + (bh * N + q) * N + k;
+    const OutT* src = &tile[rr * kStride + kPer * c];
+    if (vec) {
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    } else {
+      for (int u = 0; u < kPer && k + u < N; ++u) dst[u] = src[u];
+    }
   }
 }
 
-// dbias = bf16(sum_r parts[r]) in ascending r, four elements per thread.
-__global__ void __launch_bounds__(256) dbias_combine_kernel(const float4* __restrict__ parts, int R, size_t n4,
-                                                            uint2* __restrict__ dbias) {
-  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4;
-       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    float4 acc = __ldcs(parts + e);
-    for (int r = 1; r < R; ++r) {
-      const float4 v = __ldcs(parts + static_cast<size_t>(r) * n4 + e);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+// dbias = bf16(sum_r parts[r]) in ascending r: four elements per thread when
+// every part starts 16-byte aligned (elems a multiple of 4), else one.
+__global__ void __launch_bounds__(256) dbias_combine_kernel(const float* __restrict__ parts, int R, size_t elems,
+                                                            uint16_t* __restrict__ dbias) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const size_t t0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (elems % 4 == 0) {
+    const float4* p4 = reinterpret_cast<const float4*>(parts);
+    const size_t n4 = elems / 4;
+    for (size_t e = t0; e < n4; e += stride) {
+      float4 acc = __ldcs(p4 + e);
+      for (int r = 1; r < R; ++r) {
+        const float4 v = __ldcs(p4 + static_cast<size_t>(r) * n4 + e);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      reinterpret_cast<uint2*>(dbias)[e] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
     }
-    dbias[e] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  } else {
+    for (size_t e = t0; e < elems; e += stride) {
+      float acc = parts[e];
+      for (int r = 1; r < R; ++r) acc += parts[static_cast<size_t>(r) * elems + e];
+      dbias[e] = static_cast<uint16_t>(pack_bf16x2(acc, 0.f) & 0xFFFFu);
+    }
   }
 }
 
@@ -875,9 +917,15 @@ __global__ void __launch_bounds__(256) finish_dbias_kernel(const float* __restri
   for (int e = threadIdx.x; e < 64 * 32; e += blockDim.x) {
     const int qq = e / 32, kp = e % 32;
     const int q = q0 + qq, k = k0 + 2 * kp;
-    if (q >= N || k >= N) continue;  // N is even: k + 1 < N too
-    *reinterpret_cast<uint32_t*>(dbias + (static_cast<size_t>(blockIdx.z) * N + q) * N + k) =
-        pack_bf16x2(tile[2 * kp][qq], tile[2 * kp + 1][qq]);
+    if (q >= N || k >= N) continue;
+    uint16_t* dst = dbias + (static_cast<size_t>(blockIdx.z) * N + q) * N + k;
+    const uint32_t w = pack_bf16x2(tile[2 * kp][qq], tile[2 * kp + 1][qq]);
+    if ((N & 1) == 0) {
+      *reinterpret_cast<uint32_t*>(dst) = w;  // even N: 4-byte aligned, k + 1 < N
+    } else {
+      dst[0] = static_cast<uint16_t>(w & 0xFFFFu);
+      if (k + 1 < N) dst[1] = static_cast<uint16_t>(w >> 16);
+    }
   }
 }
 
@@ -913,14 +961,15 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_bwd_transpose_bias(const BwdArgs& a, cudaStream_t stream) {
   const unsigned t = static_cast<unsigned>((a.N + 63) / 64);
   transpose_bias_kernel<<<dim3(t, t, a.B * a.H), 256, 0, stream>>>(static_cast<const uint16_t*>(a.bias),
-                                                                   static_cast<uint16_t*>(a.biasT), a.N);
+                                                                   static_cast<uint16_t*>(a.biasT), a.N,
+                                                                   (a.N + 7) / 8 * 8);
   return cudaGetLastError();
 }
 
 template <int D, int kAtomic>
 cudaError_t launch_main_variant(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
-  dim3 grid(JK, a.N_o / BwdSmem<D>::G, a.B * a.H);
+  dim3 grid(JK, (a.N_o + BwdSmem<D>::G - 1) / BwdSmem<D>::G, a.B * a.H);
   bwd_main_kernel<D, kAtomic><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
@@ -971,22 +1020,21 @@ cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
   const size_t tiles = static_cast<size_t>(a.B) * a.H * JQ * JK;
   const unsigned blocks = static_cast<unsigned>(tiles * (BM / kSlab));
+  const int groups = (a.N_o + kGroupBwdFor(a.D) - 1) / kGroupBwdFor(a.D);
   if (a.dbias_fp32)
     reduce_dbias_kernel<float><<<blocks, kRedThreads, 0, stream>>>(
-        reinterpret_cast<const float4*>(a.dbias_part), static_cast<float*>(a.dbias), a.N, JQ, JK,
-        a.N_o / kGroupBwdFor(a.D), tiles);
+        reinterpret_cast<const float4*>(a.dbias_part), static_cast<float*>(a.dbias), a.N, JQ, JK, groups, tiles);
   else
     reduce_dbias_kernel<uint16_t><<<blocks, kRedThreads, 0, stream>>>(
-        reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK,
-        a.N_o / kGroupBwdFor(a.D), tiles);
+        reinterpret_cast<const float4*>(a.dbias_part), static_cast<uint16_t*>(a.dbias), a.N, JQ, JK, groups,
+        tiles);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dbias_combine(const float* parts, int R, size_t elems, void* dbias, cudaStream_t stream) {
   const size_t n4 = elems / 4;
-  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
-  dbias_combine_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(parts), R, n4,
-                                                   static_cast<uint2*>(dbias));
+  const unsigned blocks = static_cast<unsigned>(std::max<size_t>(1, std::min<size_t>((n4 + 255) / 256, 152 * 16)));
+  dbias_combine_kernel<<<blocks, 256, 0, stream>>>(parts, R, elems, static_cast<uint16_t*>(dbias));
   return cudaGetLastError();
 }
 

@@ -14,8 +14,8 @@
 //
 // Warp roles (20 warps):
 //   warp 0       TMA producer: the four Q tiles once; per 64-key tile one
-//                bias tile and, per slice, one K and one V tile (rings of
-//                3 / 2 / 2 stages).
+//                bias tile with the four slices' key-mask records of that
+//                tile, and per slice one K and one V tile (rings of 3 stages).
 //   warps 1, 2   tcgen05 MMA issuers (converged warps, one elected lane
 //                issues, descriptors precomputed), for slices {0,2} and
 //                {1,3}: S(j+1) = Q K^T as soon as the warpgroup has loaded
@@ -36,6 +36,17 @@
 //
 // TMEM (512 columns): slice g owns [128g, 128g + 128): scores at +0 (64),
 // P at +64 (32), O at +96 (D).
+//
+// Key mask: a small kernel writes, per (64-key tile, slice), a 144-byte
+// record (the tile's 64 additive mask values in BF16, -inf past N, then a
+// 16-byte header whose first word is nonzero when any value is), tile-major
+// so that the four slices' records of a tile are one bulk copy, loaded with
+// the tile's bias.  Without a mask and with N a multiple of 64 there
+// are no records and no tile is masked.  Nothing depends on N in shared
+// memory, so N is bounded only by the grid and the tensor maps.
+//
+// A group may extend past N_o (N_o not a multiple of 4): its extra slices
+// read records that mask every key, and nothing of theirs is stored.
 #include <type_traits>
 
 #include "kernels.cuh"
@@ -71,12 +82,12 @@ struct FwdSmem {
   static constexpr int kK = kQ + GF * kTileQ;                // GF x NSLOT K tiles
   static constexpr int kV = kK + GF * NSLOT * kTileKV;       // GF x NSLOT V tiles
   static constexpr int kBias = kV + GF * NSLOT * kTileKV;    // NBIAS x [128 q][64 k] bf16, SW128
-  static constexpr int kBar = kBias + NBIAS * BM * BN * 2;
-  static constexpr int kMask = kBar + 1024;  // GF x (JK*64) bf16 key mask, GF x JK x 8 chunk flags, GF x JK tile flags
-  static constexpr int kFixed = kMask + 1024;                // + slack for 1024-byte alignment
+  static constexpr int kRec = kBias + NBIAS * BM * BN * 2;   // NBIAS x GF key-mask records
+  static constexpr int kBar = kRec + NBIAS * GF * kFwdMaskRec;
+  static constexpr int kBytes = kBar + 1024 + 1024;          // + slack for 1024-byte alignment
   static_assert(kBias % 1024 == 0, "bias tiles need 1024-byte alignment");
-  static constexpr int bytes(int JK) { return kFixed + GF * JK * (BN * 2 + BN / 8 + 1); }
-  static constexpr int kMaxJK = (232448 - kFixed) / (GF * (BN * 2 + BN / 8 + 1));
+  static_assert(kFwdMaskRec % 16 == 0 && kRec % 16 == 0, "records are bulk copies");
+  static_assert(kBytes <= 232448, "shared memory budget");
 };
 
 struct FwdBars {
@@ -96,7 +107,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
-               const uint16_t* __restrict__ mask, uint16_t* __restrict__ out_o, float* __restrict__ out_lse,
+               const uint8_t* __restrict__ mrec, uint16_t* __restrict__ out_o, float* __restrict__ out_lse,
                uint16_t* __restrict__ out_resid, int N_o, int N, int H, int test_starve, WaitCtl wc) {
   using L = FwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -113,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / H;
   const int h = bh - b * H;
   const int JK = (N + BN - 1) / BN;
+  const int rec_slices = static_cast<int>(gridDim.z / H) * N_o + GF;  // records per key tile
 
   if (tid == 0) {
     for (int g = 0; g < GF; ++g) {
@@ -159,8 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < JK && !*abort; ++j) {
         const int bst = j % NBIAS;
         if (!mbar_wait(&bars->b_empty[bst], ((j / NBIAS) & 1) ^ 1, wc, abort)) break;
-        mbar_expect_tx(&bars->b_full[bst], BM * BN * 2);
+        mbar_expect_tx(&bars->b_full[bst], BM * BN * 2 + (mrec != nullptr ? GF * kFwdMaskRec : 0));
         tma_load_3d(sm + L::kBias + bst * (BM * BN * 2), &tm_bias, &bars->b_full[bst], j * BN, row0, bh);
+        if (mrec != nullptr)  // the four slices' records of tile j are contiguous
+          bulk_load(sm + L::kRec + bst * (GF * kFwdMaskRec), mrec + (static_cast<size_t>(j) * rec_slices + b * N_o + o0) * kFwdMaskRec,
+                    GF * kFwdMaskRec, &bars->b_full[bst]);
         const int slot = j % NSLOT;
         const uint32_t par = ((j / NSLOT) & 1) ^ 1;
         bool go = true;
@@ -248,44 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax warpgroups
-    const int ew = tid - 128;             // 0..511
     const int g = (warp - 4) >> 2;        // slice of this warpgroup
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;    // query row within the tile (= TMEM lane)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
-    const int nkeys = JK * BN;
-    uint16_t* mask2 = reinterpret_cast<uint16_t*>(sm + L::kMask);  // [GF][nkeys] bf16, -inf past N
-    uint8_t* mflag = sm + L::kMask + GF * nkeys * 2;              // [GF][JK*8]: 8-key chunk has a nonzero value
-    uint8_t* tflag = mflag + GF * JK * (BN / 8);                  // [GF][JK]: tile has a nonzero value
-
-    // Key mask of the four slices and its chunk / tile flags, staged once,
-    // before any bounded wait, so the barriers are always fully entered.
-    for (int idx = ew; idx < GF * nkeys; idx += kSoftmax) {
-      const int gg = idx / nkeys, key = idx - gg * nkeys;
-      uint16_t mv = 0xFF80u;  // -inf
-      if (key < N) {
-        mv = 0;
-        if (mask != nullptr) mv = __ldg(mask + (static_cast<size_t>(b) * N_o + o0 + gg) * N + key);
-      }
-      mask2[idx] = mv;
-    }
-    named_bar_sync(1, kSoftmax);
-    for (int idx = ew; idx < GF * JK * (BN / 8); idx += kSoftmax) {
-      bool any = false;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) any |= (mask2[idx * 8 + e] & 0x7FFFu) != 0;  // a nonzero value
-      mflag[idx] = any ? 1 : 0;
-    }
-    named_bar_sync(1, kSoftmax);
-    for (int idx = ew; idx < GF * JK; idx += kSoftmax) {
-      bool any = false;
-      for (int e = 0; e < BN / 8; ++e) any |= (mflag[idx * (BN / 8) + e] != 0);
-      tflag[idx] = any ? 1 : 0;
-    }
-    named_bar_sync(1, kSoftmax);
 
     const int q = qtile * BM + r;
+    const bool live_slice = o0 + g < N_o;
+    const bool has_rec = mrec != nullptr;
     const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + q;
 
     // running base m (natural units) and sum l of this row
@@ -324,8 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tiles keep the base and only look at the maximum when the row sum
       // of the tile exceeds 2^16 (some p > 2^16).
       const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
-      const uint16_t* mk = mask2 + (g * nkeys + j * BN);
-      const bool tile_masked = tflag[g * JK + j] != 0;
+      const uint8_t* rec_s = sm + L::kRec + (bst * GF + g) * kFwdMaskRec;
+      const uint16_t* mk = reinterpret_cast<const uint16_t*>(rec_s);  // this tile's 64 mask values
+      const bool tile_masked = has_rec && *reinterpret_cast<const uint32_t*>(rec_s + BN * 2) != 0u;
       const bool exact = j == 0 || __any_sync(0xffffffffu, l_run == 0.f);
       const float2 nb2 = make_float2(-m_run * kLog2e, -m_run * kLog2e);
       float tm = -INFINITY;
@@ -468,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 16; ++e) ov[e] = __uint_as_float(raw[e]);
         }
       }
-      if (q < N) {
+      if (q < N && live_slice) {
         const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
         uint32_t ob[D / 2], eb[D / 2];
 #pragma unroll
@@ -500,18 +487,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Key-mask records of the forward, [J_K][B*N_o + GF] (tile-major): one warp
+// per (64-key tile, slice), lane l covering keys 2l and 2l + 1.  Slices
+// b * N_o + o take the caller's mask (0 without one), -inf past N; the GF
+// slices after the last example's are padding (every key -inf) for a group
+// that extends past N_o.
+__global__ void __launch_bounds__(256) fwd_mask_records_kernel(const uint16_t* __restrict__ mask, uint8_t* __restrict__ rec,
+                                                               int N, int rec_slices, int real_slices, size_t total) {
+  const size_t w = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= total) return;  // whole warps: total is per warp
+  const int j = static_cast<int>(w / rec_slices), slice = static_cast<int>(w % rec_slices);
+  uint32_t word = 0xFF80FF80u;  // two -inf
+  if (slice < real_slices) {
+    uint16_t v[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = j * BN + 2 * lane + e;
+      v[e] = 0xFF80u;
+      if (key < N) v[e] = mask != nullptr ? __ldg(mask + static_cast<size_t>(slice) * N + key) : static_cast<uint16_t>(0);
+    }
+    word = static_cast<uint32_t>(v[0]) | (static_cast<uint32_t>(v[1]) << 16);
+  }
+  uint8_t* r = rec + static_cast<size_t>(w) * kFwdMaskRec;
+  reinterpret_cast<uint32_t*>(r)[lane] = word;
+  const bool nonzero = (word & 0x7FFF7FFFu) != 0u;  // a value other than +-0
+  const unsigned any = __ballot_sync(0xffffffffu, nonzero);
+  if (lane == 0) *reinterpret_cast<uint4*>(r + BN * 2) = make_uint4(any != 0u ? 1u : 0u, 0u, 0u, 0u);
+}
+
+// biasP[bh][q][k] = bias[bh][q][k] for k < N, 0 for N <= k < Np (Np = N rounded
+// up to a multiple of 8), so that TMA can read rows with a 16-byte stride.
+__global__ void __launch_bounds__(256) fwd_pad_bias_kernel(const uint16_t* __restrict__ bias, uint16_t* __restrict__ biasP,
+                                                           int N, int Np, size_t rows) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int chunks = Np / 8;
+  const size_t row = t / chunks;
+  if (row >= rows) return;
+  const int k0 = static_cast<int>(t % chunks) * 8;
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int k = k0 + 2 * e;
+    const uint32_t lo = k < N ? __ldg(bias + row * N + k) : 0u;
+    const uint32_t hi = k + 1 < N ? __ldg(bias + row * N + k + 1) : 0u;
+    w[e] = lo | (hi << 16);
+  }
+  *reinterpret_cast<uint4*>(biasP + row * Np + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+cudaError_t launch_fwd_prep(const FwdArgs& a, cudaStream_t stream) {
+  if (a.mrec != nullptr) {
+    const int JK = (a.N + BN - 1) / BN;
+    const int rec_slices = a.B * a.N_o + GF;
+    const size_t total = static_cast<size_t>(rec_slices) * JK;
+    fwd_mask_records_kernel<<<static_cast<unsigned>((total * 32 + 255) / 256), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a.mask), a.mrec, a.N, rec_slices, a.B * a.N_o, total);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (a.bias_padded != nullptr) {
+    const int Np = (a.N + 7) / 8 * 8;
+    const size_t rows = static_cast<size_t>(a.B) * a.H * a.N;
+    const size_t items = rows * (Np / 8);
+    fwd_pad_bias_kernel<<<static_cast<unsigned>((items + 255) / 256), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a.bias), static_cast<uint16_t*>(a.bias_padded), a.N, Np, rows);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
 template <int D>
-int fwd_smem_bytes(int N) { return FwdSmem<D>::bytes((N + BN - 1) / BN); }
+int fwd_smem_bytes() { return FwdSmem<D>::kBytes; }
 
 template <int D>
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   const int JQ = (a.N + BM - 1) / BM;
-  dim3 grid(JQ, a.N_o / GF, a.B * a.H);
-  const int JK = (a.N + BN - 1) / BN;
-  if (JK > FwdSmem<D>::kMaxJK) return cudaErrorInvalidValue;
-  fwd_kernel<D><<<grid, kThreads, FwdSmem<D>::bytes(JK), stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_bias, static_cast<const uint16_t*>(a.mask),
-      static_cast<uint16_t*>(a.o), a.lse, static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.test_starve, a.wc);
+  dim3 grid(JQ, (a.N_o + GF - 1) / GF, a.B * a.H);
+  fwd_kernel<D><<<grid, kThreads, FwdSmem<D>::kBytes, stream>>>(
+      a.tm_q, a.tm_k, a.tm_v, a.tm_bias, a.mrec, static_cast<uint16_t*>(a.o), a.lse,
+      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.test_starve, a.wc);
   return cudaGetLastError();
 }
 
@@ -538,7 +593,7 @@ template cudaError_t launch_fwd<16>(const FwdArgs&, cudaStream_t);
 template cudaError_t launch_fwd<32>(const FwdArgs&, cudaStream_t);
 template cudaError_t setup_fwd<16>();
 template cudaError_t setup_fwd<32>();
-template int fwd_smem_bytes<16>(int);
-template int fwd_smem_bytes<32>(int);
+template int fwd_smem_bytes<16>();
+template int fwd_smem_bytes<32>();
 
 }  // namespace triattn

@@ -21,9 +21,16 @@ constexpr int kGroupFwd = 4;
 // its 512 columns next to 256 for S^T and dP^T), so G = 8 at D = 16.
 constexpr int kGroupBwdFor(int D) { return D == 16 ? 8 : 4; }
 
+// Forward key-mask record per (slice, 64-key tile): 64 BF16 mask values, then
+// a 16-byte header whose first word is nonzero when any value is.
+constexpr int kFwdMaskRec = 64 * 2 + 16;
+
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_bias;  // Q: 128-row boxes; K, V: 64-row boxes
-  const void* mask;
+  const void* mask;    // [B, N_o, N] or null
+  const void* bias;    // [B*H, N, N]
+  void* bias_padded;   // workspace [B*H, N, Np] (rows padded to a multiple of 8) or null when N % 8 == 0
+  uint8_t* mrec;       // workspace [J_K][B*N_o + 4] records, or null (no mask, N % 64 == 0)
   void* o;
   float* lse;
   void* o_resid;
@@ -57,7 +64,10 @@ template <int D> cudaError_t setup_fwd();
 // false once the context that setup_fwd configured is gone (a device reset)
 bool fwd_attrs_current();
 template <int D> cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
-template <int D> int fwd_smem_bytes(int N);
+// The forward's preparation: key-mask records and the padded bias copy (each
+// only when its workspace pointer is set).
+cudaError_t launch_fwd_prep(const FwdArgs& a, cudaStream_t stream);
+template <int D> int fwd_smem_bytes();
 
 template <int D> cudaError_t setup_bwd();
 template <int D> cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream);
@@ -76,7 +86,7 @@ cudaError_t launch_dbias_combine(const float* parts, int R, size_t elems, void* 
 
 // Kernel kinds of the trace (triattn_trace_enable / triattn_trace_read).
 enum KernelKind {
-  kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine,
+  kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine, kKFwdPrep,
   kKModLnFwd, kKModLayout, kKModGemm, kKModLnBwd, kKModColSum,
   kKTmLnIn, kKTmProj, kKTmGate, kKTmContract, kKTmLnOut, kKTmOutGate, kKTmColSum, kKinds
 };

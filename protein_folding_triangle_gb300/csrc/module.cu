@@ -18,6 +18,7 @@
 #include <cublas_v2.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "kernels.cuh"
@@ -168,7 +169,8 @@ WsLayout2 ws_layout2(const ModDims& d, const triattn_shape& core) {
   w.dx = o;     o += rup(d.M * d.C * 4);
   w.pg = o;     o += rup(static_cast<size_t>(kLnBlocks) * d.C * 4);
   w.pb = o;     o += rup(static_cast<size_t>(kLnBlocks) * d.C * 4);
-  w.core = o;   o += rup(triattn_bwd_workspace_bytes(&core));
+  // the core's forward and backward workspaces (one at a time)
+  w.core = o;   o += rup(std::max(triattn_bwd_workspace_bytes(&core), triattn_fwd_workspace_bytes(&core)));
   w.total = o;
   return w;
 }
@@ -177,6 +179,9 @@ triattn_status check_module(const triattn_module_shape* s, triattn_shape* core) 
   if (s == nullptr || s->flags != 0 || s->B < 1 || s->N < 1 || s->C < 1 || s->H < 1 || s->D < 1)
     return TRIATTN_ERR_INVALID_ARG;
   if (!ln_width_ok(s->C) || s->H > 64) return TRIATTN_ERR_UNSUPPORTED;
+  // the layout kernels move 16-byte groups of pair rows: N a multiple of 8,
+  // up to 4096 tokens
+  if (s->N % 8 != 0 || s->N > 4096) return TRIATTN_ERR_UNSUPPORTED;
   // the projection GEMMs take the pair count as a 32-bit row count
   if (static_cast<size_t>(s->B) * s->N * s->N > 0x7fffffffull) return TRIATTN_ERR_UNSUPPORTED;
   *core = triattn_shape{s->B, s->N, s->N, s->H, s->D, 0u};
@@ -288,7 +293,7 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
     return TRIATTN_ERR_CUDA;
   // the attention core
   st = tri_attn_fwd(&core, cx + c.q, cx + c.k, cx + c.v, cx + c.bias, mask, cx + c.o,
-                    reinterpret_cast<float*>(cx + c.lse), cx + c.resid, stream);
+                    reinterpret_cast<float*>(cx + c.lse), cx + c.resid, ws + w.core, w.total - w.core, stream);
   if (st != TRIATTN_OK) return st;
   // out = o_flat W_o
   const uint16_t* o_core = reinterpret_cast<const uint16_t*>(cx + c.o);

@@ -11,9 +11,10 @@ parts are gathered in rank order, and ``tri_attn_dbias_combine`` adds them in
 ascending rank order and rounds once, so every rank holds the same bits and
 the result does not depend on how the gather was scheduled.
 
-Shards are whole multiples of 8 slices (both backward group sizes divide
-them).  Every compute step runs in the library's kernels; this module only
-splits ranges and moves the FP32 parts.
+Shards are cut at multiples of 8 slices where the axis allows (whole outer
+groups of both backward group sizes), the last rank taking any remainder.
+Every compute step runs in the library's kernels; this module only splits
+ranges and moves the FP32 parts.
 
 The same split also bounds memory on one GPU: ``chunked_tri_attn_bwd`` runs
 the outer axis in chunks whose FP32 partials fit a workspace cap (the
@@ -34,20 +35,23 @@ SHARD_MULTIPLE = 8
 
 
 def outer_shard(n_outer: int, rank: int, world: int, multiple: int = SHARD_MULTIPLE) -> Tuple[int, int]:
-    """Contiguous slice range [lo, hi) of ``rank``: whole blocks of ``multiple``
-    slices, the first ranks taking one block more when they do not divide
-    evenly.  Every rank gets at least one block."""
+    """Contiguous slice range [lo, hi) of ``rank``.  With at least ``multiple``
+    slices per rank the ranges are whole blocks of ``multiple`` slices (the
+    first ranks taking one block more when they do not divide evenly) and the
+    last rank also takes the ``n_outer % multiple`` slices left over; with
+    fewer, the slices are split as evenly as possible.  Every rank gets at
+    least one slice."""
     if world < 1 or not 0 <= rank < world:
         raise ValueError("rank must be in [0, world)")
-    if n_outer % multiple != 0:
-        raise ValueError(f"the outer axis ({n_outer}) must be a multiple of {multiple}")
-    blocks = n_outer // multiple
-    if blocks < world:
-        raise ValueError(f"{n_outer} slices cannot give {world} ranks {multiple} slices each")
+    if n_outer < world:
+        raise ValueError(f"{n_outer} slices cannot give {world} ranks one slice each")
+    unit = multiple if n_outer // multiple >= world else 1
+    blocks = n_outer // unit
     base, extra = divmod(blocks, world)
     lo_blk = rank * base + min(rank, extra)
     hi_blk = lo_blk + base + (1 if rank < extra else 0)
-    return lo_blk * multiple, hi_blk * multiple
+    hi = n_outer if rank == world - 1 else hi_blk * unit
+    return lo_blk * unit, hi
 
 
 def gather_rank_ordered(t: torch.Tensor, group: Optional[dist.ProcessGroup] = None) -> torch.Tensor:
@@ -72,13 +76,11 @@ def sharded_tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *,
 
 
 def chunk_slices(n_outer: int, bytes_for, max_workspace_bytes: int, multiple: int = SHARD_MULTIPLE) -> int:
-    """The largest chunk of outer slices (a multiple of ``multiple``, at most
-    ``n_outer``) whose backward workspace ``bytes_for(chunk)`` fits in
-    ``max_workspace_bytes``; raises if not even one block fits."""
-    if n_outer % multiple != 0:
-        raise ValueError(f"the outer axis ({n_outer}) must be a multiple of {multiple}")
+    """The largest chunk of outer slices -- a multiple of ``multiple`` below
+    ``n_outer``, or ``n_outer`` itself -- whose backward workspace
+    ``bytes_for(chunk)`` fits in ``max_workspace_bytes``; raises if none fits."""
     best = 0
-    for c in range(multiple, n_outer + 1, multiple):
+    for c in list(range(multiple, n_outer, multiple)) + [n_outer]:
         need = bytes_for(c)
         if need == 0:
             raise ValueError(f"unsupported shape for a chunk of {c} slices")
@@ -87,7 +89,8 @@ def chunk_slices(n_outer: int, bytes_for, max_workspace_bytes: int, multiple: in
         else:
             break  # the workspace grows with the chunk
     if best == 0:
-        raise ValueError(f"a chunk of {multiple} slices needs {bytes_for(multiple)} workspace bytes, "
+        first = min(multiple, n_outer)
+        raise ValueError(f"a chunk of {first} slices needs {bytes_for(first)} workspace bytes, "
                          f"more than {max_workspace_bytes}")
     return best
 

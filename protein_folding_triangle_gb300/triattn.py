@@ -30,7 +30,8 @@ STATUS = {
 }
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 
-EXPORTED = ("triattn_status_string", "triattn_bwd_workspace_bytes", "tri_attn_fwd", "tri_attn_bwd",
+EXPORTED = ("triattn_status_string", "triattn_fwd_workspace_bytes", "triattn_bwd_workspace_bytes", "tri_attn_fwd",
+            "tri_attn_bwd",
             "triattn_device_status", "triattn_set_wait_limit_ns", "triattn_trace_enable", "triattn_trace_read",
             "triattn_test_set_starve", "tri_attn_bwd_noalloc", "triattn_bwd_atomic_workspace_bytes",
             "tri_attn_bwd_atomic_ablation", "tri_attn_dbias_combine", "triattn_module_ctx_bytes",
@@ -78,7 +79,9 @@ def _declare(lib):
     lib.triattn_status_string.restype = ctypes.c_char_p
     lib.triattn_bwd_workspace_bytes.argtypes = [sp]
     lib.triattn_bwd_workspace_bytes.restype = ctypes.c_size_t
-    lib.tri_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.triattn_fwd_workspace_bytes.argtypes = [sp]
+    lib.triattn_fwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.tri_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.tri_attn_fwd.restype = ctypes.c_int
     lib.tri_attn_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.tri_attn_bwd.restype = ctypes.c_int
@@ -177,9 +180,16 @@ def bwd_workspace_bytes(q_or_shape) -> int:
     return int(load().triattn_bwd_workspace_bytes(ctypes.byref(s)))
 
 
-def tri_attn_fwd(q, k, v, bias, mask=None, *, save_residual: bool = True, out=None, stream=None):
+def fwd_workspace_bytes(q_or_shape) -> int:
+    s = q_or_shape if isinstance(q_or_shape, Shape) else shape_of(q_or_shape)
+    return int(load().triattn_fwd_workspace_bytes(ctypes.byref(s)))
+
+
+def tri_attn_fwd(q, k, v, bias, mask=None, *, save_residual: bool = True, out=None, workspace=None, stream=None):
     """Forward.  Returns (o [B,N_o,H,N,D] bf16, lse [B,N_o,H,N] fp32,
-    o_resid bf16 or None).  ``out`` may pass preallocated (o, lse, o_resid)."""
+    o_resid bf16 or None).  ``out`` may pass preallocated (o, lse, o_resid),
+    ``workspace`` a uint8 device buffer of ``fwd_workspace_bytes`` bytes
+    (allocated per call otherwise)."""
     s = shape_of(q)
     B, No, H, N, D = q.shape
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -193,8 +203,12 @@ def tri_attn_fwd(q, k, v, bias, mask=None, *, save_residual: bool = True, out=No
         resid = torch.empty_like(q) if save_residual else None
     else:
         o, lse, resid = out
+    if workspace is None:
+        need = fwd_workspace_bytes(s)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     code = load().tri_attn_fwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(mask), _ptr(o),
-                               _ptr(lse), _ptr(resid), _stream_ptr(stream))
+                               _ptr(lse), _ptr(resid), _ptr(workspace), ctypes.c_size_t(nbytes), _stream_ptr(stream))
     _raise(code, "tri_attn_fwd")
     return o, lse, resid
 

@@ -49,7 +49,7 @@ def call_fwd(lib, shape, **ptrs):
     p.update({"mask": None, "o_resid": None})
     p.update(ptrs)
     return lib.tri_attn_fwd(ctypes.byref(shape), p["q"], p["k"], p["v"], p["bias"], p["mask"], p["o"], p["lse"],
-                            p["o_resid"], None)
+                            p["o_resid"], None, ctypes.c_size_t(0), None)
 
 
 def call_bwd(lib, shape, ws_bytes, ws=FAKE, **ptrs):
@@ -64,10 +64,10 @@ def call_bwd(lib, shape, ws_bytes, ws=FAKE, **ptrs):
 
 @pytest.mark.parametrize("shape,code", [
     ((1, 48, 48, 2, 24, 0), T.ERR_UNSUPPORTED),   # D not in {16, 32}
-    ((1, 44, 48, 2, 16, 0), T.ERR_UNSUPPORTED),   # outer shard not a multiple of 8
     ((1, 56, 48, 2, 16, 0), T.ERR_UNSUPPORTED),   # more outer slices than N
-    ((1, 44, 44, 2, 16, 0), T.ERR_UNSUPPORTED),   # N not a multiple of 8
-    ((1, 8192, 8192, 1, 16, 0), T.ERR_UNSUPPORTED),  # N beyond 4096
+    ((1, 262145, 262145, 1, 16, 0), T.ERR_UNSUPPORTED),  # more than 65535 outer groups of 4
+    ((1, 46341, 46341, 1, 16, 0), T.ERR_UNSUPPORTED),    # N * ceil(N / 128) * 128 beyond 2^31
+    ((256, 48, 48, 256, 16, 0), T.ERR_UNSUPPORTED),      # B * H beyond the grid
     ((0, 48, 48, 2, 16, 0), T.ERR_INVALID_ARG),   # empty batch
     ((1, 0, 0, 2, 16, 0), T.ERR_INVALID_ARG),     # empty crop
     ((1, 48, 48, 0, 16, 0), T.ERR_INVALID_ARG),   # no heads
@@ -78,6 +78,48 @@ def test_bad_shapes(lib, shape, code):
     assert call_fwd(lib, s) == code
     assert call_bwd(lib, s, 1 << 40) == code
     assert lib.triattn_bwd_workspace_bytes(ctypes.byref(s)) == 0
+    assert lib.triattn_fwd_workspace_bytes(ctypes.byref(s)) == 0
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1, 16), (1, 17, 17, 2, 32), (2, 130, 130, 4, 16), (1, 1000, 1000, 1, 32),
+                                   (1, 44, 48, 2, 16), (1, 5000, 5000, 1, 16), (3, 3, 64, 2, 32)])
+def test_any_n_accepted_with_workspace_sizes(lib, shape):
+    """Any N >= 1 and any shard 1 <= N_o <= N are accepted ("TurboPairFormer",
+    Table 1 places no divisibility rule on N).  The forward's workspace holds
+    one 144-byte key-mask record per (slice, 64-key tile) with four padding
+    slices, then (N not a multiple of 8) the bias with rows padded to a
+    multiple of 8 elements; the backward's transposed bias uses that row
+    stride, and its dbias partials cover ceil(N_o / G) outer groups."""
+    B, No, N, H, D = shape
+    s = T.Shape(B, No, N, H, D, 0)
+    r256 = lambda x: (x + 255) // 256 * 256
+    jk64, jq, jk = -(-N // 64), -(-N // 128), -(-N // 128)
+    Np = -(-N // 8) * 8
+    rec = r256((B * No + 4) * jk64 * 144)
+    pad = r256(B * H * N * Np * 2) if N % 8 else 0
+    assert lib.triattn_fwd_workspace_bytes(ctypes.byref(s)) == rec + pad
+    slices = B * No * H
+    G = 4 if D == 32 else 8
+    want = (r256(slices * jq * 128 * 16) + r256(B * H * N * Np * 2) + r256(jk * slices * jq * 128 * D * 4)
+            + r256(-(-No // G) * B * H * jq * jk * 128 * 128 * 4))
+    assert lib.triattn_bwd_workspace_bytes(ctypes.byref(s)) == want
+
+
+def test_forward_workspace_checks(lib):
+    """With a mask, or N not a multiple of 64, the forward needs its
+    workspace: a missing or short one is TRIATTN_ERR_WORKSPACE before any
+    launch; without a mask and N a multiple of 64 none is needed."""
+    s = T.Shape(1, 40, 40, 2, 16, 0)
+    need = lib.triattn_fwd_workspace_bytes(ctypes.byref(s))
+    assert need > 0
+    assert call_fwd(lib, s) == T.ERR_WORKSPACE
+    p = {n: ctypes.c_void_p(FAKE) for n in ("q", "k", "v", "bias", "o", "lse")}
+    short = lib.tri_attn_fwd(ctypes.byref(s), p["q"], p["k"], p["v"], p["bias"], None, p["o"], p["lse"], None,
+                             ctypes.c_void_p(FAKE), ctypes.c_size_t(need - 256), None)
+    assert short == T.ERR_WORKSPACE
+    misaligned = lib.tri_attn_fwd(ctypes.byref(s), p["q"], p["k"], p["v"], p["bias"], None, p["o"], p["lse"], None,
+                                  ctypes.c_void_p(FAKE + 16), ctypes.c_size_t(need), None)
+    assert misaligned == T.ERR_WORKSPACE
 
 
 def test_null_and_misaligned_pointers(lib):
@@ -168,17 +210,21 @@ def test_atomic_ablation_workspace_and_mask_checks(lib):
 
 def test_outer_shard_ranges():
     from protein_folding_triangle_gb300.sharding import outer_shard
-    for n, world in ((768, 1), (768, 2), (768, 3), (768, 8), (200, 3), (48, 6), (8, 1)):
+    for n, world in ((768, 1), (768, 2), (768, 3), (768, 8), (200, 3), (48, 6), (8, 1), (771, 4), (17, 2),
+                     (16, 3), (5, 5)):
         ranges = [outer_shard(n, r, world) for r in range(world)]
         assert ranges[0][0] == 0 and ranges[-1][1] == n
         for (lo, hi), (lo2, _) in zip(ranges, ranges[1:]):
             assert hi == lo2
         sizes = [hi - lo for lo, hi in ranges]
-        assert all(sz % 8 == 0 and sz >= 8 for sz in sizes) and max(sizes) - min(sizes) <= 8
+        assert all(sz >= 1 for sz in sizes)
+        if n // 8 >= world:  # whole blocks of 8, the remainder on the last rank
+            assert all(lo % 8 == 0 for lo, _ in ranges)
+            assert max(sizes[:-1] + [sizes[-1] - n % 8]) - min(sizes[:-1] + [sizes[-1] - n % 8]) <= 8
+        else:
+            assert max(sizes) - min(sizes) <= 1
     with pytest.raises(ValueError):
-        outer_shard(44, 0, 1)
-    with pytest.raises(ValueError):
-        outer_shard(16, 0, 3)
+        outer_shard(2, 0, 3)
 
 
 def test_shard_shapes_accepted(lib):
@@ -349,8 +395,9 @@ def test_chunk_slices_picks_the_largest_fitting_multiple():
     assert SH.chunk_slices(64, per, 10 ** 9) == 64
     with pytest.raises(ValueError):
         SH.chunk_slices(64, per, 1000)          # not even 8 slices fit
-    with pytest.raises(ValueError):
-        SH.chunk_slices(60, per, 10 ** 9)       # not a multiple of 8
+    assert SH.chunk_slices(60, per, 10 ** 9) == 60   # the whole axis, not a multiple of 8
+    assert SH.chunk_slices(60, per, 1000 + 10 * 59) == 56
+    assert SH.chunk_slices(5, per, 10 ** 9) == 5
 
 
 def test_chunked_backward_workspace_is_bounded(lib):

@@ -392,3 +392,84 @@ def test_sharded_entry_point_in_one_rank_group():
         assert err <= TOL_GRAD
     finally:
         dist.destroy_process_group()
+
+
+ANY_N = [
+    # (B, N, H, D, mask) -- N not a multiple of 8 or of the tiles; N = 1 and
+    # N_o = N < 4 leave most of a four-slice group empty
+    (1, 1, 1, 16, "none"),
+    (1, 3, 3, 32, "none"),
+    (1, 17, 2, 32, "random"),
+    (1, 63, 2, 16, "tail"),
+    (1, 65, 1, 32, "random"),
+    (1, 128, 2, 32, "none"),     # no mask, N a multiple of 64: the forward needs no workspace
+    (2, 130, 2, 16, "tail"),
+    (1, 1000, 1, 32, "random"),
+]
+
+
+@pytest.mark.parametrize("case", ANY_N, ids=[f"B{c[0]}N{c[1]}H{c[2]}D{c[3]}{c[4]}" for c in ANY_N])
+def test_any_n_parity_and_replay(case):
+    """Any N >= 1 ("TurboPairFormer", Table 1 puts no divisibility rule on the
+    crop size): every element against the FP64 oracle, and five calls
+    bitwise equal."""
+    B, N, H, D, mk = case
+    w = S.custom(B, N, H, D, name="anyn", mask=mk, mask_frac=0.1 if mk != "none" else 0.0)
+    x = S.make_inputs(w, seed=N + 7 * D)
+    xd = to_dev(x)
+    out = gpu_fwd_bwd(xd)
+    replay_equal(xd, out)
+    errs = compare_full(out, oracle_full(x))
+    check_errs(errs, f"anyN{case}")
+    assert errs["lse_inf_match"]
+
+
+@pytest.mark.parametrize("N,world", [(131, 3), (61, 2), (20, 3)])
+def test_ragged_outer_shards_emulated_on_one_gpu(N, world):
+    """Outer-axis shards of any length (48, 40 and 43; 32 and 29; 7, 7 and 6
+    slices): each shard's O, lse, dQ, dK, dV are bitwise the matching slices
+    of the unsharded call, and the rank-ordered combine of their FP32 dbias
+    parts meets the FP64 bar."""
+    from protein_folding_triangle_gb300.sharding import outer_shard
+    w = S.custom(1, N, 2, 32, name="rshard", mask="random", mask_frac=0.1)
+    x = S.make_inputs(w, seed=N)
+    xd = to_dev(x)
+    full = gpu_fwd_bwd(xd)
+    parts = []
+    for r in range(world):
+        lo, hi = outer_shard(N, r, world)
+        sh = {k: (v if k == "bias" or v is None else v[:, lo:hi].contiguous()) for k, v in xd.items()}
+        o, lse, resid = T.tri_attn_fwd(sh["q"], sh["k"], sh["v"], sh["bias"], sh["mask"])
+        dq, dk, dv, part = T.tri_attn_bwd(sh["q"], sh["k"], sh["v"], sh["bias"], sh["mask"], o, resid, lse, sh["do"],
+                                          dbias_fp32=True)
+        torch.cuda.synchronize()
+        assert T.device_status() == T.OK
+        for name, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            assert torch.equal(t, full[name][:, lo:hi]), (r, name)
+        parts.append(part)
+    db = T.tri_attn_dbias_combine(torch.stack(parts).contiguous())
+    torch.cuda.synchronize()
+    err = rel_rmse(cpu64(db), oracle_full(x)["dbias"])
+    print(json.dumps({"case": f"ragged shards N{N} x{world}", "dbias": err}))
+    assert err <= TOL_GRAD
+
+
+def test_n_beyond_4096_chunked_backward():
+    """N = 4101 (odd, past the 4096 tokens the forward once staged in shared
+    memory): the forward on sampled slices and dbias rows against the FP64
+    oracle; the backward through the memory-bounded chunked path (chunks
+    under 4 GB of workspace, the last one ragged), sampled the same way."""
+    from protein_folding_triangle_gb300 import sharding as SH
+    w = S.custom(1, 4101, 1, 16, name="n4101", mask="random", mask_frac=0.05)
+    x = S.make_inputs(w, seed=41)
+    xd = to_dev(x)
+    o, lse, resid = T.tri_attn_fwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"])
+    dq, dk, dv, db = SH.chunked_tri_attn_bwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], o, resid, lse,
+                                             xd["do"], max_workspace_bytes=4 << 30)
+    torch.cuda.synchronize()
+    assert T.device_status() == T.OK
+    out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "dbias": db}
+    for t in ("o", "dq", "dk", "dv", "dbias"):
+        assert torch.isfinite(out[t].float()).all(), t
+    errs = compare_sampled(x, out, w, n_slices=3, n_rows=6, seed=9)
+    check_errs(errs, "n4101")

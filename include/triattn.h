@@ -16,7 +16,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays,
- *    16-byte aligned.  "bf16" means IEEE bfloat16 stored as uint16.
+ *    16-byte aligned, except the key mask (2-byte aligned) and lse (4-byte
+ *    aligned), so that a shard of the outer axis may start at any slice.
+ *    "bf16" means IEEE bfloat16 stored as uint16.
  *  - Layouts: q, k, v, o, o_resid, dO, dq, dk, dv  [B, N_o, H, N, D] bf16
  *             bias, dbias                         [B, H, N, N]      bf16
  *             mask (optional, additive)           [B, N_o, N]       bf16

@@ -26,6 +26,7 @@ uint32_t* g_status_ptr[64] = {};     // device address of g_status_word per devi
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 triattn_status init_device(int* dev_out) {
   int dev = 0;
@@ -136,7 +137,7 @@ WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
   const size_t slices = static_cast<size_t>(s->B) * s->N_o * s->H;
   const size_t jk = (s->N + kTileK - 1) / kTileK;
   const size_t jq = (s->N + kTileQ - 1) / kTileQ;
-  const size_t groups = (s->N_o + kGroupBwdFor(s->D) - 1) / kGroupBwdFor(s->D);
+  const size_t groups = bwd_dbias_parts(s->N_o, s->D, atomic_mask == 0);
   WsLayout w;
   w.rec_off = 0;
   w.biasT_off = round_up(slices * jq * kTileQ * 16, 256);
@@ -225,10 +226,11 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
                         size_t workspace_bytes, void* stream) {
   triattn_status st = check_shape(shape);
   if (st != TRIATTN_OK) return st;
-  const void* req[] = {q, k, v, bias, o, lse, dO, dq, dk, dv, dbias};
+  const void* req[] = {q, k, v, bias, o, dO, dq, dk, dv, dbias};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
-  if ((mask && !aligned16(mask)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
+  if (lse == nullptr || !aligned_to(lse, 4)) return TRIATTN_ERR_INVALID_ARG;
+  if ((mask && !aligned_to(mask, 2)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(shape, atomic_mask);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
     return TRIATTN_ERR_WORKSPACE;
@@ -260,6 +262,7 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
   a.H = shape->H;
   a.D = shape->D;
   a.dbias_fp32 = (shape->flags & TRIATTN_FLAG_DBIAS_FP32) ? 1 : 0;
+  a.dbias_parts = bwd_dbias_parts(shape->N_o, shape->D, atomic_mask == 0);
   a.wc = wait_ctl(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool d32 = shape->D == 32;
@@ -315,10 +318,11 @@ triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const voi
                             void* workspace, size_t workspace_bytes, void* stream) {
   triattn_status st = check_shape(shape);
   if (st != TRIATTN_OK) return st;
-  const void* req[] = {q, k, v, bias, o, lse};
+  const void* req[] = {q, k, v, bias, o};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
-  if ((mask && !aligned16(mask)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
+  if (lse == nullptr || !aligned_to(lse, 4)) return TRIATTN_ERR_INVALID_ARG;
+  if ((mask && !aligned_to(mask, 2)) || (o_resid && !aligned16(o_resid))) return TRIATTN_ERR_INVALID_ARG;
   const FwdWs fw = fwd_ws(shape, mask != nullptr);
   if (fw.total() > 0 &&
       (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < fw.total()))

@@ -137,7 +137,7 @@ WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
   const size_t slices = static_cast<size_t>(s->B) * s->N_o * s->H;
   const size_t jk = (s->N + kTileK - 1) / kTileK;
   const size_t jq = (s->N + kTileQ - 1) / kTileQ;
-  const size_t groups = bwd_dbias_parts(s->N_o, s->D, atomic_mask == 0);
+  const size_t groups = (s->N_o + kGroupBwdFor(s->D) - 1) / kGroupBwdFor(s->D);
   WsLayout w;
   w.rec_off = 0;
   w.biasT_off = round_up(slices * jq * kTileQ * 16, 256);
@@ -262,7 +262,6 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
   a.H = shape->H;
   a.D = shape->D;
   a.dbias_fp32 = (shape->flags & TRIATTN_FLAG_DBIAS_FP32) ? 1 : 0;
-  a.dbias_parts = bwd_dbias_parts(shape->N_o, shape->D, atomic_mask == 0);
   a.wc = wait_ctl(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool d32 = shape->D == 32;

@@ -209,30 +209,12 @@ struct BwdBars {
   uint64_t kv_full;
   uint64_t qdo_full[NQ], qdo_empty[NQ];
   uint64_t b_full[2], b_empty[2];
-  // dbias exchange of a CTA pair (ordered path): the peer's elementwise warps
-  // are done with its bias stage (peer_free), the peer's half of the dbias
-  // tile has landed in this CTA's bias stage (landed)
-  uint64_t peer_free[2], landed[2];
   uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full, dq_read, all_done;
   uint64_t never;  // completes no phase: a parity-1 wait on it always passes
   uint32_t tmem_slot;
   int abort;
 };
-static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
-// CTA pairs (the ordered path, kAtomic == 0): the grid's outer groups run as
-// clusters of two CTAs, groups 2p and 2p + 1 of the same (b, h, key tile).
-// After the last slice of a query tile each CTA holds the FP32 dbias tile of
-// its own group; rank 0 keeps query columns [0, 64), rank 1 [64, 128), and
-// each sends the other half to its peer through distributed shared memory,
-// into the peer's bias stage of that query tile (free once the peer's
-// elementwise warps have read it: they say so with a remote arrival).  The
-// receiving warps add the two halves -- group 2p's value plus group 2p + 1's,
-// the same two FP32 values either way -- and write one single-writer partial
-// per pair: half the partial bytes of one per group, and the reduction adds
-// ceil(groups / 2) partials in ascending pair order.  A grid with an odd
-// number of groups gets one more CTA whose slices are all past N_o (P = 0).
-//
 // kAtomic (non-deterministic ablation only; 0 in the product path): bit 0
 // adds the dQ tiles into an FP32 [slices][J_Q*128][D] accumulator, bit 1 the
 // dbias tiles into an FP32 [B*H][J_K*128 (k)][J_Q*128 (q)] accumulator, with
@@ -246,7 +228,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                     float* __restrict__ dq_part, float* __restrict__ dbias_part, int N_o, int N, int H, WaitCtl wc) {
   using L = BwdSmem<D>;
   constexpr int G = L::G;  // outer slices per CTA
-  constexpr bool kPair = kAtomic == 0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   BwdBars* bars = reinterpret_cast<BwdBars*>(sm + L::kBar);
@@ -295,11 +276,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->b_full[i], 1);
-      // every elementwise thread after its last bias read; with pairs also
-      // the receiving half after it has read the peer's dbias half
-      mbar_init(&bars->b_empty[i], kPair ? kEW + kEW / 2 : kEW);
-      mbar_init(&bars->peer_free[i], kEW / 32);  // one arrival per peer elementwise warp
-      mbar_init(&bars->landed[i], kEW / 64);     // one per peer sending warp
+      mbar_init(&bars->b_empty[i], kEW);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -318,9 +295,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
-  // the peer's barriers are initialised before anything arrives on them
-  if constexpr (kPair) cluster_sync();
-  const uint32_t crank = kPair ? cluster_rank() : 0u;
 
   // Warpgroup 0 (producer and the three issuers: one warp per TMEM lane
   // quarter) drains each dQ tile: warp w stores rows [32w, 32w + 32), all D
@@ -647,13 +621,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           }
         }
       }
-      if (g == G - 1) {
-        mbar_arrive(&bars->b_empty[bst]);  // last read of this bias tile
-        if constexpr (kPair) {  // ... and the peer may write its dbias half into this stage
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->peer_free[bst]), crank ^ 1u));
-        }
-      }
+      if (g == G - 1) mbar_arrive(&bars->b_empty[bst]);  // last read of this bias tile
       // BF16 P^T into columns this thread has read itself
       tmem_st16(tmem + lane_addr + kTS + col0 + ((wg & 1) ? 0 : 16), pw);  // = p_col(wg)
       tc_wait_st();
@@ -699,50 +667,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->ds_ready);
       if (g == G - 1) {
-        // single-writer dbias partial of this outer group (of this pair, for
-        // the receiving half) for tile (i, ktile), stored chunk-major
-        // ([16 chunks of 8 queries][128 keys] x 8 floats) with 32-byte
-        // stores, so that each warp store covers 1 KB
-        if constexpr (kPair) {
-          // landing area in the bias stage of this query tile: [2 warpgroups][128 keys][32 floats], 128-byte swizzle
-          const uint32_t land = smem_u32(sm + L::kBias + bst * (BM * BN * 2) + (wg & 1) * (BN * 128));
-          const uint32_t ph = static_cast<uint32_t>((i >> 1) & 1);
-          if ((static_cast<uint32_t>(wg) >> 1) != crank) {
-            // send: once the peer has read its bias stage
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->peer_free[bst], ph, wc, abort))) {
-              ok = false;
-              break;
-            }
-            const uint32_t rland = mapa_shared(land, crank ^ 1u);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              st_cluster_v4(rland + sw128(r, c),
-                            make_uint4(__float_as_uint(dbacc[2 * c].x), __float_as_uint(dbacc[2 * c].y),
-                                       __float_as_uint(dbacc[2 * c + 1].x), __float_as_uint(dbacc[2 * c + 1].y)));
-            fence_proxy_async_cluster();  // before the peer's TMA refills the stage
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->landed[bst]), crank ^ 1u));
-          } else {
-            // receive the peer's half, add, write the pair's partial
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->landed[bst], ph, wc, abort))) {
-              ok = false;
-              break;
-            }
-            float* dst = dbias_part +
-                         ((((static_cast<size_t>(grp >> 1) * gridDim.z + bh) * JQ + i) * gridDim.x + ktile) * (BM * BN)) +
-                         ((col0 / 8) * BN + r) * 8;
-            const uint8_t* lp = sm + L::kBias + bst * (BM * BN * 2) + (wg & 1) * (BN * 128);
-#pragma unroll
-            for (int k8 = 0; k8 < kCols / 8; ++k8) {
-              const float4 u = *reinterpret_cast<const float4*>(lp + sw128(r, 2 * k8));
-              const float4 v = *reinterpret_cast<const float4*>(lp + sw128(r, 2 * k8 + 1));
-              st_global_v8(dst + k8 * BN * 8, dbacc[4 * k8].x + u.x, dbacc[4 * k8].y + u.y, dbacc[4 * k8 + 1].x + u.z,
-                           dbacc[4 * k8 + 1].y + u.w, dbacc[4 * k8 + 2].x + v.x, dbacc[4 * k8 + 2].y + v.y,
-                           dbacc[4 * k8 + 3].x + v.z, dbacc[4 * k8 + 3].y + v.w);
-            }
-            mbar_arrive(&bars->b_empty[bst]);  // the landing area may be refilled
-          }
-        } else if constexpr ((kAtomic & 2) != 0) {
+        // single-writer dbias partial of this outer group for tile (i, ktile),
+        // stored chunk-major ([16 chunks of 8 queries][128 keys] x 8 floats)
+        // with 32-byte stores, so that each warp store covers 1 KB
+        if constexpr ((kAtomic & 2) != 0) {
           float* acc = dbias_part + ((static_cast<size_t>(bh) * gridDim.x * BN + ktile * BN + r) * JQ + i) * BM + col0;
 #pragma unroll
           for (int k4 = 0; k4 < kCols / 4; ++k4)
@@ -801,9 +729,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  // neither CTA of a pair leaves while the other may still reach its shared
-  // memory
-  if constexpr (kPair) cluster_sync();
 }
 
 // ---------------------------------------------------------------- reductions
@@ -1044,32 +969,11 @@ cudaError_t launch_bwd_transpose_bias(const BwdArgs& a, cudaStream_t stream) {
 template <int D, int kAtomic>
 cudaError_t launch_main_variant(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
-  const int groups = (a.N_o + BwdSmem<D>::G - 1) / BwdSmem<D>::G;
-  if constexpr (kAtomic == 0) {
-    // clusters of two CTAs along the outer groups (an even grid)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(JK, 2 * ((groups + 1) / 2), a.B * a.H);
-    cfg.blockDim = dim3(kMainThreads, 1, 1);
-    cfg.dynamicSmemBytes = BwdSmem<D>::kBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 2;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<D, kAtomic>, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT,
-                              static_cast<const uint16_t*>(a.mask), static_cast<const uint4*>(a.rec),
-                              static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part,
-                              a.N_o, a.N, a.H, a.wc);
-  } else {
-    dim3 grid(JK, groups, a.B * a.H);
-    bwd_main_kernel<D, kAtomic><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
-        static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
-    return cudaGetLastError();
-  }
+  dim3 grid(JK, (a.N_o + BwdSmem<D>::G - 1) / BwdSmem<D>::G, a.B * a.H);
+  bwd_main_kernel<D, kAtomic><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
+      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
+  return cudaGetLastError();
 }
 
 template <int D>
@@ -1116,7 +1020,7 @@ cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
   const size_t tiles = static_cast<size_t>(a.B) * a.H * JQ * JK;
   const unsigned blocks = static_cast<unsigned>(tiles * (BM / kSlab));
-  const int groups = a.dbias_parts;
+  const int groups = (a.N_o + kGroupBwdFor(a.D) - 1) / kGroupBwdFor(a.D);
   if (a.dbias_fp32)
     reduce_dbias_kernel<float><<<blocks, kRedThreads, 0, stream>>>(
         reinterpret_cast<const float4*>(a.dbias_part), static_cast<float*>(a.dbias), a.N, JQ, JK, groups, tiles);

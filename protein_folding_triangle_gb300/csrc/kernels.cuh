@@ -20,13 +20,6 @@ constexpr int kGroupFwd = 4;
 // Backward: dK and dV of all slices of the group stay in TMEM (2 * G * D of
 // its 512 columns next to 256 for S^T and dP^T), so G = 8 at D = 16.
 constexpr int kGroupBwdFor(int D) { return D == 16 ? 8 : 4; }
-// dbias partials of the backward: the ordered path pairs the outer groups
-// (two CTAs of a cluster add their tiles before one write); the atomic
-// ablation variant with ordered dbias writes one per group.
-inline int bwd_dbias_parts(int N_o, int D, bool pairs) {
-  const int groups = (N_o + kGroupBwdFor(D) - 1) / kGroupBwdFor(D);
-  return pairs ? (groups + 1) / 2 : groups;
-}
 
 // Forward key-mask record per (slice, 64-key tile): 64 BF16 mask values, then
 // a 16-byte header whose first word is nonzero when any value is.
@@ -64,7 +57,6 @@ struct BwdArgs {
   float* dbias_part; // [L][B*H*N*N]
   int B, N_o, N, H, D;
   int dbias_fp32;    // write dbias as FP32 (the sum over this call's slices)
-  int dbias_parts;   // dbias partials the main kernel writes (one per CTA pair, or per group)
   WaitCtl wc;
 };
 

@@ -131,63 +131,6 @@ static __device__ __forceinline__ bool mbar_wait_all(const uint32_t (&bar)[N], c
   return true;
 }
 
-// ---------------------------------------------------------------- clusters
-// Rank of this CTA in its cluster, the shared-memory address of the same
-// offset in another CTA of the cluster, and stores / mbarrier arrivals there.
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-// Arrival on an mbarrier of another CTA of the cluster; release at cluster
-// scope orders this thread's earlier memory accesses (and, through a
-// preceding __syncwarp, its warp's) before the arrival.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-// Generic-proxy writes to shared memory of the cluster ordered before later
-// async-proxy (TMA) accesses of the same bytes.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Bounded wait (as mbar_wait) whose completion acquires at cluster scope:
-// for phases completed by arrivals from other CTAs of the cluster.
-__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, "
-      "p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-static __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
-                                                         volatile int* abort) {
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait_acq_cluster(bar, parity, kSuspendHintNs)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > wc.limit_ns) {
-      atomicOr(wc.status, kDevTimeout);
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2) {

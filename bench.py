@@ -56,7 +56,8 @@ def parse():
                     help="individually timed fwd / bwd calls (after 10 warm-ups) for the median and mean")
     ap.add_argument("--ablation", choices=["atomic"], default=None,
                     help="instead of the bench line: time the ordered backward against its non-deterministic "
-                         "FP32-atomic variants (dQ; dbias; both) on the same inputs and print one JSON line")
+                         "variants (FP32 atomics for dQ, dbias, both; TMA bulk reduction for dQ) on the same inputs and print one "
+                         "JSON line")
     ap.add_argument("--module", type=int, default=0, metavar="C",
                     help="instead of the bench line: time the whole module (LayerNorm, projections with C pair "
                          "features, the core, output projection; forward + backward) and print one JSON line")
@@ -557,7 +558,8 @@ def run_ours(args):
 # ----------------------------------------------------------------------------- ablation
 def run_atomic_ablation(args):
     """Backward only: the ordered single-writer partials + fixed-order reductions
-    against FP32 atomics for dQ, for dbias, and for both (the pages' Table 12
+    against FP32 atomics for dQ, for dbias, and for both, and TMA bulk
+    reductions for dQ (the pages' Table 12
     trade-off).  Same inputs, same launch stream, CUDA events, median of
     ``--steps`` timed calls after ``--warmup``; every call re-zeroes its
     accumulators, as a training step would."""
@@ -577,7 +579,7 @@ def run_atomic_ablation(args):
     o, lse, resid = T.tri_attn_fwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"])
     outs = (torch.empty_like(xd["q"]), torch.empty_like(xd["q"]), torch.empty_like(xd["q"]), torch.empty_like(xd["bias"]))
     arms = {"ordered": None, "atomic_dq": T.ATOMIC_DQ, "atomic_dbias": T.ATOMIC_DBIAS,
-            "atomic_dbias_dq": T.ATOMIC_DBIAS_DQ}
+            "atomic_dbias_dq": T.ATOMIC_DBIAS_DQ, "bulk_dq": T.BULK_DQ, "bulk_dq_atomic_dbias": T.BULK_DQ_ATOMIC_DBIAS}
     wsb = {}
     for name, m in arms.items():
         need = T.bwd_workspace_bytes(xd["q"]) if m is None else T.bwd_atomic_workspace_bytes(xd["q"], m)
@@ -607,7 +609,7 @@ def run_atomic_ablation(args):
     if T.device_status() != T.OK:
         raise SystemExit("device status not OK after the ablation")
     med = {n: statistics.median(v) for n, v in times.items()}
-    line = {"ablation": "ordered FP32 partials vs FP32 atomics (backward only)",
+    line = {"ablation": "ordered FP32 partials vs FP32 atomics and TMA bulk reductions (backward only)",
             "config": {"workload": w.describe(), "B": w.B, "N": w.N, "H": w.H, "D": w.D},
             "steps": args.steps, "warmup": max(3, args.warmup),
             "bwd_ms_median": {n: round(v, 4) for n, v in med.items()},

@@ -212,17 +212,20 @@ triattn_status tri_attn_bwd_noalloc(const triattn_shape* shape,
  * ABLATION ONLY, not the library's backward: the same computation with the
  * single-writer FP32 partials of dQ (atomic_mask = 1), of dbias (2) or of
  * both (3) replaced by FP32 atomic adds into zero-initialised FP32
- * accumulators, which small kernels then round to BF16 (the
- * non-deterministic variants of "TurboPairFormer", Section "Deterministic
- * reductions", Table 12).  It exists to measure what the ordered partials
+ * accumulators, or the dQ partials replaced by TMA bulk reductions
+ * (cp.reduce.async.bulk ... add.f32, one per 128-row dQ tile, this GPU's
+ * memory only) into such an accumulator (4), alone or with atomic dbias (6);
+ * small kernels then round the accumulators to BF16 (the non-deterministic
+ * variants of "TurboPairFormer", Section "Deterministic reductions",
+ * Table 12).  It exists to measure what the ordered partials
  * cost; the atomically added gradients are NOT bitwise reproducible between
  * calls (FP32 addition order varies), dK, dV and the ordered one are.
  * Arguments are those of tri_attn_bwd; the workspace must hold
  * triattn_bwd_atomic_workspace_bytes(shape, atomic_mask) bytes (the row
  * records, the transposed bias, then the FP32 accumulators
  * [B*N_o*H][J_Q*128][D] for dQ and [B*H][J_K*128][J_Q*128] for dbias, or
- * the partials of the operand that stays ordered).  atomic_mask outside
- * 1..3 returns TRIATTN_ERR_INVALID_ARG (and 0 bytes).
+ * the partials of the operand that stays ordered).  atomic_mask other than
+ * 1, 2, 3, 4 or 6 returns TRIATTN_ERR_INVALID_ARG (and 0 bytes).
  */
 size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask);
 triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape,

@@ -143,7 +143,8 @@ WsLayout ws_layout(const triattn_shape* s, int atomic_mask = 0) {
   w.biasT_off = round_up(slices * jq * kTileQ * 16, 256);
   w.dq_off = w.biasT_off + round_up(static_cast<size_t>(s->B) * s->H * s->N * padded_n(s->N) * 2, 256);
   // ablation: FP32 accumulators instead of the partials (see tri_attn_bwd_atomic_ablation)
-  const size_t dq_bytes = (atomic_mask & 1) ? slices * jq * kTileQ * s->D * 4 : jk * slices * jq * kTileQ * s->D * 4;
+  const size_t dq_bytes =
+      dq_accumulated(atomic_mask) ? slices * jq * kTileQ * s->D * 4 : jk * slices * jq * kTileQ * s->D * 4;
   const size_t db_bytes = (atomic_mask & 2) ? static_cast<size_t>(s->B) * s->H * jk * kTileK * jq * kTileQ * 4
                                             : groups * s->B * s->H * jq * jk * kTileQ * kTileK * 4;
   w.db_off = w.dq_off + round_up(dq_bytes, 256);
@@ -218,8 +219,9 @@ using namespace triattn;
 
 namespace {
 
-// The backward: atomic_mask 0 is the library's ordered path; 1, 2 and 3 are
-// the non-deterministic ablation (FP32 atomics for dQ, dbias, or both).
+// The backward: atomic_mask 0 is the library's ordered path; 1, 2, 3, 4 and
+// 6 are the non-deterministic ablation (FP32 atomics for dQ, dbias, or both;
+// a TMA bulk reduction for dQ, alone or with atomic dbias).
 triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k, const void* v, const void* bias,
                         const void* mask, const void* o, const void* o_resid, const float* lse, const void* dO,
                         void* dq, void* dk, void* dv, void* dbias, int atomic_mask, void* workspace,
@@ -266,7 +268,7 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool d32 = shape->D == 32;
   cudaError_t e = cudaSuccess;
-  if (atomic_mask & 1) e = cudaMemsetAsync(ws + w.dq_off, 0, w.db_off - w.dq_off, s);
+  if (dq_accumulated(atomic_mask)) e = cudaMemsetAsync(ws + w.dq_off, 0, w.db_off - w.dq_off, s);
   if (e == cudaSuccess && (atomic_mask & 2)) e = cudaMemsetAsync(ws + w.db_off, 0, w.total - w.db_off, s);
   if (e == cudaSuccess)
     e = traced(kKPre, s, [&] { return d32 ? launch_bwd_preprocess<32>(a, s) : launch_bwd_preprocess<16>(a, s); });
@@ -277,9 +279,9 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
     e = traced(kKMainAtomic, s, [&] {
       return d32 ? launch_bwd_main_atomic<32>(a, atomic_mask, s) : launch_bwd_main_atomic<16>(a, atomic_mask, s);
     });
-  if (e == cudaSuccess && !(atomic_mask & 1))
+  if (e == cudaSuccess && !dq_accumulated(atomic_mask))
     e = traced(kKRedDq, s, [&] { return d32 ? launch_bwd_reduce_dq<32>(a, s) : launch_bwd_reduce_dq<16>(a, s); });
-  if (e == cudaSuccess && (atomic_mask & 1))
+  if (e == cudaSuccess && dq_accumulated(atomic_mask))
     e = traced(kKFinDq, s, [&] { return d32 ? launch_bwd_finish_dq<32>(a, s) : launch_bwd_finish_dq<16>(a, s); });
   if (e == cudaSuccess && !(atomic_mask & 2)) e = traced(kKRedDb, s, [&] { return launch_bwd_reduce_dbias(a, s); });
   if (e == cudaSuccess && (atomic_mask & 2)) e = traced(kKFinDb, s, [&] { return launch_bwd_finish_dbias(a, s); });
@@ -366,7 +368,7 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
 }
 
 size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask) {
-  if (check_shape(shape) != TRIATTN_OK || atomic_mask < 1 || atomic_mask > 3) return 0;
+  if (check_shape(shape) != TRIATTN_OK || !atomic_mask_ok(atomic_mask)) return 0;
   return ws_layout(shape, atomic_mask).total;
 }
 
@@ -375,7 +377,7 @@ triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape, const vo
                                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
                                             void* dbias, int atomic_mask, void* workspace, size_t workspace_bytes,
                                             void* stream) {
-  if (atomic_mask < 1 || atomic_mask > 3) return TRIATTN_ERR_INVALID_ARG;
+  if (!atomic_mask_ok(atomic_mask)) return TRIATTN_ERR_INVALID_ARG;
   if (shape != nullptr && shape->flags != 0) return TRIATTN_ERR_INVALID_ARG;
   return bwd_impl(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, atomic_mask, workspace,
                   workspace_bytes, stream);

@@ -211,6 +211,9 @@ struct BwdBars {
   uint64_t b_full[2], b_empty[2];
   uint64_t s_full, dp_full, s_cons, p_ready, ds_ready, dq_full, dq_read, all_done;
   uint64_t never;  // completes no phase: a parity-1 wait on it always passes
+  // bulk-reduction ablation only: the dQ tile staged in shared memory
+  // (staged), and its bulk read finished so the staging area is free (stage_free)
+  uint64_t staged, stage_free;
   uint32_t tmem_slot;
   int abort;
 };
@@ -218,7 +221,11 @@ struct BwdBars {
 // kAtomic (non-deterministic ablation only; 0 in the product path): bit 0
 // adds the dQ tiles into an FP32 [slices][J_Q*128][D] accumulator, bit 1 the
 // dbias tiles into an FP32 [B*H][J_K*128 (k)][J_Q*128 (q)] accumulator, with
-// FP32 atomics instead of writing single-writer partials.
+// FP32 atomics instead of writing single-writer partials; bit 2 adds the dQ
+// tiles into the same accumulator with the TMA engine's bulk reduction
+// (cp.reduce.async.bulk, this GPU's memory only): warpgroup 0 stages the
+// FP32 tile in the dS buffer once the dQ MMA has read it, one thread issues
+// the reduction, and the next dS waits until the engine has read the tile.
 template <int D, int kAtomic = 0>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -287,6 +294,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&bars->dq_read, 128);
     mbar_init(&bars->all_done, 3);
     mbar_init(&bars->never, 1);
+    mbar_init(&bars->staged, 128);
+    mbar_init(&bars->stage_free, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -318,6 +327,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     else tmem_ld16_wait(taddr, qr);
     if (!live) {
       // a padded slice of the last group: nothing to store
+    } else if constexpr ((kAtomic & 4) != 0) {
+      // FP32 row r of the tile into the staging area (row-major, the
+      // accumulator's layout), 16-byte chunks in a rotated order so that a
+      // quarter warp's stores hit distinct banks
+      uint8_t* stg = sm + L::kDS + r * (D * 4);
+#pragma unroll
+      for (int cc = 0; cc < D / 4; ++cc) {
+        const int c = (cc + r) & (D / 4 - 1);
+        *reinterpret_cast<float4*>(stg + c * 16) =
+            make_float4(__uint_as_float(qr[4 * c]) * isd, __uint_as_float(qr[4 * c + 1]) * isd,
+                        __uint_as_float(qr[4 * c + 2]) * isd, __uint_as_float(qr[4 * c + 3]) * isd);
+      }
     } else if constexpr ((kAtomic & 1) != 0) {
       float* acc = dq_part + ((slice * JQ + ti) * BM + r) * D;
 #pragma unroll
@@ -334,6 +355,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     tc_fence_before();
     mbar_arrive(&bars->dq_read);
+    if constexpr ((kAtomic & 4) != 0) {
+      fence_proxy_async_smem();  // the staged rows, before the engine reads them
+      mbar_arrive(&bars->staged);
+      if (warp == 3 && lane == 0) {
+        if (!mbar_wait(&bars->staged, t & 1, wc, abort)) return false;
+        if (live) bulk_reduce_add_f32(dq_part + (slice * JQ + ti) * (BM * D), sm + L::kDS, BM * D * 4);
+        bulk_wait_read();
+        mbar_arrive(&bars->stage_free);  // the next dS may overwrite the staging area
+      }
+    }
     return true;
   };
 
@@ -540,6 +571,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!drain_dq(s)) { ok = false; break; }
       }
     }
+    // the last bulk reduction has landed before the kernel ends
+    if constexpr ((kAtomic & 4) != 0) {
+      if (warp == 3 && lane == 0) bulk_wait_all();
+    }
     // every MMA this issuer started is complete when all_done fires
     if (elect_one()) mma_commit(&bars->all_done);
     __syncwarp();
@@ -630,8 +665,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
       // ---------------- dS-phase (dS in shared memory is free once the previous dQ tile is done)
       {
-        // dP^T(s); the dQ tile of s-1 has read dS (parity 1 passes at s = 0)
-        const uint32_t wb[2] = {smem_u32(&bars->dp_full), smem_u32(&bars->dq_full)};
+        // dP^T(s); the dQ tile of s-1 has read dS (parity 1 passes at s = 0);
+        // with the bulk reduction the staged tile of s-1 has been read too
+        const uint32_t wb[2] = {smem_u32(&bars->dp_full),
+                                smem_u32((kAtomic & 4) != 0 ? &bars->stage_free : &bars->dq_full)};
         const uint32_t wp[2] = {static_cast<uint32_t>(s & 1), static_cast<uint32_t>((s - 1) & 1)};
         if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
@@ -944,6 +981,10 @@ cudaError_t setup_bwd() {
     e = cudaFuncSetAttribute(bwd_main_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bwd_main_kernel<D, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_main_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_main_kernel<D, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
   return e;
 }
 
@@ -986,6 +1027,8 @@ cudaError_t launch_bwd_main_atomic(const BwdArgs& a, int atomic_mask, cudaStream
   if (atomic_mask == 1) return launch_main_variant<D, 1>(a, stream);
   if (atomic_mask == 2) return launch_main_variant<D, 2>(a, stream);
   if (atomic_mask == 3) return launch_main_variant<D, 3>(a, stream);
+  if (atomic_mask == 4) return launch_main_variant<D, 4>(a, stream);
+  if (atomic_mask == 6) return launch_main_variant<D, 6>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -77,7 +77,11 @@ template <int D> cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t
 cudaError_t launch_bwd_reduce_dbias(const BwdArgs& a, cudaStream_t stream);
 template <int D> int bwd_smem_bytes();
 // Non-deterministic ablation of the backward (FP32 atomics; never used by
-// tri_attn_bwd): atomic_mask 1 = dQ, 2 = dbias, 3 = dbias and dQ.
+// tri_attn_bwd): atomic_mask 1 = dQ, 2 = dbias, 3 = dbias and dQ by FP32
+// atomics; 4 = dQ by TMA bulk reduction, 6 = that and dbias by atomics.
+inline bool atomic_mask_ok(int m) { return m == 1 || m == 2 || m == 3 || m == 4 || m == 6; }
+// the dQ tiles go into an FP32 accumulator (atomics or bulk reduction)
+inline bool dq_accumulated(int m) { return (m & 5) != 0; }
 template <int D> cudaError_t launch_bwd_main_atomic(const BwdArgs& a, int atomic_mask, cudaStream_t stream);
 template <int D> cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_finish_dbias(const BwdArgs& a, cudaStream_t stream);

@@ -342,6 +342,20 @@ __device__ __forceinline__ void red_add_v4(float* p, float a0, float a1, float a
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a0), "f"(a1), "f"(a2), "f"(a3)
                : "memory");
 }
+// Bulk reduction (TMA engine): global[dst .. dst + bytes) += shared[src ..
+// src + bytes) in FP32, then commit; wait_read returns once the shared source
+// of every committed operation has been read, wait_all once the global
+// updates are complete.  16-byte aligned addresses, size a multiple of 16.
+// Used only by the non-deterministic ablation of the backward.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // 32-byte global store (address 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(float* p, float a0, float a1, float a2, float a3, float a4, float a5,
                                              float a6, float a7) {

@@ -247,7 +247,7 @@ def tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, workspace=None, ou
     return dq, dk, dv, dbias
 
 
-ATOMIC_DQ, ATOMIC_DBIAS, ATOMIC_DBIAS_DQ = 1, 2, 3
+ATOMIC_DQ, ATOMIC_DBIAS, ATOMIC_DBIAS_DQ, BULK_DQ, BULK_DQ_ATOMIC_DBIAS = 1, 2, 3, 4, 6
 
 
 def bwd_atomic_workspace_bytes(q_or_shape, atomic_mask: int) -> int:
@@ -259,9 +259,10 @@ def bwd_atomic_workspace_bytes(q_or_shape, atomic_mask: int) -> int:
 def tri_attn_bwd_atomic_ablation(q, k, v, bias, mask, o, o_resid, lse, do, atomic_mask=ATOMIC_DBIAS_DQ, *,
                                  workspace=None, out=None, stream=None):
     """Ablation only (not the library's backward): the backward with FP32
-    atomics for dQ (``atomic_mask=1``), dbias (2) or both (3) instead of the
-    ordered single-writer partials.  The atomically added gradients are not
-    bitwise reproducible between calls.  Returns (dq, dk, dv, dbias) in bf16."""
+    atomics for dQ (``atomic_mask=1``), dbias (2) or both (3), or TMA bulk
+    reductions for dQ (4; 6 with atomic dbias), instead of the ordered
+    single-writer partials.  The gradients added that way are not bitwise
+    reproducible between calls.  Returns (dq, dk, dv, dbias) in bf16."""
     s = shape_of(q)
     B, No, H, N, D = q.shape
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):

@@ -190,8 +190,9 @@ def test_combine_ranks_two_gloo_ranks():
 def test_atomic_ablation_workspace_and_mask_checks(lib):
     """The non-deterministic ablation entry point: its workspace holds FP32
     accumulators instead of the partials of the operands it adds atomically,
-    and any mask other than 1 (dQ), 2 (dbias) or 3 (dbias and dQ) is
-    rejected before anything is launched."""
+    and any mask other than 1 (atomic dQ), 2 (atomic dbias), 3 (both), 4
+    (bulk-reduced dQ) or 6 (bulk dQ, atomic dbias) is rejected before
+    anything is launched."""
     s = T.Shape(1, 136, 136, 2, 32, 0)
     r256 = lambda x: (x + 255) // 256 * 256
     slices, jq, jk = 136 * 2, 2, 2
@@ -204,7 +205,9 @@ def test_atomic_ablation_workspace_and_mask_checks(lib):
     assert lib.triattn_bwd_atomic_workspace_bytes(ctypes.byref(s), 2) == base + r256(dq_part) + r256(db_acc)
     assert lib.triattn_bwd_atomic_workspace_bytes(ctypes.byref(s), 3) == base + r256(dq_acc) + r256(db_acc)
     assert lib.triattn_bwd_workspace_bytes(ctypes.byref(s)) == base + r256(dq_part) + r256(db_part)
-    for bad in (0, 4, -1):
+    assert lib.triattn_bwd_atomic_workspace_bytes(ctypes.byref(s), 4) == base + r256(dq_acc) + r256(db_part)
+    assert lib.triattn_bwd_atomic_workspace_bytes(ctypes.byref(s), 6) == base + r256(dq_acc) + r256(db_acc)
+    for bad in (0, 5, 7, 8, -1):
         assert lib.triattn_bwd_atomic_workspace_bytes(ctypes.byref(s), bad) == 0
         fake = ctypes.c_void_p(1 << 40)
         args = [ctypes.byref(s)] + [fake] * 13 + [bad, fake, ctypes.c_size_t(1 << 40), None]

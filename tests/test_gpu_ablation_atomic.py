@@ -1,5 +1,6 @@
 """Non-deterministic ablation of the backward (FP32 atomics for dQ, dbias, or
-both, instead of the ordered single-writer partials; "TurboPairFormer",
+both, or TMA bulk reductions for dQ, instead of the ordered single-writer
+partials; "TurboPairFormer",
 Table 12).  It must meet the same error bars against the FP64 oracle, and the
 outputs that do not pass through atomics must be bitwise those of the ordered
 backward."""
@@ -24,7 +25,9 @@ def _lib():
 
 @pytest.mark.parametrize("case", [(1, 136, 2, 32, "random"), (2, 200, 2, 16, "tail")],
                          ids=["N136D32", "B2N200D16"])
-@pytest.mark.parametrize("atomic_mask", [T.ATOMIC_DQ, T.ATOMIC_DBIAS, T.ATOMIC_DBIAS_DQ], ids=["dq", "dbias", "dbias_dq"])
+@pytest.mark.parametrize("atomic_mask", [T.ATOMIC_DQ, T.ATOMIC_DBIAS, T.ATOMIC_DBIAS_DQ, T.BULK_DQ,
+                                         T.BULK_DQ_ATOMIC_DBIAS],
+                         ids=["dq", "dbias", "dbias_dq", "bulk_dq", "bulk_dq_dbias"])
 def test_atomic_ablation_parity(case, atomic_mask):
     B, N, H, D, mk = case
     w = S.custom(B, N, H, D, name="atom", mask=mk, mask_frac=0.1)
@@ -38,7 +41,7 @@ def test_atomic_ablation_parity(case, atomic_mask):
     assert torch.equal(dk, ordered["dk"]) and torch.equal(dv, ordered["dv"])
     if atomic_mask == T.ATOMIC_DBIAS:
         assert torch.equal(dq, ordered["dq"])
-    if atomic_mask == T.ATOMIC_DQ:
+    if atomic_mask in (T.ATOMIC_DQ, T.BULK_DQ):
         assert torch.equal(db, ordered["dbias"])
     out = dict(ordered)
     out.update(dq=dq, dk=dk, dv=dv, dbias=db)

@@ -6,14 +6,24 @@
 // [B, N_o, H, N, D]; Figure 9 and the Abstract describe the saved BF16
 // output-rounding residual used by the backward.
 //
-// One CTA owns (b, h, a 128-row query tile, a group of GF = 4 outer slices).
-// The four slices use the same bias tile for every key tile, so each bias
-// tile is loaded once into shared memory and read by four warpgroups.  Key
-// tiles are 64 wide, so the four slices each get their own softmax
-// warpgroup and their own score, P and O columns in TMEM.
+// A work item is (b, h, a 128-row query tile, a group of GF = 4 outer
+// slices).  The four slices use the same bias tile for every key tile, so
+// each bias tile is loaded once into shared memory and read by four
+// warpgroups.  Key tiles are 64 wide, so the four slices each get their own
+// softmax warpgroup and their own score, P and O columns in TMEM.
+//
+// The kernel is persistent: one CTA per SM takes items blockIdx.x,
+// blockIdx.x + gridDim.x, ... (the order a plain grid would run them in, so
+// neighbouring CTAs still share K, V and bias tiles in L2).  The rings run on
+// across items: the producer loads the next item's Q tiles (two stages) and
+// first key tiles while the softmax warps finish the current item, and the
+// next item's S MMAs start as soon as their operands are there; only its
+// first P.V waits until the epilogue has read the current item's O out of
+// TMEM.  A CTA per item spent a quarter of its time filling and draining
+// its pipeline.
 //
 // Warp roles (20 warps):
-//   warp 0       TMA producer: the four Q tiles once; per 64-key tile one
+//   warp 0       TMA producer: per item the four Q tiles; per 64-key tile one
 //                bias tile with the four slices' key-mask records of that
 //                tile, and per slice one K and one V tile (rings of 3 stages).
 //   warps 1, 2   tcgen05 MMA issuers (converged warps, one elected lane
@@ -47,6 +57,7 @@
 //
 // A group may extend past N_o (N_o not a multiple of 4): its extra slices
 // read records that mask every key, and nothing of theirs is stored.
+#include <algorithm>
 #include <type_traits>
 
 #include "kernels.cuh"
@@ -78,8 +89,8 @@ template <int D>
 struct FwdSmem {
   static constexpr int kTileQ = BM * D * 2;                  // one Q tile (128 rows x D bf16)
   static constexpr int kTileKV = BN * D * 2;                 // one K / V tile (64 keys x D bf16)
-  static constexpr int kQ = 0;                               // GF Q tiles
-  static constexpr int kK = kQ + GF * kTileQ;                // GF x NSLOT K tiles
+  static constexpr int kQ = 0;                               // 2 stages x GF Q tiles
+  static constexpr int kK = kQ + 2 * GF * kTileQ;            // GF x NSLOT K tiles
   static constexpr int kV = kK + GF * NSLOT * kTileKV;       // GF x NSLOT V tiles
   static constexpr int kBias = kV + GF * NSLOT * kTileKV;    // NBIAS x [128 q][64 k] bf16, SW128
   static constexpr int kRec = kBias + NBIAS * BM * BN * 2;   // NBIAS x GF key-mask records
@@ -95,7 +106,9 @@ struct FwdBars {
   uint64_t v_full[GF][NSLOT], v_empty[GF][NSLOT];
   uint64_t b_full[NBIAS], b_empty[NBIAS];
   uint64_t s_full[GF], s_cons[GF], p_full[GF], pv_done[GF];
-  uint64_t q_full, all_done;
+  uint64_t o_free[GF];          // the item's O read out of TMEM by the epilogue
+  uint64_t q_full[2], q_empty[2];
+  uint64_t never;               // completes no phase: a parity-1 wait on it always passes
   uint32_t tmem_slot;
   int abort;
 };
@@ -108,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
                const uint8_t* __restrict__ mrec, uint16_t* __restrict__ out_o, float* __restrict__ out_lse,
-               uint16_t* __restrict__ out_resid, int N_o, int N, int H, int test_starve, WaitCtl wc) {
+               uint16_t* __restrict__ out_resid, int N_o, int N, int H, int BH, int test_starve, WaitCtl wc) {
   using L = FwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -118,13 +131,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int qtile = blockIdx.x;
-  const int o0 = blockIdx.y * GF;
-  const int bh = blockIdx.z;
-  const int b = bh / H;
-  const int h = bh - b * H;
+  const int JQ = (N + BM - 1) / BM;
+  const int NG = (N_o + GF - 1) / GF;                     // outer groups
   const int JK = (N + BN - 1) / BN;
-  const int rec_slices = static_cast<int>(gridDim.z / H) * N_o + GF;  // records per key tile
+  const int rec_slices = (BH / H) * N_o + GF;             // records per key tile
+  // Work items, in the order of a (JQ, NG, B*H) grid: this CTA takes items
+  // blockIdx.x, blockIdx.x + gridDim.x, ...; nitems of them.
+  const int total = JQ * NG * BH;
+  const int nitems = blockIdx.x < total ? (total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
+  const int ntiles = nitems * JK;                         // key tiles over all of this CTA's items
+  struct Item { int qtile, o0, bh, b, h; };
+  auto item_of = [&](int k) {
+    const int it = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    Item r;
+    r.qtile = it % JQ;
+    r.o0 = ((it / JQ) % NG) * GF;
+    r.bh = it / (JQ * NG);
+    r.b = r.bh / H;
+    r.h = r.bh - r.b * H;
+    return r;
+  };
 
   if (tid == 0) {
     for (int g = 0; g < GF; ++g) {
@@ -138,13 +164,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_cons[g], 128);
       mbar_init(&bars->p_full[g], 128);
       mbar_init(&bars->pv_done[g], 1);
+      mbar_init(&bars->o_free[g], 128);
     }
     for (int i = 0; i < NBIAS; ++i) {
       mbar_init(&bars->b_full[i], 1);
       mbar_init(&bars->b_empty[i], kSoftmax);
     }
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->all_done, 2);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 2);  // both issuers, after an item's last S
+    }
+    mbar_init(&bars->never, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -164,33 +194,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_bias);
-      const int row0 = qtile * BM;
-      mbar_expect_tx(&bars->q_full, GF * L::kTileQ);
-      for (int g = 0; g < GF; ++g)
-        tma_load_3d(sm + L::kQ + g * L::kTileQ, &tm_q, &bars->q_full, 0, row0, (b * N_o + o0 + g) * H + h);
-      for (int j = 0; j < JK && !*abort; ++j) {
-        const int bst = j % NBIAS;
-        if (!mbar_wait(&bars->b_empty[bst], ((j / NBIAS) & 1) ^ 1, wc, abort)) break;
-        mbar_expect_tx(&bars->b_full[bst], BM * BN * 2 + (mrec != nullptr ? GF * kFwdMaskRec : 0));
-        tma_load_3d(sm + L::kBias + bst * (BM * BN * 2), &tm_bias, &bars->b_full[bst], j * BN, row0, bh);
-        if (mrec != nullptr)  // the four slices' records of tile j are contiguous
-          bulk_load(sm + L::kRec + bst * (GF * kFwdMaskRec), mrec + (static_cast<size_t>(j) * rec_slices + b * N_o + o0) * kFwdMaskRec,
-                    GF * kFwdMaskRec, &bars->b_full[bst]);
-        const int slot = j % NSLOT;
-        const uint32_t par = ((j / NSLOT) & 1) ^ 1;
-        bool go = true;
-        for (int g = 0; g < GF && go; ++g) {
-          const int boh = (b * N_o + o0 + g) * H + h;
-          if (!mbar_wait(&bars->k_empty[g][slot], par, wc, abort)) { go = false; break; }
-          if (!(test_starve && j == 0 && g == 0)) {
-            mbar_expect_tx(&bars->k_full[g][slot], L::kTileKV);
-            tma_load_3d(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], 0, j * BN, boh);
+      bool go = true;
+      int bst = 0, bpar = 0, slot = 0, spar = 0;  // ring positions of the current key tile
+      for (int k = 0; k < nitems && go && !*abort; ++k) {
+        const Item w = item_of(k);
+        const int row0 = w.qtile * BM;
+        const int qs = k & 1;
+        if (!mbar_wait(&bars->q_empty[qs], ((k >> 1) & 1) ^ 1, wc, abort)) break;
+        mbar_expect_tx(&bars->q_full[qs], GF * L::kTileQ);
+        for (int g = 0; g < GF; ++g)
+          tma_load_3d(sm + L::kQ + (qs * GF + g) * L::kTileQ, &tm_q, &bars->q_full[qs], 0, row0,
+                      (w.b * N_o + w.o0 + g) * H + w.h);
+        for (int j = 0; j < JK && go; ++j) {
+          if (!mbar_wait(&bars->b_empty[bst], bpar ^ 1, wc, abort)) { go = false; break; }
+          mbar_expect_tx(&bars->b_full[bst], BM * BN * 2 + (mrec != nullptr ? GF * kFwdMaskRec : 0));
+          tma_load_3d(sm + L::kBias + bst * (BM * BN * 2), &tm_bias, &bars->b_full[bst], j * BN, row0, w.bh);
+          if (mrec != nullptr)  // the four slices' records of tile j are contiguous
+            bulk_load(sm + L::kRec + bst * (GF * kFwdMaskRec),
+                      mrec + (static_cast<size_t>(j) * rec_slices + w.b * N_o + w.o0) * kFwdMaskRec, GF * kFwdMaskRec,
+                      &bars->b_full[bst]);
+          const uint32_t par = spar ^ 1;
+          for (int g = 0; g < GF && go; ++g) {
+            const int boh = (w.b * N_o + w.o0 + g) * H + w.h;
+            if (!mbar_wait(&bars->k_empty[g][slot], par, wc, abort)) { go = false; break; }
+            if (!(test_starve && k == 0 && j == 0 && g == 0)) {
+              mbar_expect_tx(&bars->k_full[g][slot], L::kTileKV);
+              tma_load_3d(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], 0, j * BN,
+                          boh);
+            }
+            if (!mbar_wait(&bars->v_empty[g][slot], par, wc, abort)) { go = false; break; }
+            mbar_expect_tx(&bars->v_full[g][slot], L::kTileKV);
+            tma_load_3d(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], 0, j * BN, boh);
           }
-          if (!mbar_wait(&bars->v_empty[g][slot], par, wc, abort)) { go = false; break; }
-          mbar_expect_tx(&bars->v_full[g][slot], L::kTileKV);
-          tma_load_3d(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], 0, j * BN, boh);
+          if (++bst == NBIAS) { bst = 0; bpar ^= 1; }
+          if (++slot == NSLOT) { slot = 0; spar ^= 1; }
         }
-        if (!go) break;
       }
     }
   } else if (warp <= 2) {
@@ -206,43 +244,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKb = smem_desc(smem_u32(sm + L::kK), 16, kSbo, kSwz);
     const uint64_t dVb = smem_desc(smem_u32(sm + L::kV), 16, kSbo, kSwz);
     const int g0 = warp - 1;  // slices g0 and g0 + 2 (one warpgroup pair)
-    auto issue_s = [&](int g, int slot) {  // S_g = Q_g K^T into the slice's score columns
+    // S_g of a key tile (ring slot `slot`, Q stage `qs`; `last` = the item's
+    // last key tile) into the slice's score columns
+    auto issue_s = [&](int g, int slot, int qs, bool last) {
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + 128 * g, dQb + g * kTileQ16 + 2 * kk, dKb + (g * NSLOT + slot) * kTile16 + 2 * kk, idS,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + 128 * g, dQb + (qs * GF + g) * kTileQ16 + 2 * kk, dKb + (g * NSLOT + slot) * kTile16 + 2 * kk,
+                 idS, kk > 0 ? 1u : 0u);
         mma_commit(&bars->s_full[g]);
         mma_commit(&bars->k_empty[g][slot]);
+        // the item's last S read its Q stage
+        if (last && g == g0 + 2) mma_commit(&bars->q_empty[qs]);
       }
       __syncwarp();
     };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wc, abort));
-    for (int g = g0; g < GF && ok; g += 2) {  // S_g(0)
+    bool ok = ntiles > 0;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[0], 0, wc, abort));
+    for (int g = g0; g < GF && ok; g += 2) {  // S_g of tile 0
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[g][0], 0, wc, abort))) { ok = false; break; }
       tc_fence_after();
-      issue_s(g, 0);
+      issue_s(g, 0, 0, JK == 1);
     }
-    for (int j = 0; j < JK && ok; ++j) {
-      const int slot = j % NSLOT, slot1 = (j + 1) % NSLOT;
-      if (j + 1 < JK) {
+    // (item k, tile j) of key tile t, its ring slot and phase; the same for t + 1
+    int j = 0, k = 0, slot = 0, spar = 0;
+    int j1 = 1, k1 = 0, slot1 = 1, spar1 = 0;
+    if (j1 == JK) { j1 = 0; k1 = 1; }
+    if (slot1 == NSLOT) { slot1 = 0; spar1 = 1; }
+    for (int t = 0; t < ntiles && ok; ++t) {
+      if (t + 1 < ntiles) {
+        if (j1 == 0) {  // the next item's Q tiles
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full[k1 & 1], (k1 >> 1) & 1, wc, abort))) {
+            ok = false;
+            break;
+          }
+        }
         for (int g = g0; g < GF; g += 2) {
-          // S(j) of slice g is in registers; K(j+1) loaded
+          // S(t) of slice g is in registers; K(t+1) loaded
           const uint32_t wb[2] = {smem_u32(&bars->s_cons[g]), smem_u32(&bars->k_full[g][slot1])};
-          const uint32_t wp[2] = {static_cast<uint32_t>(j & 1), static_cast<uint32_t>(((j + 1) / NSLOT) & 1)};
+          const uint32_t wp[2] = {static_cast<uint32_t>(t & 1), static_cast<uint32_t>(spar1)};
           if (!mbar_wait_all(wb, wp, wc, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_s(g, slot1);
+          issue_s(g, slot1, k1 & 1, j1 == JK - 1);
         }
         if (!ok) break;
       }
       for (int g = g0; g < GF; g += 2) {
-        // P(j) of slice g in TMEM; V(j) loaded
-        const uint32_t wb[2] = {smem_u32(&bars->p_full[g]), smem_u32(&bars->v_full[g][slot])};
-        const uint32_t wp[2] = {static_cast<uint32_t>(j & 1), static_cast<uint32_t>((j / NSLOT) & 1)};
+        // P(t) of slice g in TMEM; V(t) loaded; on an item's first tile the
+        // previous item's O has been read out (parity 1 passes for item 0)
+        const uint32_t wb[3] = {smem_u32(&bars->p_full[g]), smem_u32(&bars->v_full[g][slot]),
+                                smem_u32(j == 0 && k > 0 ? &bars->o_free[g] : &bars->never)};
+        const uint32_t wp[3] = {static_cast<uint32_t>(t & 1), static_cast<uint32_t>(spar),
+                                j == 0 && k > 0 ? static_cast<uint32_t>((k - 1) & 1) : 1u};
         if (!mbar_wait_all(wb, wp, wc, abort)) {
           ok = false;
           break;
@@ -258,9 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      // advance both tile positions by one
+      j = j1; k = k1; slot = slot1; spar = spar1;
+      if (++j1 == JK) { j1 = 0; ++k1; }
+      if (++slot1 == NSLOT) { slot1 = 0; spar1 ^= 1; }
     }
-    if (elect_one()) mma_commit(&bars->all_done);
-    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax warpgroups
     const int g = (warp - 4) >> 2;        // slice of this warpgroup
@@ -269,214 +327,221 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float inv_sqrt_d = rsqrtf(static_cast<float>(D));
 
-    const int q = qtile * BM + r;
-    const bool live_slice = o0 + g < N_o;
     const bool has_rec = mrec != nullptr;
-    const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + q;
-
-    // running base m (natural units) and sum l of this row
-    float m_run = 0.f, l_run = 0.f;
     const float2 c2 = make_float2(inv_sqrt_d * kLog2e, inv_sqrt_d * kLog2e);
     const float2 l2e2 = make_float2(kLog2e, kLog2e);
     const uint32_t tS = tmem + lane_addr + 128 * g;
     bool ok = true;
 
-    for (int j = 0; j < JK && ok; ++j) {
-      const int bst = j % NBIAS;
-      const uint32_t wb[2] = {smem_u32(&bars->b_full[bst]), smem_u32(&bars->s_full[g])};
-      const uint32_t wp[2] = {static_cast<uint32_t>((j / NBIAS) & 1), static_cast<uint32_t>(j & 1)};
-      if (!mbar_wait_all(wb, wp, wc, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // the tile's 64 scores into registers; the score columns are free again
-      // sv0 holds keys [0, 32), sv1 keys [32, 64)
-      uint32_t sv0[32], sv1[32];
-      tmem_ld32x2_wait(tS, sv0, tS + 32, sv1);
-      tc_fence_before();
-      mbar_arrive(&bars->s_cons[g]);
+    for (int k = 0; k < nitems && ok; ++k) {
+      // running base m (natural units) and sum l of this row
+      float m_run = 0.f, l_run = 0.f;
 
-      // P.V(j-1) is complete: the P columns are free and O is up to date
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], (j - 1) & 1, wc, abort))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      for (int j = 0; j < JK && ok; ++j) {
+        const int jj = k * JK + j;  // key tile over all of this CTA's items (ring phases)
+        const int bst = jj % NBIAS;
+        const uint32_t wb[2] = {smem_u32(&bars->b_full[bst]), smem_u32(&bars->s_full[g])};
+        const uint32_t wp[2] = {static_cast<uint32_t>((jj / NBIAS) & 1), static_cast<uint32_t>(jj & 1)};
+        if (!mbar_wait_all(wb, wp, wc, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // the tile's 64 scores into registers; the score columns are free again
+        // sv0 holds keys [0, 32), sv1 keys [32, 64)
+        uint32_t sv0[32], sv1[32];
+        tmem_ld32x2_wait(tS, sv0, tS + 32, sv1);
+        tc_fence_before();
+        mbar_arrive(&bars->s_cons[g]);
 
-      // t = (S / sqrt(D) + bias + mask - m) log2 e in place.  The exact
-      // path (first key tile, or a row of the warp with nothing accumulated
-      // yet) also takes the tile maximum and moves the base to it; later
-      // tiles keep the base and only look at the maximum when the row sum
-      // of the tile exceeds 2^16 (some p > 2^16).
-      const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
-      const uint8_t* rec_s = sm + L::kRec + (bst * GF + g) * kFwdMaskRec;
-      const uint16_t* mk = reinterpret_cast<const uint16_t*>(rec_s);  // this tile's 64 mask values
-      const bool tile_masked = has_rec && *reinterpret_cast<const uint32_t*>(rec_s + BN * 2) != 0u;
-      const bool exact = j == 0 || __any_sync(0xffffffffu, l_run == 0.f);
-      const float2 nb2 = make_float2(-m_run * kLog2e, -m_run * kLog2e);
-      float tm = -INFINITY;
-      // MASKED selects, per key tile (warp-uniform), the version of the loop
-      // that adds the key mask; WITH_MAX also takes the maximum of t
-      auto scores = [&](uint32_t (&sv)[32], const int cc0, auto masked_tile, auto with_max) {
-        constexpr bool MASKED = decltype(masked_tile)::value;
-        constexpr bool WITH_MAX = decltype(with_max)::value;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 8-key chunks
-          const int cc = cc0 + c;
-          const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + sw128(r, cc));
-          const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = c * 8 + 2 * e;
-            const float2 s2 = make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
-            const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
-            float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nb2));
-            if constexpr (MASKED) {  // the pair's two mask values, loaded where they are used
-              const uint32_t mw = *reinterpret_cast<const uint32_t*>(mk + cc * 8 + 2 * e);
-              t = ffma2(make_float2(bf16lo_to_f32(mw), bf16hi_to_f32(mw)), l2e2, t);
+        // P.V(jj-1) is complete: the P columns are free and O is up to date
+        if (jj > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], (jj - 1) & 1, wc, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+
+        // t = (S / sqrt(D) + bias + mask - m) log2 e in place.  The exact
+        // path (first key tile, or a row of the warp with nothing accumulated
+        // yet) also takes the tile maximum and moves the base to it; later
+        // tiles keep the base and only look at the maximum when the row sum
+        // of the tile exceeds 2^16 (some p > 2^16).
+        const uint8_t* bias_s = sm + L::kBias + bst * (BM * BN * 2);
+        const uint8_t* rec_s = sm + L::kRec + (bst * GF + g) * kFwdMaskRec;
+        const uint16_t* mk = reinterpret_cast<const uint16_t*>(rec_s);  // this tile's 64 mask values
+        const bool tile_masked = has_rec && *reinterpret_cast<const uint32_t*>(rec_s + BN * 2) != 0u;
+        const bool exact = j == 0 || __any_sync(0xffffffffu, l_run == 0.f);
+        const float2 nb2 = make_float2(-m_run * kLog2e, -m_run * kLog2e);
+        float tm = -INFINITY;
+        // MASKED selects, per key tile (warp-uniform), the version of the loop
+        // that adds the key mask; WITH_MAX also takes the maximum of t
+        auto scores = [&](uint32_t (&sv)[32], const int cc0, auto masked_tile, auto with_max) {
+          constexpr bool MASKED = decltype(masked_tile)::value;
+          constexpr bool WITH_MAX = decltype(with_max)::value;
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {  // 8-key chunks
+            const int cc = cc0 + c;
+            const uint4 bw = *reinterpret_cast<const uint4*>(bias_s + sw128(r, cc));
+            const uint32_t bws[4] = {bw.x, bw.y, bw.z, bw.w};
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = c * 8 + 2 * e;
+              const float2 s2 = make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
+              const float2 b2 = make_float2(bf16lo_to_f32(bws[e]), bf16hi_to_f32(bws[e]));
+              float2 t = ffma2(s2, c2, ffma2(b2, l2e2, nb2));
+              if constexpr (MASKED) {  // the pair's two mask values, loaded where they are used
+                const uint32_t mw = *reinterpret_cast<const uint32_t*>(mk + cc * 8 + 2 * e);
+                t = ffma2(make_float2(bf16lo_to_f32(mw), bf16hi_to_f32(mw)), l2e2, t);
+              }
+              if constexpr (WITH_MAX) tm = fmax3(tm, t.x, t.y);
+              sv[k] = __float_as_uint(t.x);
+              sv[k + 1] = __float_as_uint(t.y);
             }
-            if constexpr (WITH_MAX) tm = fmax3(tm, t.x, t.y);
-            sv[k] = __float_as_uint(t.x);
-            sv[k + 1] = __float_as_uint(t.y);
           }
-        }
-      };
-      auto pass1 = [&](auto with_max) {
-        if (tile_masked) {
-          scores(sv0, 0, std::true_type{}, with_max);
-          scores(sv1, 4, std::true_type{}, with_max);
-        } else {
-          scores(sv0, 0, std::false_type{}, with_max);
-          scores(sv1, 4, std::false_type{}, with_max);
-        }
-      };
-      if (exact) pass1(std::true_type{});
-      else pass1(std::false_type{});
-      mbar_arrive(&bars->b_empty[bst]);  // this thread's last read of the bias tile
+        };
+        auto pass1 = [&](auto with_max) {
+          if (tile_masked) {
+            scores(sv0, 0, std::true_type{}, with_max);
+            scores(sv1, 4, std::true_type{}, with_max);
+          } else {
+            scores(sv0, 0, std::false_type{}, with_max);
+            scores(sv1, 4, std::false_type{}, with_max);
+          }
+        };
+        if (exact) pass1(std::true_type{});
+        else pass1(std::false_type{});
+        mbar_arrive(&bars->b_empty[bst]);  // this thread's last read of the bias tile
 
 
-      // p = 2^(t - sh), the row sum, and P (BF16) into the P columns, 32
-      // keys at a time; returns the row sum
-      auto expo = [&](const float sh, auto shifted) -> float {
-        constexpr bool SHIFT = decltype(shifted)::value;
-        const float2 sh2 = make_float2(-sh, -sh);
-        float2 ls = make_float2(0.f, 0.f);
-        {
-          uint32_t pw[16];
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            float2 t = make_float2(__uint_as_float(sv0[k]), __uint_as_float(sv0[k + 1]));
-            if constexpr (SHIFT) t = fadd2(t, sh2);
-            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            ls = fadd2(ls, p);
-            pw[k / 2] = pack_bf16x2(p.x, p.y);
+        // p = 2^(t - sh), the row sum, and P (BF16) into the P columns, 32
+        // keys at a time; returns the row sum
+        auto expo = [&](const float sh, auto shifted) -> float {
+          constexpr bool SHIFT = decltype(shifted)::value;
+          const float2 sh2 = make_float2(-sh, -sh);
+          float2 ls = make_float2(0.f, 0.f);
+          {
+            uint32_t pw[16];
+  #pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              float2 t = make_float2(__uint_as_float(sv0[k]), __uint_as_float(sv0[k + 1]));
+              if constexpr (SHIFT) t = fadd2(t, sh2);
+              const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+              ls = fadd2(ls, p);
+              pw[k / 2] = pack_bf16x2(p.x, p.y);
+            }
+            tmem_st16(tS + kTP, pw);
           }
-          tmem_st16(tS + kTP, pw);
-        }
-        {
-          uint32_t pw[16];
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            float2 t = make_float2(__uint_as_float(sv1[k]), __uint_as_float(sv1[k + 1]));
-            if constexpr (SHIFT) t = fadd2(t, sh2);
-            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            ls = fadd2(ls, p);
-            pw[k / 2] = pack_bf16x2(p.x, p.y);
+          {
+            uint32_t pw[16];
+  #pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              float2 t = make_float2(__uint_as_float(sv1[k]), __uint_as_float(sv1[k + 1]));
+              if constexpr (SHIFT) t = fadd2(t, sh2);
+              const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+              ls = fadd2(ls, p);
+              pw[k / 2] = pack_bf16x2(p.x, p.y);
+            }
+            tmem_st16(tS + kTP + 16, pw);
           }
-          tmem_st16(tS + kTP + 16, pw);
-        }
-        return ls.x + ls.y;
-      };
-      // Rebase this row to sh (the maximum of its t values, or 0): m moves
-      // by sh, O and l are scaled by 2^-sh when something is accumulated.
-      // Returns the scale.
-      auto rebase = [&](const float sh) -> float {
-        const float a = (l_run > 0.f && sh != 0.f) ? ex2_approx(-sh) : 1.f;
-        m_run += sh * kLn2;
-        if (__any_sync(0xffffffffu, a != 1.f)) {
-          const uint32_t tO = tS + kTO;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t ov[16];
-            tmem_ld16_wait(tO + c0, ov);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * a);
-            tmem_st16(tO + c0, ov);
+          return ls.x + ls.y;
+        };
+        // Rebase this row to sh (the maximum of its t values, or 0): m moves
+        // by sh, O and l are scaled by 2^-sh when something is accumulated.
+        // Returns the scale.
+        auto rebase = [&](const float sh) -> float {
+          const float a = (l_run > 0.f && sh != 0.f) ? ex2_approx(-sh) : 1.f;
+          m_run += sh * kLn2;
+          if (__any_sync(0xffffffffu, a != 1.f)) {
+            const uint32_t tO = tS + kTO;
+  #pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t ov[16];
+              tmem_ld16_wait(tO + c0, ov);
+  #pragma unroll
+              for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * a);
+              tmem_st16(tO + c0, ov);
+            }
           }
-        }
-        return a;
-      };
-      float alpha = 1.f, lsum;
-      if (exact) {
-        // new base at the tile maximum: on the first tile, when the maximum
-        // overshoots the base (P would grow past 2^8), or when nothing is
-        // accumulated yet and it lies far below the base
-        const float sh =
-            (tm != -INFINITY && (j == 0 || tm > kRescaleThresh || (l_run == 0.f && tm < kLowThresh))) ? tm : 0.f;
-        alpha = rebase(sh);
-        lsum = expo(sh, std::true_type{});
-      } else {
-        lsum = expo(0.f, std::false_type{});
-        const bool need = !(lsum <= kSumThresh);
-        if (__any_sync(0xffffffffu, need)) {
-          // rare: rebase the rows whose sum overflowed to their tile maximum
-          float mx = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) mx = fmax3(mx, __uint_as_float(sv0[k]), __uint_as_float(sv0[k + 1]));
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) mx = fmax3(mx, __uint_as_float(sv1[k]), __uint_as_float(sv1[k + 1]));
-          const float sh = need ? mx : 0.f;
+          return a;
+        };
+        float alpha = 1.f, lsum;
+        if (exact) {
+          // new base at the tile maximum: on the first tile, when the maximum
+          // overshoots the base (P would grow past 2^8), or when nothing is
+          // accumulated yet and it lies far below the base
+          const float sh =
+              (tm != -INFINITY && (j == 0 || tm > kRescaleThresh || (l_run == 0.f && tm < kLowThresh))) ? tm : 0.f;
           alpha = rebase(sh);
           lsum = expo(sh, std::true_type{});
-        }
-      }
-      l_run = l_run * alpha + lsum;
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[g]);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->all_done, 0, wc, abort))) {
-      tc_fence_after();
-      float ov[D];
-      {
-        const uint32_t tO = tmem + lane_addr + 128 * g + kTO;
-        if constexpr (D == 32) {
-          uint32_t raw[32];
-          tmem_ld32_wait(tO, raw);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(raw[e]);
         } else {
-          uint32_t raw[16];
-          tmem_ld16_wait(tO, raw);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) ov[e] = __uint_as_float(raw[e]);
+          lsum = expo(0.f, std::false_type{});
+          const bool need = !(lsum <= kSumThresh);
+          if (__any_sync(0xffffffffu, need)) {
+            // rare: rebase the rows whose sum overflowed to their tile maximum
+            float mx = -INFINITY;
+  #pragma unroll
+            for (int k = 0; k < 32; k += 2) mx = fmax3(mx, __uint_as_float(sv0[k]), __uint_as_float(sv0[k + 1]));
+  #pragma unroll
+            for (int k = 0; k < 32; k += 2) mx = fmax3(mx, __uint_as_float(sv1[k]), __uint_as_float(sv1[k + 1]));
+            const float sh = need ? mx : 0.f;
+            alpha = rebase(sh);
+            lsum = expo(sh, std::true_type{});
+          }
+        }
+        l_run = l_run * alpha + lsum;
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[g]);
+      }
+
+      // ------------------------------------------------------------ epilogue of item k
+      // the item's last P.V is complete
+      if (ok && __all_sync(0xffffffffu, mbar_wait(&bars->pv_done[g], (k * JK + JK - 1) & 1, wc, abort))) {
+        tc_fence_after();
+        float ov[D];
+        {
+          const uint32_t tO = tmem + lane_addr + 128 * g + kTO;
+          if constexpr (D == 32) {
+            uint32_t raw[32];
+            tmem_ld32_wait(tO, raw);
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(raw[e]);
+          } else {
+            uint32_t raw[16];
+            tmem_ld16_wait(tO, raw);
+  #pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __uint_as_float(raw[e]);
+          }
+        }
+        // O is in registers: the next item's first P.V may overwrite it
+        tc_fence_before();
+        mbar_arrive(&bars->o_free[g]);
+        const Item w = item_of(k);  // the item's rows: computed here, no registers held in the loop
+        const int q = w.qtile * BM + r;
+        const size_t row = (static_cast<size_t>((w.b * N_o + w.o0 + g) * H + w.h)) * N + q;
+        if (q < N && w.o0 + g < N_o) {
+          const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+          uint32_t ob[D / 2], eb[D / 2];
+  #pragma unroll
+          for (int e = 0; e < D / 2; ++e) {
+            const float y0 = ov[2 * e] * inv, y1 = ov[2 * e + 1] * inv;
+            const uint32_t w = pack_bf16x2(y0, y1);
+            ob[e] = w;
+            eb[e] = pack_bf16x2(y0 - bf16lo_to_f32(w), y1 - bf16hi_to_f32(w));
+          }
+          uint4* op = reinterpret_cast<uint4*>(out_o + row * D);
+  #pragma unroll
+          for (int v4 = 0; v4 < D / 8; ++v4) op[v4] = make_uint4(ob[4 * v4], ob[4 * v4 + 1], ob[4 * v4 + 2], ob[4 * v4 + 3]);
+          if (out_resid != nullptr) {
+            uint4* ep = reinterpret_cast<uint4*>(out_resid + row * D);
+  #pragma unroll
+            for (int v4 = 0; v4 < D / 8; ++v4)
+              ep[v4] = make_uint4(eb[4 * v4], eb[4 * v4 + 1], eb[4 * v4 + 2], eb[4 * v4 + 3]);
+          }
+          out_lse[row] = l_run > 0.f ? m_run + __logf(l_run) : -INFINITY;
         }
       }
-      if (q < N && live_slice) {
-        const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-        uint32_t ob[D / 2], eb[D / 2];
-#pragma unroll
-        for (int e = 0; e < D / 2; ++e) {
-          const float y0 = ov[2 * e] * inv, y1 = ov[2 * e + 1] * inv;
-          const uint32_t w = pack_bf16x2(y0, y1);
-          ob[e] = w;
-          eb[e] = pack_bf16x2(y0 - bf16lo_to_f32(w), y1 - bf16hi_to_f32(w));
-        }
-        uint4* op = reinterpret_cast<uint4*>(out_o + row * D);
-#pragma unroll
-        for (int v4 = 0; v4 < D / 8; ++v4) op[v4] = make_uint4(ob[4 * v4], ob[4 * v4 + 1], ob[4 * v4 + 2], ob[4 * v4 + 3]);
-        if (out_resid != nullptr) {
-          uint4* ep = reinterpret_cast<uint4*>(out_resid + row * D);
-#pragma unroll
-          for (int v4 = 0; v4 < D / 8; ++v4)
-            ep[v4] = make_uint4(eb[4 * v4], eb[4 * v4 + 1], eb[4 * v4 + 2], eb[4 * v4 + 3]);
-        }
-        out_lse[row] = l_run > 0.f ? m_run + __logf(l_run) : -INFINITY;
-      }
-    }
+    }  // item k
   }
 
   tc_fence_before();
@@ -562,11 +627,18 @@ int fwd_smem_bytes() { return FwdSmem<D>::kBytes; }
 
 template <int D>
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  const int JQ = (a.N + BM - 1) / BM;
-  dim3 grid(JQ, (a.N_o + GF - 1) / GF, a.B * a.H);
+  // persistent: one CTA per SM (the shared memory allows one), each taking
+  // every gridDim.x-th item of the (query tile, outer group, b*h) items
+  const long long total = static_cast<long long>((a.N + BM - 1) / BM) * ((a.N_o + GF - 1) / GF) * a.B * a.H;
+  if (total >= (1ll << 31)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(total, sms));
   fwd_kernel<D><<<grid, kThreads, FwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_bias, a.mrec, static_cast<uint16_t*>(a.o), a.lse,
-      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.test_starve, a.wc);
+      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.B * a.H, a.test_starve, a.wc);
   return cudaGetLastError();
 }
 

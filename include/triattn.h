@@ -390,6 +390,26 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The library's tensor-core GEMM, as used by the multiplicative update and
+ * the module (exported so that it can be tested and reused; not one of the
+ * method's operations).  Row-major C[M, N] = op(A) op(B): A is [M, K] with
+ * row stride lda, or [K, M] when ta != 0; B is [K, N] with row stride ldb,
+ * or [N, K] when tb != 0; BF16 operands, FP32 accumulation; C is BF16, or
+ * FP32 when c_f32 != 0, with row stride ldc.  `batch` matrices are sA, sB,
+ * sC elements apart.  Strides are in elements: lda, ldb (and sA, sB when
+ * batch > 1) multiples of 8, A and B 16-byte aligned; C 16-byte aligned
+ * with ldc a multiple of 8 (BF16) or 4 (FP32).  When the output tiles
+ * cannot fill the GPU, K is split into FP32 partials in `workspace` (at
+ * least triattn_gemm_workspace_bytes() bytes, 16-byte aligned; NULL runs
+ * unsplit) that a second kernel adds in fixed order: bitwise reproducible.
+ * Invalid arguments return TRIATTN_ERR_INVALID_ARG before any launch.
+ */
+size_t triattn_gemm_workspace_bytes(int M, int N, int K, int batch);
+triattn_status triattn_gemm(int ta, int tb, int M, int N, int K, const void* A, long long lda, const void* B,
+                            long long ldb, void* C, long long ldc, int c_f32, int batch, long long sA, long long sB,
+                            long long sC, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * kernels set when a bounded wait gives up.  Returns TRIATTN_OK,
  * TRIATTN_ERR_TIMEOUT, or TRIATTN_ERR_CUDA if the synchronisation failed.

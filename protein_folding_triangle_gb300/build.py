@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "noalloc.cu", "module.cu", "trimul.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "noalloc.cu", "module.cu", "trimul.cu", "gemm.cu"]
 HEADERS = ["ptx.cuh", "kernels.cuh", "pairops.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

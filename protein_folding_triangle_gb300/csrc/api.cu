@@ -160,7 +160,7 @@ const char* const kKernelName[kKinds] = {"tri_attn_fwd",     "bwd_preprocess",  
                                          "module_gemm",      "module_ln_bwd",   "module_colsum",
                                          "trimul_ln_in",     "trimul_proj_gemm", "trimul_gate",
                                          "trimul_contract_gemm", "trimul_ln_out", "trimul_out_gate",
-                                         "trimul_colsum"};
+                                         "trimul_colsum",   "gemm"};
 struct TraceRec {
   int kind;
   cudaEvent_t a, b;
@@ -201,6 +201,14 @@ cudaError_t traced(int kind, cudaStream_t s, F launch) {
 
 cudaError_t trace_call(int kind, cudaStream_t s, const std::function<cudaError_t()>& launch) {
   return traced(kind, s, launch);
+}
+
+WaitCtl current_wait_ctl() {
+  int dev = 0;
+  WaitCtl wc;
+  wc.limit_ns = g_wait_limit_ns.load();
+  wc.status = (init_device(&dev) == TRIATTN_OK) ? g_status_ptr[dev] : nullptr;
+  return wc;
 }
 
 namespace {
@@ -445,5 +453,29 @@ int triattn_trace_read(triattn_trace_entry* out, int max_entries) {
 }
 
 void triattn_test_set_starve(int on) { g_test_starve.store(on != 0 ? 1 : 0); }
+
+size_t triattn_gemm_workspace_bytes(int M, int N, int K, int batch) {
+  if (M < 1 || N < 1 || K < 1 || batch < 1) return 0;
+  return gemm_splitk_bytes(M, N, K, batch);
+}
+
+triattn_status triattn_gemm(int ta, int tb, int M, int N, int K, const void* A, long long lda, const void* B,
+                            long long ldb, void* C, long long ldc, int c_f32, int batch, long long sA, long long sB,
+                            long long sC, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || batch < 1 || A == nullptr || B == nullptr || C == nullptr)
+    return TRIATTN_ERR_INVALID_ARG;
+  if (lda < (ta ? M : K) || ldb < (tb ? K : N) || ldc < N) return TRIATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  triattn_status st = init_device(&dev);
+  if (st != TRIATTN_OK) return st;
+  const WaitCtl wc = wait_ctl(dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = traced(kKGemm, s, [&] {
+    return launch_gemm(ta != 0, tb != 0, M, N, K, A, lda, B, ldb, C, ldc, c_f32 != 0, batch, sA, sB, sC, workspace,
+                       workspace_bytes, wc, s);
+  });
+  if (e == cudaErrorInvalidValue) return TRIATTN_ERR_INVALID_ARG;
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+}
 
 }  // extern "C"

@@ -1,0 +1,397 @@
+// BF16 GEMM on the tcgen05 tensor cores (sm_103a), for the pair-feature
+// projections and the per-channel contraction of the triangle multiplicative
+// update ("TurboPairFormer", Figure 12, Table 10) and the projections of the
+// triangle-attention module (Figure 6).
+//
+// Row-major C[M, N] = op(A) op(B) with A [M, K] (or [K, M]) and B [K, N] (or
+// [N, K]), BF16 operands, FP32 accumulation, C in BF16 or FP32; batched over
+// matrices a fixed stride apart; optionally split along K into FP32 partials
+// that a second kernel adds in ascending split order (deterministic, no
+// atomics), for the weight gradients whose K is the pair count.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0     TMA producer: per 64-deep K stage one 128 x 64 A tile and one
+//              BN x 64 B tile (128-byte swizzle; an operand whose M or N runs
+//              contiguously in memory is loaded as 64-wide column blocks), a
+//              ring of 4 stages.
+//   warp 1     MMA issuer: four M = 128, N = BN, K = 16 MMAs per stage into one
+//              of two TMEM accumulators (BN columns each), so the epilogue of
+//              one tile overlaps the MMAs of the next.
+//   warps 2-5  epilogue: thread = accumulator row (TMEM lane); 32-column
+//              chunks converted and stored (BF16 or FP32), ragged rows and
+//              columns masked.
+// Every mbarrier wait is bounded (WaitCtl): a wait that runs out records a
+// timeout in the device status word and the CTA stops.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace triattn {
+namespace {
+
+constexpr int GB_M = 128;   // rows of a tile (TMEM lanes)
+constexpr int GB_K = 64;    // K depth of a stage (one 128-byte swizzle row of BF16)
+constexpr int GB_S = 4;     // stages
+constexpr int kGemmThreads = 192;
+
+struct GemmBars {
+  uint64_t full[GB_S], empty[GB_S];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_slot;
+  int abort;
+};
+
+struct GemmParams {
+  int M, N, K;
+  int batch, ksplit, kchunk;  // K range of split ks: [ks * kchunk, min(K, (ks + 1) * kchunk))
+  int tiles_m, tiles_n;
+  void* C;                    // output (BF16 or FP32), or FP32 partials [ksplit][batch][M][N]
+  long long ldc, strideC;     // elements
+  int c_f32, partial;
+  WaitCtl wc;
+};
+
+template <int BN, bool A_MN, bool B_MN>
+struct GemmSmem {
+  static constexpr int kA = GB_M * GB_K * 2;       // 16 KB
+  static constexpr int kB = BN * GB_K * 2;         // 16 / 32 KB
+  static constexpr int kStage = kA + kB;
+  static constexpr int kBar = GB_S * kStage;
+  static constexpr int kBytes = kBar + 256 + 1024;  // + alignment slack
+  static_assert(kStage % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+};
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, GemmParams p) {
+  using L = GemmSmem<BN, A_MN, B_MN>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GemmBars* bars = reinterpret_cast<GemmBars*>(sm + L::kBar);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl& wc = p.wc;
+
+  const int tiles_mn = p.tiles_m * p.tiles_n;
+  const long long total = static_cast<long long>(tiles_mn) * p.batch * p.ksplit;
+  // tile t: n fastest, then m, then batch, then the K split
+  auto decode = [&](long long t, int& mt, int& nt, int& bt, int& ks) {
+    nt = static_cast<int>(t % p.tiles_n);
+    mt = static_cast<int>((t / p.tiles_n) % p.tiles_m);
+    bt = static_cast<int>((t / tiles_mn) % p.batch);
+    ks = static_cast<int>(t / (static_cast<long long>(tiles_mn) * p.batch));
+  };
+  auto kstages = [&](int ks) {
+    const int kb = ks * p.kchunk, ke = min(p.K, kb + p.kchunk);
+    return (ke - kb + GB_K - 1) / GB_K;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < GB_S; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], 128);
+    }
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_a);
+      prefetch_tmap(&tm_b);
+      int stage = 0, phase = 0;
+      for (long long t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        int mt, nt, bt, ks;
+        decode(t, mt, nt, bt, ks);
+        const int ns = kstages(ks);
+        const int m0 = mt * GB_M, n0 = nt * BN;
+        bool go = true;
+        for (int kk = 0; kk < ns; ++kk) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1, wc, abort)) { go = false; break; }
+          const int k0 = ks * p.kchunk + kk * GB_K;
+          uint8_t* sa = sm + stage * L::kStage;
+          uint8_t* sb = sa + L::kA;
+          mbar_expect_tx(&bars->full[stage], L::kStage);
+          if constexpr (A_MN) {  // A stored [K][M]: two 64-wide M blocks
+            tma_load_3d(sa, &tm_a, &bars->full[stage], m0, k0, bt);
+            tma_load_3d(sa + 64 * 128, &tm_a, &bars->full[stage], m0 + 64, k0, bt);
+          } else {
+            tma_load_3d(sa, &tm_a, &bars->full[stage], k0, m0, bt);
+          }
+          if constexpr (B_MN) {  // B stored [K][N]: BN / 64 blocks of 64 N
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 64 * 128, &tm_b, &bars->full[stage], n0 + 64 * j, k0, bt);
+          } else {
+            tma_load_3d(sb, &tm_b, &bars->full[stage], k0, n0, bt);
+          }
+          if (++stage == GB_S) { stage = 0; phase ^= 1; }
+        }
+        if (!go) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(GB_M, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+    int stage = 0, phase = 0, local = 0;
+    bool ok = true;
+    for (long long t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
+      int mt, nt, bt, ks;
+      decode(t, mt, nt, bt, ks);
+      const int ns = kstages(ks);
+      const int ab = local & 1;
+      // the epilogue has read this accumulator's previous tile (parity 1 passes at first)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[ab], ((local >> 1) & 1) ^ 1, wc, abort))) break;
+      tc_fence_after();
+      for (int kk = 0; kk < ns; ++kk) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[stage], phase, wc, abort))) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(sm + stage * L::kStage), sb = sa + L::kA;
+        if (elect_one()) {
+#pragma unroll
+          for (int k16 = 0; k16 < GB_K / 16; ++k16) {
+            // K-major: the next 16 K columns are 32 bytes further along each
+            // swizzled 128-byte row; MN-major: 16 K rows of 128 bytes further
+            const uint64_t da = A_MN ? smem_desc(sa + k16 * 2048, 64 * 128, 1024, 2) : smem_desc(sa + k16 * 32, 16, 1024, 2);
+            const uint64_t db = B_MN ? smem_desc(sb + k16 * 2048, 64 * 128, 1024, 2) : smem_desc(sb + k16 * 32, 16, 1024, 2);
+            mma_ss(tmem + ab * BN, da, db, idesc, (kk > 0 || k16 > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->empty[stage]);
+          if (kk == ns - 1) mma_commit(&bars->acc_full[ab]);
+        }
+        __syncwarp();
+        if (++stage == GB_S) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2-5)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // accumulator row = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    int local = 0;
+    for (long long t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+      int mt, nt, bt, ks;
+      decode(t, mt, nt, bt, ks);
+      const int ab = local & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[ab], (local >> 1) & 1, wc, abort))) break;
+      tc_fence_after();
+      const int row = mt * GB_M + r;
+      const int n0 = nt * BN;
+      // destination row: the output matrix, or this split's FP32 partial
+      const bool f32 = p.partial || p.c_f32;
+      long long off;
+      if (p.partial)
+        off = ((static_cast<long long>(ks) * p.batch + bt) * p.M + row) * p.N;
+      else
+        off = bt * p.strideC + static_cast<long long>(row) * p.ldc;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32_wait(tmem + lane_addr + ab * BN + c0, v);
+        const int col = n0 + c0;
+        if (row >= p.M || col >= p.N) continue;
+        if (f32) {
+          float* dst = static_cast<float*>(p.C) + off + col;
+          if (col + 32 <= p.N) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              reinterpret_cast<float4*>(dst)[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                              __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (col + e < p.N) dst[e] = __uint_as_float(v[e]);
+          }
+        } else {
+          uint16_t* dst = static_cast<uint16_t*>(p.C) + off + col;
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          if (col + 32 <= p.N) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              reinterpret_cast<uint4*>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (col + e < p.N) dst[e] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->acc_empty[ab]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// out[b][m][n] = sum over ks ascending of part[ks][b][m][n], in FP32, stored
+// BF16 or FP32 with row stride ldc and batch stride strideC.
+__global__ void __launch_bounds__(256) gemm_splitk_reduce_kernel(const float* __restrict__ part, int ksplit, int batch,
+                                                                 int M, int N, void* __restrict__ C, long long ldc,
+                                                                 long long strideC, int c_f32) {
+  const long long n_el = static_cast<long long>(batch) * M * N;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_el;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float acc = part[e];
+    for (int k = 1; k < ksplit; ++k) acc += part[static_cast<long long>(k) * n_el + e];
+    const int n = static_cast<int>(e % N);
+    const long long m = (e / N) % M, b = e / (static_cast<long long>(N) * M);
+    const long long o = b * strideC + m * ldc + n;
+    if (c_f32) static_cast<float*>(C)[o] = acc;
+    else static_cast<uint16_t*>(C)[o] = static_cast<uint16_t>(pack_bf16x2(acc, 0.f) & 0xFFFFu);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 gemm_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over [batch][rows][ld] BF16 (inner extent `inner` of each row),
+// box = box_inner x box_rows, 128-byte swizzle.
+bool gemm_map(CUtensorMap* m, const void* base, long long inner, long long rows, int batch, long long ld,
+              long long stride, unsigned box_inner, unsigned box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = gemm_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const long long bs = batch > 1 ? stride : rows * ld;
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(bs) * 2};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+cudaError_t gemm_launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
+                          cudaStream_t s) {
+  using L = GemmSmem<BN, A_MN, B_MN>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(gemm_kernel<BN, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  });
+  if (attr != cudaSuccess) return attr;
+  gemm_kernel<BN, A_MN, B_MN><<<grid, kGemmThreads, L::kBytes, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+int gemm_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 148;
+  return sms;
+}
+
+struct SplitPlan {
+  int ksplit, kchunk;
+};
+// Split K only when the output tiles cannot fill the GPU: enough splits to
+// give every SM a tile, each at least 8 stages deep.
+SplitPlan split_plan(int M, int N, int K, int batch, int BN, int sms) {
+  const long long tiles = static_cast<long long>(batch) * ((M + GB_M - 1) / GB_M) * ((N + BN - 1) / BN);
+  int ks = 1;
+  if (tiles < sms) ks = static_cast<int>(std::min<long long>((sms + tiles - 1) / tiles, std::max(1, K / (8 * GB_K))));
+  int kchunk = (K + ks - 1) / ks;
+  kchunk = (kchunk + GB_K - 1) / GB_K * GB_K;
+  ks = (K + kchunk - 1) / kchunk;
+  return {ks, kchunk};
+}
+
+}  // namespace
+
+size_t gemm_splitk_bytes(int M, int N, int K, int batch) {
+  const int BN = N > 128 ? 256 : 128;
+  const SplitPlan sp = split_plan(M, N, K, batch, BN, gemm_sms());
+  return sp.ksplit > 1 ? static_cast<size_t>(sp.ksplit) * batch * M * N * 4 : 0;
+}
+
+cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, long long lda, const void* B,
+                        long long ldb, void* C, long long ldc, bool c_f32, int batch, long long sA, long long sB,
+                        long long sC, void* ws, size_t ws_bytes, const WaitCtl& wc, cudaStream_t s) {
+  if (M < 1 || N < 1 || K < 1 || batch < 1) return cudaErrorInvalidValue;
+  // TMA: 16-byte aligned bases and row strides
+  if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) || (lda & 7) || (ldb & 7) ||
+      (batch > 1 && ((sA & 7) || (sB & 7))))
+    return cudaErrorInvalidValue;
+  const int BN = N > 128 ? 256 : 128;
+  const int sms = gemm_sms();
+  SplitPlan sp = split_plan(M, N, K, batch, BN, sms);
+  const size_t need = static_cast<size_t>(sp.ksplit) * batch * M * N * 4;
+  if (sp.ksplit > 1 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u))) {
+    sp.ksplit = 1;
+    sp.kchunk = (K + GB_K - 1) / GB_K * GB_K;
+  }
+  // the epilogue's vector stores need 16-byte aligned rows
+  if (sp.ksplit == 1 && ((reinterpret_cast<uintptr_t>(C) & 15u) || (ldc & (c_f32 ? 3 : 7)) ||
+                         (batch > 1 && (sC & (c_f32 ? 3 : 7)))))
+    return cudaErrorInvalidValue;
+  CUtensorMap tma, tmb;
+  const bool okA = ta ? gemm_map(&tma, A, M, K, batch, lda, sA, 64, 64) : gemm_map(&tma, A, K, M, batch, lda, sA, 64, 128);
+  const bool okB = tb ? gemm_map(&tmb, B, K, N, batch, ldb, sB, 64, static_cast<unsigned>(BN))
+                      : gemm_map(&tmb, B, N, K, batch, ldb, sB, 64, 64);
+  if (!okA || !okB) return cudaErrorInvalidValue;
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.batch = batch;
+  p.ksplit = sp.ksplit;
+  p.kchunk = sp.kchunk;
+  p.tiles_m = (M + GB_M - 1) / GB_M;
+  p.tiles_n = (N + BN - 1) / BN;
+  p.partial = sp.ksplit > 1 ? 1 : 0;
+  p.C = p.partial ? ws : C;
+  p.ldc = ldc;
+  p.strideC = sC;
+  p.c_f32 = c_f32 ? 1 : 0;
+  p.wc = wc;
+  const long long total = static_cast<long long>(p.tiles_m) * p.tiles_n * batch * sp.ksplit;
+  const int grid = static_cast<int>(std::min<long long>(total, sms));
+  const bool amn = ta, bmn = !tb;  // [K][M] A, [K][N] B: M / N contiguous
+  cudaError_t e;
+  if (BN == 256) {
+    if (amn) e = bmn ? gemm_launch_t<256, true, true>(tma, tmb, p, grid, s) : gemm_launch_t<256, true, false>(tma, tmb, p, grid, s);
+    else e = bmn ? gemm_launch_t<256, false, true>(tma, tmb, p, grid, s) : gemm_launch_t<256, false, false>(tma, tmb, p, grid, s);
+  } else {
+    if (amn) e = bmn ? gemm_launch_t<128, true, true>(tma, tmb, p, grid, s) : gemm_launch_t<128, true, false>(tma, tmb, p, grid, s);
+    else e = bmn ? gemm_launch_t<128, false, true>(tma, tmb, p, grid, s) : gemm_launch_t<128, false, false>(tma, tmb, p, grid, s);
+  }
+  if (e != cudaSuccess || !p.partial) return e;
+  const long long n_el = static_cast<long long>(batch) * M * N;
+  const unsigned blocks = static_cast<unsigned>(std::min<long long>((n_el + 255) / 256, static_cast<long long>(sms) * 16));
+  gemm_splitk_reduce_kernel<<<blocks, 256, 0, s>>>(static_cast<const float*>(ws), sp.ksplit, batch, M, N, C, ldc,
+                                                   batch > 1 ? sC : 0, c_f32 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace triattn

@@ -88,11 +88,24 @@ cudaError_t launch_bwd_finish_dbias(const BwdArgs& a, cudaStream_t stream);
 // dbias = bf16(sum over r of parts[r]) in ascending r (outer axis split across GPUs).
 cudaError_t launch_dbias_combine(const float* parts, int R, size_t elems, void* dbias, cudaStream_t stream);
 
+// Row-major C[M, N] = op(A) op(B) on the tensor cores (gemm.cu): A [M, K]
+// (or [K, M] when ta), B [K, N] (or [N, K] when tb), BF16 operands, FP32
+// accumulation, C BF16 or FP32 (c_f32); batched over matrices sA / sB / sC
+// elements apart.  When the output tiles cannot fill the GPU, K is split into
+// FP32 partials in `ws` (gemm_splitk_bytes) added in fixed order by a second
+// kernel; without enough `ws` it runs unsplit.
+cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, long long lda, const void* B,
+                        long long ldb, void* C, long long ldc, bool c_f32, int batch, long long sA, long long sB,
+                        long long sC, void* ws, size_t ws_bytes, const WaitCtl& wc, cudaStream_t s);
+size_t gemm_splitk_bytes(int M, int N, int K, int batch);
+// The bounded-wait control of the current device (status word, time limit).
+WaitCtl current_wait_ctl();
+
 // Kernel kinds of the trace (triattn_trace_enable / triattn_trace_read).
 enum KernelKind {
   kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine, kKFwdPrep,
   kKModLnFwd, kKModLayout, kKModGemm, kKModLnBwd, kKModColSum,
-  kKTmLnIn, kKTmProj, kKTmGate, kKTmContract, kKTmLnOut, kKTmOutGate, kKTmColSum, kKinds
+  kKTmLnIn, kKTmProj, kKTmGate, kKTmContract, kKTmLnOut, kKTmOutGate, kKTmColSum, kKGemm, kKinds
 };
 // Runs `launch` on stream `s`, bracketed by a pair of trace events while
 // tracing is on.

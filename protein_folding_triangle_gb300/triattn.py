@@ -37,7 +37,7 @@ EXPORTED = ("triattn_status_string", "triattn_fwd_workspace_bytes", "triattn_bwd
             "tri_attn_bwd_atomic_ablation", "tri_attn_dbias_combine", "triattn_module_ctx_bytes",
             "triattn_module_workspace_bytes", "tri_attn_module_fwd", "tri_attn_module_bwd",
             "triattn_trimul_ctx_bytes", "triattn_trimul_workspace_bytes", "triattn_trimul_fwd",
-            "triattn_trimul_bwd")
+            "triattn_trimul_bwd", "triattn_gemm_workspace_bytes", "triattn_gemm")
 
 FLAG_DBIAS_FP32 = 1
 
@@ -122,6 +122,12 @@ def _declare(lib):
     lib.triattn_trimul_fwd.restype = ctypes.c_int
     lib.triattn_trimul_bwd.argtypes = [tp] + [vp] * 16 + [ctypes.c_size_t, vp]
     lib.triattn_trimul_bwd.restype = ctypes.c_int
+    ll = ctypes.c_longlong
+    lib.triattn_gemm_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    lib.triattn_gemm_workspace_bytes.restype = ctypes.c_size_t
+    lib.triattn_gemm.argtypes = ([ctypes.c_int] * 5 + [vp, ll, vp, ll, vp, ll, ctypes.c_int, ctypes.c_int, ll, ll, ll,
+                                 vp, ctypes.c_size_t, vp])
+    lib.triattn_gemm.restype = ctypes.c_int
     return lib
 
 
@@ -504,6 +510,34 @@ def triattn_trimul_bwd(z, mask, ln_in_w, w_p, ln_out_w, w_o, ctx, d_out, directi
                                      _stream_ptr(stream))
     _raise(code, "triattn_trimul_bwd")
     return out
+
+
+def gemm(a, b, *, ta: bool = False, tb: bool = False, out_f32: bool = False, out=None, stream=None):
+    """The library's tensor-core GEMM: op(a) @ op(b) for BF16 CUDA tensors,
+    2-D or 3-D (batched, leading dimension), contiguous; op transposes the
+    last two dimensions when ta / tb.  FP32 accumulation; BF16 output, or
+    FP32 with ``out_f32``."""
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16 or not (a.is_cuda and b.is_cuda):
+        raise ValueError("a and b must be CUDA bfloat16 tensors")
+    if a.dim() != b.dim() or a.dim() not in (2, 3) or not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous, both 2-D or both 3-D")
+    batched = a.dim() == 3
+    a3, b3 = (a, b) if batched else (a[None], b[None])
+    batch = a3.shape[0]
+    M, K = (a3.shape[2], a3.shape[1]) if ta else (a3.shape[1], a3.shape[2])
+    Kb, N = (b3.shape[2], b3.shape[1]) if tb else (b3.shape[1], b3.shape[2])
+    if K != Kb or b3.shape[0] != batch:
+        raise ValueError("shapes do not match")
+    dt = torch.float32 if out_f32 else torch.bfloat16
+    c = out if out is not None else torch.empty((batch, M, N), dtype=dt, device=a.device)
+    lib = load()
+    need = int(lib.triattn_gemm_workspace_bytes(M, N, K, batch))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=a.device)
+    code = lib.triattn_gemm(int(ta), int(tb), M, N, K, _ptr(a3), a3.shape[2], _ptr(b3), b3.shape[2], _ptr(c), N,
+                            int(out_f32), batch, a3.shape[1] * a3.shape[2], b3.shape[1] * b3.shape[2], M * N,
+                            _ptr(ws), ctypes.c_size_t(ws.numel()), _stream_ptr(stream))
+    _raise(code, "triattn_gemm")
+    return c if batched else c[0]
 
 
 class TriAttnFunction(torch.autograd.Function):

@@ -417,3 +417,19 @@ def test_chunked_backward_workspace_is_bounded(lib):
     per = lambda c: T.bwd_workspace_bytes(T.Shape(1, c, N, H, D, T.FLAG_DBIAS_FP32))  # noqa: E731
     c = SH.chunk_slices(N, per, 16 * 2 ** 30)
     assert 8 <= c < N and per(c) <= 16 * 2 ** 30 < per(c + 8)
+
+
+def test_gemm_argument_checks(lib):
+    """The tensor-core GEMM rejects bad sizes, strides and null pointers before
+    touching the device; its split-K workspace is 0 for an invalid shape."""
+    fake = ctypes.c_void_p(1 << 20)
+    def call(ta=0, tb=0, M=128, N=128, K=64, lda=64, ldb=128, ldc=128, A=fake, B=fake, C=fake):
+        return lib.triattn_gemm(ta, tb, M, N, K, A, lda, B, ldb, C, ldc, 0, 1, 0, 0, 0, None, 0, None)
+    assert call(M=0) == T.ERR_INVALID_ARG
+    assert call(K=-1) == T.ERR_INVALID_ARG
+    assert call(lda=32) == T.ERR_INVALID_ARG          # lda < K
+    assert call(ta=1, lda=64) == T.ERR_INVALID_ARG    # A is [K, M]: lda < M
+    assert call(ldb=64) == T.ERR_INVALID_ARG          # ldb < N
+    assert call(ldc=64) == T.ERR_INVALID_ARG          # ldc < N
+    assert call(A=None) == T.ERR_INVALID_ARG
+    assert lib.triattn_gemm_workspace_bytes(0, 1, 1, 1) == 0

@@ -18,8 +18,9 @@
 //              of two TMEM accumulators (BN columns each), so the epilogue of
 //              one tile overlaps the MMAs of the next.
 //   warps 2-5  epilogue: thread = accumulator row (TMEM lane); 32-column
-//              chunks converted and stored (BF16 or FP32), ragged rows and
-//              columns masked.
+//              chunks converted (BF16 or FP32), staged in swizzled shared
+//              memory and written by TMA stores (ragged rows and columns
+//              clipped by the output tensor map).
 // Every mbarrier wait is bounded (WaitCtl): a wait that runs out records a
 // timeout in the device status word and the CTA stops.
 #include <cudaTypedefs.h>
@@ -60,13 +61,16 @@ struct GemmSmem {
   static constexpr int kB = BN * GB_K * 2;         // 16 / 32 KB
   static constexpr int kStage = kA + kB;
   static constexpr int kBar = GB_S * kStage;
-  static constexpr int kBytes = kBar + 256 + 1024;  // + alignment slack
+  static constexpr int kStg = kBar + 1024;          // epilogue staging: 4 warps x 2 x 32 x 32 x 4 bytes
+  static constexpr int kBytes = kStg + 4 * 2 * 4096 + 1024;  // + alignment slack
+  static_assert(kBytes <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 };
 
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, GemmParams p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_c, GemmParams p) {
   using L = GemmSmem<BN, A_MN, B_MN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -177,9 +181,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2-5)
+    // Each warp owns 32 accumulator rows (its TMEM lane quarter).  Per
+    // 32-column chunk a lane converts its row, writes it into a swizzled
+    // staging buffer (64-byte rows for BF16, 128-byte rows for FP32), and one
+    // lane stores the 32 x 32 block with TMA (rows and columns past the
+    // matrix are clipped by the tensor map); two buffers per warp.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // accumulator row = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool f32 = p.partial || p.c_f32;
+    uint8_t* stg = sm + L::kStg + quarter * (2 * 4096);
+    int nst = 0;  // TMA stores issued by this warp
     int local = 0;
     for (long long t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       int mt, nt, bt, ks;
@@ -187,52 +199,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int ab = local & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[ab], (local >> 1) & 1, wc, abort))) break;
       tc_fence_after();
-      const int row = mt * GB_M + r;
+      const int m0 = mt * GB_M + quarter * 32;
       const int n0 = nt * BN;
-      // destination row: the output matrix, or this split's FP32 partial
-      const bool f32 = p.partial || p.c_f32;
-      long long off;
-      if (p.partial)
-        off = ((static_cast<long long>(ks) * p.batch + bt) * p.M + row) * p.N;
-      else
-        off = bt * p.strideC + static_cast<long long>(row) * p.ldc;
+      const int zc = p.partial ? ks * p.batch + bt : bt;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
         tmem_ld32_wait(tmem + lane_addr + ab * BN + c0, v);
-        const int col = n0 + c0;
-        if (row >= p.M || col >= p.N) continue;
+        if (n0 + c0 >= p.N) continue;  // the whole chunk is past N (the same for every lane)
+        uint8_t* buf = stg + (nst & 1) * 4096;
+        if (lane == 0) bulk_wait_read_allow1();  // the store that last used this buffer has read it
+        __syncwarp();
         if (f32) {
-          float* dst = static_cast<float*>(p.C) + off + col;
-          if (col + 32 <= p.N) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              reinterpret_cast<float4*>(dst)[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                                              __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (col + e < p.N) dst[e] = __uint_as_float(v[e]);
-          }
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(buf + sw128(lane, c)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         } else {
-          uint16_t* dst = static_cast<uint16_t*>(p.C) + off + col;
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-          if (col + 32 <= p.N) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              reinterpret_cast<uint4*>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (col + e < p.N) dst[e] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
-          }
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tma_store_3d(&tm_c, buf, n0 + c0, m0, zc);
+        ++nst;
       }
+      (void)r;
       tc_fence_before();
       mbar_arrive(&bars->acc_empty[ab]);
     }
+    if (lane == 0) bulk_wait_all();  // the last stores have landed before the kernel ends
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -291,9 +292,26 @@ bool gemm_map(CUtensorMap* m, const void* base, long long inner, long long rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output map: [planes][M][ld] BF16 (64-byte swizzle) or FP32 (128-byte
+// swizzle), box = 32 columns x 32 rows.
+bool gemm_out_map(CUtensorMap* m, void* base, long long N, long long M, long long planes, long long ld,
+                  long long stride, bool f32) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = gemm_encoder();
+  if (enc == nullptr) return false;
+  const int esz = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(planes)};
+  const long long bs = planes > 1 ? stride : M * ld;
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * esz, static_cast<cuuint64_t>(bs) * esz};
+  const cuuint32_t box[3] = {32u, 32u, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, bool A_MN, bool B_MN>
-cudaError_t gemm_launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
-                          cudaStream_t s) {
+cudaError_t gemm_launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p,
+                          int grid, cudaStream_t s) {
   using L = GemmSmem<BN, A_MN, B_MN>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -301,7 +319,7 @@ cudaError_t gemm_launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const Ge
     attr = cudaFuncSetAttribute(gemm_kernel<BN, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   });
   if (attr != cudaSuccess) return attr;
-  gemm_kernel<BN, A_MN, B_MN><<<grid, kGemmThreads, L::kBytes, s>>>(ta, tb, p);
+  gemm_kernel<BN, A_MN, B_MN><<<grid, kGemmThreads, L::kBytes, s>>>(ta, tb, tc, p);
   return cudaGetLastError();
 }
 
@@ -347,7 +365,7 @@ cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, lo
   const int sms = gemm_sms();
   SplitPlan sp = split_plan(M, N, K, batch, BN, sms);
   const size_t need = static_cast<size_t>(sp.ksplit) * batch * M * N * 4;
-  if (sp.ksplit > 1 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u))) {
+  if (sp.ksplit > 1 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u) || (N & 3))) {
     sp.ksplit = 1;
     sp.kchunk = (K + GB_K - 1) / GB_K * GB_K;
   }
@@ -359,7 +377,11 @@ cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, lo
   const bool okA = ta ? gemm_map(&tma, A, M, K, batch, lda, sA, 64, 64) : gemm_map(&tma, A, K, M, batch, lda, sA, 64, 128);
   const bool okB = tb ? gemm_map(&tmb, B, K, N, batch, ldb, sB, 64, static_cast<unsigned>(BN))
                       : gemm_map(&tmb, B, N, K, batch, ldb, sB, 64, 64);
-  if (!okA || !okB) return cudaErrorInvalidValue;
+  CUtensorMap tmc;
+  const bool okC = sp.ksplit > 1 ? gemm_out_map(&tmc, ws, N, M, static_cast<long long>(sp.ksplit) * batch, N,
+                                                static_cast<long long>(M) * N, true)
+                                 : gemm_out_map(&tmc, C, N, M, batch, ldc, sC, c_f32);
+  if (!okA || !okB || !okC) return cudaErrorInvalidValue;
   GemmParams p;
   p.M = M;
   p.N = N;
@@ -380,11 +402,11 @@ cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, lo
   const bool amn = ta, bmn = !tb;  // [K][M] A, [K][N] B: M / N contiguous
   cudaError_t e;
   if (BN == 256) {
-    if (amn) e = bmn ? gemm_launch_t<256, true, true>(tma, tmb, p, grid, s) : gemm_launch_t<256, true, false>(tma, tmb, p, grid, s);
-    else e = bmn ? gemm_launch_t<256, false, true>(tma, tmb, p, grid, s) : gemm_launch_t<256, false, false>(tma, tmb, p, grid, s);
+    if (amn) e = bmn ? gemm_launch_t<256, true, true>(tma, tmb, tmc, p, grid, s) : gemm_launch_t<256, true, false>(tma, tmb, tmc, p, grid, s);
+    else e = bmn ? gemm_launch_t<256, false, true>(tma, tmb, tmc, p, grid, s) : gemm_launch_t<256, false, false>(tma, tmb, tmc, p, grid, s);
   } else {
-    if (amn) e = bmn ? gemm_launch_t<128, true, true>(tma, tmb, p, grid, s) : gemm_launch_t<128, true, false>(tma, tmb, p, grid, s);
-    else e = bmn ? gemm_launch_t<128, false, true>(tma, tmb, p, grid, s) : gemm_launch_t<128, false, false>(tma, tmb, p, grid, s);
+    if (amn) e = bmn ? gemm_launch_t<128, true, true>(tma, tmb, tmc, p, grid, s) : gemm_launch_t<128, true, false>(tma, tmb, tmc, p, grid, s);
+    else e = bmn ? gemm_launch_t<128, false, true>(tma, tmb, tmc, p, grid, s) : gemm_launch_t<128, false, false>(tma, tmb, tmc, p, grid, s);
   }
   if (e != cudaSuccess || !p.partial) return e;
   const long long n_el = static_cast<long long>(batch) * M * N;

@@ -262,10 +262,11 @@ triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* p
  *   out  = o_flat W_o                W_o [HD, C], o_flat[(b, i, j), h D + d] = o[b, i, h, j, d]
  *
  * No projection biases and no gate; the residual update z + out is left to
- * the caller.  The projections are cuBLAS GEMMs (BF16 operands, FP32
- * accumulation); the LayerNorm, the layout changes between the pair layout
- * and the core's, and the LayerNorm's parameter-gradient sums are the
- * library's kernels; the core is tri_attn_fwd / tri_attn_bwd.
+ * the caller.  The projections are the library's tensor-core GEMM
+ * (triattn_gemm: BF16 operands, FP32 accumulation); the LayerNorm, the
+ * layout changes between the pair layout and the core's, and the LayerNorm's
+ * parameter-gradient sums are the library's kernels; the core is
+ * tri_attn_fwd / tri_attn_bwd.
  *
  * Shape: B >= 1, N as for the core (multiple of 8, 8..4096), B*N*N < 2^31,
  * C a multiple of 32 up to 256, H up to 64, D 16 or 32, flags 0.  Otherwise
@@ -283,14 +284,12 @@ triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* p
  *         output residual, o_flat), read by the backward of the same inputs.
  *   workspace  triattn_module_workspace_bytes(shape) bytes, 256-byte
  *         aligned, contents ignored; either call may use it (it also serves
- *         as cuBLAS's workspace and the core backward's).
+ *         for the GEMMs' split-K partials and the core's workspaces).
  *
- * The first call on a host thread and device creates a cuBLAS handle there
- * (cuBLAS's own small allocation); the library keeps it for the thread's
- * lifetime.  Results are bitwise reproducible for a fixed shape and device:
- * the kernels' reductions have a fixed order and cuBLAS runs a fixed
- * configuration without atomics.  Argument errors return before anything is
- * launched; a failed launch or cuBLAS call returns TRIATTN_ERR_CUDA.
+ * Results are bitwise reproducible for a fixed shape and device: every
+ * reduction, the GEMMs' split-K sums included, has a fixed order.  Argument
+ * errors return before anything is launched; a failed launch returns
+ * TRIATTN_ERR_CUDA.
  */
 typedef struct {
   int B;          /* examples */
@@ -329,9 +328,9 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
  *   out = sigmoid(g) * (LayerNorm(X; ln_out_w, ln_out_b) W_o)   W_o [C_h, C_z]
  *
  * No projection biases; the residual update z + out is left to the caller.
- * The projections and the per-channel contraction are cuBLAS GEMMs (BF16
- * operands, FP32 accumulation; the contraction one strided-batched GEMM over
- * the B*C_h channel matrices); the LayerNorms, the gating and masking (with
+ * The projections and the per-channel contraction are the library's
+ * tensor-core GEMM (triattn_gemm: BF16 operands, FP32 accumulation; the
+ * contraction one batched GEMM over the B*C_h channel matrices); the LayerNorms, the gating and masking (with
  * the transposes to and from channel-major operands), the output gate and
  * the parameter-gradient sums are the library's kernels.
  *
@@ -353,12 +352,11 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
  *         and X, the output LayerNorm statistics, its output y, and
  *         u = y W_o), read by the backward of the same inputs.
  *   workspace  triattn_trimul_workspace_bytes(shape) bytes, 256-byte
- *         aligned, contents ignored (also cuBLAS's workspace).
+ *         aligned, contents ignored (also the GEMMs' split-K partials).
  *
- * Like the module entry points, the first call on a host thread and device
- * creates a cuBLAS handle there.  Bitwise reproducible for a fixed shape
- * and device.  Argument errors return before anything is launched; a failed
- * launch or cuBLAS call returns TRIATTN_ERR_CUDA.
+ * Bitwise reproducible for a fixed shape and device.  Argument errors
+ * return before anything is launched; a failed launch returns
+ * TRIATTN_ERR_CUDA.
  */
 #define TRIATTN_TRIMUL_OUTGOING 0
 #define TRIATTN_TRIMUL_INCOMING 1

@@ -68,8 +68,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         list(ex.map(compile_one, zip(srcs, objs)))
     tmp = out + f".tmp{os.getpid()}"
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(exe))), "lib64")
-    cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs + ["-L", cuda_lib, "-lcublas",
-                                                         "-Xlinker", "-rpath=" + cuda_lib]
+    cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs + ["-L", cuda_lib, "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

@@ -9,13 +9,12 @@
 //   o = core(q, k, v, bias, mask)            o      [B, N, H, N, D]
 //   out = o_flat W_o                         o_flat [M, HD], W_o [HD, C]
 //
-// The projections are plain GEMMs (cuBLAS, BF16 in, FP32 accumulate); the
-// LayerNorm, the head scatter / gather between the pair layout and the
-// core's layout, and the column sums of the LayerNorm parameter gradients are
-// the kernels below.  Every reduction has a fixed order, so results are
-// bitwise reproducible (cuBLAS is reproducible for a fixed configuration and
-// workspace).
-#include <cublas_v2.h>
+// The projections are the library's tensor-core GEMM (gemm.cu: BF16 in, FP32
+// accumulate; the weight gradients split along the pair axis into FP32
+// partials added in fixed order); the LayerNorm, the head scatter / gather
+// between the pair layout and the core's layout, and the column sums of the
+// LayerNorm parameter gradients are the kernels below.  Every reduction has
+// a fixed order, so results are bitwise reproducible.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -150,13 +149,13 @@ CtxLayout ctx_layout(const ModDims& d) {
 
 // Scratch of one forward or backward call.
 struct WsLayout2 {
-  size_t blas, w_in_pad, dw_in_pad, p, doflat, dobuf, dq, dk, dv, dbias, dx, pg, pb, core, total;
+  size_t gemm, w_in_pad, dw_in_pad, p, doflat, dobuf, dq, dk, dv, dbias, dx, pg, pb, core, total;
 };
 WsLayout2 ws_layout2(const ModDims& d, const triattn_shape& core) {
   const size_t act = d.B * d.N * d.H * d.N * d.D * 2;
   WsLayout2 w;
   size_t o = 0;
-  w.blas = o;   o += rup(kBlasWorkspace);
+  w.gemm = o;   o += rup(kGemmWorkspace);
   w.w_in_pad = o;  o += rup(d.C * d.Fp * 2);   // W_in with zero columns up to Fp
   w.dw_in_pad = o; o += rup(d.C * d.Fp * 4);   // dW_in, Fp wide
   w.p = o;      o += rup(d.M * d.Fp * 2);  // P (forward) / dP (backward)
@@ -267,8 +266,7 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* cx = static_cast<uint8_t*>(ctx);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cublasHandle_t h = nullptr;
-  if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
+  void* const gws = ws + w.gemm;
   const int M = static_cast<int>(d.M), C = static_cast<int>(d.C), HD = static_cast<int>(d.HD),
             Fp = static_cast<int>(d.Fp);
   float* mean = reinterpret_cast<float*>(cx + c.mean);
@@ -278,11 +276,11 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   if (trace_call(kKModLnFwd, s, [&] { return ln_rows_fwd(d.M, C, z, ln_w, ln_b, cx + c.x, mean, rstd, s); }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // P = x W_in
-  // (through W_in padded to Fp columns: cuBLAS is several times slower on
-  // widths that are not a multiple of 8)
+  // (through W_in padded to Fp columns: the GEMM's TMA tiles need rows whose
+  // length is a multiple of 8 elements)
   uint16_t* w_in_pad = reinterpret_cast<uint16_t*>(ws + w.w_in_pad);
   if (pad_w_in(d, w_in, w_in_pad, s) != cudaSuccess) return TRIATTN_ERR_CUDA;
-  if (gemm_traced(kKModGemm, h, s, false, false, M, Fp, C, cx + c.x, C, w_in_pad, Fp, P, Fp, CUDA_R_16BF) !=
+  if (gemm_traced(kKModGemm, gws, s, false, false, M, Fp, C, cx + c.x, C, w_in_pad, Fp, P, Fp, false) !=
       TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // q, k, v and the bias planes
@@ -299,7 +297,7 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   const uint16_t* o_core = reinterpret_cast<const uint16_t*>(cx + c.o);
   if (merge_heads(d, o_core, o_core, o_core, 1, reinterpret_cast<uint16_t*>(cx + c.oflat), HD, 0, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  return gemm_traced(kKModGemm, h, s, false, false, M, C, HD, cx + c.oflat, HD, w_o, C, out, C, CUDA_R_16BF);
+  return gemm_traced(kKModGemm, gws, s, false, false, M, C, HD, cx + c.oflat, HD, w_o, C, out, C, false);
 }
 
 triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void* z, const void* mask,
@@ -322,13 +320,12 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint8_t* cx = static_cast<const uint8_t*>(ctx);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cublasHandle_t h = nullptr;
-  if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
+  void* const gws = ws + w.gemm;
   const int M = static_cast<int>(d.M), C = static_cast<int>(d.C), HD = static_cast<int>(d.HD),
             Fp = static_cast<int>(d.Fp);
   // out = o_flat W_o:  dW_o = o_flat^T d_out,  d_oflat = d_out W_o^T
-  if (gemm_traced(kKModGemm, h, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, CUDA_R_32F) != TRIATTN_OK ||
-      gemm_traced(kKModGemm, h, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, CUDA_R_16BF) != TRIATTN_OK)
+  if (gemm_traced(kKModGemm, gws, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, true) != TRIATTN_OK ||
+      gemm_traced(kKModGemm, gws, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, false) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   uint16_t* dobuf = reinterpret_cast<uint16_t*>(ws + w.dobuf);
   if (split_heads(d, reinterpret_cast<const uint16_t*>(ws + w.doflat), HD, 0, 1, dobuf, dobuf, dobuf, s) !=
@@ -351,9 +348,9 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   uint16_t* w_in_pad = reinterpret_cast<uint16_t*>(ws + w.w_in_pad);
   float* dw_in_pad = reinterpret_cast<float*>(ws + w.dw_in_pad);
   if (pad_w_in(d, w_in, w_in_pad, s) != cudaSuccess) return TRIATTN_ERR_CUDA;
-  if (gemm_traced(kKModGemm, h, s, true, false, C, Fp, M, cx + c.x, C, dP, Fp, dw_in_pad, Fp, CUDA_R_32F) !=
+  if (gemm_traced(kKModGemm, gws, s, true, false, C, Fp, M, cx + c.x, C, dP, Fp, dw_in_pad, Fp, true) !=
           TRIATTN_OK ||
-      gemm_traced(kKModGemm, h, s, false, true, M, C, Fp, dP, Fp, w_in_pad, Fp, ws + w.dx, C, CUDA_R_32F) !=
+      gemm_traced(kKModGemm, gws, s, false, true, M, C, Fp, dP, Fp, w_in_pad, Fp, ws + w.dx, C, true) !=
           TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   if (trace_call(kKModLayout, s, [&] {

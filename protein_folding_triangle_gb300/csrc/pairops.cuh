@@ -1,10 +1,9 @@
 // Kernels and helpers shared by the pair-tensor layers (the triangle-attention
 // module and the triangle multiplicative update): LayerNorm over the feature
 // axis of a row-major [M, C] pair tensor, forward and backward, the
-// fixed-order sums of the LayerNorm parameter gradients, and the cuBLAS
-// projection GEMMs in row-major terms.
+// fixed-order sums of the LayerNorm parameter gradients, and the traced call
+// of the library's tensor-core GEMM in row-major terms.
 #pragma once
-#include <cublas_v2.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -22,7 +21,7 @@ namespace pairops {
 constexpr int kMaxC = 256;          // LayerNorm: up to 8 features per lane
 constexpr int kLnBlocks = 152 * 5;     // backward grid, one wave; the dgamma / dbeta partial rows depend on it
 constexpr int kLnFwdBlocks = 152 * 8;  // forward grid (no partials): eight blocks per SM
-constexpr size_t kBlasWorkspace = 32u << 20;
+constexpr size_t kGemmWorkspace = 32u << 20;  // split-K partials of the weight-gradient GEMMs
 
 inline bool ln_width_ok(int C) { return C >= 32 && C <= kMaxC && C % 32 == 0; }
 
@@ -281,61 +280,21 @@ inline cudaError_t column_sums(const float* pg, const float* pb, int rows, int C
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- cuBLAS
-// One handle per host thread and device (created on first use, kept for the
-// thread's lifetime), so calls from different threads never share one.
-inline cublasHandle_t blas_handle(int dev) {
-  thread_local cublasHandle_t handles[64] = {};
-  if (handles[dev] == nullptr) {
-    cublasHandle_t h = nullptr;
-    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
-    handles[dev] = h;
-  }
-  return handles[dev];
-}
-
-// The device's cuBLAS handle, bound to this call's stream and a
-// kBlasWorkspace-byte slice of the caller's workspace.
-inline triattn_status blas_for_call(void* blas_ws, cudaStream_t s, cublasHandle_t* out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TRIATTN_ERR_CUDA;
-  cublasHandle_t h = blas_handle(dev);
-  if (h == nullptr) return TRIATTN_ERR_CUDA;
-  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(h, blas_ws, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS)
-    return TRIATTN_ERR_CUDA;
-  *out = h;
-  return TRIATTN_OK;
-}
-
-// Row-major C[M, N] = op(A) op(B), A [M, K] (or [K, M] when ta), B [K, N] (or
-// [N, K] when tb); lda / ldb / ldc are the stored row lengths.  In cuBLAS's
-// column-major terms this is C^T = op(B)^T op(A)^T.  `batch` > 1 repeats it
-// over matrices strideA / strideB / strideC elements apart.
-inline cublasStatus_t gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, const void* A, int lda,
-                              const void* B, int ldb, void* C, int ldc, cudaDataType_t ct, int batch = 1,
-                              long long strideA = 0, long long strideB = 0, long long strideC = 0) {
-  const float one = 1.f, zero = 0.f;
-  const cublasOperation_t opA = ta ? CUBLAS_OP_T : CUBLAS_OP_N, opB = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
-  if (batch == 1)
-    return cublasGemmEx(h, opB, opA, N, M, K, &one, B, CUDA_R_16BF, ldb, A, CUDA_R_16BF, lda, &zero, C, ct, ldc,
-                        CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  return cublasGemmStridedBatchedEx(h, opB, opA, N, M, K, &one, B, CUDA_R_16BF, ldb, strideB, A, CUDA_R_16BF, lda,
-                                    strideA, &zero, C, ct, ldc, strideC, batch, CUBLAS_COMPUTE_32F,
-                                    CUBLAS_GEMM_DEFAULT);
-}
-
-// gemm_rm as one traced launch of kind `kind`.
-inline triattn_status gemm_traced(int kind, cublasHandle_t h, cudaStream_t s, bool ta, bool tb, int M, int N, int K,
-                                  const void* A, int lda, const void* B, int ldb, void* C, int ldc,
-                                  cudaDataType_t ct, int batch = 1, long long strideA = 0, long long strideB = 0,
+// ---------------------------------------------------------------- GEMMs
+// The library's tensor-core GEMM (gemm.cu) as one traced launch of kind
+// `kind`: row-major C[M, N] = op(A) op(B), BF16 operands, FP32 accumulation,
+// C BF16 or FP32; `gemm_ws` (kGemmWorkspace bytes of the caller's workspace)
+// holds the split-K partials of the weight gradients.
+inline triattn_status gemm_traced(int kind, void* gemm_ws, cudaStream_t s, bool ta, bool tb, int M, int N, int K,
+                                  const void* A, int lda, const void* B, int ldb, void* C, int ldc, bool c_f32,
+                                  int batch = 1, long long strideA = 0, long long strideB = 0,
                                   long long strideC = 0) {
-  cublasStatus_t bs = CUBLAS_STATUS_SUCCESS;
+  const WaitCtl wc = current_wait_ctl();
   const cudaError_t e = trace_call(kind, s, [&] {
-    bs = gemm_rm(h, ta, tb, M, N, K, A, lda, B, ldb, C, ldc, ct, batch, strideA, strideB, strideC);
-    return cudaGetLastError();
+    return launch_gemm(ta, tb, M, N, K, A, lda, B, ldb, C, ldc, c_f32, batch, strideA, strideB, strideC, gemm_ws,
+                       kGemmWorkspace, wc, s);
   });
-  return (e == cudaSuccess && bs == CUBLAS_STATUS_SUCCESS) ? TRIATTN_OK : TRIATTN_ERR_CUDA;
+  return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
 }
 
 }  // namespace pairops

@@ -20,9 +20,11 @@
 // projections into the channel-major operands (64 pairs per block through
 // shared memory), the output LayerNorm while transposing X back, the output
 // gate, and their backward passes; the projection GEMMs and the contraction
-// are cuBLAS (BF16 operands, FP32 accumulation).  No floating-point atomics:
-// every reduction has a fixed order.
-#include <cublas_v2.h>
+// are the library's tensor-core GEMM (gemm.cu: BF16 operands, FP32
+// accumulation; the contraction one batched GEMM over the channel matrices,
+// the weight gradients split along the pair axis into FP32 partials added in
+// fixed order).  No floating-point atomics: every reduction has a fixed
+// order.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -464,13 +466,13 @@ TmCtx tm_ctx(const TmDims& d) {
 }
 
 struct TmWs {
-  size_t blas, du, dp, dy, dX, dA, dB, dx, pg_in, pb_in, pg_out, pb_out, total;
+  size_t gemm, du, dp, dy, dX, dA, dB, dx, pg_in, pb_in, pg_out, pb_out, total;
 };
 TmWs tm_ws(const TmDims& d) {
   TmWs w;
   size_t o = 0;
   const size_t cm = d.B * d.Ch * d.NN * 2;
-  w.blas = o;   o += rup(kBlasWorkspace);
+  w.gemm = o;   o += rup(kGemmWorkspace);
   w.du = o;     o += rup(d.M * d.Cz * 2);
   w.dp = o;     o += rup(d.M * d.Fp * 2);
   w.dy = o;     o += rup(d.M * d.Ch * 4);
@@ -569,11 +571,11 @@ cudaError_t by_ch(size_t Ch, F&& f) {
 
 // The contraction as one strided-batched GEMM over the B * C_h channel
 // matrices: C_c = op(P_c) op(Q_c), every matrix N x N, row-major.
-triattn_status contract(cublasHandle_t h, cudaStream_t s, const TmDims& d, bool tp, bool tq, const void* P,
+triattn_status contract(void* gws, cudaStream_t s, const TmDims& d, bool tp, bool tq, const void* P,
                         const void* Q, void* C) {
   const int n = static_cast<int>(d.N);
   const long long st = static_cast<long long>(d.NN);
-  return gemm_traced(kKTmContract, h, s, tp, tq, n, n, n, P, n, Q, n, C, n, CUDA_R_16BF, static_cast<int>(d.B * d.Ch),
+  return gemm_traced(kKTmContract, gws, s, tp, tq, n, n, n, P, n, Q, n, C, n, false, static_cast<int>(d.B * d.Ch),
                      st, st, st);
 }
 
@@ -613,8 +615,7 @@ triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* cx = static_cast<uint8_t*>(ctx);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cublasHandle_t h = nullptr;
-  if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
+  void* const gws = ws + w.gemm;
   const int M = static_cast<int>(d.M), Cz = static_cast<int>(d.Cz), Ch = static_cast<int>(d.Ch),
             F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
   const uint16_t* mk = static_cast<const uint16_t*>(mask);
@@ -631,7 +632,7 @@ triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void*
                            reinterpret_cast<float*>(cx + c.rstd_in), s);
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  if (gemm_traced(kKTmProj, h, s, false, false, M, F, Cz, cx + c.x, Cz, w_p, F, P, Fp, CUDA_R_16BF) != TRIATTN_OK)
+  if (gemm_traced(kKTmProj, gws, s, false, false, M, F, Cz, cx + c.x, Cz, w_p, F, P, Fp, false) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // a, b: gated, masked, channel-major
   if (trace_call(kKTmGate, s, [&] {
@@ -639,7 +640,7 @@ triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void*
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // X_c = A_c B_c^T (outgoing) or A_c^T B_c (incoming)
-  if (contract(h, s, d, d.incoming, !d.incoming, A, Bo, X) != TRIATTN_OK) return TRIATTN_ERR_CUDA;
+  if (contract(gws, s, d, d.incoming, !d.incoming, A, Bo, X) != TRIATTN_OK) return TRIATTN_ERR_CUDA;
   // y = LayerNorm(X) (pair-major);  u = y W_o;  out = sigmoid(g) u
   if (trace_call(kKTmLnOut, s, [&] {
         return by_ch(d.Ch, [&](auto ic) {
@@ -649,7 +650,7 @@ triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void*
         });
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  if (gemm_traced(kKTmProj, h, s, false, false, M, Cz, Ch, y, Ch, w_o, Cz, u, Cz, CUDA_R_16BF) != TRIATTN_OK)
+  if (gemm_traced(kKTmProj, gws, s, false, false, M, Cz, Ch, y, Ch, w_o, Cz, u, Cz, false) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   const cudaError_t e = trace_call(kKTmOutGate, s, [&] {
     gate_out_kernel<<<blocks_for(d.M * d.Cz / 8), 256, 0, s>>>(P, Fp, 4 * Ch, u, static_cast<uint16_t*>(out), Cz,
@@ -680,8 +681,7 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint8_t* cx = static_cast<const uint8_t*>(ctx);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cublasHandle_t h = nullptr;
-  if ((st = blas_for_call(ws + w.blas, s, &h)) != TRIATTN_OK) return st;
+  void* const gws = ws + w.gemm;
   const int M = static_cast<int>(d.M), Cz = static_cast<int>(d.Cz), Ch = static_cast<int>(d.Ch),
             F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
   const uint16_t* mk = static_cast<const uint16_t*>(mask);
@@ -706,9 +706,9 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // u = y W_o:  dW_o = y^T du,  dy = du W_o^T (FP32)
-  if (gemm_traced(kKTmProj, h, s, true, false, Ch, Cz, M, cx + c.y, Ch, du, Cz, d_w_o, Cz, CUDA_R_32F) !=
+  if (gemm_traced(kKTmProj, gws, s, true, false, Ch, Cz, M, cx + c.y, Ch, du, Cz, d_w_o, Cz, true) !=
           TRIATTN_OK ||
-      gemm_traced(kKTmProj, h, s, false, true, M, Ch, Cz, du, Cz, w_o, Cz, dy, Ch, CUDA_R_32F) != TRIATTN_OK)
+      gemm_traced(kKTmProj, gws, s, false, true, M, Ch, Cz, du, Cz, w_o, Cz, dy, Ch, true) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // y = LayerNorm(X):  dX (channel-major), output-LayerNorm partial sums
   float* pg_out = reinterpret_cast<float*>(ws + w.pg_out);
@@ -725,11 +725,11 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
   // the contraction
   triattn_status cs;
   if (!d.incoming) {
-    cs = contract(h, s, d, false, false, dX, Bo, dA);                      // dA_c = dX_c B_c
-    if (cs == TRIATTN_OK) cs = contract(h, s, d, true, false, dX, A, dB);  // dB_c = dX_c^T A_c
+    cs = contract(gws, s, d, false, false, dX, Bo, dA);                      // dA_c = dX_c B_c
+    if (cs == TRIATTN_OK) cs = contract(gws, s, d, true, false, dX, A, dB);  // dB_c = dX_c^T A_c
   } else {
-    cs = contract(h, s, d, false, true, Bo, dX, dA);                       // dA_c = B_c dX_c^T
-    if (cs == TRIATTN_OK) cs = contract(h, s, d, false, false, A, dX, dB); // dB_c = A_c dX_c
+    cs = contract(gws, s, d, false, true, Bo, dX, dA);                       // dA_c = B_c dX_c^T
+    if (cs == TRIATTN_OK) cs = contract(gws, s, d, false, false, A, dX, dB); // dB_c = A_c dX_c
   }
   if (cs != TRIATTN_OK) return cs;
   // the gating:  dp's first 4 C_h columns
@@ -738,8 +738,8 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // p = x W_p:  dW_p = x^T dp,  dx = dp W_p^T (FP32)
-  if (gemm_traced(kKTmProj, h, s, true, false, Cz, F, M, cx + c.x, Cz, dp, Fp, d_w_p, F, CUDA_R_32F) != TRIATTN_OK ||
-      gemm_traced(kKTmProj, h, s, false, true, M, Cz, F, dp, Fp, w_p, F, dx, Cz, CUDA_R_32F) != TRIATTN_OK)
+  if (gemm_traced(kKTmProj, gws, s, true, false, Cz, F, M, cx + c.x, Cz, dp, Fp, d_w_p, F, true) != TRIATTN_OK ||
+      gemm_traced(kKTmProj, gws, s, false, true, M, Cz, F, dp, Fp, w_p, F, dx, Cz, true) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // x = LayerNorm(z)
   float* pg_in = reinterpret_cast<float*>(ws + w.pg_in);

@@ -1,7 +1,7 @@
 """Autograd functions and torch modules over the library's entry points.
 
-Every computation runs in libtriattn's kernels (and the cuBLAS projections it
-calls); these classes only hold parameters, keep the forward's context buffer
+Every computation runs in libtriattn's kernels; these classes only hold
+parameters, keep the forward's context buffer
 for the backward, and hand the library's gradients to autograd.  The
 library's parameter gradients are FP32; autograd casts them to each
 parameter's dtype (BF16 projection matrices, FP32 LayerNorm parameters).

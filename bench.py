@@ -767,10 +767,11 @@ def run_trimul(args):
         tr = T.trace_read()
         T.trace_enable(False)
         by = {"trimul_ln_in": M * Cz * 4 + 8 * M + M * Cz * 8 + 8 * M,
-              "trimul_gate": (M * 4 * Ch * 2 + 2 * M * Ch * 2) + (2 * M * Ch * 2 + 2 * M * 4 * Ch * 2),
+              # projection + gating: fwd reads x, writes a, b, g; bwd reads x, dA, dB, writes dp's 4 C_h columns
+              "trimul_proj_gate": (M * Cz * 2 + 2 * M * Ch * 2 + M * Cz * 2) + (M * Cz * 2 + 2 * M * Ch * 2 + M * 4 * Ch * 2),
               "trimul_ln_out": (2 * M * Ch * 2 + 8 * M) + (M * Ch * 2 + M * Ch * 4 + 8 * M + M * Ch * 2),
               "trimul_out_gate": 3 * M * Cz * 2 + 5 * M * Cz * 2}
-        fl = {"trimul_proj_gemm": 3 * (2 * M * Cz * F + 2 * M * Ch * Cz),
+        fl = {"trimul_proj_gemm": 3 * 2 * M * Ch * Cz + 2 * 2 * M * Cz * F,
               "trimul_contract_gemm": 3 * 2 * Bn * Ch * N ** 3}
         per = {}
         for name, e in tr.items():

@@ -330,9 +330,11 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
  * No projection biases; the residual update z + out is left to the caller.
  * The projections and the per-channel contraction are the library's
  * tensor-core GEMM (triattn_gemm: BF16 operands, FP32 accumulation; the
- * contraction one batched GEMM over the B*C_h channel matrices); the LayerNorms, the gating and masking (with
- * the transposes to and from channel-major operands), the output gate and
- * the parameter-gradient sums are the library's kernels.
+ * contraction one batched GEMM over the B*C_h channel matrices).  The input
+ * projection applies the gating and masking in its epilogue, from the FP32
+ * accumulators, and writes a, b channel-major and g: p itself is never
+ * stored, and the backward recomputes its branch columns.  The LayerNorms,
+ * the output gate and the parameter-gradient sums are the library's kernels.
  *
  * Shape: B >= 1; N a multiple of 8, 8..4096, B*N*N < 2^31; C_z a multiple of
  * 32 up to 256; C_h 32, 64, 96 or 128; direction TRIATTN_TRIMUL_OUTGOING or
@@ -348,7 +350,7 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
  *   w_p [C_z, 4 C_h + C_z] bf16, w_o [C_h, C_z] bf16
  *   d_w_p, d_w_o       same shapes, fp32 (overwritten, not accumulated)
  *   ctx   triattn_trimul_ctx_bytes(shape) bytes, 256-byte aligned: written
- *         by the forward (x and its statistics, p, the channel-major a, b
+ *         by the forward (x and its statistics, g, the channel-major a, b
  *         and X, the output LayerNorm statistics, its output y, and
  *         u = y W_o), read by the backward of the same inputs.
  *   workspace  triattn_trimul_workspace_bytes(shape) bytes, 256-byte

@@ -160,7 +160,7 @@ const char* const kKernelName[kKinds] = {"tri_attn_fwd",     "bwd_preprocess",  
                                          "module_gemm",      "module_ln_bwd",   "module_colsum",
                                          "trimul_ln_in",     "trimul_proj_gemm", "trimul_gate",
                                          "trimul_contract_gemm", "trimul_ln_out", "trimul_out_gate",
-                                         "trimul_colsum",   "gemm"};
+                                         "trimul_colsum",   "gemm",            "trimul_proj_gate"};
 struct TraceRec {
   int kind;
   cudaEvent_t a, b;

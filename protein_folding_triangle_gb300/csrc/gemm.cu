@@ -21,6 +21,21 @@
 //              chunks converted (BF16 or FP32), staged in swizzled shared
 //              memory and written by TMA stores (ragged rows and columns
 //              clipped by the output tensor map).
+//
+// Two further epilogues serve the input projection of the triangle
+// multiplicative update, p = x W_p with W_p's columns [a_v | a_g | b_v | b_g |
+// g] (C_h, C_h, C_h, C_h, C_z wide), so that p itself never goes to memory:
+//   gated      tile n < ceil(C_h / 64) loads the four 64-column blocks of
+//              channels [64n, 64n + 64) of the four branch projections side
+//              by side (accumulator columns [a_v | a_g | b_v | b_g]); the
+//              epilogue forms a = m sigmoid(a_g) a_v and b = m sigmoid(b_g) b_v
+//              (m the optional pair mask) and stores them channel-major,
+//              [B][C_h][N*N], through a transposed staging block (channel
+//              rows of 32 pairs); the remaining tiles hold the g columns,
+//              stored pair-major [M][C_z] like a plain tile.
+//   gate bwd   the same gated tiles, recomputed in the backward; the epilogue
+//              reads dA, dB (channel-major) and writes the four blocks of
+//              dp = d(a, b)/d(a_v, a_g, b_v, b_g) pair-major.
 // Every mbarrier wait is bounded (WaitCtl): a wait that runs out records a
 // timeout in the device status word and the CTA stops.
 #include <cudaTypedefs.h>
@@ -35,11 +50,10 @@ namespace {
 
 constexpr int GB_M = 128;   // rows of a tile (TMEM lanes)
 constexpr int GB_K = 64;    // K depth of a stage (one 128-byte swizzle row of BF16)
-constexpr int GB_S = 4;     // stages
-constexpr int kGemmThreads = 192;
+constexpr int GB_SMAX = 4;  // stages (plain tiles; the gated tiles, with twice the epilogue warps, use 3)
 
 struct GemmBars {
-  uint64_t full[GB_S], empty[GB_S];
+  uint64_t full[GB_SMAX], empty[GB_SMAX];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_slot;
   int abort;
@@ -52,26 +66,50 @@ struct GemmParams {
   void* C;                    // output (BF16 or FP32), or FP32 partials [ksplit][batch][M][N]
   long long ldc, strideC;     // elements
   int c_f32, partial;
+  // gated epilogues
+  int Ch, gated_tiles;        // channels per branch; tiles of the four branch blocks
+  long long NN;               // pairs per example
+  const uint16_t* mask;       // optional pair mask [M] (BF16)
+  const uint16_t* dA;         // gate bwd: channel-major gradients of a and b
+  const uint16_t* dB;
   WaitCtl wc;
 };
 
-template <int BN, bool A_MN, bool B_MN>
+enum GemmMode { kPlain = 0, kGated = 1, kGateBwd = 2 };
+
+
+
+// Per mode: epilogue warps (4; 16 for the gated tiles, whose epilogue does
+// the gating arithmetic: four warps per TMEM lane quarter, one per (branch,
+// 32-channel chunk)), ring stages, and bytes per staging buffer (FP32 or BF16
+// 32 x 32 blocks; the gated modes write BF16 only).
+template <int MODE> struct GemmCfg {
+  static constexpr int kEpi = MODE == 0 ? 4 : 16;
+  static constexpr int kS = MODE == 0 ? 4 : 3;
+  static constexpr int kBuf = MODE == 0 ? 4096 : 2048;
+  static constexpr int kThreads = (2 + kEpi) * 32;
+};
+
+template <int BN, int MODE>
 struct GemmSmem {
   static constexpr int kA = GB_M * GB_K * 2;       // 16 KB
   static constexpr int kB = BN * GB_K * 2;         // 16 / 32 KB
   static constexpr int kStage = kA + kB;
-  static constexpr int kBar = GB_S * kStage;
-  static constexpr int kStg = kBar + 1024;          // epilogue staging: 4 warps x 2 x 32 x 32 x 4 bytes
-  static constexpr int kBytes = kStg + 4 * 2 * 4096 + 1024;  // + alignment slack
+  static constexpr int kBar = GemmCfg<MODE>::kS * kStage;
+  static constexpr int kStg = kBar + 1024;          // epilogue staging: two buffers per warp
+  static constexpr int kBytes = kStg + GemmCfg<MODE>::kEpi * 2 * GemmCfg<MODE>::kBuf + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 };
 
-template <int BN, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int BN, bool A_MN, bool B_MN, int MODE>
+__global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                const __grid_constant__ CUtensorMap tm_c, GemmParams p) {
-  using L = GemmSmem<BN, A_MN, B_MN>;
+                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_x,
+                const __grid_constant__ CUtensorMap tm_y, GemmParams p) {
+  static_assert(MODE == kPlain || (BN == 256 && !A_MN && B_MN), "gated tiles: K-major x, N-major W_p");
+  using L = GemmSmem<BN, MODE>;
+  constexpr int GB_S = GemmCfg<MODE>::kS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   GemmBars* bars = reinterpret_cast<GemmBars*>(sm + L::kBar);
@@ -100,7 +138,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->acc_full[i], 1);
-      mbar_init(&bars->acc_empty[i], 128);
+      mbar_init(&bars->acc_empty[i], GemmCfg<MODE>::kEpi * 32);
     }
     bars->abort = 0;
     fence_mbar_init();
@@ -135,7 +173,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             tma_load_3d(sa, &tm_a, &bars->full[stage], k0, m0, bt);
           }
-          if constexpr (B_MN) {  // B stored [K][N]: BN / 64 blocks of 64 N
+          if constexpr (MODE != kPlain) {  // the four branch blocks of channels [64 nt, 64 nt + 64), or g
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int col = nt < p.gated_tiles ? j * p.Ch + 64 * nt : 4 * p.Ch + 256 * (nt - p.gated_tiles) + 64 * j;
+              tma_load_3d(sb + j * 64 * 128, &tm_b, &bars->full[stage], col, k0, bt);
+            }
+          } else if constexpr (B_MN) {  // B stored [K][N]: BN / 64 blocks of 64 N
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 64 * 128, &tm_b, &bars->full[stage], n0 + 64 * j, k0, bt);
           } else {
@@ -186,47 +230,151 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // staging buffer (64-byte rows for BF16, 128-byte rows for FP32), and one
     // lane stores the 32 x 32 block with TMA (rows and columns past the
     // matrix are clipped by the tensor map); two buffers per warp.
-    const int quarter = warp & 3;
+    constexpr int kBuf = GemmCfg<MODE>::kBuf;
+    const int quarter = warp & 3;       // TMEM lanes a warp may read: 32 * (warp id mod 4) on
+    const int part = (warp - 2) >> 2;   // gated tiles: (branch, chunk) unit; plain: column range
     const int r = quarter * 32 + lane;  // accumulator row = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const bool f32 = p.partial || p.c_f32;
-    uint8_t* stg = sm + L::kStg + quarter * (2 * 4096);
+    uint8_t* stg = sm + L::kStg + (warp - 2) * (2 * kBuf);
     int nst = 0;  // TMA stores issued by this warp
+    // the next staging buffer, once the store that last used it has read it
+    auto next_buf = [&]() -> uint8_t* {
+      uint8_t* buf = stg + (nst & 1) * kBuf;
+      if (lane == 0) bulk_wait_read_allow1();
+      __syncwarp();
+      return buf;
+    };
+    // one accumulator row of 32 FP32 values as BF16 into a 64-byte-swizzled 32 x 32 block
+    auto put_bf16 = [&](uint8_t* buf, const uint32_t (&v)[32]) {
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    };
+    auto issue = [&](const CUtensorMap* map, uint8_t* buf, int x, int y, int z) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tma_store_3d(map, buf, x, y, z);
+      ++nst;
+    };
+    // A gated tile: accumulator columns [a_v | a_g | b_v | b_g] of channels
+    // [64 nt, 64 nt + 64).  The four warps of a TMEM lane quarter take one
+    // (branch, 32-channel chunk) unit each; a warp's 32 rows are 32
+    // consecutive pairs of one example (N*N is a multiple of 32).  With
+    // sigmoid(x) = (1 + tanh(x / 2)) / 2:  m sigmoid(g) v = h + h tanh(g / 2),
+    // h = m v / 2;  its derivatives are m sigmoid(g) (value) and
+    // m v (1 - tanh(g / 2)^2) / 4 (gate).
+    const int unit_br = part >> 1, unit_c0 = 32 * (part & 1);
+    auto unit_rows = [&](int mt) { return static_cast<long long>(mt) * GB_M + quarter * 32; };
+    // gate bwd: this lane's 32 values of dA or dB (BF16 pairs), loaded before
+    // the accumulator wait
+    auto load_d = [&](int mt, int nt, uint32_t (&d)[16]) {
+      const long long mq = unit_rows(mt);
+      const int ch = 64 * nt + unit_c0;
+      if (mq >= p.M || ch >= p.Ch) return;
+      const long long bq = mq / p.NN, pos0 = mq % p.NN;
+      const uint16_t* src = (unit_br ? p.dB : p.dA) + (bq * p.Ch + ch) * p.NN + pos0 + lane;
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        d[e] = static_cast<uint32_t>(src[2 * e * p.NN]) | (static_cast<uint32_t>(src[(2 * e + 1) * p.NN]) << 16);
+    };
+    auto gated_tile = [&](int mt, int nt, int ab, const uint32_t (&d)[16]) {
+      const long long mq = unit_rows(mt);
+      const int ch = 64 * nt + unit_c0;
+      if (mq >= p.M || ch >= p.Ch) return;
+      const int bq = static_cast<int>(mq / p.NN);
+      const int pos0 = static_cast<int>(mq % p.NN);
+      const float mk = p.mask != nullptr ? bf16lo_to_f32(p.mask[mq + lane]) : 1.f;
+      const uint32_t tv = tmem + lane_addr + ab * BN + 128 * unit_br + unit_c0;  // value columns; gate at +64
+      if constexpr (MODE == kGated) {
+        // channel rows of 32 pairs (64 bytes, no swizzle), stored channel-major
+        uint8_t* buf = next_buf();
+        uint16_t* hb = reinterpret_cast<uint16_t*>(buf);
+        const float hm = 0.5f * mk;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[16], gv[16];
+          tmem_ld16x2_wait(tv + 16 * hf, v, tv + 64 + 16 * hf, gv);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float h = hm * __uint_as_float(v[e]);
+            const float o = fmaf(h, tanh_approx(0.5f * __uint_as_float(gv[e])), h);
+            hb[(16 * hf + e) * 32 + lane] = static_cast<uint16_t>(pack_bf16x2(o, 0.f) & 0xFFFFu);
+          }
+        }
+        issue(unit_br ? &tm_y : &tm_x, buf, pos0, ch, bq);
+      } else {
+        // the value and gate blocks in the warp's two buffers
+        if (lane == 0) bulk_wait_read();  // every earlier store has read its buffer
+        __syncwarp();
+        uint8_t* bval = stg;
+        uint8_t* bgate = stg + kBuf;
+        // 8 columns (one 16-byte chunk of each 64-byte-swizzled block) at a time
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[8], gv[8], wv[4], wg[4];
+          tmem_ld8x2_wait(tv + 8 * c, v, tv + 64 + 8 * c, gv);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            float dv2[2], dg2[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint32_t dw = d[4 * c + (e >> 1)];
+              const float dd = (k ? bf16hi_to_f32(dw) : bf16lo_to_f32(dw)) * mk;
+              const float t = tanh_approx(0.5f * __uint_as_float(gv[e + k]));
+              dv2[k] = dd * fmaf(0.5f, t, 0.5f);
+              dg2[k] = (0.25f * dd * __uint_as_float(v[e + k])) * fmaf(-t, t, 1.f);
+            }
+            wv[e >> 1] = pack_bf16x2(dv2[0], dv2[1]);
+            wg[e >> 1] = pack_bf16x2(dg2[0], dg2[1]);
+          }
+          const int off = lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
+          *reinterpret_cast<uint4*>(bval + off) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          *reinterpret_cast<uint4*>(bgate + off) = make_uint4(wg[0], wg[1], wg[2], wg[3]);
+        }
+        issue(&tm_c, bval, 2 * unit_br * p.Ch + ch, static_cast<int>(mq), 0);
+        issue(&tm_c, bgate, (2 * unit_br + 1) * p.Ch + ch, static_cast<int>(mq), 0);
+      }
+    };
     int local = 0;
     for (long long t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       int mt, nt, bt, ks;
       decode(t, mt, nt, bt, ks);
       const int ab = local & 1;
+      uint32_t dpre[16];
+      if constexpr (MODE == kGateBwd) load_d(mt, nt, dpre);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[ab], (local >> 1) & 1, wc, abort))) break;
       tc_fence_after();
+      if constexpr (MODE != kPlain) {
+        if (nt < p.gated_tiles) {
+          gated_tile(mt, nt, ab, dpre);
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty[ab]);
+          continue;
+        }
+      }
       const int m0 = mt * GB_M + quarter * 32;
-      const int n0 = nt * BN;
+      const int n0 = (MODE == kPlain ? nt : nt - p.gated_tiles) * BN;
       const int zc = p.partial ? ks * p.batch + bt : bt;
+      constexpr int kCols = BN * 4 / GemmCfg<MODE>::kEpi;  // columns per warp of a plain tile
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = part * kCols; c0 < (part + 1) * kCols; c0 += 32) {
         uint32_t v[32];
         tmem_ld32_wait(tmem + lane_addr + ab * BN + c0, v);
         if (n0 + c0 >= p.N) continue;  // the whole chunk is past N (the same for every lane)
-        uint8_t* buf = stg + (nst & 1) * 4096;
-        if (lane == 0) bulk_wait_read_allow1();  // the store that last used this buffer has read it
-        __syncwarp();
+        uint8_t* buf = next_buf();
         if (f32) {
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(buf + sw128(lane, c)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         } else {
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          put_bf16(buf, v);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tma_store_3d(&tm_c, buf, n0 + c0, m0, zc);
-        ++nst;
+        issue(&tm_c, buf, n0 + c0, m0, zc);
       }
       (void)r;
       tc_fence_before();
@@ -309,18 +457,24 @@ bool gemm_out_map(CUtensorMap* m, void* base, long long N, long long M, long lon
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN>
-cudaError_t gemm_launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p,
-                          int grid, cudaStream_t s) {
-  using L = GemmSmem<BN, A_MN, B_MN>;
+template <int BN, bool A_MN, bool B_MN, int MODE = kPlain>
+cudaError_t gemm_launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tx,
+                          const CUtensorMap& ty, const GemmParams& p, int grid, cudaStream_t s) {
+  using L = GemmSmem<BN, MODE>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(gemm_kernel<BN, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    attr = cudaFuncSetAttribute(gemm_kernel<BN, A_MN, B_MN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kBytes);
   });
   if (attr != cudaSuccess) return attr;
-  gemm_kernel<BN, A_MN, B_MN><<<grid, kGemmThreads, L::kBytes, s>>>(ta, tb, tc, p);
+  gemm_kernel<BN, A_MN, B_MN, MODE><<<grid, GemmCfg<MODE>::kThreads, L::kBytes, s>>>(ta, tb, tc, tx, ty, p);
   return cudaGetLastError();
+}
+template <int BN, bool A_MN, bool B_MN>
+cudaError_t gemm_launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p,
+                          int grid, cudaStream_t s) {
+  return gemm_launch_t<BN, A_MN, B_MN, kPlain>(ta, tb, tc, tc, tc, p, grid, s);
 }
 
 int gemm_sms() {
@@ -396,6 +550,10 @@ cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, lo
   p.ldc = ldc;
   p.strideC = sC;
   p.c_f32 = c_f32 ? 1 : 0;
+  p.Ch = 0;
+  p.gated_tiles = 0;
+  p.NN = 1;
+  p.mask = p.dA = p.dB = nullptr;
   p.wc = wc;
   const long long total = static_cast<long long>(p.tiles_m) * p.tiles_n * batch * sp.ksplit;
   const int grid = static_cast<int>(std::min<long long>(total, sms));
@@ -414,6 +572,92 @@ cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, lo
   gemm_splitk_reduce_kernel<<<blocks, 256, 0, s>>>(static_cast<const float*>(ws), sp.ksplit, batch, M, N, C, ldc,
                                                    batch > 1 ? sC : 0, c_f32 ? 1 : 0);
   return cudaGetLastError();
+}
+
+namespace {
+// Channel-major output map: [B][C_h][N*N] BF16, box = 32 pairs x 32 channels,
+// no swizzle (the staging block holds channel rows of 64 bytes).
+bool gemm_cm_map(CUtensorMap* m, void* base, long long NN, int Ch, int B) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = gemm_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(NN), static_cast<cuuint64_t>(Ch), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(NN) * 2, static_cast<cuuint64_t>(NN) * Ch * 2};
+  const cuuint32_t box[3] = {32u, 32u, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool al16p(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+// The gated tiles' common parameters and operand maps (x [M][C_z] K-major,
+// W_p [C_z][4 C_h + C_z] N-major).
+bool gated_setup(int B, long long NN, int Cz, int Ch, const void* x, const void* w_p, const void* mask,
+                 CUtensorMap* tma, CUtensorMap* tmb, GemmParams* p) {
+  const long long M = B * NN;
+  if (B < 1 || NN < 32 || NN % 32 != 0 || M > 0x7fffffffLL || Cz < 32 || Cz % 32 != 0 || Ch < 32 || Ch % 32 != 0 ||
+      !al16p(x) || !al16p(w_p) || (mask != nullptr && !al16p(mask)))
+    return false;
+  const int F = 4 * Ch + Cz;
+  if (!gemm_map(tma, x, Cz, M, 1, Cz, 0, 64, 128) || !gemm_map(tmb, w_p, F, Cz, 1, F, 0, 64, 64)) return false;
+  p->M = static_cast<int>(M);
+  p->K = Cz;
+  p->batch = 1;
+  p->ksplit = 1;
+  p->kchunk = (Cz + GB_K - 1) / GB_K * GB_K;
+  p->tiles_m = static_cast<int>((M + GB_M - 1) / GB_M);
+  p->partial = 0;
+  p->c_f32 = 0;
+  p->ldc = 0;
+  p->strideC = 0;
+  p->Ch = Ch;
+  p->gated_tiles = (Ch + 63) / 64;
+  p->NN = NN;
+  p->mask = static_cast<const uint16_t*>(mask);
+  p->dA = p->dB = nullptr;
+  return true;
+}
+}  // namespace
+
+cudaError_t launch_gated_proj(int B, long long NN, int Cz, int Ch, const void* x, const void* w_p, const void* mask,
+                              void* a, void* b, void* g, const WaitCtl& wc, cudaStream_t s) {
+  CUtensorMap tma, tmb, tmc, tmx, tmy;
+  GemmParams p;
+  if (!gated_setup(B, NN, Cz, Ch, x, w_p, mask, &tma, &tmb, &p) || !al16p(a) || !al16p(b) || !al16p(g))
+    return cudaErrorInvalidValue;
+  const long long M = B * NN;
+  if (!gemm_out_map(&tmc, g, Cz, M, 1, Cz, 0, false) || !gemm_cm_map(&tmx, a, NN, Ch, B) ||
+      !gemm_cm_map(&tmy, b, NN, Ch, B))
+    return cudaErrorInvalidValue;
+  p.N = Cz;  // the g tiles' columns
+  p.tiles_n = p.gated_tiles + (Cz + 255) / 256;
+  p.C = g;
+  p.wc = wc;
+  const long long total = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  const int grid = static_cast<int>(std::min<long long>(total, gemm_sms()));
+  return gemm_launch_t<256, false, true, kGated>(tma, tmb, tmc, tmx, tmy, p, grid, s);
+}
+
+cudaError_t launch_gate_bwd_proj(int B, long long NN, int Cz, int Ch, const void* x, const void* w_p,
+                                 const void* mask, const void* dA, const void* dB, void* dp, long long ldp,
+                                 const WaitCtl& wc, cudaStream_t s) {
+  CUtensorMap tma, tmb, tmc;
+  GemmParams p;
+  if (!gated_setup(B, NN, Cz, Ch, x, w_p, mask, &tma, &tmb, &p) || !al16p(dA) || !al16p(dB) || !al16p(dp) ||
+      ldp < 4 * Ch || ldp % 8 != 0)
+    return cudaErrorInvalidValue;
+  const long long M = B * NN;
+  if (!gemm_out_map(&tmc, dp, 4 * Ch, M, 1, ldp, 0, false)) return cudaErrorInvalidValue;
+  p.N = 4 * Ch;
+  p.tiles_n = p.gated_tiles;
+  p.C = dp;
+  p.dA = static_cast<const uint16_t*>(dA);
+  p.dB = static_cast<const uint16_t*>(dB);
+  p.wc = wc;
+  const long long total = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  const int grid = static_cast<int>(std::min<long long>(total, gemm_sms()));
+  return gemm_launch_t<256, false, true, kGateBwd>(tma, tmb, tmc, tmc, tmc, p, grid, s);
 }
 
 }  // namespace triattn

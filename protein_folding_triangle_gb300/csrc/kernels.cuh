@@ -98,6 +98,18 @@ cudaError_t launch_gemm(bool ta, bool tb, int M, int N, int K, const void* A, lo
                         long long ldb, void* C, long long ldc, bool c_f32, int batch, long long sA, long long sB,
                         long long sC, void* ws, size_t ws_bytes, const WaitCtl& wc, cudaStream_t s);
 size_t gemm_splitk_bytes(int M, int N, int K, int batch);
+// The triangle multiplicative update's input projection p = x W_p (x [B*NN]
+// [C_z], W_p [C_z][4 C_h + C_z] with column blocks a_v, a_g, b_v, b_g, g) on
+// the same tensor cores, p never stored: a = m sigmoid(a_g) a_v and
+// b = m sigmoid(b_g) b_v channel-major [B][C_h][NN], g pair-major [B*NN][C_z]
+// (mask m optional, [B*NN] BF16).  NN, C_z and C_h multiples of 32.
+cudaError_t launch_gated_proj(int B, long long NN, int Cz, int Ch, const void* x, const void* w_p, const void* mask,
+                              void* a, void* b, void* g, const WaitCtl& wc, cudaStream_t s);
+// Its backward through the gating: recomputes the four branch projections and
+// writes dp's first 4 C_h columns (row stride ldp) from dA, dB (channel-major).
+cudaError_t launch_gate_bwd_proj(int B, long long NN, int Cz, int Ch, const void* x, const void* w_p,
+                                 const void* mask, const void* dA, const void* dB, void* dp, long long ldp,
+                                 const WaitCtl& wc, cudaStream_t s);
 // The bounded-wait control of the current device (status word, time limit).
 WaitCtl current_wait_ctl();
 
@@ -105,7 +117,8 @@ WaitCtl current_wait_ctl();
 enum KernelKind {
   kKFwd = 0, kKPre, kKTrans, kKMain, kKRedDq, kKRedDb, kKMainAtomic, kKFinDq, kKFinDb, kKCombine, kKFwdPrep,
   kKModLnFwd, kKModLayout, kKModGemm, kKModLnBwd, kKModColSum,
-  kKTmLnIn, kKTmProj, kKTmGate, kKTmContract, kKTmLnOut, kKTmOutGate, kKTmColSum, kKGemm, kKinds
+  kKTmLnIn, kKTmProj, kKTmGate, kKTmContract, kKTmLnOut, kKTmOutGate, kKTmColSum, kKGemm, kKTmProjGate,
+  kKinds
 };
 // Runs `launch` on stream `s`, bracketed by a pair of trace events while
 // tracing is on.

@@ -8,23 +8,27 @@
 //   incoming: X[b,i,j,c] = sum_k a[b,k,i,c] b[b,k,j,c]
 //   out = sigmoid(p_g) (LayerNorm(X) W_o)          W_o   [C_h, C_z]
 //
-// Data layout.  The pair tensors z, x, p, y = LayerNorm(X), u = y W_o are
-// pair-major rows.  The branch operands a, b, the contraction output X and
+// Data layout.  The pair tensors z, x, g, y = LayerNorm(X), u = y W_o are
+// pair-major rows; p itself is never stored (below).  The branch operands a, b, the contraction output X and
 // their gradients are channel-major: [B][C_h][N][N], so that channel c of
 // example b is one row-major N x N matrix A_c (A_c[r][s] = a[b,r,s,c]).  Both
 // directions and all three products of the contraction are then one
 // strided-batched GEMM over the B*C_h matrices with the right operand flags:
 //   outgoing  X_c = A_c B_c^T    dA_c = dX_c B_c     dB_c = dX_c^T A_c
 //   incoming  X_c = A_c^T B_c    dA_c = B_c dX_c^T   dB_c = A_c dX_c
-// The kernels here do the gating and masking while transposing pair-major
-// projections into the channel-major operands (64 pairs per block through
-// shared memory), the output LayerNorm while transposing X back, the output
-// gate, and their backward passes; the projection GEMMs and the contraction
-// are the library's tensor-core GEMM (gemm.cu: BF16 operands, FP32
-// accumulation; the contraction one batched GEMM over the channel matrices,
-// the weight gradients split along the pair axis into FP32 partials added in
-// fixed order).  No floating-point atomics: every reduction has a fixed
-// order.
+// The input projection p = x W_p runs on the library's tensor-core GEMM
+// (gemm.cu) with the gating and masking in its epilogue, which writes a and b
+// channel-major and g pair-major from the FP32 accumulators, so the 4 C_h +
+// C_z wide p never goes to memory; the backward recomputes the four branch
+// projections the same way (bitwise the same values) and forms dp's branch
+// columns from dA and dB in the epilogue.  The kernels here do the output
+// LayerNorm while transposing X back (64 pairs per block through shared
+// memory), the output gate, and their backward passes; the other projections,
+// the weight gradients and the contraction are plain GEMMs on the same
+// tensor cores (BF16 operands, FP32 accumulation; the contraction one batched
+// GEMM over the channel matrices, the weight gradients split along the pair
+// axis into FP32 partials added in fixed order).  No floating-point atomics:
+// every reduction has a fixed order.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -58,9 +62,6 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 }
 __device__ __forceinline__ uint4 ld16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ void st16(uint16_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
-__device__ __forceinline__ float mask_at(const uint16_t* mask, size_t m) {
-  return mask == nullptr ? 1.f : bf16lo_to_f32(mask[m]);
-}
 
 // A [Ch][64] channel-major tile of pairs [pos0, pos0 + 64) of example b in
 // shared memory, as BF16: row c holds the 64 pairs as 32 words (even pair in
@@ -106,53 +107,6 @@ __device__ __forceinline__ float tile_h(const uint32_t* s, int c, int pr) {
 __device__ __forceinline__ void tile_h_set(uint32_t* s, int c, int pr, float v) {
   reinterpret_cast<uint16_t*>(s + c * kRowW + (pr >> 1))[pr & 1] =
       static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
-}
-
-// a = m sigmoid(p_ag) p_av and b = m sigmoid(p_bg) p_bv for 64 consecutive
-// pairs, written channel-major.  Phase 1: thread (pair couple pp, 8-channel
-// chunk cc) gates two pairs and packs them per channel into one shared word;
-// the chunk index runs fastest, so a warp reads whole contiguous row
-// segments of p.  Phase 2: every channel row of 64 pairs goes out as 8
-// 16-byte stores.
-template <int Ch>
-__global__ void __launch_bounds__(256) gate_fwd_kernel(const uint16_t* __restrict__ p, int ld,
-                                                       const uint16_t* __restrict__ mask, uint16_t* __restrict__ A,
-                                                       uint16_t* __restrict__ Bo, size_t NN) {
-  __shared__ uint32_t sA[Ch][33], sB[Ch][33];
-  const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
-  const size_t b = m0 / NN, pos0 = m0 % NN;
-  for (int it = threadIdx.x; it < 32 * (Ch / 8); it += blockDim.x) {
-    const int pp = it / (Ch / 8), cc = it % (Ch / 8);
-    float ga[2][8], gb[2][8];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const size_t m = m0 + 2 * pp + h;
-      const uint16_t* row = p + m * ld + 8 * cc;
-      float av[8], ag[8], bv[8], bg[8];
-      unpack8(ld16(row), av);
-      unpack8(ld16(row + Ch), ag);
-      unpack8(ld16(row + 2 * Ch), bv);
-      unpack8(ld16(row + 3 * Ch), bg);
-      const float mk = mask_at(mask, m);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ga[h][e] = mk * sigm(ag[e]) * av[e];
-        gb[h][e] = mk * sigm(bg[e]) * bv[e];
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      sA[8 * cc + e][pp] = pack_bf16x2(ga[0][e], ga[1][e]);
-      sB[8 * cc + e][pp] = pack_bf16x2(gb[0][e], gb[1][e]);
-    }
-  }
-  __syncthreads();
-  for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
-    const int c = it >> 3, q = it & 7;
-    const size_t off = (b * Ch + c) * NN + pos0 + 8 * q;
-    st16(A + off, make_uint4(sA[c][4 * q], sA[c][4 * q + 1], sA[c][4 * q + 2], sA[c][4 * q + 3]));
-    st16(Bo + off, make_uint4(sB[c][4 * q], sB[c][4 * q + 1], sB[c][4 * q + 2], sB[c][4 * q + 3]));
-  }
 }
 
 // y = LayerNorm(X) for 64 pairs: X channel-major in, y pair-major out (BF16),
@@ -328,59 +282,8 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
   }
 }
 
-// Backward of the gating: dp's first 4 C_h columns (pair-major) from dA, dB
-// (channel-major) and the saved projections.
-template <int Ch>
-__global__ void __launch_bounds__(256) gate_bwd_kernel(const uint16_t* __restrict__ dA,
-                                                       const uint16_t* __restrict__ dB,
-                                                       const uint16_t* __restrict__ p, int ld,
-                                                       const uint16_t* __restrict__ mask,
-                                                       uint16_t* __restrict__ dp, size_t NN) {
-  extern __shared__ uint32_t smw[];
-  uint32_t* sA = smw;               // dA tile, BF16 pairs
-  uint32_t* sB = smw + Ch * kRowW;  // dB tile
-  constexpr int kCh = Ch / 32;
-  const size_t m0 = static_cast<size_t>(blockIdx.x) * kPairs;
-  const size_t b = m0 / NN, pos0 = m0 % NN;
-  {
-    uint4 ra[Ch * 8 / 256], rb[Ch * 8 / 256];
-    fetch_cm_tile<Ch>(dA, b, pos0, NN, ra);
-    fetch_cm_tile<Ch>(dB, b, pos0, NN, rb);
-    put_cm_tile<Ch>(ra, sA);
-    put_cm_tile<Ch>(rb, sB);
-  }
-  __syncthreads();
-  const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
-  const size_t m = m0 + pr;
-  const float mk = mask_at(mask, m);
-  const uint16_t* row = p + m * ld;
-  uint16_t* drow = dp + m * ld;
-#pragma unroll
-  for (int i = 0; i < kCh; ++i) {
-    const int c0 = 8 * (qq + 4 * i);
-    float av[8], ag[8], bv[8], bg[8], dav[8], dag[8], dbv[8], dbg[8];
-    unpack8(ld16(row + c0), av);
-    unpack8(ld16(row + Ch + c0), ag);
-    unpack8(ld16(row + 2 * Ch + c0), bv);
-    unpack8(ld16(row + 3 * Ch + c0), bg);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float da = tile_h(sA, c0 + e, pr) * mk, db = tile_h(sB, c0 + e, pr) * mk;
-      const float sa = sigm(ag[e]), sb = sigm(bg[e]);
-      dav[e] = da * sa;
-      dag[e] = da * av[e] * sa * (1.f - sa);
-      dbv[e] = db * sb;
-      dbg[e] = db * bv[e] * sb * (1.f - sb);
-    }
-    st16(drow + c0, pack8(dav));
-    st16(drow + Ch + c0, pack8(dag));
-    st16(drow + 2 * Ch + c0, pack8(dbv));
-    st16(drow + 3 * Ch + c0, pack8(dbg));
-  }
-}
-
-// out = sigmoid(g) u, 8 features per thread (g = p's last C_z columns).
-__global__ void __launch_bounds__(256) gate_out_kernel(const uint16_t* __restrict__ p, int ld, int goff,
+// out = sigmoid(g) u, 8 features per thread (g, u, out [M, C_z]).
+__global__ void __launch_bounds__(256) gate_out_kernel(const uint16_t* __restrict__ g_in,
                                                        const uint16_t* __restrict__ u, uint16_t* __restrict__ out,
                                                        int Cz, size_t M) {
   const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -389,7 +292,7 @@ __global__ void __launch_bounds__(256) gate_out_kernel(const uint16_t* __restric
   const size_t m = t / chunks;
   const int c0 = 8 * static_cast<int>(t % chunks);
   float g[8], uv[8], o[8];
-  unpack8(ld16(p + m * ld + goff + c0), g);
+  unpack8(ld16(g_in + m * Cz + c0), g);
   unpack8(ld16(u + m * Cz + c0), uv);
 #pragma unroll
   for (int e = 0; e < 8; ++e) o[e] = sigm(g[e]) * uv[e];
@@ -397,8 +300,8 @@ __global__ void __launch_bounds__(256) gate_out_kernel(const uint16_t* __restric
 }
 
 // Backward of the output gate: du = d_out sigmoid(g) (BF16 [M, C_z]) and
-// dp[:, goff + c] = d_out u sigmoid(g) (1 - sigmoid(g)).
-__global__ void __launch_bounds__(256) gate_out_bwd_kernel(const uint16_t* __restrict__ p, int ld, int goff,
+// dp[:, goff + c] = d_out u sigmoid(g) (1 - sigmoid(g)) (dp row stride ld).
+__global__ void __launch_bounds__(256) gate_out_bwd_kernel(const uint16_t* __restrict__ g_in, int ld, int goff,
                                                            const uint16_t* __restrict__ u,
                                                            const uint16_t* __restrict__ d_out,
                                                            uint16_t* __restrict__ du, uint16_t* __restrict__ dp,
@@ -409,7 +312,7 @@ __global__ void __launch_bounds__(256) gate_out_bwd_kernel(const uint16_t* __res
   const size_t m = t / chunks;
   const int c0 = 8 * static_cast<int>(t % chunks);
   float g[8], uv[8], d[8], o1[8], o2[8];
-  unpack8(ld16(p + m * ld + goff + c0), g);
+  unpack8(ld16(g_in + m * Cz + c0), g);
   unpack8(ld16(u + m * Cz + c0), uv);
   unpack8(ld16(d_out + m * Cz + c0), d);
 #pragma unroll
@@ -444,7 +347,7 @@ TmDims tm_dims(const triattn_trimul_shape* s) {
 }
 
 struct TmCtx {
-  size_t x, mean_in, rstd_in, p, a, b, X, mean_out, rstd_out, y, u, total;
+  size_t x, mean_in, rstd_in, g, a, b, X, mean_out, rstd_out, y, u, total;
 };
 TmCtx tm_ctx(const TmDims& d) {
   TmCtx c;
@@ -453,7 +356,7 @@ TmCtx tm_ctx(const TmDims& d) {
   c.x = o;        o += rup(d.M * d.Cz * 2);
   c.mean_in = o;  o += rup(d.M * 4);
   c.rstd_in = o;  o += rup(d.M * 4);
-  c.p = o;        o += rup(d.M * d.Fp * 2);
+  c.g = o;        o += rup(d.M * d.Cz * 2);
   c.a = o;        o += rup(cm);
   c.b = o;        o += rup(cm);
   c.X = o;        o += rup(cm);
@@ -504,7 +407,6 @@ unsigned blocks_for(size_t n) { return static_cast<unsigned>((n + 255) / 256); }
 // Dynamic shared memory of the channel-major kernels.
 template <int Ch> constexpr int ln_cm_fwd_smem() { return Ch * kRowW * 4; }
 template <int Ch> constexpr int ln_cm_bwd_smem() { return 2 * Ch * kRow * 4 + Ch * kRowW * 4; }
-template <int Ch> constexpr int gate_bwd_smem() { return 2 * Ch * kRowW * 4; }
 
 template <int Ch>
 cudaError_t set_attrs() {
@@ -513,8 +415,6 @@ cudaError_t set_attrs() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ln_cm_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              ln_cm_bwd_smem<Ch>());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gate_bwd_kernel<Ch>, cudaFuncAttributeMaxDynamicSharedMemorySize, gate_bwd_smem<Ch>());
   return e;
 }
 
@@ -523,12 +423,6 @@ struct CmLaunch {
   const TmDims& d;
   cudaStream_t s;
 
-  template <int Ch>
-  cudaError_t gate_fwd(const uint16_t* p, const uint16_t* mask, uint16_t* A, uint16_t* B) const {
-    gate_fwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, 0, s>>>(p, static_cast<int>(d.Fp), mask, A, B,
-                                                                            d.NN);
-    return cudaGetLastError();
-  }
   template <int Ch>
   cudaError_t ln_fwd(const uint16_t* X, const float* g, const float* b, uint16_t* y, float* mean, float* rstd) const {
     cudaError_t e = set_attrs<Ch>();
@@ -544,15 +438,6 @@ struct CmLaunch {
     if (e != cudaSuccess) return e;
     const size_t tiles = d.M / kPairs;
     ln_cm_bwd_kernel<Ch><<<kCmBwdBlocks, 256, ln_cm_bwd_smem<Ch>(), s>>>(X, dy, g, mean, rstd, dX, pg, pb, d.NN, tiles);
-    return cudaGetLastError();
-  }
-  template <int Ch>
-  cudaError_t gate_bwd(const uint16_t* dA, const uint16_t* dB, const uint16_t* p, const uint16_t* mask,
-                       uint16_t* dp) const {
-    cudaError_t e = set_attrs<Ch>();
-    if (e != cudaSuccess) return e;
-    gate_bwd_kernel<Ch><<<static_cast<unsigned>(d.M / kPairs), 256, gate_bwd_smem<Ch>(), s>>>(
-        dA, dB, p, static_cast<int>(d.Fp), mask, dp, d.NN);
     return cudaGetLastError();
   }
 };
@@ -616,10 +501,9 @@ triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void*
   uint8_t* cx = static_cast<uint8_t*>(ctx);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* const gws = ws + w.gemm;
-  const int M = static_cast<int>(d.M), Cz = static_cast<int>(d.Cz), Ch = static_cast<int>(d.Ch),
-            F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
+  const int M = static_cast<int>(d.M), Cz = static_cast<int>(d.Cz), Ch = static_cast<int>(d.Ch);
   const uint16_t* mk = static_cast<const uint16_t*>(mask);
-  uint16_t* P = reinterpret_cast<uint16_t*>(cx + c.p);
+  uint16_t* G = reinterpret_cast<uint16_t*>(cx + c.g);
   uint16_t* A = reinterpret_cast<uint16_t*>(cx + c.a);
   uint16_t* Bo = reinterpret_cast<uint16_t*>(cx + c.b);
   uint16_t* X = reinterpret_cast<uint16_t*>(cx + c.X);
@@ -632,11 +516,11 @@ triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void*
                            reinterpret_cast<float*>(cx + c.rstd_in), s);
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  if (gemm_traced(kKTmProj, gws, s, false, false, M, F, Cz, cx + c.x, Cz, w_p, F, P, Fp, false) != TRIATTN_OK)
-    return TRIATTN_ERR_CUDA;
-  // a, b: gated, masked, channel-major
-  if (trace_call(kKTmGate, s, [&] {
-        return by_ch(d.Ch, [&](auto ic) { return L.template gate_fwd<decltype(ic)::value>(P, mk, A, Bo); });
+  // p = x W_p on the tensor cores with the gating in the epilogue: a, b
+  // gated, masked, channel-major; g pair-major; p itself is not stored
+  if (trace_call(kKTmProjGate, s, [&] {
+        return launch_gated_proj(static_cast<int>(d.B), static_cast<long long>(d.NN), Cz, Ch, cx + c.x, w_p, mk, A,
+                                 Bo, G, current_wait_ctl(), s);
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // X_c = A_c B_c^T (outgoing) or A_c^T B_c (incoming)
@@ -653,8 +537,7 @@ triattn_status triattn_trimul_fwd(const triattn_trimul_shape* shape, const void*
   if (gemm_traced(kKTmProj, gws, s, false, false, M, Cz, Ch, y, Ch, w_o, Cz, u, Cz, false) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   const cudaError_t e = trace_call(kKTmOutGate, s, [&] {
-    gate_out_kernel<<<blocks_for(d.M * d.Cz / 8), 256, 0, s>>>(P, Fp, 4 * Ch, u, static_cast<uint16_t*>(out), Cz,
-                                                               d.M);
+    gate_out_kernel<<<blocks_for(d.M * d.Cz / 8), 256, 0, s>>>(G, u, static_cast<uint16_t*>(out), Cz, d.M);
     return cudaGetLastError();
   });
   return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
@@ -685,7 +568,7 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
   const int M = static_cast<int>(d.M), Cz = static_cast<int>(d.Cz), Ch = static_cast<int>(d.Ch),
             F = static_cast<int>(d.F), Fp = static_cast<int>(d.Fp);
   const uint16_t* mk = static_cast<const uint16_t*>(mask);
-  const uint16_t* P = reinterpret_cast<const uint16_t*>(cx + c.p);
+  const uint16_t* G = reinterpret_cast<const uint16_t*>(cx + c.g);
   const uint16_t* A = reinterpret_cast<const uint16_t*>(cx + c.a);
   const uint16_t* Bo = reinterpret_cast<const uint16_t*>(cx + c.b);
   const uint16_t* X = reinterpret_cast<const uint16_t*>(cx + c.X);
@@ -700,7 +583,7 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
   // out = sigmoid(g) u:  du, and dp's output-gate columns
   if (trace_call(kKTmOutGate, s, [&] {
         gate_out_bwd_kernel<<<blocks_for(d.M * d.Cz / 8), 256, 0, s>>>(
-            P, Fp, 4 * Ch, reinterpret_cast<const uint16_t*>(cx + c.u), static_cast<const uint16_t*>(d_out), du, dp,
+            G, Fp, 4 * Ch, reinterpret_cast<const uint16_t*>(cx + c.u), static_cast<const uint16_t*>(d_out), du, dp,
             Cz, d.M);
         return cudaGetLastError();
       }) != cudaSuccess)
@@ -732,9 +615,11 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
     if (cs == TRIATTN_OK) cs = contract(gws, s, d, false, false, A, dX, dB); // dB_c = A_c dX_c
   }
   if (cs != TRIATTN_OK) return cs;
-  // the gating:  dp's first 4 C_h columns
-  if (trace_call(kKTmGate, s, [&] {
-        return by_ch(d.Ch, [&](auto ic) { return L.template gate_bwd<decltype(ic)::value>(dA, dB, P, mk, dp); });
+  // the gating:  dp's first 4 C_h columns, the branch projections recomputed
+  // from x on the tensor cores
+  if (trace_call(kKTmProjGate, s, [&] {
+        return launch_gate_bwd_proj(static_cast<int>(d.B), static_cast<long long>(d.NN), Cz, Ch, cx + c.x, w_p, mk,
+                                    dA, dB, dp, Fp, current_wait_ctl(), s);
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // p = x W_p:  dW_p = x^T dp,  dx = dp W_p^T (FP32)

@@ -353,8 +353,9 @@ def test_module_rejects_bad_arguments(lib):
 def test_trimul_sizes_and_argument_checks(lib):
     ctx, ws = T.trimul_sizes(1, 40, 64, 32)
     M, Cz, Ch = 40 * 40, 64, 32
-    # ctx holds at least x, p, a, b, X, y and u
-    assert ctx >= M * Cz * 2 + M * (4 * Ch + Cz) * 2 + 3 * M * Ch * 2 + M * Ch * 2 + M * Cz * 2
+    # ctx holds at least x, g, a, b, X, y and u; the projection p is never stored
+    assert ctx >= M * Cz * 2 + M * Cz * 2 + 3 * M * Ch * 2 + M * Ch * 2 + M * Cz * 2
+    assert ctx < M * Cz * 2 + M * (4 * Ch + Cz) * 2 + 3 * M * Ch * 2 + M * Ch * 2 + M * Cz * 2
     assert ws >= (32 << 20) + M * (4 * Ch + Cz) * 2
     assert T.trimul_sizes(1, 40, 64, 32, "incoming") == (ctx, ws)
     for bad in [(1, 44, 64, 32), (1, 40, 48, 32), (1, 40, 64, 160), (1, 40, 64, 48), (0, 40, 64, 32)]:

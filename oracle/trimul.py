@@ -77,9 +77,9 @@ def split_projection(p, Ch):
 def contract(a, b, direction):
     """The per-channel contraction over the third token k."""
     if direction == "outgoing":
-        return np.einsum("bikc,bjkc->bijc", a, b)
+        return np.einsum("bikc,bjkc->bijc", a, b, optimize=True)
     if direction == "incoming":
-        return np.einsum("bkic,bkjc->bijc", a, b)
+        return np.einsum("bkic,bkjc->bijc", a, b, optimize=True)
     raise ValueError(direction)
 
 
@@ -119,11 +119,11 @@ def bwd(z, mask, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o, d_out, directio
     # the contraction
     a, b = f["a"], f["b"]
     if direction == "outgoing":
-        da = np.einsum("bijc,bjkc->bikc", dX, b)
-        db = np.einsum("bijc,bikc->bjkc", dX, a)
+        da = np.einsum("bijc,bjkc->bikc", dX, b, optimize=True)
+        db = np.einsum("bijc,bikc->bjkc", dX, a, optimize=True)
     else:
-        da = np.einsum("bijc,bkjc->bkic", dX, b)
-        db = np.einsum("bijc,bkic->bkjc", dX, a)
+        da = np.einsum("bijc,bkjc->bkic", dX, b, optimize=True)
+        db = np.einsum("bijc,bkic->bkjc", dX, a, optimize=True)
     # a = m sigmoid(a_g) a_v, b likewise
     sa, sb = sigmoid(ag), sigmoid(bg)
     dav = da * m * sa
@@ -136,7 +136,7 @@ def bwd(z, mask, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o, d_out, directio
     dx = dp @ w_p.T
     dz, dln_in_w, dln_in_b = layernorm_bwd(dx, f["xhat"], f["rstd"], ln_in_w)
     return {"dz": dz, "dln_in_w": dln_in_w, "dln_in_b": dln_in_b, "dw_p": dw_p, "dln_out_w": dln_out_w,
-            "dln_out_b": dln_out_b, "dw_o": dw_o}
+            "dln_out_b": dln_out_b, "dw_o": dw_o, "out": f["out"]}
 
 
 def fwd_pairs(z, mask, ln_in_w, ln_in_b, w_p, ln_out_w, ln_out_b, w_o, direction, pairs):

@@ -3,10 +3,11 @@
 on the same seeded BF16 inputs.
 
 Tolerances (relative RMSE against FP64): out <= 1e-2, every gradient
-<= 2e-2.  The CUDA path rounds to BF16 at x, p, the gated operands a and b,
-the contraction output X, y = LayerNorm(X), u and out (forward), and at du,
-dX, dA, dB and dp (backward); each rounding is a relative 2^-8 at most and
-the contraction accumulates in FP32.  Seven to eight such roundings in
+<= 2e-2.  The CUDA path rounds to BF16 at x, the gated operands a and b (the
+projection p stays in FP32 accumulators), g, the contraction output X,
+y = LayerNorm(X), u and out (forward), and at du, dX, dA, dB and dp
+(backward); each rounding is a relative 2^-8 at most, the gates use the
+hardware tanh (relative error about 2^-11), and the GEMMs accumulate in FP32.  Seven to eight such roundings in
 sequence give a few 1e-3, the bars leave a factor two to four.
 """
 import json
@@ -107,6 +108,26 @@ def test_trimul_bitwise_deterministic():
             else:
                 for a, b in zip(first, cur):
                     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("direction", ["outgoing", "incoming"])
+def test_trimul_full_size_every_element(direction):
+    """Table 10's largest shape (B=1, N=768, C_z=C_h=128, 8% padding tokens):
+    out and every gradient against the full FP64 oracle, element by element
+    (relative RMSE over the whole tensor)."""
+    B, N, C = 1, 768, 128
+    x = S.make_trimul_inputs(B, N, C, C, seed=1, pad_frac=0.08)
+    out, grads = run_gpu(x, direction)
+    args = (x["z"], x["mask"], x["ln_in_w"], x["ln_in_b"], x["w_p"], x["ln_out_w"], x["ln_out_b"], x["w_o"])
+    ref = TMO.bwd(*args, x["d_out"], direction)
+    errs = {"out": rel_rmse(cpu64(out), ref["out"])}
+    for name, g in zip(NAMES, grads):
+        errs[name] = rel_rmse(cpu64(g), ref[name])
+    print(json.dumps({"case": f"trimul N768 C128 {direction} every element",
+                      **{k: round(v, 6) for k, v in errs.items()}}))
+    assert errs["out"] <= TOL_OUT, errs
+    for name in NAMES:
+        assert errs[name] <= TOL_GRADS, (name, errs)
 
 
 @pytest.mark.parametrize("direction", ["outgoing", "incoming"])

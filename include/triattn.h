@@ -170,6 +170,55 @@ triattn_status tri_attn_bwd(const triattn_shape* shape,
                             void* stream);
 
 /*
+ * The same forward and backward on tensors in other row layouts, e.g. the
+ * heads of a projection's pair rows read and written where they lie (the
+ * module below), with results bitwise equal to the contiguous calls on the
+ * same values.
+ *
+ * A layout places row (b, o, h, n) of a [B, N_o, H, N, D] tensor, its D
+ * features contiguous, at element  slice * (b N_o + o) + head * h + row * n
+ * from the tensor's base pointer.  The contiguous layout of the calls above
+ * is {H N D, N D, D}; H heads side by side at column c of the pair rows of a
+ * row-major [B, N, N, ld] matrix are {N ld, D, ld} from base + c.
+ * Requirements (else TRIATTN_ERR_INVALID_ARG): every stride a positive
+ * multiple of 8 elements and the rows of one tensor disjoint, nested by
+ * stride -- with a = min(head, row), b = max(head, row) and n_a, n_b the
+ * counts of heads or rows they step over (H or N): (n_a - 1) a + D <= b and
+ * (n_b - 1) b + (n_a - 1) a + D <= slice < 2^36, head and row different
+ * unless H or N is 1 (both layouts above qualify).  The caller keeps the rows of one tensor from overlapping those
+ * of another that a call writes.
+ *   qkv_layout  q, k, v (forward and backward) and dq, dk, dv (backward)
+ *   o_layout    o and o_resid (forward and backward) and dO (backward)
+ * lse, bias, mask, dbias, the workspaces and every other rule are those of
+ * tri_attn_fwd / tri_attn_bwd.  The ablation entry points take the
+ * contiguous layout only.
+ */
+typedef struct {
+  long long slice; /* elements between consecutive (b, o) slices, index b N_o + o */
+  long long head;  /* elements between consecutive heads */
+  long long row;   /* elements between consecutive tokens n */
+} triattn_layout;
+
+triattn_status tri_attn_fwd_strided(const triattn_shape* shape,
+                                    const void* q, const void* k, const void* v,
+                                    const triattn_layout* qkv_layout,
+                                    const void* bias, const void* mask,
+                                    void* o, float* lse, void* o_resid,
+                                    const triattn_layout* o_layout,
+                                    void* workspace, size_t workspace_bytes,
+                                    void* stream);
+triattn_status tri_attn_bwd_strided(const triattn_shape* shape,
+                                    const void* q, const void* k, const void* v,
+                                    const triattn_layout* qkv_layout,
+                                    const void* bias, const void* mask,
+                                    const void* o, const void* o_resid,
+                                    const triattn_layout* o_layout,
+                                    const float* lse, const void* dO,
+                                    void* dq, void* dk, void* dv, void* dbias,
+                                    void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
  * Allocation-free backward.  The paper has no counterpart to this entry
  * point; it is a deployment convenience of this library.
  *
@@ -263,10 +312,11 @@ triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* p
  *
  * No projection biases and no gate; the residual update z + out is left to
  * the caller.  The projections are the library's tensor-core GEMM
- * (triattn_gemm: BF16 operands, FP32 accumulation); the LayerNorm, the
- * layout changes between the pair layout and the core's, and the LayerNorm's
- * parameter-gradient sums are the library's kernels; the core is
- * tri_attn_fwd / tri_attn_bwd.
+ * (triattn_gemm: BF16 operands, FP32 accumulation); the core is
+ * tri_attn_fwd_strided / tri_attn_bwd_strided, reading q, k, v from P's pair
+ * rows and writing o into o_flat, dq, dk, dv into dP's pair rows where they
+ * lie; the LayerNorm, the bias planes and the LayerNorm's parameter-gradient
+ * sums are the library's kernels.
  *
  * Shape: B >= 1, N as for the core (multiple of 8, 8..4096), B*N*N < 2^31,
  * C a multiple of 32 up to 256, H up to 64, D 16 or 32, flags 0.  Otherwise
@@ -280,8 +330,9 @@ triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* p
  *   d_w_in [C, 3HD + H] fp32, d_w_o [HD, C] fp32   (overwritten, not accumulated)
  *   mask  optional [B, N, N] bf16 additive key mask of each slice (the core's)
  *   ctx   triattn_module_ctx_bytes(shape) bytes, 256-byte aligned: written by
- *         the forward (x, the LayerNorm statistics, q, k, v, bias, o, lse, the
- *         output residual, o_flat), read by the backward of the same inputs.
+ *         the forward (x, the LayerNorm statistics, P, the bias planes, lse,
+ *         the output residual, o_flat), read by the backward of the same
+ *         inputs.
  *   workspace  triattn_module_workspace_bytes(shape) bytes, 256-byte
  *         aligned, contents ignored; either call may use it (it also serves
  *         for the GEMMs' split-K partials and the core's workspaces).

@@ -78,17 +78,50 @@ triattn_status check_shape(const triattn_shape* s) {
 // to a multiple of 8 for the padded copy (TMA needs 16-byte row strides).
 int padded_n(int N) { return (N + 7) / 8 * 8; }
 
-// 3-D map over a [slices, N, D] bf16 tensor, box = box_rows rows x D.
-bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s, unsigned box_rows = 128) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->D), static_cast<cuuint64_t>(s->N),
-                              static_cast<cuuint64_t>(s->B) * s->N_o * s->H};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s->D) * 2, static_cast<cuuint64_t>(s->N) * s->D * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(s->D), box_rows, 1u};
-  const cuuint32_t es[3] = {1u, 1u, 1u};
+// 4-D map over the rows of a [B, N_o, H, N, D] bf16 tensor in layout l, its
+// dimensions ordered by stride: (D, N, H, B*N_o) or, when the heads lie
+// closer together than the rows (l.hn), (D, H, N, B*N_o); box = box_rows
+// rows x D of one (slice, head).
+bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s, const RowLayout& l,
+                   unsigned box_rows = 128) {
+  const cuuint64_t D = static_cast<cuuint64_t>(s->D), N = static_cast<cuuint64_t>(s->N),
+                   H = static_cast<cuuint64_t>(s->H), S = static_cast<cuuint64_t>(s->B) * s->N_o;
+  const cuuint64_t row = static_cast<cuuint64_t>(l.row) * 2, head = static_cast<cuuint64_t>(l.head) * 2,
+                   slice = static_cast<cuuint64_t>(l.slice) * 2;
+  const cuuint64_t dims[4] = {D, l.hn ? H : N, l.hn ? N : H, S};
+  const cuuint64_t strides[3] = {l.hn ? head : row, l.hn ? row : head, slice};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(s->D), l.hn ? 1u : box_rows, l.hn ? box_rows : 1u, 1u};
+  const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
   const CUtensorMapSwizzle sw = (s->D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A caller's row layout: strides multiples of 8 elements (16-byte rows for
+// TMA and the vector accesses), nested without overlap -- the D features of
+// a row inside the smaller of the head and row strides, all rows (or heads)
+// of that kind inside the larger one, a whole slice inside the slice stride
+// (so the maps' dimensions are ordered by stride) -- and the slice stride
+// below 2^36 elements.
+bool layout_from(const triattn_layout* u, const triattn_shape* s, RowLayout* out) {
+  if (u == nullptr) {
+    *out = contiguous_layout(s->N, s->H, s->D);
+    return true;
+  }
+  const long long D = s->D, N = s->N, H = s->H;
+  if (u->slice <= 0 || u->head <= 0 || u->row <= 0 || ((u->slice | u->head | u->row) & 7) != 0) return false;
+  if (u->slice >= (1ll << 36)) return false;
+  // equal head and row strides only where one of them steps over a single
+  // head or row (H = 1 or N = 1)
+  if (u->head == u->row && H > 1 && N > 1) return false;
+  const bool hn = u->head < u->row || (u->head == u->row && H == 1);  // heads inside a row
+  const long long inner = hn ? u->head : u->row, outer = hn ? u->row : u->head;
+  const long long n_inner = hn ? H : N, n_outer = hn ? N : H;
+  if (inner < D || (n_inner - 1) * inner + D > outer || (n_outer - 1) * outer + (n_inner - 1) * inner + D > u->slice)
+    return false;
+  *out = RowLayout{u->slice, u->head, u->row, hn ? 1 : 0};
+  return true;
 }
 
 // 3-D map over a [B*H, N, ld] bf16 matrix (the bias, its padded copy or its
@@ -230,12 +263,15 @@ namespace {
 // The backward: atomic_mask 0 is the library's ordered path; 1, 2, 3, 4 and
 // 6 are the non-deterministic ablation (FP32 atomics for dQ, dbias, or both;
 // a TMA bulk reduction for dQ, alone or with atomic dbias).
-triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k, const void* v, const void* bias,
-                        const void* mask, const void* o, const void* o_resid, const float* lse, const void* dO,
+triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                        const triattn_layout* qkv_layout, const void* bias, const void* mask, const void* o,
+                        const void* o_resid, const triattn_layout* o_layout, const float* lse, const void* dO,
                         void* dq, void* dk, void* dv, void* dbias, int atomic_mask, void* workspace,
                         size_t workspace_bytes, void* stream) {
   triattn_status st = check_shape(shape);
   if (st != TRIATTN_OK) return st;
+  RowLayout lq, lo;
+  if (!layout_from(qkv_layout, shape, &lq) || !layout_from(o_layout, shape, &lo)) return TRIATTN_ERR_INVALID_ARG;
   const void* req[] = {q, k, v, bias, o, dO, dq, dk, dv, dbias};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
@@ -250,9 +286,12 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
   std::memset(&a, 0, sizeof(a));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.biasT = ws + w.biasT_off;
-  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape) || !make_rows_map(&a.tm_v, v, shape) ||
-      !make_rows_map(&a.tm_do, dO, shape) || !make_bias_map(&a.tm_biasT, a.biasT, shape, padded_n(shape->N)))
+  if (!make_rows_map(&a.tm_q, q, shape, lq) || !make_rows_map(&a.tm_k, k, shape, lq) ||
+      !make_rows_map(&a.tm_v, v, shape, lq) || !make_rows_map(&a.tm_do, dO, shape, lo) ||
+      !make_bias_map(&a.tm_biasT, a.biasT, shape, padded_n(shape->N)))
     return TRIATTN_ERR_CUDA;
+  a.lq = lq;
+  a.lo = lo;
   a.bias = bias;
   a.mask = mask;
   a.o = o;
@@ -322,11 +361,18 @@ size_t triattn_fwd_workspace_bytes(const triattn_shape* shape) {
   return fwd_ws(shape, true).total();
 }
 
-triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const void* k, const void* v,
-                            const void* bias, const void* mask, void* o, float* lse, void* o_resid,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+triattn_status fwd_impl(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                        const triattn_layout* qkv_layout, const void* bias, const void* mask, void* o, float* lse,
+                        void* o_resid, const triattn_layout* o_layout, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   triattn_status st = check_shape(shape);
   if (st != TRIATTN_OK) return st;
+  RowLayout lq, lo;
+  if (!layout_from(qkv_layout, shape, &lq) || !layout_from(o_layout, shape, &lo)) return TRIATTN_ERR_INVALID_ARG;
   const void* req[] = {q, k, v, bias, o};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
@@ -345,8 +391,10 @@ triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const voi
   a.bias_padded = fw.pad_bytes > 0 ? ws + fw.pad_off : nullptr;
   a.bias = bias;
   const void* bias_read = a.bias_padded != nullptr ? a.bias_padded : bias;
-  if (!make_rows_map(&a.tm_q, q, shape) || !make_rows_map(&a.tm_k, k, shape, 64) ||
-      !make_rows_map(&a.tm_v, v, shape, 64) ||
+  a.lq = lq;
+  a.lo = lo;
+  if (!make_rows_map(&a.tm_q, q, shape, lq) || !make_rows_map(&a.tm_k, k, shape, lq, 64) ||
+      !make_rows_map(&a.tm_v, v, shape, lq, 64) ||
       !make_bias_map(&a.tm_bias, bias_read, shape, a.bias_padded != nullptr ? padded_n(shape->N) : shape->N))
     return TRIATTN_ERR_CUDA;
   a.mask = mask;
@@ -367,12 +415,41 @@ triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const voi
   return e == cudaSuccess ? TRIATTN_OK : TRIATTN_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+triattn_status tri_attn_fwd(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                            const void* bias, const void* mask, void* o, float* lse, void* o_resid,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(shape, q, k, v, nullptr, bias, mask, o, lse, o_resid, nullptr, workspace, workspace_bytes, stream);
+}
+
+triattn_status tri_attn_fwd_strided(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                                    const triattn_layout* qkv_layout, const void* bias, const void* mask, void* o,
+                                    float* lse, void* o_resid, const triattn_layout* o_layout, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  if (qkv_layout == nullptr || o_layout == nullptr) return TRIATTN_ERR_INVALID_ARG;
+  return fwd_impl(shape, q, k, v, qkv_layout, bias, mask, o, lse, o_resid, o_layout, workspace, workspace_bytes,
+                  stream);
+}
+
 triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const void* k, const void* v,
                             const void* bias, const void* mask, const void* o, const void* o_resid, const float* lse,
                             const void* dO, void* dq, void* dk, void* dv, void* dbias, void* workspace,
                             size_t workspace_bytes, void* stream) {
-  return bwd_impl(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, 0, workspace, workspace_bytes,
-                  stream);
+  return bwd_impl(shape, q, k, v, nullptr, bias, mask, o, o_resid, nullptr, lse, dO, dq, dk, dv, dbias, 0, workspace,
+                  workspace_bytes, stream);
+}
+
+triattn_status tri_attn_bwd_strided(const triattn_shape* shape, const void* q, const void* k, const void* v,
+                                    const triattn_layout* qkv_layout, const void* bias, const void* mask,
+                                    const void* o, const void* o_resid, const triattn_layout* o_layout,
+                                    const float* lse, const void* dO, void* dq, void* dk, void* dv, void* dbias,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (qkv_layout == nullptr || o_layout == nullptr) return TRIATTN_ERR_INVALID_ARG;
+  return bwd_impl(shape, q, k, v, qkv_layout, bias, mask, o, o_resid, o_layout, lse, dO, dq, dk, dv, dbias, 0,
+                  workspace, workspace_bytes, stream);
 }
 
 size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask) {
@@ -387,8 +464,8 @@ triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape, const vo
                                             void* stream) {
   if (!atomic_mask_ok(atomic_mask)) return TRIATTN_ERR_INVALID_ARG;
   if (shape != nullptr && shape->flags != 0) return TRIATTN_ERR_INVALID_ARG;
-  return bwd_impl(shape, q, k, v, bias, mask, o, o_resid, lse, dO, dq, dk, dv, dbias, atomic_mask, workspace,
-                  workspace_bytes, stream);
+  return bwd_impl(shape, q, k, v, nullptr, bias, mask, o, o_resid, nullptr, lse, dO, dq, dk, dv, dbias, atomic_mask,
+                  workspace, workspace_bytes, stream);
 }
 
 triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* parts, int R, void* dbias,

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
                                                          const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ e,
                                                          const float* __restrict__ lse, uint4* __restrict__ rec,
-                                                         int N, int JQ, size_t padded_rows) {
+                                                         int N, int H, int JQ, size_t padded_rows, RowLayout lo) {
   // One 16-byte chunk (8 features) of one row per thread, so that a warp's
   // loads cover consecutive rows contiguously; the D/8 lanes of a row add
   // their partial sums with a fixed butterfly.
@@ -64,10 +64,12 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
   float xs = -1e30f, acc = 0.f;
   if (live) {
     const size_t row = slice * N + q;
-    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(dO + row * D) + c);
-    const uint4 ow = __ldg(reinterpret_cast<const uint4*>(o + row * D) + c);
+    const long long bo = static_cast<long long>(slice / H);
+    const long long off = lo.offset(bo, static_cast<int>(slice - bo * H), q);
+    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(dO + off) + c);
+    const uint4 ow = __ldg(reinterpret_cast<const uint4*>(o + off) + c);
     uint4 ew = make_uint4(0, 0, 0, 0);
-    if (e != nullptr) ew = __ldg(reinterpret_cast<const uint4*>(e + row * D) + c);
+    if (e != nullptr) ew = __ldg(reinterpret_cast<const uint4*>(e + off) + c);
     const uint32_t g4[4] = {gw.x, gw.y, gw.z, gw.w}, o4[4] = {ow.x, ow.y, ow.z, ow.w},
                    e4[4] = {ew.x, ew.y, ew.z, ew.w};
 #pragma unroll
@@ -232,7 +234,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_biasT, const uint16_t* __restrict__ mask,
                     const uint4* __restrict__ rec, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv,
-                    float* __restrict__ dq_part, float* __restrict__ dbias_part, int N_o, int N, int H, WaitCtl wc) {
+                    float* __restrict__ dq_part, float* __restrict__ dbias_part, int N_o, int N, int H, RowLayout lq,
+                    RowLayout lo, WaitCtl wc) {
   using L = BwdSmem<D>;
   constexpr int G = L::G;  // outer slices per CTA
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -393,9 +396,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       prefetch_tmap(&tm_biasT);
       mbar_expect_tx(&bars->kv_full, 2 * G * L::kTile);
       for (int g = 0; g < G; ++g) {
-        const int boh = (b * N_o + o0 + g) * H + h;
-        tma_load_3d(sm + L::kK + g * L::kTile, &tm_k, &bars->kv_full, 0, ktile * BN, boh);
-        tma_load_3d(sm + L::kV + g * L::kTile, &tm_v, &bars->kv_full, 0, ktile * BN, boh);
+        const int bo = b * N_o + o0 + g;
+        tma_load_rows(sm + L::kK + g * L::kTile, &tm_k, &bars->kv_full, lq.hn, ktile * BN, h, bo);
+        tma_load_rows(sm + L::kV + g * L::kTile, &tm_v, &bars->kv_full, lq.hn, ktile * BN, h, bo);
       }
     }
     __syncwarp();
@@ -424,8 +427,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (elect_one()) {
         const int boh = (b * N_o + o0 + g) * H + h;
         mbar_expect_tx(&bars->qdo_full[st], 2 * L::kTile + kRecTile);
-        tma_load_3d(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], 0, i * BM, boh);
-        tma_load_3d(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], 0, i * BM, boh);
+        tma_load_rows(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], lq.hn, i * BM, h, b * N_o + o0 + g);
+        tma_load_rows(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], lo.hn, i * BM, h, b * N_o + o0 + g);
         bulk_load(sm + L::kRec + st * kRecTile, rec + (static_cast<size_t>(min(boh, last_rec_slice)) * JQ + i) * BM,
                   kRecTile, &bars->qdo_full[st]);
       }
@@ -734,7 +737,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int g = wg; g < G; g += kNWG)
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const size_t row = (static_cast<size_t>((b * N_o + o0 + g) * H + h)) * N + key;
+        const long long off = lq.offset(b * N_o + o0 + g, h, key);
         const uint32_t t = tmem + lane_addr + which * G * D + g * D;
         const float sc = which == 0 ? 1.f : inv_sqrt_d;
         uint32_t w[D / 2];
@@ -752,7 +755,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             w[e] = pack_bf16x2(__uint_as_float(raw[2 * e]) * sc, __uint_as_float(raw[2 * e + 1]) * sc);
         }
         if (key < N && o0 + g < N_o) {
-          uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + row * D);
+          uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + off);
 #pragma unroll
           for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
@@ -775,13 +778,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 // memory, coalesced BF16 row writes.
 template <int D>
 __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict__ part, uint16_t* __restrict__ dq,
-                                                        int N, int JQ, int JK, size_t tiles) {
+                                                        int N, int H, int JQ, int JK, size_t tiles, RowLayout lq) {
   constexpr int kChunks = BM * D / 4;      // float4 per tile
   constexpr int kStride = D + 4;           // padded row stride (floats) of the transpose buffer
   __shared__ float tile[BM * kStride];
   const size_t t = blockIdx.x;             // tile = slice * JQ + i
   const int i = static_cast<int>(t % JQ);
   const size_t slice = t / JQ;
+  const long long bo = static_cast<long long>(slice / H);
+  const int h = static_cast<int>(slice - bo * H);
   for (int e = threadIdx.x; e < kChunks; e += blockDim.x) {
     const float4* p = part + t * kChunks + e;
     float4 acc = __ldcs(p);
@@ -804,7 +809,7 @@ __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict
     const float* src = &tile[r * kStride + 8 * c8];
     const uint4 w = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]), pack_bf16x2(src[4], src[5]),
                                pack_bf16x2(src[6], src[7]));
-    *reinterpret_cast<uint4*>(dq + (slice * N + q) * D + 8 * c8) = w;
+    *reinterpret_cast<uint4*>(dq + lq.offset(bo, h, q) + 8 * c8) = w;
   }
 }
 
@@ -925,7 +930,7 @@ __global__ void __launch_bounds__(256) dbias_combine_kernel(const float* __restr
 // thread per 8 outputs.
 template <int D>
 __global__ void __launch_bounds__(256) finish_dq_kernel(const float4* __restrict__ acc, uint16_t* __restrict__ dq,
-                                                        int N, int JQ, size_t rows) {
+                                                        int N, int H, int JQ, size_t rows, RowLayout lq) {
   const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= rows * (D / 8)) return;
   const size_t row = e / (D / 8);
@@ -934,7 +939,8 @@ __global__ void __launch_bounds__(256) finish_dq_kernel(const float4* __restrict
   const int q = static_cast<int>(row % N);
   const float4* src = acc + ((slice * JQ * BM + q) * D + 8 * c8) / 4;
   const float4 x = src[0], y = src[1];
-  *reinterpret_cast<uint4*>(dq + row * D + 8 * c8) =
+  const long long bo = static_cast<long long>(slice / H);
+  *reinterpret_cast<uint4*>(dq + lq.offset(bo, static_cast<int>(slice - bo * H), q) + 8 * c8) =
       make_uint4(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w), pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
 }
 
@@ -994,8 +1000,8 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
   const size_t padded = static_cast<size_t>(a.B) * a.N_o * a.H * JQ * BM;
   const unsigned grid = static_cast<unsigned>((padded * (D / 8) + 255) / 256);
   preprocess_kernel<D><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(a.dO), static_cast<const uint16_t*>(a.o),
-                                                 static_cast<const uint16_t*>(a.o_resid), a.lse, a.rec, a.N, JQ,
-                                                 padded);
+                                                 static_cast<const uint16_t*>(a.o_resid), a.lse, a.rec, a.N, a.H,
+                                                 JQ, padded, a.lo);
   return cudaGetLastError();
 }
 
@@ -1013,7 +1019,8 @@ cudaError_t launch_main_variant(const BwdArgs& a, cudaStream_t stream) {
   dim3 grid(JK, (a.N_o + BwdSmem<D>::G - 1) / BwdSmem<D>::G, a.B * a.H);
   bwd_main_kernel<D, kAtomic><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
-      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.wc);
+      static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.lq,
+      a.lo, a.wc);
   return cudaGetLastError();
 }
 
@@ -1038,7 +1045,7 @@ cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(a.B) * a.N_o * a.H * a.N;
   const size_t items = rows * (D / 8);
   finish_dq_kernel<D><<<static_cast<unsigned>((items + 255) / 256), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, JQ, rows);
+      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, a.H, JQ, rows, a.lq);
   return cudaGetLastError();
 }
 
@@ -1055,7 +1062,7 @@ cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
   const size_t tiles = static_cast<size_t>(a.B) * a.N_o * a.H * JQ;
   reduce_dq_kernel<D><<<static_cast<unsigned>(tiles), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, JQ, JK, tiles);
+      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, a.H, JQ, JK, tiles, a.lq);
   return cudaGetLastError();
 }
 

@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
                const uint8_t* __restrict__ mrec, uint16_t* __restrict__ out_o, float* __restrict__ out_lse,
-               uint16_t* __restrict__ out_resid, int N_o, int N, int H, int BH, int test_starve, WaitCtl wc) {
+               uint16_t* __restrict__ out_resid, int N_o, int N, int H, int BH, int test_starve, RowLayout lq,
+               RowLayout lo, WaitCtl wc) {
   using L = FwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->q_empty[qs], ((k >> 1) & 1) ^ 1, wc, abort)) break;
         mbar_expect_tx(&bars->q_full[qs], GF * L::kTileQ);
         for (int g = 0; g < GF; ++g)
-          tma_load_3d(sm + L::kQ + (qs * GF + g) * L::kTileQ, &tm_q, &bars->q_full[qs], 0, row0,
-                      (w.b * N_o + w.o0 + g) * H + w.h);
+          tma_load_rows(sm + L::kQ + (qs * GF + g) * L::kTileQ, &tm_q, &bars->q_full[qs], lq.hn, row0, w.h,
+                        w.b * N_o + w.o0 + g);
         for (int j = 0; j < JK && go; ++j) {
           if (!mbar_wait(&bars->b_empty[bst], bpar ^ 1, wc, abort)) { go = false; break; }
           mbar_expect_tx(&bars->b_full[bst], BM * BN * 2 + (mrec != nullptr ? GF * kFwdMaskRec : 0));
@@ -215,16 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &bars->b_full[bst]);
           const uint32_t par = spar ^ 1;
           for (int g = 0; g < GF && go; ++g) {
-            const int boh = (w.b * N_o + w.o0 + g) * H + w.h;
+            const int bo = w.b * N_o + w.o0 + g;
             if (!mbar_wait(&bars->k_empty[g][slot], par, wc, abort)) { go = false; break; }
             if (!(test_starve && k == 0 && j == 0 && g == 0)) {
               mbar_expect_tx(&bars->k_full[g][slot], L::kTileKV);
-              tma_load_3d(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], 0, j * BN,
-                          boh);
+              tma_load_rows(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], lq.hn,
+                            j * BN, w.h, bo);
             }
             if (!mbar_wait(&bars->v_empty[g][slot], par, wc, abort)) { go = false; break; }
             mbar_expect_tx(&bars->v_full[g][slot], L::kTileKV);
-            tma_load_3d(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], 0, j * BN, boh);
+            tma_load_rows(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], lq.hn, j * BN,
+                          w.h, bo);
           }
           if (++bst == NBIAS) { bst = 0; bpar ^= 1; }
           if (++slot == NSLOT) { slot = 0; spar ^= 1; }
@@ -518,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->o_free[g]);
         const Item w = item_of(k);  // the item's rows: computed here, no registers held in the loop
         const int q = w.qtile * BM + r;
-        const size_t row = (static_cast<size_t>((w.b * N_o + w.o0 + g) * H + w.h)) * N + q;
+        const int bo = w.b * N_o + w.o0 + g;
+        const size_t row = (static_cast<size_t>(bo) * H + w.h) * N + q;  // lse row
         if (q < N && w.o0 + g < N_o) {
           const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
           uint32_t ob[D / 2], eb[D / 2];
@@ -529,11 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ob[e] = w;
             eb[e] = pack_bf16x2(y0 - bf16lo_to_f32(w), y1 - bf16hi_to_f32(w));
           }
-          uint4* op = reinterpret_cast<uint4*>(out_o + row * D);
+          uint4* op = reinterpret_cast<uint4*>(out_o + lo.offset(bo, w.h, q));
   #pragma unroll
           for (int v4 = 0; v4 < D / 8; ++v4) op[v4] = make_uint4(ob[4 * v4], ob[4 * v4 + 1], ob[4 * v4 + 2], ob[4 * v4 + 3]);
           if (out_resid != nullptr) {
-            uint4* ep = reinterpret_cast<uint4*>(out_resid + row * D);
+            uint4* ep = reinterpret_cast<uint4*>(out_resid + lo.offset(bo, w.h, q));
   #pragma unroll
             for (int v4 = 0; v4 < D / 8; ++v4)
               ep[v4] = make_uint4(eb[4 * v4], eb[4 * v4 + 1], eb[4 * v4 + 2], eb[4 * v4 + 3]);
@@ -638,7 +641,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(std::min<long long>(total, sms));
   fwd_kernel<D><<<grid, kThreads, FwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_bias, a.mrec, static_cast<uint16_t*>(a.o), a.lse,
-      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.B * a.H, a.test_starve, a.wc);
+      static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.B * a.H, a.test_starve, a.lq, a.lo, a.wc);
   return cudaGetLastError();
 }
 

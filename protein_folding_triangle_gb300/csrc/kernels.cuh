@@ -21,6 +21,30 @@ constexpr int kGroupFwd = 4;
 // its 512 columns next to 256 for S^T and dP^T), so G = 8 at D = 16.
 constexpr int kGroupBwdFor(int D) { return D == 16 ? 8 : 4; }
 
+// Where the rows of a [B, N_o, H, N, D] tensor (D features contiguous) lie:
+// row (b, o, h, n) starts slice * (b N_o + o) + head * h + row * n elements
+// from the base.  The library's own layout is {H N D, N D, D}; the
+// triangle-attention module's pair rows are {N ld, D, ld}.  Q, K, V (and dO)
+// tiles are loaded through 4-D tensor maps whose dimensions are ordered by
+// stride: (D, N, H, B N_o) when head > row (hn = 0), else (D, H, N, B N_o)
+// (hn = 1); tma_load_rows gives a row tile's coordinates in that order.
+struct RowLayout {
+  long long slice, head, row;
+  int hn;
+  __host__ __device__ long long offset(long long bo, int h, long long n) const {
+    return bo * slice + h * head + n * row;
+  }
+};
+inline RowLayout contiguous_layout(int N, int H, int D) {
+  return RowLayout{static_cast<long long>(H) * N * D, static_cast<long long>(N) * D, D, 0};
+}
+// Rows [n0, n0 + box) of slice bo, head h through a map of the layout above.
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar, int hn, int n0, int h,
+                                              int bo) {
+  if (hn) tma_load_4d(dst, map, bar, 0, h, n0, bo);
+  else tma_load_4d(dst, map, bar, 0, n0, h, bo);
+}
+
 // Forward key-mask record per (slice, 64-key tile): 64 BF16 mask values, then
 // a 16-byte header whose first word is nonzero when any value is.
 constexpr int kFwdMaskRec = 64 * 2 + 16;
@@ -34,6 +58,8 @@ struct FwdArgs {
   void* o;
   float* lse;
   void* o_resid;
+  RowLayout lq;      // q, k, v
+  RowLayout lo;      // o, o_resid
   int B, N_o, N, H;
   int test_starve;   // test hook: skip the first K-tile load
   WaitCtl wc;
@@ -55,6 +81,8 @@ struct BwdArgs {
   uint4* rec;        // [slices][J_Q * 128] query-row records (BF16 splits of -lse sqrt(D), -delta)
   float* dq_part;    // [J_K][slices][J_Q][128 x D]
   float* dbias_part; // [L][B*H*N*N]
+  RowLayout lq;      // q, k, v, dq, dk, dv
+  RowLayout lo;      // o, o_resid, dO
   int B, N_o, N, H, D;
   int dbias_fp32;    // write dbias as FP32 (the sum over this call's slices)
   WaitCtl wc;

@@ -29,49 +29,6 @@ namespace {
 
 using namespace pairops;
 
-// Pair layout -> core layout for nblk consecutive H*D blocks of a row-major
-// [M, ld] matrix: dst_t[b, i, h, j, d] = src[(b, i, j), off + t H D + h D + d]
-// for t < nblk, 8 features per thread.
-__global__ void __launch_bounds__(256) heads_split_kernel(const uint16_t* __restrict__ src, int ld, int off,
-                                                          uint16_t* __restrict__ dst0, uint16_t* __restrict__ dst1,
-                                                          uint16_t* __restrict__ dst2, int nblk, int N, int H, int D,
-                                                          size_t M) {
-  const int per = H * D / 8;
-  const int chunks = nblk * per;
-  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= M * chunks) return;
-  const size_t m = t / chunks;
-  const int c = static_cast<int>(t % chunks);
-  const int blk = c / per, cc = c % per;
-  const int h = (8 * cc) / D, d0 = (8 * cc) % D;
-  const size_t bi = m / N;
-  const int j = static_cast<int>(m % N);
-  uint16_t* dst = blk == 0 ? dst0 : (blk == 1 ? dst1 : dst2);
-  const uint4 w = *reinterpret_cast<const uint4*>(src + m * ld + off + 8 * c);
-  *reinterpret_cast<uint4*>(dst + ((bi * H + h) * N + j) * D + d0) = w;
-}
-
-// Core layout -> pair layout: dst[(b, i, j), off + t H D + h D + d] = src_t[b, i, h, j, d].
-__global__ void __launch_bounds__(256) heads_merge_kernel(const uint16_t* __restrict__ src0,
-                                                          const uint16_t* __restrict__ src1,
-                                                          const uint16_t* __restrict__ src2, int nblk,
-                                                          uint16_t* __restrict__ dst, int ld, int off, int N, int H,
-                                                          int D, size_t M) {
-  const int per = H * D / 8;
-  const int chunks = nblk * per;
-  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= M * chunks) return;
-  const size_t m = t / chunks;
-  const int c = static_cast<int>(t % chunks);
-  const int blk = c / per, cc = c % per;
-  const int h = (8 * cc) / D, d0 = (8 * cc) % D;
-  const size_t bi = m / N;
-  const int j = static_cast<int>(m % N);
-  const uint16_t* src = blk == 0 ? src0 : (blk == 1 ? src1 : src2);
-  *reinterpret_cast<uint4*>(dst + m * ld + off + 8 * c) =
-      *reinterpret_cast<const uint4*>(src + ((bi * H + h) * N + j) * D + d0);
-}
-
 // bias[b, h, q, k] = pairs[(b, q, k), off + h]   (to_pairs = false)
 // pairs[(b, q, k), off + h] = bias[b, h, q, k]   (to_pairs = true)
 // One thread per pair: its H values share one sector of the pair row, and
@@ -125,45 +82,43 @@ ModDims dims_of(const triattn_module_shape* s) {
 }
 
 // Saved between forward and backward (the caller's "context" buffer).
+// q, k, v stay in P's pair rows and o, its residual and dO in pair rows of
+// H*D features: the core reads and writes them there (tri_attn_*_strided).
 struct CtxLayout {
-  size_t x, mean, rstd, q, k, v, bias, o, lse, resid, oflat, total;
+  size_t x, mean, rstd, p, bias, lse, resid, oflat, total;
 };
 CtxLayout ctx_layout(const ModDims& d) {
-  const size_t act = d.B * d.N * d.H * d.N * d.D * 2;  // one [B, N, H, N, D] bf16 tensor
   CtxLayout c;
   size_t o = 0;
   c.x = o;     o += rup(d.M * d.C * 2);
   c.mean = o;  o += rup(d.M * 4);
   c.rstd = o;  o += rup(d.M * 4);
-  c.q = o;     o += rup(act);
-  c.k = o;     o += rup(act);
-  c.v = o;     o += rup(act);
+  c.p = o;     o += rup(d.M * d.Fp * 2);
   c.bias = o;  o += rup(d.B * d.H * d.N * d.N * 2);
-  c.o = o;     o += rup(act);
   c.lse = o;   o += rup(d.B * d.N * d.H * d.N * 4);
-  c.resid = o; o += rup(act);
+  c.resid = o; o += rup(d.M * d.HD * 2);
   c.oflat = o; o += rup(d.M * d.HD * 2);
   c.total = o;
   return c;
 }
+// q, k, v (and dq, dk, dv) in pair rows of ld = Fp; o, its residual and dO in
+// pair rows of ld = H*D
+triattn_layout pair_layout(const ModDims& d, size_t ld) {
+  return triattn_layout{static_cast<long long>(d.N * ld), static_cast<long long>(d.D), static_cast<long long>(ld)};
+}
 
 // Scratch of one forward or backward call.
 struct WsLayout2 {
-  size_t gemm, w_in_pad, dw_in_pad, p, doflat, dobuf, dq, dk, dv, dbias, dx, pg, pb, core, total;
+  size_t gemm, w_in_pad, dw_in_pad, p, doflat, dbias, dx, pg, pb, core, total;
 };
 WsLayout2 ws_layout2(const ModDims& d, const triattn_shape& core) {
-  const size_t act = d.B * d.N * d.H * d.N * d.D * 2;
   WsLayout2 w;
   size_t o = 0;
   w.gemm = o;   o += rup(kGemmWorkspace);
   w.w_in_pad = o;  o += rup(d.C * d.Fp * 2);   // W_in with zero columns up to Fp
   w.dw_in_pad = o; o += rup(d.C * d.Fp * 4);   // dW_in, Fp wide
-  w.p = o;      o += rup(d.M * d.Fp * 2);  // P (forward) / dP (backward)
+  w.p = o;      o += rup(d.M * d.Fp * 2);  // dP (backward)
   w.doflat = o; o += rup(d.M * d.HD * 2);
-  w.dobuf = o;  o += rup(act);
-  w.dq = o;     o += rup(act);
-  w.dk = o;     o += rup(act);
-  w.dv = o;     o += rup(act);
   w.dbias = o;  o += rup(d.B * d.H * d.N * d.N * 2);
   w.dx = o;     o += rup(d.M * d.C * 4);
   w.pg = o;     o += rup(static_cast<size_t>(kLnBlocks) * d.C * 4);
@@ -192,24 +147,6 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 unsigned blocks_for(size_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
-// nblk (1 or 3) consecutive H*D blocks of the pair rows, to / from as many
-// [B, N, H, N, D] tensors.
-cudaError_t split_heads(const ModDims& d, const uint16_t* src, int ld, int off, int nblk, uint16_t* d0, uint16_t* d1,
-                        uint16_t* d2, cudaStream_t s) {
-  return trace_call(kKModLayout, s, [&] {
-    heads_split_kernel<<<blocks_for(d.M * nblk * (d.HD / 8)), 256, 0, s>>>(
-        src, ld, off, d0, d1, d2, nblk, static_cast<int>(d.N), static_cast<int>(d.H), static_cast<int>(d.D), d.M);
-    return cudaGetLastError();
-  });
-}
-cudaError_t merge_heads(const ModDims& d, const uint16_t* s0, const uint16_t* s1, const uint16_t* s2, int nblk,
-                        uint16_t* dst, int ld, int off, cudaStream_t s) {
-  return trace_call(kKModLayout, s, [&] {
-    heads_merge_kernel<<<blocks_for(d.M * nblk * (d.HD / 8)), 256, 0, s>>>(
-        s0, s1, s2, nblk, dst, ld, off, static_cast<int>(d.N), static_cast<int>(d.H), static_cast<int>(d.D), d.M);
-    return cudaGetLastError();
-  });
-}
 cudaError_t bias_planes(const ModDims& d, uint16_t* pairs, int ld, int off, uint16_t* bias, bool to_pairs,
                         cudaStream_t s) {
   return trace_call(kKModLayout, s, [&] {
@@ -271,7 +208,7 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
             Fp = static_cast<int>(d.Fp);
   float* mean = reinterpret_cast<float*>(cx + c.mean);
   float* rstd = reinterpret_cast<float*>(cx + c.rstd);
-  uint16_t* P = reinterpret_cast<uint16_t*>(ws + w.p);
+  uint16_t* P = reinterpret_cast<uint16_t*>(cx + c.p);
   // x = LayerNorm(z)
   if (trace_call(kKModLnFwd, s, [&] { return ln_rows_fwd(d.M, C, z, ln_w, ln_b, cx + c.x, mean, rstd, s); }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
@@ -283,20 +220,17 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   if (gemm_traced(kKModGemm, gws, s, false, false, M, Fp, C, cx + c.x, C, w_in_pad, Fp, P, Fp, false) !=
       TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
-  // q, k, v and the bias planes
-  if (split_heads(d, P, Fp, 0, 3, reinterpret_cast<uint16_t*>(cx + c.q), reinterpret_cast<uint16_t*>(cx + c.k),
-                  reinterpret_cast<uint16_t*>(cx + c.v), s) != cudaSuccess)
-    return TRIATTN_ERR_CUDA;
+  // the bias planes
   if (bias_planes(d, P, Fp, 3 * HD, reinterpret_cast<uint16_t*>(cx + c.bias), false, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  // the attention core
-  st = tri_attn_fwd(&core, cx + c.q, cx + c.k, cx + c.v, cx + c.bias, mask, cx + c.o,
-                    reinterpret_cast<float*>(cx + c.lse), cx + c.resid, ws + w.core, w.total - w.core, stream);
+  // the attention core: q, k, v read from P's pair rows, o (and its
+  // residual) written into o_flat's
+  const triattn_layout lq = pair_layout(d, d.Fp), lo = pair_layout(d, d.HD);
+  st = tri_attn_fwd_strided(&core, P, P + HD, P + 2 * HD, &lq, cx + c.bias, mask, cx + c.oflat,
+                            reinterpret_cast<float*>(cx + c.lse), cx + c.resid, &lo, ws + w.core, w.total - w.core,
+                            stream);
   if (st != TRIATTN_OK) return st;
   // out = o_flat W_o
-  const uint16_t* o_core = reinterpret_cast<const uint16_t*>(cx + c.o);
-  if (merge_heads(d, o_core, o_core, o_core, 1, reinterpret_cast<uint16_t*>(cx + c.oflat), HD, 0, s) != cudaSuccess)
-    return TRIATTN_ERR_CUDA;
   return gemm_traced(kKModGemm, gws, s, false, false, M, C, HD, cx + c.oflat, HD, w_o, C, out, C, false);
 }
 
@@ -327,20 +261,15 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   if (gemm_traced(kKModGemm, gws, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, true) != TRIATTN_OK ||
       gemm_traced(kKModGemm, gws, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, false) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
-  uint16_t* dobuf = reinterpret_cast<uint16_t*>(ws + w.dobuf);
-  if (split_heads(d, reinterpret_cast<const uint16_t*>(ws + w.doflat), HD, 0, 1, dobuf, dobuf, dobuf, s) !=
-      cudaSuccess)
-    return TRIATTN_ERR_CUDA;
-  // the attention core
-  st = tri_attn_bwd(&core, cx + c.q, cx + c.k, cx + c.v, cx + c.bias, mask, cx + c.o, cx + c.resid,
-                    reinterpret_cast<const float*>(cx + c.lse), ws + w.dobuf, ws + w.dq, ws + w.dk, ws + w.dv,
-                    ws + w.dbias, ws + w.core, w.total - w.core, stream);
-  if (st != TRIATTN_OK) return st;
-  // dP = [dq | dk | dv | dbias] in the pair layout
+  // the attention core, dq, dk, dv written into dP = [dq | dk | dv | dbias]
+  // where they lie in the pair layout
+  const uint16_t* P = reinterpret_cast<const uint16_t*>(cx + c.p);
   uint16_t* dP = reinterpret_cast<uint16_t*>(ws + w.p);
-  if (merge_heads(d, reinterpret_cast<const uint16_t*>(ws + w.dq), reinterpret_cast<const uint16_t*>(ws + w.dk),
-                  reinterpret_cast<const uint16_t*>(ws + w.dv), 3, dP, Fp, 0, s) != cudaSuccess)
-    return TRIATTN_ERR_CUDA;
+  const triattn_layout lq = pair_layout(d, d.Fp), lo = pair_layout(d, d.HD);
+  st = tri_attn_bwd_strided(&core, P, P + HD, P + 2 * HD, &lq, cx + c.bias, mask, cx + c.oflat, cx + c.resid, &lo,
+                            reinterpret_cast<const float*>(cx + c.lse), ws + w.doflat, dP, dP + HD, dP + 2 * HD,
+                            ws + w.dbias, ws + w.core, w.total - w.core, stream);
+  if (st != TRIATTN_OK) return st;
   if (bias_planes(d, dP, Fp, 3 * HD, reinterpret_cast<uint16_t*>(ws + w.dbias), true, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
   // P = x W_in:  dW_in = x^T dP,  dx = dP W_in^T (FP32), both Fp wide (dP's

@@ -37,7 +37,8 @@ EXPORTED = ("triattn_status_string", "triattn_fwd_workspace_bytes", "triattn_bwd
             "tri_attn_bwd_atomic_ablation", "tri_attn_dbias_combine", "triattn_module_ctx_bytes",
             "triattn_module_workspace_bytes", "tri_attn_module_fwd", "tri_attn_module_bwd",
             "triattn_trimul_ctx_bytes", "triattn_trimul_workspace_bytes", "triattn_trimul_fwd",
-            "triattn_trimul_bwd", "triattn_gemm_workspace_bytes", "triattn_gemm")
+            "triattn_trimul_bwd", "triattn_gemm_workspace_bytes", "triattn_gemm", "tri_attn_fwd_strided",
+            "tri_attn_bwd_strided")
 
 FLAG_DBIAS_FP32 = 1
 
@@ -58,6 +59,12 @@ class TriAttnError(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("N_o", ctypes.c_int), ("N", ctypes.c_int), ("H", ctypes.c_int),
                 ("D", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+class Layout(ctypes.Structure):
+    """triattn_layout: row (b, o, h, n) of a [B, N_o, H, N, D] tensor starts
+    slice * (b N_o + o) + head * h + row * n elements from its base."""
+    _fields_ = [("slice", ctypes.c_longlong), ("head", ctypes.c_longlong), ("row", ctypes.c_longlong)]
 
 
 class ModuleShape(ctypes.Structure):
@@ -84,6 +91,12 @@ def _declare(lib):
     lib.tri_attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.tri_attn_fwd.restype = ctypes.c_int
     lib.tri_attn_bwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lp = ctypes.POINTER(Layout)
+    lib.tri_attn_fwd_strided.argtypes = [sp, vp, vp, vp, lp, vp, vp, vp, vp, vp, lp, vp, ctypes.c_size_t, vp]
+    lib.tri_attn_fwd_strided.restype = ctypes.c_int
+    lib.tri_attn_bwd_strided.argtypes = ([sp, vp, vp, vp, lp, vp, vp, vp, vp, lp, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.c_size_t, vp])
+    lib.tri_attn_bwd_strided.restype = ctypes.c_int
     lib.tri_attn_bwd.restype = ctypes.c_int
     lib.triattn_device_status.argtypes = [vp]
     lib.triattn_device_status.restype = ctypes.c_int
@@ -250,6 +263,81 @@ def tri_attn_bwd(q, k, v, bias, mask, o, o_resid, lse, do, *, workspace=None, ou
                                _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                                _stream_ptr(stream))
     _raise(code, "tri_attn_bwd")
+    return dq, dk, dv, dbias
+
+
+def layout_of(t: torch.Tensor) -> Layout:
+    """The row layout of a [B, N_o, H, N, D] view whose D features are
+    contiguous and whose b stride is N_o times its o stride (e.g. the heads of
+    pair rows: ``P.view(B, N, N, ld)[..., c:c + H*D].unflatten(-1, (H, D))
+    .permute(0, 1, 3, 2, 4)``)."""
+    if t.dim() != 5 or t.stride(4) != 1:
+        raise ValueError("expected a [B, N_o, H, N, D] view with contiguous features")
+    if t.shape[0] > 1 and t.stride(0) != t.shape[1] * t.stride(1):
+        raise ValueError("the b stride must be N_o times the o stride")
+    return Layout(t.stride(1), t.stride(2), t.stride(3))
+
+
+def _check_view(t, name, shape, lay: Layout):
+    if t is None or not t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a bf16 CUDA view of shape {tuple(shape)}")
+    got = layout_of(t)
+    if (got.slice, got.head, got.row) != (lay.slice, lay.head, lay.row):
+        raise ValueError(f"{name} does not share the layout of its group")
+
+
+def tri_attn_fwd_strided(q, k, v, bias, mask, o, lse, o_resid=None, *, workspace=None, stream=None):
+    """Forward on views: q, k, v share one row layout, o and o_resid another
+    (both [B, N_o, H, N, D] views, written in place); lse [B, N_o, H, N] fp32
+    contiguous.  Bitwise the same results as tri_attn_fwd on copies."""
+    s = shape_of(q)
+    B, No, H, N, D = q.shape
+    lq, lo = layout_of(q), layout_of(o)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_view(t, name, (B, No, H, N, D), lq)
+    for name, t in (("o", o), ("o_resid", o_resid)):
+        if t is not None:
+            _check_view(t, name, (B, No, H, N, D), lo)
+    _check(bias, "bias", (B, H, N, N))
+    _check(lse, "lse", (B, No, H, N), torch.float32)
+    if mask is not None:
+        _check(mask, "mask", (B, No, N))
+    if workspace is None:
+        need = fwd_workspace_bytes(s)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = load().tri_attn_fwd_strided(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), ctypes.byref(lq), _ptr(bias),
+                                       _ptr(mask), _ptr(o), _ptr(lse), _ptr(o_resid), ctypes.byref(lo),
+                                       _ptr(workspace), ctypes.c_size_t(nbytes), _stream_ptr(stream))
+    _raise(code, "tri_attn_fwd_strided")
+    return o, lse, o_resid
+
+
+def tri_attn_bwd_strided(q, k, v, bias, mask, o, o_resid, lse, do, dq, dk, dv, dbias, *, workspace=None,
+                         stream=None):
+    """Backward on views: q, k, v, dq, dk, dv share one row layout; o, o_resid
+    and do another; dq, dk, dv and dbias ([B, H, N, N] bf16) written in place."""
+    s = shape_of(q)
+    B, No, H, N, D = q.shape
+    lq, lo = layout_of(q), layout_of(o)
+    for name, t in (("q", q), ("k", k), ("v", v), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_view(t, name, (B, No, H, N, D), lq)
+    for name, t in (("o", o), ("o_resid", o_resid), ("do", do)):
+        if t is not None:
+            _check_view(t, name, (B, No, H, N, D), lo)
+    _check(bias, "bias", (B, H, N, N))
+    _check(dbias, "dbias", (B, H, N, N))
+    _check(lse, "lse", (B, No, H, N), torch.float32)
+    if mask is not None:
+        _check(mask, "mask", (B, No, N))
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_bytes(s), dtype=torch.uint8, device=q.device)
+    code = load().tri_attn_bwd_strided(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), ctypes.byref(lq), _ptr(bias),
+                                       _ptr(mask), _ptr(o), _ptr(o_resid), ctypes.byref(lo), _ptr(lse), _ptr(do),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
+                                       ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                       _stream_ptr(stream))
+    _raise(code, "tri_attn_bwd_strided")
     return dq, dk, dv, dbias
 
 

@@ -323,9 +323,10 @@ def call_module_bwd(lib, shape, ws_bytes, ws=FAKE, **ptrs):
 def test_module_sizes(lib):
     ctx, ws = T.module_sizes(1, 40, 64, 2, 16)
     B_, N, C, H, D = 1, 40, 64, 2, 16
-    act = B_ * N * H * N * D * 2
-    # ctx holds at least x, q, k, v, o, the residual, o_flat and the bias planes
-    assert ctx >= B_ * N * N * C * 2 + 5 * act + B_ * N * N * H * D * 2 + B_ * H * N * N * 2
+    M, Fp = B_ * N * N, (3 * H * D + H + 7) // 8 * 8
+    # ctx holds at least x, P (q, k, v are read where they lie in it), the
+    # residual, o_flat (the core writes o there) and the bias planes
+    assert ctx >= M * C * 2 + M * Fp * 2 + 2 * M * H * D * 2 + B_ * H * N * N * 2
     core = T.bwd_workspace_bytes(T.Shape(B_, N, N, H, D, 0))
     assert ws >= core + (32 << 20) + B_ * N * N * (3 * H * D + H) * 2
     for bad in [(1, 40, 48, 2, 16), (1, 40, 288, 2, 16), (1, 44, 64, 2, 16), (1, 40, 64, 2, 8), (0, 40, 64, 2, 16),
@@ -434,3 +435,63 @@ def test_gemm_argument_checks(lib):
     assert call(ldc=64) == T.ERR_INVALID_ARG          # ldc < N
     assert call(A=None) == T.ERR_INVALID_ARG
     assert lib.triattn_gemm_workspace_bytes(0, 1, 1, 1) == 0
+
+
+def test_strided_layout_checks(lib):
+    """tri_attn_fwd_strided / tri_attn_bwd_strided reject layouts the kernels
+    cannot address (strides not multiples of 8 elements, overlapping rows,
+    heads or slices) before any GPU work; the layouts of a contiguous tensor
+    and of heads in pair rows pass validation (the call then fails on the
+    missing workspace of this ragged shape)."""
+    s = T.Shape(1, 40, 40, 2, 32, 0)
+    f = ctypes.c_void_p(FAKE)
+
+    def fwd(lq, lo, ws=None, nbytes=0):
+        return lib.tri_attn_fwd_strided(ctypes.byref(s), f, f, f, lq, f, f, f, f, None, lo, ws,
+                                        ctypes.c_size_t(nbytes), None)
+
+    def bwd(lq, lo):
+        return lib.tri_attn_bwd_strided(ctypes.byref(s), f, f, f, lq, f, None, f, None, lo, f, f, f, f, f, f,
+                                        None, ctypes.c_size_t(0), None)
+
+    good = T.Layout(2 * 40 * 32, 40 * 32, 32)       # [B, N_o, H, N, D]
+    pair = T.Layout(40 * 200, 32, 200)              # heads side by side in pair rows of 200
+    bad = [T.Layout(2 * 40 * 32, 40 * 32, 36),      # row not a multiple of 8
+           T.Layout(2 * 40 * 32, 40 * 32, 24),      # rows overlap (row < D)
+           T.Layout(2 * 40 * 32, 16, 200),          # heads overlap (head < D)
+           T.Layout(40 * 200, 200, 200),            # head == row
+           T.Layout(1000, 32, 200),                 # slices overlap (40 rows of 200 > 1000)
+           T.Layout(40 * 200, 32, 56),              # the two heads of a row overlap (32 + 32 > 56)
+           T.Layout(2 * 40 * 32, 40 * 32 - 8, 32),  # the rows of a head run into the next head
+           T.Layout(0, 32, 200),
+           T.Layout(1 << 36, 32, 200)]              # beyond the index range
+    for lay in bad:
+        assert fwd(ctypes.byref(lay), ctypes.byref(good)) == T.ERR_INVALID_ARG
+        assert fwd(ctypes.byref(good), ctypes.byref(lay)) == T.ERR_INVALID_ARG
+        assert bwd(ctypes.byref(lay), ctypes.byref(good)) == T.ERR_INVALID_ARG
+        assert bwd(ctypes.byref(good), ctypes.byref(lay)) == T.ERR_INVALID_ARG
+    # a null layout is an argument error on the strided entry points
+    assert fwd(None, ctypes.byref(good)) == T.ERR_INVALID_ARG
+    assert bwd(ctypes.byref(pair), None) == T.ERR_INVALID_ARG
+    # one head: its head stride may equal the row stride
+    s1 = T.Shape(1, 40, 40, 1, 32, 0)
+    one = T.Layout(40 * 32, 32, 32)
+    assert lib.tri_attn_fwd_strided(ctypes.byref(s1), f, f, f, ctypes.byref(one), f, f, f, f, None,
+                                    ctypes.byref(one), None, ctypes.c_size_t(0), None) == T.ERR_WORKSPACE
+    # valid layouts get as far as the workspace check (N = 40 needs the padded bias copy)
+    assert fwd(ctypes.byref(pair), ctypes.byref(good)) == T.ERR_WORKSPACE
+    assert bwd(ctypes.byref(pair), ctypes.byref(pair)) == T.ERR_WORKSPACE
+
+
+def test_layout_of_views():
+    """layout_of reads the row layout off a [B, N_o, H, N, D] view."""
+    B, N, H, D, ld = 2, 24, 3, 16, 200
+    P = torch.zeros(B, N, N, ld, dtype=torch.bfloat16)
+    q = P[..., 8:8 + H * D].unflatten(-1, (H, D)).permute(0, 1, 3, 2, 4)
+    lay = T.layout_of(q)
+    assert (lay.slice, lay.head, lay.row) == (N * ld, D, ld)
+    c = torch.zeros(B, N, H, N, D, dtype=torch.bfloat16)
+    lay = T.layout_of(c)
+    assert (lay.slice, lay.head, lay.row) == (H * N * D, N * D, D)
+    with pytest.raises(ValueError):
+        T.layout_of(c.transpose(3, 4))

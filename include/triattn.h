@@ -185,7 +185,8 @@ triattn_status tri_attn_bwd(const triattn_shape* shape,
  * stride -- with a = min(head, row), b = max(head, row) and n_a, n_b the
  * counts of heads or rows they step over (H or N): (n_a - 1) a + D <= b and
  * (n_b - 1) b + (n_a - 1) a + D <= slice < 2^36, head and row different
- * unless H or N is 1 (both layouts above qualify).  The caller keeps the rows of one tensor from overlapping those
+ * unless H or N is 1, and slice = H head when head > row (both layouts above
+ * qualify).  The caller keeps the rows of one tensor from overlapping those
  * of another that a call writes.
  *   qkv_layout  q, k, v (forward and backward) and dq, dk, dv (backward)
  *   o_layout    o and o_resid (forward and backward) and dO (backward)

@@ -78,21 +78,29 @@ triattn_status check_shape(const triattn_shape* s) {
 // to a multiple of 8 for the padded copy (TMA needs 16-byte row strides).
 int padded_n(int N) { return (N + 7) / 8 * 8; }
 
-// 4-D map over the rows of a [B, N_o, H, N, D] bf16 tensor in layout l, its
-// dimensions ordered by stride: (D, N, H, B*N_o) or, when the heads lie
-// closer together than the rows (l.hn), (D, H, N, B*N_o); box = box_rows
-// rows x D of one (slice, head).
+// Map over the rows of a [B, N_o, H, N, D] bf16 tensor in layout l, box =
+// box_rows rows x D of one (slice, head): 3-D (D, N, B*N_o*H) when the rows
+// lie inside the heads (slice = H head), 4-D (D, H, N, B*N_o) when the heads
+// lie inside the rows (l.hn).
 bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s, const RowLayout& l,
                    unsigned box_rows = 128) {
   const cuuint64_t D = static_cast<cuuint64_t>(s->D), N = static_cast<cuuint64_t>(s->N),
                    H = static_cast<cuuint64_t>(s->H), S = static_cast<cuuint64_t>(s->B) * s->N_o;
   const cuuint64_t row = static_cast<cuuint64_t>(l.row) * 2, head = static_cast<cuuint64_t>(l.head) * 2,
                    slice = static_cast<cuuint64_t>(l.slice) * 2;
-  const cuuint64_t dims[4] = {D, l.hn ? H : N, l.hn ? N : H, S};
-  const cuuint64_t strides[3] = {l.hn ? head : row, l.hn ? row : head, slice};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(s->D), l.hn ? 1u : box_rows, l.hn ? box_rows : 1u, 1u};
-  const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
   const CUtensorMapSwizzle sw = (s->D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+  if (!l.hn) {
+    const cuuint64_t dims[3] = {D, N, S * H};
+    const cuuint64_t strides[2] = {row, head};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(s->D), box_rows, 1u};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[4] = {D, H, N, S};
+  const cuuint64_t strides[3] = {head, row, slice};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(s->D), 1u, box_rows, 1u};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -102,8 +110,9 @@ bool make_rows_map(CUtensorMap* m, const void* base, const triattn_shape* s, con
 // TMA and the vector accesses), nested without overlap -- the D features of
 // a row inside the smaller of the head and row strides, all rows (or heads)
 // of that kind inside the larger one, a whole slice inside the slice stride
-// (so the maps' dimensions are ordered by stride) -- and the slice stride
-// below 2^36 elements.
+// (so the maps' dimensions are ordered by stride); with the rows inside the
+// heads, the heads packed (slice = H head); the slice stride below 2^36
+// elements.
 bool layout_from(const triattn_layout* u, const triattn_shape* s, RowLayout* out) {
   if (u == nullptr) {
     *out = contiguous_layout(s->N, s->H, s->D);
@@ -116,6 +125,8 @@ bool layout_from(const triattn_layout* u, const triattn_shape* s, RowLayout* out
   // head or row (H = 1 or N = 1)
   if (u->head == u->row && H > 1 && N > 1) return false;
   const bool hn = u->head < u->row || (u->head == u->row && H == 1);  // heads inside a row
+  // rows inside the heads: the heads of a slice packed (one map dimension for slice and head)
+  if (!hn && u->slice != H * u->head) return false;
   const long long inner = hn ? u->head : u->row, outer = hn ? u->row : u->head;
   const long long n_inner = hn ? H : N, n_outer = hn ? N : H;
   if (inner < D || (n_inner - 1) * inner + D > outer || (n_outer - 1) * outer + (n_inner - 1) * inner + D > u->slice)

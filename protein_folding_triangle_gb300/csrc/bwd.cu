@@ -228,7 +228,10 @@ struct BwdBars {
 // (cp.reduce.async.bulk, this GPU's memory only): warpgroup 0 stages the
 // FP32 tile in the dS buffer once the dQ MMA has read it, one thread issues
 // the reduction, and the next dS waits until the engine has read the tile.
-template <int D, int kAtomic = 0>
+// HN: q, k, v have their heads inside their rows (RowLayout::hn; the ordered
+// path only): the grid runs heads first, so that the CTAs running together
+// read neighbouring heads of the same rows.
+template <int D, int kAtomic = 0, bool HN = false>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -246,18 +249,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int ktile = blockIdx.x;
+  // grid (J_K, groups, B * H), or (H * J_K, groups, B) with HN
+  const int ktile = HN ? static_cast<int>(blockIdx.x) / H : static_cast<int>(blockIdx.x);
   const int grp = blockIdx.y;
   const int o0 = grp * G;
-  const int bh = blockIdx.z;
+  const int bh = HN ? static_cast<int>(blockIdx.z) * H + static_cast<int>(blockIdx.x) % H : static_cast<int>(blockIdx.z);
   const int b = bh / H;
   const int h = bh - b * H;
+  const int nkt = HN ? static_cast<int>(gridDim.x) / H : static_cast<int>(gridDim.x);  // key tiles
+  const int nbh = HN ? static_cast<int>(gridDim.z) * H : static_cast<int>(gridDim.z);  // B * H
   const int JQ = (N + BM - 1) / BM;
   const int nsteps = JQ * G;
   // The last group may extend past N_o: its extra slices see every key
   // masked (P = 0, so they add nothing), their records are read from the
   // last real slice, and nothing of theirs is stored.
-  const int last_rec_slice = (static_cast<int>(gridDim.z) / H) * N_o * H - 1;
+  const int last_rec_slice = nbh * N_o - 1;
 
   // The swizzled tiles below need a 1024-byte aligned base.
   if ((smem_u32(sm) & 1023u) != 0) {
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int r = (warp & 3) * 32 + lane;
     const bool live = o0 + tg < N_o;
     const size_t slice = static_cast<size_t>((b * N_o + o0 + tg) * H + h);
-    const size_t nslices = static_cast<size_t>(gridDim.z) * N_o;
+    const size_t nslices = static_cast<size_t>(nbh) * N_o;
     float* out = dq_part + ((static_cast<size_t>(ktile) * nslices + slice) * JQ + ti) * (BM * D) + r * 8;
     const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kTDQ;
     const float isd = rsqrtf(static_cast<float>(D));
@@ -397,8 +403,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_expect_tx(&bars->kv_full, 2 * G * L::kTile);
       for (int g = 0; g < G; ++g) {
         const int bo = b * N_o + o0 + g;
-        tma_load_rows(sm + L::kK + g * L::kTile, &tm_k, &bars->kv_full, lq.hn, ktile * BN, h, bo);
-        tma_load_rows(sm + L::kV + g * L::kTile, &tm_v, &bars->kv_full, lq.hn, ktile * BN, h, bo);
+        tma_load_rows(sm + L::kK + g * L::kTile, &tm_k, &bars->kv_full, HN, ktile * BN, h, bo, H);
+        tma_load_rows(sm + L::kV + g * L::kTile, &tm_v, &bars->kv_full, HN, ktile * BN, h, bo, H);
       }
     }
     __syncwarp();
@@ -427,8 +433,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (elect_one()) {
         const int boh = (b * N_o + o0 + g) * H + h;
         mbar_expect_tx(&bars->qdo_full[st], 2 * L::kTile + kRecTile);
-        tma_load_rows(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], lq.hn, i * BM, h, b * N_o + o0 + g);
-        tma_load_rows(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], lo.hn, i * BM, h, b * N_o + o0 + g);
+        tma_load_rows(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], HN, i * BM, h, b * N_o + o0 + g, H);
+        tma_load_rows(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], lo.hn, i * BM, h, b * N_o + o0 + g,
+                      H);
         bulk_load(sm + L::kRec + st * kRecTile, rec + (static_cast<size_t>(min(boh, last_rec_slice)) * JQ + i) * BM,
                   kRecTile, &bars->qdo_full[st]);
       }
@@ -711,13 +718,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // stored chunk-major ([16 chunks of 8 queries][128 keys] x 8 floats)
         // with 32-byte stores, so that each warp store covers 1 KB
         if constexpr ((kAtomic & 2) != 0) {
-          float* acc = dbias_part + ((static_cast<size_t>(bh) * gridDim.x * BN + ktile * BN + r) * JQ + i) * BM + col0;
+          float* acc = dbias_part + ((static_cast<size_t>(bh) * nkt * BN + ktile * BN + r) * JQ + i) * BM + col0;
 #pragma unroll
           for (int k4 = 0; k4 < kCols / 4; ++k4)
             red_add_v4(acc + 4 * k4, dbacc[2 * k4].x, dbacc[2 * k4].y, dbacc[2 * k4 + 1].x, dbacc[2 * k4 + 1].y);
         } else {
           float* dst = dbias_part +
-                       ((((static_cast<size_t>(grp) * gridDim.z + bh) * JQ + i) * gridDim.x + ktile) * (BM * BN)) +
+                       ((((static_cast<size_t>(grp) * nbh + bh) * JQ + i) * nkt + ktile) * (BM * BN)) +
                        ((col0 / 8) * BN + r) * 8;
 #pragma unroll
           for (int k8 = 0; k8 < kCols / 8; ++k8)
@@ -991,6 +998,9 @@ cudaError_t setup_bwd() {
     e = cudaFuncSetAttribute(bwd_main_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bwd_main_kernel<D, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_main_kernel<D, 0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdSmem<D>::kBytes);
   return e;
 }
 
@@ -1016,8 +1026,12 @@ cudaError_t launch_bwd_transpose_bias(const BwdArgs& a, cudaStream_t stream) {
 template <int D, int kAtomic>
 cudaError_t launch_main_variant(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
-  dim3 grid(JK, (a.N_o + BwdSmem<D>::G - 1) / BwdSmem<D>::G, a.B * a.H);
-  bwd_main_kernel<D, kAtomic><<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
+  const int NG = (a.N_o + BwdSmem<D>::G - 1) / BwdSmem<D>::G;
+  const bool hn = a.lq.hn != 0;
+  if (hn && kAtomic != 0) return cudaErrorInvalidValue;  // the ablation takes the contiguous layout
+  const dim3 grid = hn ? dim3(JK * a.H, NG, a.B) : dim3(JK, NG, a.B * a.H);
+  auto kernel = hn ? bwd_main_kernel<D, kAtomic, true> : bwd_main_kernel<D, kAtomic, false>;
+  kernel<<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.lq,
       a.lo, a.wc);

@@ -116,7 +116,10 @@ static_assert(sizeof(FwdBars) <= 1024, "barrier block");
 
 }  // namespace
 
-template <int D>
+// HN: q, k, v have their heads inside their rows (RowLayout::hn): items run
+// heads first, so that the items running together read neighbouring heads of
+// the same rows; the tensor maps' coordinates come in that order too.
+template <int D, bool HN>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
@@ -136,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NG = (N_o + GF - 1) / GF;                     // outer groups
   const int JK = (N + BN - 1) / BN;
   const int rec_slices = (BH / H) * N_o + GF;             // records per key tile
-  // Work items, in the order of a (JQ, NG, B*H) grid: this CTA takes items
+  // Work items, in the order of a (JQ, NG, B*H) grid (heads first when they
+  // lie inside the rows of q, k, v): this CTA takes items
   // blockIdx.x, blockIdx.x + gridDim.x, ...; nitems of them.
   const int total = JQ * NG * BH;
   const int nitems = blockIdx.x < total ? (total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
@@ -145,11 +149,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto item_of = [&](int k) {
     const int it = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
     Item r;
-    r.qtile = it % JQ;
-    r.o0 = ((it / JQ) % NG) * GF;
-    r.bh = it / (JQ * NG);
-    r.b = r.bh / H;
-    r.h = r.bh - r.b * H;
+    if constexpr (HN) {
+      r.h = it % H;
+      const int rest = it / H;
+      r.qtile = rest % JQ;
+      r.o0 = ((rest / JQ) % NG) * GF;
+      r.b = rest / (JQ * NG);
+      r.bh = r.b * H + r.h;
+    } else {
+      r.qtile = it % JQ;
+      r.o0 = ((it / JQ) % NG) * GF;
+      r.bh = it / (JQ * NG);
+      r.b = r.bh / H;
+      r.h = r.bh - r.b * H;
+    }
     return r;
   };
 
@@ -204,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->q_empty[qs], ((k >> 1) & 1) ^ 1, wc, abort)) break;
         mbar_expect_tx(&bars->q_full[qs], GF * L::kTileQ);
         for (int g = 0; g < GF; ++g)
-          tma_load_rows(sm + L::kQ + (qs * GF + g) * L::kTileQ, &tm_q, &bars->q_full[qs], lq.hn, row0, w.h,
-                        w.b * N_o + w.o0 + g);
+          tma_load_rows(sm + L::kQ + (qs * GF + g) * L::kTileQ, &tm_q, &bars->q_full[qs], HN, row0, w.h,
+                        w.b * N_o + w.o0 + g, H);
         for (int j = 0; j < JK && go; ++j) {
           if (!mbar_wait(&bars->b_empty[bst], bpar ^ 1, wc, abort)) { go = false; break; }
           mbar_expect_tx(&bars->b_full[bst], BM * BN * 2 + (mrec != nullptr ? GF * kFwdMaskRec : 0));
@@ -220,13 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&bars->k_empty[g][slot], par, wc, abort)) { go = false; break; }
             if (!(test_starve && k == 0 && j == 0 && g == 0)) {
               mbar_expect_tx(&bars->k_full[g][slot], L::kTileKV);
-              tma_load_rows(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], lq.hn,
-                            j * BN, w.h, bo);
+              tma_load_rows(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], HN,
+                            j * BN, w.h, bo, H);
             }
             if (!mbar_wait(&bars->v_empty[g][slot], par, wc, abort)) { go = false; break; }
             mbar_expect_tx(&bars->v_full[g][slot], L::kTileKV);
-            tma_load_rows(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], lq.hn, j * BN,
-                          w.h, bo);
+            tma_load_rows(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], HN, j * BN,
+                          w.h, bo, H);
           }
           if (++bst == NBIAS) { bst = 0; bpar ^= 1; }
           if (++slot == NSLOT) { slot = 0; spar ^= 1; }
@@ -639,7 +652,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(total, sms));
-  fwd_kernel<D><<<grid, kThreads, FwdSmem<D>::kBytes, stream>>>(
+  auto kernel = a.lq.hn ? fwd_kernel<D, true> : fwd_kernel<D, false>;
+  kernel<<<grid, kThreads, FwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_bias, a.mrec, static_cast<uint16_t*>(a.o), a.lse,
       static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.B * a.H, a.test_starve, a.lq, a.lo, a.wc);
   return cudaGetLastError();
@@ -650,18 +664,22 @@ cudaError_t setup_fwd() {
   // setmaxnreg.inc waits until the registers it asks for are free in the
   // block's launch allocation: refuse to run a build whose launch register
   // count could not cover the split.
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  for (auto kernel : {fwd_kernel<D, false>, fwd_kernel<D, true>}) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 bool fwd_attrs_current() {
   // The attribute set by setup_fwd is lost with the context (a device
   // reset); the library then sets every attribute again.
   cudaFuncAttributes fa;
-  return cudaFuncGetAttributes(&fa, fwd_kernel<32>) == cudaSuccess && fa.maxDynamicSharedSizeBytes >= 232448;
+  return cudaFuncGetAttributes(&fa, fwd_kernel<32, false>) == cudaSuccess && fa.maxDynamicSharedSizeBytes >= 232448;
 }
 
 template cudaError_t launch_fwd<16>(const FwdArgs&, cudaStream_t);

@@ -25,9 +25,10 @@ constexpr int kGroupBwdFor(int D) { return D == 16 ? 8 : 4; }
 // row (b, o, h, n) starts slice * (b N_o + o) + head * h + row * n elements
 // from the base.  The library's own layout is {H N D, N D, D}; the
 // triangle-attention module's pair rows are {N ld, D, ld}.  Q, K, V (and dO)
-// tiles are loaded through 4-D tensor maps whose dimensions are ordered by
-// stride: (D, N, H, B N_o) when head > row (hn = 0), else (D, H, N, B N_o)
-// (hn = 1); tma_load_rows gives a row tile's coordinates in that order.
+// tiles are loaded through tensor maps: with the rows inside the heads
+// (hn = 0; then slice = H head) a 3-D map (D, N, B N_o H) whose last
+// coordinate is (b N_o + o) H + h, as for a contiguous tensor; with the heads
+// inside the rows (hn = 1) a 4-D map (D, H, N, B N_o).
 struct RowLayout {
   long long slice, head, row;
   int hn;
@@ -39,10 +40,10 @@ inline RowLayout contiguous_layout(int N, int H, int D) {
   return RowLayout{static_cast<long long>(H) * N * D, static_cast<long long>(N) * D, D, 0};
 }
 // Rows [n0, n0 + box) of slice bo, head h through a map of the layout above.
-__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar, int hn, int n0, int h,
-                                              int bo) {
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar, bool hn, int n0, int h,
+                                              int bo, int H) {
   if (hn) tma_load_4d(dst, map, bar, 0, h, n0, bo);
-  else tma_load_4d(dst, map, bar, 0, n0, h, bo);
+  else tma_load_3d(dst, map, bar, 0, n0, bo * H + h);
 }
 
 // Forward key-mask record per (slice, 64-key tile): 64 BF16 mask values, then

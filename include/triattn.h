@@ -188,8 +188,11 @@ triattn_status tri_attn_bwd(const triattn_shape* shape,
  * unless H or N is 1, and slice = H head when head > row (both layouts above
  * qualify).  The caller keeps the rows of one tensor from overlapping those
  * of another that a call writes.
- *   qkv_layout  q, k, v (forward and backward) and dq, dk, dv (backward)
- *   o_layout    o and o_resid (forward and backward) and dO (backward)
+ *   qkv_layout   q, k, v (forward and backward)
+ *   o_layout     o and o_resid (forward and backward)
+ *   do_layout    dO (backward)
+ *   dqkv_layout  dq, dk, dv (backward)
+ * (all four required on the backward).
  * lse, bias, mask, dbias, the workspaces and every other rule are those of
  * tri_attn_fwd / tri_attn_bwd.  The ablation entry points take the
  * contiguous layout only.
@@ -214,8 +217,11 @@ triattn_status tri_attn_bwd_strided(const triattn_shape* shape,
                                     const void* bias, const void* mask,
                                     const void* o, const void* o_resid,
                                     const triattn_layout* o_layout,
-                                    const float* lse, const void* dO,
-                                    void* dq, void* dk, void* dv, void* dbias,
+                                    const float* lse,
+                                    const void* dO, const triattn_layout* do_layout,
+                                    void* dq, void* dk, void* dv,
+                                    const triattn_layout* dqkv_layout,
+                                    void* dbias,
                                     void* workspace, size_t workspace_bytes,
                                     void* stream);
 

@@ -277,12 +277,15 @@ namespace {
 triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k, const void* v,
                         const triattn_layout* qkv_layout, const void* bias, const void* mask, const void* o,
                         const void* o_resid, const triattn_layout* o_layout, const float* lse, const void* dO,
-                        void* dq, void* dk, void* dv, void* dbias, int atomic_mask, void* workspace,
+                        const triattn_layout* do_layout, void* dq, void* dk, void* dv,
+                        const triattn_layout* dqkv_layout, void* dbias, int atomic_mask, void* workspace,
                         size_t workspace_bytes, void* stream) {
   triattn_status st = check_shape(shape);
   if (st != TRIATTN_OK) return st;
-  RowLayout lq, lo;
-  if (!layout_from(qkv_layout, shape, &lq) || !layout_from(o_layout, shape, &lo)) return TRIATTN_ERR_INVALID_ARG;
+  RowLayout lq, lo, ldo, lg;
+  if (!layout_from(qkv_layout, shape, &lq) || !layout_from(o_layout, shape, &lo) ||
+      !layout_from(do_layout, shape, &ldo) || !layout_from(dqkv_layout, shape, &lg))
+    return TRIATTN_ERR_INVALID_ARG;
   const void* req[] = {q, k, v, bias, o, dO, dq, dk, dv, dbias};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return TRIATTN_ERR_INVALID_ARG;
@@ -298,11 +301,13 @@ triattn_status bwd_impl(const triattn_shape* shape, const void* q, const void* k
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.biasT = ws + w.biasT_off;
   if (!make_rows_map(&a.tm_q, q, shape, lq) || !make_rows_map(&a.tm_k, k, shape, lq) ||
-      !make_rows_map(&a.tm_v, v, shape, lq) || !make_rows_map(&a.tm_do, dO, shape, lo) ||
+      !make_rows_map(&a.tm_v, v, shape, lq) || !make_rows_map(&a.tm_do, dO, shape, ldo) ||
       !make_bias_map(&a.tm_biasT, a.biasT, shape, padded_n(shape->N)))
     return TRIATTN_ERR_CUDA;
   a.lq = lq;
   a.lo = lo;
+  a.ldo = ldo;
+  a.lg = lg;
   a.bias = bias;
   a.mask = mask;
   a.o = o;
@@ -449,18 +454,20 @@ triattn_status tri_attn_bwd(const triattn_shape* shape, const void* q, const voi
                             const void* bias, const void* mask, const void* o, const void* o_resid, const float* lse,
                             const void* dO, void* dq, void* dk, void* dv, void* dbias, void* workspace,
                             size_t workspace_bytes, void* stream) {
-  return bwd_impl(shape, q, k, v, nullptr, bias, mask, o, o_resid, nullptr, lse, dO, dq, dk, dv, dbias, 0, workspace,
-                  workspace_bytes, stream);
+  return bwd_impl(shape, q, k, v, nullptr, bias, mask, o, o_resid, nullptr, lse, dO, nullptr, dq, dk, dv, nullptr,
+                  dbias, 0, workspace, workspace_bytes, stream);
 }
 
 triattn_status tri_attn_bwd_strided(const triattn_shape* shape, const void* q, const void* k, const void* v,
                                     const triattn_layout* qkv_layout, const void* bias, const void* mask,
                                     const void* o, const void* o_resid, const triattn_layout* o_layout,
-                                    const float* lse, const void* dO, void* dq, void* dk, void* dv, void* dbias,
+                                    const float* lse, const void* dO, const triattn_layout* do_layout, void* dq,
+                                    void* dk, void* dv, const triattn_layout* dqkv_layout, void* dbias,
                                     void* workspace, size_t workspace_bytes, void* stream) {
-  if (qkv_layout == nullptr || o_layout == nullptr) return TRIATTN_ERR_INVALID_ARG;
-  return bwd_impl(shape, q, k, v, qkv_layout, bias, mask, o, o_resid, o_layout, lse, dO, dq, dk, dv, dbias, 0,
-                  workspace, workspace_bytes, stream);
+  if (qkv_layout == nullptr || o_layout == nullptr || do_layout == nullptr || dqkv_layout == nullptr)
+    return TRIATTN_ERR_INVALID_ARG;
+  return bwd_impl(shape, q, k, v, qkv_layout, bias, mask, o, o_resid, o_layout, lse, dO, do_layout, dq, dk, dv,
+                  dqkv_layout, dbias, 0, workspace, workspace_bytes, stream);
 }
 
 size_t triattn_bwd_atomic_workspace_bytes(const triattn_shape* shape, int atomic_mask) {
@@ -475,8 +482,8 @@ triattn_status tri_attn_bwd_atomic_ablation(const triattn_shape* shape, const vo
                                             void* stream) {
   if (!atomic_mask_ok(atomic_mask)) return TRIATTN_ERR_INVALID_ARG;
   if (shape != nullptr && shape->flags != 0) return TRIATTN_ERR_INVALID_ARG;
-  return bwd_impl(shape, q, k, v, nullptr, bias, mask, o, o_resid, nullptr, lse, dO, dq, dk, dv, dbias, atomic_mask,
-                  workspace, workspace_bytes, stream);
+  return bwd_impl(shape, q, k, v, nullptr, bias, mask, o, o_resid, nullptr, lse, dO, nullptr, dq, dk, dv, nullptr,
+                  dbias, atomic_mask, workspace, workspace_bytes, stream);
 }
 
 triattn_status tri_attn_dbias_combine(const triattn_shape* shape, const float* parts, int R, void* dbias,

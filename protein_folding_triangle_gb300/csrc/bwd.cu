@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
                                                          const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ e,
                                                          const float* __restrict__ lse, uint4* __restrict__ rec,
-                                                         int N, int H, int JQ, size_t padded_rows, RowLayout lo) {
+                                                         int N, int H, int JQ, size_t padded_rows, RowLayout lo,
+                                                         RowLayout ldo) {
   // One 16-byte chunk (8 features) of one row per thread, so that a warp's
   // loads cover consecutive rows contiguously; the D/8 lanes of a row add
   // their partial sums with a fixed butterfly.
@@ -65,8 +66,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint16_t* __restr
   if (live) {
     const size_t row = slice * N + q;
     const long long bo = static_cast<long long>(slice / H);
-    const long long off = lo.offset(bo, static_cast<int>(slice - bo * H), q);
-    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(dO + off) + c);
+    const int hh = static_cast<int>(slice - bo * H);
+    const long long off = lo.offset(bo, hh, q);
+    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(dO + ldo.offset(bo, hh, q)) + c);
     const uint4 ow = __ldg(reinterpret_cast<const uint4*>(o + off) + c);
     uint4 ew = make_uint4(0, 0, 0, 0);
     if (e != nullptr) ew = __ldg(reinterpret_cast<const uint4*>(e + off) + c);
@@ -228,17 +230,18 @@ struct BwdBars {
 // (cp.reduce.async.bulk, this GPU's memory only): warpgroup 0 stages the
 // FP32 tile in the dS buffer once the dQ MMA has read it, one thread issues
 // the reduction, and the next dS waits until the engine has read the tile.
-// HN: q, k, v have their heads inside their rows (RowLayout::hn; the ordered
-// path only): the grid runs heads first, so that the CTAs running together
-// read neighbouring heads of the same rows.
-template <int D, int kAtomic = 0, bool HN = false>
+// HF (the ordered path only): the grid runs heads first, so that the CTAs
+// running together read or write neighbouring heads of the same rows --
+// chosen when q, k, v, dO or dq, dk, dv have their heads inside their rows
+// (RowLayout::hn).  The tensor maps follow lq.hn and ldo.hn.
+template <int D, int kAtomic = 0, bool HF = false>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_biasT, const uint16_t* __restrict__ mask,
                     const uint4* __restrict__ rec, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv,
                     float* __restrict__ dq_part, float* __restrict__ dbias_part, int N_o, int N, int H, RowLayout lq,
-                    RowLayout lo, WaitCtl wc) {
+                    RowLayout ldo, RowLayout lg, WaitCtl wc) {
   using L = BwdSmem<D>;
   constexpr int G = L::G;  // outer slices per CTA
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -249,15 +252,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // grid (J_K, groups, B * H), or (H * J_K, groups, B) with HN
-  const int ktile = HN ? static_cast<int>(blockIdx.x) / H : static_cast<int>(blockIdx.x);
+  // grid (J_K, groups, B * H), or (H * J_K, groups, B) with HF
+  const int ktile = HF ? static_cast<int>(blockIdx.x) / H : static_cast<int>(blockIdx.x);
   const int grp = blockIdx.y;
   const int o0 = grp * G;
-  const int bh = HN ? static_cast<int>(blockIdx.z) * H + static_cast<int>(blockIdx.x) % H : static_cast<int>(blockIdx.z);
+  const int bh = HF ? static_cast<int>(blockIdx.z) * H + static_cast<int>(blockIdx.x) % H : static_cast<int>(blockIdx.z);
   const int b = bh / H;
   const int h = bh - b * H;
-  const int nkt = HN ? static_cast<int>(gridDim.x) / H : static_cast<int>(gridDim.x);  // key tiles
-  const int nbh = HN ? static_cast<int>(gridDim.z) * H : static_cast<int>(gridDim.z);  // B * H
+  const int nkt = HF ? static_cast<int>(gridDim.x) / H : static_cast<int>(gridDim.x);  // key tiles
+  const int nbh = HF ? static_cast<int>(gridDim.z) * H : static_cast<int>(gridDim.z);  // B * H
   const int JQ = (N + BM - 1) / BM;
   const int nsteps = JQ * G;
   // The last group may extend past N_o: its extra slices see every key
@@ -403,8 +406,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_expect_tx(&bars->kv_full, 2 * G * L::kTile);
       for (int g = 0; g < G; ++g) {
         const int bo = b * N_o + o0 + g;
-        tma_load_rows(sm + L::kK + g * L::kTile, &tm_k, &bars->kv_full, HN, ktile * BN, h, bo, H);
-        tma_load_rows(sm + L::kV + g * L::kTile, &tm_v, &bars->kv_full, HN, ktile * BN, h, bo, H);
+        tma_load_rows(sm + L::kK + g * L::kTile, &tm_k, &bars->kv_full, lq.hn, ktile * BN, h, bo, H);
+        tma_load_rows(sm + L::kV + g * L::kTile, &tm_v, &bars->kv_full, lq.hn, ktile * BN, h, bo, H);
       }
     }
     __syncwarp();
@@ -433,8 +436,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (elect_one()) {
         const int boh = (b * N_o + o0 + g) * H + h;
         mbar_expect_tx(&bars->qdo_full[st], 2 * L::kTile + kRecTile);
-        tma_load_rows(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], HN, i * BM, h, b * N_o + o0 + g, H);
-        tma_load_rows(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], lo.hn, i * BM, h, b * N_o + o0 + g,
+        tma_load_rows(sm + L::kQ + st * L::kTile, &tm_q, &bars->qdo_full[st], lq.hn, i * BM, h, b * N_o + o0 + g, H);
+        tma_load_rows(sm + L::kDO + st * L::kTile, &tm_do, &bars->qdo_full[st], ldo.hn, i * BM, h, b * N_o + o0 + g,
                       H);
         bulk_load(sm + L::kRec + st * kRecTile, rec + (static_cast<size_t>(min(boh, last_rec_slice)) * JQ + i) * BM,
                   kRecTile, &bars->qdo_full[st]);
@@ -744,7 +747,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int g = wg; g < G; g += kNWG)
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const long long off = lq.offset(b * N_o + o0 + g, h, key);
+        const long long off = lg.offset(b * N_o + o0 + g, h, key);
         const uint32_t t = tmem + lane_addr + which * G * D + g * D;
         const float sc = which == 0 ? 1.f : inv_sqrt_d;
         uint32_t w[D / 2];
@@ -785,7 +788,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 // memory, coalesced BF16 row writes.
 template <int D>
 __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict__ part, uint16_t* __restrict__ dq,
-                                                        int N, int H, int JQ, int JK, size_t tiles, RowLayout lq) {
+                                                        int N, int H, int JQ, int JK, size_t tiles, RowLayout lg) {
   constexpr int kChunks = BM * D / 4;      // float4 per tile
   constexpr int kStride = D + 4;           // padded row stride (floats) of the transpose buffer
   __shared__ float tile[BM * kStride];
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict
     const float* src = &tile[r * kStride + 8 * c8];
     const uint4 w = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]), pack_bf16x2(src[4], src[5]),
                                pack_bf16x2(src[6], src[7]));
-    *reinterpret_cast<uint4*>(dq + lq.offset(bo, h, q) + 8 * c8) = w;
+    *reinterpret_cast<uint4*>(dq + lg.offset(bo, h, q) + 8 * c8) = w;
   }
 }
 
@@ -937,7 +940,7 @@ __global__ void __launch_bounds__(256) dbias_combine_kernel(const float* __restr
 // thread per 8 outputs.
 template <int D>
 __global__ void __launch_bounds__(256) finish_dq_kernel(const float4* __restrict__ acc, uint16_t* __restrict__ dq,
-                                                        int N, int H, int JQ, size_t rows, RowLayout lq) {
+                                                        int N, int H, int JQ, size_t rows, RowLayout lg) {
   const size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= rows * (D / 8)) return;
   const size_t row = e / (D / 8);
@@ -947,7 +950,7 @@ __global__ void __launch_bounds__(256) finish_dq_kernel(const float4* __restrict
   const float4* src = acc + ((slice * JQ * BM + q) * D + 8 * c8) / 4;
   const float4 x = src[0], y = src[1];
   const long long bo = static_cast<long long>(slice / H);
-  *reinterpret_cast<uint4*>(dq + lq.offset(bo, static_cast<int>(slice - bo * H), q) + 8 * c8) =
+  *reinterpret_cast<uint4*>(dq + lg.offset(bo, static_cast<int>(slice - bo * H), q) + 8 * c8) =
       make_uint4(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w), pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
 }
 
@@ -1011,7 +1014,7 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>((padded * (D / 8) + 255) / 256);
   preprocess_kernel<D><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(a.dO), static_cast<const uint16_t*>(a.o),
                                                  static_cast<const uint16_t*>(a.o_resid), a.lse, a.rec, a.N, a.H,
-                                                 JQ, padded, a.lo);
+                                                 JQ, padded, a.lo, a.ldo);
   return cudaGetLastError();
 }
 
@@ -1027,14 +1030,14 @@ template <int D, int kAtomic>
 cudaError_t launch_main_variant(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN;
   const int NG = (a.N_o + BwdSmem<D>::G - 1) / BwdSmem<D>::G;
-  const bool hn = a.lq.hn != 0;
+  const bool hn = a.lq.hn || a.ldo.hn || a.lg.hn;
   if (hn && kAtomic != 0) return cudaErrorInvalidValue;  // the ablation takes the contiguous layout
   const dim3 grid = hn ? dim3(JK * a.H, NG, a.B) : dim3(JK, NG, a.B * a.H);
   auto kernel = hn ? bwd_main_kernel<D, kAtomic, true> : bwd_main_kernel<D, kAtomic, false>;
   kernel<<<grid, kMainThreads, BwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_biasT, static_cast<const uint16_t*>(a.mask), a.rec,
       static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv), a.dq_part, a.dbias_part, a.N_o, a.N, a.H, a.lq,
-      a.lo, a.wc);
+      a.ldo, a.lg, a.wc);
   return cudaGetLastError();
 }
 
@@ -1059,7 +1062,7 @@ cudaError_t launch_bwd_finish_dq(const BwdArgs& a, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(a.B) * a.N_o * a.H * a.N;
   const size_t items = rows * (D / 8);
   finish_dq_kernel<D><<<static_cast<unsigned>((items + 255) / 256), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, a.H, JQ, rows, a.lq);
+      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, a.H, JQ, rows, a.lg);
   return cudaGetLastError();
 }
 
@@ -1076,7 +1079,7 @@ cudaError_t launch_bwd_reduce_dq(const BwdArgs& a, cudaStream_t stream) {
   const int JK = (a.N + BN - 1) / BN, JQ = (a.N + BM - 1) / BM;
   const size_t tiles = static_cast<size_t>(a.B) * a.N_o * a.H * JQ;
   reduce_dq_kernel<D><<<static_cast<unsigned>(tiles), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, a.H, JQ, JK, tiles, a.lq);
+      reinterpret_cast<const float4*>(a.dq_part), static_cast<uint16_t*>(a.dq), a.N, a.H, JQ, JK, tiles, a.lg);
   return cudaGetLastError();
 }
 

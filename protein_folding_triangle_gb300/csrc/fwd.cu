@@ -116,10 +116,12 @@ static_assert(sizeof(FwdBars) <= 1024, "barrier block");
 
 }  // namespace
 
-// HN: q, k, v have their heads inside their rows (RowLayout::hn): items run
-// heads first, so that the items running together read neighbouring heads of
-// the same rows; the tensor maps' coordinates come in that order too.
-template <int D, bool HN>
+// GENERAL = false: q, k, v, o and its residual in the contiguous layout
+// [B, N_o, H, N, D] (3-D tensor maps, row indices).  GENERAL = true: any row
+// layouts (the maps of q, k, v follow lq.hn, o and the residual lo's
+// strides), and the items run heads first, so that the items running
+// together read or write neighbouring heads of the same rows.
+template <int D, bool GENERAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto item_of = [&](int k) {
     const int it = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
     Item r;
-    if constexpr (HN) {
+    if constexpr (GENERAL) {
       r.h = it % H;
       const int rest = it / H;
       r.qtile = rest % JQ;
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->q_empty[qs], ((k >> 1) & 1) ^ 1, wc, abort)) break;
         mbar_expect_tx(&bars->q_full[qs], GF * L::kTileQ);
         for (int g = 0; g < GF; ++g)
-          tma_load_rows(sm + L::kQ + (qs * GF + g) * L::kTileQ, &tm_q, &bars->q_full[qs], HN, row0, w.h,
+          tma_load_rows(sm + L::kQ + (qs * GF + g) * L::kTileQ, &tm_q, &bars->q_full[qs], GENERAL && lq.hn, row0, w.h,
                         w.b * N_o + w.o0 + g, H);
         for (int j = 0; j < JK && go; ++j) {
           if (!mbar_wait(&bars->b_empty[bst], bpar ^ 1, wc, abort)) { go = false; break; }
@@ -233,12 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&bars->k_empty[g][slot], par, wc, abort)) { go = false; break; }
             if (!(test_starve && k == 0 && j == 0 && g == 0)) {
               mbar_expect_tx(&bars->k_full[g][slot], L::kTileKV);
-              tma_load_rows(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], HN,
+              tma_load_rows(sm + L::kK + (g * NSLOT + slot) * L::kTileKV, &tm_k, &bars->k_full[g][slot], GENERAL && lq.hn,
                             j * BN, w.h, bo, H);
             }
             if (!mbar_wait(&bars->v_empty[g][slot], par, wc, abort)) { go = false; break; }
             mbar_expect_tx(&bars->v_full[g][slot], L::kTileKV);
-            tma_load_rows(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], HN, j * BN,
+            tma_load_rows(sm + L::kV + (g * NSLOT + slot) * L::kTileKV, &tm_v, &bars->v_full[g][slot], GENERAL && lq.hn, j * BN,
                           w.h, bo, H);
           }
           if (++bst == NBIAS) { bst = 0; bpar ^= 1; }
@@ -545,11 +547,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ob[e] = w;
             eb[e] = pack_bf16x2(y0 - bf16lo_to_f32(w), y1 - bf16hi_to_f32(w));
           }
-          uint4* op = reinterpret_cast<uint4*>(out_o + lo.offset(bo, w.h, q));
+          const size_t off = GENERAL ? static_cast<size_t>(lo.offset(bo, w.h, q)) : row * D;
+          uint4* op = reinterpret_cast<uint4*>(out_o + off);
   #pragma unroll
           for (int v4 = 0; v4 < D / 8; ++v4) op[v4] = make_uint4(ob[4 * v4], ob[4 * v4 + 1], ob[4 * v4 + 2], ob[4 * v4 + 3]);
           if (out_resid != nullptr) {
-            uint4* ep = reinterpret_cast<uint4*>(out_resid + lo.offset(bo, w.h, q));
+            uint4* ep = reinterpret_cast<uint4*>(out_resid + off);
   #pragma unroll
             for (int v4 = 0; v4 < D / 8; ++v4)
               ep[v4] = make_uint4(eb[4 * v4], eb[4 * v4 + 1], eb[4 * v4 + 2], eb[4 * v4 + 3]);
@@ -652,7 +655,9 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(total, sms));
-  auto kernel = a.lq.hn ? fwd_kernel<D, true> : fwd_kernel<D, false>;
+  const RowLayout c = contiguous_layout(a.N, a.H, D);
+  auto same = [&](const RowLayout& l) { return l.slice == c.slice && l.head == c.head && l.row == c.row; };
+  auto kernel = (same(a.lq) && same(a.lo)) ? fwd_kernel<D, false> : fwd_kernel<D, true>;
   kernel<<<grid, kThreads, FwdSmem<D>::kBytes, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_bias, a.mrec, static_cast<uint16_t*>(a.o), a.lse,
       static_cast<uint16_t*>(a.o_resid), a.N_o, a.N, a.H, a.B * a.H, a.test_starve, a.lq, a.lo, a.wc);

@@ -36,11 +36,21 @@
 //   gate bwd   the same gated tiles, recomputed in the backward; the epilogue
 //              reads dA, dB (channel-major) and writes the four blocks of
 //              dp = d(a, b)/d(a_v, a_g, b_v, b_g) pair-major.
+//
+// A fourth serves the projections of the triangle-attention module, whose
+// rows are the pairs (b, i, j) of [B, N, N] and whose columns are nblk blocks
+// of H heads of D features (q, k, v, or dO), then H bias columns:
+//   heads      each 32-row quarter of a tile (32 consecutive j of one (b, i);
+//              N a multiple of 32) goes out per head as a D x 32 box into
+//              the core's layout [nblk][B, N, H, N, D] (5-D tensor map), and
+//              the bias columns as 32-element rows into the planes
+//              [B, H, N, N] (4-D map); padding columns are dropped.
 // Every mbarrier wait is bounded (WaitCtl): a wait that runs out records a
 // timeout in the device status word and the CTA stops.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.cuh"
@@ -72,10 +82,11 @@ struct GemmParams {
   const uint16_t* mask;       // optional pair mask [M] (BF16)
   const uint16_t* dA;         // gate bwd: channel-major gradients of a and b
   const uint16_t* dB;
+  int nblk, H, D, Ntok, nbias;  // heads epilogue: head blocks, heads, features, tokens, bias columns
   WaitCtl wc;
 };
 
-enum GemmMode { kPlain = 0, kGated = 1, kGateBwd = 2 };
+enum GemmMode { kPlain = 0, kGated = 1, kGateBwd = 2, kHeads = 3 };
 
 
 
@@ -84,9 +95,9 @@ enum GemmMode { kPlain = 0, kGated = 1, kGateBwd = 2 };
 // 32-channel chunk)), ring stages, and bytes per staging buffer (FP32 or BF16
 // 32 x 32 blocks; the gated modes write BF16 only).
 template <int MODE> struct GemmCfg {
-  static constexpr int kEpi = MODE == 0 ? 4 : 16;
-  static constexpr int kS = MODE == 0 ? 4 : 3;
-  static constexpr int kBuf = MODE == 0 ? 4096 : 2048;
+  static constexpr int kEpi = (MODE == 0 || MODE == 3) ? 4 : 16;
+  static constexpr int kS = (MODE == 0 || MODE == 3) ? 4 : 3;
+  static constexpr int kBuf = (MODE == 0 || MODE == 3) ? 4096 : 2048;
   static constexpr int kThreads = (2 + kEpi) * 32;
 };
 
@@ -107,7 +118,8 @@ __global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_x,
                 const __grid_constant__ CUtensorMap tm_y, GemmParams p) {
-  static_assert(MODE == kPlain || (BN == 256 && !A_MN && B_MN), "gated tiles: K-major x, N-major W_p");
+  static_assert(MODE == kPlain || MODE == kHeads || (BN == 256 && !A_MN && B_MN), "gated tiles: K-major x, N-major W_p");
+  static_assert(MODE != kHeads || !A_MN, "heads epilogue: K-major A");
   using L = GemmSmem<BN, MODE>;
   constexpr int GB_S = GemmCfg<MODE>::kS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -173,7 +185,7 @@ __global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
           } else {
             tma_load_3d(sa, &tm_a, &bars->full[stage], k0, m0, bt);
           }
-          if constexpr (MODE != kPlain) {  // the four branch blocks of channels [64 nt, 64 nt + 64), or g
+          if constexpr (MODE == kGated || MODE == kGateBwd) {  // the four branch blocks of channels [64 nt, 64 nt + 64), or g
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int col = nt < p.gated_tiles ? j * p.Ch + 64 * nt : 4 * p.Ch + 256 * (nt - p.gated_tiles) + 64 * j;
@@ -259,6 +271,84 @@ __global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tma_store_3d(map, buf, x, y, z);
+      ++nst;
+    };
+    // heads epilogue: 32 columns from `col` of this warp's 32 rows (pairs
+    // m0 .. m0 + 31, consecutive j of one (b, i)), routed to the core's layout
+    // or to the bias planes
+    auto heads_chunk = [&](int m0, int col, const uint32_t (&v)[32]) {
+      if (m0 >= p.M) return;
+      const int bi = m0 / p.Ntok, j0 = m0 - bi * p.Ntok;
+      const int HD = p.H * p.D, nh = p.nblk * HD;
+      if (col < nh) {
+        uint8_t* buf = next_buf();
+        if (p.D == 32) {  // one head (H D is a multiple of 32): 32 x 64-byte rows, 64-byte swizzle
+          const int t = col / HD, h = (col - t * HD) / 32;
+          put_bf16(buf, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_5d_nc(&tm_c, buf, 0, j0, h, bi, t);
+            bulk_commit();
+          }
+        } else {  // two 16-column halves, each one head of 16 features (of its own block: H D may be
+                  // an odd multiple of 16), as 32 x 32-byte blocks without swizzle; an upper half past
+                  // the head columns is bias
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[16 * hf + 2 * e]), __uint_as_float(v[16 * hf + 2 * e + 1]));
+            uint4* row = reinterpret_cast<uint4*>(buf + hf * 1024 + lane * 32);
+            row[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            row[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int ch = col + 16 * hf;
+              if (ch < nh) {
+                const int th = ch / HD;
+                tma_store_5d_nc(&tm_c, buf + hf * 1024, 0, j0, (ch - th * HD) / 16, bi, th);
+              }
+            }
+            bulk_commit();
+          }
+        }
+        ++nst;
+        if (col + 32 <= nh) return;  // else the chunk's upper half holds bias columns
+      }
+      // bias columns [nh, nh + nbias) of this chunk: one 32-element row per head
+      const int c_lo = max(col, nh), c_hi = min(col + 32, nh + p.nbias);
+      if (c_lo >= c_hi) return;
+      // the chunk row-major (64-byte swizzled rows) in the buffer's lower half,
+      // then each bias column as one 32-pair row in its upper half, 16 rows
+      // at a time at a 128-byte pitch (TMA sources are 128-byte aligned)
+      uint8_t* buf = next_buf();
+      put_bf16(buf, v);
+      __syncwarp();
+      const int b = bi / p.Ntok, i = bi - b * p.Ntok;
+      for (int cs = c_lo; cs < c_hi; cs += 16) {
+        const int ce = min(cs + 16, c_hi);
+        if (cs > c_lo) {  // the previous group's stores have read the upper half
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
+        for (int c = cs; c < ce; ++c) {
+          const int e = c - col;
+          *reinterpret_cast<uint16_t*>(buf + 2048 + (c - cs) * 128 + lane * 2) =
+              *reinterpret_cast<const uint16_t*>(buf + lane * 64 + (((e >> 3) ^ ((lane >> 1) & 3)) << 4) + (e & 7) * 2);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int c = cs; c < ce; ++c) tma_store_4d_nc(&tm_x, buf + 2048 + (c - cs) * 128, j0, i, c - nh, b);
+          bulk_commit();
+        }
+      }
       ++nst;
     };
     // A gated tile: accumulator columns [a_v | a_g | b_v | b_g] of channels
@@ -349,7 +439,7 @@ __global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
       if constexpr (MODE == kGateBwd) load_d(mt, nt, dpre);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[ab], (local >> 1) & 1, wc, abort))) break;
       tc_fence_after();
-      if constexpr (MODE != kPlain) {
+      if constexpr (MODE == kGated || MODE == kGateBwd) {
         if (nt < p.gated_tiles) {
           gated_tile(mt, nt, ab, dpre);
           tc_fence_before();
@@ -358,7 +448,7 @@ __global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
         }
       }
       const int m0 = mt * GB_M + quarter * 32;
-      const int n0 = (MODE == kPlain ? nt : nt - p.gated_tiles) * BN;
+      const int n0 = (MODE == kGated ? nt - p.gated_tiles : nt) * BN;
       const int zc = p.partial ? ks * p.batch + bt : bt;
       constexpr int kCols = BN * 4 / GemmCfg<MODE>::kEpi;  // columns per warp of a plain tile
 #pragma unroll 1
@@ -366,6 +456,10 @@ __global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
         uint32_t v[32];
         tmem_ld32_wait(tmem + lane_addr + ab * BN + c0, v);
         if (n0 + c0 >= p.N) continue;  // the whole chunk is past N (the same for every lane)
+        if constexpr (MODE == kHeads) {
+          heads_chunk(m0, n0 + c0, v);
+          continue;
+        }
         uint8_t* buf = next_buf();
         if (f32) {
 #pragma unroll
@@ -658,6 +752,76 @@ cudaError_t launch_gate_bwd_proj(int B, long long NN, int Cz, int Ch, const void
   const long long total = static_cast<long long>(p.tiles_m) * p.tiles_n;
   const int grid = static_cast<int>(std::min<long long>(total, gemm_sms()));
   return gemm_launch_t<256, false, true, kGateBwd>(tma, tmb, tmc, tmc, tmc, p, grid, s);
+}
+
+cudaError_t launch_gemm_heads(bool tb, int M, int N, int K, const void* A, long long lda, const void* B, long long ldb,
+                              int nblk, int H, int D, int Ntok, int Bx, void* heads, void* bias_planes, int nbias,
+                              const WaitCtl& wc, cudaStream_t s) {
+  if (M < 1 || N < 1 || K < 1 || (D != 16 && D != 32) || H < 1 || nblk < 1 || Ntok < 32 || Ntok % 32 != 0 ||
+      static_cast<long long>(Bx) * Ntok * Ntok != M || nblk * H * D + nbias > N || (nbias > 0 && bias_planes == nullptr))
+    return cudaErrorInvalidValue;
+  if (!al16p(A) || !al16p(B) || !al16p(heads) || (bias_planes != nullptr && !al16p(bias_planes)) || (lda & 7) ||
+      (ldb & 7))
+    return cudaErrorInvalidValue;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = gemm_encoder();
+  if (enc == nullptr) return cudaErrorInvalidValue;
+  const int BN = N > 128 ? 256 : 128;
+  CUtensorMap tma, tmb, tmc, tmx;
+  const bool okA = gemm_map(&tma, A, K, M, 1, lda, 0, 64, 128);
+  const bool okB = tb ? gemm_map(&tmb, B, K, N, 1, ldb, 0, 64, static_cast<unsigned>(BN))
+                      : gemm_map(&tmb, B, N, K, 1, ldb, 0, 64, 64);
+  if (!okA || !okB) return cudaErrorInvalidValue;
+  {  // heads: [nblk][B*Ntok (b, i)][H][Ntok (j)][D], box D x 32 rows of one (b, i, h, t)
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Ntok), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(Bx) * Ntok, static_cast<cuuint64_t>(nblk)};
+    const cuuint64_t row = static_cast<cuuint64_t>(D) * 2, head = row * Ntok, slice = head * H,
+                     blk = slice * Bx * Ntok;
+    const cuuint64_t strides[4] = {row, head, slice, blk};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(D), 32u, 1u, 1u, 1u};
+    const cuuint32_t es[5] = {1u, 1u, 1u, 1u, 1u};
+    if (enc(&tmc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, heads, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  tmx = tmc;
+  if (nbias > 0) {  // bias planes [B][H][Ntok (i)][Ntok (j)], box 32 j of one (b, h, i)
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ntok), static_cast<cuuint64_t>(Ntok),
+                                static_cast<cuuint64_t>(nbias), static_cast<cuuint64_t>(Bx)};
+    const cuuint64_t row = static_cast<cuuint64_t>(Ntok) * 2, plane = row * Ntok, ex = plane * nbias;
+    const cuuint64_t strides[3] = {row, plane, ex};
+    const cuuint32_t box[4] = {32u, 1u, 1u, 1u};
+    const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+    if (enc(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, bias_planes, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.batch = 1;
+  p.ksplit = 1;
+  p.kchunk = (K + GB_K - 1) / GB_K * GB_K;
+  p.tiles_m = (M + GB_M - 1) / GB_M;
+  p.tiles_n = (N + BN - 1) / BN;
+  p.NN = 1;
+  p.nblk = nblk;
+  p.H = H;
+  p.D = D;
+  p.Ntok = Ntok;
+  p.nbias = nbias;
+  p.wc = wc;
+  const long long total = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  const int grid = static_cast<int>(std::min<long long>(total, gemm_sms()));
+  const bool bmn = !tb;
+  if (BN == 256)
+    return bmn ? gemm_launch_t<256, false, true, kHeads>(tma, tmb, tmc, tmx, tmx, p, grid, s)
+               : gemm_launch_t<256, false, false, kHeads>(tma, tmb, tmc, tmx, tmx, p, grid, s);
+  return bmn ? gemm_launch_t<128, false, true, kHeads>(tma, tmb, tmc, tmx, tmx, p, grid, s)
+             : gemm_launch_t<128, false, false, kHeads>(tma, tmb, tmc, tmx, tmx, p, grid, s);
 }
 
 }  // namespace triattn

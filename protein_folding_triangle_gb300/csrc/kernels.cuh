@@ -82,8 +82,10 @@ struct BwdArgs {
   uint4* rec;        // [slices][J_Q * 128] query-row records (BF16 splits of -lse sqrt(D), -delta)
   float* dq_part;    // [J_K][slices][J_Q][128 x D]
   float* dbias_part; // [L][B*H*N*N]
-  RowLayout lq;      // q, k, v, dq, dk, dv
-  RowLayout lo;      // o, o_resid, dO
+  RowLayout lq;      // q, k, v
+  RowLayout lo;      // o, o_resid
+  RowLayout ldo;     // dO
+  RowLayout lg;      // dq, dk, dv
   int B, N_o, N, H, D;
   int dbias_fp32;    // write dbias as FP32 (the sum over this call's slices)
   WaitCtl wc;
@@ -134,6 +136,14 @@ size_t gemm_splitk_bytes(int M, int N, int K, int batch);
 // (mask m optional, [B*NN] BF16).  NN, C_z and C_h multiples of 32.
 cudaError_t launch_gated_proj(int B, long long NN, int Cz, int Ch, const void* x, const void* w_p, const void* mask,
                               void* a, void* b, void* g, const WaitCtl& wc, cudaStream_t s);
+// C = A op(B) (A [M, K] row-major; B [K, N], or [N, K] when tb) for the
+// triangle-attention module, its rows the pairs (b, i, j) of [Bx, Ntok, Ntok]
+// (Ntok a multiple of 32): columns [0, nblk H D) go to nblk tensors in the
+// core's layout [nblk][Bx, Ntok, H, Ntok, D] at `heads`, the next nbias
+// columns to the bias planes [Bx, nbias, Ntok, Ntok], the rest nowhere.
+cudaError_t launch_gemm_heads(bool tb, int M, int N, int K, const void* A, long long lda, const void* B, long long ldb,
+                              int nblk, int H, int D, int Ntok, int Bx, void* heads, void* bias_planes, int nbias,
+                              const WaitCtl& wc, cudaStream_t s);
 // Its backward through the gating: recomputes the four branch projections and
 // writes dp's first 4 C_h columns (row stride ldp) from dA, dB (channel-major).
 cudaError_t launch_gate_bwd_proj(int B, long long NN, int Cz, int Ch, const void* x, const void* w_p,

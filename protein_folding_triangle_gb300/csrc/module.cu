@@ -82,18 +82,26 @@ ModDims dims_of(const triattn_module_shape* s) {
 }
 
 // Saved between forward and backward (the caller's "context" buffer).
-// q, k, v stay in P's pair rows and o, its residual and dO in pair rows of
-// H*D features: the core reads and writes them there (tri_attn_*_strided).
+// Two data flows.  With N a multiple of 32 ("heads" flow) the projection
+// GEMM's epilogue writes q, k, v straight into the core's layout and the bias
+// planes, and the dO GEMM writes dO in the core's layout, so the core reads
+// contiguous tiles; otherwise q, k, v stay in P's pair rows and dO in
+// d_oflat's, read there through the strided entry points.  Either way the
+// core writes o and its residual into pair rows of H*D features and dq, dk,
+// dv into dP's pair rows.
+bool heads_flow(const ModDims& d) { return d.N % 32 == 0; }
+
 struct CtxLayout {
-  size_t x, mean, rstd, p, bias, lse, resid, oflat, total;
+  size_t x, mean, rstd, p, bias, lse, resid, oflat, total;  // p: P, or q | k | v in the core's layout
 };
 CtxLayout ctx_layout(const ModDims& d) {
   CtxLayout c;
   size_t o = 0;
+  const size_t act = d.B * d.N * d.H * d.N * d.D * 2;  // one [B, N, H, N, D] bf16 tensor
   c.x = o;     o += rup(d.M * d.C * 2);
   c.mean = o;  o += rup(d.M * 4);
   c.rstd = o;  o += rup(d.M * 4);
-  c.p = o;     o += rup(d.M * d.Fp * 2);
+  c.p = o;     o += rup(heads_flow(d) ? 3 * act : d.M * d.Fp * 2);
   c.bias = o;  o += rup(d.B * d.H * d.N * d.N * 2);
   c.lse = o;   o += rup(d.B * d.N * d.H * d.N * 4);
   c.resid = o; o += rup(d.M * d.HD * 2);
@@ -105,6 +113,10 @@ CtxLayout ctx_layout(const ModDims& d) {
 // pair rows of ld = H*D
 triattn_layout pair_layout(const ModDims& d, size_t ld) {
   return triattn_layout{static_cast<long long>(d.N * ld), static_cast<long long>(d.D), static_cast<long long>(ld)};
+}
+triattn_layout core_layout(const ModDims& d) {
+  return triattn_layout{static_cast<long long>(d.H * d.N * d.D), static_cast<long long>(d.N * d.D),
+                        static_cast<long long>(d.D)};
 }
 
 // Scratch of one forward or backward call.
@@ -118,7 +130,7 @@ WsLayout2 ws_layout2(const ModDims& d, const triattn_shape& core) {
   w.w_in_pad = o;  o += rup(d.C * d.Fp * 2);   // W_in with zero columns up to Fp
   w.dw_in_pad = o; o += rup(d.C * d.Fp * 4);   // dW_in, Fp wide
   w.p = o;      o += rup(d.M * d.Fp * 2);  // dP (backward)
-  w.doflat = o; o += rup(d.M * d.HD * 2);
+  w.doflat = o; o += rup(d.M * d.HD * 2);  // d_oflat, or dO in the core's layout (same size)
   w.dbias = o;  o += rup(d.B * d.H * d.N * d.N * 2);
   w.dx = o;     o += rup(d.M * d.C * 4);
   w.pg = o;     o += rup(static_cast<size_t>(kLnBlocks) * d.C * 4);
@@ -217,20 +229,34 @@ triattn_status tri_attn_module_fwd(const triattn_module_shape* shape, const void
   // length is a multiple of 8 elements)
   uint16_t* w_in_pad = reinterpret_cast<uint16_t*>(ws + w.w_in_pad);
   if (pad_w_in(d, w_in, w_in_pad, s) != cudaSuccess) return TRIATTN_ERR_CUDA;
-  if (gemm_traced(kKModGemm, gws, s, false, false, M, Fp, C, cx + c.x, C, w_in_pad, Fp, P, Fp, false) !=
-      TRIATTN_OK)
-    return TRIATTN_ERR_CUDA;
-  // the bias planes
-  if (bias_planes(d, P, Fp, 3 * HD, reinterpret_cast<uint16_t*>(cx + c.bias), false, s) != cudaSuccess)
-    return TRIATTN_ERR_CUDA;
-  // the attention core: q, k, v read from P's pair rows, o (and its
-  // residual) written into o_flat's
-  const triattn_layout lq = pair_layout(d, d.Fp), lo = pair_layout(d, d.HD);
-  st = tri_attn_fwd_strided(&core, P, P + HD, P + 2 * HD, &lq, cx + c.bias, mask, cx + c.oflat,
-                            reinterpret_cast<float*>(cx + c.lse), cx + c.resid, &lo, ws + w.core, w.total - w.core,
-                            stream);
+  const triattn_layout lo = pair_layout(d, d.HD);
+  if (heads_flow(d)) {
+    // q, k, v into the core's layout and the bias planes, from the GEMM's epilogue
+    const int Ni = static_cast<int>(d.N), Hi = static_cast<int>(d.H), Di = static_cast<int>(d.D);
+    if (trace_call(kKModGemm, s, [&] {
+          return launch_gemm_heads(false, M, Fp, C, cx + c.x, C, w_in_pad, Fp, 3, Hi, Di, Ni, static_cast<int>(d.B),
+                                   P, cx + c.bias, Hi, current_wait_ctl(), s);
+        }) != cudaSuccess)
+      return TRIATTN_ERR_CUDA;
+    const size_t act = d.B * d.N * d.H * d.N * d.D;
+    const triattn_layout lq = core_layout(d);
+    st = tri_attn_fwd_strided(&core, P, P + act, P + 2 * act, &lq, cx + c.bias, mask, cx + c.oflat,
+                              reinterpret_cast<float*>(cx + c.lse), cx + c.resid, &lo, ws + w.core, w.total - w.core,
+                              stream);
+  } else {
+    if (gemm_traced(kKModGemm, gws, s, false, false, M, Fp, C, cx + c.x, C, w_in_pad, Fp, P, Fp, false) !=
+        TRIATTN_OK)
+      return TRIATTN_ERR_CUDA;
+    if (bias_planes(d, P, Fp, 3 * HD, reinterpret_cast<uint16_t*>(cx + c.bias), false, s) != cudaSuccess)
+      return TRIATTN_ERR_CUDA;
+    // the core reads q, k, v from P's pair rows
+    const triattn_layout lq = pair_layout(d, d.Fp);
+    st = tri_attn_fwd_strided(&core, P, P + HD, P + 2 * HD, &lq, cx + c.bias, mask, cx + c.oflat,
+                              reinterpret_cast<float*>(cx + c.lse), cx + c.resid, &lo, ws + w.core, w.total - w.core,
+                              stream);
+  }
   if (st != TRIATTN_OK) return st;
-  // out = o_flat W_o
+  // out = o_flat W_o (the core wrote o into o_flat's pair rows)
   return gemm_traced(kKModGemm, gws, s, false, false, M, C, HD, cx + c.oflat, HD, w_o, C, out, C, false);
 }
 
@@ -257,18 +283,33 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   void* const gws = ws + w.gemm;
   const int M = static_cast<int>(d.M), C = static_cast<int>(d.C), HD = static_cast<int>(d.HD),
             Fp = static_cast<int>(d.Fp);
-  // out = o_flat W_o:  dW_o = o_flat^T d_out,  d_oflat = d_out W_o^T
-  if (gemm_traced(kKModGemm, gws, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, true) != TRIATTN_OK ||
-      gemm_traced(kKModGemm, gws, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, false) != TRIATTN_OK)
+  // out = o_flat W_o:  dW_o = o_flat^T d_out,  d_oflat = d_out W_o^T (in the
+  // heads flow straight into dO in the core's layout)
+  if (gemm_traced(kKModGemm, gws, s, true, false, HD, C, M, cx + c.oflat, HD, d_out, C, d_w_o, C, true) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
+  const bool hf = heads_flow(d);
+  if (hf) {
+    const int Ni = static_cast<int>(d.N), Hi = static_cast<int>(d.H), Di = static_cast<int>(d.D);
+    if (trace_call(kKModGemm, s, [&] {
+          return launch_gemm_heads(true, M, HD, C, d_out, C, w_o, C, 1, Hi, Di, Ni, static_cast<int>(d.B),
+                                   ws + w.doflat, nullptr, 0, current_wait_ctl(), s);
+        }) != cudaSuccess)
+      return TRIATTN_ERR_CUDA;
+  } else if (gemm_traced(kKModGemm, gws, s, false, true, M, HD, C, d_out, C, w_o, C, ws + w.doflat, HD, false) !=
+             TRIATTN_OK) {
+    return TRIATTN_ERR_CUDA;
+  }
   // the attention core, dq, dk, dv written into dP = [dq | dk | dv | dbias]
   // where they lie in the pair layout
   const uint16_t* P = reinterpret_cast<const uint16_t*>(cx + c.p);
   uint16_t* dP = reinterpret_cast<uint16_t*>(ws + w.p);
-  const triattn_layout lq = pair_layout(d, d.Fp), lo = pair_layout(d, d.HD);
-  st = tri_attn_bwd_strided(&core, P, P + HD, P + 2 * HD, &lq, cx + c.bias, mask, cx + c.oflat, cx + c.resid, &lo,
-                            reinterpret_cast<const float*>(cx + c.lse), ws + w.doflat, dP, dP + HD, dP + 2 * HD,
-                            ws + w.dbias, ws + w.core, w.total - w.core, stream);
+  const size_t act = d.B * d.N * d.H * d.N * d.D;
+  const triattn_layout lq = hf ? core_layout(d) : pair_layout(d, d.Fp), lo = pair_layout(d, d.HD),
+                       ldo = hf ? core_layout(d) : pair_layout(d, d.HD), lg = pair_layout(d, d.Fp);
+  const size_t step = hf ? act : static_cast<size_t>(HD);
+  st = tri_attn_bwd_strided(&core, P, P + step, P + 2 * step, &lq, cx + c.bias, mask, cx + c.oflat, cx + c.resid,
+                            &lo, reinterpret_cast<const float*>(cx + c.lse), ws + w.doflat, &ldo, dP, dP + HD,
+                            dP + 2 * HD, &lg, ws + w.dbias, ws + w.core, w.total - w.core, stream);
   if (st != TRIATTN_OK) return st;
   if (bias_planes(d, dP, Fp, 3 * HD, reinterpret_cast<uint16_t*>(ws + w.dbias), true, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;

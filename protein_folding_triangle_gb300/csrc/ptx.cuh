@@ -158,6 +158,21 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+// The same for 4-D and 5-D maps, without the commit (several stores may form
+// one bulk group: bulk_commit closes it).
+__device__ __forceinline__ void tma_store_4d_nc(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_5d_nc(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                                int c3, int c4) {
+  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_allow1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }

@@ -94,7 +94,7 @@ def _declare(lib):
     lp = ctypes.POINTER(Layout)
     lib.tri_attn_fwd_strided.argtypes = [sp, vp, vp, vp, lp, vp, vp, vp, vp, vp, lp, vp, ctypes.c_size_t, vp]
     lib.tri_attn_fwd_strided.restype = ctypes.c_int
-    lib.tri_attn_bwd_strided.argtypes = ([sp, vp, vp, vp, lp, vp, vp, vp, vp, lp, vp, vp, vp, vp, vp, vp, vp,
+    lib.tri_attn_bwd_strided.argtypes = ([sp, vp, vp, vp, lp, vp, vp, vp, vp, lp, vp, vp, lp, vp, vp, vp, lp, vp, vp,
                                           ctypes.c_size_t, vp])
     lib.tri_attn_bwd_strided.restype = ctypes.c_int
     lib.tri_attn_bwd.restype = ctypes.c_int
@@ -315,16 +315,16 @@ def tri_attn_fwd_strided(q, k, v, bias, mask, o, lse, o_resid=None, *, workspace
 
 def tri_attn_bwd_strided(q, k, v, bias, mask, o, o_resid, lse, do, dq, dk, dv, dbias, *, workspace=None,
                          stream=None):
-    """Backward on views: q, k, v, dq, dk, dv share one row layout; o, o_resid
-    and do another; dq, dk, dv and dbias ([B, H, N, N] bf16) written in place."""
+    """Backward on views: q, k, v share one row layout, o and o_resid a
+    second, do a third and dq, dk, dv a fourth; dq, dk, dv and dbias
+    ([B, H, N, N] bf16) written in place."""
     s = shape_of(q)
     B, No, H, N, D = q.shape
-    lq, lo = layout_of(q), layout_of(o)
-    for name, t in (("q", q), ("k", k), ("v", v), ("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_view(t, name, (B, No, H, N, D), lq)
-    for name, t in (("o", o), ("o_resid", o_resid), ("do", do)):
+    lq, lo, ldo, lg = layout_of(q), layout_of(o), layout_of(do), layout_of(dq)
+    for name, t, lay in (("q", q, lq), ("k", k, lq), ("v", v, lq), ("dq", dq, lg), ("dk", dk, lg), ("dv", dv, lg),
+                         ("o", o, lo), ("o_resid", o_resid, lo), ("do", do, ldo)):
         if t is not None:
-            _check_view(t, name, (B, No, H, N, D), lo)
+            _check_view(t, name, (B, No, H, N, D), lay)
     _check(bias, "bias", (B, H, N, N))
     _check(dbias, "dbias", (B, H, N, N))
     _check(lse, "lse", (B, No, H, N), torch.float32)
@@ -334,7 +334,8 @@ def tri_attn_bwd_strided(q, k, v, bias, mask, o, o_resid, lse, do, dq, dk, dv, d
         workspace = torch.empty(bwd_workspace_bytes(s), dtype=torch.uint8, device=q.device)
     code = load().tri_attn_bwd_strided(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), ctypes.byref(lq), _ptr(bias),
                                        _ptr(mask), _ptr(o), _ptr(o_resid), ctypes.byref(lo), _ptr(lse), _ptr(do),
-                                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
+                                       ctypes.byref(ldo), _ptr(dq), _ptr(dk), _ptr(dv), ctypes.byref(lg),
+                                       _ptr(dbias), _ptr(workspace),
                                        ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                                        _stream_ptr(stream))
     _raise(code, "tri_attn_bwd_strided")

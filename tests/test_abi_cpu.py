@@ -451,7 +451,7 @@ def test_strided_layout_checks(lib):
                                         ctypes.c_size_t(nbytes), None)
 
     def bwd(lq, lo):
-        return lib.tri_attn_bwd_strided(ctypes.byref(s), f, f, f, lq, f, None, f, None, lo, f, f, f, f, f, f,
+        return lib.tri_attn_bwd_strided(ctypes.byref(s), f, f, f, lq, f, None, f, None, lo, f, f, lo, f, f, f, lq, f,
                                         None, ctypes.c_size_t(0), None)
 
     good = T.Layout(2 * 40 * 32, 40 * 32, 32)       # [B, N_o, H, N, D]

@@ -63,6 +63,12 @@ CASES = [
     # H = 3 gives a projection width of 291 (padded to 296)
     (1, 40, 96, 2, 16, 0.0),
     (1, 32, 192, 3, 32, 0.1),
+    # N a multiple of 32: q, k, v, the bias planes and dO written by the GEMM
+    # epilogues in the core's layout (the cases above with other N read the
+    # pair rows in place); D = 16 with H = 3 puts a head and the bias columns
+    # in one 32-column chunk
+    (1, 64, 64, 3, 16, 0.1),
+    (2, 32, 128, 4, 32, 0.2),
 ]
 
 

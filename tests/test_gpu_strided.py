@@ -81,6 +81,15 @@ def test_strided_matches_contiguous_bitwise(case):
     for got, ref in ((dqs, dq), (dks, dk), (dvs, dv)):
         assert torch.equal(got.contiguous().view(torch.int16), ref.view(torch.int16))
     assert torch.equal(dbs.view(torch.int16), db.view(torch.int16))
+    # mixed layouts: q, k, v and dO contiguous, o and its residual in pair rows,
+    # dq, dk, dv into pair rows (the module's backward)
+    dP.copy_(dP0)
+    dbs.zero_()
+    T.tri_attn_bwd_strided(q, k, v, bias, mask, os_, es, lse_s, do, dqs, dks, dvs, dbs)
+    torch.cuda.synchronize()
+    for got, ref in ((dqs, dq), (dks, dk), (dvs, dv)):
+        assert torch.equal(got.contiguous().view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(dbs.view(torch.int16), db.view(torch.int16))
     keep = torch.ones(ldq, dtype=torch.bool)
     keep[off:off + 3 * H * D] = False
     assert torch.equal(dP[..., keep].view(torch.int16), dP0[..., keep].view(torch.int16))

@@ -191,27 +191,35 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
   const int rc = threadIdx.x % Ch, rpart = threadIdx.x / Ch;
   const bool reducer = threadIdx.x < kSplit * Ch;
   float accg = 0.f, accb = 0.f;
-  uint4 xr[Ch * 8 / 256];
-  float4 dyr[kCh][2];
-  float mean = 0.f, rstd = 0.f;
-  auto fetch = [&](size_t tile) {
+  // this tile's X, dy and statistics, and the next tile's in flight: the next
+  // loads are issued as soon as this tile's X is in shared memory
+  struct Regs {
+    uint4 xr[Ch * 8 / 256];
+    float4 dyr[kCh][2];
+    float mean, rstd;
+  };
+  Regs cur, nxt;
+  auto fetch = [&](size_t tile, Regs& r) {
     const size_t m0 = tile * kPairs;
-    fetch_cm_tile<Ch>(X, m0 / NN, m0 % NN, NN, xr);
+    fetch_cm_tile<Ch>(X, m0 / NN, m0 % NN, NN, r.xr);
     const size_t m = m0 + pr;
 #pragma unroll
     for (int i = 0; i < kCh; ++i) {
       const int c0 = 8 * (qq + 4 * i);
-      dyr[i][0] = *reinterpret_cast<const float4*>(dy + m * Ch + c0);
-      dyr[i][1] = *reinterpret_cast<const float4*>(dy + m * Ch + c0 + 4);
+      r.dyr[i][0] = *reinterpret_cast<const float4*>(dy + m * Ch + c0);
+      r.dyr[i][1] = *reinterpret_cast<const float4*>(dy + m * Ch + c0 + 4);
     }
-    mean = mean_in[m];
-    rstd = rstd_in[m];
+    r.mean = mean_in[m];
+    r.rstd = rstd_in[m];
   };
-  if (blockIdx.x < tiles) fetch(blockIdx.x);
+  if (blockIdx.x < tiles) fetch(blockIdx.x, cur);
   for (size_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const size_t m0 = tile * kPairs;
     const size_t b = m0 / NN, pos0 = m0 % NN;
-    put_cm_tile<Ch>(xr, sXh);
+    put_cm_tile<Ch>(cur.xr, sXh);
+    if (tile + gridDim.x < tiles) fetch(tile + gridDim.x, nxt);
+    const auto& dyr = cur.dyr;
+    const float mean = cur.mean, rstd = cur.rstd;
     __syncthreads();
     float sg = 0.f, sgx = 0.f;
 #pragma unroll
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
       accg += (g4[0] + g4[1]) + (g4[2] + g4[3]);
       accb += (b4[0] + b4[1]) + (b4[2] + b4[3]);
     }
-    if (tile + gridDim.x < tiles) fetch(tile + gridDim.x);
+    cur = nxt;
     __syncthreads();
   }
   if (reducer) {

@@ -92,12 +92,14 @@ enum GemmMode { kPlain = 0, kGated = 1, kGateBwd = 2, kHeads = 3 };
 
 // Per mode: epilogue warps (4; 16 for the gated tiles, whose epilogue does
 // the gating arithmetic: four warps per TMEM lane quarter, one per (branch,
-// 32-channel chunk)), ring stages, and bytes per staging buffer (FP32 or BF16
-// 32 x 32 blocks; the gated modes write BF16 only).
+// 32-channel chunk), and for the heads epilogue, whose many small stores of
+// a short-K (HBM-bound) GEMM are latency-bound with 4), ring stages, and bytes
+// per staging buffer (FP32 or BF16 32 x 32 blocks; the gated and heads modes
+// write BF16 only).
 template <int MODE> struct GemmCfg {
-  static constexpr int kEpi = (MODE == 0 || MODE == 3) ? 4 : 16;
-  static constexpr int kS = (MODE == 0 || MODE == 3) ? 4 : 3;
-  static constexpr int kBuf = (MODE == 0 || MODE == 3) ? 4096 : 2048;
+  static constexpr int kEpi = MODE == 0 ? 4 : 16;
+  static constexpr int kS = MODE == 0 ? 4 : 3;
+  static constexpr int kBuf = MODE == 0 ? 4096 : 2048;
   static constexpr int kThreads = (2 + kEpi) * 32;
 };
 
@@ -324,28 +326,27 @@ __global__ void __launch_bounds__(GemmCfg<MODE>::kThreads, 1)
       // bias columns [nh, nh + nbias) of this chunk: one 32-element row per head
       const int c_lo = max(col, nh), c_hi = min(col + 32, nh + p.nbias);
       if (c_lo >= c_hi) return;
-      // the chunk row-major (64-byte swizzled rows) in the buffer's lower half,
-      // then each bias column as one 32-pair row in its upper half, 16 rows
-      // at a time at a 128-byte pitch (TMA sources are 128-byte aligned)
+      // the chunk row-major (64-byte swizzled rows) in one staging buffer,
+      // then each bias column as one 32-pair row in the other, 16 rows at a
+      // time at a 128-byte pitch (TMA sources are 128-byte aligned)
       uint8_t* buf = next_buf();
       put_bf16(buf, v);
-      __syncwarp();
+      ++nst;
+      uint8_t* rows = stg + (nst & 1) * kBuf;
       const int b = bi / p.Ntok, i = bi - b * p.Ntok;
       for (int cs = c_lo; cs < c_hi; cs += 16) {
         const int ce = min(cs + 16, c_hi);
-        if (cs > c_lo) {  // the previous group's stores have read the upper half
-          if (lane == 0) bulk_wait_read();
-          __syncwarp();
-        }
+        if (lane == 0) bulk_wait_read();  // every earlier store has read its buffer
+        __syncwarp();
         for (int c = cs; c < ce; ++c) {
           const int e = c - col;
-          *reinterpret_cast<uint16_t*>(buf + 2048 + (c - cs) * 128 + lane * 2) =
+          *reinterpret_cast<uint16_t*>(rows + (c - cs) * 128 + lane * 2) =
               *reinterpret_cast<const uint16_t*>(buf + lane * 64 + (((e >> 3) ^ ((lane >> 1) & 3)) << 4) + (e & 7) * 2);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          for (int c = cs; c < ce; ++c) tma_store_4d_nc(&tm_x, buf + 2048 + (c - cs) * 128, j0, i, c - nh, b);
+          for (int c = cs; c < ce; ++c) tma_store_4d_nc(&tm_x, rows + (c - cs) * 128, j0, i, c - nh, b);
           bulk_commit();
         }
       }

@@ -30,19 +30,27 @@ def heads_view(buf, col, H, D):
 
 
 CASES = [
-    # (B, N, H, D, mask, ld_qkv, ld_o): ragged N, D = 16 and 32, extra columns on both sides
+    # (B, N, H, D, mask, ld_qkv, ld_o[, N_o]): ragged N, D = 16 and 32, extra columns on
+    # both sides, an outer-axis shard of 37 of 48 slices (groups of 4 past N_o)
     (1, 136, 2, 32, "tail", 3 * 2 * 32 + 2 + 6, 2 * 32 + 8),
     (2, 40, 3, 16, "random", 3 * 3 * 16 + 3 + 5 + 16, 3 * 16),
     (1, 200, 4, 32, None, 3 * 4 * 32 + 4 + 4, 4 * 32),
     (1, 17, 1, 32, "random", 3 * 32 + 8 + 8, 32),
+    (2, 48, 2, 32, "tail", 3 * 2 * 32 + 2 + 14, 2 * 32, 37),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}N{c[1]}H{c[2]}D{c[3]}" for c in CASES])
+@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}N{c[1]}H{c[2]}D{c[3]}No{c[7] if len(c) > 7 else c[1]}"
+                                             for c in CASES])
 def test_strided_matches_contiguous_bitwise(case):
-    B, N, H, D, mask_kind, ldq, ldo = case
+    B, N, H, D, mask_kind, ldq, ldo = case[:7]
+    No = case[7] if len(case) > 7 else N
     g = torch.Generator().manual_seed(N + H + D)
     x = S.make_inputs(S.custom(B, N, H, D, mask=mask_kind or "none", mask_frac=0.1 if mask_kind else 0.0), seed=N)
+    if No < N:  # an outer-axis shard: the first No slices
+        for n in ("q", "k", "v", "do", "mask"):
+            if x[n] is not None:
+                x[n] = x[n][:, :No].contiguous()
     dev = torch.device("cuda")
     q, k, v, bias, do = (x[n].to(dev) for n in ("q", "k", "v", "bias", "do"))
     mask = x["mask"].to(dev) if x["mask"] is not None else None
@@ -51,13 +59,13 @@ def test_strided_matches_contiguous_bitwise(case):
 
     # pair-row buffers filled with random junk; the heads copied in at offsets
     off = 8 if ldq % 8 == 0 and ldq >= 3 * H * D + 8 else 0
-    P = torch.randn(B, N, N, ldq, generator=g).to(torch.bfloat16).to(dev)
+    P = torch.randn(B, No, N, ldq, generator=g).to(torch.bfloat16).to(dev)
     qs, ks, vs = (heads_view(P, off + t * H * D, H, D) for t in range(3))
     qs.copy_(q); ks.copy_(k); vs.copy_(v)
     P0 = P.clone()
-    Ob = torch.randn(B, N, N, ldo, generator=g).to(torch.bfloat16).to(dev)
-    Eb = torch.randn(B, N, N, ldo, generator=g).to(torch.bfloat16).to(dev)
-    Gb = torch.randn(B, N, N, ldo, generator=g).to(torch.bfloat16).to(dev)
+    Ob = torch.randn(B, No, N, ldo, generator=g).to(torch.bfloat16).to(dev)
+    Eb = torch.randn(B, No, N, ldo, generator=g).to(torch.bfloat16).to(dev)
+    Gb = torch.randn(B, No, N, ldo, generator=g).to(torch.bfloat16).to(dev)
     os_, es, dos = heads_view(Ob, 0, H, D), heads_view(Eb, 0, H, D), heads_view(Gb, 0, H, D)
     dos.copy_(do)
     Ob0, Eb0 = Ob.clone(), Eb.clone()
@@ -72,7 +80,7 @@ def test_strided_matches_contiguous_bitwise(case):
     for buf, ref in ((Ob, Ob0), (Eb, Eb0)):
         assert torch.equal(buf[..., H * D:].view(torch.int16), ref[..., H * D:].view(torch.int16))
 
-    dP = torch.randn(B, N, N, ldq, generator=g).to(torch.bfloat16).to(dev)
+    dP = torch.randn(B, No, N, ldq, generator=g).to(torch.bfloat16).to(dev)
     dP0 = dP.clone()
     dqs, dks, dvs = (heads_view(dP, off + t * H * D, H, D) for t in range(3))
     dbs = torch.empty_like(db)

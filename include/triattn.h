@@ -19,7 +19,9 @@
  *    16-byte aligned, except the key mask (2-byte aligned) and lse (4-byte
  *    aligned), so that a shard of the outer axis may start at any slice.
  *    "bf16" means IEEE bfloat16 stored as uint16.
- *  - Layouts: q, k, v, o, o_resid, dO, dq, dk, dv  [B, N_o, H, N, D] bf16
+ *  - Layouts (the strided entry points below take q, k, v, o, o_resid, dO,
+ *    dq, dk, dv in other row layouts):
+ *             q, k, v, o, o_resid, dO, dq, dk, dv  [B, N_o, H, N, D] bf16
  *             bias, dbias                         [B, H, N, N]      bf16
  *             mask (optional, additive)           [B, N_o, N]       bf16
  *             lse                                 [B, N_o, H, N]    fp32 (natural log)

@@ -681,7 +681,7 @@ def run_module(args):
     fl_core = flops(w)[2]
     gemm_flop = 3 * (2 * M * C * F + 2 * M * HD * C)  # forward, then dX and dW of each projection
     by = {"module_ln_fwd": M * C * 4 + M * 8,             # z in, x out, mean and rstd
-          "module_ln_bwd": M * C * 8 + M * 8,             # z, dx (FP32) in, dz out, mean and rstd
+          "module_ln_bwd": M * C * 6 + M * 8,             # z, dx (BF16) in, dz out, mean and rstd
           "module_layout": 2 * (7 * act + 2 * Bn * H * N * N * 2)}  # q k v o / do dq dk dv, bias and dbias planes
     pk = peaks()
     per = {}
@@ -766,10 +766,12 @@ def run_trimul(args):
         torch.cuda.synchronize(dev)
         tr = T.trace_read()
         T.trace_enable(False)
-        by = {"trimul_ln_in": M * Cz * 4 + 8 * M + M * Cz * 8 + 8 * M,
+        # input LayerNorm: fwd reads z, writes x and the statistics; bwd reads z, dx (BF16) and the statistics
+        by = {"trimul_ln_in": M * Cz * 4 + 8 * M + M * Cz * 6 + 8 * M,
               # projection + gating: fwd reads x, writes a, b, g; bwd reads x, dA, dB, writes dp's 4 C_h columns
               "trimul_proj_gate": (M * Cz * 2 + 2 * M * Ch * 2 + M * Cz * 2) + (M * Cz * 2 + 2 * M * Ch * 2 + M * 4 * Ch * 2),
-              "trimul_ln_out": (2 * M * Ch * 2 + 8 * M) + (M * Ch * 2 + M * Ch * 4 + 8 * M + M * Ch * 2),
+              # output LayerNorm: fwd reads X, writes y and the statistics; bwd reads X, dy (BF16), writes dX
+              "trimul_ln_out": (2 * M * Ch * 2 + 8 * M) + (M * Ch * 2 + M * Ch * 2 + 8 * M + M * Ch * 2),
               "trimul_out_gate": 3 * M * Cz * 2 + 5 * M * Cz * 2}
         fl = {"trimul_proj_gemm": 3 * 2 * M * Ch * Cz + 2 * 2 * M * Cz * F,
               "trimul_contract_gemm": 3 * 2 * Bn * Ch * N ** 3}

@@ -132,7 +132,7 @@ WsLayout2 ws_layout2(const ModDims& d, const triattn_shape& core) {
   w.p = o;      o += rup(d.M * d.Fp * 2);  // dP (backward)
   w.doflat = o; o += rup(d.M * d.HD * 2);  // d_oflat, or dO in the core's layout (same size)
   w.dbias = o;  o += rup(d.B * d.H * d.N * d.N * 2);
-  w.dx = o;     o += rup(d.M * d.C * 4);
+  w.dx = o;     o += rup(d.M * d.C * 2);
   w.pg = o;     o += rup(static_cast<size_t>(kLnBlocks) * d.C * 4);
   w.pb = o;     o += rup(static_cast<size_t>(kLnBlocks) * d.C * 4);
   // the core's forward and backward workspaces (one at a time)
@@ -313,14 +313,14 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   if (st != TRIATTN_OK) return st;
   if (bias_planes(d, dP, Fp, 3 * HD, reinterpret_cast<uint16_t*>(ws + w.dbias), true, s) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  // P = x W_in:  dW_in = x^T dP,  dx = dP W_in^T (FP32), both Fp wide (dP's
+  // P = x W_in:  dW_in = x^T dP,  dx = dP W_in^T (BF16), both Fp wide (dP's
   // padding columns are zero, so are W_in's); dW_in's first F columns copied out
   uint16_t* w_in_pad = reinterpret_cast<uint16_t*>(ws + w.w_in_pad);
   float* dw_in_pad = reinterpret_cast<float*>(ws + w.dw_in_pad);
   if (pad_w_in(d, w_in, w_in_pad, s) != cudaSuccess) return TRIATTN_ERR_CUDA;
   if (gemm_traced(kKModGemm, gws, s, true, false, C, Fp, M, cx + c.x, C, dP, Fp, dw_in_pad, Fp, true) !=
           TRIATTN_OK ||
-      gemm_traced(kKModGemm, gws, s, false, true, M, C, Fp, dP, Fp, w_in_pad, Fp, ws + w.dx, C, true) !=
+      gemm_traced(kKModGemm, gws, s, false, true, M, C, Fp, dP, Fp, w_in_pad, Fp, ws + w.dx, C, false) !=
           TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   if (trace_call(kKModLayout, s, [&] {
@@ -331,7 +331,7 @@ triattn_status tri_attn_module_bwd(const triattn_module_shape* shape, const void
   float* pg = reinterpret_cast<float*>(ws + w.pg);
   float* pb = reinterpret_cast<float*>(ws + w.pb);
   if (trace_call(kKModLnBwd, s, [&] {
-        return ln_rows_bwd(d.M, C, z, reinterpret_cast<const float*>(ws + w.dx), ln_w,
+        return ln_rows_bwd(d.M, C, z, ws + w.dx, ln_w,
                           reinterpret_cast<const float*>(cx + c.mean), reinterpret_cast<const float*>(cx + c.rstd),
                           dz, pg, pb, s);
       }) != cudaSuccess)

@@ -19,8 +19,10 @@ namespace {
 namespace pairops {
 
 constexpr int kMaxC = 256;          // LayerNorm: up to 8 features per lane
-constexpr int kLnBlocks = 152 * 5;     // backward grid, one wave; the dgamma / dbeta partial rows depend on it
-constexpr int kLnFwdBlocks = 152 * 8;  // forward grid (no partials): eight blocks per SM
+constexpr int kLnBwdPerSm = 3;                   // backward blocks resident per SM (register bound)
+constexpr int kLnBlocks = 152 * kLnBwdPerSm;     // backward grid, one wave; the dgamma / dbeta partial rows depend on it
+constexpr int kLnFwdPerSm = 4;                   // forward blocks resident per SM
+constexpr int kLnFwdBlocks = 152 * kLnFwdPerSm;  // forward grid (no partials), one wave
 constexpr size_t kGemmWorkspace = 32u << 20;  // split-K partials of the weight-gradient GEMMs
 
 inline bool ln_width_ok(int C) { return C >= 32 && C <= kMaxC && C % 32 == 0; }
@@ -113,56 +115,115 @@ __device__ __forceinline__ void ld_f32(const float* p, float (&f)[K]) {
   }
 }
 
+// K consecutive BF16 features of one row kept packed (two per word; for odd
+// K the last word holds one), loaded with the widest aligned accesses, and
+// their unpacking: a warp can keep several rows in flight for the registers
+// of one unpacked row.
+template <int K>
+struct Packed {
+  uint32_t w[(K + 1) / 2];
+};
+template <int K>
+__device__ __forceinline__ void ld_packed(const uint16_t* p, Packed<K>& r) {
+  if constexpr (K % 8 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 8; ++j) {
+      const uint4 v = reinterpret_cast<const uint4*>(p)[j];
+      r.w[4 * j] = v.x;
+      r.w[4 * j + 1] = v.y;
+      r.w[4 * j + 2] = v.z;
+      r.w[4 * j + 3] = v.w;
+    }
+  } else if constexpr (K % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 4; ++j) {
+      const uint2 v = reinterpret_cast<const uint2*>(p)[j];
+      r.w[2 * j] = v.x;
+      r.w[2 * j + 1] = v.y;
+    }
+  } else if constexpr (K % 2 == 0) {
+#pragma unroll
+    for (int j = 0; j < K / 2; ++j) r.w[j] = reinterpret_cast<const uint32_t*>(p)[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < (K + 1) / 2; ++j)
+      r.w[j] = static_cast<uint32_t>(p[2 * j]) | (2 * j + 1 < K ? static_cast<uint32_t>(p[2 * j + 1]) << 16 : 0u);
+  }
+}
+template <int K>
+__device__ __forceinline__ void unpack(const Packed<K>& r, float (&f)[K]) {
+#pragma unroll
+  for (int e = 0; e < K; ++e) f[e] = (e & 1) ? bf16hi_to_f32(r.w[e >> 1]) : bf16lo_to_f32(r.w[e >> 1]);
+}
+
 // One warp per pair: x = (z - mean) * rstd * gamma + beta (BF16), mean and
 // rstd saved in FP32.  Lane l holds the C / 32 consecutive features from
-// l C / 32.
+// l C / 32; the loads of several pairs are in flight together.
 template <int C>
-__global__ void __launch_bounds__(256) ln_fwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ gamma,
-                                                     const float* __restrict__ beta, uint16_t* __restrict__ x,
-                                                     float* __restrict__ mean_out, float* __restrict__ rstd_out,
-                                                     size_t M) {
+__global__ void __launch_bounds__(256, kLnFwdPerSm) ln_fwd_kernel(const uint16_t* __restrict__ z,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ beta,
+                                                                  uint16_t* __restrict__ x,
+                                                                  float* __restrict__ mean_out,
+                                                                  float* __restrict__ rstd_out, size_t M) {
   constexpr int kPer = C / 32;
+  constexpr int kRows = C <= 128 ? 8 : 4;  // rows a warp has in flight
   const int lane = threadIdx.x & 31;
   const int c0 = lane * kPer;
   float gm[kPer], bt[kPer];
   ld_f32<kPer>(gamma + c0, gm);
   ld_f32<kPer>(beta + c0, bt);
   const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
-  for (size_t m = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; m < M; m += warps) {
-    float v[kPer];
-    ld_bf16<kPer>(z + m * C + c0, v);
-    float s = 0.f;
+  for (size_t m0 = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; m0 < M;
+       m0 += kRows * warps) {
+    // the loads of all kRows rows in flight before the first reduction
+    Packed<kPer> zr[kRows];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) s += v[e];
-    const float mean = warp_sum(s) * (1.f / C);
-    float ss = 0.f;
+    for (int r = 0; r < kRows; ++r)
+      if (m0 + r * warps < M) ld_packed<kPer>(z + (m0 + r * warps) * C + c0, zr[r]);
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) ss += (v[e] - mean) * (v[e] - mean);
-    const float rstd = rsqrtf(warp_sum(ss) * (1.f / C) + 1e-5f);
-    float o[kPer];
+    for (int r = 0; r < kRows; ++r) {
+      const size_t m = m0 + r * warps;
+      if (m >= M) break;  // the same m in every lane
+      float v[kPer];
+      unpack<kPer>(zr[r], v);
+      float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) o[e] = (v[e] - mean) * rstd * gm[e] + bt[e];
-    st_bf16<kPer>(x + m * C + c0, o);
-    if (lane == 0) {
-      mean_out[m] = mean;
-      rstd_out[m] = rstd;
+      for (int e = 0; e < kPer; ++e) s += v[e];
+      const float mean = warp_sum(s) * (1.f / C);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) ss += (v[e] - mean) * (v[e] - mean);
+      const float rstd = rsqrtf(warp_sum(ss) * (1.f / C) + 1e-5f);
+      float o[kPer];
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) o[e] = (v[e] - mean) * rstd * gm[e] + bt[e];
+      st_bf16<kPer>(x + m * C + c0, o);
+      if (lane == 0) {
+        mean_out[m] = mean;
+        rstd_out[m] = rstd;
+      }
     }
   }
 }
 
-// One warp per pair: dz = rstd (g - mean(g) - xhat mean(g xhat)), g = dx gamma.
-// The warp also accumulates dgamma = sum dx xhat and dbeta = sum dx over its
-// pairs (fixed grid-stride assignment); the block adds its 8 warps' sums in
-// warp order and writes one partial row per block.  Lane l holds the C / 32
-// consecutive features from l C / 32.
+// One warp per pair: dz = rstd (g - mean(g) - xhat mean(g xhat)), g = dx gamma,
+// dx BF16.  The warp also accumulates dgamma = sum dx xhat and dbeta = sum dx
+// over its pairs (fixed grid-stride assignment, ascending); the block adds
+// its 8 warps' sums in warp order and writes one partial row per block.  Lane
+// l holds the C / 32 consecutive features from l C / 32; the loads of
+// several pairs are in flight together.
 template <int C>
-__global__ void __launch_bounds__(256) ln_bwd_kernel(const uint16_t* __restrict__ z, const float* __restrict__ dx,
-                                                     const float* __restrict__ gamma,
-                                                     const float* __restrict__ mean_in,
-                                                     const float* __restrict__ rstd_in, uint16_t* __restrict__ dz,
-                                                     float* __restrict__ part_gamma, float* __restrict__ part_beta,
-                                                     size_t M) {
+__global__ void __launch_bounds__(256, kLnBwdPerSm) ln_bwd_kernel(const uint16_t* __restrict__ z,
+                                                                  const uint16_t* __restrict__ dx,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ mean_in,
+                                                                  const float* __restrict__ rstd_in,
+                                                                  uint16_t* __restrict__ dz,
+                                                                  float* __restrict__ part_gamma,
+                                                                  float* __restrict__ part_beta, size_t M) {
   constexpr int kPer = C / 32;
+  constexpr int kRows = C <= 128 ? 4 : (C <= 192 ? 2 : 1);  // rows a warp has in flight
   __shared__ float red_g[8][C], red_b[8][C];
   const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
   const int c0 = lane * kPer;
@@ -172,26 +233,42 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const uint16_t* __restrict_
   float accg[kPer], accb[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) accg[e] = accb[e] = 0.f;
-  for (size_t m = static_cast<size_t>(blockIdx.x) * 8 + warp; m < M; m += warps) {
-    const float mean = mean_in[m], rstd = rstd_in[m];
-    float xh[kPer], d[kPer], g[kPer];
-    ld_bf16<kPer>(z + m * C + c0, xh);
-    ld_f32<kPer>(dx + m * C + c0, d);
-    float sg = 0.f, sgx = 0.f;
+  for (size_t m0 = static_cast<size_t>(blockIdx.x) * 8 + warp; m0 < M; m0 += kRows * warps) {
+    Packed<kPer> zr[kRows], dr[kRows];
+    float mu[kRows], rs[kRows];
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      xh[e] = (xh[e] - mean) * rstd;
-      accg[e] += d[e] * xh[e];
-      accb[e] += d[e];
-      g[e] = d[e] * gm[e];
-      sg += g[e];
-      sgx += g[e] * xh[e];
+    for (int r = 0; r < kRows; ++r)
+      if (m0 + r * warps < M) {
+        const size_t m = m0 + r * warps;
+        ld_packed<kPer>(z + m * C + c0, zr[r]);
+        ld_packed<kPer>(dx + m * C + c0, dr[r]);
+        mu[r] = mean_in[m];
+        rs[r] = rstd_in[m];
+      }
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const size_t m = m0 + r * warps;
+      if (m >= M) break;  // the same m in every lane
+      const float mean = mu[r], rstd = rs[r];
+      float xh[kPer], d[kPer], g[kPer];
+      unpack<kPer>(zr[r], xh);
+      unpack<kPer>(dr[r], d);
+      float sg = 0.f, sgx = 0.f;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        xh[e] = (xh[e] - mean) * rstd;
+        accg[e] += d[e] * xh[e];
+        accb[e] += d[e];
+        g[e] = d[e] * gm[e];
+        sg += g[e];
+        sgx += g[e] * xh[e];
+      }
+      const float a = warp_sum(sg) * (1.f / C), bb = warp_sum(sgx) * (1.f / C);
+      float o[kPer];
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) o[e] = rstd * (g[e] - a - xh[e] * bb);
+      st_bf16<kPer>(dz + m * C + c0, o);
     }
-    const float a = warp_sum(sg) * (1.f / C), bb = warp_sum(sgx) * (1.f / C);
-    float o[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) o[e] = rstd * (g[e] - a - xh[e] * bb);
-    st_bf16<kPer>(dz + m * C + c0, o);
   }
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
@@ -235,9 +312,10 @@ cudaError_t ln_fwd_launch(size_t M, const void* z, const float* g, const float* 
   return cudaGetLastError();
 }
 template <int C>
-cudaError_t ln_bwd_launch(size_t M, const void* z, const float* dx, const float* g, const float* mean,
+cudaError_t ln_bwd_launch(size_t M, const void* z, const void* dx, const float* g, const float* mean,
                           const float* rstd, void* dz, float* pg, float* pb, cudaStream_t s) {
-  ln_bwd_kernel<C><<<kLnBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), dx, g, mean, rstd,
+  ln_bwd_kernel<C><<<kLnBlocks, 256, 0, s>>>(static_cast<const uint16_t*>(z), static_cast<const uint16_t*>(dx), g,
+                                             mean, rstd,
                                              static_cast<uint16_t*>(dz), pg, pb, M);
   return cudaGetLastError();
 }
@@ -257,8 +335,8 @@ inline cudaError_t ln_rows_fwd(size_t M, int C, const void* z, const float* g, c
   }
   return cudaErrorInvalidValue;
 }
-// dz (BF16) from dx (FP32); kLnBlocks partial rows of dgamma and dbeta.
-inline cudaError_t ln_rows_bwd(size_t M, int C, const void* z, const float* dx, const float* g, const float* mean,
+// dz (BF16) from dx (BF16); kLnBlocks partial rows of dgamma and dbeta.
+inline cudaError_t ln_rows_bwd(size_t M, int C, const void* z, const void* dx, const float* g, const float* mean,
                                const float* rstd, void* dz, float* pg, float* pb, cudaStream_t s) {
   switch (C) {
     case 32: return ln_bwd_launch<32>(M, z, dx, g, mean, rstd, dz, pg, pb, s);

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restri
 }
 
 // Backward of the output LayerNorm: dX (channel-major BF16) from dy (pair-major
-// FP32) and X.  Each block walks its tiles of 64 pairs with the next tile's X
+// BF16) and X.  Each block walks its tiles of 64 pairs with the next tile's X
 // and dy loads issued while the current one drains.  dgamma / dbeta: per
 // tile, the 256 / C_h threads of a channel each add a fixed run of the
 // tile's pairs (four interleaved partial sums, combined in a fixed order)
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restri
 // partial row per block.
 template <int Ch>
 __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restrict__ X,
-                                                        const float* __restrict__ dy,
+                                                        const uint16_t* __restrict__ dy,
                                                         const float* __restrict__ gamma,
                                                         const float* __restrict__ mean_in,
                                                         const float* __restrict__ rstd_in,
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
   // loads are issued as soon as this tile's X is in shared memory
   struct Regs {
     uint4 xr[Ch * 8 / 256];
-    float4 dyr[kCh][2];
+    uint4 dyr[kCh];  // 8 BF16 channels each
     float mean, rstd;
   };
   Regs cur, nxt;
@@ -206,8 +206,7 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
 #pragma unroll
     for (int i = 0; i < kCh; ++i) {
       const int c0 = 8 * (qq + 4 * i);
-      r.dyr[i][0] = *reinterpret_cast<const float4*>(dy + m * Ch + c0);
-      r.dyr[i][1] = *reinterpret_cast<const float4*>(dy + m * Ch + c0 + 4);
+      r.dyr[i] = ld16(dy + m * Ch + c0);
     }
     r.mean = mean_in[m];
     r.rstd = rstd_in[m];
@@ -224,8 +223,9 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
     float sg = 0.f, sgx = 0.f;
 #pragma unroll
     for (int i = 0; i < kCh; ++i) {
-      const float dv[8] = {dyr[i][0].x, dyr[i][0].y, dyr[i][0].z, dyr[i][0].w,
-                           dyr[i][1].x, dyr[i][1].y, dyr[i][1].z, dyr[i][1].w};
+      const float dv[8] = {bf16lo_to_f32(dyr[i].x), bf16hi_to_f32(dyr[i].x), bf16lo_to_f32(dyr[i].y),
+                           bf16hi_to_f32(dyr[i].y), bf16lo_to_f32(dyr[i].z), bf16hi_to_f32(dyr[i].z),
+                           bf16lo_to_f32(dyr[i].w), bf16hi_to_f32(dyr[i].w)};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int c = 8 * (qq + 4 * i) + e;
@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restri
     // each thread overwrites only the X entries it read itself
 #pragma unroll
     for (int i = 0; i < kCh; ++i) {
-      const float dv[8] = {dyr[i][0].x, dyr[i][0].y, dyr[i][0].z, dyr[i][0].w,
-                           dyr[i][1].x, dyr[i][1].y, dyr[i][1].z, dyr[i][1].w};
+      const float dv[8] = {bf16lo_to_f32(dyr[i].x), bf16hi_to_f32(dyr[i].x), bf16lo_to_f32(dyr[i].y),
+                           bf16hi_to_f32(dyr[i].y), bf16lo_to_f32(dyr[i].z), bf16hi_to_f32(dyr[i].z),
+                           bf16lo_to_f32(dyr[i].w), bf16hi_to_f32(dyr[i].w)};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int c = 8 * (qq + 4 * i) + e;
@@ -386,11 +387,11 @@ TmWs tm_ws(const TmDims& d) {
   w.gemm = o;   o += rup(kGemmWorkspace);
   w.du = o;     o += rup(d.M * d.Cz * 2);
   w.dp = o;     o += rup(d.M * d.Fp * 2);
-  w.dy = o;     o += rup(d.M * d.Ch * 4);
+  w.dy = o;     o += rup(d.M * d.Ch * 2);
   w.dX = o;     o += rup(cm);
   w.dA = o;     o += rup(cm);
   w.dB = o;     o += rup(cm);
-  w.dx = o;     o += rup(d.M * d.Cz * 4);
+  w.dx = o;     o += rup(d.M * d.Cz * 2);
   w.pg_in = o;  o += rup(static_cast<size_t>(kLnBlocks) * d.Cz * 4);
   w.pb_in = o;  o += rup(static_cast<size_t>(kLnBlocks) * d.Cz * 4);
   w.pg_out = o; o += rup(static_cast<size_t>(kCmBwdBlocks) * d.Ch * 4);
@@ -440,7 +441,7 @@ struct CmLaunch {
     return cudaGetLastError();
   }
   template <int Ch>
-  cudaError_t ln_bwd(const uint16_t* X, const float* dy, const float* g, const float* mean, const float* rstd,
+  cudaError_t ln_bwd(const uint16_t* X, const uint16_t* dy, const float* g, const float* mean, const float* rstd,
                      uint16_t* dX, float* pg, float* pb) const {
     cudaError_t e = set_attrs<Ch>();
     if (e != cudaSuccess) return e;
@@ -582,11 +583,11 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
   const uint16_t* X = reinterpret_cast<const uint16_t*>(cx + c.X);
   uint16_t* du = reinterpret_cast<uint16_t*>(ws + w.du);
   uint16_t* dp = reinterpret_cast<uint16_t*>(ws + w.dp);
-  float* dy = reinterpret_cast<float*>(ws + w.dy);
+  uint16_t* dy = reinterpret_cast<uint16_t*>(ws + w.dy);
   uint16_t* dX = reinterpret_cast<uint16_t*>(ws + w.dX);
   uint16_t* dA = reinterpret_cast<uint16_t*>(ws + w.dA);
   uint16_t* dB = reinterpret_cast<uint16_t*>(ws + w.dB);
-  float* dx = reinterpret_cast<float*>(ws + w.dx);
+  uint16_t* dx = reinterpret_cast<uint16_t*>(ws + w.dx);
   const CmLaunch L{d, s};
   // out = sigmoid(g) u:  du, and dp's output-gate columns
   if (trace_call(kKTmOutGate, s, [&] {
@@ -596,10 +597,10 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
         return cudaGetLastError();
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  // u = y W_o:  dW_o = y^T du,  dy = du W_o^T (FP32)
+  // u = y W_o:  dW_o = y^T du,  dy = du W_o^T (BF16, as every activation gradient here)
   if (gemm_traced(kKTmProj, gws, s, true, false, Ch, Cz, M, cx + c.y, Ch, du, Cz, d_w_o, Cz, true) !=
           TRIATTN_OK ||
-      gemm_traced(kKTmProj, gws, s, false, true, M, Ch, Cz, du, Cz, w_o, Cz, dy, Ch, true) != TRIATTN_OK)
+      gemm_traced(kKTmProj, gws, s, false, true, M, Ch, Cz, du, Cz, w_o, Cz, dy, Ch, false) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // y = LayerNorm(X):  dX (channel-major), output-LayerNorm partial sums
   float* pg_out = reinterpret_cast<float*>(ws + w.pg_out);
@@ -630,9 +631,9 @@ triattn_status triattn_trimul_bwd(const triattn_trimul_shape* shape, const void*
                                     dA, dB, dp, Fp, current_wait_ctl(), s);
       }) != cudaSuccess)
     return TRIATTN_ERR_CUDA;
-  // p = x W_p:  dW_p = x^T dp,  dx = dp W_p^T (FP32)
+  // p = x W_p:  dW_p = x^T dp,  dx = dp W_p^T (BF16)
   if (gemm_traced(kKTmProj, gws, s, true, false, Cz, F, M, cx + c.x, Cz, dp, Fp, d_w_p, F, true) != TRIATTN_OK ||
-      gemm_traced(kKTmProj, gws, s, false, true, M, Cz, F, dp, Fp, w_p, F, dx, Cz, true) != TRIATTN_OK)
+      gemm_traced(kKTmProj, gws, s, false, true, M, Cz, F, dp, Fp, w_p, F, dx, Cz, false) != TRIATTN_OK)
     return TRIATTN_ERR_CUDA;
   // x = LayerNorm(z)
   float* pg_in = reinterpret_cast<float*>(ws + w.pg_in);

@@ -45,7 +45,6 @@ namespace {
 using namespace pairops;
 
 constexpr int kPairs = 64;         // pairs per block of the channel-major kernels
-constexpr int kRow = kPairs + 1;   // padded shared-memory row (floats)
 constexpr int kCmBwdBlocks = 152 * 2;  // fixed: the output-LayerNorm partial rows depend on it
 
 __device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + __expf(-x)); }
@@ -104,10 +103,6 @@ __device__ __forceinline__ float tile_h(const uint32_t* s, int c, int pr) {
   const uint32_t w = s[c * kRowW + (pr >> 1)];
   return (pr & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
 }
-__device__ __forceinline__ void tile_h_set(uint32_t* s, int c, int pr, float v) {
-  reinterpret_cast<uint16_t*>(s + c * kRowW + (pr >> 1))[pr & 1] =
-      static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
-}
 
 // y = LayerNorm(X) for 64 pairs: X channel-major in, y pair-major out (BF16),
 // mean and rstd saved.  Thread (pair pr, quarter qq) owns the 8-channel
@@ -164,130 +159,168 @@ __global__ void __launch_bounds__(256) ln_cm_fwd_kernel(const uint16_t* __restri
   }
 }
 
+// 16-byte global -> shared copies that bypass the registers (cp.async, L2
+// only), in commit groups; wait<n> returns once at most n groups are pending.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int n>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory"); }
+
 // Backward of the output LayerNorm: dX (channel-major BF16) from dy (pair-major
-// BF16) and X.  Each block walks its tiles of 64 pairs with the next tile's X
-// and dy loads issued while the current one drains.  dgamma / dbeta: per
-// tile, the 256 / C_h threads of a channel each add a fixed run of the
-// tile's pairs (four interleaved partial sums, combined in a fixed order)
-// into their own accumulator; at the end the runs are added in order: one
-// partial row per block.
+// BF16) and X.  A block walks its tiles of 64 pairs.  Thread (pair slot pl,
+// part p) takes the C_h / 8 channels [p C_h / 8, (p + 1) C_h / 8) of pairs
+// pl and pl + 32; a pair's sums are a butterfly over its 8 part threads.
+// The X tile comes into shared memory by cp.async, double buffered (the next
+// tile's copy, and its dy and statistics in registers, are in flight while
+// this one is worked on), as channel rows of 128 bytes whose 16-byte chunks
+// are rotated by XOR with the row's part, so that the 8 parts reading one
+// pair hit distinct banks; dX overwrites it in place and is stored
+// channel-major from there.  dgamma / dbeta: each thread adds its channels
+// over its pairs in register accumulators (tile order); at the end a fixed
+// butterfly adds the 4 pair slots of a warp and the block adds its 8 warps in
+// order: one partial row per block.
 template <int Ch>
-__global__ void __launch_bounds__(256) ln_cm_bwd_kernel(const uint16_t* __restrict__ X,
-                                                        const uint16_t* __restrict__ dy,
-                                                        const float* __restrict__ gamma,
-                                                        const float* __restrict__ mean_in,
-                                                        const float* __restrict__ rstd_in,
-                                                        uint16_t* __restrict__ dX, float* __restrict__ part_g,
-                                                        float* __restrict__ part_b, size_t NN, size_t tiles) {
-  extern __shared__ float sm[];
-  float* sG = sm;                                                   // dy * xhat
-  float* sD = sm + Ch * kRow;                                       // dy
-  uint32_t* sXh = reinterpret_cast<uint32_t*>(sm + 2 * Ch * kRow);  // X, then dX (BF16)
-  constexpr int kCh = Ch / 32;
-  constexpr int kSplit = 256 / Ch;      // threads per channel in the per-tile sums
-  constexpr int kPP = kPairs / kSplit;  // pairs each of them adds
-  static_assert(kPP % 4 == 0, "per-thread pair run");
-  const int pr = threadIdx.x >> 2, qq = threadIdx.x & 3;
-  const int rc = threadIdx.x % Ch, rpart = threadIdx.x / Ch;
-  const bool reducer = threadIdx.x < kSplit * Ch;
-  float accg = 0.f, accb = 0.f;
-  // this tile's X, dy and statistics, and the next tile's in flight: the next
-  // loads are issued as soon as this tile's X is in shared memory
-  struct Regs {
-    uint4 xr[Ch * 8 / 256];
-    uint4 dyr[kCh];  // 8 BF16 channels each
-    float mean, rstd;
-  };
-  Regs cur, nxt;
-  auto fetch = [&](size_t tile, Regs& r) {
-    const size_t m0 = tile * kPairs;
-    fetch_cm_tile<Ch>(X, m0 / NN, m0 % NN, NN, r.xr);
-    const size_t m = m0 + pr;
+struct CmBwd {
+  static constexpr int kCT = Ch / 8;            // channels per thread
+  static constexpr int kTileBytes = Ch * 128;   // one X tile: Ch rows of 64 BF16 pairs
+  static constexpr int kGam = 2 * kTileBytes;   // gamma [Ch] fp32
+  static constexpr int kRed = kGam + Ch * 4;    // [8 warps][2][Ch] fp32
+  static constexpr int kBytes = kRed + 8 * 2 * Ch * 4;
+};
+template <int Ch>
+__global__ void __launch_bounds__(256, 2) ln_cm_bwd_kernel(const uint16_t* __restrict__ X,
+                                                           const uint16_t* __restrict__ dy,
+                                                           const float* __restrict__ gamma,
+                                                           const float* __restrict__ mean_in,
+                                                           const float* __restrict__ rstd_in,
+                                                           uint16_t* __restrict__ dX, float* __restrict__ part_g,
+                                                           float* __restrict__ part_b, size_t NN, size_t tiles) {
+  using L = CmBwd<Ch>;
+  constexpr int kCT = L::kCT;
+  extern __shared__ __align__(128) uint8_t smc[];
+  float* sGam = reinterpret_cast<float*>(smc + L::kGam);
+  float* sRed = reinterpret_cast<float*>(smc + L::kRed);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int p = tid & 7, pl = tid >> 3;
+  const int c0 = p * kCT;
+  for (int c = tid; c < Ch; c += 256) sGam[c] = gamma[c];
+  float accg[kCT], accb[kCT];
 #pragma unroll
-    for (int i = 0; i < kCh; ++i) {
-      const int c0 = 8 * (qq + 4 * i);
-      r.dyr[i] = ld16(dy + m * Ch + c0);
-    }
-    r.mean = mean_in[m];
-    r.rstd = rstd_in[m];
-  };
-  if (blockIdx.x < tiles) fetch(blockIdx.x, cur);
-  for (size_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+  for (int j = 0; j < kCT; ++j) accg[j] = accb[j] = 0.f;
+  // X tile -> buffer bb (one commit group)
+  auto fill = [&](size_t tile, int bb) {
     const size_t m0 = tile * kPairs;
     const size_t b = m0 / NN, pos0 = m0 % NN;
-    put_cm_tile<Ch>(cur.xr, sXh);
-    if (tile + gridDim.x < tiles) fetch(tile + gridDim.x, nxt);
-    const auto& dyr = cur.dyr;
-    const float mean = cur.mean, rstd = cur.rstd;
-    __syncthreads();
-    float sg = 0.f, sgx = 0.f;
+    uint8_t* buf = smc + bb * L::kTileBytes;
 #pragma unroll
-    for (int i = 0; i < kCh; ++i) {
-      const float dv[8] = {bf16lo_to_f32(dyr[i].x), bf16hi_to_f32(dyr[i].x), bf16lo_to_f32(dyr[i].y),
-                           bf16hi_to_f32(dyr[i].y), bf16lo_to_f32(dyr[i].z), bf16hi_to_f32(dyr[i].z),
-                           bf16lo_to_f32(dyr[i].w), bf16hi_to_f32(dyr[i].w)};
+    for (int k = 0; k < Ch * 8 / 256; ++k) {
+      const int it = tid + 256 * k;
+      const int c = it >> 3, q = it & 7;
+      cp_async16(buf + c * 128 + ((q ^ (c / kCT)) << 4), X + (b * Ch + c) * NN + pos0 + 8 * q);
+    }
+    cp_async_commit();
+  };
+  struct Dy {
+    Packed<kCT> d[2];
+    float mean[2], rstd[2];
+  };
+  auto fetch = [&](size_t tile, Dy& r) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = 8 * (qq + 4 * i) + e;
-        const float xh = (tile_h(sXh, c, pr) - mean) * rstd;
-        const float g = dv[e] * gamma[c];
+    for (int s = 0; s < 2; ++s) {
+      const size_t m = tile * kPairs + 32 * s + pl;
+      ld_packed<kCT>(dy + m * Ch + c0, r.d[s]);
+      r.mean[s] = mean_in[m];
+      r.rstd[s] = rstd_in[m];
+    }
+  };
+  Dy cur, nxt;
+  if (blockIdx.x < tiles) {
+    fill(blockIdx.x, 0);
+    fetch(blockIdx.x, cur);
+  }
+  int k = 0;
+  for (size_t tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++k) {
+    const int bb = k & 1;
+    if (tile + gridDim.x < tiles) {
+      fill(tile + gridDim.x, bb ^ 1);  // that buffer was drained before the last barrier
+      fetch(tile + gridDim.x, nxt);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // this tile's X (and gamma) visible to every thread
+    uint8_t* buf = smc + bb * L::kTileBytes;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int pr = 32 * s + pl, w = pr >> 1;
+      // byte offset of this pair's element in a channel row of this part
+      const int off = (((w >> 2) ^ p) << 4) + (w & 3) * 4 + (pr & 1) * 2;
+      uint16_t* xp = reinterpret_cast<uint16_t*>(buf + c0 * 128 + off);
+      const float mean = cur.mean[s], rstd = cur.rstd[s];
+      float d[kCT], xh[kCT];
+      unpack<kCT>(cur.d[s], d);
+      float sg = 0.f, sgx = 0.f;
+#pragma unroll
+      for (int j = 0; j < kCT; ++j) {
+        xh[j] = (bf16lo_to_f32(xp[j * 64]) - mean) * rstd;  // rows are 64 halfwords apart
+        const float g = d[j] * sGam[c0 + j];
         sg += g;
-        sgx += g * xh;
-        sG[c * kRow + pr] = dv[e] * xh;
-        sD[c * kRow + pr] = dv[e];
+        sgx += g * xh[j];
+        accg[j] += d[j] * xh[j];
+        accb[j] += d[j];
       }
-    }
-    sg += __shfl_xor_sync(0xffffffffu, sg, 1);
-    sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-    sgx += __shfl_xor_sync(0xffffffffu, sgx, 1);
-    sgx += __shfl_xor_sync(0xffffffffu, sgx, 2);
-    const float a = sg * (1.f / Ch), bb = sgx * (1.f / Ch);
-    // each thread overwrites only the X entries it read itself
 #pragma unroll
-    for (int i = 0; i < kCh; ++i) {
-      const float dv[8] = {bf16lo_to_f32(dyr[i].x), bf16hi_to_f32(dyr[i].x), bf16lo_to_f32(dyr[i].y),
-                           bf16hi_to_f32(dyr[i].y), bf16lo_to_f32(dyr[i].z), bf16hi_to_f32(dyr[i].z),
-                           bf16lo_to_f32(dyr[i].w), bf16hi_to_f32(dyr[i].w)};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = 8 * (qq + 4 * i) + e;
-        const float xh = (tile_h(sXh, c, pr) - mean) * rstd;
-        tile_h_set(sXh, c, pr, rstd * (dv[e] * gamma[c] - a - xh * bb));
+      for (int off2 = 1; off2 < 8; off2 <<= 1) {
+        sg += __shfl_xor_sync(0xffffffffu, sg, off2);
+        sgx += __shfl_xor_sync(0xffffffffu, sgx, off2);
       }
+      const float a = sg * (1.f / Ch), bb2 = sgx * (1.f / Ch);
+#pragma unroll
+      for (int j = 0; j < kCT; ++j)
+        xp[j * 64] = static_cast<uint16_t>(pack_bf16x2(rstd * (d[j] * sGam[c0 + j] - a - xh[j] * bb2), 0.f) & 0xFFFFu);
     }
-    __syncthreads();
-    store_cm_tile_h<Ch>(sXh, dX, b, pos0, NN);
-    if (reducer) {
-      const float* rg = sG + rc * kRow + rpart * kPP;
-      const float* rd = sD + rc * kRow + rpart * kPP;
-      float g4[4] = {0.f, 0.f, 0.f, 0.f}, b4[4] = {0.f, 0.f, 0.f, 0.f};
+    __syncthreads();  // dX of the tile complete in the buffer
+    {
+      const size_t m0 = tile * kPairs;
+      const size_t b = m0 / NN, pos0 = m0 % NN;
 #pragma unroll
-      for (int q = 0; q < kPP; q += 4)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          g4[u] += rg[q + u];
-          b4[u] += rd[q + u];
-        }
-      accg += (g4[0] + g4[1]) + (g4[2] + g4[3]);
-      accb += (b4[0] + b4[1]) + (b4[2] + b4[3]);
+      for (int kk = 0; kk < Ch * 8 / 256; ++kk) {
+        const int it = tid + 256 * kk;
+        const int c = it >> 3, q = it & 7;
+        st16(dX + (b * Ch + c) * NN + pos0 + 8 * q,
+             *reinterpret_cast<const uint4*>(buf + c * 128 + ((q ^ (c / kCT)) << 4)));
+      }
     }
     cur = nxt;
-    __syncthreads();
+    __syncthreads();  // the buffer is drained before the next iteration refills it
   }
-  if (reducer) {
-    sG[rpart * Ch + rc] = accg;
-    sD[rpart * Ch + rc] = accb;
+  // the 4 pair slots of a warp (lanes 8 apart), then the 8 warps in order
+#pragma unroll
+  for (int j = 0; j < kCT; ++j)
+#pragma unroll
+    for (int off2 = 8; off2 < 32; off2 <<= 1) {
+      accg[j] += __shfl_xor_sync(0xffffffffu, accg[j], off2);
+      accb[j] += __shfl_xor_sync(0xffffffffu, accb[j], off2);
+    }
+  if (lane < 8) {
+#pragma unroll
+    for (int j = 0; j < kCT; ++j) {
+      sRed[(warp * 2) * Ch + c0 + j] = accg[j];
+      sRed[(warp * 2 + 1) * Ch + c0 + j] = accb[j];
+    }
   }
   __syncthreads();
-  if (threadIdx.x < Ch) {
+  for (int c = tid; c < Ch; c += 256) {
     float g = 0.f, bsum = 0.f;
 #pragma unroll
-    for (int p = 0; p < kSplit; ++p) {
-      g += sG[p * Ch + threadIdx.x];
-      bsum += sD[p * Ch + threadIdx.x];
+    for (int w = 0; w < 8; ++w) {
+      g += sRed[(w * 2) * Ch + c];
+      bsum += sRed[(w * 2 + 1) * Ch + c];
     }
-    part_g[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = g;
-    part_b[static_cast<size_t>(blockIdx.x) * Ch + threadIdx.x] = bsum;
+    part_g[static_cast<size_t>(blockIdx.x) * Ch + c] = g;
+    part_b[static_cast<size_t>(blockIdx.x) * Ch + c] = bsum;
   }
 }
 
@@ -415,7 +448,7 @@ unsigned blocks_for(size_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
 // Dynamic shared memory of the channel-major kernels.
 template <int Ch> constexpr int ln_cm_fwd_smem() { return Ch * kRowW * 4; }
-template <int Ch> constexpr int ln_cm_bwd_smem() { return 2 * Ch * kRow * 4 + Ch * kRowW * 4; }
+template <int Ch> constexpr int ln_cm_bwd_smem() { return CmBwd<Ch>::kBytes; }
 
 template <int Ch>
 cudaError_t set_attrs() {

@@ -784,8 +784,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 // ---------------------------------------------------------------- reductions
 // dQ[row, :] = sum_{t = 0 .. J_K-1} dq_part[t][row, :]   (ascending t, FP32).
 // One block per 128-row tile of one slice: coalesced float4 reads of the
-// chunk-major partials, FP32 sums in fixed order, transpose through shared
-// memory, coalesced BF16 row writes.
+// chunk-major partials (four partials' loads in flight per thread), FP32 sums
+// in fixed order, transpose through shared memory, coalesced BF16 row writes.
 template <int D>
 __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict__ part, uint16_t* __restrict__ dq,
                                                         int N, int H, int JQ, int JK, size_t tiles, RowLayout lg) {
@@ -797,11 +797,27 @@ __global__ void __launch_bounds__(256) reduce_dq_kernel(const float4* __restrict
   const size_t slice = t / JQ;
   const long long bo = static_cast<long long>(slice / H);
   const int h = static_cast<int>(slice - bo * H);
+  const size_t kstep = tiles * kChunks;    // float4 between key tiles' partials
   for (int e = threadIdx.x; e < kChunks; e += blockDim.x) {
     const float4* p = part + t * kChunks + e;
     float4 acc = __ldcs(p);
-    for (int kt = 1; kt < JK; ++kt) {
-      const float4 v = __ldcs(p + static_cast<size_t>(kt) * tiles * kChunks);
+    // the loads of four consecutive partials issued together, the adds in
+    // ascending order
+    int kt = 1;
+    for (; kt + 4 <= JK; kt += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(p + static_cast<size_t>(kt + u) * kstep);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
+    }
+    for (; kt < JK; ++kt) {
+      const float4 v = __ldcs(p + static_cast<size_t>(kt) * kstep);
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;

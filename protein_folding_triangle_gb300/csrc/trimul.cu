@@ -63,9 +63,10 @@ __device__ __forceinline__ uint4 ld16(const uint16_t* p) { return *reinterpret_c
 __device__ __forceinline__ void st16(uint16_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // A [Ch][64] channel-major tile of pairs [pos0, pos0 + 64) of example b in
-// shared memory, as BF16: row c holds the 64 pairs as 32 words (even pair in
-// the low half) plus one padding word, so that both the row-wise fills /
-// drains and the column-wise reads of one pair are free of bank conflicts.
+// shared memory, as BF16 (the output LayerNorm forward): row c holds the 64
+// pairs as 32 words (even pair in the low half) plus one padding word, so
+// that both the row-wise fills and the column-wise reads of one pair are free
+// of bank conflicts.
 constexpr int kRowW = kPairs / 2 + 1;
 // The same fill in two steps, so that all of a thread's loads are in flight
 // before the first shared-memory store (every kernel here runs 256 threads).
@@ -88,15 +89,6 @@ __device__ __forceinline__ void put_cm_tile(const uint4 (&r)[Ch * 8 / 256], uint
     d[1] = r[k].y;
     d[2] = r[k].z;
     d[3] = r[k].w;
-  }
-}
-template <int Ch>
-__device__ __forceinline__ void store_cm_tile_h(const uint32_t* s, uint16_t* __restrict__ dst, size_t b, size_t pos0,
-                                                size_t NN) {
-  for (int it = threadIdx.x; it < Ch * 8; it += blockDim.x) {
-    const int c = it >> 3, q = it & 7;
-    const uint32_t* r = s + c * kRowW + 4 * q;
-    st16(dst + (b * Ch + c) * NN + pos0 + 8 * q, make_uint4(r[0], r[1], r[2], r[3]));
   }
 }
 __device__ __forceinline__ float tile_h(const uint32_t* s, int c, int pr) {

@@ -351,6 +351,31 @@ def test_module_rejects_bad_arguments(lib):
     assert call_module_bwd(lib, s, 0) == T.ERR_WORKSPACE
 
 
+def test_trimul_and_module_workspace_layouts(lib):
+    """The scratch layouts, each part 256-byte aligned: the GEMMs' 32 MiB of
+    split-K partials, then (TriMul) du, dp, dy, the channel-major dX, dA, dB,
+    dx and the LayerNorm partial rows; (module) W_in padded to Fp columns, its
+    FP32 gradient, dP, d_oflat, dbias, dx, the LayerNorm partial rows and the
+    core's workspace.  The activation gradients dy and dx are BF16 (2 bytes
+    per element); the LayerNorm backwards write one partial row per block of
+    their fixed grids (456 pair-major, 304 channel-major)."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    B, N, Cz, Ch = 1, 40, 64, 32
+    M, NN = B * N * N, N * N
+    Fp = (4 * Ch + Cz + 7) // 8 * 8
+    want = (r256(32 << 20) + r256(M * Cz * 2) + r256(M * Fp * 2) + r256(M * Ch * 2) + 3 * r256(B * Ch * NN * 2)
+            + r256(M * Cz * 2) + 2 * r256(456 * Cz * 4) + 2 * r256(304 * Ch * 4))
+    assert T.trimul_sizes(B, N, Cz, Ch)[1] == want
+    B, N, C, H, D = 1, 40, 64, 2, 16
+    M, HD = B * N * N, H * D
+    Fp = (3 * HD + H + 7) // 8 * 8
+    core = max(T.bwd_workspace_bytes(T.Shape(B, N, N, H, D, 0)), lib.triattn_fwd_workspace_bytes(
+        ctypes.byref(T.Shape(B, N, N, H, D, 0))))
+    want = (r256(32 << 20) + r256(C * Fp * 2) + r256(C * Fp * 4) + r256(M * Fp * 2) + r256(M * HD * 2)
+            + r256(B * H * N * N * 2) + r256(M * C * 2) + 2 * r256(456 * C * 4) + r256(core))
+    assert T.module_sizes(B, N, C, H, D)[1] == want
+
+
 def test_trimul_sizes_and_argument_checks(lib):
     ctx, ws = T.trimul_sizes(1, 40, 64, 32)
     M, Cz, Ch = 40 * 40, 64, 32

@@ -520,3 +520,25 @@ def test_layout_of_views():
     assert (lay.slice, lay.head, lay.row) == (H * N * D, N * D, D)
     with pytest.raises(ValueError):
         T.layout_of(c.transpose(3, 4))
+
+
+def test_layers_parameters_and_no_cpu_path():
+    """The torch modules hold the library's parameter layouts (W_in [C, 3HD + H]
+    and W_o [HD, C] for triangle attention; W_p [C_z, 4C_h + C_z] and W_o [C_h,
+    C_z] for the multiplicative update; BF16 weights, FP32 LayerNorm
+    parameters), reject an unknown direction, and refuse CPU tensors instead of
+    computing anything on the host."""
+    from protein_folding_triangle_gb300 import layers
+    att = layers.TriangleAttention(c_z=64, n_heads=2, head_dim=16)
+    assert tuple(att.w_in.shape) == (64, 3 * 2 * 16 + 2) and att.w_in.dtype == torch.bfloat16
+    assert tuple(att.w_o.shape) == (2 * 16, 64) and att.w_o.dtype == torch.bfloat16
+    assert att.ln_w.dtype == torch.float32 and tuple(att.ln_b.shape) == (64,)
+    mul = layers.TriangleMultiplication(c_z=64, c_hidden=32, direction="incoming")
+    assert tuple(mul.w_p.shape) == (64, 4 * 32 + 64) and tuple(mul.w_o.shape) == (32, 64)
+    assert tuple(mul.ln_out_w.shape) == (32,) and mul.ln_in_w.dtype == torch.float32
+    with pytest.raises(ValueError):
+        layers.TriangleMultiplication(c_z=64, c_hidden=32, direction="sideways")
+    z = torch.zeros(1, 8, 8, 64, dtype=torch.bfloat16)
+    for module in (att, mul):
+        with pytest.raises((ValueError, RuntimeError)):
+            module(z)
